@@ -1,0 +1,374 @@
+"""Schedule oracle: how the output tiles and their K loops are split over units.
+
+TEST INFRASTRUCTURE (see the package docstring): plain, slow Python written from
+the page "Split-K and Stream-K: The Last Wave of a GEMM" (kanthi.in). Every
+function below names the passage it follows. Where the page leaves a step open,
+the reading taken is stated at the function.
+
+Terms (page, "Mental model" table): an output tile is BM x BN = 128 x 128; a
+MAC-loop iteration is one BK = 64 step of a tile's K loop; a unit is one
+persistent CTA (one per SM); the fixup combines a split tile's FP32 partials.
+
+Map format produced by `plan_map` (int32 list), the contract the C library's
+sk_plan must reproduce exactly:
+  header (12): version, mode_resolved, tiles, iters, workers, sk_tiles, sk_units,
+               n_segments, splits, label, label_splits, n_slots
+  n_segments rows (9): unit, order, tile, k_begin, k_end, role, slot, peer_begin, n_peers
+  tiles rows (2): owner_unit, n_contrib
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+TILE_M = 128
+TILE_N = 128
+BLK_K = 64
+
+# decomposition modes (C-ABI enum values)
+DP, SPLITK, STREAMK, HYBRID = 0, 1, 2, 3
+# segment roles
+FULL, OWNER, PRODUCER, SLAB = 0, 1, 2, 3
+# heuristic labels
+LABEL_NONE, LABEL_DP, LABEL_SPLITK, LABEL_STREAMK = -1, 0, 1, 2
+
+MAP_VERSION = 1
+HEADER_LEN = 12
+SEG_LEN = 9
+TILE_ROW_LEN = 2
+
+
+def cdiv(a: int, b: int) -> int:
+    return -(-a // b)
+
+
+# ---------------------------------------------------------------------------
+# Wave arithmetic (page, Case 1 "Count the waves before you tune anything")
+# ---------------------------------------------------------------------------
+def waves(m: int, n: int, sms: int, tile_m: int = TILE_M, tile_n: int = TILE_N):
+    """Tiles, waves, CTAs in the final wave, and utilization tiles / (waves * SMs)."""
+    tiles = cdiv(m, tile_m) * cdiv(n, tile_n)
+    w = cdiv(tiles, sms)
+    tail = tiles - (w - 1) * sms
+    return tiles, w, tail, tiles / (w * sms)
+
+
+def problem_shape(M: int, N: int, K: int):
+    """Tile grid and K-loop length of a GEMM (page, Case 2 report: tiles and iters by ceiling)."""
+    tiles_m, tiles_n = cdiv(M, TILE_M), cdiv(N, TILE_N)
+    return tiles_m, tiles_n, tiles_m * tiles_n, cdiv(K, BLK_K)
+
+
+# ---------------------------------------------------------------------------
+# Unit ranges of the flattened (tile, k) space
+# ---------------------------------------------------------------------------
+def divmod_bounds(total: int, units: int):
+    """Stream-K split (page, Case 2 stream_k_units; "Try this" calls it the CUTLASS split):
+    q, big = divmod(total, units); the first `big` units take q + 1 iterations, the rest q."""
+    q, big = divmod(total, units)
+    out, it = [], 0
+    for u in range(units):
+        n = q + 1 if u < big else q
+        out.append((it, it + n))
+        it += n
+    return out
+
+
+def cdiv_bounds(total: int, units: int):
+    """Variant of the page's Triton listing (Case 3): q = ceil(total / units), unit u owns
+    [u*q, min((u+1)*q, total)). Documented variant only; the plans use divmod_bounds."""
+    q = cdiv(total, units)
+    return [(min(u * q, total), min((u + 1) * q, total)) for u in range(units)]
+
+
+def floor_bounds(total: int, units: int):
+    """Variant of the docc StreamK rewrite: block b owns [b*T/N, (b+1)*T/N) with floor division."""
+    return [(b * total // units, (b + 1) * total // units) for b in range(units)]
+
+
+# ---------------------------------------------------------------------------
+# CUTLASS decision rule (page, Case 2 cutlass_heuristic; Case 4 knob table)
+# ---------------------------------------------------------------------------
+def heuristic(tiles: int, iters: int, sms: int, min_iters: int = 8):
+    """Return (label, sk_tiles, sk_units, label_splits).
+
+    Data-parallel when the tiles fill whole waves or the K loop is at most `min_iters`
+    iterations, or when the tail wave is at least half full. Otherwise keep all full
+    waves but the last data-parallel, give the remaining tiles to Stream-K over
+    min(sms, iters * sk_tiles // min_iters) units, and call it Split-K when the units
+    divide evenly over more than one per tile."""
+    full_waves = tiles // sms
+    total_waves = cdiv(tiles, sms)
+    if full_waves == total_waves or iters <= min_iters:
+        return LABEL_DP, 0, 0, 0
+    tail = tiles - full_waves * sms
+    if 2 * tail >= sms:
+        return LABEL_DP, 0, 0, 0
+    dp_waves = full_waves - 1 if full_waves > 1 else 0
+    sk_tiles = tiles - dp_waves * sms
+    sk_units = min(sms, (iters * sk_tiles) // min_iters)
+    if sk_tiles < sk_units and sk_units % sk_tiles == 0:
+        return LABEL_SPLITK, sk_tiles, sk_units, sk_units // sk_tiles
+    return LABEL_STREAMK, sk_tiles, sk_units, 0
+
+
+def heuristic_text(label: int, sk_tiles: int, sk_units: int, label_splits: int) -> str:
+    """The decision as the page's report prints it."""
+    if label == LABEL_DP:
+        return "DataParallel"
+    name = f"SplitK(s={label_splits})" if label == LABEL_SPLITK else "StreamK"
+    return f"{name} sk_tiles={sk_tiles} units={sk_units}"
+
+
+# ---------------------------------------------------------------------------
+# Work-unit plan
+# ---------------------------------------------------------------------------
+@dataclass
+class Segment:
+    unit: int
+    order: int
+    tile: int
+    k_begin: int
+    k_end: int
+    role: int
+    slot: int = -1
+    peer_begin: int = -1
+    n_peers: int = 0
+
+
+@dataclass
+class Plan:
+    mode: int
+    tiles: int
+    iters: int
+    tiles_n: int
+    workers: int
+    sk_tiles: int = 0
+    sk_units: int = 0
+    splits: int = 0
+    label: int = LABEL_NONE
+    label_splits: int = 0
+    n_slots: int = 0
+    units: list = field(default_factory=list)   # units[w] = list of Segment in execution order
+
+    def segments(self):
+        return [s for segs in self.units for s in segs]
+
+
+def _streamk_region(tiles_base: int, n_tiles: int, iters: int, n_units: int):
+    """Per-unit segments of Stream-K over tiles [tiles_base, tiles_base + n_tiles).
+
+    Follows the page's per-unit algorithm (Case 2 stream_k_units; Mental model): each unit
+    walks its contiguous range of the flattened space one tile at a time. A segment that
+    covers a whole tile is FULL. A segment that starts at the tile's k = 0 but stops short
+    is the OWNER: it waits for the later units whose ranges start before the tile ends
+    (its peers, in k order) and runs the fixup. Any other segment is a PRODUCER that stores
+    an FP32 partial and raises a flag. Reading taken: each unit has one partial slot, its
+    own index, so a tile's peers occupy consecutive slots owner+1 .. owner+n_peers."""
+    bounds = divmod_bounds(n_tiles * iters, n_units)
+    out = []
+    for u, (b, e) in enumerate(bounds):
+        segs = []
+        it = b
+        while it < e:
+            local = it // iters
+            tile_begin = local * iters
+            tile_end = tile_begin + iters
+            seg_end = min(e, tile_end)
+            kb, ke = it - tile_begin, seg_end - tile_begin
+            tile = tiles_base + local
+            if kb == 0 and ke == iters:
+                segs.append(Segment(u, 0, tile, kb, ke, FULL))
+            elif kb == 0:
+                peers = []
+                v = u + 1
+                while v < n_units and bounds[v][0] < tile_end:
+                    peers.append(v)
+                    v += 1
+                segs.append(Segment(u, 0, tile, kb, ke, OWNER, -1, u + 1, len(peers)))
+            else:
+                owner = next(v for v in range(n_units) if bounds[v][0] <= tile_begin < bounds[v][1])
+                segs.append(Segment(u, 0, tile, kb, ke, PRODUCER, u, owner + 1, 0))
+            it = seg_end
+        out.append(segs)
+    return out
+
+
+def build_plan(M: int, N: int, K: int, num_sms: int, mode: int, splits: int = 1,
+               units: int = 0, min_iters: int = 8, split_partials: bool = False) -> Plan:
+    """The integer work-unit map for one GEMM.
+
+    `units` > 0 replaces num_sms as the number of persistent units (the toy case is
+    "forced to 4 units"). Readings of the page where it leaves the step open:
+      - DP (Mental model, Case 2 data_parallel): unit w runs tiles w, w + W, ... with
+        W = min(units, tiles), each tile FULL.
+      - Split-K (Case 2 split_k; the split-K report's "final split is clamped"): split j
+        of a tile covers k-iterations [j*chunk, min((j+1)*chunk, iters)), chunk =
+        ceil(iters / s); empty trailing splits are dropped (s_eff = ceil(iters / chunk)).
+        Split 0 owns the tile and reduces splits 1..s_eff-1 in k order. Work items are
+        queued tile by tile with the owner last, item i -> tile i // s_eff, split
+        s_eff-1 - i % s_eff, and unit w runs items w, w + W, ... (W = min(units, items)):
+        every producer is queued before its owner, so no unit ever waits on work queued
+        behind it. Slots: tile t's split j >= 1 uses slot t*(s_eff-1) + j-1.
+        With split_partials every split is a SLAB that writes its own [M,N] FP32 slab j.
+      - Stream-K: units = min(units, tiles * iters) so that no unit is empty.
+      - Hybrid (Case 2 hybrid; "gives the last 160 tiles ... to Stream-K"): the
+        heuristic's Stream-K tiles are the last sk_tiles tile ids, split over sk_units
+        units; the first tiles - sk_tiles run data-parallel over W units. Each unit runs
+        its Stream-K range first, then its data-parallel tiles. A SplitK(s) label is
+        planned with the same Stream-K partition (the page's hybrid simulates it so).
+    """
+    if min(M, N, K) < 1 or num_sms < 1 or units < 0 or min_iters < 1:
+        raise ValueError("bad problem")
+    if mode not in (DP, SPLITK, STREAMK, HYBRID):
+        raise ValueError("bad mode")
+    if split_partials and mode != SPLITK:
+        raise ValueError("split partials need Split-K")
+    _, tiles_n, tiles, iters = problem_shape(M, N, K)
+    S = units if units > 0 else num_sms
+
+    if mode == HYBRID:
+        label, sk_tiles, sk_units, lsp = heuristic(tiles, iters, S, min_iters)
+        if label == LABEL_DP:
+            p = build_plan(M, N, K, num_sms, DP, units=units)
+            p.label, p.label_splits = label, lsp
+            return p
+        dp_tiles = tiles - sk_tiles
+        W = max(sk_units, min(S, dp_tiles))
+        p = Plan(HYBRID, tiles, iters, tiles_n, W, sk_tiles, sk_units, 0, label, lsp, sk_units)
+        region = _streamk_region(dp_tiles, sk_tiles, iters, sk_units)
+        for w in range(W):
+            segs = list(region[w]) if w < sk_units else []
+            for t in range(w, dp_tiles, W):
+                segs.append(Segment(w, 0, t, 0, iters, FULL))
+            p.units.append(segs)
+    elif mode == DP:
+        W = min(S, tiles)
+        p = Plan(DP, tiles, iters, tiles_n, W)
+        for w in range(W):
+            p.units.append([Segment(w, 0, t, 0, iters, FULL) for t in range(w, tiles, W)])
+    elif mode == STREAMK:
+        U = min(S, tiles * iters)
+        p = Plan(STREAMK, tiles, iters, tiles_n, U, tiles, U, 0, LABEL_NONE, 0, U)
+        p.units = _streamk_region(0, tiles, iters, U)
+    else:  # SPLITK
+        if splits < 1 or splits > iters:
+            raise ValueError("bad splits")
+        chunk = cdiv(iters, splits)
+        s_eff = cdiv(iters, chunk)
+        items = tiles * s_eff
+        W = min(S, items)
+        n_slots = 0 if split_partials else tiles * (s_eff - 1)
+        p = Plan(SPLITK, tiles, iters, tiles_n, W, 0, 0, s_eff, LABEL_NONE, 0, n_slots)
+        for w in range(W):
+            segs = []
+            for i in range(w, items, W):
+                t = i // s_eff
+                j = s_eff - 1 - i % s_eff
+                kb, ke = j * chunk, min((j + 1) * chunk, iters)
+                if split_partials:
+                    segs.append(Segment(w, 0, t, kb, ke, SLAB, j, -1, 0))
+                elif s_eff == 1:
+                    segs.append(Segment(w, 0, t, kb, ke, FULL))
+                elif j == 0:
+                    segs.append(Segment(w, 0, t, kb, ke, OWNER, -1, t * (s_eff - 1), s_eff - 1))
+                else:
+                    segs.append(Segment(w, 0, t, kb, ke, PRODUCER, t * (s_eff - 1) + j - 1,
+                                        t * (s_eff - 1), 0))
+            p.units.append(segs)
+    for w, segs in enumerate(p.units):
+        for i, s in enumerate(segs):
+            s.unit, s.order = w, i
+    return p
+
+
+def tile_rows(p: Plan):
+    """Per tile: the unit that runs its k = 0 segment (the fixup owner) and the number of
+    segments that cover it."""
+    owner = [-1] * p.tiles
+    n = [0] * p.tiles
+    for s in p.segments():
+        n[s.tile] += 1
+        if s.k_begin == 0:
+            owner[s.tile] = s.unit
+    return list(zip(owner, n))
+
+
+def plan_map(p: Plan):
+    segs = p.segments()
+    out = [MAP_VERSION, p.mode, p.tiles, p.iters, p.workers, p.sk_tiles, p.sk_units,
+           len(segs), p.splits, p.label, p.label_splits, p.n_slots]
+    for s in segs:
+        out += [s.unit, s.order, s.tile, s.k_begin, s.k_end, s.role, s.slot, s.peer_begin, s.n_peers]
+    for o, c in tile_rows(p):
+        out += [o, c]
+    return out
+
+
+# ---------------------------------------------------------------------------
+# Cost model (page, Case 2: 1 per MAC-loop iteration, EPI per finished tile,
+# PART per FP32 partial tile stored or loaded)
+# ---------------------------------------------------------------------------
+def makespan(p: Plan, EPI: float = 2.0, PART: float = 2.0) -> float:
+    """Finish time of the slowest unit when every unit starts at 0 and runs its
+    segments in order: a segment costs its iterations; a PRODUCER then pays PART to
+    store its partial and signals; an OWNER waits for each peer's signal in k order,
+    paying PART per partial loaded, then EPI; a FULL tile pays EPI."""
+    signal = {}
+    done = {}
+
+    def unit_time(w):
+        if w in done:
+            return done[w]
+        t = 0.0
+        for s in p.units[w]:
+            t += s.k_end - s.k_begin
+            if s.role == PRODUCER:
+                t += PART
+                signal[s.slot] = t
+            elif s.role == OWNER:
+                for slot in range(s.peer_begin, s.peer_begin + s.n_peers):
+                    if slot not in signal:
+                        unit_time(_producer_unit(p, slot))
+                    t = max(t, signal[slot]) + PART
+                t += EPI
+            elif s.role == SLAB:
+                t += PART
+            else:
+                t += EPI
+        done[w] = t
+        return t
+
+    return max(unit_time(w) for w in range(len(p.units))) if p.units else 0.0
+
+
+def _producer_unit(p: Plan, slot: int) -> int:
+    for s in p.segments():
+        if s.role == PRODUCER and s.slot == slot:
+            return s.unit
+    raise KeyError(slot)
+
+
+def split_k_makespan(tiles: int, iters: int, sms: int, s: int, EPI: float = 2.0, PART: float = 2.0):
+    """The page's closed form for Split-K (Case 2 split_k): ceil(tiles*s / sms) waves of the
+    worst unit (chunk iterations plus one partial store or load), then the owner's s-1
+    further partial loads and the epilogue."""
+    chunk = cdiv(iters, s)
+    return cdiv(tiles * s, sms) * (chunk + PART) + (s - 1) * PART + EPI
+
+
+def report_rows(m: int, n: int, k: int, sms: int, EPI: float = 2.0, PART: float = 2.0):
+    """The five rows of the page's schedule report for one shape: (name, makespan, eff),
+    plus the ideal makespan tiles * (iters + EPI) / sms."""
+    _, _, tiles, iters = problem_shape(m, n, k)
+    ideal = tiles * (iters + EPI) / sms
+    rows = [("data-parallel", makespan(build_plan(m, n, k, sms, DP), EPI, PART))]
+    for s in (2, 4):
+        rows.append((f"split-K s={s}", split_k_makespan(tiles, iters, sms, s, EPI, PART)))
+    rows.append(("stream-K (all tiles, 1 unit/SM)", makespan(build_plan(m, n, k, sms, STREAMK), EPI, PART)))
+    hp = build_plan(m, n, k, sms, HYBRID)
+    if hp.label == LABEL_DP:
+        text = heuristic_text(LABEL_DP, 0, 0, 0)
+    else:
+        text = heuristic_text(hp.label, hp.sk_tiles, hp.sk_units, hp.label_splits)
+    rows.append((f"CUTLASS heuristic -> {text}", makespan(hp, EPI, PART)))
+    return tiles, iters, ideal, [(name, t, ideal / t) for name, t in rows]

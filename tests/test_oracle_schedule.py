@@ -1,0 +1,218 @@
+"""Pins for the schedule oracle against what the pages print and what the mathematics fixes.
+
+Each pin checks the oracle against something other than itself: the printed wave table and
+schedule report ("Split-K and Stream-K: The Last Wave of a GEMM", Cases 1 and 2), the toy
+4-SM case of its Mental model figure, the Triton driver's printed partition (Case 3), and
+brute force over small shapes (every (tile, k) iteration covered exactly once, balanced
+units, the owner being the lowest contributor).
+"""
+import csv
+import itertools
+import os
+
+import pytest
+
+from oracle import schedule as S
+
+
+def _rows(path, delimiter=","):
+    with open(path) as f:
+        return [r for r in csv.reader((l for l in f if not l.startswith("#")), delimiter=delimiter)]
+
+
+def test_wave_table(golden_dir):
+    rows = _rows(os.path.join(golden_dir, "wave_table.csv"))
+    assert len(rows) == 15
+    for m, n, sms, tiles, w, tail, util in rows:
+        t, ww, tl, u = S.waves(int(m), int(n), int(sms))
+        assert (t, ww, tl) == (int(tiles), int(w), int(tail))
+        assert f"{100 * u:.1f}" == util
+
+
+def test_thesis_example():
+    # 144 tiles on a 132-SM part: the second wave keeps 12 SMs busy, 54.5% overall.
+    tiles, w, tail, util = S.waves(1536, 1536, 132)
+    assert (tiles, w, tail) == (144, 2, 12)
+    assert round(100 * util, 1) == 54.5
+
+
+def test_schedule_report(golden_dir):
+    rows = _rows(os.path.join(golden_dir, "schedule_sim.psv"), delimiter="|")
+    assert len(rows) == 20
+    by_shape = {}
+    for r in rows:
+        by_shape.setdefault(tuple(int(x) for x in r[:4]), []).append(r)
+    for (m, n, k, sms), expect in by_shape.items():
+        tiles, iters, ideal, got = S.report_rows(m, n, k, sms)
+        assert (tiles, iters) == (int(expect[0][4]), int(expect[0][5]))
+        assert f"{ideal:.1f}" == expect[0][6]
+        assert len(got) == len(expect) == 5
+        for (name, t, eff), e in zip(got, expect):
+            assert name == e[7]
+            assert f"{t:.1f}" == e[8], (m, n, k, name)
+            assert f"{100 * eff:.1f}" == e[9]
+
+
+def test_toy_case(golden_dir):
+    # Mental model: 4 SMs, 5 tiles x 4 iterations (M=128, N=640, K=256), forced to 4 units.
+    dp = S.build_plan(128, 640, 256, 4, S.DP)
+    assert (dp.tiles, dp.iters) == (5, 4)
+    t = S.makespan(dp, EPI=0, PART=0)
+    assert t == 8
+    assert 20 / (t * 4) == 0.625
+    sk = S.build_plan(128, 640, 256, 4, S.STREAMK)
+    per_unit = [sum(s.k_end - s.k_begin for s in segs) for segs in sk.units]
+    assert per_unit == [5, 5, 5, 5]
+    assert S.makespan(sk, EPI=0, PART=0) == 5
+    expect = _rows(os.path.join(golden_dir, "toy_streamk_map.csv"))
+    roles = {"FULL": S.FULL, "OWNER": S.OWNER, "PRODUCER": S.PRODUCER}
+    got = [(s.unit, s.tile, s.k_begin, s.k_end, s.role) for s in sk.segments()]
+    assert got == [(int(u), int(t), int(a), int(b), roles[r]) for u, t, a, b, r in expect]
+    # Units 1..3 start with the partial they hand off; the k=0 holder owns the fixup.
+    assert [segs[0].role for segs in sk.units] == [S.FULL, S.PRODUCER, S.PRODUCER, S.PRODUCER]
+    assert [o for o, _ in S.tile_rows(sk)] == [0, 0, 1, 2, 3]
+    # Same toy through the units override rather than the SM count.
+    sk2 = S.build_plan(128, 640, 256, 148, S.STREAMK, units=4)
+    assert S.plan_map(sk2) == S.plan_map(sk)
+
+
+def test_triton_partition(golden_dir):
+    for units, tiles, ipt, total, q, peers in _rows(os.path.join(golden_dir, "triton_partition.csv")):
+        units, ipt, total = int(units), int(ipt), int(total)
+        assert int(tiles) * ipt == total
+        b = S.cdiv_bounds(total, units)
+        assert b[0][1] - b[0][0] == int(q)
+        if peers:
+            most = 0
+            for t in range(int(tiles)):
+                lo, hi = t * ipt, (t + 1) * ipt
+                most = max(most, sum(1 for (x, y) in b if x < hi and y > lo))
+            assert most == int(peers)
+
+
+def test_heuristic_decisions():
+    # Case 2 narrative: 2 x 12 < 132 -> all 144 tiles to 132 Stream-K units; on B200 the rule
+    # keeps five full waves data-parallel and gives the last 160 tiles to Stream-K; a tail
+    # of 100/132 stays data-parallel.
+    assert S.heuristic(144, 64, 132) == (S.LABEL_STREAMK, 144, 132, 0)
+    assert S.heuristic(900, 64, 148) == (S.LABEL_STREAMK, 160, 148, 0)
+    assert S.heuristic(1024, 64, 132)[0] == S.LABEL_DP
+    # iters <= min_iters stays data-parallel; whole waves stay data-parallel.
+    assert S.heuristic(144, 8, 132)[0] == S.LABEL_DP
+    assert S.heuristic(264, 64, 132)[0] == S.LABEL_DP
+    # units dividing evenly over fewer tiles: Split-K label (4 tiles, 32 iters, 148 SMs
+    # -> sk_units = min(148, 128 // 8 = 16) = 16 = 4 per tile).
+    assert S.heuristic(4, 32, 148) == (S.LABEL_SPLITK, 4, 16, 4)
+
+
+def _check_plan_invariants(p, M, N, K, sms):
+    """Properties any correct plan has, checked by brute force over every iteration."""
+    cover = {}
+    for s in p.segments():
+        assert 0 <= s.k_begin < s.k_end <= p.iters
+        for k in range(s.k_begin, s.k_end):
+            key = (s.tile, k)
+            assert key not in cover, key
+            cover[key] = s
+    assert len(cover) == p.tiles * p.iters
+    owners = {}
+    for s in p.segments():
+        if s.k_begin == 0:
+            owners[s.tile] = s
+    assert len(owners) == p.tiles
+    for t, o in owners.items():
+        contrib = [s for s in p.segments() if s.tile == t]
+        if len(contrib) == 1:
+            assert o.role in (S.FULL, S.SLAB) and o.k_end == p.iters
+        elif o.role != S.SLAB:
+            assert o.role == S.OWNER and o.n_peers == len(contrib) - 1
+            peers = sorted((s for s in contrib if s is not o), key=lambda s: s.k_begin)
+            assert [s.slot for s in peers] == list(range(o.peer_begin, o.peer_begin + o.n_peers))
+            assert all(s.role == S.PRODUCER and s.peer_begin == o.peer_begin for s in peers)
+    slots = [s.slot for s in p.segments() if s.role == S.PRODUCER]
+    assert len(slots) == len(set(slots))
+    assert all(0 <= x < p.n_slots for x in slots)
+
+
+def test_streamk_bruteforce():
+    # Every small flattened space: divmod ranges are contiguous, balanced within one
+    # iteration, each unit has at most one producer (its first segment) and one owner (its
+    # last), the owner of a split tile is its lowest contributor, and contributors are
+    # consecutive units (n_contrib == u_last - u_first + 1, as in the Triton fixup).
+    for tiles, iters, units in itertools.product(range(1, 13), range(1, 10), range(1, 30)):
+        if units > tiles * iters:
+            continue
+        b = S.divmod_bounds(tiles * iters, units)
+        sizes = [e - s for s, e in b]
+        assert max(sizes) - min(sizes) <= 1 and sum(sizes) == tiles * iters
+        assert all(b[i][1] == b[i + 1][0] for i in range(units - 1))
+        segs = S._streamk_region(0, tiles, iters, units)
+        for u, ss in enumerate(segs):
+            roles = [s.role for s in ss]
+            assert roles.count(S.PRODUCER) <= 1 and roles.count(S.OWNER) <= 1
+            if S.PRODUCER in roles:
+                assert roles[0] == S.PRODUCER
+            if S.OWNER in roles:
+                assert roles[-1] == S.OWNER
+        for t in range(tiles):
+            us = [u for u, (s, e) in enumerate(b) if s < (t + 1) * iters and e > t * iters]
+            assert us == list(range(us[0], us[-1] + 1))
+            owner = [s.unit for ss in segs for s in ss if s.tile == t and s.k_begin == 0]
+            assert owner == [us[0]]
+
+
+@pytest.mark.parametrize("mode", [S.DP, S.SPLITK, S.STREAMK, S.HYBRID])
+def test_plan_invariants_small(mode):
+    for M, N, K in [(128, 640, 256), (300, 200, 1000), (640, 640, 512), (128, 128, 64), (1, 1, 1)]:
+        for sms in (1, 3, 4, 7, 16):
+            splits = (1, 2, 3) if mode == S.SPLITK else (1,)
+            for s in splits:
+                if mode == S.SPLITK and s > S.problem_shape(M, N, K)[3]:
+                    continue
+                p = S.build_plan(M, N, K, sms, mode, splits=s)
+                _check_plan_invariants(p, M, N, K, sms)
+                if mode == S.SPLITK:
+                    p2 = S.build_plan(M, N, K, sms, mode, splits=s, split_partials=True)
+                    _check_plan_invariants(p2, M, N, K, sms)
+
+
+def test_splitk_clamped_and_dropped():
+    # iters = 5, s = 4: chunk 2 -> splits [0,2) [2,4) [4,5); the empty fourth split is dropped.
+    p = S.build_plan(128, 128, 320, 8, S.SPLITK, splits=4)
+    assert p.splits == 3
+    assert sorted((s.k_begin, s.k_end) for s in p.segments()) == [(0, 2), (2, 4), (4, 5)]
+    with pytest.raises(ValueError):
+        S.build_plan(128, 128, 320, 8, S.SPLITK, splits=6)
+
+
+def test_splitk_producers_before_owner():
+    # Many rounds of work items: a unit never waits on an item queued behind it.
+    p = S.build_plan(1024, 1024, 1024, 5, S.SPLITK, splits=3)
+    pos = {}
+    for s in p.segments():
+        pos[(s.tile, s.k_begin)] = (s.order * p.workers + s.unit)
+    for s in p.segments():
+        if s.role == S.OWNER:
+            for q in p.segments():
+                if q.tile == s.tile and q.role == S.PRODUCER:
+                    assert pos[(q.tile, q.k_begin)] < pos[(s.tile, s.k_begin)]
+
+
+def test_hybrid_waveq_on_148():
+    # Wave-quantized shape: 16 x 19 = 304 tiles x 64 iterations on 148 SMs = 2 full waves + 8.
+    p = S.build_plan(2048, 2432, 4096, 148, S.HYBRID)
+    assert (p.tiles, p.iters) == (304, 64)
+    assert p.mode == S.HYBRID and p.label == S.LABEL_STREAMK
+    assert (p.sk_tiles, p.sk_units, p.workers) == (156, 148, 148)
+    q, big = divmod(156 * 64, 148)
+    assert (q, big) == (67, 68)
+    assert max(c for _, c in S.tile_rows(p)) == 2
+    dp_tiles = [s.tile for s in p.segments() if s.role == S.FULL and s.tile < 148]
+    assert sorted(dp_tiles) == list(range(148))
+
+
+def test_map_layout():
+    p = S.build_plan(128, 640, 256, 4, S.STREAMK)
+    m = S.plan_map(p)
+    assert m[:S.HEADER_LEN] == [1, S.STREAMK, 5, 4, 4, 5, 4, 8, 0, -1, 0, 4]
+    assert len(m) == S.HEADER_LEN + 8 * S.SEG_LEN + 5 * S.TILE_ROW_LEN
