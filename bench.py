@@ -1,0 +1,407 @@
+"""Benchmark of the work-decomposed BF16 GEMM on GB300.
+
+One step = one sk_gemm call: the whole hot path (schedule walk, TMA/tcgen05 MAC loop,
+partial-tile fixup, epilogue) over the workload's synthetic BF16 inputs, resident in HBM.
+Default workload: the wave-quantized GEMM 2048 x 2432 x 4096 (304 tiles of 128 x 128 =
+2 waves + 8 on 148 SMs), BF16 out, the hybrid rule on 148 SMs. Between timed steps a
+256 MiB buffer is written to flush L2 (the inputs, 47 MB, fit in L2). Each step is timed
+with CUDA events on the launching stream; the headline value is TFLOP/s = 2MNK / time.
+
+Prints ONE JSON line (rank 0). `--impl reference` times the CPU oracle (FP64 dot products
+over the BF16 inputs) on a bounded row sample of the same workload instead.
+Multi-GPU (torchrun): every rank runs its own independent instance (weak scaling); a
+barrier brackets the timed region and the slowest rank's time is reported.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synth  # noqa: E402
+
+PEAKS_FALLBACK = {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0, "bf16_tflops_sustained": 1700.0}
+METRIC = "BF16 GEMM TFLOP/s and % tensor peak vs tile count, per schedule, 1xGB300"
+WORKLOADS = {"waveq": synth.WAVEQ, "skinny": synth.SKINNY, "large": synth.LARGE,
+             "smallm96": synth.SMALLM_96, "smallm256": synth.SMALLM_256, "toy": synth.TOY}
+# Per-launch DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of the GEMM kernel
+# from one ncu capture, keyed by workload/schedule; valid only for the kernel source it
+# was taken on (sha256 of sk_kernels.cu, first 16 hex digits).
+TRAFFIC = {}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return PEAKS_FALLBACK, "fallback"
+
+
+def kernel_sha():
+    p = os.path.join(ROOT, "gemm_work_decomposition_gb300", "csrc", "sk_kernels.cu")
+    with open(p, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.idx = gpu_id
+        self.proc = None
+        self.lines = []
+
+    def _query(self, loop=False):
+        cmd = ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits"]
+        if loop:
+            cmd.append("-lms=100")
+        return cmd
+
+    def start(self):
+        try:
+            self.lines += subprocess.run(self._query(), capture_output=True, text=True, timeout=20).stdout.splitlines()
+            self.proc = subprocess.Popen(self._query(True), stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=10)
+                self.lines += out.splitlines()
+            except Exception:
+                self.proc.kill()
+        try:
+            self.lines += subprocess.run(self._query(), capture_output=True, text=True, timeout=20).stdout.splitlines()
+        except Exception:
+            pass
+
+    def summary(self):
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        mhz, mx, reasons = [], 0.0, set()
+        for line in self.lines:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                mhz.append(float(f[1]))
+                mx = max(mx, float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": float(np.median(mhz)) if mhz else None, "sm_max_mhz": mx or None,
+                "reasons": sorted(reasons), "samples": len(mhz)}
+
+
+def dist_info():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def cpu_oracle_sample(w, seconds: float, rows_per_block: int = 256):
+    """Time the oracle's FP64 GEMM on row blocks of the workload for about `seconds`."""
+    from oracle import gemm as og
+    A_bits, B_bits = synth.make_inputs(w)
+    rows = min(rows_per_block, w.M)
+    flops = 0.0
+    t0 = time.perf_counter()
+    n = 0
+    while True:
+        r0 = (n * rows) % max(1, w.M - rows + 1)
+        og.ref_gemm(A_bits[r0:r0 + rows], B_bits, w.layout)
+        flops += 2.0 * rows * w.N * w.K
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    return flops / el / 1e12, el, n, rows
+
+
+def run_reference(args, w, rank, world):
+    if rank != 0:
+        return
+    seconds = args.ref_seconds
+    for _ in range(args.warmup):
+        cpu_oracle_sample(w, 0.0)
+    times, flops = [], 0.0
+    rows = min(256, w.M)
+    for _ in range(args.steps):
+        v, el, n, rows = cpu_oracle_sample(w, seconds / max(1, args.steps))
+        times.append(el / n)
+        flops = 2.0 * rows * w.N * w.K
+    ms = float(np.mean(times)) * 1e3
+    value = flops / (ms / 1e3) / 1e12
+    cores = os.cpu_count()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "layout": w.layout,
+                   "step": f"FP64 oracle GEMM on {rows} rows of C (bounded sample)"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{rows} x {w.N} x {w.K} FP64 per step (numpy matmul, default BLAS threads)"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_sweep(sk, torch, dev, path, red, flush, stream, peak_tf, dev_sms):
+    """Tile-count sweep: M = N = 128 .. 4096, K = 4096, every schedule plus the hybrid
+    rule's choice, on 148 SMs and on the device's SM count; one JSON line per point."""
+    with open(path, "w") as f:
+        for m in synth.SWEEP_SIZES:
+            ww = synth.sweep(m)
+            A_bits, B_bits = synth.make_inputs(ww)
+            A = torch.from_numpy(A_bits.view(np.int16)).view(torch.bfloat16).to(dev)
+            B = torch.from_numpy(B_bits.view(np.int16)).view(torch.bfloat16).to(dev)
+            C = torch.empty((m, m), dtype=torch.bfloat16, device=dev)
+            fl = 2.0 * m * m * ww.K
+            for nsms in (148, dev_sms):
+                for name, mode, s in (("dp", sk.SK_DP, 1), ("splitk2", sk.SK_SPLITK, 2), ("splitk4", sk.SK_SPLITK, 4),
+                                      ("streamk", sk.SK_STREAMK, 1), ("hybrid", sk.SK_HYBRID, 1)):
+                    sch = sk.schedule(mode, s)
+                    nb = sk.sk_workspace_size(m, m, ww.K, nsms, sch, red)
+                    ws = torch.zeros(nb, dtype=torch.uint8, device=dev)
+                    plan = sk.sk_plan(m, m, ww.K, nsms, sch)
+                    for _ in range(5):
+                        sk.sk_gemm(A, B, C, sk.SK_BF16, m, m, ww.K, sk.SK_NN, sch, red, nsms, ws, nb, stream)
+                    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                          for _ in range(30)]
+                    for a, b in ev:
+                        flush.zero_()
+                        a.record(stream)
+                        sk.sk_gemm(A, B, C, sk.SK_BF16, m, m, ww.K, sk.SK_NN, sch, red, nsms, ws, nb, stream)
+                        b.record(stream)
+                    torch.cuda.synchronize(dev)
+                    assert sk.sk_status(ws, stream) == sk.SK_OK
+                    t = float(np.median([a.elapsed_time(b) for a, b in ev]))
+                    tf = fl / (t / 1e3) / 1e12
+                    f.write(json.dumps({"M": m, "N": m, "K": ww.K, "tiles": int(plan[2]), "num_sms": nsms,
+                                        "schedule": name, "resolved_mode": int(plan[1]), "label": int(plan[9]),
+                                        "us": t * 1e3, "tflops": tf, "frac_of_measured_peak": tf / peak_tf}) + "\n")
+                    f.flush()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--workload", default="waveq", choices=sorted(WORKLOADS))
+    ap.add_argument("--sms", type=int, default=148, help="SM count the schedule is built for (0 = device)")
+    ap.add_argument("--mode", default="hybrid", choices=["dp", "splitk", "streamk", "hybrid"])
+    ap.add_argument("--splits", type=int, default=2)
+    ap.add_argument("--reduction", default="deterministic", choices=["deterministic", "atomic"])
+    ap.add_argument("--no-extras", action="store_true", help="skip the schedule table, e2e and CPU baseline")
+    ap.add_argument("--ref-seconds", type=float, default=10.0)
+    ap.add_argument("--sweep", default="", help="also write the tile-count sweep (JSON lines) to this file")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    rank, world, local = dist_info()
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w, rank, world)
+        return
+
+    import torch
+    import torch.distributed as dist
+
+    import gemm_work_decomposition_gb300 as sk
+    from gemm_work_decomposition_gb300 import build as skbuild
+
+    skbuild.build()
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if world > 1 else 0)
+    props = torch.cuda.get_device_properties(dev)
+    dev_sms = props.multi_processor_count
+    sms = args.sms if args.sms > 0 else dev_sms
+    peaks, peaks_src = load_peaks()
+    peak_tf = float(peaks["bf16_tflops"])
+
+    modes = {"dp": sk.SK_DP, "splitk": sk.SK_SPLITK, "streamk": sk.SK_STREAMK, "hybrid": sk.SK_HYBRID}
+    red = sk.SK_DETERMINISTIC if args.reduction == "deterministic" else sk.SK_ATOMIC
+    out_code = sk.SK_BF16 if w.out == "bf16" else sk.SK_F32
+    lay = sk.SK_NN if w.layout == "NN" else sk.SK_NT
+    flops = 2.0 * w.M * w.N * w.K
+
+    # Inputs: seeded per rank (independent instances), copied once into HBM.
+    wr = synth.Workload(w.name, w.M, w.N, w.K, w.layout, w.dist, w.seed + 1000 * rank, w.zero_first_row,
+                        w.scale_last_row, w.out)
+    A_bits, B_bits = synth.make_inputs(wr)
+    A_host = torch.from_numpy(A_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
+    B_host = torch.from_numpy(B_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
+    A = A_host.to(dev)
+    B = B_host.to(dev)
+    cdt = torch.bfloat16 if w.out == "bf16" else torch.float32
+    C = torch.empty((w.M, w.N), dtype=cdt, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def make(mode_name, nsms, splits=1):
+        sch = sk.schedule(modes[mode_name], splits if mode_name == "splitk" else 1)
+        nb = sk.sk_workspace_size(w.M, w.N, w.K, nsms, sch, red)
+        ws = torch.zeros(nb, dtype=torch.uint8, device=dev)
+        return sch, ws, nb
+
+    def timed(sch, ws, nb, nsms, steps, warmup):
+        for _ in range(warmup):
+            sk.sk_gemm(A, B, C, out_code, w.M, w.N, w.K, lay, sch, red, nsms, ws, nb, stream)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        torch.cuda.synchronize(dev)
+        for s, e in ev:
+            flush.zero_()
+            s.record(stream)
+            sk.sk_gemm(A, B, C, out_code, w.M, w.N, w.K, lay, sch, red, nsms, ws, nb, stream)
+            e.record(stream)
+        torch.cuda.synchronize(dev)
+        st = sk.sk_status(ws, stream)
+        if st != sk.SK_OK:
+            raise RuntimeError(f"device status {sk.sk_strerror(st)}")
+        return np.array([s.elapsed_time(e) for s, e in ev])  # ms
+
+    sch, ws, nb = make(args.mode, sms, args.splits)
+    plan = sk.sk_plan(w.M, w.N, w.K, sms, sch)
+    launches_per_step = 1  # one persistent GEMM kernel per step (no split-slab reduction here)
+
+    # ---- the timed region: K steps, barrier + synchronize on both sides
+    for _ in range(args.warmup):
+        sk.sk_gemm(A, B, C, out_code, w.M, w.N, w.K, lay, sch, red, sms, ws, nb, stream)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    clocks = ClockSampler(f"GPU-{props.uuid}")
+    clocks.start()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    wall0 = time.perf_counter()
+    for s, e in ev:
+        flush.zero_()
+        s.record(stream)
+        sk.sk_gemm(A, B, C, out_code, w.M, w.N, w.K, lay, sch, red, sms, ws, nb, stream)
+        e.record(stream)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    wall = time.perf_counter() - wall0
+    clocks.stop()
+    status = sk.sk_status(ws, stream)
+    if status != sk.SK_OK:
+        raise RuntimeError(f"device status {sk.sk_strerror(status)}")
+    step_ms = np.array([s.elapsed_time(e) for s, e in ev])
+    total_ms = float(step_ms.sum())
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = world * flops * args.steps / (total_ms / 1e3) / 1e12
+    kernel_tflops = flops / (ms_per_step / 1e3) / 1e12
+
+    extras = {}
+    if not args.no_extras and rank == 0:
+        # ---- per-schedule table (the metric is per schedule)
+        table = {}
+        for name, nsms in (("dp", 148), ("splitk2", 148), ("streamk", 148), ("hybrid", 148),
+                           ("dp", dev_sms), ("streamk", dev_sms), ("hybrid", dev_sms)):
+            mname = "splitk" if name.startswith("splitk") else name
+            s2, ws2, nb2 = make(mname, nsms, 2)
+            t = timed(s2, ws2, nb2, nsms, 200, 10)
+            med = float(np.median(t))
+            table[f"{name}@{nsms}"] = {"us_median": med * 1e3, "us_p10": float(np.percentile(t, 10)) * 1e3,
+                                       "us_p90": float(np.percentile(t, 90)) * 1e3,
+                                       "tflops": flops / (med / 1e3) / 1e12,
+                                       "frac_of_measured_peak": flops / (med / 1e3) / 1e12 / peak_tf}
+        extras["schedules"] = table
+
+        # ---- e2e: host buffers, copies inside the timed region, through the C ABI
+        C_host = torch.empty((w.M, w.N), dtype=cdt).pin_memory()
+        A2 = torch.empty_like(A)
+        B2 = torch.empty_like(B)
+        for _ in range(3):
+            A2.copy_(A_host, non_blocking=True)
+            B2.copy_(B_host, non_blocking=True)
+            sk.sk_gemm(A2, B2, C, out_code, w.M, w.N, w.K, lay, sch, red, sms, ws, nb, stream)
+            C_host.copy_(C, non_blocking=True)
+        torch.cuda.synchronize(dev)
+        n_e2e = max(10, min(200, args.steps))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n_e2e):
+            A2.copy_(A_host, non_blocking=True)
+            B2.copy_(B_host, non_blocking=True)
+            sk.sk_gemm(A2, B2, C, out_code, w.M, w.N, w.K, lay, sch, red, sms, ws, nb, stream)
+            C_host.copy_(C, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = e0.elapsed_time(e1) / n_e2e
+        extras["e2e"] = {"value": flops / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
+                         "h2d_bytes_per_step": int(A.numel() * 2 + B.numel() * 2),
+                         "d2h_bytes_per_step": int(C.numel() * C.element_size()), "ms_per_step": e2e_ms}
+        assert sk.sk_status(ws, stream) == sk.SK_OK
+
+        # ---- CPU oracle baseline on a bounded sample
+        cpu_v, cpu_s, cpu_n, cpu_rows = cpu_oracle_sample(w, args.ref_seconds)
+        extras["cpu_baseline"] = {"value": cpu_v, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+                                  "sample": f"{cpu_n} x FP64 GEMM of {cpu_rows} rows x {w.N} x {w.K} "
+                                            f"({cpu_s:.1f} s, numpy matmul, default BLAS threads)"}
+
+        if args.sweep:
+            run_sweep(sk, torch, dev, args.sweep, red, flush, stream, peak_tf, dev_sms)
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    sha = kernel_sha()
+    tr = TRAFFIC.get(f"{w.name}/{args.mode}@{sms}")
+    traffic = tr["bytes"] if tr and tr.get("kernel_sha") == sha else None
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "layout": w.layout, "out": w.out,
+                   "schedule": args.mode, "reduction": args.reduction, "num_sms": sms, "device_sms": dev_sms,
+                   "tiles": int(plan[2]), "iters": int(plan[3]), "workers": int(plan[4]),
+                   "resolved_mode": int(plan[1]), "sk_tiles": int(plan[5]), "sk_units": int(plan[6]),
+                   "l2": "flushed between timed steps (256 MiB write)", "accumulate": "fp32"},
+        "roofline": {"bound": "tensor", "achieved": kernel_tflops, "peak": peak_tf, "unit": "TFLOP/s",
+                     "frac": kernel_tflops / peak_tf, "traffic": traffic,
+                     "peak_source": f"{peaks_src} bf16 burst", "kernel": "sk_gemm_kernel"},
+        "gpu_launches": args.steps * launches_per_step,
+        "clocks": clocks.summary(),
+        "wall_s_timed_region": wall,
+    }
+    line.update(extras)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,386 @@
+// sk_api.cu - the C ABI (include/sk.h): planning, validation, tensor-map encoding and
+// launch. Host code only; the kernels live in sk_kernels.cu.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+#include <stdint.h>
+
+#include <climits>
+#include <mutex>
+#include <vector>
+
+#include "sk.h"
+#include "sk_kernels.h"
+#include "sk_schedule.h"
+
+using namespace sk;
+
+namespace {
+
+constexpr int64_t kDefaultTimeoutNs = 2000000000ll;
+constexpr int kMaxDevices = 64;
+
+// The decision rule of the page "Split-K and Stream-K: The Last Wave of a GEMM", Case 2
+// (cutlass_heuristic): stay data-parallel when tiles fill whole waves, the K loop is at
+// most min_iters long, or the tail wave is at least half full; otherwise keep all full
+// waves but the last data-parallel and give the rest to Stream-K over
+// min(sms, iters * sk_tiles / min_iters) units, labelled Split-K when those units divide
+// evenly over more than one per tile.
+void heuristic(int64_t tiles, int64_t iters, int64_t sms, int64_t min_iters, int32_t* label, int64_t* sk_tiles,
+               int64_t* sk_units, int32_t* label_splits) {
+    const int64_t full_waves = tiles / sms;
+    const int64_t total_waves = (tiles + sms - 1) / sms;
+    *label = kLabelDP;
+    *sk_tiles = 0;
+    *sk_units = 0;
+    *label_splits = 0;
+    if (full_waves == total_waves || iters <= min_iters) return;
+    const int64_t tail = tiles - full_waves * sms;
+    if (2 * tail >= sms) return;
+    const int64_t dp_waves = full_waves > 1 ? full_waves - 1 : 0;
+    const int64_t skt = tiles - dp_waves * sms;
+    int64_t sku = (iters * skt) / min_iters;
+    if (sku > sms) sku = sms;
+    *sk_tiles = skt;
+    *sk_units = sku;
+    if (skt < sku && sku % skt == 0) {
+        *label = kLabelSplitK;
+        *label_splits = static_cast<int32_t>(sku / skt);
+    } else {
+        *label = kLabelStreamK;
+    }
+}
+
+void set_streamk(Sched& o, int64_t base, int64_t sk_tiles, int64_t units) {
+    const int64_t total = sk_tiles * o.iters;
+    o.sk_base = static_cast<int32_t>(base);
+    o.sk_tiles = static_cast<int32_t>(sk_tiles);
+    o.sk_units = static_cast<int32_t>(units);
+    o.sk_q = static_cast<int32_t>(total / units);
+    o.sk_big = static_cast<int32_t>(total % units);
+    o.n_slots = static_cast<int32_t>(units);
+}
+
+int32_t make_sched(int32_t M, int32_t N, int32_t K, int32_t num_sms, const sk_schedule& s, Sched& o) {
+    if (M < 1 || N < 1 || K < 1 || num_sms < 1 || s.units < 0 || s.min_iters < 0) return SK_EINVAL;
+    if (s.mode < SK_DP || s.mode > SK_HYBRID) return SK_EINVAL;
+    if (s.split_partials != 0 && (s.mode != SK_SPLITK || s.split_partials != 1)) return SK_EINVAL;
+    const int64_t tiles_n = (static_cast<int64_t>(N) + kTileN - 1) / kTileN;
+    const int64_t tiles = ((static_cast<int64_t>(M) + kTileM - 1) / kTileM) * tiles_n;
+    const int64_t iters = (static_cast<int64_t>(K) + kBlkK - 1) / kBlkK;
+    if (tiles * iters > INT32_MAX) return SK_EINVAL;
+    const int64_t S = s.units > 0 ? s.units : num_sms;
+    const int64_t min_iters = s.min_iters > 0 ? s.min_iters : 8;
+
+    o = Sched{};
+    o.tiles = static_cast<int32_t>(tiles);
+    o.iters = static_cast<int32_t>(iters);
+    o.tiles_n = static_cast<int32_t>(tiles_n);
+    o.label = kLabelNone;
+
+    int32_t mode = s.mode;
+    if (mode == SK_HYBRID) {
+        int32_t label, lsp;
+        int64_t skt, sku;
+        heuristic(tiles, iters, S, min_iters, &label, &skt, &sku, &lsp);
+        o.label = label;
+        o.label_splits = lsp;
+        if (label == kLabelDP) {
+            mode = SK_DP;
+        } else {
+            const int64_t dp_tiles = tiles - skt;
+            o.mode = kHybrid;
+            set_streamk(o, dp_tiles, skt, sku);
+            o.dp_tiles = static_cast<int32_t>(dp_tiles);
+            const int64_t dpw = dp_tiles < S ? dp_tiles : S;
+            o.workers = static_cast<int32_t>(sku > dpw ? sku : dpw);
+            return SK_OK;
+        }
+    }
+    if (mode == SK_DP) {
+        o.mode = kDP;
+        o.dp_tiles = static_cast<int32_t>(tiles);
+        o.workers = static_cast<int32_t>(tiles < S ? tiles : S);
+    } else if (mode == SK_STREAMK) {
+        const int64_t total = tiles * iters;
+        const int64_t U = total < S ? total : S;
+        o.mode = kStreamK;
+        set_streamk(o, 0, tiles, U);
+        o.workers = static_cast<int32_t>(U);
+    } else {  // SK_SPLITK
+        if (s.splits < 1 || s.splits > iters) return SK_EINVAL;
+        const int64_t chunk = (iters + s.splits - 1) / s.splits;
+        const int64_t s_eff = (iters + chunk - 1) / chunk;
+        const int64_t items = tiles * s_eff;
+        if (items > INT32_MAX || tiles * (s_eff - 1) > INT32_MAX) return SK_EINVAL;
+        o.mode = kSplitK;
+        o.splits = static_cast<int32_t>(s_eff);
+        o.chunk = static_cast<int32_t>(chunk);
+        o.partials = s.split_partials;
+        o.n_slots = s.split_partials ? 0 : static_cast<int32_t>(tiles * (s_eff - 1));
+        o.workers = static_cast<int32_t>(items < S ? items : S);
+    }
+    return SK_OK;
+}
+
+int64_t count_segments(const Sched& s) {
+    int64_t n = 0;
+    for (int32_t w = 0; w < s.workers; ++w) {
+        Walk wk;
+        wk.init(s, w);
+        Seg g;
+        while (wk.next(s, g)) ++n;
+    }
+    return n;
+}
+
+int64_t map_size(const Sched& s) {
+    return SK_MAP_HEADER + SK_MAP_SEG * count_segments(s) + static_cast<int64_t>(SK_MAP_TILE) * s.tiles;
+}
+
+int64_t align_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
+
+// Workspace: header | flags (one int32 per slot, 256-aligned) | slots (64 KiB each);
+// split-partials: header | slabs [splits][M][N] FP32.
+int64_t flags_offset() { return SK_WS_HEADER_BYTES; }
+int64_t slots_offset(const Sched& s) { return SK_WS_HEADER_BYTES + align_up(4ll * s.n_slots, 256); }
+int64_t workspace_bytes(const Sched& s, int32_t M, int32_t N) {
+    if (s.partials) return SK_WS_HEADER_BYTES + 4ll * s.splits * M * N;
+    return slots_offset(s) + static_cast<int64_t>(s.n_slots) * kSlotFloats * 4;
+}
+
+struct DeviceInfo {
+    bool ready = false;
+    cudaError_t err = cudaSuccess;
+    int sms = 0;
+    int ctas_per_sm = 0;
+};
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_mu;
+
+cudaError_t device_info(int* sms, int* ctas) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceInfo& d = g_dev[dev];
+    if (!d.ready) {
+        d.err = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+        if (d.err == cudaSuccess) d.err = prepare_device(&d.ctas_per_sm);
+        d.ready = true;
+    }
+    *sms = d.sms;
+    *ctas = d.ctas_per_sm;
+    return d.err;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// Row-major BF16 matrix of `outer` rows x `inner` columns, copied in boxes of
+// box_outer x box_inner with the 128-byte swizzle; out-of-range elements read as zero.
+bool encode_2d(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_inner,
+               uint32_t box_outer) {
+    PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {inner * 2};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+}  // namespace
+
+extern "C" {
+
+const char* sk_strerror(int32_t code) {
+    switch (code) {
+        case SK_OK: return "success";
+        case SK_EINVAL: return "invalid argument (sizes, schedule, alignment or layout)";
+        case SK_EWORKSPACE: return "workspace missing, misaligned or too small";
+        case SK_ECUDA: return "CUDA call failed";
+        case SK_ETIMEOUT: return "a device-side wait ran past its time limit";
+        case SK_ECAPACITY: return "map buffer smaller than sk_plan_size";
+        case SK_ERESIDENCY: return "more persistent units than the device can hold at once";
+        default: return "unknown error code";
+    }
+}
+
+int64_t sk_plan_size(int32_t M, int32_t N, int32_t K, int32_t num_sms, sk_schedule s) {
+    Sched sch;
+    const int32_t e = make_sched(M, N, K, num_sms, s, sch);
+    if (e != SK_OK) return e;
+    return map_size(sch);
+}
+
+int32_t sk_plan(int32_t M, int32_t N, int32_t K, int32_t num_sms, sk_schedule s, int32_t* map, int64_t cap) {
+    Sched sch;
+    const int32_t e = make_sched(M, N, K, num_sms, s, sch);
+    if (e != SK_OK) return e;
+    const int64_t need = map_size(sch);
+    if (!map || cap < need) return SK_ECAPACITY;
+    const int64_t nseg = (need - SK_MAP_HEADER - static_cast<int64_t>(SK_MAP_TILE) * sch.tiles) / SK_MAP_SEG;
+    int32_t* h = map;
+    h[0] = SK_MAP_VERSION;
+    h[1] = sch.mode;
+    h[2] = sch.tiles;
+    h[3] = sch.iters;
+    h[4] = sch.workers;
+    h[5] = sch.sk_tiles;
+    h[6] = sch.sk_units;
+    h[7] = static_cast<int32_t>(nseg);
+    h[8] = sch.mode == kSplitK ? sch.splits : 0;
+    h[9] = sch.label;
+    h[10] = sch.label_splits;
+    h[11] = sch.n_slots;
+    int32_t* seg = map + SK_MAP_HEADER;
+    int32_t* trow = seg + SK_MAP_SEG * nseg;
+    for (int32_t t = 0; t < sch.tiles; ++t) {
+        trow[2 * t] = -1;
+        trow[2 * t + 1] = 0;
+    }
+    for (int32_t w = 0; w < sch.workers; ++w) {
+        Walk wk;
+        wk.init(sch, w);
+        Seg g;
+        int32_t order = 0;
+        while (wk.next(sch, g)) {
+            const int32_t row[SK_MAP_SEG] = {w, order++, g.tile, g.k_begin, g.k_end, g.role, g.slot, g.peer_begin,
+                                             g.n_peers};
+            for (int i = 0; i < SK_MAP_SEG; ++i) seg[i] = row[i];
+            seg += SK_MAP_SEG;
+            trow[2 * g.tile + 1] += 1;
+            if (g.k_begin == 0) trow[2 * g.tile] = w;
+        }
+    }
+    return SK_OK;
+}
+
+int64_t sk_workspace_size(int32_t M, int32_t N, int32_t K, int32_t num_sms, sk_schedule s, sk_reduction r) {
+    if (r != SK_DETERMINISTIC && r != SK_ATOMIC) return SK_EINVAL;
+    Sched sch;
+    const int32_t e = make_sched(M, N, K, num_sms, s, sch);
+    if (e != SK_OK) return e;
+    return workspace_bytes(sch, M, N);
+}
+
+int32_t sk_gemm_debug(const void* A, const void* B, void* C, sk_dtype c_dtype, int32_t M, int32_t N, int32_t K,
+                      sk_layout layout, sk_schedule s, sk_reduction r, int32_t num_sms, void* workspace,
+                      size_t ws_bytes, void* stream, const sk_debug_opts* opts) {
+    if (M < 0 || N < 0 || K < 0 || num_sms < 1) return SK_EINVAL;
+    if (c_dtype != SK_F32 && c_dtype != SK_BF16) return SK_EINVAL;
+    if (layout != SK_NN && layout != SK_NT) return SK_EINVAL;
+    if (r != SK_DETERMINISTIC && r != SK_ATOMIC) return SK_EINVAL;
+    if (M == 0 || N == 0) return SK_OK;
+    if (!C || !aligned(C, 16) || N % 8 != 0) return SK_EINVAL;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const size_t esz = c_dtype == SK_BF16 ? 2 : 4;
+    if (K == 0) {
+        return cudaMemsetAsync(C, 0, static_cast<size_t>(M) * N * esz, st) == cudaSuccess ? SK_OK : SK_ECUDA;
+    }
+    if (!A || !B || !aligned(A, 16) || !aligned(B, 16) || K % 8 != 0) return SK_EINVAL;
+    Sched sch;
+    int32_t e = make_sched(M, N, K, num_sms, s, sch);
+    if (e != SK_OK) return e;
+    const int64_t need = workspace_bytes(sch, M, N);
+    if (!workspace || !aligned(workspace, 256) || static_cast<int64_t>(ws_bytes) < need) return SK_EWORKSPACE;
+
+    int dev_sms = 0, ctas = 0;
+    if (device_info(&dev_sms, &ctas) != cudaSuccess) return SK_ECUDA;
+    if (static_cast<int64_t>(sch.workers) > static_cast<int64_t>(dev_sms) * ctas) return SK_ERESIDENCY;
+
+    CUtensorMap tmA, tmB;
+    if (!encode_2d(&tmA, A, static_cast<uint64_t>(K), static_cast<uint64_t>(M), kBlkK, kTileM)) return SK_ECUDA;
+    const bool nt = layout == SK_NT;
+    const bool okb = nt ? encode_2d(&tmB, B, static_cast<uint64_t>(K), static_cast<uint64_t>(N), kBlkK, kTileN)
+                        : encode_2d(&tmB, B, static_cast<uint64_t>(N), static_cast<uint64_t>(K), 64, kBlkK);
+    if (!okb) return SK_ECUDA;
+
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    KArgs a = {};
+    a.sch = sch;
+    a.C = C;
+    a.status = reinterpret_cast<int32_t*>(ws);
+    a.flags = reinterpret_cast<int32_t*>(ws + flags_offset());
+    a.slots = reinterpret_cast<float*>(ws + slots_offset(sch));
+    a.slabs = sch.partials ? reinterpret_cast<float*>(ws + SK_WS_HEADER_BYTES) : nullptr;
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.c_bf16 = c_dtype == SK_BF16 ? 1 : 0;
+    a.atomic = r == SK_ATOMIC ? 1 : 0;
+    a.timeout_ns = static_cast<uint64_t>(kDefaultTimeoutNs);
+    if (opts) {
+        a.reverse = opts->reverse_units ? 1 : 0;
+        a.skip_signal = opts->skip_producer_signal ? 1 : 0;
+        if (opts->timeout_ns > 0) a.timeout_ns = static_cast<uint64_t>(opts->timeout_ns);
+        a.dump = opts->dump;
+        if (a.dump && !aligned(a.dump, 16)) return SK_EINVAL;
+    }
+    if (launch_gemm(tmA, tmB, nt, a, st) != cudaSuccess) {
+        cudaGetLastError();
+        return SK_ECUDA;
+    }
+    if (sch.partials) {
+        if (launch_reduce(a.slabs, C, a.c_bf16, sch.splits, static_cast<int64_t>(M) * N, dev_sms, st) !=
+            cudaSuccess) {
+            cudaGetLastError();
+            return SK_ECUDA;
+        }
+    }
+    return SK_OK;
+}
+
+int32_t sk_gemm(const void* A, const void* B, void* C, sk_dtype c_dtype, int32_t M, int32_t N, int32_t K,
+                sk_layout layout, sk_schedule s, sk_reduction r, int32_t num_sms, void* workspace, size_t ws_bytes,
+                void* stream) {
+    return sk_gemm_debug(A, B, C, c_dtype, M, N, K, layout, s, r, num_sms, workspace, ws_bytes, stream, nullptr);
+}
+
+int32_t sk_reduce_splits(const float* P, void* C, sk_dtype c_dtype, int32_t splits, int64_t mn, void* stream) {
+    if (splits < 1 || mn < 0 || mn % 4 != 0) return SK_EINVAL;
+    if (c_dtype != SK_F32 && c_dtype != SK_BF16) return SK_EINVAL;
+    if (mn == 0) return SK_OK;
+    if (!P || !C || !aligned(P, 16) || !aligned(C, 16)) return SK_EINVAL;
+    int dev_sms = 0, ctas = 0;
+    if (device_info(&dev_sms, &ctas) != cudaSuccess) return SK_ECUDA;
+    if (launch_reduce(P, C, c_dtype == SK_BF16 ? 1 : 0, splits, mn, dev_sms, static_cast<cudaStream_t>(stream)) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return SK_ECUDA;
+    }
+    return SK_OK;
+}
+
+int32_t sk_status(void* workspace, void* stream) {
+    if (!workspace) return SK_EWORKSPACE;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(st) != cudaSuccess) return SK_ECUDA;
+    int32_t v = 0;
+    if (cudaMemcpy(&v, workspace, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return SK_ECUDA;
+    if (v != SK_OK) {
+        const int32_t zero = SK_OK;
+        if (cudaMemcpy(workspace, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return SK_ECUDA;
+    }
+    return v;
+}
+
+}  // extern "C"

@@ -1,0 +1,162 @@
+// sk_schedule.h - the work decomposition, shared by the host planner (sk_plan) and the
+// persistent GEMM kernel. Both walk a unit's segments with SkWalk, so the map that
+// sk_plan reports is, segment for segment, what each CTA executes.
+//
+// Sources: "Split-K and Stream-K: The Last Wave of a GEMM" (kanthi.in): Mental model
+// (roles, k = 0 owner), Case 2 (data_parallel, split_k, stream_k_units,
+// cutlass_heuristic, hybrid), Case 4 (decomposition modes). Readings where the page
+// leaves a step open are stated at each branch.
+#pragma once
+#include <stdint.h>
+
+#if defined(__CUDACC__)
+#define SK_HD __host__ __device__ __forceinline__
+#else
+#define SK_HD inline
+#endif
+
+namespace sk {
+
+enum Mode : int32_t { kDP = 0, kSplitK = 1, kStreamK = 2, kHybrid = 3 };
+enum Role : int32_t { kFull = 0, kOwner = 1, kProducer = 2, kSlab = 3 };
+enum Label : int32_t { kLabelNone = -1, kLabelDP = 0, kLabelSplitK = 1, kLabelStreamK = 2 };
+
+constexpr int32_t kTileM = 128;
+constexpr int32_t kTileN = 128;
+constexpr int32_t kBlkK = 64;
+
+// Everything a unit needs to enumerate its segments; O(1) in size.
+struct Sched {
+    int32_t mode;          // resolved mode
+    int32_t tiles, iters, tiles_n;
+    int32_t workers;       // persistent units launched
+    // Stream-K region: tiles [sk_base, sk_base + sk_tiles) over sk_units units,
+    // unit u owning flattened iterations [u*q + min(u, big), (u+1)*q + min(u+1, big)).
+    int32_t sk_tiles, sk_units, sk_q, sk_big, sk_base;
+    // Data-parallel region: tiles [0, dp_tiles), unit w runs w, w + workers, ...
+    int32_t dp_tiles;
+    // Split-K: effective split count, k-iterations per split, slab mode flag.
+    int32_t splits, chunk, partials;
+    int32_t label, label_splits, n_slots;
+};
+
+struct Seg {
+    int32_t tile, k_begin, k_end, role, slot, peer_begin, n_peers;
+};
+
+SK_HD int32_t cdiv(int32_t a, int32_t b) { return (a + b - 1) / b; }
+SK_HD int32_t imin(int32_t a, int32_t b) { return a < b ? a : b; }
+SK_HD int32_t imax(int32_t a, int32_t b) { return a > b ? a : b; }
+
+// First flattened iteration of Stream-K unit u (divmod split, the first `big` units
+// one iteration longer: Case 2 stream_k_units).
+SK_HD int32_t sk_unit_begin(const Sched& s, int32_t u) { return u * s.sk_q + imin(u, s.sk_big); }
+
+// The unit whose range holds flattened iteration i.
+SK_HD int32_t sk_unit_of(const Sched& s, int32_t i) {
+    const int32_t edge = s.sk_big * (s.sk_q + 1);
+    return i < edge ? i / (s.sk_q + 1) : s.sk_big + (i - edge) / s.sk_q;
+}
+
+// Iterator over one unit's segments in run order: its Stream-K range first (if any),
+// then its data-parallel tiles or Split-K work items.
+struct Walk {
+    int32_t unit;
+    int32_t phase;   // 0: Stream-K range, 1: strided items, 2: done
+    int32_t it, end; // Stream-K cursor / end, or the next item index
+
+    SK_HD void init(const Sched& s, int32_t w) {
+        unit = w;
+        if ((s.mode == kStreamK || s.mode == kHybrid) && w < s.sk_units) {
+            phase = 0;
+            it = sk_unit_begin(s, w);
+            end = sk_unit_begin(s, w + 1);
+        } else {
+            phase = 1;
+            it = w;
+            end = 0;
+        }
+    }
+
+    SK_HD int32_t n_items(const Sched& s) const {
+        return s.mode == kSplitK ? s.tiles * s.splits : s.dp_tiles;
+    }
+
+    SK_HD bool next(const Sched& s, Seg& g) {
+        if (phase == 0) {
+            if (it < end) {
+                // One segment: the rest of the current tile inside this unit's range.
+                const int32_t local = it / s.iters;
+                const int32_t tb = local * s.iters;
+                const int32_t te = tb + s.iters;
+                const int32_t se = imin(end, te);
+                g.tile = s.sk_base + local;
+                g.k_begin = it - tb;
+                g.k_end = se - tb;
+                g.slot = -1;
+                g.peer_begin = -1;
+                g.n_peers = 0;
+                if (g.k_begin == 0 && g.k_end == s.iters) {
+                    g.role = kFull;
+                } else if (g.k_begin == 0) {
+                    // k = 0 holder owns the fixup; its peers are the later units whose
+                    // ranges start before the tile ends, i.e. up to the unit of te - 1.
+                    g.role = kOwner;
+                    g.peer_begin = unit + 1;
+                    g.n_peers = sk_unit_of(s, te - 1) - unit;
+                } else {
+                    // Partial handed to the owner; one slot per unit (its index).
+                    g.role = kProducer;
+                    g.slot = unit;
+                    g.peer_begin = sk_unit_of(s, tb) + 1;
+                }
+                it = se;
+                return true;
+            }
+            phase = 1;
+            it = unit;
+        }
+        if (phase == 1) {
+            if (it < n_items(s)) {
+                g.slot = -1;
+                g.peer_begin = -1;
+                g.n_peers = 0;
+                if (s.mode == kSplitK) {
+                    // Work items queued tile by tile with the owner (split 0) last, so a
+                    // unit never waits on an item queued behind it.
+                    const int32_t t = it / s.splits;
+                    const int32_t j = s.splits - 1 - it % s.splits;
+                    g.tile = t;
+                    g.k_begin = j * s.chunk;
+                    g.k_end = imin(g.k_begin + s.chunk, s.iters);
+                    const int32_t base = t * (s.splits - 1);
+                    if (s.partials) {
+                        g.role = kSlab;
+                        g.slot = j;
+                    } else if (s.splits == 1) {
+                        g.role = kFull;
+                    } else if (j == 0) {
+                        g.role = kOwner;
+                        g.peer_begin = base;
+                        g.n_peers = s.splits - 1;
+                    } else {
+                        g.role = kProducer;
+                        g.slot = base + j - 1;
+                        g.peer_begin = base;
+                    }
+                } else {
+                    g.tile = it;
+                    g.k_begin = 0;
+                    g.k_end = s.iters;
+                    g.role = kFull;
+                }
+                it += s.workers;
+                return true;
+            }
+            phase = 2;
+        }
+        return false;
+    }
+};
+
+}  // namespace sk

@@ -1,0 +1,180 @@
+/*
+ * sk.h - C ABI of the work-decomposed BF16 GEMM for GB300 (sm_103a).
+ *
+ * C = A . B with BF16 inputs and FP32 accumulation, the output tiles and their
+ * K loops spread over persistent CTAs by one of four schedules: data-parallel,
+ * Split-K, Stream-K, or the hybrid rule ("Split-K and Stream-K: The Last Wave of
+ * a GEMM", kanthi.in: Mental model, Case 2 and Case 4).
+ *
+ * Conventions shared by every entry point
+ *   - Output tile 128 x 128, MAC-loop iteration BK = 64 (page above, Mental model
+ *     table and Case 2): tiles = ceil(M/128) * ceil(N/128), iters = ceil(K/64).
+ *     Tile t covers rows (t / tiles_n) * 128 and columns (t % tiles_n) * 128.
+ *   - A is [M, K] row-major BF16. Layout SK_NN: B is [K, N] row-major. Layout
+ *     SK_NT: B is stored [N, K] row-major ("Consecutive-B split-K NAX GEMM",
+ *     Contract). C is [M, N] row-major, FP32 or BF16 (round to nearest even,
+ *     once, after the fixup).
+ *   - The caller owns every buffer. No entry point allocates memory.
+ *   - Device pointers are plain CUDA device addresses; `stream` is a cudaStream_t
+ *     (NULL = the legacy default stream). sk_gemm and sk_reduce_splits are
+ *     asynchronous on that stream.
+ *   - Return value: SK_OK (0) or a negative SK_E* code; sk_strerror names it.
+ */
+#ifndef SK_H_
+#define SK_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Decomposition modes ("Split-K and Stream-K: The Last Wave of a GEMM", Case 4:
+ * DataParallel | SplitK | StreamK | Heuristic). SK_HYBRID is the heuristic:
+ * data-parallel when the tail wave is at least half full, otherwise the last
+ * two waves' tiles go to Stream-K with at least min_iters k-iterations per unit
+ * (Case 2, cutlass_heuristic and hybrid). */
+typedef enum { SK_DP = 0, SK_SPLITK = 1, SK_STREAMK = 2, SK_HYBRID = 3 } sk_mode;
+typedef enum { SK_NN = 0, SK_NT = 1 } sk_layout;
+/* Reduction modes (Case 4): deterministic = the owner adds its peers' FP32
+ * partials in k order (a turnstile); atomic = peers add FP32 partials into one
+ * workspace tile with atomics, so rounding depends on arrival order once a tile
+ * has three or more contributors (Case 3). */
+typedef enum { SK_DETERMINISTIC = 0, SK_ATOMIC = 1 } sk_reduction;
+typedef enum { SK_F32 = 0, SK_BF16 = 1 } sk_dtype;
+/* Segment roles in the work-unit map. FULL: one unit runs the whole K loop of a
+ * tile and writes C. OWNER: the unit holding the tile's k = 0 iteration; it waits
+ * for its peers, adds their partials and writes C. PRODUCER: a later segment of a
+ * split tile; it stores its FP32 partial and raises a flag (Mental model; Case 2
+ * stream_k_units). SLAB: a Split-K split that writes its own FP32 [M,N] slab,
+ * reduced afterwards by sk_reduce_splits (split-K report, Contract). */
+typedef enum { SK_ROLE_FULL = 0, SK_ROLE_OWNER = 1, SK_ROLE_PRODUCER = 2, SK_ROLE_SLAB = 3 } sk_role;
+
+typedef struct {
+    int32_t mode;           /* sk_mode */
+    int32_t splits;         /* Split-K split count s, 1 <= s <= iters (SK_SPLITK only) */
+    int32_t units;          /* 0: num_sms persistent units; > 0: use this many instead */
+    int32_t min_iters;      /* hybrid rule's minimum k-iterations per Stream-K unit; 0 = 8 */
+    int32_t split_partials; /* SK_SPLITK only: 1 = every split writes an FP32 slab into the
+                               workspace and a second kernel reduces the slabs into C */
+} sk_schedule;
+
+#define SK_OK          0
+#define SK_EINVAL     -1  /* bad argument: sizes, schedule, alignment or layout */
+#define SK_EWORKSPACE -2  /* workspace missing, misaligned or smaller than sk_workspace_size */
+#define SK_ECUDA      -3  /* a CUDA runtime or driver call failed */
+#define SK_ETIMEOUT   -4  /* a device-side wait ran past its time limit (from sk_status) */
+#define SK_ECAPACITY  -5  /* sk_plan: the map buffer is smaller than sk_plan_size */
+#define SK_ERESIDENCY -6  /* more persistent units than the device can hold at once */
+
+#define SK_TILE_M 128
+#define SK_TILE_N 128
+#define SK_BLK_K 64
+
+/* Work-unit map layout (int32). Header of SK_MAP_HEADER values:
+ *   [0] version (SK_MAP_VERSION)   [1] resolved mode (sk_mode; the hybrid rule resolves
+ *   to SK_DP or SK_HYBRID)   [2] tiles   [3] iters   [4] workers = units launched
+ *   [5] sk_tiles: tiles in the Stream-K region (the last sk_tiles tile ids)
+ *   [6] sk_units: units over that region   [7] n_segments
+ *   [8] splits: effective Split-K split count (empty trailing splits dropped), else 0
+ *   [9] hybrid label (-1 none, 0 DataParallel, 1 SplitK, 2 StreamK)
+ *   [10] the label's split count   [11] n_slots: FP32 partial-tile slots used
+ * then n_segments rows of SK_MAP_SEG values, in (unit, run order) order:
+ *   unit, order, tile, k_begin, k_end, role, slot, peer_begin, n_peers
+ *   (k_begin/k_end in k-iterations; PRODUCER: slot = its partial slot; OWNER: its peers'
+ *   partials are slots peer_begin .. peer_begin + n_peers - 1 in k order; PRODUCER rows
+ *   carry their owner's peer_begin, which is also the tile's slot in atomic mode;
+ *   SLAB: slot = split index; unused fields are -1 or 0)
+ * then `tiles` rows of SK_MAP_TILE values: owner unit (runs k = 0), contributors. */
+#define SK_MAP_VERSION 1
+#define SK_MAP_HEADER 12
+#define SK_MAP_SEG 9
+#define SK_MAP_TILE 2
+
+/* Workspace layout: bytes [0, SK_WS_HEADER_BYTES) hold the device status word
+ * (int32 at offset 0). In split-partials mode the FP32 slabs P[j][M][N] follow at
+ * offset SK_WS_HEADER_BYTES, j = 0 .. splits-1, row-major. In the other modes one
+ * int32 flag (or counter) per slot follows, then the 64 KiB partial slots. */
+#define SK_WS_HEADER_BYTES 256
+
+/* Number of int32 values sk_plan writes for this problem, or a negative SK_E* code.
+ * M, N, K >= 1; num_sms >= 1 (the SM count the schedule is built for). */
+int64_t sk_plan_size(int32_t M, int32_t N, int32_t K, int32_t num_sms, sk_schedule s);
+
+/* Write the work-unit map (layout above) into the host buffer `map` of `cap` int32.
+ * Host-only; touches no GPU. Each persistent unit of sk_gemm runs exactly the
+ * segments listed for it here, in this order. Stream-K ranges use q, big =
+ * divmod(tiles * iters, units) with the first `big` units one iteration longer
+ * (Case 2 stream_k_units; "Try this" calls it the CUTLASS split). Returns SK_OK,
+ * SK_EINVAL, or SK_ECAPACITY when cap < sk_plan_size. */
+int32_t sk_plan(int32_t M, int32_t N, int32_t K, int32_t num_sms, sk_schedule s,
+                int32_t* map, int64_t cap);
+
+/* Bytes of device workspace sk_gemm needs for this problem, schedule and reduction
+ * (at least SK_WS_HEADER_BYTES), or a negative SK_E* code. Host-only.
+ * The workspace must be 256-byte aligned and ZERO-FILLED before its first use; a
+ * successful sk_gemm leaves every flag, counter and atomic slot at zero again, so
+ * the same workspace can be reused call after call without clearing. */
+int64_t sk_workspace_size(int32_t M, int32_t N, int32_t K, int32_t num_sms, sk_schedule s,
+                          sk_reduction r);
+
+/* C = A . B on `stream` (Mental model; Case 2; Case 4 of the page above).
+ * A: device [M,K] BF16; B: device BF16, [K,N] (SK_NN) or [N,K] (SK_NT); C: device
+ * [M,N] of c_dtype. Requirements: K % 8 == 0 and N % 8 == 0 (16-byte row strides for
+ * the tensor-memory-access loads and vector stores); A and B 16-byte aligned, C
+ * 16-byte aligned; inputs must not overlap C or the workspace. M == 0 or N == 0 does
+ * nothing; K == 0 writes zeros. The persistent units run as one cooperative launch
+ * of `workers` CTAs, one per SM, so workers may not exceed the device's SM count
+ * (else SK_ERESIDENCY). Errors are returned before anything is enqueued. A device-side
+ * wait that runs past its limit makes the kernel stop early and record SK_ETIMEOUT in
+ * the workspace status word (read it with sk_status); C is then undefined and the
+ * workspace must be zero-filled again before reuse. Concurrent calls must not share
+ * a workspace. */
+int32_t sk_gemm(const void* A, const void* B, void* C, sk_dtype c_dtype,
+                int32_t M, int32_t N, int32_t K, sk_layout layout, sk_schedule s,
+                sk_reduction r, int32_t num_sms, void* workspace, size_t ws_bytes,
+                void* stream);
+
+/* Diagnostic controls for sk_gemm_debug (used by the tests; sk_gemm uses the defaults). */
+typedef struct {
+    int32_t reverse_units;        /* 1: CTA b runs unit workers-1-b, another dispatch order of
+                                     the same units (the page's Case 3 varies arrival order
+                                     with a unit permutation) */
+    int32_t skip_producer_signal; /* 1: producers store their partials but never raise their
+                                     flag, so every owner's wait runs out (time-out test) */
+    int64_t timeout_ns;           /* limit of every device-side wait, from kernel start;
+                                     0 = the default of 2 s */
+    float* dump;                  /* NULL, or a device buffer of tiles * iters * 16384 FP32:
+                                     the segment of tile t starting at k-iteration k writes
+                                     its own accumulator (before any fixup), row-major
+                                     128 x 128, at offset (t * iters + k) * 16384 */
+} sk_debug_opts;
+
+/* sk_gemm with diagnostic controls; opts == NULL behaves exactly like sk_gemm. */
+int32_t sk_gemm_debug(const void* A, const void* B, void* C, sk_dtype c_dtype,
+                      int32_t M, int32_t N, int32_t K, sk_layout layout, sk_schedule s,
+                      sk_reduction r, int32_t num_sms, void* workspace, size_t ws_bytes,
+                      void* stream, const sk_debug_opts* opts);
+
+/* Split-K reduction pass ("Consecutive-B split-K NAX GEMM", Contract: FP32 partials
+ * [splits, M, N] reduced by an accumulation kernel; first page, Case 3 fixup_kernel
+ * sums partials in k order). C[i] = P[0][i] + P[1][i] + ... + P[splits-1][i], summed
+ * left to right in FP32, then stored as c_dtype. P: device FP32, `splits` slabs of
+ * `mn` values each, 16-byte aligned; C: device, 16-byte aligned; mn % 4 == 0. */
+int32_t sk_reduce_splits(const float* P, void* C, sk_dtype c_dtype, int32_t splits,
+                         int64_t mn, void* stream);
+
+/* Synchronise `stream`, read the workspace status word, reset it to SK_OK and return
+ * it: SK_OK, or SK_ETIMEOUT when a kernel on that workspace stopped at a wait limit.
+ * Returns SK_ECUDA if the copy fails. */
+int32_t sk_status(void* workspace, void* stream);
+
+/* Static description of an SK_* code. */
+const char* sk_strerror(int32_t code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SK_H_ */

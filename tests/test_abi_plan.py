@@ -1,0 +1,148 @@
+"""The C ABI on the host: the library loads and exports every declared entry point, and
+sk_plan's work-unit map equals the oracle's bit for bit.
+
+The kernel walks each unit's segments with the same code that writes this map, so the map
+comparison checks the device's schedule too. No GPU is used here.
+"""
+import ctypes
+import itertools
+import os
+import re
+
+import numpy as np
+import pytest
+
+from oracle import schedule as S
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def sk():
+    from gemm_work_decomposition_gb300 import build
+    build.build()
+    import gemm_work_decomposition_gb300 as pkg
+    pkg.lib()
+    return pkg
+
+
+def _declared():
+    names = set()
+    inc = os.path.join(ROOT, "include")
+    for f in os.listdir(inc):
+        if f.endswith(".h"):
+            text = open(os.path.join(inc, f)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names |= set(re.findall(r"\b(sk_[a-z_0-9]+)\s*\(", text))
+    return names
+
+
+def test_exports_every_declared_symbol(sk):
+    declared = _declared()
+    assert {"sk_plan", "sk_plan_size", "sk_gemm", "sk_workspace_size", "sk_status", "sk_strerror",
+            "sk_reduce_splits", "sk_gemm_debug"} <= declared
+    lib = ctypes.CDLL(sk.LIB_PATH)
+    for name in sorted(declared):
+        assert hasattr(lib, name), name
+    assert set(sk.EXPORTS) == declared
+
+
+def _cmp(sk, M, N, K, sms, mode, splits=1, units=0, min_iters=0, partials=0):
+    want = S.plan_map(S.build_plan(M, N, K, sms, mode, splits=splits, units=units,
+                                   min_iters=min_iters or 8, split_partials=bool(partials)))
+    got = sk.sk_plan(M, N, K, sms, sk.schedule(mode, splits, units, min_iters, partials))
+    assert got.tolist() == want, (M, N, K, sms, mode, splits, units, partials)
+    return got
+
+
+def test_plan_matches_oracle_on_workloads(sk):
+    cases = [
+        (128, 640, 256, 4, S.DP), (128, 640, 256, 4, S.STREAMK),            # toy, forced to 4 units
+        (2048, 2432, 4096, 148, S.DP), (2048, 2432, 4096, 148, S.STREAMK),  # wave-quantized
+        (2048, 2432, 4096, 148, S.HYBRID), (2048, 2432, 4096, 152, S.HYBRID),
+        (96, 512, 2048, 148, S.STREAMK), (256, 512, 2048, 148, S.STREAMK),  # small-M NT
+        (96, 512, 2048, 148, S.HYBRID), (256, 512, 2048, 148, S.HYBRID),
+        (8192, 8192, 8192, 148, S.HYBRID), (512, 512, 65536, 148, S.HYBRID),
+        (512, 512, 65536, 148, S.STREAMK),
+    ]
+    for M, N, K, sms, mode in cases:
+        _cmp(sk, M, N, K, sms, mode)
+    for s in (2, 4, 8, 16):
+        for M in (96, 256):
+            _cmp(sk, M, 512, 2048, 148, S.SPLITK, splits=s, partials=1)
+            _cmp(sk, M, 512, 2048, 148, S.SPLITK, splits=s)
+    _cmp(sk, 2048, 2432, 4096, 148, S.SPLITK, splits=2)
+    for m in range(128, 4097, 128):
+        for mode in (S.DP, S.STREAMK, S.HYBRID):
+            _cmp(sk, m, m, 4096, 148, mode)
+        for s in (2, 4):
+            _cmp(sk, m, m, 4096, 148, S.SPLITK, splits=s)
+
+
+def test_plan_toy_units_override(sk):
+    a = _cmp(sk, 128, 640, 256, 148, S.STREAMK, units=4)
+    b = _cmp(sk, 128, 640, 256, 4, S.STREAMK)
+    assert np.array_equal(a, b)
+
+
+def test_plan_bruteforce_small(sk):
+    # M, N <= 640, K <= 512, 1..20 SMs, every mode.
+    for M, N, K in itertools.product((1, 128, 129, 300, 640), (8, 128, 256, 640), (8, 64, 65, 200, 512)):
+        for sms in range(1, 21):
+            for mode in (S.DP, S.STREAMK, S.HYBRID):
+                _cmp(sk, M, N, K, sms, mode)
+            iters = S.cdiv(K, 64)
+            for s in range(1, min(iters, 5) + 1):
+                _cmp(sk, M, N, K, sms, S.SPLITK, splits=s)
+                _cmp(sk, M, N, K, sms, S.SPLITK, splits=s, partials=1)
+
+
+def test_plan_min_iters(sk):
+    for mi in (1, 4, 8, 16, 64):
+        for m in (1536, 1664, 3840):
+            _cmp(sk, m, m, 4096, 132, S.HYBRID, min_iters=mi)
+
+
+def test_workspace_size(sk):
+    for M, N, K, sms, mode, s, part in [(2048, 2432, 4096, 148, S.HYBRID, 1, 0), (128, 640, 256, 4, S.STREAMK, 1, 0),
+                                        (96, 512, 2048, 148, S.SPLITK, 8, 1), (2048, 2432, 4096, 148, S.SPLITK, 2, 0),
+                                        (2048, 2432, 4096, 148, S.DP, 1, 0)]:
+        sch = sk.schedule(mode, s, 0, 0, part)
+        m = sk.sk_plan(M, N, K, sms, sch)
+        n_slots, splits = int(m[11]), int(m[8])
+        if part:
+            want = 256 + 4 * splits * M * N
+        else:
+            want = 256 + -(-4 * n_slots // 256) * 256 + n_slots * 65536
+        for r in (sk.SK_DETERMINISTIC, sk.SK_ATOMIC):
+            assert sk.sk_workspace_size(M, N, K, sms, sch, r) == want
+
+
+def test_errors(sk):
+    bad = [
+        (0, 128, 128, 4, sk.schedule(sk.SK_DP)),
+        (128, 128, 128, 0, sk.schedule(sk.SK_DP)),
+        (128, 128, 128, 4, sk.schedule(7)),
+        (128, 128, 128, 4, sk.schedule(sk.SK_SPLITK, 3)),          # s > iters (2)
+        (128, 128, 128, 4, sk.schedule(sk.SK_SPLITK, 0)),
+        (128, 128, 128, 4, sk.schedule(sk.SK_STREAMK, 1, 0, 0, 1)),  # slabs need Split-K
+        (128, 128, 128, 4, sk.schedule(sk.SK_DP, 1, -1)),
+    ]
+    for M, N, K, sms, sch in bad:
+        with pytest.raises(sk.SkError) as e:
+            sk.sk_plan_size(M, N, K, sms, sch)
+        assert e.value.code == sk.SK_EINVAL
+    L = sk.lib()
+    buf = (ctypes.c_int32 * 4)()
+    assert L.sk_plan(128, 640, 256, 4, sk.schedule(sk.SK_STREAMK), buf, 4) == sk.SK_ECAPACITY
+    assert sk.sk_strerror(sk.SK_ETIMEOUT).startswith("a device-side wait")
+    # sk_gemm argument checks happen before any CUDA call.
+    sch = sk.schedule(sk.SK_DP)
+    assert L.sk_gemm(16, 16, 16, sk.SK_F32, 128, 100, 64, sk.SK_NN, sch, 0, 148, 256, 1 << 20, None) == sk.SK_EINVAL
+    assert L.sk_gemm(16, 16, 16, sk.SK_F32, 128, 128, 60, sk.SK_NN, sch, 0, 148, 256, 1 << 20, None) == sk.SK_EINVAL
+    assert L.sk_gemm(16, 16, 17, sk.SK_F32, 128, 128, 64, sk.SK_NN, sch, 0, 148, 256, 1 << 20, None) == sk.SK_EINVAL
+    assert L.sk_gemm(16, 16, 16, sk.SK_F32, 128, 128, 64, sk.SK_NN, sch, 0, 148, 0, 1 << 20, None) == sk.SK_EWORKSPACE
+    assert L.sk_gemm(16, 16, 16, sk.SK_F32, 128, 128, 64, sk.SK_NN, sch, 0, 148, 256, 8, None) == sk.SK_EWORKSPACE
+    assert L.sk_gemm(0, 0, 0, sk.SK_F32, 0, 128, 64, sk.SK_NN, sch, 0, 148, 0, 0, None) == sk.SK_OK
+    assert L.sk_reduce_splits(16, 16, sk.SK_F32, 0, 64, None) == sk.SK_EINVAL
+    assert L.sk_reduce_splits(16, 16, sk.SK_F32, 2, 6, None) == sk.SK_EINVAL

@@ -1,0 +1,306 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle.
+
+Every schedule (data-parallel, Split-K, Stream-K, hybrid), both reductions (deterministic
+turnstile, FP32 atomics) and both layouts (NN, NT) on the workloads' shapes, at sizes that
+span several tiles with ragged edges, and at the full workload sizes. Pass criteria per
+result: max |err| <= 2e-2 * max(1, |ref|) and relative Frobenius error <= 5e-3 against the
+FP64 oracle, for the whole matrix and for every 128 x 128 tile; integer-valued inputs must
+match exactly; sentinels and guards as in the split-K report's protocol.
+"""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from oracle import gemm as og
+from oracle import schedule as osch
+
+from . import gpu_util as U
+
+pytestmark = pytest.mark.gpu
+
+DET, ATOM = 0, 1
+
+
+@pytest.fixture(scope="module")
+def sk():
+    import __graft_entry__ as ge
+    ge.build()
+    import gemm_work_decomposition_gb300 as pkg
+    return pkg
+
+
+@pytest.fixture(scope="module")
+def dev():
+    assert torch.cuda.is_available()
+    return torch.device("cuda:0")
+
+
+@pytest.fixture(scope="module")
+def dev_sms(dev):
+    return torch.cuda.get_device_properties(dev).multi_processor_count
+
+
+def _run(sk, dev, w, sched, red, sms, ws=None, **debug):
+    A_bits, B_bits = U.inputs(w)
+    A, B = U.to_dev(A_bits, dev), U.to_dev(B_bits, dev)
+    got, guards, ws, status = U.gemm(sk, A, B, w.M, w.N, w.K, w.layout, sched, red, sms, w.out, dev, ws, **debug)
+    assert status == sk.SK_OK
+    assert guards
+    return got, ws
+
+
+SCHEDULES = [
+    ("dp", dict(mode=0)),
+    ("splitk2", dict(mode=1, splits=2)),
+    ("splitk3", dict(mode=1, splits=3)),
+    ("streamk", dict(mode=2)),
+    ("hybrid", dict(mode=3)),
+    ("slabs2", dict(mode=1, splits=2, split_partials=1)),
+]
+
+
+# --------------------------------------------------------------------------- toy
+@pytest.mark.parametrize("red", [DET, ATOM])
+@pytest.mark.parametrize("name,kw", SCHEDULES)
+def test_toy(sk, dev, name, kw, red):
+    # 5 tiles x 4 k-iterations on 4 units (Mental model figure).
+    w = synth.TOY
+    sched = sk.schedule(units=4, **kw)
+    got, _ = _run(sk, dev, w, sched, red, 4)
+    assert not np.any(got == U.SENTINEL)
+    U.assert_close(got, U.reference(w), name)
+
+
+# --------------------------------------------------------------------------- exact
+@pytest.mark.parametrize("layout", ["NN", "NT"])
+@pytest.mark.parametrize("red", [DET, ATOM])
+@pytest.mark.parametrize("sms", [3, 7, 152])
+@pytest.mark.parametrize("name,kw", SCHEDULES)
+def test_integer_exact(sk, dev, name, kw, red, sms, layout):
+    # Ragged in M, N and K (300 x 264 x 520: 3 x 3 tiles, 9 k-iterations, the last one
+    # 8 deep); integer inputs in [-4, 4] keep every partial sum exact in FP32, so every
+    # schedule and reduction must equal the oracle exactly.
+    M, N, K = 300, 264, 520
+    A_bits, B_bits = synth.small_int_inputs(M, N, K, layout, 17)
+    A, B = U.to_dev(A_bits, dev), U.to_dev(B_bits, dev)
+    ref = og.ref_gemm(A_bits, B_bits, layout)
+    got, guards, _, status = U.gemm(sk, A, B, M, N, K, layout, sk.schedule(**kw), red, sms, "f32", dev)
+    assert status == sk.SK_OK and guards
+    assert np.array_equal(got, ref)
+    # BF16 output: the exact value rounded once to nearest even.
+    got16, guards, _, status = U.gemm(sk, A, B, M, N, K, layout, sk.schedule(**kw), red, sms, "bf16", dev)
+    assert status == sk.SK_OK and guards
+    want16 = torch.from_numpy(ref.astype(np.float32)).to(torch.bfloat16).float().numpy()
+    assert np.array_equal(got16, want16.astype(np.float64))
+
+
+# --------------------------------------------------------------------------- wave-quantized
+@pytest.mark.parametrize("red", [DET, ATOM])
+@pytest.mark.parametrize("name,kw,sms", [
+    ("dp", dict(mode=0), 148), ("splitk2", dict(mode=1, splits=2), 148), ("streamk", dict(mode=2), 148),
+    ("hybrid", dict(mode=3), 148), ("hybrid_dev", dict(mode=3), None), ("streamk_dev", dict(mode=2), None)])
+def test_waveq_full(sk, dev, dev_sms, name, kw, sms, red):
+    # 2048 x 2432 x 4096: 304 tiles = 2 waves + 8 on 148 SMs, BF16 out; full comparison.
+    w = synth.WAVEQ
+    got, _ = _run(sk, dev, w, sk.schedule(**kw), red, sms or dev_sms)
+    U.assert_close(got, U.reference(w), name)
+
+
+def test_waveq_atomic_equals_deterministic_two_contributors(sk, dev):
+    # The hybrid plan splits each tile over at most 2 units; 0 + a + b = 0 + b + a, so the
+    # atomic reduction gives the deterministic bits here (first page, Case 3).
+    w = synth.WAVEQ
+    sched = sk.schedule(3)
+    m = sk.sk_plan(w.M, w.N, w.K, 148, sched)
+    assert max(m[-2 * int(m[2]) + 1::2]) == 2
+    det, _ = _run(sk, dev, w, sched, DET, 148)
+    atom, _ = _run(sk, dev, w, sched, ATOM, 148)
+    assert np.array_equal(det, atom)
+
+
+# --------------------------------------------------------------------------- small-M NT
+@pytest.mark.parametrize("w", [synth.SMALLM_96, synth.SMALLM_256], ids=["m96", "m256"])
+@pytest.mark.parametrize("s", [2, 4, 8, 16])
+def test_smallm_split_slabs(sk, dev, dev_sms, w, s):
+    # [splits, M, N] FP32 slabs then the reduction pass (split-K report, Contract): every
+    # slab against FP64 dot products over its own K range, and the reduced C.
+    sched = sk.schedule(1, splits=s, split_partials=1)
+    got, (ws, _) = _run(sk, dev, w, sched, DET, dev_sms)
+    A_bits, B_bits = U.inputs(w)
+    P_ref = og.ref_split_partials(A_bits, B_bits, "NT", s)
+    P = ws[sk.SK_WS_HEADER_BYTES:sk.SK_WS_HEADER_BYTES + 4 * s * w.M * w.N].view(torch.float32)
+    P = P.cpu().numpy().astype(np.float64).reshape(s, w.M, w.N)
+    for j in range(s):
+        U.assert_close(P[j], P_ref[j], f"slab {j}")
+        assert np.abs(P[j] - P_ref[j]).max() <= 1e-4 * max(1.0, np.abs(P_ref[j]).max())
+    ref = U.reference(w)
+    U.assert_close(got, ref, "reduced")
+    # A row 0 = 0 -> C row 0 is exactly +0.
+    assert np.all(got[0] == 0.0) and not np.any(np.signbit(got[0]))
+    # The reduction sums the slabs left to right in FP32.
+    fold = P[0].astype(np.float32)
+    for j in range(1, s):
+        fold = fold + P[j].astype(np.float32)
+    assert np.array_equal(got, fold.astype(np.float64))
+
+
+@pytest.mark.parametrize("w", [synth.SMALLM_96, synth.SMALLM_256], ids=["m96", "m256"])
+@pytest.mark.parametrize("name,kw", [("streamk", dict(mode=2)), ("hybrid", dict(mode=3)),
+                                     ("splitk4", dict(mode=1, splits=4)), ("dp", dict(mode=0))])
+@pytest.mark.parametrize("red", [DET, ATOM])
+def test_smallm_fixup(sk, dev, w, name, kw, red):
+    got, _ = _run(sk, dev, w, sk.schedule(**kw), red, 148)
+    ref = U.reference(w)
+    U.assert_close(got, ref, name)
+    assert np.all(got[0] == 0.0)
+    assert np.abs(got - ref).max() <= 1e-4 * max(1.0, np.abs(ref).max())
+
+
+# --------------------------------------------------------------------------- sweep
+@pytest.mark.parametrize("m", [128, 640, 1152, 1536, 2560, 4096])
+@pytest.mark.parametrize("name,kw", [("dp", dict(mode=0)), ("splitk2", dict(mode=1, splits=2)),
+                                     ("streamk", dict(mode=2)), ("hybrid", dict(mode=3))])
+def test_sweep(sk, dev, m, name, kw):
+    w = synth.sweep(m)
+    got, _ = _run(sk, dev, w, sk.schedule(**kw), DET, 148)
+    A_bits, B_bits = U.inputs(w)
+    rows = U.sample_rows(m, 32, seed=m)
+    U.assert_close(got[rows], og.ref_rows(A_bits, B_bits, "NN", rows), name)
+
+
+# --------------------------------------------------------------------------- large / long-K
+@pytest.mark.parametrize("name,kw", [("hybrid", dict(mode=3)), ("streamk", dict(mode=2))])
+def test_skinny_long_k(sk, dev, name, kw):
+    # 512 x 512 x 65536: 16 tiles x 1024 k-iterations, up to 11 contributors per tile.
+    w = synth.SKINNY
+    got, _ = _run(sk, dev, w, sk.schedule(**kw), DET, 148)
+    U.assert_close(got, U.reference(w), name)
+
+
+def test_large_8192(sk, dev, dev_sms):
+    w = synth.LARGE
+    got, _ = _run(sk, dev, w, sk.schedule(3), DET, dev_sms)
+    A_bits, B_bits = U.inputs(w)
+    rows = U.sample_rows(w.M, 24, seed=5)
+    U.assert_close(got[rows], og.ref_rows(A_bits, B_bits, "NN", rows), "8192^3")
+
+
+# --------------------------------------------------------------------------- determinism
+@pytest.mark.parametrize("w,sched_kw,units", [
+    (synth.WAVEQ, dict(mode=3), 148), (synth.SKINNY, dict(mode=2), 148),
+    (synth.sweep(256), dict(mode=2), 40)])
+def test_deterministic_repeatable(sk, dev, w, sched_kw, units):
+    # Deterministic mode: bit-identical over 10 runs and under the reversed unit -> CTA
+    # order (the first page's Case 3 varies arrival order through a unit permutation).
+    sched = sk.schedule(**sched_kw)
+    first, ws = _run(sk, dev, w, sched, DET, units)
+    for i in range(9):
+        again, ws = _run(sk, dev, w, sched, DET, units, ws=ws, reverse_units=i % 2)
+        assert np.array_equal(first, again)
+
+
+def test_turnstile_k_order(sk, dev):
+    # FP32 output, Stream-K over 40 units on 4 tiles x 64 iterations (about ten
+    # contributors a tile): C must be the left fold, in k order, of every segment's own
+    # FP32 partial.
+    w = synth.Workload("t256", 256, 256, 4096, "NN", "normal", 31, out="f32")
+    sched = sk.schedule(2, units=40)
+    plan = osch.build_plan(w.M, w.N, w.K, 40, osch.STREAMK)
+    dump = torch.zeros(plan.tiles * plan.iters * 16384, dtype=torch.float32, device=dev)
+    got, _ = _run(sk, dev, w, sched, DET, 40, dump=dump)
+    D = dump.cpu().numpy().reshape(plan.tiles, plan.iters, 128, 128)
+    want = np.zeros((w.M, w.N), dtype=np.float32)
+    most = 0
+    for t in range(plan.tiles):
+        segs = sorted((s for s in plan.segments() if s.tile == t), key=lambda s: s.k_begin)
+        most = max(most, len(segs))
+        acc = D[t, segs[0].k_begin].copy()
+        for s in segs[1:]:
+            acc = acc + D[t, s.k_begin]
+        r0, c0 = (t // plan.tiles_n) * 128, (t % plan.tiles_n) * 128
+        want[r0:r0 + 128, c0:c0 + 128] = acc
+    assert most >= 4
+    assert np.array_equal(got, want.astype(np.float64))
+    U.assert_close(got, U.reference(w), "turnstile")
+
+
+# --------------------------------------------------------------------------- atomics
+def test_atomic_many_contributors(sk, dev):
+    # Skinny shape, up to 11 contributors per tile: within tolerance (bits may vary with
+    # arrival order once a tile has three or more contributors).
+    w = synth.SKINNY
+    got, ws = _run(sk, dev, w, sk.schedule(2), ATOM, 148)
+    U.assert_close(got, U.reference(w), "atomic")
+    again, _ = _run(sk, dev, w, sk.schedule(2), ATOM, 148, ws=ws, reverse_units=1)
+    U.assert_close(again, U.reference(w), "atomic reversed")
+
+
+# --------------------------------------------------------------------------- edges
+@pytest.mark.parametrize("M,N,K", [(1, 8, 8), (1, 8, 4096), (129, 136, 72), (128, 128, 8), (200, 1000, 1000),
+                                   (127, 8, 65536 // 8)])
+@pytest.mark.parametrize("name,kw", [("dp", dict(mode=0)), ("streamk", dict(mode=2)), ("hybrid", dict(mode=3)),
+                                     ("splitk", dict(mode=1, splits=1))])
+def test_edges(sk, dev, M, N, K, name, kw):
+    w = synth.Workload("e", M, N, K, "NT", "normal", 3, out="f32")
+    got, _ = _run(sk, dev, w, sk.schedule(**kw), DET, 152)
+    U.assert_close(got, U.reference(w), name)
+
+
+def test_k_zero_and_empty(sk, dev):
+    C = torch.full((16 * 8 + 64,), 7.0, device=dev)
+    st = torch.cuda.current_stream(dev)
+    sk.sk_gemm(0, 0, C, sk.SK_F32, 16, 8, 0, sk.SK_NN, sk.schedule(0), 0, 148, 0, 0, st)
+    torch.cuda.synchronize()
+    h = C.cpu().numpy()
+    assert np.all(h[:128] == 0.0) and np.all(h[128:] == 7.0)
+    sk.sk_gemm(0, 0, C, sk.SK_F32, 0, 8, 64, sk.SK_NN, sk.schedule(0), 0, 148, 0, 0, st)
+    torch.cuda.synchronize()
+    assert np.all(C.cpu().numpy()[:128] == 0.0)
+
+
+def test_residency_limit(sk, dev, dev_sms):
+    w = synth.sweep(4096)
+    A = torch.zeros((8, 8), dtype=torch.bfloat16, device=dev)
+    ws = torch.zeros(1 << 20, dtype=torch.uint8, device=dev)
+    C = torch.zeros((4096, 4096), dtype=torch.float32, device=dev)
+    with pytest.raises(sk.SkError) as e:
+        sk.sk_gemm(A, A, C, sk.SK_F32, w.M, w.N, w.K, sk.SK_NN, sk.schedule(0), 0, dev_sms + 1, ws, 1 << 20)
+    assert e.value.code == sk.SK_ERESIDENCY
+
+
+# --------------------------------------------------------------------------- reduce pass
+@pytest.mark.parametrize("s,mn,out", [(1, 4096, "f32"), (3, 1 << 20, "f32"), (16, 96 * 512, "bf16")])
+def test_reduce_splits(sk, dev, s, mn, out):
+    P = torch.randn(s * mn, dtype=torch.float32, generator=torch.Generator().manual_seed(s)).to(dev)
+    dt = torch.float32 if out == "f32" else torch.bfloat16
+    C = torch.full((mn + 64,), 11.0, dtype=dt, device=dev)
+    sk.sk_reduce_splits(P, C, sk.SK_F32 if out == "f32" else sk.SK_BF16, s, mn, torch.cuda.current_stream(dev))
+    torch.cuda.synchronize()
+    h = P.cpu().numpy().reshape(s, mn)
+    fold = h[0].copy()
+    for j in range(1, s):
+        fold = fold + h[j]
+    want = torch.from_numpy(fold).to(dt).float().numpy()
+    got = C.float().cpu().numpy()
+    assert np.array_equal(got[:mn], want) and np.all(got[mn:] == 11.0)
+
+
+# --------------------------------------------------------------------------- time-out
+def test_wait_timeout_reports_status(sk, dev):
+    # Producers store but never raise their flag: every owner's wait runs out after 50 ms,
+    # the kernel unwinds and records SK_ETIMEOUT; the context stays usable and the
+    # workspace works again once zeroed.
+    w = synth.TOY
+    sched = sk.schedule(2, units=4)
+    A_bits, B_bits = U.inputs(w)
+    A, B = U.to_dev(A_bits, dev), U.to_dev(B_bits, dev)
+    ws = U.new_workspace(sk, w.M, w.N, w.K, 4, sched, DET, dev)
+    _, _, _, status = U.gemm(sk, A, B, w.M, w.N, w.K, "NN", sched, DET, 4, "f32", dev, ws,
+                             skip_producer_signal=1, timeout_ns=50_000_000)
+    assert status == sk.SK_ETIMEOUT
+    assert sk.sk_status(ws[0]) == sk.SK_OK
+    ws[0].zero_()
+    got, guards, _, status = U.gemm(sk, A, B, w.M, w.N, w.K, "NN", sched, DET, 4, "f32", dev, ws)
+    assert status == sk.SK_OK and guards
+    U.assert_close(got, U.reference(w), "after time-out")
