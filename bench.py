@@ -17,7 +17,6 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
-import math
 import os
 import subprocess
 import sys
@@ -38,7 +37,10 @@ WORKLOADS = {"waveq": synth.WAVEQ, "skinny": synth.SKINNY, "large": synth.LARGE,
 # Per-launch DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of the GEMM kernel
 # from one ncu capture, keyed by workload/schedule; valid only for the kernel source it
 # was taken on (sha256 of sk_kernels.cu, first 16 hex digits).
-TRAFFIC = {}
+TRAFFIC = {
+    "waveq_2048x2432x4096/hybrid@148": {"bytes": 36744704 + 168960, "kernel_sha": "f3a64766608abaf7",
+                                        "profile": "profiles/sk_gemm_kernel_waveq_2048x2432x4096_hybrid148.md"},
+}
 
 
 def load_peaks():
@@ -110,6 +112,27 @@ class ClockSampler:
                     reasons.add(n)
         return {"sm_mhz": float(np.median(mhz)) if mhz else None, "sm_max_mhz": mx or None,
                 "reasons": sorted(reasons), "samples": len(mhz)}
+
+
+def rank_workload(w, rank: int):
+    """Each rank's independent instance: the same shape with its own input seed."""
+    import dataclasses
+    return dataclasses.replace(w, seed=w.seed + 1000 * rank)
+
+
+def max_over_ranks(x: float, dist, device) -> float:
+    """The slowest rank's value (float64 all-reduce MAX); x itself on one rank."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(world: int, flops_per_step: float, steps: int, total_ms: float) -> float:
+    """Whole-job throughput: every rank's steps over the slowest rank's time."""
+    return world * flops_per_step * steps / (total_ms / 1e3) / 1e12
 
 
 def dist_info():
@@ -251,8 +274,7 @@ def main():
     flops = 2.0 * w.M * w.N * w.K
 
     # Inputs: seeded per rank (independent instances), copied once into HBM.
-    wr = synth.Workload(w.name, w.M, w.N, w.K, w.layout, w.dist, w.seed + 1000 * rank, w.zero_first_row,
-                        w.scale_last_row, w.out)
+    wr = rank_workload(w, rank)
     A_bits, B_bits = synth.make_inputs(wr)
     A_host = torch.from_numpy(A_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
     B_host = torch.from_numpy(B_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
@@ -313,13 +335,9 @@ def main():
     if status != sk.SK_OK:
         raise RuntimeError(f"device status {sk.sk_strerror(status)}")
     step_ms = np.array([s.elapsed_time(e) for s, e in ev])
-    total_ms = float(step_ms.sum())
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(float(step_ms.sum()), dist if world > 1 else None, dev)
     ms_per_step = total_ms / args.steps
-    value = world * flops * args.steps / (total_ms / 1e3) / 1e12
+    value = job_tflops(world, flops, args.steps, total_ms)
     kernel_tflops = flops / (ms_per_step / 1e3) / 1e12
 
     extras = {}
