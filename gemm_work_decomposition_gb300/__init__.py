@@ -28,7 +28,8 @@ SK_MAP_VERSION, SK_MAP_HEADER, SK_MAP_SEG, SK_MAP_TILE = 1, 12, 9, 2
 SK_WS_HEADER_BYTES = 256
 
 EXPORTS = ("sk_plan_size", "sk_plan", "sk_workspace_size", "sk_gemm", "sk_gemm_debug", "sk_reduce_splits",
-           "sk_status", "sk_strerror")
+           "sk_status", "sk_strerror", "sk_gemm_noalloc")
+SK_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
 class sk_schedule(ctypes.Structure):
@@ -77,6 +78,8 @@ def lib() -> ctypes.CDLL:
         L.sk_reduce_splits.restype = i32
         L.sk_status.argtypes = [vp, vp]
         L.sk_status.restype = i32
+        L.sk_gemm_noalloc.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, sk_schedule, i32, i32, vp]
+        L.sk_gemm_noalloc.restype = i32
         L.sk_strerror.argtypes = [i32]
         L.sk_strerror.restype = ctypes.c_char_p
         _lib = L
@@ -150,3 +153,10 @@ def sk_status(workspace, stream=None) -> int:
     if code in (SK_ECUDA, SK_EWORKSPACE):
         raise SkError(code, "sk_status")
     return code
+
+
+def sk_gemm_noalloc(A, B, C, c_dtype: int, M: int, N: int, K: int, layout: int, sched: sk_schedule, reduction: int,
+                    num_sms: int, stream=None) -> int:
+    """sk_gemm on the library-owned scratch (no workspace argument); see include/sk.h."""
+    return _check(lib().sk_gemm_noalloc(_ptr(A), _ptr(B), _ptr(C), c_dtype, M, N, K, layout, sched, reduction,
+                                        num_sms, _stream(stream)), "sk_gemm_noalloc")

@@ -165,6 +165,27 @@ int32_t sk_gemm_debug(const void* A, const void* B, void* C, sk_dtype c_dtype,
 int32_t sk_reduce_splits(const float* P, void* C, sk_dtype c_dtype, int32_t splits,
                          int64_t mn, void* stream);
 
+/* Scratch size of sk_gemm_noalloc: 16 MiB of device memory on every GPU that loads the
+ * library, held until the process exits. */
+#define SK_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+/* sk_gemm without a caller workspace, for callers that cannot allocate device memory
+ * (plug-ins whose host application owns every allocation, processes held to a memory
+ * budget fixed at start-up, loops where cudaMalloc / cudaFree would synchronise the
+ * device). The pages have no counterpart: this is a deployment convenience.
+ * Arguments are those of sk_gemm minus the workspace. The scratch is one library-owned
+ * device array of SK_NOALLOC_SCRATCH_BYTES per GPU; problems whose sk_workspace_size
+ * exceeds it return SK_EWORKSPACE and nothing is enqueued. The first call on a device
+ * looks up the array's address with that device current; make it before any stream
+ * capture. Every call enqueues a clear of the part that must start at zero (status word,
+ * flags, and the partial tiles for SK_ATOMIC), then the GEMM. All calls on a device share
+ * the array: calls whose work overlaps on the GPU (other streams, other host threads)
+ * race. A device-side time-out is recorded in the scratch and not reported; use sk_gemm
+ * and sk_status to observe it. Allocates nothing. */
+int32_t sk_gemm_noalloc(const void* A, const void* B, void* C, sk_dtype c_dtype,
+                        int32_t M, int32_t N, int32_t K, sk_layout layout, sk_schedule s,
+                        sk_reduction r, int32_t num_sms, void* stream);
+
 /* Synchronise `stream`, read the workspace status word, reset it to SK_OK and return
  * it: SK_OK, or SK_ETIMEOUT when a kernel on that workspace stopped at a wait limit.
  * Returns SK_ECUDA if the copy fails. */
