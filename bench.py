@@ -3,7 +3,9 @@
 One step = one sk_gemm call: the whole hot path (schedule walk, TMA/tcgen05 MAC loop,
 partial-tile fixup, epilogue) over the workload's synthetic BF16 inputs, resident in HBM.
 Default workload: the wave-quantized GEMM 2048 x 2432 x 4096 (304 tiles of 128 x 128 =
-2 waves + 8 on 148 SMs), BF16 out, the hybrid rule on 148 SMs. Between timed steps a
+2 waves + 8 on 148 SMs), BF16 out, the hybrid rule on 148 SMs, computed with 256 x 256
+CTA-pair tiles (80 tiles on 74 pairs: again 2 waves with a short tail); the per-schedule
+table also reports the pages' 128 x 128 tile. Between timed steps a
 256 MiB buffer is written to flush L2 (the inputs, 47 MB, fit in L2). Each step is timed
 with CUDA events on the launching stream; the headline value is TFLOP/s = 2MNK / time.
 
@@ -38,7 +40,7 @@ WORKLOADS = {"waveq": synth.WAVEQ, "skinny": synth.SKINNY, "large": synth.LARGE,
 # from one ncu capture, keyed by workload/schedule; valid only for the kernel source it
 # was taken on (sha256 of sk_kernels.cu, first 16 hex digits).
 TRAFFIC = {
-    "waveq_2048x2432x4096/hybrid@148": {"bytes": 36744704 + 168960, "kernel_sha": "f3a64766608abaf7",
+    "waveq_2048x2432x4096/hybrid/tile0@148": {"bytes": 36744704 + 168960, "kernel_sha": "f3a64766608abaf7",
                                         "profile": "profiles/sk_gemm_kernel_waveq_2048x2432x4096_hybrid148.md"},
 }
 
@@ -236,6 +238,9 @@ def main():
     ap.add_argument("--sms", type=int, default=148, help="SM count the schedule is built for (0 = device)")
     ap.add_argument("--mode", default="hybrid", choices=["dp", "splitk", "streamk", "hybrid"])
     ap.add_argument("--splits", type=int, default=2)
+    ap.add_argument("--tile", type=int, default=2,
+                    help="work-tile shape: 0 = 128x128 (one CTA), 1 = 256x128 (CTA pair), "
+                         "2 = 256x256 (CTA pair), 3 = 128x256 (one CTA)")
     ap.add_argument("--reduction", default="deterministic", choices=["deterministic", "atomic"])
     ap.add_argument("--no-extras", action="store_true", help="skip the schedule table, e2e and CPU baseline")
     ap.add_argument("--ref-seconds", type=float, default=10.0)
@@ -285,8 +290,8 @@ def main():
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    def make(mode_name, nsms, splits=1):
-        sch = sk.schedule(modes[mode_name], splits if mode_name == "splitk" else 1)
+    def make(mode_name, nsms, splits=1, tile=args.tile):
+        sch = sk.schedule(modes[mode_name], splits if mode_name == "splitk" else 1, tile=tile)
         nb = sk.sk_workspace_size(w.M, w.N, w.K, nsms, sch, red)
         ws = torch.zeros(nb, dtype=torch.uint8, device=dev)
         return sch, ws, nb
@@ -344,13 +349,17 @@ def main():
     if not args.no_extras and rank == 0:
         # ---- per-schedule table (the metric is per schedule)
         table = {}
-        for name, nsms in (("dp", 148), ("splitk2", 148), ("streamk", 148), ("hybrid", 148),
-                           ("dp", dev_sms), ("streamk", dev_sms), ("hybrid", dev_sms)):
+        tile_names = {0: "128x128", 1: "pair256x128", 2: "pair256x256", 3: "128x256"}
+        for tile, name, nsms in ((0, "dp", 148), (0, "splitk2", 148), (0, "streamk", 148), (0, "hybrid", 148),
+                                 (0, "dp", dev_sms), (0, "hybrid", dev_sms),
+                                 (2, "dp", 148), (2, "splitk2", 148), (2, "streamk", 148), (2, "hybrid", 148),
+                                 (2, "dp", dev_sms), (2, "hybrid", dev_sms),
+                                 (3, "hybrid", 148), (1, "hybrid", 148)):
             mname = "splitk" if name.startswith("splitk") else name
-            s2, ws2, nb2 = make(mname, nsms, 2)
+            s2, ws2, nb2 = make(mname, nsms, 2, tile)
             t = timed(s2, ws2, nb2, nsms, 200, 10)
             med = float(np.median(t))
-            table[f"{name}@{nsms}"] = {"us_median": med * 1e3, "us_p10": float(np.percentile(t, 10)) * 1e3,
+            table[f"{tile_names[tile]}/{name}@{nsms}"] = {"us_median": med * 1e3, "us_p10": float(np.percentile(t, 10)) * 1e3,
                                        "us_p90": float(np.percentile(t, 90)) * 1e3,
                                        "tflops": flops / (med / 1e3) / 1e12,
                                        "frac_of_measured_peak": flops / (med / 1e3) / 1e12 / peak_tf}
@@ -397,7 +406,7 @@ def main():
         return
 
     sha = kernel_sha()
-    tr = TRAFFIC.get(f"{w.name}/{args.mode}@{sms}")
+    tr = TRAFFIC.get(f"{w.name}/{args.mode}/tile{args.tile}@{sms}")
     traffic = tr["bytes"] if tr and tr.get("kernel_sha") == sha else None
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
@@ -405,6 +414,8 @@ def main():
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "layout": w.layout, "out": w.out,
                    "schedule": args.mode, "reduction": args.reduction, "num_sms": sms, "device_sms": dev_sms,
+                   "tile": {0: "128x128", 1: "256x128 CTA pair", 2: "256x256 CTA pair", 3: "128x256"}[args.tile],
+                   "tile_m": int(plan[12]), "tile_n": int(plan[13]), "ctas_per_tile": int(plan[14]),
                    "tiles": int(plan[2]), "iters": int(plan[3]), "workers": int(plan[4]),
                    "resolved_mode": int(plan[1]), "sk_tiles": int(plan[5]), "sk_units": int(plan[6]),
                    "l2": "flushed between timed steps (256 MiB write)", "accumulate": "fp32"},

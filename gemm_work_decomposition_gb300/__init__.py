@@ -24,8 +24,11 @@ SK_F32, SK_BF16 = 0, 1
 SK_ROLE_FULL, SK_ROLE_OWNER, SK_ROLE_PRODUCER, SK_ROLE_SLAB = 0, 1, 2, 3
 SK_OK, SK_EINVAL, SK_EWORKSPACE, SK_ECUDA, SK_ETIMEOUT, SK_ECAPACITY, SK_ERESIDENCY = 0, -1, -2, -3, -4, -5, -6
 SK_TILE_M, SK_TILE_N, SK_BLK_K = 128, 128, 64
-SK_MAP_VERSION, SK_MAP_HEADER, SK_MAP_SEG, SK_MAP_TILE = 1, 12, 9, 2
+SK_MAP_VERSION, SK_MAP_HEADER, SK_MAP_SEG, SK_MAP_TILE = 1, 15, 9, 2
+SK_TILE_128x128, SK_TILE_256x128_PAIR, SK_TILE_256x256_PAIR, SK_TILE_128x256 = 0, 1, 2, 3
 SK_WS_HEADER_BYTES = 256
+SK_TRACE_SEGS = 15
+SK_TRACE_WORDS = 4 + 4 * SK_TRACE_SEGS
 
 EXPORTS = ("sk_plan_size", "sk_plan", "sk_workspace_size", "sk_gemm", "sk_gemm_debug", "sk_reduce_splits",
            "sk_status", "sk_strerror", "sk_gemm_noalloc")
@@ -34,12 +37,12 @@ SK_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 class sk_schedule(ctypes.Structure):
     _fields_ = [("mode", ctypes.c_int32), ("splits", ctypes.c_int32), ("units", ctypes.c_int32),
-                ("min_iters", ctypes.c_int32), ("split_partials", ctypes.c_int32)]
+                ("min_iters", ctypes.c_int32), ("split_partials", ctypes.c_int32), ("tile", ctypes.c_int32)]
 
 
 class sk_debug_opts(ctypes.Structure):
     _fields_ = [("reverse_units", ctypes.c_int32), ("skip_producer_signal", ctypes.c_int32),
-                ("timeout_ns", ctypes.c_int64), ("dump", ctypes.c_void_p)]
+                ("timeout_ns", ctypes.c_int64), ("dump", ctypes.c_void_p), ("trace", ctypes.c_void_p)]
 
 
 class SkError(RuntimeError):
@@ -48,8 +51,9 @@ class SkError(RuntimeError):
         super().__init__(f"{where}: {sk_strerror(code)} ({code})")
 
 
-def schedule(mode: int, splits: int = 1, units: int = 0, min_iters: int = 0, split_partials: int = 0) -> sk_schedule:
-    return sk_schedule(mode, splits, units, min_iters, split_partials)
+def schedule(mode: int, splits: int = 1, units: int = 0, min_iters: int = 0, split_partials: int = 0,
+             tile: int = 0) -> sk_schedule:
+    return sk_schedule(mode, splits, units, min_iters, split_partials, tile)
 
 
 _lib = None
@@ -136,8 +140,8 @@ def sk_gemm(A, B, C, c_dtype: int, M: int, N: int, K: int, layout: int, sched: s
 
 def sk_gemm_debug(A, B, C, c_dtype: int, M: int, N: int, K: int, layout: int, sched: sk_schedule, reduction: int,
                   num_sms: int, workspace, ws_bytes: int, stream=None, reverse_units: int = 0,
-                  skip_producer_signal: int = 0, timeout_ns: int = 0, dump=None) -> int:
-    opts = sk_debug_opts(reverse_units, skip_producer_signal, timeout_ns, _ptr(dump) or None)
+                  skip_producer_signal: int = 0, timeout_ns: int = 0, dump=None, trace=None) -> int:
+    opts = sk_debug_opts(reverse_units, skip_producer_signal, timeout_ns, _ptr(dump) or None, _ptr(trace) or None)
     return _check(lib().sk_gemm_debug(_ptr(A), _ptr(B), _ptr(C), c_dtype, M, N, K, layout, sched, reduction,
                                       num_sms, _ptr(workspace), ws_bytes, _stream(stream), ctypes.byref(opts)),
                   "sk_gemm_debug")

@@ -65,11 +65,14 @@ int32_t make_sched(int32_t M, int32_t N, int32_t K, int32_t num_sms, const sk_sc
     if (M < 1 || N < 1 || K < 1 || num_sms < 1 || s.units < 0 || s.min_iters < 0) return SK_EINVAL;
     if (s.mode < SK_DP || s.mode > SK_HYBRID) return SK_EINVAL;
     if (s.split_partials != 0 && (s.mode != SK_SPLITK || s.split_partials != 1)) return SK_EINVAL;
-    const int64_t tiles_n = (static_cast<int64_t>(N) + kTileN - 1) / kTileN;
-    const int64_t tiles = ((static_cast<int64_t>(M) + kTileM - 1) / kTileM) * tiles_n;
+    int32_t tm = 0, tn = 0, cg = 0;
+    if (!tile_shape(s.tile, &tm, &tn, &cg)) return SK_EINVAL;
+    const int64_t tiles_n = (static_cast<int64_t>(N) + tn - 1) / tn;
+    const int64_t tiles = ((static_cast<int64_t>(M) + tm - 1) / tm) * tiles_n;
     const int64_t iters = (static_cast<int64_t>(K) + kBlkK - 1) / kBlkK;
     if (tiles * iters > INT32_MAX) return SK_EINVAL;
-    const int64_t S = s.units > 0 ? s.units : num_sms;
+    const int64_t S = s.units > 0 ? s.units : num_sms / cg;
+    if (S < 1) return SK_EINVAL;
     const int64_t min_iters = s.min_iters > 0 ? s.min_iters : 8;
 
     o = Sched{};
@@ -77,6 +80,9 @@ int32_t make_sched(int32_t M, int32_t N, int32_t K, int32_t num_sms, const sk_sc
     o.iters = static_cast<int32_t>(iters);
     o.tiles_n = static_cast<int32_t>(tiles_n);
     o.label = kLabelNone;
+    o.tile_m = tm;
+    o.tile_n = tn;
+    o.cg = cg;
 
     int32_t mode = s.mode;
     if (mode == SK_HYBRID) {
@@ -140,25 +146,25 @@ int64_t map_size(const Sched& s) {
 
 int64_t align_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
 
-// Workspace: header | flags (one int32 per slot, 256-aligned) | slots (64 KiB each);
-// split-partials: header | slabs [splits][M][N] FP32.
+// Workspace: header | flags (one int32 per slot and CTA of the tile, 256-aligned) |
+// slots (tile_m x tile_n FP32 each); split-partials: header | slabs [splits][M][N] FP32.
 int64_t flags_offset() { return SK_WS_HEADER_BYTES; }
-int64_t slots_offset(const Sched& s) { return SK_WS_HEADER_BYTES + align_up(4ll * s.n_slots, 256); }
+int64_t slots_offset(const Sched& s) { return SK_WS_HEADER_BYTES + align_up(4ll * s.n_slots * s.cg, 256); }
 int64_t workspace_bytes(const Sched& s, int32_t M, int32_t N) {
     if (s.partials) return SK_WS_HEADER_BYTES + 4ll * s.splits * M * N;
-    return slots_offset(s) + static_cast<int64_t>(s.n_slots) * kSlotFloats * 4;
+    return slots_offset(s) + static_cast<int64_t>(s.n_slots) * s.tile_m * s.tile_n * 4;
 }
 
 struct DeviceInfo {
     bool ready = false;
     cudaError_t err = cudaSuccess;
     int sms = 0;
-    int ctas_per_sm = 0;
+    int max_units[4] = {0, 0, 0, 0};  // resident units per sk_tile value
 };
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_mu;
 
-cudaError_t device_info(int* sms, int* ctas) {
+cudaError_t device_info(int* sms, int* max_units) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -167,11 +173,11 @@ cudaError_t device_info(int* sms, int* ctas) {
     DeviceInfo& d = g_dev[dev];
     if (!d.ready) {
         d.err = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
-        if (d.err == cudaSuccess) d.err = prepare_device(&d.ctas_per_sm);
+        if (d.err == cudaSuccess) d.err = prepare_device(d.sms, d.max_units);
         d.ready = true;
     }
     *sms = d.sms;
-    *ctas = d.ctas_per_sm;
+    for (int i = 0; i < 4; ++i) max_units[i] = d.max_units[i];
     return d.err;
 }
 
@@ -202,6 +208,23 @@ bool encode_2d(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, 
     CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// Output map: rows of `inner` elements of `esize` bytes, `outer` rows per slab and `slabs`
+// slabs, stored in boxes of 32 rows x 128 bytes (one box per epilogue warp and store) with
+// the 128-byte swizzle the epilogue's staging uses.
+bool encode_out(CUtensorMap* m, void* ptr, bool bf16, uint64_t inner, uint64_t outer, uint64_t slabs, uint32_t rank) {
+    PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+    if (!fn) return false;
+    const uint64_t esize = bf16 ? 2 : 4;
+    cuuint64_t dims[3] = {inner, outer, slabs};
+    cuuint64_t strides[2] = {inner * esize, inner * outer * esize};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / esize), 32, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, rank,
+                    ptr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
@@ -251,6 +274,9 @@ int32_t sk_plan(int32_t M, int32_t N, int32_t K, int32_t num_sms, sk_schedule s,
     h[9] = sch.label;
     h[10] = sch.label_splits;
     h[11] = sch.n_slots;
+    h[12] = sch.tile_m;
+    h[13] = sch.tile_n;
+    h[14] = sch.cg;
     int32_t* seg = map + SK_MAP_HEADER;
     int32_t* trow = seg + SK_MAP_SEG * nseg;
     for (int32_t t = 0; t < sch.tiles; ++t) {
@@ -303,14 +329,17 @@ int32_t sk_gemm_debug(const void* A, const void* B, void* C, sk_dtype c_dtype, i
     const int64_t need = workspace_bytes(sch, M, N);
     if (!workspace || !aligned(workspace, 256) || static_cast<int64_t>(ws_bytes) < need) return SK_EWORKSPACE;
 
-    int dev_sms = 0, ctas = 0;
-    if (device_info(&dev_sms, &ctas) != cudaSuccess) return SK_ECUDA;
-    if (static_cast<int64_t>(sch.workers) > static_cast<int64_t>(dev_sms) * ctas) return SK_ERESIDENCY;
+    int dev_sms = 0, max_units[4];
+    if (device_info(&dev_sms, max_units) != cudaSuccess) return SK_ECUDA;
+    if (sch.workers > max_units[s.tile]) return SK_ERESIDENCY;
 
+    // A in 128-row boxes (one CTA's rows); B in boxes of one CTA's share of the tile's
+    // columns (NT) or in 64 x 64 boxes (NN).
     CUtensorMap tmA, tmB;
-    if (!encode_2d(&tmA, A, static_cast<uint64_t>(K), static_cast<uint64_t>(M), kBlkK, kTileM)) return SK_ECUDA;
+    if (!encode_2d(&tmA, A, static_cast<uint64_t>(K), static_cast<uint64_t>(M), kBlkK, kCtaRows)) return SK_ECUDA;
     const bool nt = layout == SK_NT;
-    const bool okb = nt ? encode_2d(&tmB, B, static_cast<uint64_t>(K), static_cast<uint64_t>(N), kBlkK, kTileN)
+    const uint32_t b_rows = static_cast<uint32_t>(sch.tile_n / sch.cg);
+    const bool okb = nt ? encode_2d(&tmB, B, static_cast<uint64_t>(K), static_cast<uint64_t>(N), kBlkK, b_rows)
                         : encode_2d(&tmB, B, static_cast<uint64_t>(N), static_cast<uint64_t>(K), 64, kBlkK);
     if (!okb) return SK_ECUDA;
 
@@ -334,8 +363,15 @@ int32_t sk_gemm_debug(const void* A, const void* B, void* C, sk_dtype c_dtype, i
         if (opts->timeout_ns > 0) a.timeout_ns = static_cast<uint64_t>(opts->timeout_ns);
         a.dump = opts->dump;
         if (a.dump && !aligned(a.dump, 16)) return SK_EINVAL;
+        a.trace = opts->trace;
+        if (a.trace && !aligned(a.trace, 8)) return SK_EINVAL;
     }
-    if (launch_gemm(tmA, tmB, nt, a, st) != cudaSuccess) {
+    CUtensorMap tmC;
+    const bool okc = sch.partials ? encode_out(&tmC, a.slabs, false, static_cast<uint64_t>(N), static_cast<uint64_t>(M),
+                                               static_cast<uint64_t>(sch.splits), 3)
+                                  : encode_out(&tmC, C, a.c_bf16 != 0, static_cast<uint64_t>(N), static_cast<uint64_t>(M), 1, 2);
+    if (!okc) return SK_ECUDA;
+    if (launch_gemm(tmA, tmB, tmC, nt, a, st) != cudaSuccess) {
         cudaGetLastError();
         return SK_ECUDA;
     }
@@ -360,8 +396,8 @@ int32_t sk_reduce_splits(const float* P, void* C, sk_dtype c_dtype, int32_t spli
     if (c_dtype != SK_F32 && c_dtype != SK_BF16) return SK_EINVAL;
     if (mn == 0) return SK_OK;
     if (!P || !C || !aligned(P, 16) || !aligned(C, 16)) return SK_EINVAL;
-    int dev_sms = 0, ctas = 0;
-    if (device_info(&dev_sms, &ctas) != cudaSuccess) return SK_ECUDA;
+    int dev_sms = 0, max_units[4];
+    if (device_info(&dev_sms, max_units) != cudaSuccess) return SK_ECUDA;
     if (launch_reduce(P, C, c_dtype == SK_BF16 ? 1 : 0, splits, mn, dev_sms, static_cast<cudaStream_t>(stream)) !=
         cudaSuccess) {
         cudaGetLastError();

@@ -1,14 +1,17 @@
 // sk_kernels.cu - the persistent work-decomposed BF16 GEMM for sm_103a and the Split-K
 // slab reduction.
 //
-// One CTA per persistent unit ("Split-K and Stream-K: The Last Wave of a GEMM",
-// Mental model: one persistent CTA per SM, each walking its share of the flattened
-// tile-by-k space). Each CTA walks its segments (sk_schedule.h) with three roles:
+// One persistent unit per CTA, or per CTA pair for the pair tile shapes ("Split-K and
+// Stream-K: The Last Wave of a GEMM", Mental model: one persistent CTA per SM, each
+// walking its share of the flattened tile-by-k space). Each CTA walks its unit's segments
+// (sk_schedule.h) with three roles:
 //   warp 0      TMA producer: streams the A and B slabs of every k-iteration of every
-//               segment into a kStages-deep shared-memory ring;
-//   warp 1      MMA issuer: one thread issues tcgen05.mma (128 x 128 x 16, BF16 -> FP32)
-//               into one of two TMEM accumulators, alternating per segment, so the
-//               epilogue of one segment overlaps the MAC loop of the next;
+//               segment into a shared-memory ring;
+//   warp 1      MMA issuer: one thread issues tcgen05.mma (BF16 -> FP32) into one of two
+//               TMEM accumulators, alternating per segment, so the epilogue of one segment
+//               overlaps the MAC loop of the next. For a CTA pair only the leader (rank 0)
+//               issues: tcgen05 cta_group::2 reads A rows and B columns from both CTAs'
+//               shared memory and writes each CTA's rows into that CTA's TMEM;
 //   warps 2..5  epilogue: read the accumulator from TMEM and act on the segment's role:
 //               FULL -> write C; PRODUCER -> store the FP32 partial to its workspace slot
 //               and raise a flag (or add it atomically and bump a counter); OWNER -> wait
@@ -31,15 +34,16 @@ namespace {
 constexpr int32_t kErrTimeout = -4;  // SK_ETIMEOUT
 constexpr uint64_t kDrainNs = 20ull * 1000 * 1000;
 
+template <class S>
 struct Smem {
     uint32_t base;  // shared address of the 1024-aligned ring
-    __device__ uint32_t a(int s) const { return base + s * kABytes; }
-    __device__ uint32_t b(int s) const { return base + kStages * kABytes + s * kBBytes; }
-    __device__ uint32_t full(int s) const { return base + kSmemBarOff + 8 * s; }
-    __device__ uint32_t empty(int s) const { return base + kSmemBarOff + 8 * (kStages + s); }
-    __device__ uint32_t tfull(int b) const { return base + kSmemBarOff + 8 * (2 * kStages + b); }
-    __device__ uint32_t tempty(int b) const { return base + kSmemBarOff + 8 * (2 * kStages + 2 + b); }
-    __device__ uint32_t done() const { return base + kSmemBarOff + 8 * (2 * kStages + 4); }
+    __device__ uint32_t a(int s) const { return base + s * S::kABytes; }
+    __device__ uint32_t b(int s) const { return base + S::kStages * S::kABytes + s * S::kBBytes; }
+    __device__ uint32_t full(int s) const { return base + S::kSmemBarOff + 8 * s; }
+    __device__ uint32_t empty(int s) const { return base + S::kSmemBarOff + 8 * (S::kStages + s); }
+    __device__ uint32_t tfull(int b) const { return base + S::kSmemBarOff + 8 * (2 * S::kStages + b); }
+    __device__ uint32_t tempty(int b) const { return base + S::kSmemBarOff + 8 * (2 * S::kStages + 2 + b); }
+    __device__ uint32_t done() const { return base + S::kSmemBarOff + 8 * (2 * S::kStages + 4); }
 };
 
 __device__ __forceinline__ void record_timeout(const KArgs& a, volatile int* abort_flag) {
@@ -48,9 +52,11 @@ __device__ __forceinline__ void record_timeout(const KArgs& a, volatile int* abo
 }
 
 // --------------------------------------------------------------------------- warp 0
-template <bool kNT>
-__device__ void run_producer(const KArgs& a, const CUtensorMap* tmA, const CUtensorMap* tmB, const Smem& sm,
-                             int unit, uint64_t deadline, volatile int* abort_flag) {
+template <bool kNT, int kCG, int kBN>
+__device__ void run_producer(const KArgs& a, const CUtensorMap* tmA, const CUtensorMap* tmB,
+                             const Smem<Shape<kCG, kBN>>& sm, int unit, uint32_t rank, uint64_t deadline,
+                             volatile int* abort_flag) {
+    using S = Shape<kCG, kBN>;
     Walk w;
     w.init(a.sch, unit);
     Seg g;
@@ -59,45 +65,65 @@ __device__ void run_producer(const KArgs& a, const CUtensorMap* tmA, const CUten
     uint32_t issued = 0;
     bool ok = true;
     while (ok && w.next(a.sch, g)) {
-        const int32_t m0 = (g.tile / a.sch.tiles_n) * kTileM;
-        const int32_t n0 = (g.tile % a.sch.tiles_n) * kTileN;
+        // This CTA's rows of the tile and its half of the tile's columns of B.
+        const int32_t m0 = (g.tile / a.sch.tiles_n) * (kCtaRows * kCG) + static_cast<int32_t>(rank) * kCtaRows;
+        const int32_t nb = (g.tile % a.sch.tiles_n) * kBN + static_cast<int32_t>(rank) * S::kBNc;
         for (int32_t k = g.k_begin; k < g.k_end; ++k) {
             if (!mbar_wait(sm.empty(stage), phase ^ 1u, abort_flag, deadline)) {
                 ok = false;
                 break;
             }
             const int32_t k0 = k * kBlkK;
-            mbar_arrive_expect_tx(sm.full(stage), kStageBytes);
-            tma_load_2d(sm.a(stage), tmA, sm.full(stage), k0, m0);
-            if (kNT) {
-                tma_load_2d(sm.b(stage), tmB, sm.full(stage), k0, n0);
+            if (kCG == 1) {
+                mbar_arrive_expect_tx(sm.full(stage), S::kTxBytes);
+                tma_load_2d(sm.a(stage), tmA, sm.full(stage), k0, m0);
+                if (kNT) {
+                    tma_load_2d(sm.b(stage), tmB, sm.full(stage), k0, nb);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < S::kBNc / 64; ++j)
+                        tma_load_2d(sm.b(stage) + j * 8192, tmB, sm.full(stage), nb + 64 * j, k0);
+                }
             } else {
-                // B [K,N]: two 64-column boxes (128-byte swizzle spans 64 BF16 columns).
-                tma_load_2d(sm.b(stage), tmB, sm.full(stage), n0, k0);
-                tma_load_2d(sm.b(stage) + kBBytes / 2, tmB, sm.full(stage), n0 + 64, k0);
+                // Both CTAs' loads complete on the leader's barrier, which the leader arms
+                // for the bytes of both.
+                const uint32_t fb = mapa_shared(sm.full(stage), 0);
+                if (rank == 0) mbar_arrive_expect_tx(sm.full(stage), S::kTxBytes);
+                tma_load_2d_pair(sm.a(stage), tmA, fb, k0, m0);
+                if (kNT) {
+                    tma_load_2d_pair(sm.b(stage), tmB, fb, k0, nb);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < S::kBNc / 64; ++j)
+                        tma_load_2d_pair(sm.b(stage) + j * 8192, tmB, fb, nb + 64 * j, k0);
+                }
             }
             ++issued;
-            if (++stage == kStages) {
+            if (++stage == S::kStages) {
                 stage = 0;
                 phase ^= 1u;
             }
         }
     }
     if (!ok) record_timeout(a, abort_flag);
-    // Let the last loads land before the CTA can exit (they complete quickly; bounded).
-    const uint64_t drain = globaltimer() + kDrainNs;
-    const uint32_t outstanding = issued < static_cast<uint32_t>(kStages) ? issued : kStages;
-    for (uint32_t i = 0; i < outstanding; ++i) {
-        const uint32_t pos = issued - 1 - i;
-        if (!mbar_wait_until(sm.full(pos % kStages), (pos / kStages) & 1u, drain)) break;
+    // Let the last loads land before the CTA can exit (bounded). A pair's loads all
+    // complete on the leader's barriers, so the leader drains for both.
+    if (rank == 0) {
+        const uint64_t drain = globaltimer() + kDrainNs;
+        const uint32_t outstanding = issued < static_cast<uint32_t>(S::kStages) ? issued : S::kStages;
+        for (uint32_t i = 0; i < outstanding; ++i) {
+            const uint32_t pos = issued - 1 - i;
+            if (!mbar_wait_until(sm.full(pos % S::kStages), (pos / S::kStages) & 1u, drain)) break;
+        }
     }
 }
 
 // --------------------------------------------------------------------------- warp 1
-template <bool kNT>
-__device__ void run_mma(const KArgs& a, const Smem& sm, uint32_t tmem_base, int unit, uint64_t deadline,
-                        volatile int* abort_flag) {
-    constexpr uint32_t kIdesc = idesc_bf16_f32(kTileM, kTileN, kNT ? 0u : 1u);
+template <bool kNT, int kCG, int kBN>
+__device__ void run_mma(const KArgs& a, const Smem<Shape<kCG, kBN>>& sm, uint32_t tmem_base, int unit,
+                        uint64_t deadline, volatile int* abort_flag) {
+    using S = Shape<kCG, kBN>;
+    constexpr uint32_t kIdesc = idesc_bf16_f32(kCtaRows * kCG, kBN, kNT ? 0u : 1u);
     // K advance per 16-deep MMA inside one 64-deep stage: K-major operands move 32 bytes
     // along the swizzled row; the MN-major B of NN moves 16 rows of 128 bytes.
     constexpr uint32_t kAStep = (16 * 2) >> 4;
@@ -110,44 +136,61 @@ __device__ void run_mma(const KArgs& a, const Smem& sm, uint32_t tmem_base, int 
     int buf = 0;
     uint32_t uses[2] = {0u, 0u};
     bool ok = true;
+    uint64_t* tr = a.trace ? a.trace + static_cast<int64_t>(blockIdx.x) * kTraceWords : nullptr;
+    int seg = 0;
     while (ok && w.next(a.sch, g)) {
-        if (!mbar_wait(sm.tempty(buf), uses[buf] ^ 1u, abort_flag, deadline)) {
+        if (!mbar_wait<kCG == 2>(sm.tempty(buf), uses[buf] ^ 1u, abort_flag, deadline)) {
             ok = false;
             break;
         }
         tc_fence_after();
-        const uint32_t d = tmem_base + static_cast<uint32_t>(buf * kTileN);
+        const uint32_t d = tmem_base + static_cast<uint32_t>(buf * kBN);
         for (int32_t k = g.k_begin; k < g.k_end; ++k) {
             if (!mbar_wait(sm.full(stage), phase, abort_flag, deadline)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
+            if (tr && k == g.k_begin && seg < kTraceSegs) tr[4 + 4 * seg] = globaltimer();
             // A: K-major, 8-row groups 1024 bytes apart. B: K-major likewise (NT), or
-            // MN-major (NN) with its two 64-column halves 8 KiB apart.
+            // MN-major (NN) in 64-column boxes 8 KiB apart.
             const uint64_t adesc = smem_desc_sw128(sm.a(stage), 16, 1024);
-            const uint64_t bdesc = kNT ? smem_desc_sw128(sm.b(stage), 16, 1024)
-                                       : smem_desc_sw128(sm.b(stage), kBBytes / 2, 1024);
+            const uint64_t bdesc =
+                kNT ? smem_desc_sw128(sm.b(stage), 16, 1024) : smem_desc_sw128(sm.b(stage), 8192, 1024);
 #pragma unroll
             for (int kk = 0; kk < kBlkK / 16; ++kk) {
-                umma_bf16(d, adesc + kk * kAStep, bdesc + kk * kBStep, kIdesc,
-                          (k > g.k_begin || kk > 0) ? 1u : 0u);
+                const uint32_t acc = (k > g.k_begin || kk > 0) ? 1u : 0u;
+                if (kCG == 1)
+                    umma_bf16(d, adesc + kk * kAStep, bdesc + kk * kBStep, kIdesc, acc);
+                else
+                    umma_bf16_pair(d, adesc + kk * kAStep, bdesc + kk * kBStep, kIdesc, acc);
             }
-            umma_commit(sm.empty(stage));
-            if (++stage == kStages) {
+            if (kCG == 1)
+                umma_commit(sm.empty(stage));
+            else
+                umma_commit_pair(sm.empty(stage), 0x3);
+            if (++stage == S::kStages) {
                 stage = 0;
                 phase ^= 1u;
             }
         }
         if (!ok) break;
-        umma_commit(sm.tfull(buf));
+        if (kCG == 1)
+            umma_commit(sm.tfull(buf));
+        else
+            umma_commit_pair(sm.tfull(buf), 0x3);
+        if (tr && seg < kTraceSegs) tr[4 + 4 * seg + 1] = globaltimer();
+        ++seg;
         uses[buf] ^= 1u;
         buf ^= 1;
     }
     if (!ok) record_timeout(a, abort_flag);
-    // Every MMA issued so far has finished reading shared memory and writing TMEM
-    // before this thread moves on to the exit barrier.
-    umma_commit(sm.done());
+    // Every MMA issued so far has finished reading shared memory and writing TMEM (of
+    // both CTAs of a pair) before this thread moves on to the exit barrier.
+    if (kCG == 1)
+        umma_commit(sm.done());
+    else
+        umma_commit_pair(sm.done(), 0x1);
     mbar_wait_until(sm.done(), 0u, globaltimer() + kDrainNs);
 }
 
@@ -176,74 +219,96 @@ __device__ __forceinline__ bool wait_flag(const int32_t* f, int32_t target, uint
     return ok;
 }
 
-// Partial-slot layout: element (row r, column 4q + e of chunk c) at float4 index
-// (c * 8 + q) * 128 + r, so a warp's 32 rows touch 512 contiguous bytes per access.
-__device__ __forceinline__ int slot_f4(int c, int q, int row) { return ((c * 8 + q) * kTileM + row) * 4; }
+// Partial-slot layout within one 128-column slice of a CTA's rows: element (row r, column
+// 4q + e of 32-column chunk c) at float4 index (c * 8 + q) * 128 + r, so a warp's 32 rows
+// touch 512 contiguous bytes per access.
+__device__ __forceinline__ int slot_f4(int c, int q, int row) { return ((c * 8 + q) * kCtaRows + row) * 4; }
 
-__device__ __forceinline__ void store_row_chunk(const KArgs& a, const float (&v)[128], int32_t gr, int32_t n0) {
-    if (gr >= a.M) return;
-    if (a.c_bf16) {
-        __nv_bfloat16* crow = static_cast<__nv_bfloat16*>(a.C) + static_cast<int64_t>(gr) * a.N;
+// Store a 128-column slice of this warp's 32 rows (one row per lane, in registers) through
+// the warp's two 4 KiB staging boxes with TMA tensor stores: BF16 C in two boxes of 64
+// columns, FP32 C or slab in four boxes of 32 columns, each box 32 rows x 128 bytes in the
+// 128-byte swizzled layout (16-byte chunk j of row r at chunk j ^ (r % 8)), so the shared
+// stores are conflict-free and the TMA clips the box at M and N. `slab` < 0 stores to C.
+__device__ __forceinline__ void store_slice(const KArgs& a, const CUtensorMap* tmC, uint32_t staging,
+                                            uint32_t& nstore, const float (&v)[128], int32_t x0, int32_t y0,
+                                            int32_t slab) {
+    const int lane = threadIdx.x & 31;
+    const bool bf16 = a.c_bf16 && slab < 0;
+    const int boxes = bf16 ? 2 : 4;
+    const int cols = bf16 ? 64 : 32;
+    if (y0 >= a.M) return;  // the warp's 32 rows lie below C
 #pragma unroll
-        for (int g8 = 0; g8 < 16; ++g8) {
-            const int32_t gc = n0 + g8 * 8;
-            if (gc < a.N) {
-                __nv_bfloat162 p0 = __floats2bfloat162_rn(v[g8 * 8 + 0], v[g8 * 8 + 1]);
-                __nv_bfloat162 p1 = __floats2bfloat162_rn(v[g8 * 8 + 2], v[g8 * 8 + 3]);
-                __nv_bfloat162 p2 = __floats2bfloat162_rn(v[g8 * 8 + 4], v[g8 * 8 + 5]);
-                __nv_bfloat162 p3 = __floats2bfloat162_rn(v[g8 * 8 + 6], v[g8 * 8 + 7]);
-                uint4 pk;
-                pk.x = *reinterpret_cast<uint32_t*>(&p0);
-                pk.y = *reinterpret_cast<uint32_t*>(&p1);
-                pk.z = *reinterpret_cast<uint32_t*>(&p2);
-                pk.w = *reinterpret_cast<uint32_t*>(&p3);
-                *reinterpret_cast<uint4*>(crow + gc) = pk;
-            }
+    for (int b = 0; b < 4; ++b) {
+        if (b >= boxes) break;
+        const int32_t x = x0 + b * cols;
+        if (x >= a.N) break;
+        const uint32_t buf = staging + (nstore & 1u) * 4096u;
+        if (nstore >= 2) {
+            // The store issued two boxes ago used this buffer: wait until the TMA read it.
+            if (lane == 0) bulk_wait_group_read<1>();
+            __syncwarp();
         }
-    } else {
-        float* crow = static_cast<float*>(a.C) + static_cast<int64_t>(gr) * a.N;
+        const uint32_t row = buf + static_cast<uint32_t>(lane) * 128u;
 #pragma unroll
-        for (int g8 = 0; g8 < 16; ++g8) {
-            const int32_t gc = n0 + g8 * 8;
-            if (gc < a.N) {
-                *reinterpret_cast<float4*>(crow + gc) =
-                    make_float4(v[g8 * 8 + 0], v[g8 * 8 + 1], v[g8 * 8 + 2], v[g8 * 8 + 3]);
-                *reinterpret_cast<float4*>(crow + gc + 4) =
-                    make_float4(v[g8 * 8 + 4], v[g8 * 8 + 5], v[g8 * 8 + 6], v[g8 * 8 + 7]);
+        for (int j = 0; j < 8; ++j) {
+            uint32_t w0, w1, w2, w3;
+            if (bf16) {
+                const int i = b * 64 + j * 8;
+                __nv_bfloat162 p0 = __floats2bfloat162_rn(v[i + 0], v[i + 1]);
+                __nv_bfloat162 p1 = __floats2bfloat162_rn(v[i + 2], v[i + 3]);
+                __nv_bfloat162 p2 = __floats2bfloat162_rn(v[i + 4], v[i + 5]);
+                __nv_bfloat162 p3 = __floats2bfloat162_rn(v[i + 6], v[i + 7]);
+                w0 = *reinterpret_cast<uint32_t*>(&p0);
+                w1 = *reinterpret_cast<uint32_t*>(&p1);
+                w2 = *reinterpret_cast<uint32_t*>(&p2);
+                w3 = *reinterpret_cast<uint32_t*>(&p3);
+            } else {
+                const int i = b * 32 + j * 4;
+                w0 = __float_as_uint(v[i + 0]);
+                w1 = __float_as_uint(v[i + 1]);
+                w2 = __float_as_uint(v[i + 2]);
+                w3 = __float_as_uint(v[i + 3]);
             }
+            st_shared_v4(row + static_cast<uint32_t>((j ^ (lane & 7)) * 16), w0, w1, w2, w3);
         }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            if (slab < 0)
+                tma_store_2d(tmC, buf, x, y0);
+            else
+                tma_store_3d(tmC, buf, x, y0, slab);
+            bulk_commit_group();
+        }
+        ++nstore;
     }
 }
 
-__device__ __forceinline__ void store_slab(const KArgs& a, const float (&v)[128], int32_t slab, int32_t gr,
-                                           int32_t n0) {
-    if (gr >= a.M) return;
-    float* row = a.slabs + static_cast<int64_t>(slab) * a.M * a.N + static_cast<int64_t>(gr) * a.N;
-#pragma unroll
-    for (int g8 = 0; g8 < 16; ++g8) {
-        const int32_t gc = n0 + g8 * 8;
-        if (gc < a.N) {
-            *reinterpret_cast<float4*>(row + gc) =
-                make_float4(v[g8 * 8 + 0], v[g8 * 8 + 1], v[g8 * 8 + 2], v[g8 * 8 + 3]);
-            *reinterpret_cast<float4*>(row + gc + 4) =
-                make_float4(v[g8 * 8 + 4], v[g8 * 8 + 5], v[g8 * 8 + 6], v[g8 * 8 + 7]);
-        }
-    }
-}
-
-__device__ void run_epilogue(const KArgs& a, const Smem& sm, uint32_t tmem_base, int unit, uint64_t deadline,
+template <int kCG, int kBN>
+__device__ void run_epilogue(const KArgs& a, const CUtensorMap* tmC, const Smem<Shape<kCG, kBN>>& sm,
+                             uint32_t tmem_base, int unit, uint32_t rank, uint64_t deadline,
                              volatile int* abort_flag) {
+    using S = Shape<kCG, kBN>;
+    constexpr int kHalves = kBN / 128;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int et = threadIdx.x - 64;          // 0..127 among the epilogue threads
     const int quad = warp & 3;                // TMEM lanes this warp may read: 32*quad ..
-    const int row = quad * 32 + lane;         // tile row owned by this thread
+    const int row = quad * 32 + lane;         // row of this CTA's part of the tile
     const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
+    // The accumulator-empty barriers live in the leader CTA.
+    const uint32_t tempty_addr[2] = {kCG == 1 ? sm.tempty(0) : mapa_shared(sm.tempty(0), 0),
+                                     kCG == 1 ? sm.tempty(1) : mapa_shared(sm.tempty(1), 0)};
+    const int32_t r = static_cast<int32_t>(rank);
+    const uint32_t staging = sm.base + S::kStagingOff + static_cast<uint32_t>(warp - 2) * 8192u;
+    uint32_t nstore = 0;
     Walk w;
     w.init(a.sch, unit);
     Seg g;
     int buf = 0;
     uint32_t uses[2] = {0u, 0u};
+    uint64_t* tr = (a.trace && et == 0) ? a.trace + static_cast<int64_t>(blockIdx.x) * kTraceWords : nullptr;
+    int seg = 0;
     while (w.next(a.sch, g)) {
         const bool got = mbar_wait(sm.tfull(buf), uses[buf], abort_flag, deadline);
         if (named_bar_or(1, kEpiThreads, !got || *abort_flag != 0)) {
@@ -251,66 +316,75 @@ __device__ void run_epilogue(const KArgs& a, const Smem& sm, uint32_t tmem_base,
             break;
         }
         tc_fence_after();
-        float v[128];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            uint32_t r[32];
-            tmem_ld_32x32b_x32_sync(tmem_base + lane_addr + static_cast<uint32_t>(buf * kTileN + c * 32), r);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) v[c * 32 + i] = __uint_as_float(r[i]);
-        }
-        tc_fence_before();
-        mbar_arrive(sm.tempty(buf));
-        uses[buf] ^= 1u;
-        buf ^= 1;
+        if (tr && seg < kTraceSegs) tr[4 + 4 * seg + 2] = globaltimer();
 
-        const int32_t m0 = (g.tile / a.sch.tiles_n) * kTileM;
-        const int32_t n0 = (g.tile % a.sch.tiles_n) * kTileN;
-        const int32_t gr = m0 + row;
-
-        if (a.dump) {
-            float* d = a.dump + (static_cast<int64_t>(g.tile) * a.sch.iters + g.k_begin) * kSlotFloats +
-                       row * kTileN;
-#pragma unroll
-            for (int q = 0; q < 32; ++q)
-                *reinterpret_cast<float4*>(d + 4 * q) = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-        }
-
-        if (g.role == kProducer) {
-            if (a.atomic) {
-                float* s = a.slots + static_cast<int64_t>(g.peer_begin) * kSlotFloats;
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        const int i = c * 32 + q * 4;
-                        red_add_v4_f32(s + slot_f4(c, q, row), v[i], v[i + 1], v[i + 2], v[i + 3]);
-                    }
-            } else {
-                float* s = a.slots + static_cast<int64_t>(g.slot) * kSlotFloats;
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        const int i = c * 32 + q * 4;
-                        st_cg_f4(s + slot_f4(c, q, row), make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]));
-                    }
-            }
-            __threadfence();
-            named_bar_sync(1, kEpiThreads);
-            if (et == 0 && !a.skip_signal) {
-                if (a.atomic)
-                    red_release_add_gpu(a.flags + g.peer_begin, 1);
-                else
-                    st_release_gpu(a.flags + g.slot, 1);
-            }
-        } else if (g.role == kOwner) {
-            // Turnstile: fold the peers' partials into this unit's own in k order.
+        // Owner: wait for every peer's partial (this CTA's share of it) before folding.
+        if (g.role == kOwner) {
             bool ok = true;
             if (a.atomic) {
-                ok = wait_flag(a.flags + g.peer_begin, g.n_peers, deadline, abort_flag);
-                if (ok) {
-                    float* s = a.slots + static_cast<int64_t>(g.peer_begin) * kSlotFloats;
+                ok = wait_flag(a.flags + g.peer_begin * kCG + r, g.n_peers, deadline, abort_flag);
+            } else {
+                for (int32_t pi = 0; pi < g.n_peers && ok; ++pi)
+                    ok = wait_flag(a.flags + (g.peer_begin + pi) * kCG + r, 1, deadline, abort_flag);
+            }
+            if (named_bar_or(1, kEpiThreads, !ok)) {
+                record_timeout(a, abort_flag);
+                break;
+            }
+        }
+
+        const int32_t m0 = (g.tile / a.sch.tiles_n) * (kCtaRows * kCG) + r * kCtaRows;
+        const int32_t n0 = (g.tile % a.sch.tiles_n) * kBN;
+        const int32_t wy = m0 + quad * 32;  // first row of this warp's 32
+
+#pragma unroll 1
+        for (int h = 0; h < kHalves; ++h) {
+            float v[128];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t rr[32];
+                tmem_ld_32x32b_x32_sync(
+                    tmem_base + lane_addr + static_cast<uint32_t>(buf * kBN + h * 128 + c * 32), rr);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[c * 32 + i] = __uint_as_float(rr[i]);
+            }
+            if (h == kHalves - 1) {
+                // The accumulator is in registers: hand it back to the MMA issuer.
+                tc_fence_before();
+                if (kCG == 1)
+                    mbar_arrive(tempty_addr[buf]);
+                else
+                    mbar_arrive_cluster(tempty_addr[buf]);
+            }
+
+            if (a.dump) {
+                float* d = a.dump +
+                           (static_cast<int64_t>(g.tile) * a.sch.iters + g.k_begin) * (kCtaRows * kCG * kBN) +
+                           static_cast<int64_t>(r * kCtaRows + row) * kBN + h * 128;
+#pragma unroll
+                for (int q = 0; q < 32; ++q)
+                    *reinterpret_cast<float4*>(d + 4 * q) =
+                        make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+            }
+
+            if (g.role == kProducer) {
+                const int32_t s_idx = a.atomic ? g.peer_begin : g.slot;
+                float* s = a.slots + static_cast<int64_t>(s_idx * kCG + r) * S::kCtaSlotFloats + h * S::kHalfFloats;
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        const int i = c * 32 + q * 4;
+                        if (a.atomic)
+                            red_add_v4_f32(s + slot_f4(c, q, row), v[i], v[i + 1], v[i + 2], v[i + 3]);
+                        else
+                            st_cg_f4(s + slot_f4(c, q, row), make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]));
+                    }
+            } else if (g.role == kOwner) {
+                // Turnstile: fold the peers' partials into this unit's own in k order.
+                if (a.atomic) {
+                    float* s = a.slots + static_cast<int64_t>(g.peer_begin * kCG + r) * S::kCtaSlotFloats +
+                               h * S::kHalfFloats;
                     const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
                     for (int c = 0; c < 4; ++c)
@@ -324,72 +398,92 @@ __device__ void run_epilogue(const KArgs& a, const Smem& sm, uint32_t tmem_base,
                             v[i + 3] += p.w;
                             st_cg_f4(s + slot_f4(c, q, row), z);
                         }
+                } else {
+                    for (int32_t pi = 0; pi < g.n_peers; ++pi) {
+                        const float* s = a.slots +
+                                         static_cast<int64_t>((g.peer_begin + pi) * kCG + r) * S::kCtaSlotFloats +
+                                         h * S::kHalfFloats;
+#pragma unroll
+                        for (int c = 0; c < 4; ++c)
+#pragma unroll
+                            for (int q = 0; q < 8; ++q) {
+                                const int i = c * 32 + q * 4;
+                                const float4 p = ld_cg_f4(s + slot_f4(c, q, row));
+                                v[i] += p.x;
+                                v[i + 1] += p.y;
+                                v[i + 2] += p.z;
+                                v[i + 3] += p.w;
+                            }
+                    }
                 }
+                store_slice(a, tmC, staging, nstore, v, n0 + h * 128, wy, -1);
+            } else if (g.role == kSlab) {
+                store_slice(a, tmC, staging, nstore, v, n0 + h * 128, wy, g.slot);
             } else {
-                for (int32_t pi = 0; pi < g.n_peers && ok; ++pi) {
-                    const int32_t slot = g.peer_begin + pi;
-                    ok = wait_flag(a.flags + slot, 1, deadline, abort_flag);
-                    if (!ok) break;
-                    const float* s = a.slots + static_cast<int64_t>(slot) * kSlotFloats;
-#pragma unroll
-                    for (int c = 0; c < 4; ++c)
-#pragma unroll
-                        for (int q = 0; q < 8; ++q) {
-                            const int i = c * 32 + q * 4;
-                            const float4 p = ld_cg_f4(s + slot_f4(c, q, row));
-                            v[i] += p.x;
-                            v[i + 1] += p.y;
-                            v[i + 2] += p.z;
-                            v[i + 3] += p.w;
-                        }
-                }
+                store_slice(a, tmC, staging, nstore, v, n0 + h * 128, wy, -1);
             }
-            if (named_bar_or(1, kEpiThreads, !ok)) {
-                record_timeout(a, abort_flag);
-                break;
+        }
+        uses[buf] ^= 1u;
+        buf ^= 1;
+
+        if (g.role == kProducer) {
+            // Every epilogue thread's share is stored: publish it.
+            __threadfence();
+            named_bar_sync(1, kEpiThreads);
+            if (et == 0 && !a.skip_signal) {
+                if (a.atomic)
+                    red_release_add_gpu(a.flags + g.peer_begin * kCG + r, 1);
+                else
+                    st_release_gpu(a.flags + g.slot * kCG + r, 1);
             }
+        } else if (g.role == kOwner) {
             // Every epilogue thread has read the partials: re-arm the flags / counter.
+            named_bar_sync(1, kEpiThreads);
             if (et == 0) {
                 if (a.atomic) {
-                    a.flags[g.peer_begin] = 0;
+                    a.flags[g.peer_begin * kCG + r] = 0;
                 } else {
-                    for (int32_t pi = 0; pi < g.n_peers; ++pi) a.flags[g.peer_begin + pi] = 0;
+                    for (int32_t pi = 0; pi < g.n_peers; ++pi) a.flags[(g.peer_begin + pi) * kCG + r] = 0;
                 }
             }
-            store_row_chunk(a, v, gr, n0);
-        } else if (g.role == kSlab) {
-            store_slab(a, v, g.slot, gr, n0);
-        } else {
-            store_row_chunk(a, v, gr, n0);
         }
+        if (tr && seg < kTraceSegs) tr[4 + 4 * seg + 3] = globaltimer();
+        ++seg;
     }
+    // Every TMA store of this warp has written C before the CTA may exit.
+    if (lane == 0) bulk_wait_group_all();
+    __syncwarp();
+    if (tr) tr[2] = static_cast<uint64_t>(seg);
 }
 
 // --------------------------------------------------------------------------- kernel
-template <bool kNT>
+template <bool kNT, int kCG, int kBN>
 __global__ void __launch_bounds__(kThreads, 1)
     sk_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const KArgs args) {
+                   const __grid_constant__ CUtensorMap tmC, const KArgs args) {
+    using S = Shape<kCG, kBN>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    Smem sm{smem_u32(smem)};
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + kSmemBarOff + 192);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kSmemBarOff + 196);
+    Smem<S> sm{smem_u32(smem)};
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + S::kSmemBarOff + 192);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + S::kSmemBarOff + 196);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int unit = args.reverse ? static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x)
-                                  : static_cast<int>(blockIdx.x);
+    const uint32_t rank = kCG == 2 ? cluster_ctarank() : 0u;
+    const int units = static_cast<int>(gridDim.x) / kCG;
+    const int cid = static_cast<int>(blockIdx.x) / kCG;
+    const int unit = args.reverse ? units - 1 - cid : cid;
     const uint64_t deadline = globaltimer() + args.timeout_ns;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < S::kStages; ++s) {
             mbar_init(sm.full(s), 1);
             mbar_init(sm.empty(s), 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(sm.tfull(b), 1);
-            mbar_init(sm.tempty(b), kEpiThreads);
+            mbar_init(sm.tempty(b), kEpiThreads * kCG);
         }
         mbar_init(sm.done(), 1);
         *abort_flag = 0;
@@ -398,30 +492,52 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0 && lane == 0) {
         prefetch_tmap(&tmA);
         prefetch_tmap(&tmB);
+        prefetch_tmap(&tmC);
     }
     if (warp == 1) {
-        tmem_alloc(smem_u32(tmem_holder), kTmemCols);
-        tmem_relinquish();
+        if (kCG == 1) {
+            tmem_alloc(smem_u32(tmem_holder), S::kTmemCols);
+            tmem_relinquish();
+        } else {
+            tmem_alloc_pair(smem_u32(tmem_holder), S::kTmemCols);
+            tmem_relinquish_pair();
+        }
     }
     tc_fence_before();
-    __syncthreads();
+    if (kCG == 2)
+        cluster_sync();
+    else
+        __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_holder);
+    if (args.trace && threadIdx.x == 0) args.trace[static_cast<int64_t>(blockIdx.x) * kTraceWords] = globaltimer();
 
+    // Warps 0 and 1 reconverge before the exit barrier: a CTA barrier counts a warp once
+    // any of its threads arrives, so all 32 lanes must arrive together.
     if (warp == 0) {
-        if (lane == 0) run_producer<kNT>(args, &tmA, &tmB, sm, unit, deadline, abort_flag);
+        if (lane == 0) run_producer<kNT, kCG, kBN>(args, &tmA, &tmB, sm, unit, rank, deadline, abort_flag);
+        __syncwarp();
     } else if (warp == 1) {
-        if (lane == 0) run_mma<kNT>(args, sm, tmem_base, unit, deadline, abort_flag);
+        if (lane == 0 && rank == 0) run_mma<kNT, kCG, kBN>(args, sm, tmem_base, unit, deadline, abort_flag);
+        __syncwarp();
     } else {
-        run_epilogue(args, sm, tmem_base, unit, deadline, abort_flag);
+        run_epilogue<kCG, kBN>(args, &tmC, sm, tmem_base, unit, rank, deadline, abort_flag);
     }
 
     tc_fence_before();
-    __syncthreads();
+    if (kCG == 2)
+        cluster_sync();
+    else
+        __syncthreads();
+    if (args.trace && threadIdx.x == 0)
+        args.trace[static_cast<int64_t>(blockIdx.x) * kTraceWords + 1] = globaltimer();
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
-        tmem_dealloc(tmem_base, kTmemCols);
+        if (kCG == 1)
+            tmem_dealloc(tmem_base, S::kTmemCols);
+        else
+            tmem_dealloc_pair(tmem_base, S::kTmemCols);
     }
 }
 
@@ -452,37 +568,110 @@ __global__ void __launch_bounds__(256)
     }
 }
 
-}  // namespace
+// --------------------------------------------------------------------------- host side
+bool g_pair_coop = true;  // cleared if this device rejects cooperative cluster launches
 
-cudaError_t prepare_device(int* gemm_ctas_per_sm) {
-    cudaError_t e = cudaFuncSetAttribute(sk_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kSmemBytes);
+template <bool kNT, int kCG, int kBN>
+cudaError_t launch_shape(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC, const KArgs& a,
+                         cudaStream_t stream) {
+    using S = Shape<kCG, kBN>;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(a.sch.workers * kCG), 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = S::kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    int n = 0;
+    const bool coop = kCG == 1 || g_pair_coop;
+    if (coop) {
+        attr[n].id = cudaLaunchAttributeCooperative;
+        attr[n].val.cooperative = 1;
+        ++n;
+    }
+    if (kCG == 2) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = 2;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = n;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, sk_gemm_kernel<kNT, kCG, kBN>, tmA, tmB, tmC, a);
+    if (e != cudaSuccess && kCG == 2 && coop) {
+        // Cooperative launch of clusters is not available: the host has already checked
+        // that every pair fits on the device at once, so launch the clusters plainly.
+        cudaGetLastError();
+        g_pair_coop = false;
+        cfg.attrs = attr + 1;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, sk_gemm_kernel<kNT, kCG, kBN>, tmA, tmB, tmC, a);
+    }
+    return e;
+}
+
+template <int kCG, int kBN>
+cudaError_t prepare_shape(int num_sms, int* max_units) {
+    using S = Shape<kCG, kBN>;
+    cudaError_t e = cudaFuncSetAttribute(sk_gemm_kernel<false, kCG, kBN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         S::kSmemBytes);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(sk_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    e = cudaFuncSetAttribute(sk_gemm_kernel<true, kCG, kBN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             S::kSmemBytes);
     if (e != cudaSuccess) return e;
-    int n0 = 0, n1 = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n0, sk_gemm_kernel<false>, kThreads, kSmemBytes);
+    if (kCG == 1) {
+        int n0 = 0, n1 = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n0, sk_gemm_kernel<false, kCG, kBN>, kThreads,
+                                                          S::kSmemBytes);
+        if (e != cudaSuccess) return e;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n1, sk_gemm_kernel<true, kCG, kBN>, kThreads,
+                                                          S::kSmemBytes);
+        if (e != cudaSuccess) return e;
+        *max_units = (n0 < n1 ? n0 : n1) * num_sms;
+        return cudaSuccess;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * num_sms), 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = S::kSmemBytes;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int c0 = 0, c1 = 0;
+    e = cudaOccupancyMaxActiveClusters(&c0, sk_gemm_kernel<false, kCG, kBN>, &cfg);
     if (e != cudaSuccess) return e;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n1, sk_gemm_kernel<true>, kThreads, kSmemBytes);
+    e = cudaOccupancyMaxActiveClusters(&c1, sk_gemm_kernel<true, kCG, kBN>, &cfg);
     if (e != cudaSuccess) return e;
-    *gemm_ctas_per_sm = n0 < n1 ? n0 : n1;
+    *max_units = c0 < c1 ? c0 : c1;
     return cudaSuccess;
 }
 
-cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, bool nt, const KArgs& a,
-                        cudaStream_t stream) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(a.sch.workers), 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = kSmemBytes;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeCooperative;
-    attr[0].val.cooperative = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    if (nt) return cudaLaunchKernelEx(&cfg, sk_gemm_kernel<true>, tmA, tmB, a);
-    return cudaLaunchKernelEx(&cfg, sk_gemm_kernel<false>, tmA, tmB, a);
+}  // namespace
+
+cudaError_t prepare_device(int num_sms, int* max_units) {
+    cudaError_t e = prepare_shape<1, 128>(num_sms, &max_units[0]);
+    if (e == cudaSuccess) e = prepare_shape<2, 128>(num_sms, &max_units[1]);
+    if (e == cudaSuccess) e = prepare_shape<2, 256>(num_sms, &max_units[2]);
+    if (e == cudaSuccess) e = prepare_shape<1, 256>(num_sms, &max_units[3]);
+    return e;
+}
+
+cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC, bool nt,
+                        const KArgs& a, cudaStream_t stream) {
+    const int cg = a.sch.cg, bn = a.sch.tile_n;
+#define SK_LAUNCH(CG, BN)                                                                 \
+    return nt ? launch_shape<true, CG, BN>(tmA, tmB, tmC, a, stream)                     \
+              : launch_shape<false, CG, BN>(tmA, tmB, tmC, a, stream)
+    if (cg == 1 && bn == 128) SK_LAUNCH(1, 128);
+    if (cg == 2 && bn == 128) SK_LAUNCH(2, 128);
+    if (cg == 2 && bn == 256) SK_LAUNCH(2, 256);
+    if (cg == 1 && bn == 256) SK_LAUNCH(1, 256);
+#undef SK_LAUNCH
+    return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_reduce(const float* P, void* C, int c_bf16, int splits, int64_t mn, int num_sms,

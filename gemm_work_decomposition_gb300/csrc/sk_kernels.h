@@ -9,39 +9,61 @@
 
 namespace sk {
 
-constexpr int kStages = 6;                           // TMA -> shared-memory ring depth
-constexpr int kABytes = kTileM * kBlkK * 2;          // 16 KiB: A slab 128 x 64 BF16
-constexpr int kBBytes = kTileN * kBlkK * 2;          // 16 KiB: B slab 64 x 128 BF16
-constexpr int kStageBytes = kABytes + kBBytes;
-constexpr int kThreads = 192;                        // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
+constexpr int kThreads = 192;     // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
 constexpr int kEpiThreads = 128;
-constexpr int kTmemCols = 256;                       // two 128 x 128 FP32 accumulators
-constexpr int kSlotFloats = kTileM * kTileN;         // one FP32 partial tile = 64 KiB
-constexpr int kSmemBarOff = kStages * kStageBytes;   // barriers after the ring
-constexpr int kSmemBytes = kSmemBarOff + 256 + 1024; // + barrier block + 1 KiB alignment slack
+constexpr int kCtaRows = 128;     // rows of a work tile held by one CTA (its TMEM lanes)
+constexpr int kRingBytes = 196608;
+constexpr int kTraceSegs = 15;                  // SK_TRACE_SEGS
+constexpr int kTraceWords = 4 + 4 * kTraceSegs; // SK_TRACE_WORDS
+
+// Compile-time shape of one kernel instance: kCG CTAs per work tile (1, or a pair with
+// tcgen05 cta_group::2), work tile (128 * kCG) x kBN, k-iteration depth 64.
+template <int kCG, int kBN>
+struct Shape {
+    static constexpr int kBNc = kBN / kCG;                 // B columns held by one CTA
+    static constexpr int kABytes = kCtaRows * kBlkK * 2;   // 16 KiB of A per stage
+    static constexpr int kBBytes = kBNc * kBlkK * 2;       // 8 / 16 / 32 KiB of B per stage
+    static constexpr int kStageBytes = kABytes + kBBytes;
+    static constexpr int kStages = (kRingBytes / kStageBytes) > 8 ? 8 : (kRingBytes / kStageBytes);
+    // Epilogue staging after the ring: per epilogue warp two 4 KiB boxes (32 rows x 128 B)
+    // that the TMA stores to C; then the barrier block and 1 KiB of alignment.
+    static constexpr int kStagingOff = kStages * kStageBytes;
+    static constexpr int kStagingBytes = 4 * 2 * 4096;
+    static constexpr int kSmemBarOff = kStagingOff + kStagingBytes;
+    static constexpr int kSmemBytes = kSmemBarOff + 256 + 1024;
+    static constexpr int kTmemCols = 2 * kBN;               // two accumulators of kBN columns
+    static constexpr int kTxBytes = kCG * kStageBytes;      // bytes landing on the leader per stage
+    static constexpr int kHalfFloats = kCtaRows * 128;      // one 128-column slice of a CTA's rows
+    static constexpr int kCtaSlotFloats = kCtaRows * kBN;   // a CTA's share of one partial slot
+    static_assert(kBNc % 64 == 0 && kBN % 128 == 0, "tile shape");
+};
 
 struct KArgs {
     Sched sch;
     void* C;            // [M,N] FP32 or BF16
     float* slabs;       // split-partials: [splits][M][N] FP32
-    float* slots;       // n_slots x 64 KiB partial tiles
-    int32_t* flags;     // n_slots flags (deterministic) or counters (atomic)
+    float* slots;       // n_slots x tile_m x tile_n FP32 partial tiles
+    int32_t* flags;     // n_slots x CTAs-per-tile flags (deterministic) or counters (atomic)
     int32_t* status;    // workspace status word
     float* dump;        // optional: every segment's own FP32 accumulator, by (tile*iters + k_begin)
+    uint64_t* trace;    // optional: per-CTA %globaltimer record (kTraceWords each)
     uint64_t timeout_ns;
     int32_t M, N, K;
     int32_t c_bf16;
     int32_t atomic;
-    int32_t reverse;    // run unit gridDim.x-1-blockIdx.x on CTA blockIdx.x
+    int32_t reverse;    // unit order reversed over the CTAs (or CTA pairs)
     int32_t skip_signal;// producers store but never raise their flag (time-out test)
 };
 
-// Launch the persistent GEMM (cooperative, `a.sch.workers` CTAs). Returns a cudaError_t.
-cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, bool nt, const KArgs& a,
-                        cudaStream_t stream);
-// Configure the kernels' shared-memory limit on the current device and report how many
-// GEMM CTAs fit on one SM.
-cudaError_t prepare_device(int* gemm_ctas_per_sm);
+// Launch the persistent GEMM for a.sch's tile shape: a.sch.workers units of a.sch.cg CTAs,
+// cooperative where the device allows it. Returns a cudaError_t.
+// tmC: the output map — C [M,N] (FP32 or BF16) in boxes of 32 rows x 128 bytes, or for
+// Split-K slabs the FP32 [splits][M][N] map in boxes of 1 x 32 rows x 32 columns.
+cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC, bool nt,
+                        const KArgs& a, cudaStream_t stream);
+// Configure the kernels' shared-memory limit on the current device and report, per
+// sk_tile value, how many units of that shape can be resident at once.
+cudaError_t prepare_device(int num_sms, int* max_units);
 // C = sum_j P[j] in j order, FP32 -> c_bf16 ? BF16 : FP32. mn % 4 == 0.
 cudaError_t launch_reduce(const float* P, void* C, int c_bf16, int splits, int64_t mn, int num_sms,
                           cudaStream_t stream);

@@ -20,6 +20,7 @@
 #include <mutex>
 
 #include "sk.h"
+#include "sk_schedule.h"
 
 namespace {
 
@@ -63,8 +64,9 @@ extern "C" int32_t sk_gemm_noalloc(const void* A, const void* B, void* C, sk_dty
     // reduction also the partial tiles, which peers accumulate into. Split-K slabs are
     // written in full, so only the status word matters there.
     int64_t clear = SK_WS_HEADER_BYTES;
-    if (!s.split_partials) {
-        const int64_t slot_bytes = 128ll * 128 * 4;
+    int32_t tm = 0, tn = 0, cg = 0;
+    if (!s.split_partials && sk::tile_shape(s.tile, &tm, &tn, &cg)) {
+        const int64_t slot_bytes = static_cast<int64_t>(tm) * tn * 4;
         const int64_t n_slots = (need - SK_WS_HEADER_BYTES) / slot_bytes;
         clear = r == SK_ATOMIC ? need : need - n_slots * slot_bytes;
     }

@@ -38,7 +38,20 @@ struct Sched {
     // Split-K: effective split count, k-iterations per split, slab mode flag.
     int32_t splits, chunk, partials;
     int32_t label, label_splits, n_slots;
+    // Work-tile shape and CTAs per tile (a unit is one CTA or one CTA pair).
+    int32_t tile_m, tile_n, cg;
 };
+
+// (tile_m, tile_n, CTAs per tile) of each sk_tile value; false for an unknown value.
+SK_HD bool tile_shape(int32_t tile, int32_t* tm, int32_t* tn, int32_t* cg) {
+    switch (tile) {
+        case 0: *tm = 128; *tn = 128; *cg = 1; return true;
+        case 1: *tm = 256; *tn = 128; *cg = 2; return true;
+        case 2: *tm = 256; *tn = 256; *cg = 2; return true;
+        case 3: *tm = 128; *tn = 256; *cg = 1; return true;
+        default: return false;
+    }
+}
 
 struct Seg {
     int32_t tile, k_begin, k_end, role, slot, peer_begin, n_peers;

@@ -51,6 +51,13 @@ typedef enum { SK_F32 = 0, SK_BF16 = 1 } sk_dtype;
  * reduced afterwards by sk_reduce_splits (split-K report, Contract). */
 typedef enum { SK_ROLE_FULL = 0, SK_ROLE_OWNER = 1, SK_ROLE_PRODUCER = 2, SK_ROLE_SLAB = 3 } sk_role;
 
+/* Work-tile shapes. The pages' tile is 128 x 128 computed by one CTA (SK_TILE_128x128).
+ * The pair shapes are computed by two CTAs on neighbouring SMs together (tcgen05
+ * cta_group::2, each CTA holding half of the tile's rows and half of B's columns), so a
+ * persistent unit is a CTA pair and num_sms SMs give num_sms / 2 units; CUTLASS
+ * example 74 on the first page uses the 256 x 128 pair tile. */
+typedef enum { SK_TILE_128x128 = 0, SK_TILE_256x128_PAIR = 1, SK_TILE_256x256_PAIR = 2, SK_TILE_128x256 = 3 } sk_tile;
+
 typedef struct {
     int32_t mode;           /* sk_mode */
     int32_t splits;         /* Split-K split count s, 1 <= s <= iters (SK_SPLITK only) */
@@ -58,6 +65,7 @@ typedef struct {
     int32_t min_iters;      /* hybrid rule's minimum k-iterations per Stream-K unit; 0 = 8 */
     int32_t split_partials; /* SK_SPLITK only: 1 = every split writes an FP32 slab into the
                                workspace and a second kernel reduces the slabs into C */
+    int32_t tile;           /* sk_tile; 0 = 128 x 128 */
 } sk_schedule;
 
 #define SK_OK          0
@@ -68,18 +76,20 @@ typedef struct {
 #define SK_ECAPACITY  -5  /* sk_plan: the map buffer is smaller than sk_plan_size */
 #define SK_ERESIDENCY -6  /* more persistent units than the device can hold at once */
 
-#define SK_TILE_M 128
+#define SK_TILE_M 128   /* tile of SK_TILE_128x128 */
 #define SK_TILE_N 128
 #define SK_BLK_K 64
 
 /* Work-unit map layout (int32). Header of SK_MAP_HEADER values:
  *   [0] version (SK_MAP_VERSION)   [1] resolved mode (sk_mode; the hybrid rule resolves
  *   to SK_DP or SK_HYBRID)   [2] tiles   [3] iters   [4] workers = units launched
+ *   (CTA pairs for the pair tiles)
  *   [5] sk_tiles: tiles in the Stream-K region (the last sk_tiles tile ids)
  *   [6] sk_units: units over that region   [7] n_segments
  *   [8] splits: effective Split-K split count (empty trailing splits dropped), else 0
  *   [9] hybrid label (-1 none, 0 DataParallel, 1 SplitK, 2 StreamK)
  *   [10] the label's split count   [11] n_slots: FP32 partial-tile slots used
+ *   [12] tile_m   [13] tile_n   [14] CTAs per tile (1 or 2)
  * then n_segments rows of SK_MAP_SEG values, in (unit, run order) order:
  *   unit, order, tile, k_begin, k_end, role, slot, peer_begin, n_peers
  *   (k_begin/k_end in k-iterations; PRODUCER: slot = its partial slot; OWNER: its peers'
@@ -88,14 +98,15 @@ typedef struct {
  *   SLAB: slot = split index; unused fields are -1 or 0)
  * then `tiles` rows of SK_MAP_TILE values: owner unit (runs k = 0), contributors. */
 #define SK_MAP_VERSION 1
-#define SK_MAP_HEADER 12
+#define SK_MAP_HEADER 15
 #define SK_MAP_SEG 9
 #define SK_MAP_TILE 2
 
 /* Workspace layout: bytes [0, SK_WS_HEADER_BYTES) hold the device status word
  * (int32 at offset 0). In split-partials mode the FP32 slabs P[j][M][N] follow at
  * offset SK_WS_HEADER_BYTES, j = 0 .. splits-1, row-major. In the other modes one
- * int32 flag (or counter) per slot follows, then the 64 KiB partial slots. */
+ * int32 flag (or counter) per slot and CTA of the tile follows (256-aligned), then the
+ * partial slots of tile_m x tile_n FP32 each. */
 #define SK_WS_HEADER_BYTES 256
 
 /* Number of int32 values sk_plan writes for this problem, or a negative SK_E* code.
@@ -145,11 +156,23 @@ typedef struct {
                                      flag, so every owner's wait runs out (time-out test) */
     int64_t timeout_ns;           /* limit of every device-side wait, from kernel start;
                                      0 = the default of 2 s */
-    float* dump;                  /* NULL, or a device buffer of tiles * iters * 16384 FP32:
-                                     the segment of tile t starting at k-iteration k writes
-                                     its own accumulator (before any fixup), row-major
-                                     128 x 128, at offset (t * iters + k) * 16384 */
+    float* dump;                  /* NULL, or a device buffer of tiles * iters * tile_m *
+                                     tile_n FP32: the segment of tile t starting at
+                                     k-iteration k writes its own accumulator (before any
+                                     fixup), row-major tile_m x tile_n, at offset
+                                     (t * iters + k) * tile_m * tile_n */
+    uint64_t* trace;              /* NULL, or a device buffer of SK_TRACE_WORDS uint64 per
+                                     CTA (workers * CTAs per tile): %globaltimer stamps in
+                                     ns, layout below */
 } sk_debug_opts;
+
+/* Per-CTA trace record (sk_debug_opts.trace), indexed by blockIdx: [0] start (after set-up),
+ * [1] end (before the exit barrier), [2] segments walked, [3] reserved; then for segment i
+ * < SK_TRACE_SEGS, at 4 + 4 * i: [0] MMA issue of its first k-iteration (leader CTA only),
+ * [1] MMA commit of its last, [2] epilogue has the accumulator, [3] epilogue done (after the
+ * fixup and the stores). Unused words stay as the caller left them. */
+#define SK_TRACE_SEGS 15
+#define SK_TRACE_WORDS (4 + 4 * SK_TRACE_SEGS)
 
 /* sk_gemm with diagnostic controls; opts == NULL behaves exactly like sk_gemm. */
 int32_t sk_gemm_debug(const void* A, const void* B, void* C, sk_dtype c_dtype,

@@ -11,8 +11,8 @@ persistent CTA (one per SM); the fixup combines a split tile's FP32 partials.
 
 Map format produced by `plan_map` (int32 list), the contract the C library's
 sk_plan must reproduce exactly:
-  header (12): version, mode_resolved, tiles, iters, workers, sk_tiles, sk_units,
-               n_segments, splits, label, label_splits, n_slots
+  header (15): version, mode_resolved, tiles, iters, workers, sk_tiles, sk_units,
+               n_segments, splits, label, label_splits, n_slots, tile_m, tile_n, cta_group
   n_segments rows (9): unit, order, tile, k_begin, k_end, role, slot, peer_begin, n_peers
   tiles rows (2): owner_unit, n_contrib
 """
@@ -31,8 +31,12 @@ FULL, OWNER, PRODUCER, SLAB = 0, 1, 2, 3
 # heuristic labels
 LABEL_NONE, LABEL_DP, LABEL_SPLITK, LABEL_STREAMK = -1, 0, 1, 2
 
+# work-tile shapes: (tile_m, tile_n, CTAs per tile). A tile of the pair shapes is computed by
+# two CTAs together, so a unit is a CTA pair and num_sms SMs give num_sms // 2 units.
+TILE_SHAPES = {0: (128, 128, 1), 1: (256, 128, 2), 2: (256, 256, 2), 3: (128, 256, 1)}
+
 MAP_VERSION = 1
-HEADER_LEN = 12
+HEADER_LEN = 15
 SEG_LEN = 9
 TILE_ROW_LEN = 2
 
@@ -52,9 +56,9 @@ def waves(m: int, n: int, sms: int, tile_m: int = TILE_M, tile_n: int = TILE_N):
     return tiles, w, tail, tiles / (w * sms)
 
 
-def problem_shape(M: int, N: int, K: int):
+def problem_shape(M: int, N: int, K: int, tile_m: int = TILE_M, tile_n: int = TILE_N):
     """Tile grid and K-loop length of a GEMM (page, Case 2 report: tiles and iters by ceiling)."""
-    tiles_m, tiles_n = cdiv(M, TILE_M), cdiv(N, TILE_N)
+    tiles_m, tiles_n = cdiv(M, tile_m), cdiv(N, tile_n)
     return tiles_m, tiles_n, tiles_m * tiles_n, cdiv(K, BLK_K)
 
 
@@ -149,6 +153,9 @@ class Plan:
     label_splits: int = 0
     n_slots: int = 0
     units: list = field(default_factory=list)   # units[w] = list of Segment in execution order
+    tile_m: int = TILE_M
+    tile_n: int = TILE_N
+    cta_group: int = 1
 
     def segments(self):
         return [s for segs in self.units for s in segs]
@@ -194,13 +201,16 @@ def _streamk_region(tiles_base: int, n_tiles: int, iters: int, n_units: int):
 
 
 def build_plan(M: int, N: int, K: int, num_sms: int, mode: int, splits: int = 1,
-               units: int = 0, min_iters: int = 8, split_partials: bool = False) -> Plan:
+               units: int = 0, min_iters: int = 8, split_partials: bool = False, tile: int = 0) -> Plan:
     """The integer work-unit map for one GEMM.
 
     `units` > 0 replaces num_sms as the number of persistent units (the toy case is
     "forced to 4 units"). Readings of the page where it leaves the step open:
       - DP (Mental model, Case 2 data_parallel): unit w runs tiles w, w + W, ... with
         W = min(units, tiles), each tile FULL.
+      - Tile shape (`tile`, TILE_SHAPES): the pages' tile is 128 x 128 (tile 0). The
+        CTA-pair shapes make one unit of two SMs, so `units` defaults to num_sms // 2;
+        the schedule itself is the same over the coarser tile grid.
       - Split-K (Case 2 split_k; the split-K report's "final split is clamped"): split j
         of a tile covers k-iterations [j*chunk, min((j+1)*chunk, iters)), chunk =
         ceil(iters / s); empty trailing splits are dropped (s_eff = ceil(iters / chunk)).
@@ -223,13 +233,23 @@ def build_plan(M: int, N: int, K: int, num_sms: int, mode: int, splits: int = 1,
         raise ValueError("bad mode")
     if split_partials and mode != SPLITK:
         raise ValueError("split partials need Split-K")
-    _, tiles_n, tiles, iters = problem_shape(M, N, K)
-    S = units if units > 0 else num_sms
+    if tile not in TILE_SHAPES:
+        raise ValueError("bad tile shape")
+    tile_m, tile_n, cg = TILE_SHAPES[tile]
+    _, tiles_n, tiles, iters = problem_shape(M, N, K, tile_m, tile_n)
+    S = units if units > 0 else num_sms // cg
+    if S < 1:
+        raise ValueError("no units")
+    p = _build(S, mode, splits, min_iters, split_partials, tiles, tiles_n, iters)
+    p.tile_m, p.tile_n, p.cta_group = tile_m, tile_n, cg
+    return p
 
+
+def _build(S, mode, splits, min_iters, split_partials, tiles, tiles_n, iters) -> Plan:
     if mode == HYBRID:
         label, sk_tiles, sk_units, lsp = heuristic(tiles, iters, S, min_iters)
         if label == LABEL_DP:
-            p = build_plan(M, N, K, num_sms, DP, units=units)
+            p = _build(S, DP, 1, min_iters, False, tiles, tiles_n, iters)
             p.label, p.label_splits = label, lsp
             return p
         dp_tiles = tiles - sk_tiles
@@ -296,7 +316,7 @@ def tile_rows(p: Plan):
 def plan_map(p: Plan):
     segs = p.segments()
     out = [MAP_VERSION, p.mode, p.tiles, p.iters, p.workers, p.sk_tiles, p.sk_units,
-           len(segs), p.splits, p.label, p.label_splits, p.n_slots]
+           len(segs), p.splits, p.label, p.label_splits, p.n_slots, p.tile_m, p.tile_n, p.cta_group]
     for s in segs:
         out += [s.unit, s.order, s.tile, s.k_begin, s.k_end, s.role, s.slot, s.peer_begin, s.n_peers]
     for o, c in tile_rows(p):

@@ -47,11 +47,17 @@ def test_exports_every_declared_symbol(sk):
     assert set(sk.EXPORTS) == declared
 
 
-def _cmp(sk, M, N, K, sms, mode, splits=1, units=0, min_iters=0, partials=0):
-    want = S.plan_map(S.build_plan(M, N, K, sms, mode, splits=splits, units=units,
-                                   min_iters=min_iters or 8, split_partials=bool(partials)))
-    got = sk.sk_plan(M, N, K, sms, sk.schedule(mode, splits, units, min_iters, partials))
-    assert got.tolist() == want, (M, N, K, sms, mode, splits, units, partials)
+def _cmp(sk, M, N, K, sms, mode, splits=1, units=0, min_iters=0, partials=0, tile=0):
+    try:
+        want = S.plan_map(S.build_plan(M, N, K, sms, mode, splits=splits, units=units,
+                                       min_iters=min_iters or 8, split_partials=bool(partials), tile=tile))
+    except ValueError:
+        with pytest.raises(sk.SkError) as e:
+            sk.sk_plan(M, N, K, sms, sk.schedule(mode, splits, units, min_iters, partials, tile))
+        assert e.value.code == sk.SK_EINVAL
+        return None
+    got = sk.sk_plan(M, N, K, sms, sk.schedule(mode, splits, units, min_iters, partials, tile))
+    assert got.tolist() == want, (M, N, K, sms, mode, splits, units, partials, tile)
     return got
 
 
@@ -73,10 +79,14 @@ def test_plan_matches_oracle_on_workloads(sk):
             _cmp(sk, M, 512, 2048, 148, S.SPLITK, splits=s)
     _cmp(sk, 2048, 2432, 4096, 148, S.SPLITK, splits=2)
     for m in range(128, 4097, 128):
-        for mode in (S.DP, S.STREAMK, S.HYBRID):
-            _cmp(sk, m, m, 4096, 148, mode)
-        for s in (2, 4):
-            _cmp(sk, m, m, 4096, 148, S.SPLITK, splits=s)
+        for tile in (0, 1, 2, 3):
+            for mode in (S.DP, S.STREAMK, S.HYBRID):
+                _cmp(sk, m, m, 4096, 148, mode, tile=tile)
+            for s in (2, 4):
+                _cmp(sk, m, m, 4096, 148, S.SPLITK, splits=s, tile=tile)
+    for tile in (1, 2, 3):
+        for M, N, K, sms, mode in cases:
+            _cmp(sk, M, N, K, sms, mode, tile=tile)
 
 
 def test_plan_toy_units_override(sk):
@@ -89,12 +99,13 @@ def test_plan_bruteforce_small(sk):
     # M, N <= 640, K <= 512, 1..20 SMs, every mode.
     for M, N, K in itertools.product((1, 128, 129, 300, 640), (8, 128, 256, 640), (8, 64, 65, 200, 512)):
         for sms in range(1, 21):
-            for mode in (S.DP, S.STREAMK, S.HYBRID):
-                _cmp(sk, M, N, K, sms, mode)
-            iters = S.cdiv(K, 64)
-            for s in range(1, min(iters, 5) + 1):
-                _cmp(sk, M, N, K, sms, S.SPLITK, splits=s)
-                _cmp(sk, M, N, K, sms, S.SPLITK, splits=s, partials=1)
+            for tile in (0, 1, 2, 3):
+                for mode in (S.DP, S.STREAMK, S.HYBRID):
+                    _cmp(sk, M, N, K, sms, mode, tile=tile)
+                iters = S.cdiv(K, 64)
+                for s in range(1, min(iters, 5) + 1):
+                    _cmp(sk, M, N, K, sms, S.SPLITK, splits=s, tile=tile)
+                    _cmp(sk, M, N, K, sms, S.SPLITK, splits=s, partials=1, tile=tile)
 
 
 def test_plan_min_iters(sk):
@@ -104,16 +115,18 @@ def test_plan_min_iters(sk):
 
 
 def test_workspace_size(sk):
-    for M, N, K, sms, mode, s, part in [(2048, 2432, 4096, 148, S.HYBRID, 1, 0), (128, 640, 256, 4, S.STREAMK, 1, 0),
-                                        (96, 512, 2048, 148, S.SPLITK, 8, 1), (2048, 2432, 4096, 148, S.SPLITK, 2, 0),
-                                        (2048, 2432, 4096, 148, S.DP, 1, 0)]:
-        sch = sk.schedule(mode, s, 0, 0, part)
+    for (M, N, K, sms, mode, s, part), tile in itertools.product(
+            [(2048, 2432, 4096, 148, S.HYBRID, 1, 0), (128, 640, 256, 4, S.STREAMK, 1, 0),
+             (96, 512, 2048, 148, S.SPLITK, 8, 1), (2048, 2432, 4096, 148, S.SPLITK, 2, 0),
+             (2048, 2432, 4096, 148, S.DP, 1, 0)], (0, 1, 2, 3)):
+        sch = sk.schedule(mode, s, 0, 0, part, tile)
         m = sk.sk_plan(M, N, K, sms, sch)
         n_slots, splits = int(m[11]), int(m[8])
+        tm, tn, cg = int(m[12]), int(m[13]), int(m[14])
         if part:
             want = 256 + 4 * splits * M * N
         else:
-            want = 256 + -(-4 * n_slots // 256) * 256 + n_slots * 65536
+            want = 256 + -(-4 * n_slots * cg // 256) * 256 + n_slots * tm * tn * 4
         for r in (sk.SK_DETERMINISTIC, sk.SK_ATOMIC):
             assert sk.sk_workspace_size(M, N, K, sms, sch, r) == want
 
@@ -127,6 +140,8 @@ def test_errors(sk):
         (128, 128, 128, 4, sk.schedule(sk.SK_SPLITK, 0)),
         (128, 128, 128, 4, sk.schedule(sk.SK_STREAMK, 1, 0, 0, 1)),  # slabs need Split-K
         (128, 128, 128, 4, sk.schedule(sk.SK_DP, 1, -1)),
+        (128, 128, 128, 4, sk.schedule(sk.SK_DP, 1, 0, 0, 0, 4)),      # unknown tile shape
+        (128, 128, 128, 1, sk.schedule(sk.SK_DP, 1, 0, 0, 0, 1)),      # a pair needs 2 SMs
     ]
     for M, N, K, sms, sch in bad:
         with pytest.raises(sk.SkError) as e:

@@ -61,23 +61,29 @@ SCHEDULES = [
 
 
 # --------------------------------------------------------------------------- toy
+TILES = [0, 1, 2, 3]
+
+
+@pytest.mark.parametrize("tile", TILES)
 @pytest.mark.parametrize("red", [DET, ATOM])
 @pytest.mark.parametrize("name,kw", SCHEDULES)
-def test_toy(sk, dev, name, kw, red):
-    # 5 tiles x 4 k-iterations on 4 units (Mental model figure).
+def test_toy(sk, dev, name, kw, red, tile):
+    # 5 tiles x 4 k-iterations on 4 units (Mental model figure); the pair and wide tile
+    # shapes run the same problem over their coarser grids.
     w = synth.TOY
-    sched = sk.schedule(units=4, **kw)
+    sched = sk.schedule(units=4, tile=tile, **kw)
     got, _ = _run(sk, dev, w, sched, red, 4)
     assert not np.any(got == U.SENTINEL)
     U.assert_close(got, U.reference(w), name)
 
 
 # --------------------------------------------------------------------------- exact
+@pytest.mark.parametrize("tile", TILES)
 @pytest.mark.parametrize("layout", ["NN", "NT"])
 @pytest.mark.parametrize("red", [DET, ATOM])
 @pytest.mark.parametrize("sms", [3, 7, 152])
 @pytest.mark.parametrize("name,kw", SCHEDULES)
-def test_integer_exact(sk, dev, name, kw, red, sms, layout):
+def test_integer_exact(sk, dev, name, kw, red, sms, layout, tile):
     # Ragged in M, N and K (300 x 264 x 520: 3 x 3 tiles, 9 k-iterations, the last one
     # 8 deep); integer inputs in [-4, 4] keep every partial sum exact in FP32, so every
     # schedule and reduction must equal the oracle exactly.
@@ -85,11 +91,12 @@ def test_integer_exact(sk, dev, name, kw, red, sms, layout):
     A_bits, B_bits = synth.small_int_inputs(M, N, K, layout, 17)
     A, B = U.to_dev(A_bits, dev), U.to_dev(B_bits, dev)
     ref = og.ref_gemm(A_bits, B_bits, layout)
-    got, guards, _, status = U.gemm(sk, A, B, M, N, K, layout, sk.schedule(**kw), red, sms, "f32", dev)
+    sched = sk.schedule(tile=tile, **kw)
+    got, guards, _, status = U.gemm(sk, A, B, M, N, K, layout, sched, red, sms, "f32", dev)
     assert status == sk.SK_OK and guards
     assert np.array_equal(got, ref)
     # BF16 output: the exact value rounded once to nearest even.
-    got16, guards, _, status = U.gemm(sk, A, B, M, N, K, layout, sk.schedule(**kw), red, sms, "bf16", dev)
+    got16, guards, _, status = U.gemm(sk, A, B, M, N, K, layout, sched, red, sms, "bf16", dev)
     assert status == sk.SK_OK and guards
     want16 = torch.from_numpy(ref.astype(np.float32)).to(torch.bfloat16).float().numpy()
     assert np.array_equal(got16, want16.astype(np.float64))
@@ -99,7 +106,11 @@ def test_integer_exact(sk, dev, name, kw, red, sms, layout):
 @pytest.mark.parametrize("red", [DET, ATOM])
 @pytest.mark.parametrize("name,kw,sms", [
     ("dp", dict(mode=0), 148), ("splitk2", dict(mode=1, splits=2), 148), ("streamk", dict(mode=2), 148),
-    ("hybrid", dict(mode=3), 148), ("hybrid_dev", dict(mode=3), None), ("streamk_dev", dict(mode=2), None)])
+    ("hybrid", dict(mode=3), 148), ("hybrid_dev", dict(mode=3), None), ("streamk_dev", dict(mode=2), None),
+    ("dp_pair128", dict(mode=0, tile=1), 148), ("hybrid_pair128", dict(mode=3, tile=1), 148),
+    ("streamk_pair128", dict(mode=2, tile=1), 148), ("splitk2_pair128", dict(mode=1, splits=2, tile=1), 148),
+    ("hybrid_pair256", dict(mode=3, tile=2), 148), ("streamk_pair256", dict(mode=2, tile=2), None),
+    ("hybrid_wide256", dict(mode=3, tile=3), 148), ("streamk_wide256", dict(mode=2, tile=3), 148)])
 def test_waveq_full(sk, dev, dev_sms, name, kw, sms, red):
     # 2048 x 2432 x 4096: 304 tiles = 2 waves + 8 on 148 SMs, BF16 out; full comparison.
     w = synth.WAVEQ
@@ -120,12 +131,13 @@ def test_waveq_atomic_equals_deterministic_two_contributors(sk, dev):
 
 
 # --------------------------------------------------------------------------- small-M NT
+@pytest.mark.parametrize("tile", [0, 1])
 @pytest.mark.parametrize("w", [synth.SMALLM_96, synth.SMALLM_256], ids=["m96", "m256"])
 @pytest.mark.parametrize("s", [2, 4, 8, 16])
-def test_smallm_split_slabs(sk, dev, dev_sms, w, s):
+def test_smallm_split_slabs(sk, dev, dev_sms, w, s, tile):
     # [splits, M, N] FP32 slabs then the reduction pass (split-K report, Contract): every
     # slab against FP64 dot products over its own K range, and the reduced C.
-    sched = sk.schedule(1, splits=s, split_partials=1)
+    sched = sk.schedule(1, splits=s, split_partials=1, tile=tile)
     got, (ws, _) = _run(sk, dev, w, sched, DET, dev_sms)
     A_bits, B_bits = U.inputs(w)
     P_ref = og.ref_split_partials(A_bits, B_bits, "NT", s)
@@ -145,12 +157,13 @@ def test_smallm_split_slabs(sk, dev, dev_sms, w, s):
     assert np.array_equal(got, fold.astype(np.float64))
 
 
+@pytest.mark.parametrize("tile", TILES)
 @pytest.mark.parametrize("w", [synth.SMALLM_96, synth.SMALLM_256], ids=["m96", "m256"])
 @pytest.mark.parametrize("name,kw", [("streamk", dict(mode=2)), ("hybrid", dict(mode=3)),
                                      ("splitk4", dict(mode=1, splits=4)), ("dp", dict(mode=0))])
 @pytest.mark.parametrize("red", [DET, ATOM])
-def test_smallm_fixup(sk, dev, w, name, kw, red):
-    got, _ = _run(sk, dev, w, sk.schedule(**kw), red, 148)
+def test_smallm_fixup(sk, dev, w, name, kw, red, tile):
+    got, _ = _run(sk, dev, w, sk.schedule(tile=tile, **kw), red, 148)
     ref = U.reference(w)
     U.assert_close(got, ref, name)
     assert np.all(got[0] == 0.0)
@@ -158,29 +171,33 @@ def test_smallm_fixup(sk, dev, w, name, kw, red):
 
 
 # --------------------------------------------------------------------------- sweep
+@pytest.mark.parametrize("tile", [0, 1, 2])
 @pytest.mark.parametrize("m", [128, 640, 1152, 1536, 2560, 4096])
 @pytest.mark.parametrize("name,kw", [("dp", dict(mode=0)), ("splitk2", dict(mode=1, splits=2)),
                                      ("streamk", dict(mode=2)), ("hybrid", dict(mode=3))])
-def test_sweep(sk, dev, m, name, kw):
+def test_sweep(sk, dev, m, name, kw, tile):
     w = synth.sweep(m)
-    got, _ = _run(sk, dev, w, sk.schedule(**kw), DET, 148)
+    got, _ = _run(sk, dev, w, sk.schedule(tile=tile, **kw), DET, 148)
     A_bits, B_bits = U.inputs(w)
     rows = U.sample_rows(m, 32, seed=m)
     U.assert_close(got[rows], og.ref_rows(A_bits, B_bits, "NN", rows), name)
 
 
 # --------------------------------------------------------------------------- large / long-K
+@pytest.mark.parametrize("tile", [0, 1, 2])
 @pytest.mark.parametrize("name,kw", [("hybrid", dict(mode=3)), ("streamk", dict(mode=2))])
-def test_skinny_long_k(sk, dev, name, kw):
-    # 512 x 512 x 65536: 16 tiles x 1024 k-iterations, up to 11 contributors per tile.
+def test_skinny_long_k(sk, dev, name, kw, tile):
+    # 512 x 512 x 65536: 16 tiles x 1024 k-iterations, up to 11 contributors per tile
+    # (4 tiles over 74 pairs with the 256 x 256 pair tile: about 19 per tile).
     w = synth.SKINNY
-    got, _ = _run(sk, dev, w, sk.schedule(**kw), DET, 148)
+    got, _ = _run(sk, dev, w, sk.schedule(tile=tile, **kw), DET, 148)
     U.assert_close(got, U.reference(w), name)
 
 
-def test_large_8192(sk, dev, dev_sms):
+@pytest.mark.parametrize("tile", [0, 2])
+def test_large_8192(sk, dev, dev_sms, tile):
     w = synth.LARGE
-    got, _ = _run(sk, dev, w, sk.schedule(3), DET, dev_sms)
+    got, _ = _run(sk, dev, w, sk.schedule(3, tile=tile), DET, dev_sms)
     A_bits, B_bits = U.inputs(w)
     rows = U.sample_rows(w.M, 24, seed=5)
     U.assert_close(got[rows], og.ref_rows(A_bits, B_bits, "NN", rows), "8192^3")
@@ -189,7 +206,8 @@ def test_large_8192(sk, dev, dev_sms):
 # --------------------------------------------------------------------------- determinism
 @pytest.mark.parametrize("w,sched_kw,units", [
     (synth.WAVEQ, dict(mode=3), 148), (synth.SKINNY, dict(mode=2), 148),
-    (synth.sweep(256), dict(mode=2), 40)])
+    (synth.sweep(256), dict(mode=2), 40), (synth.WAVEQ, dict(mode=3, tile=1), 148),
+    (synth.SKINNY, dict(mode=2, tile=2), 148), (synth.sweep(512), dict(mode=2, tile=1, units=20), 148)])
 def test_deterministic_repeatable(sk, dev, w, sched_kw, units):
     # Deterministic mode: bit-identical over 10 runs and under the reversed unit -> CTA
     # order (the first page's Case 3 varies arrival order through a unit permutation).
@@ -200,16 +218,17 @@ def test_deterministic_repeatable(sk, dev, w, sched_kw, units):
         assert np.array_equal(first, again)
 
 
-def test_turnstile_k_order(sk, dev):
-    # FP32 output, Stream-K over 40 units on 4 tiles x 64 iterations (about ten
-    # contributors a tile): C must be the left fold, in k order, of every segment's own
-    # FP32 partial.
-    w = synth.Workload("t256", 256, 256, 4096, "NN", "normal", 31, out="f32")
-    sched = sk.schedule(2, units=40)
-    plan = osch.build_plan(w.M, w.N, w.K, 40, osch.STREAMK)
-    dump = torch.zeros(plan.tiles * plan.iters * 16384, dtype=torch.float32, device=dev)
-    got, _ = _run(sk, dev, w, sched, DET, 40, dump=dump)
-    D = dump.cpu().numpy().reshape(plan.tiles, plan.iters, 128, 128)
+@pytest.mark.parametrize("tile,units", [(0, 40), (1, 20), (2, 10), (3, 20)])
+def test_turnstile_k_order(sk, dev, tile, units):
+    # FP32 output, Stream-K over many units on few tiles (several contributors a tile): C
+    # must be the left fold, in k order, of every segment's own FP32 partial.
+    w = synth.Workload("t512", 512, 512, 4096, "NN", "normal", 31, out="f32")
+    sched = sk.schedule(2, units=units, tile=tile)
+    plan = osch.build_plan(w.M, w.N, w.K, 148, osch.STREAMK, units=units, tile=tile)
+    tm, tn = plan.tile_m, plan.tile_n
+    dump = torch.zeros(plan.tiles * plan.iters * tm * tn, dtype=torch.float32, device=dev)
+    got, _ = _run(sk, dev, w, sched, DET, 148, dump=dump)
+    D = dump.cpu().numpy().reshape(plan.tiles, plan.iters, tm, tn)
     want = np.zeros((w.M, w.N), dtype=np.float32)
     most = 0
     for t in range(plan.tiles):
@@ -218,32 +237,34 @@ def test_turnstile_k_order(sk, dev):
         acc = D[t, segs[0].k_begin].copy()
         for s in segs[1:]:
             acc = acc + D[t, s.k_begin]
-        r0, c0 = (t // plan.tiles_n) * 128, (t % plan.tiles_n) * 128
-        want[r0:r0 + 128, c0:c0 + 128] = acc
+        r0, c0 = (t // plan.tiles_n) * tm, (t % plan.tiles_n) * tn
+        want[r0:r0 + tm, c0:c0 + tn] = acc[:min(tm, w.M - r0), :min(tn, w.N - c0)]
     assert most >= 4
     assert np.array_equal(got, want.astype(np.float64))
     U.assert_close(got, U.reference(w), "turnstile")
 
 
 # --------------------------------------------------------------------------- atomics
-def test_atomic_many_contributors(sk, dev):
+@pytest.mark.parametrize("tile", [0, 1, 2])
+def test_atomic_many_contributors(sk, dev, tile):
     # Skinny shape, up to 11 contributors per tile: within tolerance (bits may vary with
     # arrival order once a tile has three or more contributors).
     w = synth.SKINNY
-    got, ws = _run(sk, dev, w, sk.schedule(2), ATOM, 148)
+    got, ws = _run(sk, dev, w, sk.schedule(2, tile=tile), ATOM, 148)
     U.assert_close(got, U.reference(w), "atomic")
-    again, _ = _run(sk, dev, w, sk.schedule(2), ATOM, 148, ws=ws, reverse_units=1)
+    again, _ = _run(sk, dev, w, sk.schedule(2, tile=tile), ATOM, 148, ws=ws, reverse_units=1)
     U.assert_close(again, U.reference(w), "atomic reversed")
 
 
 # --------------------------------------------------------------------------- edges
 @pytest.mark.parametrize("M,N,K", [(1, 8, 8), (1, 8, 4096), (129, 136, 72), (128, 128, 8), (200, 1000, 1000),
                                    (127, 8, 65536 // 8)])
+@pytest.mark.parametrize("tile", TILES)
 @pytest.mark.parametrize("name,kw", [("dp", dict(mode=0)), ("streamk", dict(mode=2)), ("hybrid", dict(mode=3)),
                                      ("splitk", dict(mode=1, splits=1))])
-def test_edges(sk, dev, M, N, K, name, kw):
+def test_edges(sk, dev, M, N, K, name, kw, tile):
     w = synth.Workload("e", M, N, K, "NT", "normal", 3, out="f32")
-    got, _ = _run(sk, dev, w, sk.schedule(**kw), DET, 152)
+    got, _ = _run(sk, dev, w, sk.schedule(tile=tile, **kw), DET, 152)
     U.assert_close(got, U.reference(w), name)
 
 
@@ -287,12 +308,13 @@ def test_reduce_splits(sk, dev, s, mn, out):
 
 
 # --------------------------------------------------------------------------- time-out
-def test_wait_timeout_reports_status(sk, dev):
+@pytest.mark.parametrize("tile", [0, 1])
+def test_wait_timeout_reports_status(sk, dev, tile):
     # Producers store but never raise their flag: every owner's wait runs out after 50 ms,
     # the kernel unwinds and records SK_ETIMEOUT; the context stays usable and the
     # workspace works again once zeroed.
     w = synth.TOY
-    sched = sk.schedule(2, units=4)
+    sched = sk.schedule(2, units=4, tile=tile)
     A_bits, B_bits = U.inputs(w)
     A, B = U.to_dev(A_bits, dev), U.to_dev(B_bits, dev)
     ws = U.new_workspace(sk, w.M, w.N, w.K, 4, sched, DET, dev)

@@ -214,5 +214,23 @@ def test_hybrid_waveq_on_148():
 def test_map_layout():
     p = S.build_plan(128, 640, 256, 4, S.STREAMK)
     m = S.plan_map(p)
-    assert m[:S.HEADER_LEN] == [1, S.STREAMK, 5, 4, 4, 5, 4, 8, 0, -1, 0, 4]
+    assert m[:S.HEADER_LEN] == [1, S.STREAMK, 5, 4, 4, 5, 4, 8, 0, -1, 0, 4, 128, 128, 1]
     assert len(m) == S.HEADER_LEN + 8 * S.SEG_LEN + 5 * S.TILE_ROW_LEN
+
+
+@pytest.mark.parametrize("tile", [0, 1, 2, 3])
+def test_tile_shapes(tile):
+    # A pair tile is one unit of two SMs: 148 SMs give 74 units over 256-row tiles; the
+    # wave-quantized shape keeps its 2 waves + a short tail (152 pair tiles on 74 units).
+    tm, tn, cg = S.TILE_SHAPES[tile]
+    p = S.build_plan(2048, 2432, 4096, 148, S.HYBRID, tile=tile)
+    assert (p.tile_m, p.tile_n, p.cta_group) == (tm, tn, cg)
+    assert p.tiles == S.cdiv(2048, tm) * S.cdiv(2432, tn)
+    assert p.workers <= 148 // cg
+    _check_plan_invariants(p, 2048, 2432, 4096, 148)
+    if tile == 1:
+        assert p.tiles == 152 and p.sk_units == 74 and p.sk_tiles == 152 - 74
+    for mode in (S.DP, S.STREAMK, S.SPLITK):
+        _check_plan_invariants(S.build_plan(300, 520, 1000, 7, mode, splits=2, tile=tile), 300, 520, 1000, 7)
+    with pytest.raises(ValueError):
+        S.build_plan(128, 128, 64, 1, S.DP, tile=1) if cg == 2 else S.build_plan(128, 128, 64, 1, S.DP, tile=9)
