@@ -44,6 +44,7 @@ struct Smem {
     __device__ uint32_t tfull(int b) const { return base + S::kSmemBarOff + 8 * (2 * S::kStages + b); }
     __device__ uint32_t tempty(int b) const { return base + S::kSmemBarOff + 8 * (2 * S::kStages + 2 + b); }
     __device__ uint32_t done() const { return base + S::kSmemBarOff + 8 * (2 * S::kStages + 4); }
+    __device__ uint32_t tready() const { return base + S::kSmemBarOff + 8 * (2 * S::kStages + 5); }
 };
 
 __device__ __forceinline__ void record_timeout(const KArgs& a, volatile int* abort_flag) {
@@ -134,12 +135,14 @@ __device__ void run_mma(const KArgs& a, const Smem<Shape<kCG, kBN>>& sm, uint32_
     int stage = 0;
     uint32_t phase = 0;
     int buf = 0;
-    uint32_t uses[2] = {0u, 0u};
+    uint32_t uses0 = 0u, uses1 = 0u;  // phase parities of the two accumulators
     bool ok = true;
     uint64_t* tr = a.trace ? a.trace + static_cast<int64_t>(blockIdx.x) * kTraceWords : nullptr;
     int seg = 0;
+    // A pair's MMA writes both CTAs' TMEM: wait until the peer has allocated its part.
+    if (kCG == 2 && !mbar_wait<true>(sm.tready(), 0u, abort_flag, deadline)) ok = false;
     while (ok && w.next(a.sch, g)) {
-        if (!mbar_wait<kCG == 2>(sm.tempty(buf), uses[buf] ^ 1u, abort_flag, deadline)) {
+        if (!mbar_wait<kCG == 2>(sm.tempty(buf), (buf ? uses1 : uses0) ^ 1u, abort_flag, deadline)) {
             ok = false;
             break;
         }
@@ -181,7 +184,10 @@ __device__ void run_mma(const KArgs& a, const Smem<Shape<kCG, kBN>>& sm, uint32_
             umma_commit_pair(sm.tfull(buf), 0x3);
         if (tr && seg < kTraceSegs) tr[4 + 4 * seg + 1] = globaltimer();
         ++seg;
-        uses[buf] ^= 1u;
+        if (buf)
+            uses1 ^= 1u;
+        else
+            uses0 ^= 1u;
         buf ^= 1;
     }
     if (!ok) record_timeout(a, abort_flag);
@@ -219,40 +225,65 @@ __device__ __forceinline__ bool wait_flag(const int32_t* f, int32_t target, uint
     return ok;
 }
 
-// Partial-slot layout within one 128-column slice of a CTA's rows: element (row r, column
-// 4q + e of 32-column chunk c) at float4 index (c * 8 + q) * 128 + r, so a warp's 32 rows
-// touch 512 contiguous bytes per access.
-__device__ __forceinline__ int slot_f4(int c, int q, int row) { return ((c * 8 + q) * kCtaRows + row) * 4; }
+// Partial-slot layout: a CTA's share of a slot (128 rows x kBN columns FP32) is split into
+// one contiguous block per epilogue warp (its 32 rows x kCols columns, block index
+// chalf * 4 + quad); inside a block, element (lane, column 32c + 4q + e) sits at float4
+// index (c * 8 + q) * 32 + lane, so each warp access covers 512 contiguous bytes.
+__device__ __forceinline__ int slot_f4(int c, int q, int lane) { return ((c * 8 + q) * 32 + lane) * 4; }
 
-// Store a 128-column slice of this warp's 32 rows (one row per lane, in registers) through
-// the warp's two 4 KiB staging boxes with TMA tensor stores: BF16 C in two boxes of 64
-// columns, FP32 C or slab in four boxes of 32 columns, each box 32 rows x 128 bytes in the
-// 128-byte swizzled layout (16-byte chunk j of row r at chunk j ^ (r % 8)), so the shared
-// stores are conflict-free and the TMA clips the box at M and N. `slab` < 0 stores to C.
-__device__ __forceinline__ void store_slice(const KArgs& a, const CUtensorMap* tmC, uint32_t staging,
-                                            uint32_t& nstore, const float (&v)[128], int32_t x0, int32_t y0,
-                                            int32_t slab) {
+// Store kCols columns of this warp's 32 rows (one row per lane, in registers) through the
+// warp's two 4 KiB staging boxes with TMA tensor stores: BF16 C in boxes of 64 columns, FP32
+// C or slab in boxes of 32 columns, each box 32 rows x 128 bytes in the 128-byte swizzled
+// layout (16-byte chunk j of row r at chunk j ^ (r % 8)), so the shared stores are
+// conflict-free and the TMA clips the box at M and N. `slab` < 0 stores to C.
+// One 32-row x 128-byte box of this warp's rows (8 chunks of 16 bytes per row, given as
+// 32-bit words w[j][0..3]) through staging buffer nstore & 1, stored by the TMA at (x, y0)
+// (or (x, y0, slab)).
+template <class F>
+__device__ __forceinline__ void store_box(const CUtensorMap* tmC, uint32_t staging, uint32_t& nstore, int32_t x,
+                                          int32_t y0, int32_t slab, F&& words) {
     const int lane = threadIdx.x & 31;
-    const bool bf16 = a.c_bf16 && slab < 0;
-    const int boxes = bf16 ? 2 : 4;
-    const int cols = bf16 ? 64 : 32;
+    const uint32_t buf = staging + (nstore & 1u) * 4096u;
+    if (nstore >= 2) {
+        // The store issued two boxes ago used this buffer: wait until the TMA read it.
+        if (lane == 0) bulk_wait_group_read<1>();
+        __syncwarp();
+    }
+    const uint32_t row = buf + static_cast<uint32_t>(lane) * 128u;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        uint32_t w0, w1, w2, w3;
+        words(j, w0, w1, w2, w3);
+        st_shared_v4(row + static_cast<uint32_t>((j ^ (lane & 7)) * 16), w0, w1, w2, w3);
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+        if (slab < 0)
+            tma_store_2d(tmC, buf, x, y0);
+        else
+            tma_store_3d(tmC, buf, x, y0, slab);
+        bulk_commit_group();
+    }
+    ++nstore;
+}
+
+// Store kCols columns of this warp's 32 rows (one row per lane, in registers) with TMA
+// tensor stores through the warp's two 4 KiB staging boxes: BF16 C in boxes of 64 columns,
+// FP32 C or slab in boxes of 32 columns, each box 32 rows x 128 bytes in the 128-byte
+// swizzled layout (16-byte chunk j of row r at chunk j ^ (r % 8)), so the shared stores are
+// conflict-free and the TMA clips the box at M and N. `slab` < 0 stores to C.
+template <int kCols>
+__device__ __forceinline__ void store_slice(const KArgs& a, const CUtensorMap* tmC, uint32_t staging,
+                                            uint32_t& nstore, const float (&v)[kCols], int32_t x0, int32_t y0,
+                                            int32_t slab) {
     if (y0 >= a.M) return;  // the warp's 32 rows lie below C
+    if (a.c_bf16 && slab < 0) {
 #pragma unroll
-    for (int b = 0; b < 4; ++b) {
-        if (b >= boxes) break;
-        const int32_t x = x0 + b * cols;
-        if (x >= a.N) break;
-        const uint32_t buf = staging + (nstore & 1u) * 4096u;
-        if (nstore >= 2) {
-            // The store issued two boxes ago used this buffer: wait until the TMA read it.
-            if (lane == 0) bulk_wait_group_read<1>();
-            __syncwarp();
-        }
-        const uint32_t row = buf + static_cast<uint32_t>(lane) * 128u;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            uint32_t w0, w1, w2, w3;
-            if (bf16) {
+        for (int b = 0; b < kCols / 64; ++b) {
+            const int32_t x = x0 + b * 64;
+            if (x >= a.N) break;
+            store_box(tmC, staging, nstore, x, y0, slab, [&](int j, uint32_t& w0, uint32_t& w1, uint32_t& w2, uint32_t& w3) {
                 const int i = b * 64 + j * 8;
                 __nv_bfloat162 p0 = __floats2bfloat162_rn(v[i + 0], v[i + 1]);
                 __nv_bfloat162 p1 = __floats2bfloat162_rn(v[i + 2], v[i + 3]);
@@ -262,64 +293,91 @@ __device__ __forceinline__ void store_slice(const KArgs& a, const CUtensorMap* t
                 w1 = *reinterpret_cast<uint32_t*>(&p1);
                 w2 = *reinterpret_cast<uint32_t*>(&p2);
                 w3 = *reinterpret_cast<uint32_t*>(&p3);
-            } else {
+            });
+        }
+    } else {
+#pragma unroll
+        for (int b = 0; b < kCols / 32; ++b) {
+            const int32_t x = x0 + b * 32;
+            if (x >= a.N) break;
+            store_box(tmC, staging, nstore, x, y0, slab, [&](int j, uint32_t& w0, uint32_t& w1, uint32_t& w2, uint32_t& w3) {
                 const int i = b * 32 + j * 4;
                 w0 = __float_as_uint(v[i + 0]);
                 w1 = __float_as_uint(v[i + 1]);
                 w2 = __float_as_uint(v[i + 2]);
                 w3 = __float_as_uint(v[i + 3]);
-            }
-            st_shared_v4(row + static_cast<uint32_t>((j ^ (lane & 7)) * 16), w0, w1, w2, w3);
+            });
         }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-            if (slab < 0)
-                tma_store_2d(tmC, buf, x, y0);
-            else
-                tma_store_3d(tmC, buf, x, y0, slab);
-            bulk_commit_group();
-        }
-        ++nstore;
     }
 }
 
-template <int kCG, int kBN>
-__device__ void run_epilogue(const KArgs& a, const CUtensorMap* tmC, const Smem<Shape<kCG, kBN>>& sm,
-                             uint32_t tmem_base, int unit, uint32_t rank, uint64_t deadline,
-                             volatile int* abort_flag) {
-    using S = Shape<kCG, kBN>;
-    constexpr int kHalves = kBN / 128;
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
-    const int et = threadIdx.x - 64;          // 0..127 among the epilogue threads
-    const int quad = warp & 3;                // TMEM lanes this warp may read: 32*quad ..
-    const int row = quad * 32 + lane;         // row of this CTA's part of the tile
-    const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
-    // The accumulator-empty barriers live in the leader CTA.
-    const uint32_t tempty_addr[2] = {kCG == 1 ? sm.tempty(0) : mapa_shared(sm.tempty(0), 0),
-                                     kCG == 1 ? sm.tempty(1) : mapa_shared(sm.tempty(1), 0)};
-    const int32_t r = static_cast<int32_t>(rank);
-    const uint32_t staging = sm.base + S::kStagingOff + static_cast<uint32_t>(warp - 2) * 8192u;
-    uint32_t nstore = 0;
-    Walk w;
-    w.init(a.sch, unit);
-    Seg g;
-    int buf = 0;
-    uint32_t uses[2] = {0u, 0u};
-    uint64_t* tr = (a.trace && et == 0) ? a.trace + static_cast<int64_t>(blockIdx.x) * kTraceWords : nullptr;
-    int seg = 0;
-    while (w.next(a.sch, g)) {
-        const bool got = mbar_wait(sm.tfull(buf), uses[buf], abort_flag, deadline);
-        if (named_bar_or(1, kEpiThreads, !got || *abort_flag != 0)) {
-            if (!got) record_timeout(a, abort_flag);
-            break;
+// v (+)= kPassCols columns (chunks c0, c0 + 1, ...) of this warp's block of a partial slot;
+// kZero clears what it read (the atomic slot re-arms itself).
+template <bool kAdd, bool kZero>
+__device__ __forceinline__ void load_partial(float (&v)[kPassCols], float* blk, int c0, int lane) {
+#pragma unroll
+    for (int c = 0; c < kPassCols / 32; ++c)
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const int i = c * 32 + q * 4;
+            float* p = blk + slot_f4(c0 + c, q, lane);
+            const float4 x = ld_cg_f4(p);
+            if (kAdd) {
+                v[i] += x.x;
+                v[i + 1] += x.y;
+                v[i + 2] += x.z;
+                v[i + 3] += x.w;
+            } else {
+                v[i] = x.x;
+                v[i + 1] = x.y;
+                v[i + 2] = x.z;
+                v[i + 3] = x.w;
+            }
+            if (kZero) st_cg_f4(p, make_float4(0.f, 0.f, 0.f, 0.f));
         }
-        tc_fence_after();
-        if (tr && seg < kTraceSegs) tr[4 + 4 * seg + 2] = globaltimer();
+}
 
-        // Owner: wait for every peer's partial (this CTA's share of it) before folding.
-        if (g.role == kOwner) {
+// Columns [o, o + 64) of one accumulator row (held in t) into the debug dump at d.
+template <int kN>
+__device__ __forceinline__ void dump_row(float* d, const uint32_t (&t)[kN], int o) {
+#pragma unroll
+    for (int q = 0; q < 16; ++q)
+        *reinterpret_cast<float4*>(d + 4 * q) =
+            make_float4(__uint_as_float(t[o + 4 * q]), __uint_as_float(t[o + 4 * q + 1]),
+                        __uint_as_float(t[o + 4 * q + 2]), __uint_as_float(t[o + 4 * q + 3]));
+}
+
+// Per-CTA epilogue state shared by the segments of one unit.
+template <int kCG, int kBN>
+struct Epi {
+    using S = Shape<kCG, kBN>;
+    const KArgs& a;
+    const CUtensorMap* tmC;
+    const Smem<S>& sm;
+    uint32_t tmem_base;
+    uint64_t deadline;
+    volatile int* abort_flag;
+    int lane, et, quad, chalf, row;
+    int32_t r;
+    uint32_t tcol, staging, nstore;
+    uint32_t tempty0, tempty1;   // accumulator-empty barriers (in the leader CTA)
+    int64_t blk_off;
+    int buf;                     // accumulator in use (0 or 1) and its phase parities
+    uint32_t uses0, uses1;
+
+    __device__ __forceinline__ float* block(int32_t slot) const {
+        return a.slots + static_cast<int64_t>(slot * kCG + r) * S::kCtaSlotFloats + blk_off;
+    }
+
+    // One segment. Returns false when a wait gave up (the caller then stops).
+    template <bool kOwner>
+    __device__ __forceinline__ bool segment(const Seg& g, uint64_t* tr, int seg) {
+        constexpr int kChunks = kPassCols / 32;  // TMEM loads per pass
+        float v[kPassCols];
+        if (kOwner) {
+            // Wait for every peer (this CTA's share of the partials), then fetch the first pass
+            // of the first partial (or of the atomic sum) while this segment's MAC loop is
+            // still running.
             bool ok = true;
             if (a.atomic) {
                 ok = wait_flag(a.flags + g.peer_begin * kCG + r, g.n_peers, deadline, abort_flag);
@@ -329,106 +387,104 @@ __device__ void run_epilogue(const KArgs& a, const CUtensorMap* tmC, const Smem<
             }
             if (named_bar_or(1, kEpiThreads, !ok)) {
                 record_timeout(a, abort_flag);
-                break;
+                return false;
             }
+            if (a.atomic)
+                load_partial<false, true>(v, block(g.peer_begin), 0, lane);
+            else
+                load_partial<false, false>(v, block(g.peer_begin), 0, lane);
         }
+        const bool got = mbar_wait(sm.tfull(buf), buf ? uses1 : uses0, abort_flag, deadline);
+        if (named_bar_or(1, kEpiThreads, !got || *abort_flag != 0)) {
+            if (!got) record_timeout(a, abort_flag);
+            return false;
+        }
+        tc_fence_after();
+        if (tr && seg < kTraceSegs) tr[4 + 4 * seg + 2] = globaltimer();
 
         const int32_t m0 = (g.tile / a.sch.tiles_n) * (kCtaRows * kCG) + r * kCtaRows;
-        const int32_t n0 = (g.tile % a.sch.tiles_n) * kBN;
+        const int32_t n0 = (g.tile % a.sch.tiles_n) * kBN + chalf * S::kCols;
         const int32_t wy = m0 + quad * 32;  // first row of this warp's 32
+        float* dump = a.dump ? a.dump +
+                                   (static_cast<int64_t>(g.tile) * a.sch.iters + g.k_begin) * (kCtaRows * kCG * kBN) +
+                                   static_cast<int64_t>(r * kCtaRows + row) * kBN + chalf * S::kCols
+                             : nullptr;
 
 #pragma unroll 1
-        for (int h = 0; h < kHalves; ++h) {
-            float v[128];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t rr[32];
-                tmem_ld_32x32b_x32_sync(
-                    tmem_base + lane_addr + static_cast<uint32_t>(buf * kBN + h * 128 + c * 32), rr);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) v[c * 32 + i] = __uint_as_float(rr[i]);
+        for (int p = 0; p < S::kPasses; ++p) {
+            if (kOwner && p > 0) {
+                if (a.atomic)
+                    load_partial<false, true>(v, block(g.peer_begin), kChunks * p, lane);
+                else
+                    load_partial<false, false>(v, block(g.peer_begin), kChunks * p, lane);
             }
-            if (h == kHalves - 1) {
-                // The accumulator is in registers: hand it back to the MMA issuer.
+            // This pass of the segment's own accumulator: one TMEM load for the whole pass,
+            // or for an owner 64 columns at a time added to the first partial (own + P1: the
+            // first step of the k-order fold).
+            const uint32_t taddr = tmem_base + tcol + static_cast<uint32_t>(buf * kBN + p * kPassCols);
+            if (kOwner) {
+#pragma unroll
+                for (int h = 0; h < kPassCols / 64; ++h) {
+                    uint32_t t[64];
+                    tmem_ld_32x32b_x64_sync(taddr + static_cast<uint32_t>(h * 64), t);
+#pragma unroll
+                    for (int i = 0; i < 64; ++i) v[h * 64 + i] = __uint_as_float(t[i]) + v[h * 64 + i];
+                    if (dump) dump_row<64>(dump + p * kPassCols + h * 64, t, 0);
+                }
+            } else {
+                uint32_t t[kPassCols];
+                tmem_ld_pass_sync(taddr, t);
+#pragma unroll
+                for (int i = 0; i < kPassCols; ++i) v[i] = __uint_as_float(t[i]);
+                if (dump) {
+#pragma unroll
+                    for (int h = 0; h < kPassCols / 64; ++h) dump_row<kPassCols>(dump + p * kPassCols + h * 64, t, h * 64);
+                }
+            }
+            if (p == S::kPasses - 1) {
+                // The whole accumulator has been read: hand it back to the MMA issuer.
                 tc_fence_before();
                 if (kCG == 1)
-                    mbar_arrive(tempty_addr[buf]);
+                    mbar_arrive(buf ? tempty1 : tempty0);
                 else
-                    mbar_arrive_cluster(tempty_addr[buf]);
+                    mbar_arrive_cluster(buf ? tempty1 : tempty0);
             }
 
-            if (a.dump) {
-                float* d = a.dump +
-                           (static_cast<int64_t>(g.tile) * a.sch.iters + g.k_begin) * (kCtaRows * kCG * kBN) +
-                           static_cast<int64_t>(r * kCtaRows + row) * kBN + h * 128;
+            if (kOwner) {
+                // Turnstile: the remaining peers' partials, in k order.
+                if (!a.atomic) {
+                    for (int32_t pi = 1; pi < g.n_peers; ++pi)
+                        load_partial<true, false>(v, block(g.peer_begin + pi), kChunks * p, lane);
+                }
+                store_slice<kPassCols>(a, tmC, staging, nstore, v, n0 + p * kPassCols, wy, -1);
+            } else if (g.role == kProducer) {
+                float* blk = block(a.atomic ? g.peer_begin : g.slot);
 #pragma unroll
-                for (int q = 0; q < 32; ++q)
-                    *reinterpret_cast<float4*>(d + 4 * q) =
-                        make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-            }
-
-            if (g.role == kProducer) {
-                const int32_t s_idx = a.atomic ? g.peer_begin : g.slot;
-                float* s = a.slots + static_cast<int64_t>(s_idx * kCG + r) * S::kCtaSlotFloats + h * S::kHalfFloats;
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
+                for (int c = 0; c < kChunks; ++c)
 #pragma unroll
                     for (int q = 0; q < 8; ++q) {
                         const int i = c * 32 + q * 4;
+                        float* dst = blk + slot_f4(kChunks * p + c, q, lane);
                         if (a.atomic)
-                            red_add_v4_f32(s + slot_f4(c, q, row), v[i], v[i + 1], v[i + 2], v[i + 3]);
+                            red_add_v4_f32(dst, v[i], v[i + 1], v[i + 2], v[i + 3]);
                         else
-                            st_cg_f4(s + slot_f4(c, q, row), make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]));
+                            st_cg_f4(dst, make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]));
                     }
-            } else if (g.role == kOwner) {
-                // Turnstile: fold the peers' partials into this unit's own in k order.
-                if (a.atomic) {
-                    float* s = a.slots + static_cast<int64_t>(g.peer_begin * kCG + r) * S::kCtaSlotFloats +
-                               h * S::kHalfFloats;
-                    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                    for (int c = 0; c < 4; ++c)
-#pragma unroll
-                        for (int q = 0; q < 8; ++q) {
-                            const int i = c * 32 + q * 4;
-                            const float4 p = ld_cg_f4(s + slot_f4(c, q, row));
-                            v[i] += p.x;
-                            v[i + 1] += p.y;
-                            v[i + 2] += p.z;
-                            v[i + 3] += p.w;
-                            st_cg_f4(s + slot_f4(c, q, row), z);
-                        }
-                } else {
-                    for (int32_t pi = 0; pi < g.n_peers; ++pi) {
-                        const float* s = a.slots +
-                                         static_cast<int64_t>((g.peer_begin + pi) * kCG + r) * S::kCtaSlotFloats +
-                                         h * S::kHalfFloats;
-#pragma unroll
-                        for (int c = 0; c < 4; ++c)
-#pragma unroll
-                            for (int q = 0; q < 8; ++q) {
-                                const int i = c * 32 + q * 4;
-                                const float4 p = ld_cg_f4(s + slot_f4(c, q, row));
-                                v[i] += p.x;
-                                v[i + 1] += p.y;
-                                v[i + 2] += p.z;
-                                v[i + 3] += p.w;
-                            }
-                    }
-                }
-                store_slice(a, tmC, staging, nstore, v, n0 + h * 128, wy, -1);
             } else if (g.role == kSlab) {
-                store_slice(a, tmC, staging, nstore, v, n0 + h * 128, wy, g.slot);
+                store_slice<kPassCols>(a, tmC, staging, nstore, v, n0 + p * kPassCols, wy, g.slot);
             } else {
-                store_slice(a, tmC, staging, nstore, v, n0 + h * 128, wy, -1);
+                store_slice<kPassCols>(a, tmC, staging, nstore, v, n0 + p * kPassCols, wy, -1);
             }
         }
-        uses[buf] ^= 1u;
+        if (buf)
+            uses1 ^= 1u;
+        else
+            uses0 ^= 1u;
         buf ^= 1;
 
         if (g.role == kProducer) {
-            // Every epilogue thread's share is stored: publish it.
-            __threadfence();
+            // Every epilogue thread's share is stored: publish it. The barrier orders all of
+            // them before one thread's release at GPU scope (release is cumulative).
             named_bar_sync(1, kEpiThreads);
             if (et == 0 && !a.skip_signal) {
                 if (a.atomic)
@@ -436,7 +492,7 @@ __device__ void run_epilogue(const KArgs& a, const CUtensorMap* tmC, const Smem<
                 else
                     st_release_gpu(a.flags + g.slot * kCG + r, 1);
             }
-        } else if (g.role == kOwner) {
+        } else if (kOwner) {
             // Every epilogue thread has read the partials: re-arm the flags / counter.
             named_bar_sync(1, kEpiThreads);
             if (et == 0) {
@@ -447,11 +503,45 @@ __device__ void run_epilogue(const KArgs& a, const CUtensorMap* tmC, const Smem<
                 }
             }
         }
+        return true;
+    }
+};
+
+template <int kCG, int kBN>
+__device__ void run_epilogue(const KArgs& a, const CUtensorMap* tmC, const Smem<Shape<kCG, kBN>>& sm,
+                             uint32_t tmem_base, int unit, uint32_t rank, uint64_t deadline,
+                             volatile int* abort_flag) {
+    using S = Shape<kCG, kBN>;
+    const int warp = threadIdx.x >> 5;
+    Epi<kCG, kBN> e{a, tmC, sm, tmem_base, deadline, abort_flag};
+    e.lane = threadIdx.x & 31;
+    e.et = threadIdx.x - 64;                  // index among the epilogue threads
+    e.quad = warp & 3;                        // TMEM lanes this warp may read: 32*quad ..
+    e.chalf = (warp - 2) >> 2;                // which part of the tile's columns (0 with 4 warps)
+    e.row = e.quad * 32 + e.lane;             // row of this CTA's part of the tile
+    e.r = static_cast<int32_t>(rank);
+    e.tcol = static_cast<uint32_t>(e.quad * 32) << 16 | static_cast<uint32_t>(e.chalf * S::kCols);
+    e.staging = sm.base + S::kStagingOff + static_cast<uint32_t>(warp - 2) * 8192u;
+    e.nstore = 0;
+    // The accumulator-empty barriers live in the leader CTA.
+    e.tempty0 = kCG == 1 ? sm.tempty(0) : mapa_shared(sm.tempty(0), 0);
+    e.tempty1 = kCG == 1 ? sm.tempty(1) : mapa_shared(sm.tempty(1), 0);
+    e.blk_off = static_cast<int64_t>(e.chalf * 4 + e.quad) * S::kWarpSlotFloats;
+    e.buf = 0;
+    e.uses0 = e.uses1 = 0u;
+    uint64_t* tr = (a.trace && e.et == 0) ? a.trace + static_cast<int64_t>(blockIdx.x) * kTraceWords : nullptr;
+    Walk w;
+    w.init(a.sch, unit);
+    Seg g;
+    int seg = 0;
+    while (w.next(a.sch, g)) {
+        const bool ok = g.role == kOwner ? e.template segment<true>(g, tr, seg) : e.template segment<false>(g, tr, seg);
+        if (!ok) break;
         if (tr && seg < kTraceSegs) tr[4 + 4 * seg + 3] = globaltimer();
         ++seg;
     }
     // Every TMA store of this warp has written C before the CTA may exit.
-    if (lane == 0) bulk_wait_group_all();
+    if (e.lane == 0) bulk_wait_group_all();
     __syncwarp();
     if (tr) tr[2] = static_cast<uint64_t>(seg);
 }
@@ -486,15 +576,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(sm.tempty(b), kEpiThreads * kCG);
         }
         mbar_init(sm.done(), 1);
+        mbar_init(sm.tready(), 1);
         *abort_flag = 0;
         fence_mbar_init();
-    }
-    if (warp == 0 && lane == 0) {
         prefetch_tmap(&tmA);
         prefetch_tmap(&tmB);
         prefetch_tmap(&tmC);
     }
-    if (warp == 1) {
+    // Barriers are initialised (in both CTAs of a pair) before anyone signals them. TMEM is
+    // allocated afterwards, while the producer's first loads are already in flight.
+    if (kCG == 2)
+        cluster_sync();
+    else
+        __syncthreads();
+    if (args.trace && threadIdx.x == 0) args.trace[static_cast<int64_t>(blockIdx.x) * kTraceWords] = globaltimer();
+
+    // Warps 0 and 1 reconverge before the exit barrier: a CTA barrier counts a warp once
+    // any of its threads arrives, so all 32 lanes must arrive together.
+    uint32_t tmem_base = 0;
+    if (warp == 0) {
+        if (lane == 0) run_producer<kNT, kCG, kBN>(args, &tmA, &tmB, sm, unit, rank, deadline, abort_flag);
+        __syncwarp();
+    } else if (warp == 1) {
         if (kCG == 1) {
             tmem_alloc(smem_u32(tmem_holder), S::kTmemCols);
             tmem_relinquish();
@@ -502,25 +605,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_alloc_pair(smem_u32(tmem_holder), S::kTmemCols);
             tmem_relinquish_pair();
         }
-    }
-    tc_fence_before();
-    if (kCG == 2)
-        cluster_sync();
-    else
-        __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_holder);
-    if (args.trace && threadIdx.x == 0) args.trace[static_cast<int64_t>(blockIdx.x) * kTraceWords] = globaltimer();
-
-    // Warps 0 and 1 reconverge before the exit barrier: a CTA barrier counts a warp once
-    // any of its threads arrives, so all 32 lanes must arrive together.
-    if (warp == 0) {
-        if (lane == 0) run_producer<kNT, kCG, kBN>(args, &tmA, &tmB, sm, unit, rank, deadline, abort_flag);
+        // Hand the address to the epilogue warps (named barrier 2: this warp + the epilogue)
+        // and, in a pair, tell the leader's MMA issuer that the peer's TMEM is allocated (the
+        // leader's own allocation precedes its MMAs in this warp's program order).
+        tc_fence_before();
+        named_bar_arrive(2, 32 + kEpiThreads);
+        if (kCG == 2 && rank != 0 && lane == 0) mbar_arrive_cluster(mapa_shared(sm.tready(), 0));
         __syncwarp();
-    } else if (warp == 1) {
+        tc_fence_after();
+        tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_holder);
         if (lane == 0 && rank == 0) run_mma<kNT, kCG, kBN>(args, sm, tmem_base, unit, deadline, abort_flag);
         __syncwarp();
     } else {
+        named_bar_sync(2, 32 + kEpiThreads);
+        tc_fence_after();
+        tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_holder);
         run_epilogue<kCG, kBN>(args, &tmC, sm, tmem_base, unit, rank, deadline, abort_flag);
     }
 

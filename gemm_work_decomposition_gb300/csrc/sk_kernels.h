@@ -9,10 +9,15 @@
 
 namespace sk {
 
-constexpr int kThreads = 192;     // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
-constexpr int kEpiThreads = 128;
+#ifndef SK_EPI_WARPS
+#define SK_EPI_WARPS 4
+#endif
+constexpr int kEpiWarps = SK_EPI_WARPS;  // one per TMEM lane quadrant (4) or two on half the columns (8)
+constexpr int kThreads = 64 + 32 * kEpiWarps;   // warp 0 TMA, warp 1 MMA, then the epilogue warps
+constexpr int kEpiThreads = 32 * kEpiWarps;
+constexpr int kPassCols = kEpiWarps == 4 ? 128 : 64;  // accumulator columns a thread holds at once
 constexpr int kCtaRows = 128;     // rows of a work tile held by one CTA (its TMEM lanes)
-constexpr int kRingBytes = 196608;
+constexpr int kRingBytes = kEpiWarps == 4 ? 196608 : 163840;
 constexpr int kTraceSegs = 15;                  // SK_TRACE_SEGS
 constexpr int kTraceWords = 4 + 4 * kTraceSegs; // SK_TRACE_WORDS
 
@@ -28,12 +33,14 @@ struct Shape {
     // Epilogue staging after the ring: per epilogue warp two 4 KiB boxes (32 rows x 128 B)
     // that the TMA stores to C; then the barrier block and 1 KiB of alignment.
     static constexpr int kStagingOff = kStages * kStageBytes;
-    static constexpr int kStagingBytes = 4 * 2 * 4096;
+    static constexpr int kStagingBytes = kEpiWarps * 2 * 4096;
     static constexpr int kSmemBarOff = kStagingOff + kStagingBytes;
     static constexpr int kSmemBytes = kSmemBarOff + 256 + 1024;
     static constexpr int kTmemCols = 2 * kBN;               // two accumulators of kBN columns
     static constexpr int kTxBytes = kCG * kStageBytes;      // bytes landing on the leader per stage
-    static constexpr int kHalfFloats = kCtaRows * 128;      // one 128-column slice of a CTA's rows
+    static constexpr int kCols = kBN * 4 / kEpiWarps;       // accumulator columns per epilogue thread
+    static constexpr int kPasses = kCols / kPassCols;       // processed kPassCols at a time
+    static constexpr int kWarpSlotFloats = 32 * kCols;      // one epilogue warp's block of a partial
     static constexpr int kCtaSlotFloats = kCtaRows * kBN;   // a CTA's share of one partial slot
     static_assert(kBNc % 64 == 0 && kBN % 128 == 0, "tile shape");
 };
