@@ -40,8 +40,10 @@ WORKLOADS = {"waveq": synth.WAVEQ, "skinny": synth.SKINNY, "large": synth.LARGE,
 # from one ncu capture, keyed by workload/schedule; valid only for the kernel source it
 # was taken on (sha256 of sk_kernels.cu, first 16 hex digits).
 TRAFFIC = {
+    "waveq_2048x2432x4096/hybrid/tile2@148": {"bytes": 36772608 + 1757440, "kernel_sha": "ff6e724716bc24a7",
+                                              "profile": "profiles/sk_gemm_kernel_waveq_2048x2432x4096_pair256_hybrid148.md"},
     "waveq_2048x2432x4096/hybrid/tile0@148": {"bytes": 36744704 + 168960, "kernel_sha": "f3a64766608abaf7",
-                                        "profile": "profiles/sk_gemm_kernel_waveq_2048x2432x4096_hybrid148.md"},
+                                        "profile": "profiles/sk_gemm_kernel_waveq_2048x2432x4096_tile128_hybrid148.md"},
 }
 
 
@@ -364,6 +366,31 @@ def main():
                                        "tflops": flops / (med / 1e3) / 1e12,
                                        "frac_of_measured_peak": flops / (med / 1e3) / 1e12 / peak_tf}
         extras["schedules"] = table
+
+        # ---- tail-wave idle SM-time from one traced launch each (outside the timed region):
+        # sum over SMs of (last SM's end - this SM's end), DP against the headline schedule.
+        def idle(mode_name, nsms, tile):
+            s3, ws3, nb3 = make(mode_name, nsms, 2, tile)
+            plan3 = sk.sk_plan(w.M, w.N, w.K, nsms, s3)
+            ncta = int(plan3[4]) * int(plan3[14])
+            tr = torch.zeros(ncta * sk.SK_TRACE_WORDS, dtype=torch.int64, device=dev)
+            vals = []
+            for _ in range(5):
+                flush.zero_()
+                sk.sk_gemm_debug(A, B, C, out_code, w.M, w.N, w.K, lay, s3, red, nsms, ws3, nb3, stream, trace=tr)
+                torch.cuda.synchronize(dev)
+                T = tr.cpu().numpy().reshape(ncta, sk.SK_TRACE_WORDS).astype(np.int64)
+                end = (T[:, 1] - T[:, 0].min()) / 1e3
+                # SMs without a CTA idle for the whole span
+                vals.append((float(np.sum(end.max() - end)) + (dev_sms - ncta) * float(end.max()), float(end.max())))
+            assert sk.sk_status(ws3, stream) == sk.SK_OK
+            v = sorted(vals)[len(vals) // 2]
+            return {"tail_idle_sm_us": v[0], "span_us": v[1], "ctas": ncta}
+        dp_idle = idle("dp", sms, args.tile)
+        hd_idle = idle(args.mode, sms, args.tile)
+        extras["tail_idle"] = {"dp": dp_idle, args.mode: hd_idle,
+                               "dp_over_schedule": dp_idle["tail_idle_sm_us"] / max(1e-9, hd_idle["tail_idle_sm_us"]),
+                               "definition": "sum over the device's SMs of (kernel end - SM end), per-CTA globaltimer"}
 
         # ---- e2e: host buffers, copies inside the timed region, through the C ABI
         C_host = torch.empty((w.M, w.N), dtype=cdt).pin_memory()

@@ -668,8 +668,10 @@ __global__ void __launch_bounds__(256)
 }
 
 // --------------------------------------------------------------------------- host side
-bool g_pair_coop = true;  // cleared if this device rejects cooperative cluster launches
-
+// One-CTA shapes launch cooperatively (the launch fails unless every unit is resident at
+// once). Pair shapes launch as clusters of 2 without that attribute: the host has checked
+// that every pair fits on the device at once (cudaOccupancyMaxActiveClusters), and an
+// owner only ever waits for producer segments that run first in their own units.
 template <bool kNT, int kCG, int kBN>
 cudaError_t launch_shape(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC, const KArgs& a,
                          cudaStream_t stream) {
@@ -681,8 +683,7 @@ cudaError_t launch_shape(const CUtensorMap& tmA, const CUtensorMap& tmB, const C
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
     int n = 0;
-    const bool coop = kCG == 1 || g_pair_coop;
-    if (coop) {
+    if (kCG == 1) {
         attr[n].id = cudaLaunchAttributeCooperative;
         attr[n].val.cooperative = 1;
         ++n;
@@ -696,17 +697,7 @@ cudaError_t launch_shape(const CUtensorMap& tmA, const CUtensorMap& tmB, const C
     }
     cfg.attrs = attr;
     cfg.numAttrs = n;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, sk_gemm_kernel<kNT, kCG, kBN>, tmA, tmB, tmC, a);
-    if (e != cudaSuccess && kCG == 2 && coop) {
-        // Cooperative launch of clusters is not available: the host has already checked
-        // that every pair fits on the device at once, so launch the clusters plainly.
-        cudaGetLastError();
-        g_pair_coop = false;
-        cfg.attrs = attr + 1;
-        cfg.numAttrs = 1;
-        e = cudaLaunchKernelEx(&cfg, sk_gemm_kernel<kNT, kCG, kBN>, tmA, tmB, tmC, a);
-    }
-    return e;
+    return cudaLaunchKernelEx(&cfg, sk_gemm_kernel<kNT, kCG, kBN>, tmA, tmB, tmC, a);
 }
 
 template <int kCG, int kBN>
