@@ -52,6 +52,18 @@ __device__ __forceinline__ void record_timeout(const KArgs& a, volatile int* abo
     atomicCAS(a.status, 0, kErrTimeout);
 }
 
+// A Stream-K producer segment covers [k_begin, iters) of its tile: it runs its k-loop from
+// the last k-iteration down, so that all units start on the same k-slab of A and B (shared
+// through L2) instead of each on its own (an HBM burst of every unit's data at once when
+// the caches are cold). The order of the MMAs inside one segment's accumulator is free;
+// the k order of the fold across segments is unchanged.
+__device__ __forceinline__ bool reversed_segment(const Sched& s, const Seg& g) {
+    return g.role == kProducer && g.k_end == s.iters;
+}
+__device__ __forceinline__ int32_t seg_k(const Seg& g, bool rev, int32_t i) {
+    return rev ? g.k_end - 1 - i : g.k_begin + i;
+}
+
 // --------------------------------------------------------------------------- warp 0
 template <bool kNT, int kCG, int kBN>
 __device__ void run_producer(const KArgs& a, const CUtensorMap* tmA, const CUtensorMap* tmB,
@@ -69,12 +81,13 @@ __device__ void run_producer(const KArgs& a, const CUtensorMap* tmA, const CUten
         // This CTA's rows of the tile and its half of the tile's columns of B.
         const int32_t m0 = (g.tile / a.sch.tiles_n) * (kCtaRows * kCG) + static_cast<int32_t>(rank) * kCtaRows;
         const int32_t nb = (g.tile % a.sch.tiles_n) * kBN + static_cast<int32_t>(rank) * S::kBNc;
-        for (int32_t k = g.k_begin; k < g.k_end; ++k) {
+        const bool rev = reversed_segment(a.sch, g);
+        for (int32_t i = 0; i < g.k_end - g.k_begin; ++i) {
             if (!mbar_wait(sm.empty(stage), phase ^ 1u, abort_flag, deadline)) {
                 ok = false;
                 break;
             }
-            const int32_t k0 = k * kBlkK;
+            const int32_t k0 = seg_k(g, rev, i) * kBlkK;
             if (kCG == 1) {
                 mbar_arrive_expect_tx(sm.full(stage), S::kTxBytes);
                 tma_load_2d(sm.a(stage), tmA, sm.full(stage), k0, m0);
@@ -148,13 +161,13 @@ __device__ void run_mma(const KArgs& a, const Smem<Shape<kCG, kBN>>& sm, uint32_
         }
         tc_fence_after();
         const uint32_t d = tmem_base + static_cast<uint32_t>(buf * kBN);
-        for (int32_t k = g.k_begin; k < g.k_end; ++k) {
+        for (int32_t i = 0; i < g.k_end - g.k_begin; ++i) {
             if (!mbar_wait(sm.full(stage), phase, abort_flag, deadline)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            if (tr && k == g.k_begin && seg < kTraceSegs) tr[4 + 4 * seg] = globaltimer();
+            if (tr && i == 0 && seg < kTraceSegs) tr[4 + 4 * seg] = globaltimer();
             // A: K-major, 8-row groups 1024 bytes apart. B: K-major likewise (NT), or
             // MN-major (NN) in 64-column boxes 8 KiB apart.
             const uint64_t adesc = smem_desc_sw128(sm.a(stage), 16, 1024);
@@ -162,7 +175,7 @@ __device__ void run_mma(const KArgs& a, const Smem<Shape<kCG, kBN>>& sm, uint32_
                 kNT ? smem_desc_sw128(sm.b(stage), 16, 1024) : smem_desc_sw128(sm.b(stage), 8192, 1024);
 #pragma unroll
             for (int kk = 0; kk < kBlkK / 16; ++kk) {
-                const uint32_t acc = (k > g.k_begin || kk > 0) ? 1u : 0u;
+                const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
                 if (kCG == 1)
                     umma_bf16(d, adesc + kk * kAStep, bdesc + kk * kBStep, kIdesc, acc);
                 else
