@@ -195,7 +195,8 @@ def run_reference(args, w, rank, world):
 
 def run_sweep(sk, torch, dev, path, red, flush, stream, peak_tf, dev_sms):
     """Tile-count sweep: M = N = 128 .. 4096, K = 4096, every schedule plus the hybrid
-    rule's choice, on 148 SMs and on the device's SM count; one JSON line per point."""
+    rule's choice, with the pages' 128 x 128 tile and the 256 x 256 CTA-pair tile, on 148
+    SMs and on the device's SM count; one JSON line per point."""
     with open(path, "w") as f:
         for m in synth.SWEEP_SIZES:
             ww = synth.sweep(m)
@@ -204,10 +205,10 @@ def run_sweep(sk, torch, dev, path, red, flush, stream, peak_tf, dev_sms):
             B = torch.from_numpy(B_bits.view(np.int16)).view(torch.bfloat16).to(dev)
             C = torch.empty((m, m), dtype=torch.bfloat16, device=dev)
             fl = 2.0 * m * m * ww.K
-            for nsms in (148, dev_sms):
+            for nsms, tile in ((148, 0), (dev_sms, 0), (148, 2), (dev_sms, 2)):
                 for name, mode, s in (("dp", sk.SK_DP, 1), ("splitk2", sk.SK_SPLITK, 2), ("splitk4", sk.SK_SPLITK, 4),
                                       ("streamk", sk.SK_STREAMK, 1), ("hybrid", sk.SK_HYBRID, 1)):
-                    sch = sk.schedule(mode, s)
+                    sch = sk.schedule(mode, s, tile=tile)
                     nb = sk.sk_workspace_size(m, m, ww.K, nsms, sch, red)
                     ws = torch.zeros(nb, dtype=torch.uint8, device=dev)
                     plan = sk.sk_plan(m, m, ww.K, nsms, sch)
@@ -224,10 +225,58 @@ def run_sweep(sk, torch, dev, path, red, flush, stream, peak_tf, dev_sms):
                     assert sk.sk_status(ws, stream) == sk.SK_OK
                     t = float(np.median([a.elapsed_time(b) for a, b in ev]))
                     tf = fl / (t / 1e3) / 1e12
-                    f.write(json.dumps({"M": m, "N": m, "K": ww.K, "tiles": int(plan[2]), "num_sms": nsms,
+                    f.write(json.dumps({"M": m, "N": m, "K": ww.K, "tile": tile, "tiles": int(plan[2]), "num_sms": nsms,
                                         "schedule": name, "resolved_mode": int(plan[1]), "label": int(plan[9]),
                                         "us": t * 1e3, "tflops": tf, "frac_of_measured_peak": tf / peak_tf}) + "\n")
                     f.flush()
+
+
+def run_smallm(sk, torch, dev, flush, stream, dev_sms):
+    """The split-K report's shapes (B stored [N,K], FP32 out): M = 96 and 256, N = 512,
+    K = 2048. The [splits, M, N] slab chain (GEMM + reduction pass, two launches) at
+    s = 2, 4, 8, 16, and the one-launch in-kernel fixups, timed one GEMM per event pair
+    (L2 flushed before each) and packed 8 back to back (complete GPU time / 8)."""
+    out = {}
+    for w in (synth.SMALLM_96, synth.SMALLM_256):
+        A_bits, B_bits = synth.make_inputs(w)
+        A = torch.from_numpy(A_bits.view(np.int16)).view(torch.bfloat16).to(dev)
+        B = torch.from_numpy(B_bits.view(np.int16)).view(torch.bfloat16).to(dev)
+        C = torch.empty((w.M, w.N), dtype=torch.float32, device=dev)
+        fl = 2.0 * w.M * w.N * w.K
+        rows = {}
+        cases = [(f"slabs_s{s}", sk.schedule(sk.SK_SPLITK, s, split_partials=1), dev_sms) for s in (2, 4, 8, 16)]
+        cases += [("splitk8_fixup", sk.schedule(sk.SK_SPLITK, 8), dev_sms), ("streamk", sk.schedule(sk.SK_STREAMK), dev_sms),
+                  ("hybrid", sk.schedule(sk.SK_HYBRID), dev_sms)]
+        for name, sch, nsms in cases:
+            nb = sk.sk_workspace_size(w.M, w.N, w.K, nsms, sch, 0)
+            ws = torch.zeros(nb, dtype=torch.uint8, device=dev)
+            g = lambda: sk.sk_gemm(A, B, C, sk.SK_F32, w.M, w.N, w.K, sk.SK_NT, sch, 0, nsms, ws, nb, stream)
+            for _ in range(5):
+                g()
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(40)]
+            for a0, a1 in ev:
+                flush.zero_()
+                a0.record(stream)
+                g()
+                a1.record(stream)
+            torch.cuda.synchronize(dev)
+            one = float(np.median([a0.elapsed_time(a1) for a0, a1 in ev])) * 1e3
+            packs = []
+            for _ in range(20):
+                flush.zero_()
+                a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a0.record(stream)
+                for _ in range(8):
+                    g()
+                a1.record(stream)
+                packs.append((a0, a1))
+            torch.cuda.synchronize(dev)
+            pack8 = float(np.median([a0.elapsed_time(a1) for a0, a1 in packs])) * 1e3 / 8
+            assert sk.sk_status(ws, stream) == sk.SK_OK
+            launches = 2 if "slabs" in name else 1
+            rows[name] = {"us": one, "us_pack8": pack8, "launches": launches, "tflops": fl / (one / 1e6) / 1e12}
+        out[w.name] = rows
+    return out
 
 
 def main():
@@ -423,6 +472,8 @@ def main():
         extras["cpu_baseline"] = {"value": cpu_v, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
                                   "sample": f"{cpu_n} x FP64 GEMM of {cpu_rows} rows x {w.N} x {w.K} "
                                             f"({cpu_s:.1f} s, numpy matmul, default BLAS threads)"}
+
+        extras["smallm_nt"] = run_smallm(sk, torch, dev, flush, stream, dev_sms)
 
         if args.sweep:
             run_sweep(sk, torch, dev, args.sweep, red, flush, stream, peak_tf, dev_sms)

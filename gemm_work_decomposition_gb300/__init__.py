@@ -22,7 +22,7 @@ SK_NN, SK_NT = 0, 1
 SK_DETERMINISTIC, SK_ATOMIC = 0, 1
 SK_F32, SK_BF16 = 0, 1
 SK_ROLE_FULL, SK_ROLE_OWNER, SK_ROLE_PRODUCER, SK_ROLE_SLAB = 0, 1, 2, 3
-SK_OK, SK_EINVAL, SK_EWORKSPACE, SK_ECUDA, SK_ETIMEOUT, SK_ECAPACITY, SK_ERESIDENCY = 0, -1, -2, -3, -4, -5, -6
+SK_OK, SK_EINVAL, SK_EWORKSPACE, SK_ECUDA, SK_ETIMEOUT, SK_ECAPACITY, SK_ERESIDENCY, SK_EBOUNDS = 0, -1, -2, -3, -4, -5, -6, -7
 SK_TILE_M, SK_TILE_N, SK_BLK_K = 128, 128, 64
 SK_MAP_VERSION, SK_MAP_HEADER, SK_MAP_SEG, SK_MAP_TILE = 1, 15, 9, 2
 SK_TILE_128x128, SK_TILE_256x128_PAIR, SK_TILE_256x256_PAIR, SK_TILE_128x256 = 0, 1, 2, 3

@@ -147,11 +147,12 @@ int64_t map_size(const Sched& s) {
 int64_t align_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
 
 // Workspace: header | flags (one int32 per slot and CTA of the tile, 256-aligned) |
-// slots (tile_m x tile_n FP32 each); split-partials: header | slabs [splits][M][N] FP32.
+// slots (tile_m x tile_n FP32 each); split-partials: header | slabs [splits][M][N] FP32 |
+// arrival counters (one int32 per tile and CTA of the tile, 256-aligned).
 int64_t flags_offset() { return SK_WS_HEADER_BYTES; }
 int64_t slots_offset(const Sched& s) { return SK_WS_HEADER_BYTES + align_up(4ll * s.n_slots * s.cg, 256); }
 int64_t workspace_bytes(const Sched& s, int32_t M, int32_t N) {
-    if (s.partials) return SK_WS_HEADER_BYTES + 4ll * s.splits * M * N;
+    if (s.partials) return slab_workspace_bytes(s.splits, M, N, s.tiles, s.cg);
     return slots_offset(s) + static_cast<int64_t>(s.n_slots) * s.tile_m * s.tile_n * 4;
 }
 
@@ -243,6 +244,7 @@ const char* sk_strerror(int32_t code) {
         case SK_ETIMEOUT: return "a device-side wait ran past its time limit";
         case SK_ECAPACITY: return "map buffer smaller than sk_plan_size";
         case SK_ERESIDENCY: return "more persistent units than the device can hold at once";
+        case SK_EBOUNDS: return "a device-side index check failed and the access was skipped";
         default: return "unknown error code";
     }
 }
@@ -351,6 +353,7 @@ int32_t sk_gemm_debug(const void* A, const void* B, void* C, sk_dtype c_dtype, i
     a.flags = reinterpret_cast<int32_t*>(ws + flags_offset());
     a.slots = reinterpret_cast<float*>(ws + slots_offset(sch));
     a.slabs = sch.partials ? reinterpret_cast<float*>(ws + SK_WS_HEADER_BYTES) : nullptr;
+    a.counters = sch.partials ? reinterpret_cast<int32_t*>(ws + slab_counters_offset(sch.splits, M, N)) : nullptr;
     a.M = M;
     a.N = N;
     a.K = K;
@@ -366,21 +369,20 @@ int32_t sk_gemm_debug(const void* A, const void* B, void* C, sk_dtype c_dtype, i
         a.trace = opts->trace;
         if (a.trace && !aligned(a.trace, 8)) return SK_EINVAL;
     }
-    CUtensorMap tmC;
-    const bool okc = sch.partials ? encode_out(&tmC, a.slabs, false, static_cast<uint64_t>(N), static_cast<uint64_t>(M),
-                                               static_cast<uint64_t>(sch.splits), 3)
-                                  : encode_out(&tmC, C, a.c_bf16 != 0, static_cast<uint64_t>(N), static_cast<uint64_t>(M), 1, 2);
-    if (!okc) return SK_ECUDA;
-    if (launch_gemm(tmA, tmB, tmC, nt, a, st) != cudaSuccess) {
+    // tmD: C. tmC: where segments store — C, or the FP32 slabs in split-partials mode, whose
+    // last split per tile then writes the slabs' sum to C (one launch).
+    CUtensorMap tmC, tmD;
+    if (!encode_out(&tmD, C, a.c_bf16 != 0, static_cast<uint64_t>(N), static_cast<uint64_t>(M), 1, 2)) return SK_ECUDA;
+    if (sch.partials) {
+        if (!encode_out(&tmC, a.slabs, false, static_cast<uint64_t>(N), static_cast<uint64_t>(M),
+                        static_cast<uint64_t>(sch.splits), 3))
+            return SK_ECUDA;
+    } else {
+        tmC = tmD;
+    }
+    if (launch_gemm(tmA, tmB, tmC, tmD, nt, a, st) != cudaSuccess) {
         cudaGetLastError();
         return SK_ECUDA;
-    }
-    if (sch.partials) {
-        if (launch_reduce(a.slabs, C, a.c_bf16, sch.splits, static_cast<int64_t>(M) * N, dev_sms, st) !=
-            cudaSuccess) {
-            cudaGetLastError();
-            return SK_ECUDA;
-        }
     }
     return SK_OK;
 }

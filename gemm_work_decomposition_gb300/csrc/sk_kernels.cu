@@ -32,6 +32,7 @@ namespace sk {
 namespace {
 
 constexpr int32_t kErrTimeout = -4;  // SK_ETIMEOUT
+constexpr int32_t kErrBounds = -7;   // SK_EBOUNDS
 constexpr uint64_t kDrainNs = 20ull * 1000 * 1000;
 
 template <class S>
@@ -366,6 +367,7 @@ struct Epi {
     using S = Shape<kCG, kBN>;
     const KArgs& a;
     const CUtensorMap* tmC;
+    const CUtensorMap* tmD;
     const Smem<S>& sm;
     uint32_t tmem_base;
     uint64_t deadline;
@@ -377,15 +379,77 @@ struct Epi {
     int64_t blk_off;
     int buf;                     // accumulator in use (0 or 1) and its phase parities
     uint32_t uses0, uses1;
+    volatile int* last_flag;     // shared word: this CTA took a tile's last slab
 
     __device__ __forceinline__ float* block(int32_t slot) const {
         return a.slots + static_cast<int64_t>(slot * kCG + r) * S::kCtaSlotFloats + blk_off;
     }
 
-    // One segment. Returns false when a wait gave up (the caller then stops).
+    // Split-K slabs, last arriver: this CTA's rows of tile g.tile in C = P[0] + P[1] + ...
+    // + P[splits-1], summed left to right in FP32.
+    __device__ __forceinline__ void reduce_slabs(const Seg& g) {
+        const int32_t m0 = (g.tile / a.sch.tiles_n) * (kCtaRows * kCG) + r * kCtaRows;
+        const int32_t n0 = (g.tile % a.sch.tiles_n) * kBN + chalf * S::kCols;
+        const int32_t gr = m0 + row;
+        const int64_t slab = static_cast<int64_t>(a.M) * a.N;
+#pragma unroll 1
+        for (int p = 0; p < S::kPasses; ++p) {
+            const int32_t c0 = n0 + p * kPassCols;
+            float v[kPassCols];
+#pragma unroll
+            for (int i = 0; i < kPassCols; ++i) v[i] = 0.f;
+            if (gr < a.M) {
+                const float* rowp = a.slabs + static_cast<int64_t>(gr) * a.N + c0;
+#pragma unroll
+                for (int q = 0; q < kPassCols / 4; ++q) {
+                    if (c0 + 4 * q < a.N) {
+                        const float4 x = ld_cg_f4(rowp + 4 * q);
+                        v[4 * q] = x.x;
+                        v[4 * q + 1] = x.y;
+                        v[4 * q + 2] = x.z;
+                        v[4 * q + 3] = x.w;
+                    }
+                }
+#pragma unroll 1
+                for (int32_t j = 1; j < a.sch.splits; ++j) {
+#pragma unroll
+                    for (int q = 0; q < kPassCols / 4; ++q) {
+                        if (c0 + 4 * q < a.N) {
+                            const float4 x = ld_cg_f4(rowp + j * slab + 4 * q);
+                            v[4 * q] += x.x;
+                            v[4 * q + 1] += x.y;
+                            v[4 * q + 2] += x.z;
+                            v[4 * q + 3] += x.w;
+                        }
+                    }
+                }
+            }
+            store_slice<kPassCols>(a, tmD, staging, nstore, v, c0, m0 + quad * 32, -1);
+        }
+    }
+
+    // The workspace indices a segment will use lie inside the extents the host sized.
+    __device__ __forceinline__ bool in_bounds(const Seg& g) const {
+        if (g.tile < 0 || g.tile >= a.sch.tiles) return false;
+        if (g.role == kProducer) {
+            const int32_t s = a.atomic ? g.peer_begin : g.slot;
+            return s >= 0 && s < a.sch.n_slots;
+        }
+        if (g.role == kOwner)
+            return g.peer_begin >= 0 && g.n_peers >= 1 && g.peer_begin + g.n_peers <= a.sch.n_slots;
+        if (g.role == kSlab) return g.slot >= 0 && g.slot < a.sch.splits && a.counters != nullptr;
+        return true;
+    }
+
+    // One segment. Returns false when a wait gave up or a check failed (the caller stops).
     template <bool kOwner>
     __device__ __forceinline__ bool segment(const Seg& g, uint64_t* tr, int seg) {
         constexpr int kChunks = kPassCols / 32;  // TMEM loads per pass
+        if (!in_bounds(g)) {  // same answer in every epilogue thread
+            *abort_flag = 1;
+            atomicCAS(a.status, 0, kErrBounds);
+            return false;
+        }
         float v[kPassCols];
         if (kOwner) {
             // Wait for every peer (this CTA's share of the partials), then fetch the first pass
@@ -495,7 +559,27 @@ struct Epi {
             uses0 ^= 1u;
         buf ^= 1;
 
-        if (g.role == kProducer) {
+        if (g.role == kSlab) {
+            // Split-K slab: publish it and count the arrival at the tile; the split that
+            // arrives last sums the tile's slabs in split order into C (aligned split with a
+            // per-tile arrival counter, as in the docc StreamK rewrite).
+            if (lane == 0) {
+                bulk_wait_group_all();
+                fence_proxy_async_global();
+            }
+            __syncwarp();
+            named_bar_sync(1, kEpiThreads);
+            if (et == 0)
+                *last_flag = atom_add_acq_rel_gpu(a.counters + g.tile * kCG + r, 1) ==
+                             static_cast<uint32_t>(a.sch.splits - 1);
+            named_bar_sync(1, kEpiThreads);
+            if (*last_flag) {
+                (void)ld_acquire_gpu(a.counters + g.tile * kCG + r);
+                reduce_slabs(g);
+                named_bar_sync(1, kEpiThreads);
+                if (et == 0) a.counters[g.tile * kCG + r] = 0;
+            }
+        } else if (g.role == kProducer) {
             // Every epilogue thread's share is stored: publish it. The barrier orders all of
             // them before one thread's release at GPU scope (release is cumulative).
             named_bar_sync(1, kEpiThreads);
@@ -521,12 +605,13 @@ struct Epi {
 };
 
 template <int kCG, int kBN>
-__device__ void run_epilogue(const KArgs& a, const CUtensorMap* tmC, const Smem<Shape<kCG, kBN>>& sm,
-                             uint32_t tmem_base, int unit, uint32_t rank, uint64_t deadline,
-                             volatile int* abort_flag) {
+__device__ void run_epilogue(const KArgs& a, const CUtensorMap* tmC, const CUtensorMap* tmD,
+                             const Smem<Shape<kCG, kBN>>& sm, uint32_t tmem_base, int unit, uint32_t rank,
+                             uint64_t deadline, volatile int* abort_flag, volatile int* last_flag) {
     using S = Shape<kCG, kBN>;
     const int warp = threadIdx.x >> 5;
-    Epi<kCG, kBN> e{a, tmC, sm, tmem_base, deadline, abort_flag};
+    Epi<kCG, kBN> e{a, tmC, tmD, sm, tmem_base, deadline, abort_flag};
+    e.last_flag = last_flag;
     e.lane = threadIdx.x & 31;
     e.et = threadIdx.x - 64;                  // index among the epilogue threads
     e.quad = warp & 3;                        // TMEM lanes this warp may read: 32*quad ..
@@ -563,13 +648,15 @@ __device__ void run_epilogue(const KArgs& a, const CUtensorMap* tmC, const Smem<
 template <bool kNT, int kCG, int kBN>
 __global__ void __launch_bounds__(kThreads, 1)
     sk_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ CUtensorMap tmC, const KArgs args) {
+                   const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmD,
+                   const KArgs args) {
     using S = Shape<kCG, kBN>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     Smem<S> sm{smem_u32(smem)};
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + S::kSmemBarOff + 192);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + S::kSmemBarOff + 196);
+    volatile int* last_flag = reinterpret_cast<volatile int*>(smem + S::kSmemBarOff + 200);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -595,6 +682,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tmap(&tmA);
         prefetch_tmap(&tmB);
         prefetch_tmap(&tmC);
+        prefetch_tmap(&tmD);
     }
     // Barriers are initialised (in both CTAs of a pair) before anyone signals them. TMEM is
     // allocated afterwards, while the producer's first loads are already in flight.
@@ -633,7 +721,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         named_bar_sync(2, 32 + kEpiThreads);
         tc_fence_after();
         tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_holder);
-        run_epilogue<kCG, kBN>(args, &tmC, sm, tmem_base, unit, rank, deadline, abort_flag);
+        run_epilogue<kCG, kBN>(args, &tmC, &tmD, sm, tmem_base, unit, rank, deadline, abort_flag, last_flag);
     }
 
     tc_fence_before();
@@ -686,8 +774,8 @@ __global__ void __launch_bounds__(256)
 // that every pair fits on the device at once (cudaOccupancyMaxActiveClusters), and an
 // owner only ever waits for producer segments that run first in their own units.
 template <bool kNT, int kCG, int kBN>
-cudaError_t launch_shape(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC, const KArgs& a,
-                         cudaStream_t stream) {
+cudaError_t launch_shape(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
+                         const CUtensorMap& tmD, const KArgs& a, cudaStream_t stream) {
     using S = Shape<kCG, kBN>;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(a.sch.workers * kCG), 1, 1);
@@ -710,7 +798,7 @@ cudaError_t launch_shape(const CUtensorMap& tmA, const CUtensorMap& tmB, const C
     }
     cfg.attrs = attr;
     cfg.numAttrs = n;
-    return cudaLaunchKernelEx(&cfg, sk_gemm_kernel<kNT, kCG, kBN>, tmA, tmB, tmC, a);
+    return cudaLaunchKernelEx(&cfg, sk_gemm_kernel<kNT, kCG, kBN>, tmA, tmB, tmC, tmD, a);
 }
 
 template <int kCG, int kBN>
@@ -763,12 +851,12 @@ cudaError_t prepare_device(int num_sms, int* max_units) {
     return e;
 }
 
-cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC, bool nt,
-                        const KArgs& a, cudaStream_t stream) {
+cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
+                        const CUtensorMap& tmD, bool nt, const KArgs& a, cudaStream_t stream) {
     const int cg = a.sch.cg, bn = a.sch.tile_n;
 #define SK_LAUNCH(CG, BN)                                                                 \
-    return nt ? launch_shape<true, CG, BN>(tmA, tmB, tmC, a, stream)                     \
-              : launch_shape<false, CG, BN>(tmA, tmB, tmC, a, stream)
+    return nt ? launch_shape<true, CG, BN>(tmA, tmB, tmC, tmD, a, stream)                \
+              : launch_shape<false, CG, BN>(tmA, tmB, tmC, tmD, a, stream)
     if (cg == 1 && bn == 128) SK_LAUNCH(1, 128);
     if (cg == 2 && bn == 128) SK_LAUNCH(2, 128);
     if (cg == 2 && bn == 256) SK_LAUNCH(2, 256);

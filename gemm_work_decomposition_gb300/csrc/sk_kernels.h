@@ -49,6 +49,7 @@ struct KArgs {
     Sched sch;
     void* C;            // [M,N] FP32 or BF16
     float* slabs;       // split-partials: [splits][M][N] FP32
+    int32_t* counters;  // split-partials: arrivals per tile and CTA of the tile
     float* slots;       // n_slots x tile_m x tile_n FP32 partial tiles
     int32_t* flags;     // n_slots x CTAs-per-tile flags (deterministic) or counters (atomic)
     int32_t* status;    // workspace status word
@@ -64,10 +65,11 @@ struct KArgs {
 
 // Launch the persistent GEMM for a.sch's tile shape: a.sch.workers units of a.sch.cg CTAs,
 // cooperative where the device allows it. Returns a cudaError_t.
-// tmC: the output map — C [M,N] (FP32 or BF16) in boxes of 32 rows x 128 bytes, or for
-// Split-K slabs the FP32 [splits][M][N] map in boxes of 1 x 32 rows x 32 columns.
-cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC, bool nt,
-                        const KArgs& a, cudaStream_t stream);
+// tmC: where segments store — C [M,N] (FP32 or BF16) in boxes of 32 rows x 128 bytes, or
+// for Split-K slabs the FP32 [splits][M][N] map in boxes of 1 x 32 rows x 32 columns.
+// tmD: the C map (the last split of a tile writes the sum of the slabs there).
+cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
+                        const CUtensorMap& tmD, bool nt, const KArgs& a, cudaStream_t stream);
 // Configure the kernels' shared-memory limit on the current device and report, per
 // sk_tile value, how many units of that shape can be resident at once.
 cudaError_t prepare_device(int num_sms, int* max_units);

@@ -60,18 +60,25 @@ extern "C" int32_t sk_gemm_noalloc(const void* A, const void* B, void* C, sk_dty
     void* ws = nullptr;
     const int32_t e = scratch_address(&ws);
     if (e != SK_OK) return e;
-    // What must start at zero: the status word and the per-slot flags/counters; with atomic
-    // reduction also the partial tiles, which peers accumulate into. Split-K slabs are
-    // written in full, so only the status word matters there.
-    int64_t clear = SK_WS_HEADER_BYTES;
+    // What must start at zero: the status word; the per-slot flags/counters (and, with
+    // atomic reduction, the partial tiles, which peers accumulate into); in split-partials
+    // mode the per-tile arrival counters after the slabs (the slabs are written in full).
     int32_t tm = 0, tn = 0, cg = 0;
-    if (!s.split_partials && sk::tile_shape(s.tile, &tm, &tn, &cg)) {
+    if (!sk::tile_shape(s.tile, &tm, &tn, &cg)) return SK_EINVAL;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int64_t clear = SK_WS_HEADER_BYTES;
+    int64_t tail = 0;  // bytes to clear at the end of the used region
+    if (s.split_partials) {
+        const int64_t tiles = ((static_cast<int64_t>(M) + tm - 1) / tm) * ((static_cast<int64_t>(N) + tn - 1) / tn);
+        tail = (4 * tiles * cg + 255) / 256 * 256;
+    } else {
         const int64_t slot_bytes = static_cast<int64_t>(tm) * tn * 4;
         const int64_t n_slots = (need - SK_WS_HEADER_BYTES) / slot_bytes;
         clear = r == SK_ATOMIC ? need : need - n_slots * slot_bytes;
     }
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (cudaMemsetAsync(ws, 0, static_cast<size_t>(clear), st) != cudaSuccess) {
+    if (cudaMemsetAsync(ws, 0, static_cast<size_t>(clear), st) != cudaSuccess ||
+        (tail > 0 && cudaMemsetAsync(static_cast<unsigned char*>(ws) + need - tail, 0, static_cast<size_t>(tail), st) !=
+                         cudaSuccess)) {
         cudaGetLastError();
         return SK_ECUDA;
     }

@@ -53,6 +53,16 @@ SK_HD bool tile_shape(int32_t tile, int32_t* tm, int32_t* tn, int32_t* cg) {
     }
 }
 
+// Split-partials workspace: [0, 256) status | FP32 slabs [splits][M][N] from byte 256 |
+// one arrival counter per tile and CTA of the tile from slab_counters_offset (256-aligned).
+SK_HD int64_t slab_counters_offset(int32_t splits, int32_t M, int32_t N) {
+    const int64_t end = 256 + 4ll * splits * M * N;
+    return (end + 255) / 256 * 256;
+}
+SK_HD int64_t slab_workspace_bytes(int32_t splits, int32_t M, int32_t N, int32_t tiles, int32_t cg) {
+    return slab_counters_offset(splits, M, N) + (4ll * tiles * cg + 255) / 256 * 256;
+}
+
 struct Seg {
     int32_t tile, k_begin, k_end, role, slot, peer_begin, n_peers;
 };

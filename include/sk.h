@@ -64,7 +64,8 @@ typedef struct {
     int32_t units;          /* 0: num_sms persistent units; > 0: use this many instead */
     int32_t min_iters;      /* hybrid rule's minimum k-iterations per Stream-K unit; 0 = 8 */
     int32_t split_partials; /* SK_SPLITK only: 1 = every split writes an FP32 slab into the
-                               workspace and a second kernel reduces the slabs into C */
+                               workspace and the last split of each tile reduces the tile's
+                               slabs into C in split order */
     int32_t tile;           /* sk_tile; 0 = 128 x 128 */
 } sk_schedule;
 
@@ -75,6 +76,7 @@ typedef struct {
 #define SK_ETIMEOUT   -4  /* a device-side wait ran past its time limit (from sk_status) */
 #define SK_ECAPACITY  -5  /* sk_plan: the map buffer is smaller than sk_plan_size */
 #define SK_ERESIDENCY -6  /* more persistent units than the device can hold at once */
+#define SK_EBOUNDS    -7  /* a device-side index check failed; the access was skipped (from sk_status) */
 
 #define SK_TILE_M 128   /* tile of SK_TILE_128x128 */
 #define SK_TILE_N 128
@@ -104,9 +106,11 @@ typedef struct {
 
 /* Workspace layout: bytes [0, SK_WS_HEADER_BYTES) hold the device status word
  * (int32 at offset 0). In split-partials mode the FP32 slabs P[j][M][N] follow at
- * offset SK_WS_HEADER_BYTES, j = 0 .. splits-1, row-major. In the other modes one
- * int32 flag (or counter) per slot and CTA of the tile follows (256-aligned), then the
- * partial slots of tile_m x tile_n FP32 each. */
+ * offset SK_WS_HEADER_BYTES, j = 0 .. splits-1, row-major, then (256-aligned) one int32
+ * arrival counter per tile and CTA of the tile: the split that arrives last at a tile
+ * sums that tile's slabs in split order into C, so the whole chain is one launch. In the
+ * other modes one int32 flag (or counter) per slot and CTA of the tile follows
+ * (256-aligned), then the partial slots of tile_m x tile_n FP32 each. */
 #define SK_WS_HEADER_BYTES 256
 
 /* Number of int32 values sk_plan writes for this problem, or a negative SK_E* code.
@@ -211,7 +215,8 @@ int32_t sk_gemm_noalloc(const void* A, const void* B, void* C, sk_dtype c_dtype,
 
 /* Synchronise `stream`, read the workspace status word, reset it to SK_OK and return
  * it: SK_OK, or SK_ETIMEOUT when a kernel on that workspace stopped at a wait limit.
- * Returns SK_ECUDA if the copy fails. */
+ * Also SK_EBOUNDS if a kernel found a workspace index outside the extents it was given
+ * (it skips that access and stops). Returns SK_ECUDA if the copy fails. */
 int32_t sk_status(void* workspace, void* stream);
 
 /* Static description of an SK_* code. */

@@ -124,7 +124,7 @@ def test_workspace_size(sk):
         n_slots, splits = int(m[11]), int(m[8])
         tm, tn, cg = int(m[12]), int(m[13]), int(m[14])
         if part:
-            want = 256 + 4 * splits * M * N
+            want = 256 + -(-4 * splits * M * N // 256) * 256 + -(-4 * int(m[2]) * cg // 256) * 256
         else:
             want = 256 + -(-4 * n_slots * cg // 256) * 256 + n_slots * tm * tn * 4
         for r in (sk.SK_DETERMINISTIC, sk.SK_ATOMIC):
