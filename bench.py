@@ -233,9 +233,11 @@ def run_sweep(sk, torch, dev, path, red, flush, stream, peak_tf, dev_sms):
 
 def run_smallm(sk, torch, dev, flush, stream, dev_sms):
     """The split-K report's shapes (B stored [N,K], FP32 out): M = 96 and 256, N = 512,
-    K = 2048. The [splits, M, N] slab chain (GEMM + reduction pass, two launches) at
-    s = 2, 4, 8, 16, and the one-launch in-kernel fixups, timed one GEMM per event pair
-    (L2 flushed before each) and packed 8 back to back (complete GPU time / 8)."""
+    K = 2048. The [splits, M, N] slab chain at s = 2, 4, 8, 16 (every split stores its
+    slab; a reduction pass sums them, two launches), the same slabs summed by the last
+    split to arrive at each tile (one launch), and the owner-wait fixups, timed one GEMM
+    per event pair (L2 flushed before each) and packed 8 back to back (complete GPU time
+    / 8)."""
     out = {}
     for w in (synth.SMALLM_96, synth.SMALLM_256):
         A_bits, B_bits = synth.make_inputs(w)
@@ -245,6 +247,7 @@ def run_smallm(sk, torch, dev, flush, stream, dev_sms):
         fl = 2.0 * w.M * w.N * w.K
         rows = {}
         cases = [(f"slabs_s{s}", sk.schedule(sk.SK_SPLITK, s, split_partials=1), dev_sms) for s in (2, 4, 8, 16)]
+        cases += [(f"slabs_last_s{s}", sk.schedule(sk.SK_SPLITK, s, split_partials=2), dev_sms) for s in (2, 4, 8, 16)]
         cases += [("splitk8_fixup", sk.schedule(sk.SK_SPLITK, 8), dev_sms), ("streamk", sk.schedule(sk.SK_STREAMK), dev_sms),
                   ("hybrid", sk.schedule(sk.SK_HYBRID), dev_sms)]
         for name, sch, nsms in cases:
@@ -273,7 +276,7 @@ def run_smallm(sk, torch, dev, flush, stream, dev_sms):
             torch.cuda.synchronize(dev)
             pack8 = float(np.median([a0.elapsed_time(a1) for a0, a1 in packs])) * 1e3 / 8
             assert sk.sk_status(ws, stream) == sk.SK_OK
-            launches = 2 if "slabs" in name else 1
+            launches = 2 if name.startswith("slabs_s") else 1
             rows[name] = {"us": one, "us_pack8": pack8, "launches": launches, "tflops": fl / (one / 1e6) / 1e12}
         out[w.name] = rows
     return out

@@ -64,7 +64,8 @@ void set_streamk(Sched& o, int64_t base, int64_t sk_tiles, int64_t units) {
 int32_t make_sched(int32_t M, int32_t N, int32_t K, int32_t num_sms, const sk_schedule& s, Sched& o) {
     if (M < 1 || N < 1 || K < 1 || num_sms < 1 || s.units < 0 || s.min_iters < 0) return SK_EINVAL;
     if (s.mode < SK_DP || s.mode > SK_HYBRID) return SK_EINVAL;
-    if (s.split_partials != 0 && (s.mode != SK_SPLITK || s.split_partials != 1)) return SK_EINVAL;
+    if (s.split_partials < 0 || s.split_partials > 2) return SK_EINVAL;
+    if (s.split_partials != 0 && s.mode != SK_SPLITK) return SK_EINVAL;
     int32_t tm = 0, tn = 0, cg = 0;
     if (!tile_shape(s.tile, &tm, &tn, &cg)) return SK_EINVAL;
     const int64_t tiles_n = (static_cast<int64_t>(N) + tn - 1) / tn;
@@ -353,7 +354,7 @@ int32_t sk_gemm_debug(const void* A, const void* B, void* C, sk_dtype c_dtype, i
     a.flags = reinterpret_cast<int32_t*>(ws + flags_offset());
     a.slots = reinterpret_cast<float*>(ws + slots_offset(sch));
     a.slabs = sch.partials ? reinterpret_cast<float*>(ws + SK_WS_HEADER_BYTES) : nullptr;
-    a.counters = sch.partials ? reinterpret_cast<int32_t*>(ws + slab_counters_offset(sch.splits, M, N)) : nullptr;
+    a.counters = sch.partials == 2 ? reinterpret_cast<int32_t*>(ws + slab_counters_offset(sch.splits, M, N)) : nullptr;
     a.M = M;
     a.N = N;
     a.K = K;
@@ -369,8 +370,8 @@ int32_t sk_gemm_debug(const void* A, const void* B, void* C, sk_dtype c_dtype, i
         a.trace = opts->trace;
         if (a.trace && !aligned(a.trace, 8)) return SK_EINVAL;
     }
-    // tmD: C. tmC: where segments store — C, or the FP32 slabs in split-partials mode, whose
-    // last split per tile then writes the slabs' sum to C (one launch).
+    // tmD: C. tmC: where segments store — C, or the FP32 slabs in split-partials mode,
+    // summed into C by the reduction pass (1) or by the last split of each tile (2).
     CUtensorMap tmC, tmD;
     if (!encode_out(&tmD, C, a.c_bf16 != 0, static_cast<uint64_t>(N), static_cast<uint64_t>(M), 1, 2)) return SK_ECUDA;
     if (sch.partials) {
@@ -383,6 +384,13 @@ int32_t sk_gemm_debug(const void* A, const void* B, void* C, sk_dtype c_dtype, i
     if (launch_gemm(tmA, tmB, tmC, tmD, nt, a, st) != cudaSuccess) {
         cudaGetLastError();
         return SK_ECUDA;
+    }
+    if (sch.partials == 1) {
+        if (launch_reduce(a.slabs, C, a.c_bf16, sch.splits, static_cast<int64_t>(M) * N, dev_sms, st) !=
+            cudaSuccess) {
+            cudaGetLastError();
+            return SK_ECUDA;
+        }
     }
     return SK_OK;
 }

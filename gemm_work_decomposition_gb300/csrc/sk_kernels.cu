@@ -437,7 +437,8 @@ struct Epi {
         }
         if (g.role == kOwner)
             return g.peer_begin >= 0 && g.n_peers >= 1 && g.peer_begin + g.n_peers <= a.sch.n_slots;
-        if (g.role == kSlab) return g.slot >= 0 && g.slot < a.sch.splits && a.counters != nullptr;
+        if (g.role == kSlab)
+            return g.slot >= 0 && g.slot < a.sch.splits && (a.sch.partials != 2 || a.counters != nullptr);
         return true;
     }
 
@@ -559,10 +560,11 @@ struct Epi {
             uses0 ^= 1u;
         buf ^= 1;
 
-        if (g.role == kSlab) {
-            // Split-K slab: publish it and count the arrival at the tile; the split that
-            // arrives last sums the tile's slabs in split order into C (aligned split with a
-            // per-tile arrival counter, as in the docc StreamK rewrite).
+        if (g.role == kSlab && a.sch.partials == 2) {
+            // Split-K slab, last-arriver reduction: publish the slab and count the arrival
+            // at the tile; the split that arrives last sums the tile's slabs in split order
+            // into C (aligned split with a per-tile arrival counter, as in the docc StreamK
+            // rewrite). With split_partials = 1 a separate pass does that sum instead.
             if (lane == 0) {
                 bulk_wait_group_all();
                 fence_proxy_async_global();

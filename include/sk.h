@@ -63,9 +63,12 @@ typedef struct {
     int32_t splits;         /* Split-K split count s, 1 <= s <= iters (SK_SPLITK only) */
     int32_t units;          /* 0: num_sms persistent units; > 0: use this many instead */
     int32_t min_iters;      /* hybrid rule's minimum k-iterations per Stream-K unit; 0 = 8 */
-    int32_t split_partials; /* SK_SPLITK only: 1 = every split writes an FP32 slab into the
-                               workspace and the last split of each tile reduces the tile's
-                               slabs into C in split order */
+    int32_t split_partials; /* SK_SPLITK only. 0: the k = 0 split owns the tile's fixup.
+                               1: every split writes an FP32 slab P[j] into the workspace
+                               and a second launch (the sk_reduce_splits pass) sums the
+                               slabs in split order into C.
+                               2: as 1, but inside the one launch: the split that arrives
+                               last at a tile sums that tile's slabs into C */
     int32_t tile;           /* sk_tile; 0 = 128 x 128 */
 } sk_schedule;
 
@@ -107,10 +110,11 @@ typedef struct {
 /* Workspace layout: bytes [0, SK_WS_HEADER_BYTES) hold the device status word
  * (int32 at offset 0). In split-partials mode the FP32 slabs P[j][M][N] follow at
  * offset SK_WS_HEADER_BYTES, j = 0 .. splits-1, row-major, then (256-aligned) one int32
- * arrival counter per tile and CTA of the tile: the split that arrives last at a tile
- * sums that tile's slabs in split order into C, so the whole chain is one launch. In the
- * other modes one int32 flag (or counter) per slot and CTA of the tile follows
- * (256-aligned), then the partial slots of tile_m x tile_n FP32 each. */
+ * arrival counter per tile and CTA of the tile, used by split_partials = 2 (the split
+ * that arrives last at a tile sums that tile's slabs in split order into C) and kept at
+ * zero between launches. In the other modes one int32 flag (or counter) per slot and CTA
+ * of the tile follows (256-aligned), then the partial slots of tile_m x tile_n FP32
+ * each. */
 #define SK_WS_HEADER_BYTES 256
 
 /* Number of int32 values sk_plan writes for this problem, or a negative SK_E* code.

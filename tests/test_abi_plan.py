@@ -76,6 +76,7 @@ def test_plan_matches_oracle_on_workloads(sk):
     for s in (2, 4, 8, 16):
         for M in (96, 256):
             _cmp(sk, M, 512, 2048, 148, S.SPLITK, splits=s, partials=1)
+            _cmp(sk, M, 512, 2048, 148, S.SPLITK, splits=s, partials=2)
             _cmp(sk, M, 512, 2048, 148, S.SPLITK, splits=s)
     _cmp(sk, 2048, 2432, 4096, 148, S.SPLITK, splits=2)
     for m in range(128, 4097, 128):
@@ -117,7 +118,8 @@ def test_plan_min_iters(sk):
 def test_workspace_size(sk):
     for (M, N, K, sms, mode, s, part), tile in itertools.product(
             [(2048, 2432, 4096, 148, S.HYBRID, 1, 0), (128, 640, 256, 4, S.STREAMK, 1, 0),
-             (96, 512, 2048, 148, S.SPLITK, 8, 1), (2048, 2432, 4096, 148, S.SPLITK, 2, 0),
+             (96, 512, 2048, 148, S.SPLITK, 8, 1), (96, 512, 2048, 148, S.SPLITK, 8, 2),
+            (2048, 2432, 4096, 148, S.SPLITK, 2, 0),
              (2048, 2432, 4096, 148, S.DP, 1, 0)], (0, 1, 2, 3)):
         sch = sk.schedule(mode, s, 0, 0, part, tile)
         m = sk.sk_plan(M, N, K, sms, sch)
@@ -139,6 +141,7 @@ def test_errors(sk):
         (128, 128, 128, 4, sk.schedule(sk.SK_SPLITK, 3)),          # s > iters (2)
         (128, 128, 128, 4, sk.schedule(sk.SK_SPLITK, 0)),
         (128, 128, 128, 4, sk.schedule(sk.SK_STREAMK, 1, 0, 0, 1)),  # slabs need Split-K
+        (128, 128, 128, 4, sk.schedule(sk.SK_SPLITK, 2, 0, 0, 3)),   # unknown slab reduction
         (128, 128, 128, 4, sk.schedule(sk.SK_DP, 1, -1)),
         (128, 128, 128, 4, sk.schedule(sk.SK_DP, 1, 0, 0, 0, 4)),      # unknown tile shape
         (128, 128, 128, 1, sk.schedule(sk.SK_DP, 1, 0, 0, 0, 1)),      # a pair needs 2 SMs

@@ -57,6 +57,7 @@ SCHEDULES = [
     ("streamk", dict(mode=2)),
     ("hybrid", dict(mode=3)),
     ("slabs2", dict(mode=1, splits=2, split_partials=1)),
+    ("slabs2_last", dict(mode=1, splits=2, split_partials=2)),
 ]
 
 
@@ -131,13 +132,15 @@ def test_waveq_atomic_equals_deterministic_two_contributors(sk, dev):
 
 
 # --------------------------------------------------------------------------- small-M NT
+@pytest.mark.parametrize("partials", [1, 2], ids=["pass", "last"])
 @pytest.mark.parametrize("tile", [0, 1])
 @pytest.mark.parametrize("w", [synth.SMALLM_96, synth.SMALLM_256], ids=["m96", "m256"])
 @pytest.mark.parametrize("s", [2, 4, 8, 16])
-def test_smallm_split_slabs(sk, dev, dev_sms, w, s, tile):
-    # [splits, M, N] FP32 slabs then the reduction pass (split-K report, Contract): every
-    # slab against FP64 dot products over its own K range, and the reduced C.
-    sched = sk.schedule(1, splits=s, split_partials=1, tile=tile)
+def test_smallm_split_slabs(sk, dev, dev_sms, w, s, tile, partials):
+    # [splits, M, N] FP32 slabs then their sum (split-K report, Contract): every slab
+    # against FP64 dot products over its own K range, and the reduced C. partials = 1
+    # reduces in a second pass, 2 in the last split to arrive at each tile.
+    sched = sk.schedule(1, splits=s, split_partials=partials, tile=tile)
     got, (ws, _) = _run(sk, dev, w, sched, DET, dev_sms)
     A_bits, B_bits = U.inputs(w)
     P_ref = og.ref_split_partials(A_bits, B_bits, "NT", s)
@@ -155,6 +158,9 @@ def test_smallm_split_slabs(sk, dev, dev_sms, w, s, tile):
     for j in range(1, s):
         fold = fold + P[j].astype(np.float32)
     assert np.array_equal(got, fold.astype(np.float64))
+    # The per-tile arrival counters after the slabs are back at zero for the next launch.
+    off = -(-(sk.SK_WS_HEADER_BYTES + 4 * s * w.M * w.N) // 256) * 256
+    assert not torch.any(ws[off:] != 0)
 
 
 @pytest.mark.parametrize("tile", TILES)
