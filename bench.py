@@ -40,10 +40,10 @@ WORKLOADS = {"waveq": synth.WAVEQ, "skinny": synth.SKINNY, "large": synth.LARGE,
 # from one ncu capture, keyed by workload/schedule; valid only for the kernel source it
 # was taken on (sha256 of sk_kernels.cu, first 16 hex digits).
 TRAFFIC = {
-    "waveq_2048x2432x4096/hybrid/tile2@148": {"bytes": 36772608 + 1757440, "kernel_sha": "ff6e724716bc24a7",
+    "waveq_2048x2432x4096/hybrid/tile2@148": {"bytes": 36783872 + 1778176, "kernel_sha": "c9541a39e3c22e75",
                                               "profile": "profiles/sk_gemm_kernel_waveq_2048x2432x4096_pair256_hybrid148.md"},
-    "waveq_2048x2432x4096/hybrid/tile0@148": {"bytes": 36744704 + 168960, "kernel_sha": "f3a64766608abaf7",
-                                        "profile": "profiles/sk_gemm_kernel_waveq_2048x2432x4096_tile128_hybrid148.md"},
+    "waveq_2048x2432x4096/hybrid/tile0@148": {"bytes": 36777728 + 130560, "kernel_sha": "c9541a39e3c22e75",
+                                              "profile": "profiles/sk_gemm_kernel_waveq_2048x2432x4096_tile128_hybrid148.md"},
 }
 
 
