@@ -432,7 +432,11 @@ def main():
                 sk.sk_gemm_debug(A, B, C, out_code, w.M, w.N, w.K, lay, s3, red, nsms, ws3, nb3, stream, trace=tr)
                 torch.cuda.synchronize(dev)
                 T = tr.cpu().numpy().reshape(ncta, sk.SK_TRACE_WORDS).astype(np.int64)
-                end = (T[:, 1] - T[:, 0].min()) / 1e3
+                # A CTA ends no earlier than any stamp it wrote: the compiler may schedule a
+                # %globaltimer read ahead of the exit barrier, so the exit stamp alone can read early.
+                nseg = np.minimum(T[:, 2], sk.SK_TRACE_SEGS).astype(np.int64)
+                last = np.array([T[c, 4:4 + 4 * nseg[c]].max(initial=0) for c in range(ncta)])
+                end = (np.maximum(T[:, 1], last) - T[:, 0].min()) / 1e3
                 # SMs without a CTA idle for the whole span
                 vals.append((float(np.sum(end.max() - end)) + (dev_sms - ncta) * float(end.max()), float(end.max())))
             assert sk.sk_status(ws3, stream) == sk.SK_OK

@@ -240,9 +240,9 @@ __device__ __forceinline__ bool wait_flag(const int32_t* f, int32_t target, uint
 }
 
 // Partial-slot layout: a CTA's share of a slot (128 rows x kBN columns FP32) is split into
-// one contiguous block per epilogue warp (its 32 rows x kCols columns, block index
-// chalf * 4 + quad); inside a block, element (lane, column 32c + 4q + e) sits at float4
-// index (c * 8 + q) * 32 + lane, so each warp access covers 512 contiguous bytes.
+// one contiguous block per TMEM lane quadrant (its 32 rows x kBN columns, block index quad);
+// inside a block, element (lane, column 32c + 4q + e) sits at float4 index
+// (c * 8 + q) * 32 + lane, so each warp access covers 512 contiguous bytes.
 __device__ __forceinline__ int slot_f4(int c, int q, int lane) { return ((c * 8 + q) * 32 + lane) * 4; }
 
 // Store kCols columns of this warp's 32 rows (one row per lane, in registers) through the
@@ -251,16 +251,16 @@ __device__ __forceinline__ int slot_f4(int c, int q, int lane) { return ((c * 8 
 // layout (16-byte chunk j of row r at chunk j ^ (r % 8)), so the shared stores are
 // conflict-free and the TMA clips the box at M and N. `slab` < 0 stores to C.
 // One 32-row x 128-byte box of this warp's rows (8 chunks of 16 bytes per row, given as
-// 32-bit words w[j][0..3]) through staging buffer nstore & 1, stored by the TMA at (x, y0)
-// (or (x, y0, slab)).
+// 32-bit words w[j][0..3]) through staging buffer nstore % kBoxes, stored by the TMA at
+// (x, y0) (or (x, y0, slab)).
 template <class F>
 __device__ __forceinline__ void store_box(const CUtensorMap* tmC, uint32_t staging, uint32_t& nstore, int32_t x,
                                           int32_t y0, int32_t slab, F&& words) {
     const int lane = threadIdx.x & 31;
-    const uint32_t buf = staging + (nstore & 1u) * 4096u;
-    if (nstore >= 2) {
-        // The store issued two boxes ago used this buffer: wait until the TMA read it.
-        if (lane == 0) bulk_wait_group_read<1>();
+    const uint32_t buf = staging + (kBoxes == 1 ? 0u : (nstore & 1u) * 4096u);
+    if (nstore >= static_cast<uint32_t>(kBoxes)) {
+        // The store issued kBoxes boxes ago used this buffer: wait until the TMA read it.
+        if (lane == 0) bulk_wait_group_read<kBoxes - 1>();
         __syncwarp();
     }
     const uint32_t row = buf + static_cast<uint32_t>(lane) * 128u;
@@ -283,7 +283,7 @@ __device__ __forceinline__ void store_box(const CUtensorMap* tmC, uint32_t stagi
 }
 
 // Store kCols columns of this warp's 32 rows (one row per lane, in registers) with TMA
-// tensor stores through the warp's two 4 KiB staging boxes: BF16 C in boxes of 64 columns,
+// tensor stores through the warp's 4 KiB staging boxes: BF16 C in boxes of 64 columns,
 // FP32 C or slab in boxes of 32 columns, each box 32 rows x 128 bytes in the 128-byte
 // swizzled layout (16-byte chunk j of row r at chunk j ^ (r % 8)), so the shared stores are
 // conflict-free and the TMA clips the box at M and N. `slab` < 0 stores to C.
@@ -361,10 +361,15 @@ __device__ __forceinline__ void dump_row(float* d, const uint32_t (&t)[kN], int 
                         __uint_as_float(t[o + 4 * q + 2]), __uint_as_float(t[o + 4 * q + 3]));
 }
 
-// Per-CTA epilogue state shared by the segments of one unit.
-template <int kCG, int kBN>
+// Epilogue state of one group of four warps (128 threads, one TMEM lane quadrant each), shared
+// by the segments of one unit that the group takes.
+template <int kCG, int kBN, int kGroup>
 struct Epi {
     using S = Shape<kCG, kBN>;
+    // The group's named barrier (barrier 2 is the TMEM hand-off), and, with two groups, the
+    // accumulator every segment of this group uses.
+    static constexpr uint32_t kBar = kGroup == 0 ? 1u : 3u;
+    static constexpr bool kFixedBuf = kEpiGroups == 2;
     const KArgs& a;
     const CUtensorMap* tmC;
     const CUtensorMap* tmD;
@@ -372,14 +377,14 @@ struct Epi {
     uint32_t tmem_base;
     uint64_t deadline;
     volatile int* abort_flag;
-    int lane, et, quad, chalf, row;
+    int lane, gt, quad, row;     // gt: thread index within the group
     int32_t r;
     uint32_t tcol, staging, nstore;
     uint32_t tempty0, tempty1;   // accumulator-empty barriers (in the leader CTA)
     int64_t blk_off;
-    int buf;                     // accumulator in use (0 or 1) and its phase parities
+    int buf;                     // accumulator of the next segment (one group), and the phase parities
     uint32_t uses0, uses1;
-    volatile int* last_flag;     // shared word: this CTA took a tile's last slab
+    volatile int* last_flag;     // shared word: this group took a tile's last slab
 
     __device__ __forceinline__ float* block(int32_t slot) const {
         return a.slots + static_cast<int64_t>(slot * kCG + r) * S::kCtaSlotFloats + blk_off;
@@ -389,7 +394,7 @@ struct Epi {
     // + P[splits-1], summed left to right in FP32.
     __device__ __forceinline__ void reduce_slabs(const Seg& g) {
         const int32_t m0 = (g.tile / a.sch.tiles_n) * (kCtaRows * kCG) + r * kCtaRows;
-        const int32_t n0 = (g.tile % a.sch.tiles_n) * kBN + chalf * S::kCols;
+        const int32_t n0 = (g.tile % a.sch.tiles_n) * kBN;
         const int32_t gr = m0 + row;
         const int64_t slab = static_cast<int64_t>(a.M) * a.N;
 #pragma unroll 1
@@ -463,7 +468,7 @@ struct Epi {
                 for (int32_t pi = 0; pi < g.n_peers && ok; ++pi)
                     ok = wait_flag(a.flags + (g.peer_begin + pi) * kCG + r, 1, deadline, abort_flag);
             }
-            if (named_bar_or(1, kEpiThreads, !ok)) {
+            if (named_bar_or(kBar, kGroupThreads, !ok)) {
                 record_timeout(a, abort_flag);
                 return false;
             }
@@ -472,8 +477,9 @@ struct Epi {
             else
                 load_partial<false, false>(v, block(g.peer_begin), 0, lane);
         }
-        const bool got = mbar_wait(sm.tfull(buf), buf ? uses1 : uses0, abort_flag, deadline);
-        if (named_bar_or(1, kEpiThreads, !got || *abort_flag != 0)) {
+        const int b = kFixedBuf ? kGroup : buf;
+        const bool got = mbar_wait(sm.tfull(b), b ? uses1 : uses0, abort_flag, deadline);
+        if (named_bar_or(kBar, kGroupThreads, !got || *abort_flag != 0)) {
             if (!got) record_timeout(a, abort_flag);
             return false;
         }
@@ -481,11 +487,11 @@ struct Epi {
         if (tr && seg < kTraceSegs) tr[4 + 4 * seg + 2] = globaltimer();
 
         const int32_t m0 = (g.tile / a.sch.tiles_n) * (kCtaRows * kCG) + r * kCtaRows;
-        const int32_t n0 = (g.tile % a.sch.tiles_n) * kBN + chalf * S::kCols;
+        const int32_t n0 = (g.tile % a.sch.tiles_n) * kBN;
         const int32_t wy = m0 + quad * 32;  // first row of this warp's 32
         float* dump = a.dump ? a.dump +
                                    (static_cast<int64_t>(g.tile) * a.sch.iters + g.k_begin) * (kCtaRows * kCG * kBN) +
-                                   static_cast<int64_t>(r * kCtaRows + row) * kBN + chalf * S::kCols
+                                   static_cast<int64_t>(r * kCtaRows + row) * kBN
                              : nullptr;
 
 #pragma unroll 1
@@ -499,7 +505,7 @@ struct Epi {
             // This pass of the segment's own accumulator: one TMEM load for the whole pass,
             // or for an owner 64 columns at a time added to the first partial (own + P1: the
             // first step of the k-order fold).
-            const uint32_t taddr = tmem_base + tcol + static_cast<uint32_t>(buf * kBN + p * kPassCols);
+            const uint32_t taddr = tmem_base + tcol + static_cast<uint32_t>(b * kBN + p * kPassCols);
             if (kOwner) {
 #pragma unroll
                 for (int h = 0; h < kPassCols / 64; ++h) {
@@ -523,9 +529,9 @@ struct Epi {
                 // The whole accumulator has been read: hand it back to the MMA issuer.
                 tc_fence_before();
                 if (kCG == 1)
-                    mbar_arrive(buf ? tempty1 : tempty0);
+                    mbar_arrive(b ? tempty1 : tempty0);
                 else
-                    mbar_arrive_cluster(buf ? tempty1 : tempty0);
+                    mbar_arrive_cluster(b ? tempty1 : tempty0);
             }
 
             if (kOwner) {
@@ -554,11 +560,11 @@ struct Epi {
                 store_slice<kPassCols>(a, tmC, staging, nstore, v, n0 + p * kPassCols, wy, -1);
             }
         }
-        if (buf)
+        if (b)
             uses1 ^= 1u;
         else
             uses0 ^= 1u;
-        buf ^= 1;
+        if (!kFixedBuf) buf ^= 1;
 
         if (g.role == kSlab && a.sch.partials == 2) {
             // Split-K slab, last-arriver reduction: publish the slab and count the arrival
@@ -570,22 +576,22 @@ struct Epi {
                 fence_proxy_async_global();
             }
             __syncwarp();
-            named_bar_sync(1, kEpiThreads);
-            if (et == 0)
+            named_bar_sync(kBar, kGroupThreads);
+            if (gt == 0)
                 *last_flag = atom_add_acq_rel_gpu(a.counters + g.tile * kCG + r, 1) ==
                              static_cast<uint32_t>(a.sch.splits - 1);
-            named_bar_sync(1, kEpiThreads);
+            named_bar_sync(kBar, kGroupThreads);
             if (*last_flag) {
                 (void)ld_acquire_gpu(a.counters + g.tile * kCG + r);
                 reduce_slabs(g);
-                named_bar_sync(1, kEpiThreads);
-                if (et == 0) a.counters[g.tile * kCG + r] = 0;
+                named_bar_sync(kBar, kGroupThreads);
+                if (gt == 0) a.counters[g.tile * kCG + r] = 0;
             }
         } else if (g.role == kProducer) {
             // Every epilogue thread's share is stored: publish it. The barrier orders all of
             // them before one thread's release at GPU scope (release is cumulative).
-            named_bar_sync(1, kEpiThreads);
-            if (et == 0 && !a.skip_signal) {
+            named_bar_sync(kBar, kGroupThreads);
+            if (gt == 0 && !a.skip_signal) {
                 if (a.atomic)
                     red_release_add_gpu(a.flags + g.peer_begin * kCG + r, 1);
                 else
@@ -593,8 +599,8 @@ struct Epi {
             }
         } else if (kOwner) {
             // Every epilogue thread has read the partials: re-arm the flags / counter.
-            named_bar_sync(1, kEpiThreads);
-            if (et == 0) {
+            named_bar_sync(kBar, kGroupThreads);
+            if (gt == 0) {
                 if (a.atomic) {
                     a.flags[g.peer_begin * kCG + r] = 0;
                 } else {
@@ -606,44 +612,58 @@ struct Epi {
     }
 };
 
-template <int kCG, int kBN>
-__device__ void run_epilogue(const KArgs& a, const CUtensorMap* tmC, const CUtensorMap* tmD,
-                             const Smem<Shape<kCG, kBN>>& sm, uint32_t tmem_base, int unit, uint32_t rank,
-                             uint64_t deadline, volatile int* abort_flag, volatile int* last_flag) {
+template <int kCG, int kBN, int kGroup>
+__device__ void run_epilogue_group(const KArgs& a, const CUtensorMap* tmC, const CUtensorMap* tmD,
+                                   const Smem<Shape<kCG, kBN>>& sm, uint32_t tmem_base, int unit, uint32_t rank,
+                                   uint64_t deadline, volatile int* abort_flag, volatile int* last_flag) {
     using S = Shape<kCG, kBN>;
     const int warp = threadIdx.x >> 5;
-    Epi<kCG, kBN> e{a, tmC, tmD, sm, tmem_base, deadline, abort_flag};
-    e.last_flag = last_flag;
+    const int ew = warp - 2;                  // index among the epilogue warps
+    Epi<kCG, kBN, kGroup> e{a, tmC, tmD, sm, tmem_base, deadline, abort_flag};
+    e.last_flag = last_flag + kGroup;
     e.lane = threadIdx.x & 31;
-    e.et = threadIdx.x - 64;                  // index among the epilogue threads
+    e.gt = (ew & 3) * 32 + e.lane;            // index within the group
     e.quad = warp & 3;                        // TMEM lanes this warp may read: 32*quad ..
-    e.chalf = (warp - 2) >> 2;                // which part of the tile's columns (0 with 4 warps)
     e.row = e.quad * 32 + e.lane;             // row of this CTA's part of the tile
     e.r = static_cast<int32_t>(rank);
-    e.tcol = static_cast<uint32_t>(e.quad * 32) << 16 | static_cast<uint32_t>(e.chalf * S::kCols);
-    e.staging = sm.base + S::kStagingOff + static_cast<uint32_t>(warp - 2) * 8192u;
+    e.tcol = static_cast<uint32_t>(e.quad * 32) << 16;
+    e.staging = sm.base + S::kStagingOff + static_cast<uint32_t>(ew * kBoxes) * 4096u;
     e.nstore = 0;
     // The accumulator-empty barriers live in the leader CTA.
     e.tempty0 = kCG == 1 ? sm.tempty(0) : mapa_shared(sm.tempty(0), 0);
     e.tempty1 = kCG == 1 ? sm.tempty(1) : mapa_shared(sm.tempty(1), 0);
-    e.blk_off = static_cast<int64_t>(e.chalf * 4 + e.quad) * S::kWarpSlotFloats;
+    e.blk_off = static_cast<int64_t>(e.quad) * S::kWarpSlotFloats;
     e.buf = 0;
     e.uses0 = e.uses1 = 0u;
-    uint64_t* tr = (a.trace && e.et == 0) ? a.trace + static_cast<int64_t>(blockIdx.x) * kTraceWords : nullptr;
+    uint64_t* tr = (a.trace && e.gt == 0) ? a.trace + static_cast<int64_t>(blockIdx.x) * kTraceWords : nullptr;
     Walk w;
     w.init(a.sch, unit);
     Seg g;
-    int seg = 0;
+    int seg = 0;  // the unit's segment index; the MMA issuer puts segment i in accumulator i % 2
     while (w.next(a.sch, g)) {
-        const bool ok = g.role == kOwner ? e.template segment<true>(g, tr, seg) : e.template segment<false>(g, tr, seg);
-        if (!ok) break;
-        if (tr && seg < kTraceSegs) tr[4 + 4 * seg + 3] = globaltimer();
+        if (seg % kEpiGroups == kGroup) {
+            const bool ok =
+                g.role == kOwner ? e.template segment<true>(g, tr, seg) : e.template segment<false>(g, tr, seg);
+            if (!ok) break;
+            if (tr && seg < kTraceSegs) tr[4 + 4 * seg + 3] = globaltimer();
+        }
         ++seg;
     }
     // Every TMA store of this warp has written C before the CTA may exit.
     if (e.lane == 0) bulk_wait_group_all();
     __syncwarp();
-    if (tr) tr[2] = static_cast<uint64_t>(seg);
+    if (tr && kGroup == 0) tr[2] = static_cast<uint64_t>(seg);
+}
+
+// Epilogue warps: group 0 (warps 2-5) and, with two groups, group 1 (warps 6-9).
+template <int kCG, int kBN>
+__device__ void run_epilogue(const KArgs& a, const CUtensorMap* tmC, const CUtensorMap* tmD,
+                             const Smem<Shape<kCG, kBN>>& sm, uint32_t tmem_base, int unit, uint32_t rank,
+                             uint64_t deadline, volatile int* abort_flag, volatile int* last_flag) {
+    if (kEpiGroups == 1 || (threadIdx.x >> 5) < 6)
+        run_epilogue_group<kCG, kBN, 0>(a, tmC, tmD, sm, tmem_base, unit, rank, deadline, abort_flag, last_flag);
+    else
+        run_epilogue_group<kCG, kBN, 1>(a, tmC, tmD, sm, tmem_base, unit, rank, deadline, abort_flag, last_flag);
 }
 
 // --------------------------------------------------------------------------- kernel
@@ -658,7 +678,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     Smem<S> sm{smem_u32(smem)};
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + S::kSmemBarOff + 192);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + S::kSmemBarOff + 196);
-    volatile int* last_flag = reinterpret_cast<volatile int*>(smem + S::kSmemBarOff + 200);
+    volatile int* last_flag = reinterpret_cast<volatile int*>(smem + S::kSmemBarOff + 200);  // one per group
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -675,7 +695,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(sm.tfull(b), 1);
-            mbar_init(sm.tempty(b), kEpiThreads * kCG);
+            mbar_init(sm.tempty(b), kGroupThreads * kCG);  // one group reads each accumulator
         }
         mbar_init(sm.done(), 1);
         mbar_init(sm.tready(), 1);

@@ -9,15 +9,22 @@
 
 namespace sk {
 
-#ifndef SK_EPI_WARPS
-#define SK_EPI_WARPS 4
+#ifndef SK_EPI_GROUPS
+#define SK_EPI_GROUPS 1
 #endif
-constexpr int kEpiWarps = SK_EPI_WARPS;  // one per TMEM lane quadrant (4) or two on half the columns (8)
+// Epilogue groups of four warps, one warp per TMEM lane quadrant. With two groups, group g
+// takes the segments whose accumulator is buffer g, so a segment's stores or fixup never
+// queue behind the previous segment's; with one, the group takes every segment in turn.
+constexpr int kEpiGroups = SK_EPI_GROUPS;
+static_assert(kEpiGroups == 1 || kEpiGroups == 2, "one or two epilogue groups");
+constexpr int kEpiWarps = 4 * kEpiGroups;
 constexpr int kThreads = 64 + 32 * kEpiWarps;   // warp 0 TMA, warp 1 MMA, then the epilogue warps
 constexpr int kEpiThreads = 32 * kEpiWarps;
-constexpr int kPassCols = kEpiWarps == 4 ? 128 : 64;  // accumulator columns a thread holds at once
+constexpr int kGroupThreads = 128;
+constexpr int kPassCols = kEpiGroups == 1 ? 128 : 64;  // accumulator columns a thread holds at once
+constexpr int kBoxes = 2 / kEpiGroups;          // 4 KiB staging boxes per epilogue warp
 constexpr int kCtaRows = 128;     // rows of a work tile held by one CTA (its TMEM lanes)
-constexpr int kRingBytes = kEpiWarps == 4 ? 196608 : 163840;
+constexpr int kRingBytes = 196608;
 constexpr int kTraceSegs = 15;                  // SK_TRACE_SEGS
 constexpr int kTraceWords = 4 + 4 * kTraceSegs; // SK_TRACE_WORDS
 
@@ -30,17 +37,16 @@ struct Shape {
     static constexpr int kBBytes = kBNc * kBlkK * 2;       // 8 / 16 / 32 KiB of B per stage
     static constexpr int kStageBytes = kABytes + kBBytes;
     static constexpr int kStages = (kRingBytes / kStageBytes) > 8 ? 8 : (kRingBytes / kStageBytes);
-    // Epilogue staging after the ring: per epilogue warp two 4 KiB boxes (32 rows x 128 B)
+    // Epilogue staging after the ring: per epilogue warp kBoxes 4 KiB boxes (32 rows x 128 B)
     // that the TMA stores to C; then the barrier block and 1 KiB of alignment.
     static constexpr int kStagingOff = kStages * kStageBytes;
-    static constexpr int kStagingBytes = kEpiWarps * 2 * 4096;
+    static constexpr int kStagingBytes = kEpiWarps * kBoxes * 4096;
     static constexpr int kSmemBarOff = kStagingOff + kStagingBytes;
     static constexpr int kSmemBytes = kSmemBarOff + 256 + 1024;
     static constexpr int kTmemCols = 2 * kBN;               // two accumulators of kBN columns
     static constexpr int kTxBytes = kCG * kStageBytes;      // bytes landing on the leader per stage
-    static constexpr int kCols = kBN * 4 / kEpiWarps;       // accumulator columns per epilogue thread
-    static constexpr int kPasses = kCols / kPassCols;       // processed kPassCols at a time
-    static constexpr int kWarpSlotFloats = 32 * kCols;      // one epilogue warp's block of a partial
+    static constexpr int kPasses = kBN / kPassCols;         // a thread's row, kPassCols at a time
+    static constexpr int kWarpSlotFloats = 32 * kBN;        // one epilogue warp's block of a partial
     static constexpr int kCtaSlotFloats = kCtaRows * kBN;   // a CTA's share of one partial slot
     static_assert(kBNc % 64 == 0 && kBN % 128 == 0, "tile shape");
 };
