@@ -249,6 +249,7 @@ def run_smallm(sk, torch, dev, flush, stream, dev_sms):
         cases = [(f"slabs_s{s}", sk.schedule(sk.SK_SPLITK, s, split_partials=1), dev_sms) for s in (2, 4, 8, 16)]
         cases += [(f"slabs_last_s{s}", sk.schedule(sk.SK_SPLITK, s, split_partials=2), dev_sms) for s in (2, 4, 8, 16)]
         cases += [("splitk8_fixup", sk.schedule(sk.SK_SPLITK, 8), dev_sms), ("streamk", sk.schedule(sk.SK_STREAMK), dev_sms),
+                  ("streamk_pass", sk.schedule(sk.SK_STREAMK, split_partials=1), dev_sms),
                   ("hybrid", sk.schedule(sk.SK_HYBRID), dev_sms)]
         for name, sch, nsms in cases:
             nb = sk.sk_workspace_size(w.M, w.N, w.K, nsms, sch, 0)
@@ -276,8 +277,47 @@ def run_smallm(sk, torch, dev, flush, stream, dev_sms):
             torch.cuda.synchronize(dev)
             pack8 = float(np.median([a0.elapsed_time(a1) for a0, a1 in packs])) * 1e3 / 8
             assert sk.sk_status(ws, stream) == sk.SK_OK
-            launches = 2 if name.startswith("slabs_s") else 1
+            launches = 2 if (name.startswith("slabs_s") or name.endswith("_pass")) else 1
             rows[name] = {"us": one, "us_pack8": pack8, "launches": launches, "tflops": fl / (one / 1e6) / 1e12}
+        out[w.name] = rows
+    return out
+
+
+def run_fixups(sk, torch, dev, flush, stream):
+    """Stream-K fixups compared on the skinny shape 512 x 512 x 65536 (many contributors per
+    tile) and on the wave-quantized shape: the owner waits and sums in k order, FP32
+    atomics, and the separate fixup pass (every partial to its slot, then a second
+    launch sums each tile in k order). 128 x 128 and 256 x 256 pair tiles, 148 SMs."""
+    out = {}
+    for w, mode in ((synth.SKINNY, sk.SK_STREAMK), (synth.WAVEQ, sk.SK_HYBRID)):
+        A_bits, B_bits = synth.make_inputs(w)
+        A = torch.from_numpy(A_bits.view(np.int16)).view(torch.bfloat16).to(dev)
+        B = torch.from_numpy(B_bits.view(np.int16)).view(torch.bfloat16).to(dev)
+        C = torch.empty((w.M, w.N), dtype=torch.bfloat16, device=dev)
+        fl = 2.0 * w.M * w.N * w.K
+        rows = {}
+        for tile, tname in ((0, "128x128"), (2, "pair256x256")):
+            plan = sk.sk_plan(w.M, w.N, w.K, 148, sk.schedule(mode, tile=tile))
+            contrib = plan[-2 * int(plan[2]) + 1::2]
+            for name, part, red in (("owner", 0, sk.SK_DETERMINISTIC), ("atomic", 0, sk.SK_ATOMIC),
+                                    ("pass", 1, sk.SK_DETERMINISTIC)):
+                sch = sk.schedule(mode, split_partials=part, tile=tile)
+                nb = sk.sk_workspace_size(w.M, w.N, w.K, 148, sch, red)
+                ws = torch.zeros(nb, dtype=torch.uint8, device=dev)
+                g = lambda: sk.sk_gemm(A, B, C, sk.SK_BF16, w.M, w.N, w.K, sk.SK_NN, sch, red, 148, ws, nb, stream)
+                for _ in range(5):
+                    g()
+                ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(40)]
+                for a0, a1 in ev:
+                    flush.zero_()
+                    a0.record(stream)
+                    g()
+                    a1.record(stream)
+                torch.cuda.synchronize(dev)
+                assert sk.sk_status(ws, stream) == sk.SK_OK
+                us = float(np.median([a0.elapsed_time(a1) for a0, a1 in ev])) * 1e3
+                rows[f"{tname}/{name}"] = {"us": us, "tflops": fl / (us / 1e6) / 1e12, "launches": 2 if part else 1,
+                                           "max_contributors_per_tile": int(max(contrib))}
         out[w.name] = rows
     return out
 
@@ -481,6 +521,7 @@ def main():
                                             f"({cpu_s:.1f} s, numpy matmul, default BLAS threads)"}
 
         extras["smallm_nt"] = run_smallm(sk, torch, dev, flush, stream, dev_sms)
+        extras["fixups"] = run_fixups(sk, torch, dev, flush, stream)
 
         if args.sweep:
             run_sweep(sk, torch, dev, args.sweep, red, flush, stream, peak_tf, dev_sms)

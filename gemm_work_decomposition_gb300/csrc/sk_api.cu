@@ -51,21 +51,25 @@ void heuristic(int64_t tiles, int64_t iters, int64_t sms, int64_t min_iters, int
     }
 }
 
-void set_streamk(Sched& o, int64_t base, int64_t sk_tiles, int64_t units) {
+void set_streamk(Sched& o, int64_t base, int64_t sk_tiles, int64_t units, bool sep) {
     const int64_t total = sk_tiles * o.iters;
     o.sk_base = static_cast<int32_t>(base);
     o.sk_tiles = static_cast<int32_t>(sk_tiles);
     o.sk_units = static_cast<int32_t>(units);
     o.sk_q = static_cast<int32_t>(total / units);
     o.sk_big = static_cast<int32_t>(total % units);
-    o.n_slots = static_cast<int32_t>(units);
+    o.sep = sep ? 1 : 0;
+    o.n_slots = static_cast<int32_t>((sep ? 2 : 1) * units);
 }
 
 int32_t make_sched(int32_t M, int32_t N, int32_t K, int32_t num_sms, const sk_schedule& s, Sched& o) {
     if (M < 1 || N < 1 || K < 1 || num_sms < 1 || s.units < 0 || s.min_iters < 0) return SK_EINVAL;
     if (s.mode < SK_DP || s.mode > SK_HYBRID) return SK_EINVAL;
+    // split_partials: Split-K slabs (1 pass, 2 last arriver), or for Stream-K and the hybrid
+    // rule (1) the separate fixup pass; data-parallel tiles have no partials.
     if (s.split_partials < 0 || s.split_partials > 2) return SK_EINVAL;
-    if (s.split_partials != 0 && s.mode != SK_SPLITK) return SK_EINVAL;
+    if (s.split_partials == 2 && s.mode != SK_SPLITK) return SK_EINVAL;
+    if (s.split_partials != 0 && s.mode == SK_DP) return SK_EINVAL;
     int32_t tm = 0, tn = 0, cg = 0;
     if (!tile_shape(s.tile, &tm, &tn, &cg)) return SK_EINVAL;
     const int64_t tiles_n = (static_cast<int64_t>(N) + tn - 1) / tn;
@@ -97,7 +101,7 @@ int32_t make_sched(int32_t M, int32_t N, int32_t K, int32_t num_sms, const sk_sc
         } else {
             const int64_t dp_tiles = tiles - skt;
             o.mode = kHybrid;
-            set_streamk(o, dp_tiles, skt, sku);
+            set_streamk(o, dp_tiles, skt, sku, s.split_partials == 1);
             o.dp_tiles = static_cast<int32_t>(dp_tiles);
             const int64_t dpw = dp_tiles < S ? dp_tiles : S;
             o.workers = static_cast<int32_t>(sku > dpw ? sku : dpw);
@@ -112,7 +116,7 @@ int32_t make_sched(int32_t M, int32_t N, int32_t K, int32_t num_sms, const sk_sc
         const int64_t total = tiles * iters;
         const int64_t U = total < S ? total : S;
         o.mode = kStreamK;
-        set_streamk(o, 0, tiles, U);
+        set_streamk(o, 0, tiles, U, s.split_partials == 1);
         o.workers = static_cast<int32_t>(U);
     } else {  // SK_SPLITK
         if (s.splits < 1 || s.splits > iters) return SK_EINVAL;
@@ -388,6 +392,12 @@ int32_t sk_gemm_debug(const void* A, const void* B, void* C, sk_dtype c_dtype, i
     if (sch.partials == 1) {
         if (launch_reduce(a.slabs, C, a.c_bf16, sch.splits, static_cast<int64_t>(M) * N, dev_sms, st) !=
             cudaSuccess) {
+            cudaGetLastError();
+            return SK_ECUDA;
+        }
+    }
+    if (sch.sep) {
+        if (launch_fixup(sch, a.slots, C, M, N, a.c_bf16, dev_sms, st) != cudaSuccess) {
             cudaGetLastError();
             return SK_ECUDA;
         }

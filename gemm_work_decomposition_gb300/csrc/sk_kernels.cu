@@ -292,6 +292,10 @@ __device__ __forceinline__ void store_slice(const KArgs& a, const CUtensorMap* t
                                             uint32_t& nstore, const float (&v)[kCols], int32_t x0, int32_t y0,
                                             int32_t slab) {
     if (y0 >= a.M) return;  // the warp's 32 rows lie below C
+    if (x0 < 0 || y0 < 0) {  // never reached by a valid plan: record it and skip the stores
+        atomicCAS(a.status, 0, kErrBounds);
+        return;
+    }
     if (a.c_bf16 && slab < 0) {
 #pragma unroll
         for (int b = 0; b < kCols / 64; ++b) {
@@ -437,9 +441,10 @@ struct Epi {
     __device__ __forceinline__ bool in_bounds(const Seg& g) const {
         if (g.tile < 0 || g.tile >= a.sch.tiles) return false;
         if (g.role == kProducer) {
-            const int32_t s = a.atomic ? g.peer_begin : g.slot;
+            const int32_t s = (a.atomic && !a.sch.sep) ? g.peer_begin : g.slot;
             return s >= 0 && s < a.sch.n_slots;
         }
+        if (g.role == kOwner && a.sch.sep) return g.slot >= 0 && g.slot < a.sch.n_slots;
         if (g.role == kOwner)
             return g.peer_begin >= 0 && g.n_peers >= 1 && g.peer_begin + g.n_peers <= a.sch.n_slots;
         if (g.role == kSlab)
@@ -447,8 +452,10 @@ struct Epi {
         return true;
     }
 
-    // One segment. Returns false when a wait gave up or a check failed (the caller stops).
-    template <bool kOwner>
+    // One segment. kFixup: this segment is a split tile's owner and sums its peers' partials
+    // here (without the separate fixup pass). Returns false when a wait gave up or a check
+    // failed (the caller stops).
+    template <bool kFixup>
     __device__ __forceinline__ bool segment(const Seg& g, uint64_t* tr, int seg) {
         constexpr int kChunks = kPassCols / 32;  // TMEM loads per pass
         if (!in_bounds(g)) {  // same answer in every epilogue thread
@@ -457,7 +464,7 @@ struct Epi {
             return false;
         }
         float v[kPassCols];
-        if (kOwner) {
+        if (kFixup) {
             // Wait for every peer (this CTA's share of the partials), then fetch the first pass
             // of the first partial (or of the atomic sum) while this segment's MAC loop is
             // still running.
@@ -496,7 +503,7 @@ struct Epi {
 
 #pragma unroll 1
         for (int p = 0; p < S::kPasses; ++p) {
-            if (kOwner && p > 0) {
+            if (kFixup && p > 0) {
                 if (a.atomic)
                     load_partial<false, true>(v, block(g.peer_begin), kChunks * p, lane);
                 else
@@ -506,7 +513,7 @@ struct Epi {
             // or for an owner 64 columns at a time added to the first partial (own + P1: the
             // first step of the k-order fold).
             const uint32_t taddr = tmem_base + tcol + static_cast<uint32_t>(b * kBN + p * kPassCols);
-            if (kOwner) {
+            if (kFixup) {
 #pragma unroll
                 for (int h = 0; h < kPassCols / 64; ++h) {
                     uint32_t t[64];
@@ -534,22 +541,25 @@ struct Epi {
                     mbar_arrive_cluster(b ? tempty1 : tempty0);
             }
 
-            if (kOwner) {
+            if (kFixup) {
                 // Turnstile: the remaining peers' partials, in k order.
                 if (!a.atomic) {
                     for (int32_t pi = 1; pi < g.n_peers; ++pi)
                         load_partial<true, false>(v, block(g.peer_begin + pi), kChunks * p, lane);
                 }
                 store_slice<kPassCols>(a, tmC, staging, nstore, v, n0 + p * kPassCols, wy, -1);
-            } else if (g.role == kProducer) {
-                float* blk = block(a.atomic ? g.peer_begin : g.slot);
+            } else if (g.role == kProducer || g.role == sk::kOwner) {
+                // A producer's partial; with the separate fixup pass, an owner's too. The
+                // pass sums them in k order, so the reduction mode does not apply there.
+                const bool atomic = a.atomic && !a.sch.sep;
+                float* blk = block(atomic ? g.peer_begin : g.slot);
 #pragma unroll
                 for (int c = 0; c < kChunks; ++c)
 #pragma unroll
                     for (int q = 0; q < 8; ++q) {
                         const int i = c * 32 + q * 4;
                         float* dst = blk + slot_f4(kChunks * p + c, q, lane);
-                        if (a.atomic)
+                        if (atomic)
                             red_add_v4_f32(dst, v[i], v[i + 1], v[i + 2], v[i + 3]);
                         else
                             st_cg_f4(dst, make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]));
@@ -587,9 +597,10 @@ struct Epi {
                 named_bar_sync(kBar, kGroupThreads);
                 if (gt == 0) a.counters[g.tile * kCG + r] = 0;
             }
-        } else if (g.role == kProducer) {
+        } else if (g.role == kProducer && !a.sch.sep) {
             // Every epilogue thread's share is stored: publish it. The barrier orders all of
-            // them before one thread's release at GPU scope (release is cumulative).
+            // them before one thread's release at GPU scope (release is cumulative). With
+            // the separate fixup pass nobody waits: the pass runs after this launch.
             named_bar_sync(kBar, kGroupThreads);
             if (gt == 0 && !a.skip_signal) {
                 if (a.atomic)
@@ -597,7 +608,7 @@ struct Epi {
                 else
                     st_release_gpu(a.flags + g.slot * kCG + r, 1);
             }
-        } else if (kOwner) {
+        } else if (kFixup) {
             // Every epilogue thread has read the partials: re-arm the flags / counter.
             named_bar_sync(kBar, kGroupThreads);
             if (gt == 0) {
@@ -642,8 +653,8 @@ __device__ void run_epilogue_group(const KArgs& a, const CUtensorMap* tmC, const
     int seg = 0;  // the unit's segment index; the MMA issuer puts segment i in accumulator i % 2
     while (w.next(a.sch, g)) {
         if (seg % kEpiGroups == kGroup) {
-            const bool ok =
-                g.role == kOwner ? e.template segment<true>(g, tr, seg) : e.template segment<false>(g, tr, seg);
+            const bool ok = (g.role == kOwner && !a.sch.sep) ? e.template segment<true>(g, tr, seg)
+                                                              : e.template segment<false>(g, tr, seg);
             if (!ok) break;
             if (tr && seg < kTraceSegs) tr[4 + 4 * seg + 3] = globaltimer();
         }
@@ -790,6 +801,88 @@ __global__ void __launch_bounds__(256)
     }
 }
 
+// --------------------------------------------------------------------------- fixup pass
+// Separate fixup pass for the Stream-K tiles (first page, Case 3: every partial sits in a
+// fixed slot per (unit, first/last segment), and a second kernel sums a split tile's
+// partials in k order). Contributor u of local tile t holds slot 2u if t is the tile its
+// range starts in, else 2u + 1; contributors u_first .. u_last in unit order are k order,
+// and the sum runs left to right in FP32 exactly like the owner's turnstile.
+// One warp per (split tile, CTA rank, lane quadrant, 32-column chunk, 8-column group):
+// lane l takes row 32 * quad + l of the CTA's 128 rows and columns 32c + 8h .. + 7, which
+// in the slot layout are the float4s (8c + 2h) * 32 + l and that + 32 (512 contiguous bytes
+// per warp access).
+__global__ void __launch_bounds__(256)
+    sk_fixup_kernel(const Sched sch, const float* __restrict__ slots, void* __restrict__ C, int32_t M, int32_t N,
+                    int c_bf16) {
+    const int lane = threadIdx.x & 31;
+    const int chunks = sch.tile_n / 32;
+    const int64_t per_tile = static_cast<int64_t>(sch.cg) * 4 * chunks * 4;
+    const int64_t total = static_cast<int64_t>(sch.sk_tiles) * per_tile;
+    const int64_t cta_floats = static_cast<int64_t>(kCtaRows) * sch.tile_n;
+    const int64_t warps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    for (int64_t wi = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; wi < total; wi += warps) {
+        const int32_t lt = static_cast<int32_t>(wi / per_tile);
+        int32_t rem = static_cast<int32_t>(wi % per_tile);
+        const int h = rem & 3;
+        rem >>= 2;
+        const int c = rem % chunks;
+        rem /= chunks;
+        const int quad = rem & 3;
+        const int r = rem >> 2;
+        const int32_t tb = lt * sch.iters;
+        const int32_t u0 = sk_unit_of(sch, tb);
+        const int32_t u1 = sk_unit_of(sch, tb + sch.iters - 1);
+        if (u0 == u1) continue;  // the tile was finished inside one unit
+        const int64_t f4 = static_cast<int64_t>(((c * 8 + 2 * h) * 32 + lane) * 4);
+        const int64_t blk_off = static_cast<int64_t>(quad) * 32 * sch.tile_n + f4;
+        float acc[8];
+        // Contributors four at a time: the loads go out together, the adds stay in k order.
+        for (int32_t u = u0; u <= u1; u += 4) {
+            float4 x[4][2];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int32_t uj = u + j;
+                if (uj <= u1) {
+                    const int32_t first_tile = sk_unit_begin(sch, uj) / sch.iters;
+                    const int32_t slot = 2 * uj + (first_tile == lt ? 0 : 1);
+                    const float* p = slots + (static_cast<int64_t>(slot) * sch.cg + r) * cta_floats + blk_off;
+                    x[j][0] = __ldcg(reinterpret_cast<const float4*>(p));
+                    x[j][1] = __ldcg(reinterpret_cast<const float4*>(p + 128));
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                if (u + j > u1) break;
+                const float y[8] = {x[j][0].x, x[j][0].y, x[j][0].z, x[j][0].w,
+                                    x[j][1].x, x[j][1].y, x[j][1].z, x[j][1].w};
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[e] = (u + j == u0) ? y[e] : acc[e] + y[e];
+            }
+        }
+        const int32_t tile = sch.sk_base + lt;
+        const int64_t row = static_cast<int64_t>(tile / sch.tiles_n) * sch.tile_m + r * kCtaRows + quad * 32 + lane;
+        const int32_t col = (tile % sch.tiles_n) * sch.tile_n + c * 32 + 8 * h;
+        if (row >= M) continue;
+        // N is a multiple of 4 (FP32 C) or 8 (BF16 C), so each 4-column half is all in or out.
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            const int32_t cc = col + 4 * half;
+            if (cc >= N) break;
+            if (c_bf16) {
+                __nv_bfloat162 lo = __floats2bfloat162_rn(acc[4 * half], acc[4 * half + 1]);
+                __nv_bfloat162 hi = __floats2bfloat162_rn(acc[4 * half + 2], acc[4 * half + 3]);
+                uint2 pk;
+                pk.x = *reinterpret_cast<uint32_t*>(&lo);
+                pk.y = *reinterpret_cast<uint32_t*>(&hi);
+                *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(C) + row * N + cc) = pk;
+            } else {
+                *reinterpret_cast<float4*>(static_cast<float*>(C) + row * N + cc) =
+                    make_float4(acc[4 * half], acc[4 * half + 1], acc[4 * half + 2], acc[4 * half + 3]);
+            }
+        }
+    }
+}
+
 // --------------------------------------------------------------------------- host side
 // One-CTA shapes launch cooperatively (the launch fails unless every unit is resident at
 // once). Pair shapes launch as clusters of 2 without that attribute: the host has checked
@@ -895,6 +988,17 @@ cudaError_t launch_reduce(const float* P, void* C, int c_bf16, int splits, int64
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
     sk_reduce_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(P, C, c_bf16, splits, n4);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_fixup(const Sched& sch, const float* slots, void* C, int32_t M, int32_t N, int c_bf16, int num_sms,
+                         cudaStream_t stream) {
+    const int64_t warps = static_cast<int64_t>(sch.sk_tiles) * sch.cg * 4 * (sch.tile_n / 32) * 4;
+    if (warps == 0) return cudaSuccess;
+    int64_t blocks = (warps + 7) / 8;
+    const int64_t cap = static_cast<int64_t>(num_sms) * 8;
+    if (blocks > cap) blocks = cap;
+    sk_fixup_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(sch, slots, C, M, N, c_bf16);
     return cudaGetLastError();
 }
 

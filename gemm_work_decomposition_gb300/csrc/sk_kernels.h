@@ -79,6 +79,10 @@ cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CU
 // Configure the kernels' shared-memory limit on the current device and report, per
 // sk_tile value, how many units of that shape can be resident at once.
 cudaError_t prepare_device(int num_sms, int* max_units);
+// Separate fixup pass for a plan with sch.sep: every Stream-K tile covered by more than one
+// unit gets C = its partial slots summed in k order (FP32), stored as BF16 or FP32.
+cudaError_t launch_fixup(const Sched& sch, const float* slots, void* C, int32_t M, int32_t N, int c_bf16, int num_sms,
+                         cudaStream_t stream);
 // C = sum_j P[j] in j order, FP32 -> c_bf16 ? BF16 : FP32. mn % 4 == 0.
 cudaError_t launch_reduce(const float* P, void* C, int c_bf16, int splits, int64_t mn, int num_sms,
                           cudaStream_t stream);

@@ -35,8 +35,12 @@ struct Sched {
     int32_t sk_tiles, sk_units, sk_q, sk_big, sk_base;
     // Data-parallel region: tiles [0, dp_tiles), unit w runs w, w + workers, ...
     int32_t dp_tiles;
-    // Split-K: effective split count, k-iterations per split, slab mode flag.
+    // Split-K: effective split count, k-iterations per split, slab mode (1 reduction pass,
+    // 2 last arriver).
     int32_t splits, chunk, partials;
+    // Stream-K tiles merged by a separate fixup pass (every partial segment stores to slot
+    // 2 * unit for the unit's first segment, 2 * unit + 1 for its last; nobody waits).
+    int32_t sep;
     int32_t label, label_splits, n_slots;
     // Work-tile shape and CTAs per tile (a unit is one CTA or one CTA pair).
     int32_t tile_m, tile_n, cg;
@@ -109,6 +113,7 @@ struct Walk {
         if (phase == 0) {
             if (it < end) {
                 // One segment: the rest of the current tile inside this unit's range.
+                const bool first = it == sk_unit_begin(s, unit);
                 const int32_t local = it / s.iters;
                 const int32_t tb = local * s.iters;
                 const int32_t te = tb + s.iters;
@@ -127,10 +132,12 @@ struct Walk {
                     g.role = kOwner;
                     g.peer_begin = unit + 1;
                     g.n_peers = sk_unit_of(s, te - 1) - unit;
+                    if (s.sep) g.slot = 2 * unit + (first ? 0 : 1);
                 } else {
-                    // Partial handed to the owner; one slot per unit (its index).
+                    // Partial handed to the owner; one slot per unit (its index). A producer
+                    // is always its unit's first segment.
                     g.role = kProducer;
-                    g.slot = unit;
+                    g.slot = s.sep ? 2 * unit : unit;
                     g.peer_begin = sk_unit_of(s, tb) + 1;
                 }
                 it = se;

@@ -63,12 +63,20 @@ typedef struct {
     int32_t splits;         /* Split-K split count s, 1 <= s <= iters (SK_SPLITK only) */
     int32_t units;          /* 0: num_sms persistent units; > 0: use this many instead */
     int32_t min_iters;      /* hybrid rule's minimum k-iterations per Stream-K unit; 0 = 8 */
-    int32_t split_partials; /* SK_SPLITK only. 0: the k = 0 split owns the tile's fixup.
-                               1: every split writes an FP32 slab P[j] into the workspace
-                               and a second launch (the sk_reduce_splits pass) sums the
-                               slabs in split order into C.
-                               2: as 1, but inside the one launch: the split that arrives
-                               last at a tile sums that tile's slabs into C */
+    int32_t split_partials; /* 0: the unit holding a split tile's k = 0 iteration waits
+                               for its peers and sums their partials (in-kernel fixup).
+                               SK_SPLITK, 1: every split writes an FP32 slab P[j] into the
+                               workspace and a second launch (the sk_reduce_splits pass)
+                               sums the slabs in split order into C.
+                               SK_SPLITK, 2: as 1, but inside the one launch: the split that
+                               arrives last at a tile sums that tile's slabs into C.
+                               SK_STREAMK / SK_HYBRID, 1: separate fixup pass (first page,
+                               Case 3): every partial segment, the owner's too, stores its
+                               FP32 partial to a fixed slot (2u for unit u's first segment,
+                               2u + 1 for its last) and nobody waits; a second launch sums
+                               each split tile's slots in k order into C. The sum order is
+                               the turnstile's, so `r` does not apply.
+                               SK_DP takes 0 only. */
     int32_t tile;           /* sk_tile; 0 = 128 x 128 */
 } sk_schedule;
 
@@ -100,6 +108,8 @@ typedef struct {
  *   (k_begin/k_end in k-iterations; PRODUCER: slot = its partial slot; OWNER: its peers'
  *   partials are slots peer_begin .. peer_begin + n_peers - 1 in k order; PRODUCER rows
  *   carry their owner's peer_begin, which is also the tile's slot in atomic mode;
+ *   with the separate Stream-K fixup pass, OWNER and PRODUCER rows hold their own slot,
+ *   2 * unit or 2 * unit + 1, and the peer fields only describe the tile;
  *   SLAB: slot = split index; unused fields are -1 or 0)
  * then `tiles` rows of SK_MAP_TILE values: owner unit (runs k = 0), contributors. */
 #define SK_MAP_VERSION 1

@@ -161,7 +161,7 @@ class Plan:
         return [s for segs in self.units for s in segs]
 
 
-def _streamk_region(tiles_base: int, n_tiles: int, iters: int, n_units: int):
+def _streamk_region(tiles_base: int, n_tiles: int, iters: int, n_units: int, separate: bool = False):
     """Per-unit segments of Stream-K over tiles [tiles_base, tiles_base + n_tiles).
 
     Follows the page's per-unit algorithm (Case 2 stream_k_units; Mental model): each unit
@@ -170,7 +170,13 @@ def _streamk_region(tiles_base: int, n_tiles: int, iters: int, n_units: int):
     is the OWNER: it waits for the later units whose ranges start before the tile ends
     (its peers, in k order) and runs the fixup. Any other segment is a PRODUCER that stores
     an FP32 partial and raises a flag. Reading taken: each unit has one partial slot, its
-    own index, so a tile's peers occupy consecutive slots owner+1 .. owner+n_peers."""
+    own index, so a tile's peers occupy consecutive slots owner+1 .. owner+n_peers.
+
+    With `separate` (the page's Case 3 kernel: a separate fixup pass instead of waiting)
+    every partial segment, the owner's too, stores to a fixed slot per (unit, first/last
+    segment): slot 2u for the unit's first segment, 2u + 1 for a later one. A unit has at
+    most two partial segments, its first and its last; a producer is always a unit's first
+    segment."""
     bounds = divmod_bounds(n_tiles * iters, n_units)
     out = []
     for u, (b, e) in enumerate(bounds):
@@ -191,17 +197,18 @@ def _streamk_region(tiles_base: int, n_tiles: int, iters: int, n_units: int):
                 while v < n_units and bounds[v][0] < tile_end:
                     peers.append(v)
                     v += 1
-                segs.append(Segment(u, 0, tile, kb, ke, OWNER, -1, u + 1, len(peers)))
+                slot = (2 * u + (0 if it == b else 1)) if separate else -1
+                segs.append(Segment(u, 0, tile, kb, ke, OWNER, slot, u + 1, len(peers)))
             else:
                 owner = next(v for v in range(n_units) if bounds[v][0] <= tile_begin < bounds[v][1])
-                segs.append(Segment(u, 0, tile, kb, ke, PRODUCER, u, owner + 1, 0))
+                segs.append(Segment(u, 0, tile, kb, ke, PRODUCER, 2 * u if separate else u, owner + 1, 0))
             it = seg_end
         out.append(segs)
     return out
 
 
 def build_plan(M: int, N: int, K: int, num_sms: int, mode: int, splits: int = 1,
-               units: int = 0, min_iters: int = 8, split_partials: bool = False, tile: int = 0) -> Plan:
+               units: int = 0, min_iters: int = 8, split_partials: int = 0, tile: int = 0) -> Plan:
     """The integer work-unit map for one GEMM.
 
     `units` > 0 replaces num_sms as the number of persistent units (the toy case is
@@ -219,20 +226,28 @@ def build_plan(M: int, N: int, K: int, num_sms: int, mode: int, splits: int = 1,
         s_eff-1 - i % s_eff, and unit w runs items w, w + W, ... (W = min(units, items)):
         every producer is queued before its owner, so no unit ever waits on work queued
         behind it. Slots: tile t's split j >= 1 uses slot t*(s_eff-1) + j-1.
-        With split_partials every split is a SLAB that writes its own [M,N] FP32 slab j.
+        With split_partials (1 or 2) every split is a SLAB that writes its own [M,N] FP32
+        slab j; 1 and 2 differ only in who sums the slabs, not in the plan.
       - Stream-K: units = min(units, tiles * iters) so that no unit is empty.
       - Hybrid (Case 2 hybrid; "gives the last 160 tiles ... to Stream-K"): the
         heuristic's Stream-K tiles are the last sk_tiles tile ids, split over sk_units
         units; the first tiles - sk_tiles run data-parallel over W units. Each unit runs
         its Stream-K range first, then its data-parallel tiles. A SplitK(s) label is
         planned with the same Stream-K partition (the page's hybrid simulates it so).
+      - Stream-K and hybrid with split_partials = 1: the Stream-K tiles are merged by a
+        separate fixup pass (Case 3), so every partial segment stores to its (unit,
+        first/last) slot; see _streamk_region. A hybrid that resolves to DP has no partials.
     """
     if min(M, N, K) < 1 or num_sms < 1 or units < 0 or min_iters < 1:
         raise ValueError("bad problem")
     if mode not in (DP, SPLITK, STREAMK, HYBRID):
         raise ValueError("bad mode")
-    if split_partials and mode != SPLITK:
-        raise ValueError("split partials need Split-K")
+    if split_partials not in (0, 1, 2):
+        raise ValueError("bad split_partials")
+    if split_partials == 2 and mode != SPLITK:
+        raise ValueError("the last-arriver sum needs Split-K slabs")
+    if split_partials and mode == DP:
+        raise ValueError("data-parallel tiles have no partials")
     if tile not in TILE_SHAPES:
         raise ValueError("bad tile shape")
     tile_m, tile_n, cg = TILE_SHAPES[tile]
@@ -249,13 +264,15 @@ def _build(S, mode, splits, min_iters, split_partials, tiles, tiles_n, iters) ->
     if mode == HYBRID:
         label, sk_tiles, sk_units, lsp = heuristic(tiles, iters, S, min_iters)
         if label == LABEL_DP:
-            p = _build(S, DP, 1, min_iters, False, tiles, tiles_n, iters)
+            p = _build(S, DP, 1, min_iters, 0, tiles, tiles_n, iters)
             p.label, p.label_splits = label, lsp
             return p
         dp_tiles = tiles - sk_tiles
         W = max(sk_units, min(S, dp_tiles))
-        p = Plan(HYBRID, tiles, iters, tiles_n, W, sk_tiles, sk_units, 0, label, lsp, sk_units)
-        region = _streamk_region(dp_tiles, sk_tiles, iters, sk_units)
+        sep = bool(split_partials)
+        p = Plan(HYBRID, tiles, iters, tiles_n, W, sk_tiles, sk_units, 0, label, lsp,
+                 (2 if sep else 1) * sk_units)
+        region = _streamk_region(dp_tiles, sk_tiles, iters, sk_units, sep)
         for w in range(W):
             segs = list(region[w]) if w < sk_units else []
             for t in range(w, dp_tiles, W):
@@ -268,8 +285,9 @@ def _build(S, mode, splits, min_iters, split_partials, tiles, tiles_n, iters) ->
             p.units.append([Segment(w, 0, t, 0, iters, FULL) for t in range(w, tiles, W)])
     elif mode == STREAMK:
         U = min(S, tiles * iters)
-        p = Plan(STREAMK, tiles, iters, tiles_n, U, tiles, U, 0, LABEL_NONE, 0, U)
-        p.units = _streamk_region(0, tiles, iters, U)
+        sep = bool(split_partials)
+        p = Plan(STREAMK, tiles, iters, tiles_n, U, tiles, U, 0, LABEL_NONE, 0, (2 if sep else 1) * U)
+        p.units = _streamk_region(0, tiles, iters, U, sep)
     else:  # SPLITK
         if splits < 1 or splits > iters:
             raise ValueError("bad splits")
@@ -299,6 +317,17 @@ def _build(S, mode, splits, min_iters, split_partials, tiles, tiles_n, iters) ->
         for i, s in enumerate(segs):
             s.unit, s.order = w, i
     return p
+
+
+def fixup_slots(p: Plan):
+    """For the separate fixup pass (Case 3 fixup_kernel): {tile: [slot, ...]} for every
+    tile covered by more than one segment, the slots in ascending k order. The pass sums
+    them left to right in FP32, the same order as the owner's turnstile."""
+    by_tile = {}
+    for s in p.segments():
+        if s.role in (OWNER, PRODUCER):
+            by_tile.setdefault(s.tile, []).append((s.k_begin, s.slot))
+    return {t: [slot for _, slot in sorted(v)] for t, v in by_tile.items()}
 
 
 def tile_rows(p: Plan):

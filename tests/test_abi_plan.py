@@ -50,7 +50,7 @@ def test_exports_every_declared_symbol(sk):
 def _cmp(sk, M, N, K, sms, mode, splits=1, units=0, min_iters=0, partials=0, tile=0):
     try:
         want = S.plan_map(S.build_plan(M, N, K, sms, mode, splits=splits, units=units,
-                                       min_iters=min_iters or 8, split_partials=bool(partials), tile=tile))
+                                       min_iters=min_iters or 8, split_partials=partials, tile=tile))
     except ValueError:
         with pytest.raises(sk.SkError) as e:
             sk.sk_plan(M, N, K, sms, sk.schedule(mode, splits, units, min_iters, partials, tile))
@@ -73,6 +73,8 @@ def test_plan_matches_oracle_on_workloads(sk):
     ]
     for M, N, K, sms, mode in cases:
         _cmp(sk, M, N, K, sms, mode)
+        if mode != S.DP:
+            _cmp(sk, M, N, K, sms, mode, partials=1)  # Stream-K / hybrid: separate fixup pass
     for s in (2, 4, 8, 16):
         for M in (96, 256):
             _cmp(sk, M, 512, 2048, 148, S.SPLITK, splits=s, partials=1)
@@ -103,6 +105,8 @@ def test_plan_bruteforce_small(sk):
             for tile in (0, 1, 2, 3):
                 for mode in (S.DP, S.STREAMK, S.HYBRID):
                     _cmp(sk, M, N, K, sms, mode, tile=tile)
+                for mode in (S.STREAMK, S.HYBRID):
+                    _cmp(sk, M, N, K, sms, mode, partials=1, tile=tile)
                 iters = S.cdiv(K, 64)
                 for s in range(1, min(iters, 5) + 1):
                     _cmp(sk, M, N, K, sms, S.SPLITK, splits=s, tile=tile)
@@ -119,13 +123,14 @@ def test_workspace_size(sk):
     for (M, N, K, sms, mode, s, part), tile in itertools.product(
             [(2048, 2432, 4096, 148, S.HYBRID, 1, 0), (128, 640, 256, 4, S.STREAMK, 1, 0),
              (96, 512, 2048, 148, S.SPLITK, 8, 1), (96, 512, 2048, 148, S.SPLITK, 8, 2),
-            (2048, 2432, 4096, 148, S.SPLITK, 2, 0),
+            (2048, 2432, 4096, 148, S.SPLITK, 2, 0), (2048, 2432, 4096, 148, S.HYBRID, 1, 1),
+            (512, 512, 65536, 148, S.STREAMK, 1, 1),
              (2048, 2432, 4096, 148, S.DP, 1, 0)], (0, 1, 2, 3)):
         sch = sk.schedule(mode, s, 0, 0, part, tile)
         m = sk.sk_plan(M, N, K, sms, sch)
         n_slots, splits = int(m[11]), int(m[8])
         tm, tn, cg = int(m[12]), int(m[13]), int(m[14])
-        if part:
+        if part and mode == S.SPLITK:
             want = 256 + -(-4 * splits * M * N // 256) * 256 + -(-4 * int(m[2]) * cg // 256) * 256
         else:
             want = 256 + -(-4 * n_slots * cg // 256) * 256 + n_slots * tm * tn * 4
@@ -140,7 +145,8 @@ def test_errors(sk):
         (128, 128, 128, 4, sk.schedule(7)),
         (128, 128, 128, 4, sk.schedule(sk.SK_SPLITK, 3)),          # s > iters (2)
         (128, 128, 128, 4, sk.schedule(sk.SK_SPLITK, 0)),
-        (128, 128, 128, 4, sk.schedule(sk.SK_STREAMK, 1, 0, 0, 1)),  # slabs need Split-K
+        (128, 128, 128, 4, sk.schedule(sk.SK_STREAMK, 1, 0, 0, 2)),  # the last-arriver sum needs slabs
+        (128, 128, 128, 4, sk.schedule(sk.SK_DP, 1, 0, 0, 1)),       # data-parallel tiles have no partials
         (128, 128, 128, 4, sk.schedule(sk.SK_SPLITK, 2, 0, 0, 3)),   # unknown slab reduction
         (128, 128, 128, 4, sk.schedule(sk.SK_DP, 1, -1)),
         (128, 128, 128, 4, sk.schedule(sk.SK_DP, 1, 0, 0, 0, 4)),      # unknown tile shape

@@ -58,6 +58,8 @@ SCHEDULES = [
     ("hybrid", dict(mode=3)),
     ("slabs2", dict(mode=1, splits=2, split_partials=1)),
     ("slabs2_last", dict(mode=1, splits=2, split_partials=2)),
+    ("streamk_sep", dict(mode=2, split_partials=1)),
+    ("hybrid_sep", dict(mode=3, split_partials=1)),
 ]
 
 
@@ -111,7 +113,9 @@ def test_integer_exact(sk, dev, name, kw, red, sms, layout, tile):
     ("dp_pair128", dict(mode=0, tile=1), 148), ("hybrid_pair128", dict(mode=3, tile=1), 148),
     ("streamk_pair128", dict(mode=2, tile=1), 148), ("splitk2_pair128", dict(mode=1, splits=2, tile=1), 148),
     ("hybrid_pair256", dict(mode=3, tile=2), 148), ("streamk_pair256", dict(mode=2, tile=2), None),
-    ("hybrid_wide256", dict(mode=3, tile=3), 148), ("streamk_wide256", dict(mode=2, tile=3), 148)])
+    ("hybrid_wide256", dict(mode=3, tile=3), 148), ("streamk_wide256", dict(mode=2, tile=3), 148),
+    ("hybrid_sep", dict(mode=3, split_partials=1), 148),
+    ("hybrid_pair256_sep", dict(mode=3, tile=2, split_partials=1), 148)])
 def test_waveq_full(sk, dev, dev_sms, name, kw, sms, red):
     # 2048 x 2432 x 4096: 304 tiles = 2 waves + 8 on 148 SMs, BF16 out; full comparison.
     w = synth.WAVEQ
@@ -166,7 +170,8 @@ def test_smallm_split_slabs(sk, dev, dev_sms, w, s, tile, partials):
 @pytest.mark.parametrize("tile", TILES)
 @pytest.mark.parametrize("w", [synth.SMALLM_96, synth.SMALLM_256], ids=["m96", "m256"])
 @pytest.mark.parametrize("name,kw", [("streamk", dict(mode=2)), ("hybrid", dict(mode=3)),
-                                     ("splitk4", dict(mode=1, splits=4)), ("dp", dict(mode=0))])
+                                     ("splitk4", dict(mode=1, splits=4)), ("dp", dict(mode=0)),
+                                     ("streamk_sep", dict(mode=2, split_partials=1))])
 @pytest.mark.parametrize("red", [DET, ATOM])
 def test_smallm_fixup(sk, dev, w, name, kw, red, tile):
     got, _ = _run(sk, dev, w, sk.schedule(tile=tile, **kw), red, 148)
@@ -191,7 +196,8 @@ def test_sweep(sk, dev, m, name, kw, tile):
 
 # --------------------------------------------------------------------------- large / long-K
 @pytest.mark.parametrize("tile", [0, 1, 2])
-@pytest.mark.parametrize("name,kw", [("hybrid", dict(mode=3)), ("streamk", dict(mode=2))])
+@pytest.mark.parametrize("name,kw", [("hybrid", dict(mode=3)), ("streamk", dict(mode=2)),
+                                     ("streamk_sep", dict(mode=2, split_partials=1))])
 def test_skinny_long_k(sk, dev, name, kw, tile):
     # 512 x 512 x 65536: 16 tiles x 1024 k-iterations, up to 11 contributors per tile
     # (4 tiles over 74 pairs with the 256 x 256 pair tile: about 19 per tile).
@@ -213,7 +219,8 @@ def test_large_8192(sk, dev, dev_sms, tile):
 @pytest.mark.parametrize("w,sched_kw,units", [
     (synth.WAVEQ, dict(mode=3), 148), (synth.SKINNY, dict(mode=2), 148),
     (synth.sweep(256), dict(mode=2), 40), (synth.WAVEQ, dict(mode=3, tile=1), 148),
-    (synth.SKINNY, dict(mode=2, tile=2), 148), (synth.sweep(512), dict(mode=2, tile=1, units=20), 148)])
+    (synth.SKINNY, dict(mode=2, tile=2), 148), (synth.sweep(512), dict(mode=2, tile=1, units=20), 148),
+    (synth.SKINNY, dict(mode=2, tile=2, split_partials=1), 148)])
 def test_deterministic_repeatable(sk, dev, w, sched_kw, units):
     # Deterministic mode: bit-identical over 10 runs and under the reversed unit -> CTA
     # order (the first page's Case 3 varies arrival order through a unit permutation).
@@ -224,12 +231,14 @@ def test_deterministic_repeatable(sk, dev, w, sched_kw, units):
         assert np.array_equal(first, again)
 
 
+@pytest.mark.parametrize("sep", [0, 1], ids=["owner", "pass"])
 @pytest.mark.parametrize("tile,units", [(0, 40), (1, 20), (2, 10), (3, 20)])
-def test_turnstile_k_order(sk, dev, tile, units):
+def test_turnstile_k_order(sk, dev, tile, units, sep):
     # FP32 output, Stream-K over many units on few tiles (several contributors a tile): C
-    # must be the left fold, in k order, of every segment's own FP32 partial.
+    # must be the left fold, in k order, of every segment's own FP32 partial, whether the
+    # owner sums in-kernel or the separate fixup pass does.
     w = synth.Workload("t512", 512, 512, 4096, "NN", "normal", 31, out="f32")
-    sched = sk.schedule(2, units=units, tile=tile)
+    sched = sk.schedule(2, units=units, tile=tile, split_partials=sep)
     plan = osch.build_plan(w.M, w.N, w.K, 148, osch.STREAMK, units=units, tile=tile)
     tm, tn = plan.tile_m, plan.tile_n
     dump = torch.zeros(plan.tiles * plan.iters * tm * tn, dtype=torch.float32, device=dev)
@@ -250,6 +259,20 @@ def test_turnstile_k_order(sk, dev, tile, units):
     U.assert_close(got, U.reference(w), "turnstile")
 
 
+@pytest.mark.parametrize("w,kw,sms", [
+    (synth.WAVEQ, dict(mode=3), 148), (synth.WAVEQ, dict(mode=3, tile=2), 148),
+    (synth.SKINNY, dict(mode=2), 148), (synth.SKINNY, dict(mode=2, tile=2), 148),
+    (synth.SKINNY, dict(mode=2, tile=3), 148), (synth.SMALLM_96, dict(mode=3), 148),
+    (synth.sweep(640), dict(mode=2, tile=1, units=11), 148)], ids=lambda v: getattr(v, "name", str(v)))
+def test_separate_pass_equals_owner_fixup(sk, dev, w, kw, sms):
+    # The separate fixup pass sums a split tile's partials in the owner's turnstile order
+    # (own, then peers in k order), so it reproduces the deterministic in-kernel fixup bit
+    # for bit.
+    owner, _ = _run(sk, dev, w, sk.schedule(**kw), DET, sms)
+    sep, _ = _run(sk, dev, w, sk.schedule(split_partials=1, **kw), DET, sms)
+    assert np.array_equal(owner, sep)
+
+
 # --------------------------------------------------------------------------- atomics
 @pytest.mark.parametrize("tile", [0, 1, 2])
 def test_atomic_many_contributors(sk, dev, tile):
@@ -267,7 +290,8 @@ def test_atomic_many_contributors(sk, dev, tile):
                                    (127, 8, 65536 // 8)])
 @pytest.mark.parametrize("tile", TILES)
 @pytest.mark.parametrize("name,kw", [("dp", dict(mode=0)), ("streamk", dict(mode=2)), ("hybrid", dict(mode=3)),
-                                     ("splitk", dict(mode=1, splits=1))])
+                                     ("splitk", dict(mode=1, splits=1)),
+                                     ("streamk_sep", dict(mode=2, split_partials=1))])
 def test_edges(sk, dev, M, N, K, name, kw, tile):
     w = synth.Workload("e", M, N, K, "NT", "normal", 3, out="f32")
     got, _ = _run(sk, dev, w, sk.schedule(tile=tile, **kw), DET, 152)

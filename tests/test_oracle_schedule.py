@@ -172,8 +172,52 @@ def test_plan_invariants_small(mode):
                 p = S.build_plan(M, N, K, sms, mode, splits=s)
                 _check_plan_invariants(p, M, N, K, sms)
                 if mode == S.SPLITK:
-                    p2 = S.build_plan(M, N, K, sms, mode, splits=s, split_partials=True)
+                    p2 = S.build_plan(M, N, K, sms, mode, splits=s, split_partials=1)
                     _check_plan_invariants(p2, M, N, K, sms)
+
+
+@pytest.mark.parametrize("mode", [S.STREAMK, S.HYBRID])
+def test_separate_fixup_slots(mode):
+    # The separate fixup pass (first page, Case 3). The kernel there writes a unit's first
+    # partial segment to slot 2u and a later one to 2u + 1. Its fixup_kernel finds tile t's
+    # contributors u_first .. u_last from the range bounds and reads slot 2u if t is the
+    # tile unit u's range starts in, else 2u + 1. That formula is written out here from the
+    # bounds alone; the segment walk must produce exactly those slots, in k order, and
+    # change nothing else.
+    for M, N, K in [(128, 640, 256), (300, 200, 1000), (640, 640, 512), (128, 128, 64), (1, 1, 1),
+                    (2048, 2432, 4096), (512, 512, 65536)]:
+        for sms in (1, 3, 4, 7, 16, 148):
+            for tile in (0, 2):
+                if S.TILE_SHAPES[tile][2] > sms:
+                    continue
+                base = S.build_plan(M, N, K, sms, mode, tile=tile)
+                sep = S.build_plan(M, N, K, sms, mode, tile=tile, split_partials=1)
+                key = lambda q: [(x.unit, x.order, x.tile, x.k_begin, x.k_end, x.role) for x in q.segments()]
+                assert key(sep) == key(base)
+                if not sep.sk_tiles:  # the hybrid rule chose data-parallel: no partials
+                    assert sep.n_slots == base.n_slots == 0 or sep.mode == S.DP
+                    continue
+                assert sep.n_slots == 2 * sep.sk_units
+                iters = sep.iters
+                bounds = S.divmod_bounds(sep.sk_tiles * iters, sep.sk_units)
+                unit_of = lambda i: next(u for u, (b, e) in enumerate(bounds) if b <= i < e)
+                want = {}
+                for lt in range(sep.sk_tiles):
+                    u_first, u_last = unit_of(lt * iters), unit_of((lt + 1) * iters - 1)
+                    if u_first == u_last:
+                        continue
+                    want[sep.tiles - sep.sk_tiles + lt] = [
+                        2 * u + (0 if bounds[u][0] // iters == lt else 1) for u in range(u_first, u_last + 1)]
+                assert S.fixup_slots(sep) == want, (M, N, K, sms, tile)
+                used = [x.slot for x in sep.segments() if x.role in (S.OWNER, S.PRODUCER)]
+                assert len(used) == len(set(used)) and all(0 <= v < sep.n_slots for v in used)
+
+
+def test_separate_fixup_rejected_where_meaningless():
+    with pytest.raises(ValueError):
+        S.build_plan(128, 640, 256, 4, S.DP, split_partials=1)
+    with pytest.raises(ValueError):
+        S.build_plan(128, 640, 256, 4, S.STREAMK, split_partials=2)
 
 
 def test_splitk_clamped_and_dropped():
