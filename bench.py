@@ -322,6 +322,64 @@ def run_fixups(sk, torch, dev, flush, stream):
     return out
 
 
+def run_experiments(sk, torch, dev, flush, stream, path):
+    """The first page's "Try this" simulator experiments, timed on the GPU. M x 4096 x 4096
+    with the 128 x 128 tile and the schedule built for 132 units (the page's H100 count):
+    data-parallel, Split-K s = 2 and 4, Stream-K and the hybrid rule's choice. At M = 128
+    also Split-K whose reduction is a second launch (slabs, s = 2, 4, 8), Split-K with the
+    owner's fixup, and Stream-K with the owner's fixup and with the separate fixup pass.
+    One JSON line per measurement; the cost model's makespans for the same shapes come
+    from the schedule simulator, outside this run."""
+    SMS, N, K = 132, 4096, 4096
+    ms = list(range(128, 2049, 128)) + [2432, 2944, 4096]
+    big = synth.Workload("mxk", max(ms), N, K, "NN", "normal_sqrtk", 7)
+    A_bits, B_bits = synth.make_inputs(big)
+    A_all = torch.from_numpy(A_bits.view(np.int16)).view(torch.bfloat16).to(dev)
+    B = torch.from_numpy(B_bits.view(np.int16)).view(torch.bfloat16).to(dev)
+
+    def timed(m, sch):
+        A = A_all[:m]
+        C = torch.empty((m, N), dtype=torch.bfloat16, device=dev)
+        nb = sk.sk_workspace_size(m, N, K, SMS, sch, sk.SK_DETERMINISTIC)
+        ws = torch.zeros(nb, dtype=torch.uint8, device=dev)
+        g = lambda: sk.sk_gemm(A, B, C, sk.SK_BF16, m, N, K, sk.SK_NN, sch, sk.SK_DETERMINISTIC, SMS, ws, nb, stream)
+        for _ in range(5):
+            g()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(30)]
+        for a0, a1 in ev:
+            flush.zero_()
+            a0.record(stream)
+            g()
+            a1.record(stream)
+        torch.cuda.synchronize(dev)
+        assert sk.sk_status(ws, stream) == sk.SK_OK
+        plan = sk.sk_plan(m, N, K, SMS, sch)
+        return float(np.median([a0.elapsed_time(a1) for a0, a1 in ev])) * 1e3, plan
+
+    def line(f, **kw):
+        f.write(json.dumps(kw) + "\n")
+        f.flush()
+
+    with open(path, "w") as f:
+        for m in ms:
+            for name, sch in (("data-parallel", sk.schedule(sk.SK_DP)), ("split-K s=2", sk.schedule(sk.SK_SPLITK, 2)),
+                              ("split-K s=4", sk.schedule(sk.SK_SPLITK, 4)), ("stream-K", sk.schedule(sk.SK_STREAMK)),
+                              ("rule", sk.schedule(sk.SK_HYBRID))):
+                us, plan = timed(m, sch)
+                line(f, experiment="rule_vs_four", M=m, N=N, K=K, num_sms=SMS, tile="128x128", schedule=name,
+                     us=us, tiles=int(plan[2]), iters=int(plan[3]), resolved_mode=int(plan[1]), label=int(plan[9]),
+                     sk_tiles=int(plan[5]), sk_units=int(plan[6]))
+        m = 128
+        cases = [(f"split-K s={s} separate reduction", sk.schedule(sk.SK_SPLITK, s, split_partials=1)) for s in (2, 4, 8)]
+        cases += [(f"split-K s={s} owner fixup", sk.schedule(sk.SK_SPLITK, s)) for s in (2, 4, 8)]
+        cases += [("stream-K owner fixup", sk.schedule(sk.SK_STREAMK)),
+                  ("stream-K separate pass", sk.schedule(sk.SK_STREAMK, split_partials=1))]
+        for name, sch in cases:
+            us, plan = timed(m, sch)
+            line(f, experiment="separate_reduction_m128", M=m, N=N, K=K, num_sms=SMS, tile="128x128", schedule=name,
+                 us=us, launches=2 if "separate" in name else 1)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -339,6 +397,8 @@ def main():
     ap.add_argument("--no-extras", action="store_true", help="skip the schedule table, e2e and CPU baseline")
     ap.add_argument("--ref-seconds", type=float, default=10.0)
     ap.add_argument("--sweep", default="", help="also write the tile-count sweep (JSON lines) to this file")
+    ap.add_argument("--experiments", default="",
+                    help="also write the simulator experiments timed on the GPU (JSON lines) to this file")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -525,6 +585,8 @@ def main():
 
         if args.sweep:
             run_sweep(sk, torch, dev, args.sweep, red, flush, stream, peak_tf, dev_sms)
+        if args.experiments:
+            run_experiments(sk, torch, dev, flush, stream, args.experiments)
 
     if rank != 0:
         if world > 1:

@@ -405,6 +405,43 @@ def split_k_makespan(tiles: int, iters: int, sms: int, s: int, EPI: float = 2.0,
     return cdiv(tiles * s, sms) * (chunk + PART) + (s - 1) * PART + EPI
 
 
+def split_k_separate_makespan(tiles: int, iters: int, sms: int, s: int, EPI: float = 2.0, PART: float = 2.0):
+    """Split-K whose reduction is its own wave of work (the page's "Try this": a Split-K
+    variant with a separate reduction kernel). Reading taken: every split, split 0 too,
+    stores its partial (chunk + PART per work item, ceil(tiles*s / sms) waves); then one
+    reduction unit per tile loads its s partials and runs the epilogue (s*PART + EPI per
+    unit, ceil(tiles / sms) waves). Nobody waits on anybody inside a wave."""
+    chunk = cdiv(iters, s)
+    return cdiv(tiles * s, sms) * (chunk + PART) + cdiv(tiles, sms) * (s * PART + EPI)
+
+
+def schedule_choice(m: int, n: int, k: int, sms: int, EPI: float = 2.0, PART: float = 2.0):
+    """The four schedules' makespans for one shape under (EPI, PART), the hybrid rule's
+    label and makespan, and whether the rule's choice is (one of) the best of the four.
+    Ties count as best."""
+    rows = report_rows(m, n, k, sms, EPI, PART)[3]
+    four = {name: t for name, t, _ in rows[:4]}
+    rule_name, rule_t, _ = rows[4]
+    best = min(four.values())
+    return {"m": m, "four": four, "rule": rule_name, "rule_makespan": rule_t, "best": best,
+            "rule_is_best": rule_t <= best + 1e-9}
+
+
+def rule_stops_best(ms, n: int, k: int, sms: int, EPI: float = 2.0, PART: float = 2.0):
+    """Scan m over `ms` (ascending): the first m at which the rule's choice is not the best
+    of the four schedules after it was the best at the previous m (None if that never
+    happens), and the list of every m where it is not the best."""
+    prev, first, misses = None, None, []
+    for m in ms:
+        ok = schedule_choice(m, n, k, sms, EPI, PART)["rule_is_best"]
+        if not ok:
+            misses.append(m)
+            if prev and first is None:
+                first = m
+        prev = ok
+    return first, misses
+
+
 def report_rows(m: int, n: int, k: int, sms: int, EPI: float = 2.0, PART: float = 2.0):
     """The five rows of the page's schedule report for one shape: (name, makespan, eff),
     plus the ideal makespan tiles * (iters + EPI) / sms."""

@@ -278,3 +278,73 @@ def test_tile_shapes(tile):
         _check_plan_invariants(S.build_plan(300, 520, 1000, 7, mode, splits=2, tile=tile), 300, 520, 1000, 7)
     with pytest.raises(ValueError):
         S.build_plan(128, 128, 64, 1, S.DP, tile=1) if cg == 2 else S.build_plan(128, 128, 64, 1, S.DP, tile=9)
+
+
+def test_rule_is_best_matches_printed_report():
+    # The printed report (first page, Case 2): the rule's row equals the best of the four
+    # schedules for 1536^2 on H100 and 3840^2 on B200, and loses to Split-K s = 4 at
+    # 128 x 4096 and to Stream-K at 4096^2 on H100.
+    want = {(1536, 1536, 132): True, (128, 4096, 132): False, (3840, 3840, 148): True, (4096, 4096, 132): False}
+    for (m, n, sms), ok in want.items():
+        c = S.schedule_choice(m, n, 4096, sms, 2, 2)
+        assert c["rule_is_best"] is ok, (m, n, c)
+    assert S.schedule_choice(128, 4096, 4096, 132, 2, 2)["best"] == 26.0
+
+
+def _two_wave_list_schedule(item_costs, red_costs, sms):
+    # Brute force: SMs take the next work item whenever they are free; the reduction
+    # wave starts when every item of the first wave has finished.
+    import heapq
+    free = [0.0] * sms
+    heapq.heapify(free)
+    end = 0.0
+    for c in item_costs:
+        t = heapq.heappop(free) + c
+        end = max(end, t)
+        heapq.heappush(free, t)
+    free = [end] * sms
+    heapq.heapify(free)
+    for c in red_costs:
+        t = heapq.heappop(free) + c
+        end = max(end, t)
+        heapq.heappush(free, t)
+    return end
+
+
+@pytest.mark.parametrize("tiles,iters,sms,s", [(32, 64, 132, 2), (32, 64, 132, 4), (32, 64, 132, 8), (144, 64, 132, 4),
+                                               (5, 4, 4, 2), (300, 16, 7, 4), (1, 64, 8, 16)])
+@pytest.mark.parametrize("EPI,PART", [(2, 2), (2, 8), (0, 0), (3, 5)])
+def test_split_k_separate_makespan_bruteforce(tiles, iters, sms, s, EPI, PART):
+    # Splits divide iters here, so every item costs chunk + PART; each of the tiles'
+    # reductions costs s * PART + EPI.
+    chunk = iters // s
+    items = [chunk + PART] * (tiles * s)
+    reds = [s * PART + EPI] * tiles
+    assert S.split_k_separate_makespan(tiles, iters, sms, s, EPI, PART) == _two_wave_list_schedule(items, reds, sms)
+
+
+def test_rule_stops_best_scan():
+    first, misses = S.rule_stops_best(range(128, 2049, 128), 4096, 4096, 132, 2, 2)
+    assert misses[:3] == [128, 256, 384] and first == 896
+    for m in misses:
+        assert not S.schedule_choice(m, 4096, 4096, 132, 2, 2)["rule_is_best"]
+
+
+def test_model_vs_gpu_report_fits_synthetic_timings(tmp_path, capsys):
+    # The report's least-squares fit recovers a known unit: timings made from the model
+    # itself at PART = 8 (10 us + 250 ns per k-iteration) fit exactly at PART = 8, and the
+    # model then picks the fastest schedule on every shape.
+    import json
+    from oracle import model_vs_gpu as R
+    ms = [128, 640, 1024, 2048]
+    path = tmp_path / "exp.jsonl"
+    with open(path, "w") as f:
+        for m in ms:
+            mr = R.model_rows(m, 8.0)
+            for name in R.FOUR + ["rule"]:
+                f.write(json.dumps({"experiment": "rule_vs_four", "M": m, "schedule": name,
+                                    "us": 10.0 + 0.25 * mr[name]}) + "\n")
+    R.main(str(path))
+    out = capsys.readouterr().out
+    assert f"PART=   8: model picks the measured best on {len(ms)}/{len(ms)} shapes" in out
+    assert "fit us = 10.00 + 250.0 ns x makespan, rms relative error 0.0%" in out
