@@ -298,7 +298,7 @@ def run_fixups(sk, torch, dev, flush, stream):
         rows = {}
         for tile, tname in ((0, "128x128"), (2, "pair256x256")):
             plan = sk.sk_plan(w.M, w.N, w.K, 148, sk.schedule(mode, tile=tile))
-            contrib = plan[-2 * int(plan[2]) + 1::2]
+            contrib = plan[-sk.SK_MAP_TILE * int(plan[2]) + 1::sk.SK_MAP_TILE]
             for name, part, red in (("owner", 0, sk.SK_DETERMINISTIC), ("atomic", 0, sk.SK_ATOMIC),
                                     ("pass", 1, sk.SK_DETERMINISTIC)):
                 sch = sk.schedule(mode, split_partials=part, tile=tile)
@@ -319,6 +319,37 @@ def run_fixups(sk, torch, dev, flush, stream):
                 rows[f"{tname}/{name}"] = {"us": us, "tflops": fl / (us / 1e6) / 1e12, "launches": 2 if part else 1,
                                            "max_contributors_per_tile": int(max(contrib))}
         out[w.name] = rows
+    return out
+
+
+def run_raster(sk, torch, dev, flush, stream, peak_tf):
+    """Tile-id order on the 8192^3 GEMM (A and B, 268 MB, exceed the 129 MB L2): data-parallel
+    256 x 256 pair tiles on 148 SMs, along N or M, with and without swizzled strips."""
+    w = synth.LARGE
+    A_bits, B_bits = synth.make_inputs(w)
+    A = torch.from_numpy(A_bits.view(np.int16)).view(torch.bfloat16).to(dev)
+    B = torch.from_numpy(B_bits.view(np.int16)).view(torch.bfloat16).to(dev)
+    C = torch.empty((w.M, w.N), dtype=torch.bfloat16, device=dev)
+    fl = 2.0 * w.M * w.N * w.K
+    out = {}
+    for raster, sw in ((0, 0), (0, 2), (0, 4), (0, 8), (0, 16), (1, 0), (1, 4), (1, 8)):
+        sch = sk.schedule(sk.SK_DP, tile=2, raster=raster, swizzle=sw)
+        nb = sk.sk_workspace_size(w.M, w.N, w.K, 148, sch, sk.SK_DETERMINISTIC)
+        ws = torch.zeros(nb, dtype=torch.uint8, device=dev)
+        g = lambda: sk.sk_gemm(A, B, C, sk.SK_BF16, w.M, w.N, w.K, sk.SK_NN, sch, sk.SK_DETERMINISTIC, 148, ws, nb, stream)
+        for _ in range(3):
+            g()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(15)]
+        for a0, a1 in ev:
+            flush.zero_()
+            a0.record(stream)
+            g()
+            a1.record(stream)
+        torch.cuda.synchronize(dev)
+        assert sk.sk_status(ws, stream) == sk.SK_OK
+        us = float(np.median([a0.elapsed_time(a1) for a0, a1 in ev])) * 1e3
+        out[f"{'along_n' if raster == 0 else 'along_m'}/swizzle{sw}"] = {
+            "us": us, "tflops": fl / (us / 1e6) / 1e12, "frac_of_measured_peak": fl / (us / 1e6) / 1e12 / peak_tf}
     return out
 
 
@@ -394,6 +425,8 @@ def main():
                     help="work-tile shape: 0 = 128x128 (one CTA), 1 = 256x128 (CTA pair), "
                          "2 = 256x256 (CTA pair), 3 = 128x256 (one CTA)")
     ap.add_argument("--reduction", default="deterministic", choices=["deterministic", "atomic"])
+    ap.add_argument("--raster", type=int, default=0, choices=[0, 1], help="tile ids along N (0) or M (1)")
+    ap.add_argument("--swizzle", type=int, default=0, help="tile-id strips this many tiles deep (0: none)")
     ap.add_argument("--no-extras", action="store_true", help="skip the schedule table, e2e and CPU baseline")
     ap.add_argument("--ref-seconds", type=float, default=10.0)
     ap.add_argument("--sweep", default="", help="also write the tile-count sweep (JSON lines) to this file")
@@ -444,8 +477,9 @@ def main():
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    def make(mode_name, nsms, splits=1, tile=args.tile):
-        sch = sk.schedule(modes[mode_name], splits if mode_name == "splitk" else 1, tile=tile)
+    def make(mode_name, nsms, splits=1, tile=args.tile, raster=args.raster, swizzle=args.swizzle):
+        sch = sk.schedule(modes[mode_name], splits if mode_name == "splitk" else 1, tile=tile, raster=raster,
+                          swizzle=swizzle)
         nb = sk.sk_workspace_size(w.M, w.N, w.K, nsms, sch, red)
         ws = torch.zeros(nb, dtype=torch.uint8, device=dev)
         return sch, ws, nb
@@ -582,6 +616,7 @@ def main():
 
         extras["smallm_nt"] = run_smallm(sk, torch, dev, flush, stream, dev_sms)
         extras["fixups"] = run_fixups(sk, torch, dev, flush, stream)
+        extras["raster_8192"] = run_raster(sk, torch, dev, flush, stream, peak_tf)
 
         if args.sweep:
             run_sweep(sk, torch, dev, args.sweep, red, flush, stream, peak_tf, dev_sms)
@@ -594,7 +629,8 @@ def main():
         return
 
     sha = kernel_sha()
-    tr = TRAFFIC.get(f"{w.name}/{args.mode}/tile{args.tile}@{sms}")
+    order = "" if (args.raster, args.swizzle) in ((0, 0), (0, 1)) else f"/r{args.raster}s{args.swizzle}"
+    tr = TRAFFIC.get(f"{w.name}/{args.mode}/tile{args.tile}@{sms}{order}")
     traffic = tr["bytes"] if tr and tr.get("kernel_sha") == sha else None
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
@@ -604,6 +640,7 @@ def main():
                    "schedule": args.mode, "reduction": args.reduction, "num_sms": sms, "device_sms": dev_sms,
                    "tile": {0: "128x128", 1: "256x128 CTA pair", 2: "256x256 CTA pair", 3: "128x256"}[args.tile],
                    "tile_m": int(plan[12]), "tile_n": int(plan[13]), "ctas_per_tile": int(plan[14]),
+                   "raster": "along_n" if args.raster == 0 else "along_m", "swizzle": args.swizzle,
                    "tiles": int(plan[2]), "iters": int(plan[3]), "workers": int(plan[4]),
                    "resolved_mode": int(plan[1]), "sk_tiles": int(plan[5]), "sk_units": int(plan[6]),
                    "l2": "flushed between timed steps (256 MiB write)", "accumulate": "fp32"},

@@ -24,7 +24,7 @@ SK_F32, SK_BF16 = 0, 1
 SK_ROLE_FULL, SK_ROLE_OWNER, SK_ROLE_PRODUCER, SK_ROLE_SLAB = 0, 1, 2, 3
 SK_OK, SK_EINVAL, SK_EWORKSPACE, SK_ECUDA, SK_ETIMEOUT, SK_ECAPACITY, SK_ERESIDENCY, SK_EBOUNDS = 0, -1, -2, -3, -4, -5, -6, -7
 SK_TILE_M, SK_TILE_N, SK_BLK_K = 128, 128, 64
-SK_MAP_VERSION, SK_MAP_HEADER, SK_MAP_SEG, SK_MAP_TILE = 1, 15, 9, 2
+SK_MAP_VERSION, SK_MAP_HEADER, SK_MAP_SEG, SK_MAP_TILE = 2, 17, 9, 4
 SK_TILE_128x128, SK_TILE_256x128_PAIR, SK_TILE_256x256_PAIR, SK_TILE_128x256 = 0, 1, 2, 3
 SK_WS_HEADER_BYTES = 256
 SK_TRACE_SEGS = 15
@@ -37,7 +37,8 @@ SK_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 class sk_schedule(ctypes.Structure):
     _fields_ = [("mode", ctypes.c_int32), ("splits", ctypes.c_int32), ("units", ctypes.c_int32),
-                ("min_iters", ctypes.c_int32), ("split_partials", ctypes.c_int32), ("tile", ctypes.c_int32)]
+                ("min_iters", ctypes.c_int32), ("split_partials", ctypes.c_int32), ("tile", ctypes.c_int32),
+                ("raster", ctypes.c_int32), ("swizzle", ctypes.c_int32)]
 
 
 class sk_debug_opts(ctypes.Structure):
@@ -52,8 +53,8 @@ class SkError(RuntimeError):
 
 
 def schedule(mode: int, splits: int = 1, units: int = 0, min_iters: int = 0, split_partials: int = 0,
-             tile: int = 0) -> sk_schedule:
-    return sk_schedule(mode, splits, units, min_iters, split_partials, tile)
+             tile: int = 0, raster: int = 0, swizzle: int = 0) -> sk_schedule:
+    return sk_schedule(mode, splits, units, min_iters, split_partials, tile, raster, swizzle)
 
 
 _lib = None

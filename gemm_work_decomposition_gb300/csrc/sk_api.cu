@@ -72,6 +72,7 @@ int32_t make_sched(int32_t M, int32_t N, int32_t K, int32_t num_sms, const sk_sc
     if (s.split_partials != 0 && s.mode == SK_DP) return SK_EINVAL;
     int32_t tm = 0, tn = 0, cg = 0;
     if (!tile_shape(s.tile, &tm, &tn, &cg)) return SK_EINVAL;
+    if (s.raster < 0 || s.raster > 1 || s.swizzle < 0 || s.swizzle > 256) return SK_EINVAL;
     const int64_t tiles_n = (static_cast<int64_t>(N) + tn - 1) / tn;
     const int64_t tiles = ((static_cast<int64_t>(M) + tm - 1) / tm) * tiles_n;
     const int64_t iters = (static_cast<int64_t>(K) + kBlkK - 1) / kBlkK;
@@ -88,6 +89,9 @@ int32_t make_sched(int32_t M, int32_t N, int32_t K, int32_t num_sms, const sk_sc
     o.tile_m = tm;
     o.tile_n = tn;
     o.cg = cg;
+    o.tiles_m = static_cast<int32_t>(tiles / tiles_n);
+    o.raster = s.raster;
+    o.swizzle = s.swizzle;
 
     int32_t mode = s.mode;
     if (mode == SK_HYBRID) {
@@ -284,11 +288,14 @@ int32_t sk_plan(int32_t M, int32_t N, int32_t K, int32_t num_sms, sk_schedule s,
     h[12] = sch.tile_m;
     h[13] = sch.tile_n;
     h[14] = sch.cg;
+    h[15] = sch.raster;
+    h[16] = sch.swizzle;
     int32_t* seg = map + SK_MAP_HEADER;
     int32_t* trow = seg + SK_MAP_SEG * nseg;
     for (int32_t t = 0; t < sch.tiles; ++t) {
-        trow[2 * t] = -1;
-        trow[2 * t + 1] = 0;
+        trow[SK_MAP_TILE * t] = -1;
+        trow[SK_MAP_TILE * t + 1] = 0;
+        tile_coords(sch, t, &trow[SK_MAP_TILE * t + 2], &trow[SK_MAP_TILE * t + 3]);
     }
     for (int32_t w = 0; w < sch.workers; ++w) {
         Walk wk;
@@ -300,8 +307,8 @@ int32_t sk_plan(int32_t M, int32_t N, int32_t K, int32_t num_sms, sk_schedule s,
                                              g.n_peers};
             for (int i = 0; i < SK_MAP_SEG; ++i) seg[i] = row[i];
             seg += SK_MAP_SEG;
-            trow[2 * g.tile + 1] += 1;
-            if (g.k_begin == 0) trow[2 * g.tile] = w;
+            trow[SK_MAP_TILE * g.tile + 1] += 1;
+            if (g.k_begin == 0) trow[SK_MAP_TILE * g.tile] = w;
         }
     }
     return SK_OK;

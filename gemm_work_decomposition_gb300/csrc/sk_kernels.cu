@@ -80,8 +80,10 @@ __device__ void run_producer(const KArgs& a, const CUtensorMap* tmA, const CUten
     bool ok = true;
     while (ok && w.next(a.sch, g)) {
         // This CTA's rows of the tile and its half of the tile's columns of B.
-        const int32_t m0 = (g.tile / a.sch.tiles_n) * (kCtaRows * kCG) + static_cast<int32_t>(rank) * kCtaRows;
-        const int32_t nb = (g.tile % a.sch.tiles_n) * kBN + static_cast<int32_t>(rank) * S::kBNc;
+        int32_t trow, tcolumn;
+        tile_coords(a.sch, g.tile, &trow, &tcolumn);
+        const int32_t m0 = trow * (kCtaRows * kCG) + static_cast<int32_t>(rank) * kCtaRows;
+        const int32_t nb = tcolumn * kBN + static_cast<int32_t>(rank) * S::kBNc;
         const bool rev = reversed_segment(a.sch, g);
         for (int32_t i = 0; i < g.k_end - g.k_begin; ++i) {
             if (!mbar_wait(sm.empty(stage), phase ^ 1u, abort_flag, deadline)) {
@@ -397,8 +399,10 @@ struct Epi {
     // Split-K slabs, last arriver: this CTA's rows of tile g.tile in C = P[0] + P[1] + ...
     // + P[splits-1], summed left to right in FP32.
     __device__ __forceinline__ void reduce_slabs(const Seg& g) {
-        const int32_t m0 = (g.tile / a.sch.tiles_n) * (kCtaRows * kCG) + r * kCtaRows;
-        const int32_t n0 = (g.tile % a.sch.tiles_n) * kBN;
+        int32_t trow, tcolumn;
+        tile_coords(a.sch, g.tile, &trow, &tcolumn);
+        const int32_t m0 = trow * (kCtaRows * kCG) + r * kCtaRows;
+        const int32_t n0 = tcolumn * kBN;
         const int32_t gr = m0 + row;
         const int64_t slab = static_cast<int64_t>(a.M) * a.N;
 #pragma unroll 1
@@ -493,8 +497,10 @@ struct Epi {
         tc_fence_after();
         if (tr && seg < kTraceSegs) tr[4 + 4 * seg + 2] = globaltimer();
 
-        const int32_t m0 = (g.tile / a.sch.tiles_n) * (kCtaRows * kCG) + r * kCtaRows;
-        const int32_t n0 = (g.tile % a.sch.tiles_n) * kBN;
+        int32_t trow, tcolumn;
+        tile_coords(a.sch, g.tile, &trow, &tcolumn);
+        const int32_t m0 = trow * (kCtaRows * kCG) + r * kCtaRows;
+        const int32_t n0 = tcolumn * kBN;
         const int32_t wy = m0 + quad * 32;  // first row of this warp's 32
         float* dump = a.dump ? a.dump +
                                    (static_cast<int64_t>(g.tile) * a.sch.iters + g.k_begin) * (kCtaRows * kCG * kBN) +
@@ -859,9 +865,10 @@ __global__ void __launch_bounds__(256)
                 for (int e = 0; e < 8; ++e) acc[e] = (u + j == u0) ? y[e] : acc[e] + y[e];
             }
         }
-        const int32_t tile = sch.sk_base + lt;
-        const int64_t row = static_cast<int64_t>(tile / sch.tiles_n) * sch.tile_m + r * kCtaRows + quad * 32 + lane;
-        const int32_t col = (tile % sch.tiles_n) * sch.tile_n + c * 32 + 8 * h;
+        int32_t trow, tcolumn;
+        tile_coords(sch, sch.sk_base + lt, &trow, &tcolumn);
+        const int64_t row = static_cast<int64_t>(trow) * sch.tile_m + r * kCtaRows + quad * 32 + lane;
+        const int32_t col = tcolumn * sch.tile_n + c * 32 + 8 * h;
         if (row >= M) continue;
         // N is a multiple of 4 (FP32 C) or 8 (BF16 C), so each 4-column half is all in or out.
 #pragma unroll

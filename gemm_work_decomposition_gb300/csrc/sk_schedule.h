@@ -44,6 +44,9 @@ struct Sched {
     int32_t label, label_splits, n_slots;
     // Work-tile shape and CTAs per tile (a unit is one CTA or one CTA pair).
     int32_t tile_m, tile_n, cg;
+    // Rasterization of the tile grid: tile ids walk along N (0) or M (1), in strips of
+    // `swizzle` tiles across the walk (0 or 1: no strips).
+    int32_t tiles_m, raster, swizzle;
 };
 
 // (tile_m, tile_n, CTAs per tile) of each sk_tile value; false for an unknown value.
@@ -74,6 +77,24 @@ struct Seg {
 SK_HD int32_t cdiv(int32_t a, int32_t b) { return (a + b - 1) / b; }
 SK_HD int32_t imin(int32_t a, int32_t b) { return a < b ? a : b; }
 SK_HD int32_t imax(int32_t a, int32_t b) { return a > b ? a : b; }
+
+// (tile row, tile column) of tile id t ("Threadblock Rasterization" on the CUTLASS page:
+// raster order along N or M, swizzled into bands for L2 reuse). With raster 0 and no
+// swizzle, tile t sits at row t / tiles_n, column t % tiles_n (the first page's order). A
+// swizzle w >= 2 cuts the dimension across the walk into strips w tiles deep; ids fill
+// one strip at a time, across its (up to) w tiles first, then along the walk.
+SK_HD void tile_coords(const Sched& s, int32_t t, int32_t* row, int32_t* col) {
+    const int32_t across = s.raster == 0 ? s.tiles_m : s.tiles_n;
+    const int32_t along = s.raster == 0 ? s.tiles_n : s.tiles_m;
+    const int32_t w = s.swizzle > 1 ? s.swizzle : 1;
+    const int32_t strip = t / (w * along);
+    const int32_t i = t - strip * w * along;
+    const int32_t h = imin(w, across - strip * w);
+    const int32_t a = strip * w + i % h;
+    const int32_t b = i / h;
+    *row = s.raster == 0 ? a : b;
+    *col = s.raster == 0 ? b : a;
+}
 
 // First flattened iteration of Stream-K unit u (divmod split, the first `big` units
 // one iteration longer: Case 2 stream_k_units).

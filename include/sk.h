@@ -78,6 +78,13 @@ typedef struct {
                                the turnstile's, so `r` does not apply.
                                SK_DP takes 0 only. */
     int32_t tile;           /* sk_tile; 0 = 128 x 128 */
+    int32_t raster;         /* tile-id order ("Threadblock Rasterization", CUTLASS page):
+                               0 = along N (row-major, tile t at tile row t / tiles_n),
+                               1 = along M (column-major) */
+    int32_t swizzle;        /* 0 or 1: none; w = 2 .. 256: the dimension across the walk is
+                               cut into strips w tiles deep, and ids fill one strip at a
+                               time, across its w tiles first (tiles that run together
+                               then share A and B panels in L2) */
 } sk_schedule;
 
 #define SK_OK          0
@@ -103,6 +110,7 @@ typedef struct {
  *   [9] hybrid label (-1 none, 0 DataParallel, 1 SplitK, 2 StreamK)
  *   [10] the label's split count   [11] n_slots: FP32 partial-tile slots used
  *   [12] tile_m   [13] tile_n   [14] CTAs per tile (1 or 2)
+ *   [15] raster   [16] swizzle (the tile-id order of sk_schedule)
  * then n_segments rows of SK_MAP_SEG values, in (unit, run order) order:
  *   unit, order, tile, k_begin, k_end, role, slot, peer_begin, n_peers
  *   (k_begin/k_end in k-iterations; PRODUCER: slot = its partial slot; OWNER: its peers'
@@ -111,11 +119,13 @@ typedef struct {
  *   with the separate Stream-K fixup pass, OWNER and PRODUCER rows hold their own slot,
  *   2 * unit or 2 * unit + 1, and the peer fields only describe the tile;
  *   SLAB: slot = split index; unused fields are -1 or 0)
- * then `tiles` rows of SK_MAP_TILE values: owner unit (runs k = 0), contributors. */
-#define SK_MAP_VERSION 1
-#define SK_MAP_HEADER 15
+ * then `tiles` rows of SK_MAP_TILE values: owner unit (runs k = 0), contributors, and
+ * the tile's row and column in the tile grid (its output rows start at row * tile_m, its
+ * columns at column * tile_n). */
+#define SK_MAP_VERSION 2
+#define SK_MAP_HEADER 17
 #define SK_MAP_SEG 9
-#define SK_MAP_TILE 2
+#define SK_MAP_TILE 4
 
 /* Workspace layout: bytes [0, SK_WS_HEADER_BYTES) hold the device status word
  * (int32 at offset 0). In split-partials mode the FP32 slabs P[j][M][N] follow at

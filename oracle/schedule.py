@@ -11,10 +11,11 @@ persistent CTA (one per SM); the fixup combines a split tile's FP32 partials.
 
 Map format produced by `plan_map` (int32 list), the contract the C library's
 sk_plan must reproduce exactly:
-  header (15): version, mode_resolved, tiles, iters, workers, sk_tiles, sk_units,
-               n_segments, splits, label, label_splits, n_slots, tile_m, tile_n, cta_group
+  header (17): version, mode_resolved, tiles, iters, workers, sk_tiles, sk_units,
+               n_segments, splits, label, label_splits, n_slots, tile_m, tile_n, cta_group,
+               raster, swizzle
   n_segments rows (9): unit, order, tile, k_begin, k_end, role, slot, peer_begin, n_peers
-  tiles rows (2): owner_unit, n_contrib
+  tiles rows (4): owner_unit, n_contrib, tile row, tile column
 """
 from __future__ import annotations
 
@@ -35,10 +36,10 @@ LABEL_NONE, LABEL_DP, LABEL_SPLITK, LABEL_STREAMK = -1, 0, 1, 2
 # two CTAs together, so a unit is a CTA pair and num_sms SMs give num_sms // 2 units.
 TILE_SHAPES = {0: (128, 128, 1), 1: (256, 128, 2), 2: (256, 256, 2), 3: (128, 256, 1)}
 
-MAP_VERSION = 1
-HEADER_LEN = 15
+MAP_VERSION = 2
+HEADER_LEN = 17
 SEG_LEN = 9
-TILE_ROW_LEN = 2
+TILE_ROW_LEN = 4
 
 
 def cdiv(a: int, b: int) -> int:
@@ -156,6 +157,9 @@ class Plan:
     tile_m: int = TILE_M
     tile_n: int = TILE_N
     cta_group: int = 1
+    tiles_m: int = 0
+    raster: int = 0
+    swizzle: int = 0
 
     def segments(self):
         return [s for segs in self.units for s in segs]
@@ -208,7 +212,8 @@ def _streamk_region(tiles_base: int, n_tiles: int, iters: int, n_units: int, sep
 
 
 def build_plan(M: int, N: int, K: int, num_sms: int, mode: int, splits: int = 1,
-               units: int = 0, min_iters: int = 8, split_partials: int = 0, tile: int = 0) -> Plan:
+               units: int = 0, min_iters: int = 8, split_partials: int = 0, tile: int = 0,
+               raster: int = 0, swizzle: int = 0) -> Plan:
     """The integer work-unit map for one GEMM.
 
     `units` > 0 replaces num_sms as the number of persistent units (the toy case is
@@ -250,14 +255,33 @@ def build_plan(M: int, N: int, K: int, num_sms: int, mode: int, splits: int = 1,
         raise ValueError("data-parallel tiles have no partials")
     if tile not in TILE_SHAPES:
         raise ValueError("bad tile shape")
+    if raster not in (0, 1) or not 0 <= swizzle <= 256:
+        raise ValueError("bad rasterization")
     tile_m, tile_n, cg = TILE_SHAPES[tile]
-    _, tiles_n, tiles, iters = problem_shape(M, N, K, tile_m, tile_n)
+    tiles_m, tiles_n, tiles, iters = problem_shape(M, N, K, tile_m, tile_n)
     S = units if units > 0 else num_sms // cg
     if S < 1:
         raise ValueError("no units")
     p = _build(S, mode, splits, min_iters, split_partials, tiles, tiles_n, iters)
     p.tile_m, p.tile_n, p.cta_group = tile_m, tile_n, cg
+    p.tiles_m, p.raster, p.swizzle = tiles_m, raster, swizzle
     return p
+
+
+def tile_coords(p: Plan, t: int):
+    """(tile row, tile column) of tile id t: the rasterization of the tile grid (the
+    CUTLASS page, "Threadblock Rasterization": raster order along N or M, and a swizzle
+    that keeps consecutive tiles in a band for L2 reuse). Reading taken: raster 0 walks the
+    ids along N (row-major, the first page's tile order, tile t at row t // tiles_n); raster
+    1 walks along M. A swizzle w >= 2 cuts the dimension across the walk into strips w
+    tiles deep; ids fill one strip at a time, going across the strip's w tiles first and
+    then along the walk. w = 0 or 1 is no swizzle."""
+    across, along = (p.tiles_m, p.tiles_n) if p.raster == 0 else (p.tiles_n, p.tiles_m)
+    w = max(1, p.swizzle)
+    strip, i = divmod(t, w * along)
+    h = min(w, across - strip * w)        # the last strip may be shallower
+    a, b = strip * w + i % h, i // h      # position across and along the walk
+    return (a, b) if p.raster == 0 else (b, a)
 
 
 def _build(S, mode, splits, min_iters, split_partials, tiles, tiles_n, iters) -> Plan:
@@ -345,11 +369,12 @@ def tile_rows(p: Plan):
 def plan_map(p: Plan):
     segs = p.segments()
     out = [MAP_VERSION, p.mode, p.tiles, p.iters, p.workers, p.sk_tiles, p.sk_units,
-           len(segs), p.splits, p.label, p.label_splits, p.n_slots, p.tile_m, p.tile_n, p.cta_group]
+           len(segs), p.splits, p.label, p.label_splits, p.n_slots, p.tile_m, p.tile_n, p.cta_group,
+           p.raster, p.swizzle]
     for s in segs:
         out += [s.unit, s.order, s.tile, s.k_begin, s.k_end, s.role, s.slot, s.peer_begin, s.n_peers]
-    for o, c in tile_rows(p):
-        out += [o, c]
+    for t, (o, c) in enumerate(tile_rows(p)):
+        out += [o, c, *tile_coords(p, t)]
     return out
 
 

@@ -47,17 +47,18 @@ def test_exports_every_declared_symbol(sk):
     assert set(sk.EXPORTS) == declared
 
 
-def _cmp(sk, M, N, K, sms, mode, splits=1, units=0, min_iters=0, partials=0, tile=0):
+def _cmp(sk, M, N, K, sms, mode, splits=1, units=0, min_iters=0, partials=0, tile=0, raster=0, swizzle=0):
     try:
         want = S.plan_map(S.build_plan(M, N, K, sms, mode, splits=splits, units=units,
-                                       min_iters=min_iters or 8, split_partials=partials, tile=tile))
+                                       min_iters=min_iters or 8, split_partials=partials, tile=tile,
+                                       raster=raster, swizzle=swizzle))
     except ValueError:
         with pytest.raises(sk.SkError) as e:
-            sk.sk_plan(M, N, K, sms, sk.schedule(mode, splits, units, min_iters, partials, tile))
+            sk.sk_plan(M, N, K, sms, sk.schedule(mode, splits, units, min_iters, partials, tile, raster, swizzle))
         assert e.value.code == sk.SK_EINVAL
         return None
-    got = sk.sk_plan(M, N, K, sms, sk.schedule(mode, splits, units, min_iters, partials, tile))
-    assert got.tolist() == want, (M, N, K, sms, mode, splits, units, partials, tile)
+    got = sk.sk_plan(M, N, K, sms, sk.schedule(mode, splits, units, min_iters, partials, tile, raster, swizzle))
+    assert got.tolist() == want, (M, N, K, sms, mode, splits, units, partials, tile, raster, swizzle)
     return got
 
 
@@ -90,6 +91,20 @@ def test_plan_matches_oracle_on_workloads(sk):
     for tile in (1, 2, 3):
         for M, N, K, sms, mode in cases:
             _cmp(sk, M, N, K, sms, mode, tile=tile)
+
+
+def test_plan_rasterization(sk):
+    # The tile rows of the map carry each tile's grid position, so the host's tile_coords
+    # (the same code the kernels run) is checked against the oracle here.
+    for M, N, K in [(640, 384, 128), (2048, 2432, 4096), (8192, 8192, 8192), (129, 1000, 72), (512, 512, 65536)]:
+        for tile in (0, 2):
+            for raster in (0, 1):
+                for sw in (0, 1, 2, 3, 4, 8, 256):
+                    for mode in (S.DP, S.STREAMK, S.HYBRID):
+                        _cmp(sk, M, N, K, 148, mode, tile=tile, raster=raster, swizzle=sw)
+    for bad in ((2, 0), (-1, 0), (0, -1), (0, 257)):
+        with pytest.raises(sk.SkError):
+            sk.sk_plan(128, 128, 64, 4, sk.schedule(0, raster=bad[0], swizzle=bad[1]))
 
 
 def test_plan_toy_units_override(sk):

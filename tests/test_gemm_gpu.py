@@ -129,7 +129,7 @@ def test_waveq_atomic_equals_deterministic_two_contributors(sk, dev):
     w = synth.WAVEQ
     sched = sk.schedule(3)
     m = sk.sk_plan(w.M, w.N, w.K, 148, sched)
-    assert max(m[-2 * int(m[2]) + 1::2]) == 2
+    assert max(m[-sk.SK_MAP_TILE * int(m[2]) + 1::sk.SK_MAP_TILE]) == 2
     det, _ = _run(sk, dev, w, sched, DET, 148)
     atom, _ = _run(sk, dev, w, sched, ATOM, 148)
     assert np.array_equal(det, atom)
@@ -252,7 +252,8 @@ def test_turnstile_k_order(sk, dev, tile, units, sep):
         acc = D[t, segs[0].k_begin].copy()
         for s in segs[1:]:
             acc = acc + D[t, s.k_begin]
-        r0, c0 = (t // plan.tiles_n) * tm, (t % plan.tiles_n) * tn
+        tr, tc = osch.tile_coords(plan, t)
+        r0, c0 = tr * tm, tc * tn
         want[r0:r0 + tm, c0:c0 + tn] = acc[:min(tm, w.M - r0), :min(tn, w.N - c0)]
     assert most >= 4
     assert np.array_equal(got, want.astype(np.float64))
@@ -271,6 +272,34 @@ def test_separate_pass_equals_owner_fixup(sk, dev, w, kw, sms):
     owner, _ = _run(sk, dev, w, sk.schedule(**kw), DET, sms)
     sep, _ = _run(sk, dev, w, sk.schedule(split_partials=1, **kw), DET, sms)
     assert np.array_equal(owner, sep)
+
+
+# --------------------------------------------------------------------------- rasterization
+@pytest.mark.parametrize("raster,swizzle", [(0, 2), (0, 3), (1, 0), (1, 4), (0, 256)])
+@pytest.mark.parametrize("name,kw", [("dp", dict(mode=0)), ("splitk3", dict(mode=1, splits=3)),
+                                     ("streamk", dict(mode=2)), ("hybrid", dict(mode=3)),
+                                     ("slabs2", dict(mode=1, splits=2, split_partials=1)),
+                                     ("streamk_sep", dict(mode=2, split_partials=1))])
+@pytest.mark.parametrize("tile", [0, 2])
+def test_rasterized_tile_order(sk, dev, name, kw, raster, swizzle, tile):
+    # A ragged 1000 x 1016 x 520 NT problem (8 x 8 tiles of 128, 4 x 4 of 256) in every tile
+    # order: each tile lands where tile_coords puts it, edges clipped.
+    w = synth.Workload("r", 1000, 1016, 520, "NT", "normal", 41, out="f32")
+    got, _ = _run(sk, dev, w, sk.schedule(tile=tile, raster=raster, swizzle=swizzle, **kw), DET, 37)
+    assert not np.any(got == U.SENTINEL)
+    U.assert_close(got, U.reference(w), name)
+
+
+@pytest.mark.parametrize("raster,swizzle", [(0, 4), (1, 8)])
+def test_rasterized_waveq_and_large(sk, dev, raster, swizzle):
+    w = synth.WAVEQ
+    got, _ = _run(sk, dev, w, sk.schedule(3, tile=2, raster=raster, swizzle=swizzle), DET, 148)
+    U.assert_close(got, U.reference(w), "waveq")
+    w = synth.LARGE
+    got, _ = _run(sk, dev, w, sk.schedule(0, tile=2, raster=raster, swizzle=swizzle), DET, 148)
+    A_bits, B_bits = U.inputs(w)
+    rows = U.sample_rows(w.M, 16, seed=raster * 10 + swizzle)
+    U.assert_close(got[rows], og.ref_rows(A_bits, B_bits, "NN", rows), "8192^3")
 
 
 # --------------------------------------------------------------------------- atomics

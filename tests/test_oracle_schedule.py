@@ -258,8 +258,10 @@ def test_hybrid_waveq_on_148():
 def test_map_layout():
     p = S.build_plan(128, 640, 256, 4, S.STREAMK)
     m = S.plan_map(p)
-    assert m[:S.HEADER_LEN] == [1, S.STREAMK, 5, 4, 4, 5, 4, 8, 0, -1, 0, 4, 128, 128, 1]
+    assert m[:S.HEADER_LEN] == [2, S.STREAMK, 5, 4, 4, 5, 4, 8, 0, -1, 0, 4, 128, 128, 1, 0, 0]
     assert len(m) == S.HEADER_LEN + 8 * S.SEG_LEN + 5 * S.TILE_ROW_LEN
+    # The toy's five tiles in one tile row, t at column t (the page's tile order).
+    assert m[-5 * S.TILE_ROW_LEN:] == [0, 1, 0, 0, 0, 2, 0, 1, 1, 2, 0, 2, 2, 2, 0, 3, 3, 1, 0, 4]
 
 
 @pytest.mark.parametrize("tile", [0, 1, 2, 3])
@@ -348,3 +350,37 @@ def test_model_vs_gpu_report_fits_synthetic_timings(tmp_path, capsys):
     out = capsys.readouterr().out
     assert f"PART=   8: model picks the measured best on {len(ms)}/{len(ms)} shapes" in out
     assert "fit us = 10.00 + 250.0 ns x makespan, rms relative error 0.0%" in out
+
+
+def test_raster_default_is_the_page_tile_order():
+    # First page, Case 3 listing: tile t covers rows (t // tiles_n) * BM and columns
+    # (t % tiles_n) * BN. Raster 0 with no swizzle (0 or 1) is exactly that order.
+    for M, N in [(640, 384), (2048, 2432), (128, 640), (1, 8), (4096, 4096)]:
+        for sw in (0, 1):
+            p = S.build_plan(M, N, 64, 4, S.DP, swizzle=sw)
+            assert [S.tile_coords(p, t) for t in range(p.tiles)] == [divmod(t, p.tiles_n) for t in range(p.tiles)]
+
+
+def test_raster_worked_examples():
+    # 5 x 3 tiles (640 x 384), strips of 2. Along N: ids go down a 2-row strip, then along
+    # N; the last strip (tile row 4) is one row deep. Along M: the transpose.
+    p = S.build_plan(640, 384, 64, 4, S.DP, swizzle=2)
+    assert [S.tile_coords(p, t) for t in range(15)] == [
+        (0, 0), (1, 0), (0, 1), (1, 1), (0, 2), (1, 2), (2, 0), (3, 0), (2, 1), (3, 1), (2, 2), (3, 2),
+        (4, 0), (4, 1), (4, 2)]
+    p = S.build_plan(640, 384, 64, 4, S.DP, raster=1)
+    assert [S.tile_coords(p, t) for t in range(15)] == [(t % 5, t // 5) for t in range(15)]
+    p = S.build_plan(640, 384, 64, 4, S.DP, raster=1, swizzle=2)
+    assert [S.tile_coords(p, t) for t in range(15)] == [
+        (0, 0), (0, 1), (1, 0), (1, 1), (2, 0), (2, 1), (3, 0), (3, 1), (4, 0), (4, 1),
+        (0, 2), (1, 2), (2, 2), (3, 2), (4, 2)]
+
+
+def test_raster_is_a_bijection():
+    for tm in (1, 2, 3, 5, 16, 17):
+        for tn in (1, 2, 4, 7, 19):
+            for raster in (0, 1):
+                for sw in (0, 1, 2, 3, 4, 8, 16, 256):
+                    p = S.build_plan(128 * tm, 128 * tn, 64, 4, S.DP, raster=raster, swizzle=sw)
+                    got = [S.tile_coords(p, t) for t in range(p.tiles)]
+                    assert sorted(got) == [(r, c) for r in range(tm) for c in range(tn)], (tm, tn, raster, sw)
