@@ -40,10 +40,12 @@ WORKLOADS = {"waveq": synth.WAVEQ, "skinny": synth.SKINNY, "large": synth.LARGE,
 # from one ncu capture, keyed by workload/schedule; valid only for the kernel source it
 # was taken on (sha256 of sk_kernels.cu, first 16 hex digits).
 TRAFFIC = {
-    "waveq_2048x2432x4096/hybrid/tile2@148": {"bytes": 36783872 + 1778176, "kernel_sha": "c9541a39e3c22e75",
+    "waveq_2048x2432x4096/hybrid/tile2@148": {"bytes": 36782336 + 1787392, "kernel_sha": "2df42cadca90d73c",
                                               "profile": "profiles/sk_gemm_kernel_waveq_2048x2432x4096_pair256_hybrid148.md"},
-    "waveq_2048x2432x4096/hybrid/tile0@148": {"bytes": 36777728 + 130560, "kernel_sha": "c9541a39e3c22e75",
-                                              "profile": "profiles/sk_gemm_kernel_waveq_2048x2432x4096_tile128_hybrid148.md"},
+    "large_8192x8192x8192/dp/tile2@148": {"bytes": 2065232640 + 129725440, "kernel_sha": "2df42cadca90d73c",
+                                          "profile": "profiles/sk_gemm_kernel_large_8192_pair256_dp148_raster.md"},
+    "large_8192x8192x8192/dp/tile2@148/r0s8": {"bytes": 1048659456 + 125740544, "kernel_sha": "2df42cadca90d73c",
+                                               "profile": "profiles/sk_gemm_kernel_large_8192_pair256_dp148_raster.md"},
 }
 
 
@@ -427,6 +429,8 @@ def main():
     ap.add_argument("--reduction", default="deterministic", choices=["deterministic", "atomic"])
     ap.add_argument("--raster", type=int, default=0, choices=[0, 1], help="tile ids along N (0) or M (1)")
     ap.add_argument("--swizzle", type=int, default=0, help="tile-id strips this many tiles deep (0: none)")
+    ap.add_argument("--partials", type=int, default=0, choices=[0, 1, 2],
+                    help="split_partials of the timed schedule (Split-K slabs; Stream-K/hybrid separate fixup pass)")
     ap.add_argument("--no-extras", action="store_true", help="skip the schedule table, e2e and CPU baseline")
     ap.add_argument("--ref-seconds", type=float, default=10.0)
     ap.add_argument("--sweep", default="", help="also write the tile-count sweep (JSON lines) to this file")
@@ -501,8 +505,15 @@ def main():
         return np.array([s.elapsed_time(e) for s, e in ev])  # ms
 
     sch, ws, nb = make(args.mode, sms, args.splits)
+    if args.partials:
+        sch = sk.schedule(modes[args.mode], args.splits if args.mode == "splitk" else 1, split_partials=args.partials,
+                          tile=args.tile, raster=args.raster, swizzle=args.swizzle)
+        nb = sk.sk_workspace_size(w.M, w.N, w.K, sms, sch, red)
+        ws = torch.zeros(nb, dtype=torch.uint8, device=dev)
     plan = sk.sk_plan(w.M, w.N, w.K, sms, sch)
-    launches_per_step = 1  # one persistent GEMM kernel per step (no split-slab reduction here)
+    # One persistent GEMM kernel per step, plus the reduction or fixup pass when partials are
+    # summed in a second launch.
+    launches_per_step = 2 if args.partials == 1 else 1
 
     # ---- the timed region: K steps, barrier + synchronize on both sides
     for _ in range(args.warmup):
@@ -637,7 +648,7 @@ def main():
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "layout": w.layout, "out": w.out,
-                   "schedule": args.mode, "reduction": args.reduction, "num_sms": sms, "device_sms": dev_sms,
+                   "schedule": args.mode, "split_partials": args.partials, "reduction": args.reduction, "num_sms": sms, "device_sms": dev_sms,
                    "tile": {0: "128x128", 1: "256x128 CTA pair", 2: "256x256 CTA pair", 3: "128x256"}[args.tile],
                    "tile_m": int(plan[12]), "tile_n": int(plan[13]), "ctas_per_tile": int(plan[14]),
                    "raster": "along_n" if args.raster == 0 else "along_m", "swizzle": args.swizzle,
