@@ -40,11 +40,11 @@ WORKLOADS = {"waveq": synth.WAVEQ, "skinny": synth.SKINNY, "large": synth.LARGE,
 # from one ncu capture, keyed by workload/schedule; valid only for the kernel source it
 # was taken on (sha256 of sk_kernels.cu, first 16 hex digits).
 TRAFFIC = {
-    "waveq_2048x2432x4096/hybrid/tile2@148": {"bytes": 36782336 + 1787392, "kernel_sha": "2df42cadca90d73c",
+    "waveq_2048x2432x4096/hybrid/tile2@148": {"bytes": 36792064 + 2104320, "kernel_sha": "e906c78655be9b7d",
                                               "profile": "profiles/sk_gemm_kernel_waveq_2048x2432x4096_pair256_hybrid148.md"},
-    "large_8192x8192x8192/dp/tile2@148": {"bytes": 2065232640 + 129725440, "kernel_sha": "2df42cadca90d73c",
+    "large_8192x8192x8192/dp/tile2@148": {"bytes": 2056086016 + 129275904, "kernel_sha": "e906c78655be9b7d",
                                           "profile": "profiles/sk_gemm_kernel_large_8192_pair256_dp148_raster.md"},
-    "large_8192x8192x8192/dp/tile2@148/r0s8": {"bytes": 1048659456 + 125740544, "kernel_sha": "2df42cadca90d73c",
+    "large_8192x8192x8192/dp/tile2@148/r0s8": {"bytes": 1066447872 + 126214400, "kernel_sha": "e906c78655be9b7d",
                                                "profile": "profiles/sk_gemm_kernel_large_8192_pair256_dp148_raster.md"},
 }
 

@@ -1,6 +1,6 @@
 """Build libsk.so (the C ABI of include/sk.h) in-tree with nvcc for sm_103a.
 
-The two translation units compile in parallel; the library links the CUDA runtime
+The translation units compile in parallel; the library links the CUDA runtime
 statically and reaches the driver's tensor-map encoder through the runtime's driver
 entry-point query, so it needs no libcuda at link time.
 """
@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libsk.so")
-SOURCES = ("sk_kernels.cu", "sk_api.cu", "sk_noalloc.cu")
+SOURCES = ("sk_kernels.cu", "sk_passes.cu", "sk_api.cu", "sk_noalloc.cu")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -1,0 +1,149 @@
+// sk_passes.cu - the second launches that sum FP32 partials into C: the Split-K slab
+// reduction and the separate fixup pass for Stream-K tiles. Both sum in k order, left to
+// right in FP32, and convert to the output type once.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "sk_kernels.h"
+
+namespace sk {
+namespace {
+
+// --------------------------------------------------------------------------- Split-K slab reduction
+__global__ void __launch_bounds__(256)
+    sk_reduce_kernel(const float* __restrict__ P, void* __restrict__ C, int c_bf16, int splits, int64_t n4) {
+    const float4* P4 = reinterpret_cast<const float4*>(P);
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4; i += stride) {
+        float4 acc = __ldcs(P4 + i);
+        for (int j = 1; j < splits; ++j) {
+            const float4 x = __ldcs(P4 + static_cast<int64_t>(j) * n4 + i);
+            acc.x += x.x;
+            acc.y += x.y;
+            acc.z += x.z;
+            acc.w += x.w;
+        }
+        if (c_bf16) {
+            __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+            __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+            uint2 pk;
+            pk.x = *reinterpret_cast<uint32_t*>(&lo);
+            pk.y = *reinterpret_cast<uint32_t*>(&hi);
+            reinterpret_cast<uint2*>(C)[i] = pk;
+        } else {
+            reinterpret_cast<float4*>(C)[i] = acc;
+        }
+    }
+}
+
+// --------------------------------------------------------------------------- fixup pass
+// Separate fixup pass for the Stream-K tiles (first page, Case 3: every partial sits in a
+// fixed slot per (unit, first/last segment), and a second kernel sums a split tile's
+// partials in k order). Contributor u of local tile t holds slot 2u if t is the tile its
+// range starts in, else 2u + 1; contributors u_first .. u_last in unit order are k order,
+// and the sum runs left to right in FP32 exactly like the owner's turnstile.
+// One warp per (split tile, CTA rank, lane quadrant, 32-column chunk, 8-column group):
+// lane l takes row 32 * quad + l of the CTA's 128 rows and columns 32c + 8h .. + 7, which
+// in the slot layout are the float4s (8c + 2h) * 32 + l and that + 32 (512 contiguous bytes
+// per warp access).
+__global__ void __launch_bounds__(256)
+    sk_fixup_kernel(const Sched sch, const float* __restrict__ slots, void* __restrict__ C, int32_t M, int32_t N,
+                    int c_bf16) {
+    const int lane = threadIdx.x & 31;
+    const int chunks = sch.tile_n / 32;
+    const int64_t per_tile = static_cast<int64_t>(sch.cg) * 4 * chunks * 4;
+    const int64_t total = static_cast<int64_t>(sch.sk_tiles) * per_tile;
+    const int64_t cta_floats = static_cast<int64_t>(kCtaRows) * sch.tile_n;
+    const int64_t warps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    for (int64_t wi = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; wi < total; wi += warps) {
+        const int32_t lt = static_cast<int32_t>(wi / per_tile);
+        int32_t rem = static_cast<int32_t>(wi % per_tile);
+        const int h = rem & 3;
+        rem >>= 2;
+        const int c = rem % chunks;
+        rem /= chunks;
+        const int quad = rem & 3;
+        const int r = rem >> 2;
+        const int32_t tb = lt * sch.iters;
+        const int32_t u0 = sk_unit_of(sch, tb);
+        const int32_t u1 = sk_unit_of(sch, tb + sch.iters - 1);
+        if (u0 == u1) continue;  // the tile was finished inside one unit
+        const int64_t f4 = static_cast<int64_t>(((c * 8 + 2 * h) * 32 + lane) * 4);
+        const int64_t blk_off = static_cast<int64_t>(quad) * 32 * sch.tile_n + f4;
+        float acc[8];
+        // Contributors kBatch at a time: the loads go out together, the adds stay in k order.
+        constexpr int kBatch = 8;
+        for (int32_t u = u0; u <= u1; u += kBatch) {
+            float4 x[kBatch][2];
+#pragma unroll
+            for (int j = 0; j < kBatch; ++j) {
+                const int32_t uj = u + j;
+                if (uj <= u1) {
+                    const int32_t first_tile = sk_unit_begin(sch, uj) / sch.iters;
+                    const int32_t slot = 2 * uj + (first_tile == lt ? 0 : 1);
+                    const float* p = slots + (static_cast<int64_t>(slot) * sch.cg + r) * cta_floats + blk_off;
+                    x[j][0] = __ldcg(reinterpret_cast<const float4*>(p));
+                    x[j][1] = __ldcg(reinterpret_cast<const float4*>(p + 128));
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < kBatch; ++j) {
+                if (u + j > u1) break;
+                const float y[8] = {x[j][0].x, x[j][0].y, x[j][0].z, x[j][0].w,
+                                    x[j][1].x, x[j][1].y, x[j][1].z, x[j][1].w};
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[e] = (u + j == u0) ? y[e] : acc[e] + y[e];
+            }
+        }
+        int32_t trow, tcolumn;
+        tile_coords(sch, sch.sk_base + lt, &trow, &tcolumn);
+        const int64_t row = static_cast<int64_t>(trow) * sch.tile_m + r * kCtaRows + quad * 32 + lane;
+        const int32_t col = tcolumn * sch.tile_n + c * 32 + 8 * h;
+        if (row >= M) continue;
+        // N is a multiple of 4 (FP32 C) or 8 (BF16 C), so each 4-column half is all in or out.
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            const int32_t cc = col + 4 * half;
+            if (cc >= N) break;
+            if (c_bf16) {
+                __nv_bfloat162 lo = __floats2bfloat162_rn(acc[4 * half], acc[4 * half + 1]);
+                __nv_bfloat162 hi = __floats2bfloat162_rn(acc[4 * half + 2], acc[4 * half + 3]);
+                uint2 pk;
+                pk.x = *reinterpret_cast<uint32_t*>(&lo);
+                pk.y = *reinterpret_cast<uint32_t*>(&hi);
+                *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(C) + row * N + cc) = pk;
+            } else {
+                *reinterpret_cast<float4*>(static_cast<float*>(C) + row * N + cc) =
+                    make_float4(acc[4 * half], acc[4 * half + 1], acc[4 * half + 2], acc[4 * half + 3]);
+            }
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_reduce(const float* P, void* C, int c_bf16, int splits, int64_t mn, int num_sms,
+                          cudaStream_t stream) {
+    const int64_t n4 = mn / 4;
+    int64_t blocks = (n4 + 255) / 256;
+    const int64_t cap = static_cast<int64_t>(num_sms) * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    sk_reduce_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(P, C, c_bf16, splits, n4);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_fixup(const Sched& sch, const float* slots, void* C, int32_t M, int32_t N, int c_bf16, int num_sms,
+                         cudaStream_t stream) {
+    const int64_t warps = static_cast<int64_t>(sch.sk_tiles) * sch.cg * 4 * (sch.tile_n / 32) * 4;
+    if (warps == 0) return cudaSuccess;
+    int64_t blocks = (warps + 7) / 8;
+    const int64_t cap = static_cast<int64_t>(num_sms) * 8;
+    if (blocks > cap) blocks = cap;
+    sk_fixup_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(sch, slots, C, M, N, c_bf16);
+    return cudaGetLastError();
+}
+
+}  // namespace sk
