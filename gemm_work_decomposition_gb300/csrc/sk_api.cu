@@ -132,6 +132,7 @@ int32_t make_sched(int32_t M, int32_t N, int32_t K, int32_t num_sms, const sk_sc
         o.splits = static_cast<int32_t>(s_eff);
         o.chunk = static_cast<int32_t>(chunk);
         o.partials = s.split_partials;
+        o.coop = (s.split_partials == 2 && items <= S) ? 1 : 0;
         o.n_slots = s.split_partials ? 0 : static_cast<int32_t>(tiles * (s_eff - 1));
         o.workers = static_cast<int32_t>(items < S ? items : S);
     }

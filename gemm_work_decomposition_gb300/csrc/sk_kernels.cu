@@ -441,6 +441,52 @@ struct Epi {
         }
     }
 
+    // Split-K slabs, shared sum: split g.slot's share of this CTA's 128 rows of tile g.tile,
+    // rows [j * R, (j + 1) * R) with R = ceil(128 / splits), summed over the slabs in split
+    // order (the reduction pass's order) and stored to C. Warp w takes rows w, w + 4, ...;
+    // lane l takes columns 4l .. 4l + 3 of every 128, so each load covers 512 contiguous bytes.
+    __device__ __forceinline__ void reduce_slab_share(const Seg& g) {
+        int32_t trow, tcolumn;
+        tile_coords(a.sch, g.tile, &trow, &tcolumn);
+        const int32_t rows_per = (kCtaRows + a.sch.splits - 1) / a.sch.splits;
+        const int32_t r_begin = g.slot * rows_per;
+        const int32_t r_end = imin(kCtaRows, r_begin + rows_per);
+        const int32_t m0 = trow * (kCtaRows * kCG) + r * kCtaRows;
+        const int32_t n0 = tcolumn * kBN;
+        const int64_t slab = static_cast<int64_t>(a.M) * a.N;
+#pragma unroll 1
+        for (int32_t rr = r_begin + (gt >> 5); rr < r_end; rr += 4) {
+            const int32_t gr = m0 + rr;
+            if (gr >= a.M) break;  // rows ascend
+#pragma unroll
+            for (int q = 0; q < kBN / 128; ++q) {
+                const int32_t gc = n0 + q * 128 + lane * 4;
+                if (gc >= a.N) break;  // N % 8 == 0: each group of 4 columns is all in or out
+                const float* p = a.slabs + static_cast<int64_t>(gr) * a.N + gc;
+                float4 acc = ld_cg_f4(p);
+#pragma unroll 4
+                for (int32_t j = 1; j < a.sch.splits; ++j) {
+                    const float4 x = ld_cg_f4(p + j * slab);
+                    acc.x += x.x;
+                    acc.y += x.y;
+                    acc.z += x.z;
+                    acc.w += x.w;
+                }
+                const int64_t off = static_cast<int64_t>(gr) * a.N + gc;
+                if (a.c_bf16) {
+                    __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+                    __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+                    uint2 pk;
+                    pk.x = *reinterpret_cast<uint32_t*>(&lo);
+                    pk.y = *reinterpret_cast<uint32_t*>(&hi);
+                    *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.C) + off) = pk;
+                } else {
+                    *reinterpret_cast<float4*>(static_cast<float*>(a.C) + off) = acc;
+                }
+            }
+        }
+    }
+
     // The workspace indices a segment will use lie inside the extents the host sized.
     __device__ __forceinline__ bool in_bounds(const Seg& g) const {
         if (g.tile < 0 || g.tile >= a.sch.tiles) return false;
@@ -583,19 +629,36 @@ struct Epi {
         if (!kFixedBuf) buf ^= 1;
 
         if (g.role == kSlab && a.sch.partials == 2) {
-            // Split-K slab, last-arriver reduction: publish the slab and count the arrival
-            // at the tile; the split that arrives last sums the tile's slabs in split order
-            // into C (aligned split with a per-tile arrival counter, as in the docc StreamK
-            // rewrite). With split_partials = 1 a separate pass does that sum instead.
+            // Split-K slab, summed inside this launch (aligned split with a per-tile arrival
+            // counter, as in the docc StreamK rewrite): publish the slab and count the arrival
+            // at the tile. When every split of the tile is running at once, the splits share
+            // the sum; otherwise the split that arrives last sums the tile's slabs alone. Both
+            // add in split order. With split_partials = 1 a separate pass does the sum.
             if (lane == 0) {
                 bulk_wait_group_all();
                 fence_proxy_async_global();
             }
             __syncwarp();
             named_bar_sync(kBar, kGroupThreads);
-            if (gt == 0)
-                *last_flag = atom_add_acq_rel_gpu(a.counters + g.tile * kCG + r, 1) ==
-                             static_cast<uint32_t>(a.sch.splits - 1);
+            int32_t* cnt = a.counters + g.tile * kCG + r;
+            if (a.sch.coop) {
+                // Every split of the tile is running (one work item per unit): wait until all
+                // have arrived, then each sums its share of the rows. The counter goes on to
+                // 2 * splits as the shares finish; the last to finish resets it to zero (by
+                // then every split has passed its wait).
+                if (gt == 0) (void)atom_add_acq_rel_gpu(cnt, 1);
+                const bool all = wait_flag(cnt, a.sch.splits, deadline, abort_flag);
+                if (named_bar_or(kBar, kGroupThreads, !all)) {
+                    record_timeout(a, abort_flag);
+                    return false;
+                }
+                reduce_slab_share(g);
+                named_bar_sync(kBar, kGroupThreads);
+                if (gt == 0 && atom_add_acq_rel_gpu(cnt, 1) == static_cast<uint32_t>(2 * a.sch.splits - 1))
+                    atomicExch(cnt, 0);
+                return true;
+            }
+            if (gt == 0) *last_flag = atom_add_acq_rel_gpu(cnt, 1) == static_cast<uint32_t>(a.sch.splits - 1);
             named_bar_sync(kBar, kGroupThreads);
             if (*last_flag) {
                 (void)ld_acquire_gpu(a.counters + g.tile * kCG + r);

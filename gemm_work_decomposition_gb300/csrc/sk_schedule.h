@@ -36,8 +36,9 @@ struct Sched {
     // Data-parallel region: tiles [0, dp_tiles), unit w runs w, w + workers, ...
     int32_t dp_tiles;
     // Split-K: effective split count, k-iterations per split, slab mode (1 reduction pass,
-    // 2 last arriver).
-    int32_t splits, chunk, partials;
+    // 2 in the one launch), and whether the splits of a tile share the sum (2, when every
+    // work item has a unit of its own and so all splits of a tile run at once).
+    int32_t splits, chunk, partials, coop;
     // Stream-K tiles merged by a separate fixup pass (every partial segment stores to slot
     // 2 * unit for the unit's first segment, 2 * unit + 1 for its last; nobody waits).
     int32_t sep;

@@ -68,8 +68,11 @@ typedef struct {
                                SK_SPLITK, 1: every split writes an FP32 slab P[j] into the
                                workspace and a second launch (the sk_reduce_splits pass)
                                sums the slabs in split order into C.
-                               SK_SPLITK, 2: as 1, but inside the one launch: the split that
-                               arrives last at a tile sums that tile's slabs into C.
+                               SK_SPLITK, 2: as 1, but inside the one launch. When every
+                               work item gets a unit of its own (tiles * splits <= units),
+                               the splits of a tile wait for each other and each sums a
+                               share of the tile's rows; otherwise the split that arrives
+                               last at a tile sums that tile's slabs into C.
                                SK_STREAMK / SK_HYBRID, 1: separate fixup pass (first page,
                                Case 3): every partial segment, the owner's too, stores its
                                FP32 partial to a fixed slot (2u for unit u's first segment,
