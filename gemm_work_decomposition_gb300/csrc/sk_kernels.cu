@@ -443,8 +443,9 @@ struct Epi {
 
     // Split-K slabs, shared sum: split g.slot's share of this CTA's 128 rows of tile g.tile,
     // rows [j * R, (j + 1) * R) with R = ceil(128 / splits), summed over the slabs in split
-    // order (the reduction pass's order) and stored to C. Warp w takes rows w, w + 4, ...;
-    // lane l takes columns 4l .. 4l + 3 of every 128, so each load covers 512 contiguous bytes.
+    // order (the reduction pass's order) and stored to C. Work items are (row, 4 columns),
+    // consecutive threads on consecutive columns of a row (512 contiguous bytes per warp
+    // load); an item's loads from all slabs go out together, 8 at a time.
     __device__ __forceinline__ void reduce_slab_share(const Seg& g) {
         int32_t trow, tcolumn;
         tile_coords(a.sch, g.tile, &trow, &tcolumn);
@@ -454,35 +455,45 @@ struct Epi {
         const int32_t m0 = trow * (kCtaRows * kCG) + r * kCtaRows;
         const int32_t n0 = tcolumn * kBN;
         const int64_t slab = static_cast<int64_t>(a.M) * a.N;
+        constexpr int kGroups = kBN / 4;  // 4-column groups per row
+        constexpr int kBatch = 8;
+        const int32_t items = (r_end > r_begin ? r_end - r_begin : 0) * kGroups;
 #pragma unroll 1
-        for (int32_t rr = r_begin + (gt >> 5); rr < r_end; rr += 4) {
-            const int32_t gr = m0 + rr;
-            if (gr >= a.M) break;  // rows ascend
+        for (int32_t it = gt; it < items; it += kGroupThreads) {
+            const int32_t gr = m0 + r_begin + it / kGroups;
+            const int32_t gc = n0 + (it % kGroups) * 4;
+            if (gr >= a.M || gc >= a.N) continue;  // N % 8 == 0: each group is all in or out
+            const float* p = a.slabs + static_cast<int64_t>(gr) * a.N + gc;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 1
+            for (int32_t j0 = 0; j0 < a.sch.splits; j0 += kBatch) {
+                float4 x[kBatch];
 #pragma unroll
-            for (int q = 0; q < kBN / 128; ++q) {
-                const int32_t gc = n0 + q * 128 + lane * 4;
-                if (gc >= a.N) break;  // N % 8 == 0: each group of 4 columns is all in or out
-                const float* p = a.slabs + static_cast<int64_t>(gr) * a.N + gc;
-                float4 acc = ld_cg_f4(p);
-#pragma unroll 4
-                for (int32_t j = 1; j < a.sch.splits; ++j) {
-                    const float4 x = ld_cg_f4(p + j * slab);
-                    acc.x += x.x;
-                    acc.y += x.y;
-                    acc.z += x.z;
-                    acc.w += x.w;
+                for (int jj = 0; jj < kBatch; ++jj)
+                    if (j0 + jj < a.sch.splits) x[jj] = ld_cg_f4(p + (j0 + jj) * slab);
+#pragma unroll
+                for (int jj = 0; jj < kBatch; ++jj) {
+                    if (j0 + jj >= a.sch.splits) break;
+                    if (j0 + jj == 0) {
+                        acc = x[0];
+                    } else {
+                        acc.x += x[jj].x;
+                        acc.y += x[jj].y;
+                        acc.z += x[jj].z;
+                        acc.w += x[jj].w;
+                    }
                 }
-                const int64_t off = static_cast<int64_t>(gr) * a.N + gc;
-                if (a.c_bf16) {
-                    __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
-                    __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
-                    uint2 pk;
-                    pk.x = *reinterpret_cast<uint32_t*>(&lo);
-                    pk.y = *reinterpret_cast<uint32_t*>(&hi);
-                    *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.C) + off) = pk;
-                } else {
-                    *reinterpret_cast<float4*>(static_cast<float*>(a.C) + off) = acc;
-                }
+            }
+            const int64_t off = static_cast<int64_t>(gr) * a.N + gc;
+            if (a.c_bf16) {
+                __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+                __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+                uint2 pk;
+                pk.x = *reinterpret_cast<uint32_t*>(&lo);
+                pk.y = *reinterpret_cast<uint32_t*>(&hi);
+                *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.C) + off) = pk;
+            } else {
+                *reinterpret_cast<float4*>(static_cast<float*>(a.C) + off) = acc;
             }
         }
     }
