@@ -40,11 +40,11 @@ WORKLOADS = {"waveq": synth.WAVEQ, "skinny": synth.SKINNY, "large": synth.LARGE,
 # from one ncu capture, keyed by workload/schedule; valid only for the kernel source it
 # was taken on (sha256 of sk_kernels.cu, first 16 hex digits).
 TRAFFIC = {
-    "waveq_2048x2432x4096/hybrid/tile2@148": {"bytes": 36792064 + 2104320, "kernel_sha": "e906c78655be9b7d",
+    "waveq_2048x2432x4096/hybrid/tile2@148": {"bytes": 36792064 + 2155264, "kernel_sha": "6365d48343b9231a",
                                               "profile": "profiles/sk_gemm_kernel_waveq_2048x2432x4096_pair256_hybrid148.md"},
-    "large_8192x8192x8192/dp/tile2@148": {"bytes": 2056086016 + 129275904, "kernel_sha": "e906c78655be9b7d",
+    "large_8192x8192x8192/dp/tile2@148": {"bytes": 2162909952 + 128773632, "kernel_sha": "6365d48343b9231a",
                                           "profile": "profiles/sk_gemm_kernel_large_8192_pair256_dp148_raster.md"},
-    "large_8192x8192x8192/dp/tile2@148/r0s8": {"bytes": 1066447872 + 126214400, "kernel_sha": "e906c78655be9b7d",
+    "large_8192x8192x8192/dp/tile2@148/r0s8": {"bytes": 1057028864 + 126583552, "kernel_sha": "6365d48343b9231a",
                                                "profile": "profiles/sk_gemm_kernel_large_8192_pair256_dp148_raster.md"},
 }
 
@@ -236,10 +236,10 @@ def run_sweep(sk, torch, dev, path, red, flush, stream, peak_tf, dev_sms):
 def run_smallm(sk, torch, dev, flush, stream, dev_sms):
     """The split-K report's shapes (B stored [N,K], FP32 out): M = 96 and 256, N = 512,
     K = 2048. The [splits, M, N] slab chain at s = 2, 4, 8, 16 (every split stores its
-    slab; a reduction pass sums them, two launches), the same slabs summed by the last
-    split to arrive at each tile (one launch), and the owner-wait fixups, timed one GEMM
-    per event pair (L2 flushed before each) and packed 8 back to back (complete GPU time
-    / 8)."""
+    slab; a reduction pass sums them, two launches), the same slabs summed inside the one
+    launch (the splits of a tile share the sum when all run at once, else the last to
+    arrive sums it), and the owner-wait fixups, timed one GEMM per event pair (L2 flushed
+    before each) and packed 8 back to back (complete GPU time / 8)."""
     out = {}
     for w in (synth.SMALLM_96, synth.SMALLM_256):
         A_bits, B_bits = synth.make_inputs(w)
@@ -249,7 +249,7 @@ def run_smallm(sk, torch, dev, flush, stream, dev_sms):
         fl = 2.0 * w.M * w.N * w.K
         rows = {}
         cases = [(f"slabs_s{s}", sk.schedule(sk.SK_SPLITK, s, split_partials=1), dev_sms) for s in (2, 4, 8, 16)]
-        cases += [(f"slabs_last_s{s}", sk.schedule(sk.SK_SPLITK, s, split_partials=2), dev_sms) for s in (2, 4, 8, 16)]
+        cases += [(f"slabs_1launch_s{s}", sk.schedule(sk.SK_SPLITK, s, split_partials=2), dev_sms) for s in (2, 4, 8, 16)]
         cases += [("splitk8_fixup", sk.schedule(sk.SK_SPLITK, 8), dev_sms), ("streamk", sk.schedule(sk.SK_STREAMK), dev_sms),
                   ("streamk_pass", sk.schedule(sk.SK_STREAMK, split_partials=1), dev_sms),
                   ("hybrid", sk.schedule(sk.SK_HYBRID), dev_sms)]

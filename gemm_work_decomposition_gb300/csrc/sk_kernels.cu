@@ -12,11 +12,15 @@
 //               overlaps the MAC loop of the next. For a CTA pair only the leader (rank 0)
 //               issues: tcgen05 cta_group::2 reads A rows and B columns from both CTAs'
 //               shared memory and writes each CTA's rows into that CTA's TMEM;
-//   warps 2..5  epilogue: read the accumulator from TMEM and act on the segment's role:
+//   warps 2..5  epilogue (and warps 6..9 with two epilogue groups): read the accumulator
+//               from TMEM and act on the segment's role:
 //               FULL -> write C; PRODUCER -> store the FP32 partial to its workspace slot
 //               and raise a flag (or add it atomically and bump a counter); OWNER -> wait
 //               for its peers in k order, add their partials, write C (Mental model;
-//               Case 4 reduction modes); SLAB -> write the split's FP32 [M,N] slab.
+//               Case 4 reduction modes). With the separate fixup pass (Case 3) OWNER and
+//               PRODUCER both store to their (unit, first/last) slot and nobody waits.
+//               SLAB -> write the split's FP32 [M,N] slab; with the in-launch sum, count
+//               the arrival and sum a share of the tile (or, arriving last, all of it).
 // Every wait is bounded by a deadline; on expiry the CTA records SK_ETIMEOUT in the
 // workspace status word, unwinds its pipeline and returns.
 #include <cuda.h>
