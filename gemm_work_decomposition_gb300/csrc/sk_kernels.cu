@@ -288,6 +288,34 @@ __device__ __forceinline__ void store_box(const CUtensorMap* tmC, uint32_t stagi
     ++nstore;
 }
 
+// One 4 KiB chunk of this warp's block of a partial slot (32 columns: float4 q of lane l at
+// byte (32 q + l) * 16, the slot's own order, so the chunk is one contiguous copy) through
+// staging buffer nstore % kBoxes, stored by a TMA bulk copy to dst. The lanes' shared stores
+// are 512 contiguous bytes per q, conflict-free.
+template <class F>
+__device__ __forceinline__ void store_partial_chunk(float* dst, uint32_t staging, uint32_t& nstore, F&& value) {
+    const int lane = threadIdx.x & 31;
+    const uint32_t buf = staging + (kBoxes == 1 ? 0u : (nstore & 1u) * 4096u);
+    if (nstore >= static_cast<uint32_t>(kBoxes)) {
+        // The copy issued kBoxes chunks ago used this buffer: wait until the TMA read it.
+        if (lane == 0) bulk_wait_group_read<kBoxes - 1>();
+        __syncwarp();
+    }
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        const float4 x = value(q);
+        st_shared_v4(buf + static_cast<uint32_t>((q * 32 + lane) * 16), __float_as_uint(x.x), __float_as_uint(x.y),
+                     __float_as_uint(x.z), __float_as_uint(x.w));
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+        bulk_store_s2g(dst, buf, 4096u);
+        bulk_commit_group();
+    }
+    ++nstore;
+}
+
 // Store kCols columns of this warp's 32 rows (one row per lane, in registers) with TMA
 // tensor stores through the warp's 4 KiB staging boxes: BF16 C in boxes of 64 columns,
 // FP32 C or slab in boxes of 32 columns, each box 32 rows x 128 bytes in the 128-byte
@@ -621,16 +649,20 @@ struct Epi {
                 const bool atomic = a.atomic && !a.sch.sep;
                 float* blk = block(atomic ? g.peer_begin : g.slot);
 #pragma unroll
-                for (int c = 0; c < kChunks; ++c)
+                for (int c = 0; c < kChunks; ++c) {
+                    if (atomic) {
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        const int i = c * 32 + q * 4;
-                        float* dst = blk + slot_f4(kChunks * p + c, q, lane);
-                        if (atomic)
-                            red_add_v4_f32(dst, v[i], v[i + 1], v[i + 2], v[i + 3]);
-                        else
-                            st_cg_f4(dst, make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]));
+                        for (int q = 0; q < 8; ++q) {
+                            const int i = c * 32 + q * 4;
+                            red_add_v4_f32(blk + slot_f4(kChunks * p + c, q, lane), v[i], v[i + 1], v[i + 2], v[i + 3]);
+                        }
+                    } else {
+                        store_partial_chunk(blk + slot_f4(kChunks * p + c, 0, 0), staging, nstore, [&](int q) {
+                            const int i = c * 32 + q * 4;
+                            return make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+                        });
                     }
+                }
             } else if (g.role == kSlab) {
                 store_slice<kPassCols>(a, tmC, staging, nstore, v, n0 + p * kPassCols, wy, g.slot);
             } else {
@@ -682,9 +714,15 @@ struct Epi {
                 if (gt == 0) a.counters[g.tile * kCG + r] = 0;
             }
         } else if (g.role == kProducer && !a.sch.sep) {
-            // Every epilogue thread's share is stored: publish it. The barrier orders all of
-            // them before one thread's release at GPU scope (release is cumulative). With
-            // the separate fixup pass nobody waits: the pass runs after this launch.
+            // Every epilogue thread's share is stored: publish it. Each warp's bulk copies
+            // must have written the slot (async proxy) before the barrier, which orders all of
+            // them before one thread's release at GPU scope (release is cumulative). With the
+            // separate fixup pass nobody waits: the pass runs after this launch.
+            if (!a.atomic && lane == 0) {
+                bulk_wait_group_all();
+                fence_proxy_async_global();
+            }
+            __syncwarp();
             named_bar_sync(kBar, kGroupThreads);
             if (gt == 0 && !a.skip_signal) {
                 if (a.atomic)

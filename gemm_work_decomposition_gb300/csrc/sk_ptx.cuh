@@ -101,6 +101,12 @@ __device__ __forceinline__ void tma_store_3d(const void* tmap, uint32_t src, int
                  : "memory");
 }
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Copy `bytes` contiguous bytes of shared memory to global memory with the TMA unit (bulk
+// group completion). Both addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_store_s2g(void* gdst, uint32_t ssrc, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(ssrc), "r"(bytes)
+                 : "memory");
+}
 // Wait until at most N of this thread's bulk groups still read their shared-memory source.
 template <int N>
 __device__ __forceinline__ void bulk_wait_group_read() {
