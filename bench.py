@@ -40,11 +40,11 @@ WORKLOADS = {"waveq": synth.WAVEQ, "skinny": synth.SKINNY, "large": synth.LARGE,
 # from one ncu capture, keyed by workload/schedule; valid only for the kernel source it
 # was taken on (sha256 of sk_kernels.cu, first 16 hex digits).
 TRAFFIC = {
-    "waveq_2048x2432x4096/hybrid/tile2@148": {"bytes": 36792064 + 2155264, "kernel_sha": "6365d48343b9231a",
+    "waveq_2048x2432x4096/hybrid/tile2@148": {"bytes": 36786944 + 1604864, "kernel_sha": "ec85194d81863f1c",
                                               "profile": "profiles/sk_gemm_kernel_waveq_2048x2432x4096_pair256_hybrid148.md"},
-    "large_8192x8192x8192/dp/tile2@148": {"bytes": 2162909952 + 128773632, "kernel_sha": "6365d48343b9231a",
+    "large_8192x8192x8192/dp/tile2@148": {"bytes": 2065371392 + 129376768, "kernel_sha": "ec85194d81863f1c",
                                           "profile": "profiles/sk_gemm_kernel_large_8192_pair256_dp148_raster.md"},
-    "large_8192x8192x8192/dp/tile2@148/r0s8": {"bytes": 1057028864 + 126583552, "kernel_sha": "6365d48343b9231a",
+    "large_8192x8192x8192/dp/tile2@148/r0s8": {"bytes": 1032425984 + 125851904, "kernel_sha": "ec85194d81863f1c",
                                                "profile": "profiles/sk_gemm_kernel_large_8192_pair256_dp148_raster.md"},
 }
 

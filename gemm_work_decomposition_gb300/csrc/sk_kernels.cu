@@ -693,7 +693,7 @@ struct Epi {
                 // have arrived, then each sums its share of the rows. The counter goes on to
                 // 2 * splits as the shares finish; the last to finish resets it to zero (by
                 // then every split has passed its wait).
-                if (gt == 0) (void)atom_add_acq_rel_gpu(cnt, 1);
+                if (gt == 0 && !a.skip_signal) (void)atom_add_acq_rel_gpu(cnt, 1);
                 const bool all = wait_flag(cnt, a.sch.splits, deadline, abort_flag);
                 if (named_bar_or(kBar, kGroupThreads, !all)) {
                     record_timeout(a, abort_flag);

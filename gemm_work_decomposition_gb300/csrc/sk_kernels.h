@@ -66,7 +66,8 @@ struct KArgs {
     int32_t c_bf16;
     int32_t atomic;
     int32_t reverse;    // unit order reversed over the CTAs (or CTA pairs)
-    int32_t skip_signal;// producers store but never raise their flag (time-out test)
+    int32_t skip_signal;// producers store but never raise their flag, and slab splits that share
+                        // the sum never count their arrival (time-out tests)
 };
 
 // Launch the persistent GEMM for a.sch's tile shape: a.sch.workers units of a.sch.cg CTAs,

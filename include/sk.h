@@ -184,7 +184,9 @@ typedef struct {
                                      the same units (the page's Case 3 varies arrival order
                                      with a unit permutation) */
     int32_t skip_producer_signal; /* 1: producers store their partials but never raise their
-                                     flag, so every owner's wait runs out (time-out test) */
+                                     flag, so every owner's wait runs out; Split-K slab splits
+                                     that share the sum never count their arrival, so their
+                                     wait runs out too (time-out tests) */
     int64_t timeout_ns;           /* limit of every device-side wait, from kernel start;
                                      0 = the default of 2 s */
     float* dump;                  /* NULL, or a device buffer of tiles * iters * tile_m *

@@ -385,3 +385,23 @@ def test_wait_timeout_reports_status(sk, dev, tile):
     got, guards, _, status = U.gemm(sk, A, B, w.M, w.N, w.K, "NN", sched, DET, 4, "f32", dev, ws)
     assert status == sk.SK_OK and guards
     U.assert_close(got, U.reference(w), "after time-out")
+
+
+@pytest.mark.parametrize("s", [2, 8])
+def test_shared_slab_wait_timeout(sk, dev, dev_sms, s):
+    # Split-K slabs summed in the launch, every split on a unit of its own (small-M: 4 tiles
+    # x s splits): the splits wait for each other before sharing the sum. With their
+    # arrivals suppressed the wait runs out after 50 ms and the kernel records SK_ETIMEOUT;
+    # the context stays usable and the workspace works again once zeroed.
+    w = synth.SMALLM_96
+    sched = sk.schedule(1, s, split_partials=2)
+    A_bits, B_bits = U.inputs(w)
+    A, B = U.to_dev(A_bits, dev), U.to_dev(B_bits, dev)
+    ws = U.new_workspace(sk, w.M, w.N, w.K, dev_sms, sched, DET, dev)
+    _, _, _, status = U.gemm(sk, A, B, w.M, w.N, w.K, "NT", sched, DET, dev_sms, "f32", dev, ws,
+                             skip_producer_signal=1, timeout_ns=50_000_000)
+    assert status == sk.SK_ETIMEOUT
+    ws[0].zero_()
+    got, guards, _, status = U.gemm(sk, A, B, w.M, w.N, w.K, "NT", sched, DET, dev_sms, "f32", dev, ws)
+    assert status == sk.SK_OK and guards
+    U.assert_close(got, U.reference(w), "after time-out")
