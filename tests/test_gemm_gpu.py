@@ -405,3 +405,32 @@ def test_shared_slab_wait_timeout(sk, dev, dev_sms, s):
     got, guards, _, status = U.gemm(sk, A, B, w.M, w.N, w.K, "NT", sched, DET, dev_sms, "f32", dev, ws)
     assert status == sk.SK_OK and guards
     U.assert_close(got, U.reference(w), "after time-out")
+
+
+# --------------------------------------------------------------------------- page, Case 3 claims
+def test_case3_interpreter_claims(sk, dev):
+    # The first page's Case 3 run, at its structure with this library's tiles: 16 tiles x 32
+    # k-iterations (512 x 512 x 2048 with 128 x 128 x 64), Stream-K on 12 and on 40 units,
+    # FP32 output. Claims: Stream-K and data-parallel are both within tolerance but not the
+    # same bits; a fixed-order fixup does not change under reversed unit order (nor between
+    # the owner's in-kernel fixup and the separate fixup pass); atomics with at most 2
+    # contributors per tile equal the fixed-order bits. With up to 4 contributors, atomics
+    # may differ from run to run: only the tolerance is required there.
+    w = synth.Workload("case3", 512, 512, 2048, "NN", "normal", 33, out="f32")
+    ref = U.reference(w)
+    dp, _ = _run(sk, dev, w, sk.schedule(0), DET, 16)
+    sk12, ws12 = _run(sk, dev, w, sk.schedule(2, units=12), DET, 148)
+    U.assert_close(dp, ref, "dp")
+    U.assert_close(sk12, ref, "streamk 12")
+    assert np.count_nonzero(dp != sk12) > 0
+    rev12, _ = _run(sk, dev, w, sk.schedule(2, units=12), DET, 148, reverse_units=1)
+    assert np.array_equal(sk12, rev12)
+    at12, _ = _run(sk, dev, w, sk.schedule(2, units=12), ATOM, 148, reverse_units=1)
+    assert np.array_equal(sk12, at12)
+    plan40 = osch.build_plan(w.M, w.N, w.K, 148, osch.STREAMK, units=40)
+    assert max(c for _, c in osch.tile_rows(plan40)) == 4
+    own40, _ = _run(sk, dev, w, sk.schedule(2, units=40), DET, 148)
+    rev40, _ = _run(sk, dev, w, sk.schedule(2, units=40, split_partials=1), DET, 148, reverse_units=1)
+    assert np.array_equal(own40, rev40)
+    at40, _ = _run(sk, dev, w, sk.schedule(2, units=40), ATOM, 148, reverse_units=1)
+    U.assert_close(at40, ref, "atomic 40")
