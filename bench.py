@@ -39,6 +39,10 @@ WORKLOADS = {"waveq": synth.WAVEQ, "skinny": synth.SKINNY, "large": synth.LARGE,
 # Per-launch DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of the GEMM kernel
 # from one ncu capture, keyed by workload/schedule; valid only for the kernel source it
 # was taken on (sha256 of sk_kernels.cu, first 16 hex digits).
+# Nominal dense BF16 tensor peak and HBM bandwidth of one GB300, for context beside the measured
+# peaks (MEASURED_PEAKS.json) that the roofline fractions use.
+NOMINAL_BF16_TFLOPS = 2250.0
+NOMINAL_HBM_GBS = 8000.0
 TRAFFIC = {
     "waveq_2048x2432x4096/hybrid/tile2@148": {"bytes": 36786944 + 1604864, "kernel_sha": "ec85194d81863f1c",
                                               "profile": "profiles/sk_gemm_kernel_waveq_2048x2432x4096_pair256_hybrid148.md"},
@@ -285,7 +289,7 @@ def run_smallm(sk, torch, dev, flush, stream, dev_sms):
     return out
 
 
-def run_fixups(sk, torch, dev, flush, stream):
+def run_fixups(sk, torch, dev, flush, stream, peak_tf, peak_gbs):
     """Stream-K fixups compared on the skinny shape 512 x 512 x 65536 (many contributors per
     tile) and on the wave-quantized shape: the owner waits and sums in k order, FP32
     atomics, and the separate fixup pass (every partial to its slot, then a second
@@ -297,7 +301,11 @@ def run_fixups(sk, torch, dev, flush, stream):
         B = torch.from_numpy(B_bits.view(np.int16)).view(torch.bfloat16).to(dev)
         C = torch.empty((w.M, w.N), dtype=torch.bfloat16, device=dev)
         fl = 2.0 * w.M * w.N * w.K
-        rows = {}
+        # The shape's roofline time: the larger of its tensor time at the measured peak and the
+        # time to move A, B and C once at the measured HBM bandwidth.
+        hbm_bytes = 2.0 * (w.M * w.K + w.K * w.N) + 2.0 * w.M * w.N
+        bound_us = max(fl / (peak_tf * 1e12), hbm_bytes / (peak_gbs * 1e9)) * 1e6
+        rows = {"roofline_us": bound_us}
         for tile, tname in ((0, "128x128"), (2, "pair256x256")):
             plan = sk.sk_plan(w.M, w.N, w.K, 148, sk.schedule(mode, tile=tile))
             contrib = plan[-sk.SK_MAP_TILE * int(plan[2]) + 1::sk.SK_MAP_TILE]
@@ -319,7 +327,8 @@ def run_fixups(sk, torch, dev, flush, stream):
                 assert sk.sk_status(ws, stream) == sk.SK_OK
                 us = float(np.median([a0.elapsed_time(a1) for a0, a1 in ev])) * 1e3
                 rows[f"{tname}/{name}"] = {"us": us, "tflops": fl / (us / 1e6) / 1e12, "launches": 2 if part else 1,
-                                           "max_contributors_per_tile": int(max(contrib))}
+                                           "max_contributors_per_tile": int(max(contrib)),
+                                           "frac_of_roofline": bound_us / us}
         out[w.name] = rows
     return out
 
@@ -561,7 +570,8 @@ def main():
             table[f"{tile_names[tile]}/{name}@{nsms}"] = {"us_median": med * 1e3, "us_p10": float(np.percentile(t, 10)) * 1e3,
                                        "us_p90": float(np.percentile(t, 90)) * 1e3,
                                        "tflops": flops / (med / 1e3) / 1e12,
-                                       "frac_of_measured_peak": flops / (med / 1e3) / 1e12 / peak_tf}
+                                       "frac_of_measured_peak": flops / (med / 1e3) / 1e12 / peak_tf,
+                                       "frac_of_nominal_peak": flops / (med / 1e3) / 1e12 / NOMINAL_BF16_TFLOPS}
         extras["schedules"] = table
 
         # ---- tail-wave idle SM-time from one traced launch each (outside the timed region):
@@ -680,7 +690,7 @@ def main():
                                             f"({cpu_s:.1f} s, numpy matmul, default BLAS threads)"}
 
         extras["smallm_nt"] = run_smallm(sk, torch, dev, flush, stream, dev_sms)
-        extras["fixups"] = run_fixups(sk, torch, dev, flush, stream)
+        extras["fixups"] = run_fixups(sk, torch, dev, flush, stream, peak_tf, float(peaks["hbm_gbs"]))
         extras["raster_8192"] = run_raster(sk, torch, dev, flush, stream, peak_tf)
 
         if args.sweep:
@@ -711,6 +721,7 @@ def main():
                    "l2": "flushed between timed steps (256 MiB write)", "accumulate": "fp32"},
         "roofline": {"bound": "tensor", "achieved": kernel_tflops, "peak": peak_tf, "unit": "TFLOP/s",
                      "frac": kernel_tflops / peak_tf, "traffic": traffic,
+                     "nominal_peak": NOMINAL_BF16_TFLOPS, "frac_of_nominal": kernel_tflops / NOMINAL_BF16_TFLOPS,
                      "peak_source": f"{peaks_src} bf16 burst", "kernel": "sk_gemm_kernel"},
         "gpu_launches": args.steps * launches_per_step,
         "clocks": clocks.summary(),
