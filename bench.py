@@ -5,9 +5,13 @@ partial-tile fixup, epilogue) over the workload's synthetic BF16 inputs, residen
 Default workload: the wave-quantized GEMM 2048 x 2432 x 4096 (304 tiles of 128 x 128 =
 2 waves + 8 on 148 SMs), BF16 out, the hybrid rule on 148 SMs, computed with 256 x 256
 CTA-pair tiles (80 tiles on 74 pairs: again 2 waves with a short tail); the per-schedule
-table also reports the pages' 128 x 128 tile. Between timed steps a
-256 MiB buffer is written to flush L2 (the inputs, 47 MB, fit in L2). Each step is timed
-with CUDA events on the launching stream; the headline value is TFLOP/s = 2MNK / time.
+table also reports the pages' 128 x 128 tile. The headline steps run back to back on one
+stream, step i on input set i mod R, where the R copies of A, B and C (R = 12 here, 560 MB)
+are at least 4x the L2, so each step reads its operands from HBM. Each launch overlaps the
+one before it (programmatic dependent launch; --overlap 0 turns it off). One pair of CUDA
+events on the launching stream brackets the K steps; the headline value is TFLOP/s = 2MNK
+/ (time / K). `--timing flush` times one launch per event pair with a 256 MiB L2 flush
+before each instead (also reported, as `isolated_launch`).
 
 Prints ONE JSON line (rank 0). `--impl reference` times the CPU oracle (FP64 dot products
 over the BF16 inputs) on a bounded row sample of the same workload instead.
@@ -440,6 +444,11 @@ def main():
     ap.add_argument("--swizzle", type=int, default=0, help="tile-id strips this many tiles deep (0: none)")
     ap.add_argument("--partials", type=int, default=0, choices=[0, 1, 2],
                     help="split_partials of the timed schedule (Split-K slabs; Stream-K/hybrid separate fixup pass)")
+    ap.add_argument("--overlap", type=int, default=1, choices=[0, 1],
+                    help="launch each step overlapped with the one before it (programmatic dependent launch)")
+    ap.add_argument("--timing", default="stream", choices=["stream", "flush"],
+                    help="stream: steps back to back over rotating input sets of at least 4x the L2; "
+                         "flush: one event pair per step with a 256 MiB L2 flush before each")
     ap.add_argument("--no-extras", action="store_true", help="skip the schedule table, e2e and CPU baseline")
     ap.add_argument("--ref-seconds", type=float, default=10.0)
     ap.add_argument("--sweep", default="", help="also write the tile-count sweep (JSON lines) to this file")
@@ -490,9 +499,16 @@ def main():
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    def make(mode_name, nsms, splits=1, tile=args.tile, raster=args.raster, swizzle=args.swizzle):
+    # Rotating input sets for back-to-back timing: enough copies of A, B and C that one pass
+    # over them is at least 4x the L2, so every step finds its operands in HBM, not in L2.
+    l2_bytes = int(getattr(props, "L2_cache_size", 0) or (129 << 20))
+    set_bytes = A.numel() * 2 + B.numel() * 2 + C.numel() * C.element_size()
+    n_sets = max(2, -(-4 * l2_bytes // set_bytes))
+    sets = [(A, B, C)] + [(A.clone(), B.clone(), torch.empty_like(C)) for _ in range(n_sets - 1)]
+
+    def make(mode_name, nsms, splits=1, tile=args.tile, raster=args.raster, swizzle=args.swizzle, overlap=0):
         sch = sk.schedule(modes[mode_name], splits if mode_name == "splitk" else 1, tile=tile, raster=raster,
-                          swizzle=swizzle)
+                          swizzle=swizzle, overlap=overlap)
         nb = sk.sk_workspace_size(w.M, w.N, w.K, nsms, sch, red)
         ws = torch.zeros(nb, dtype=torch.uint8, device=dev)
         return sch, ws, nb
@@ -513,10 +529,30 @@ def main():
             raise RuntimeError(f"device status {sk.sk_strerror(st)}")
         return np.array([s.elapsed_time(e) for s, e in ev])  # ms
 
-    sch, ws, nb = make(args.mode, sms, args.splits)
+    def launch_set(i, sch, ws, nb, nsms):
+        a_, b_, c_ = sets[i % n_sets]
+        sk.sk_gemm(a_, b_, c_, out_code, w.M, w.N, w.K, lay, sch, red, nsms, ws, nb, stream)
+
+    def stream_timed(sch, ws, nb, nsms, steps, warmup):
+        """Mean ms per step of `steps` launches back to back over the rotating sets."""
+        for i in range(warmup):
+            launch_set(i, sch, ws, nb, nsms)
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        t0.record(stream)
+        for i in range(steps):
+            launch_set(i, sch, ws, nb, nsms)
+        t1.record(stream)
+        torch.cuda.synchronize(dev)
+        st = sk.sk_status(ws, stream)
+        if st != sk.SK_OK:
+            raise RuntimeError(f"device status {sk.sk_strerror(st)}")
+        return t0.elapsed_time(t1) / steps
+
+    sch, ws, nb = make(args.mode, sms, args.splits, overlap=args.overlap)
     if args.partials:
         sch = sk.schedule(modes[args.mode], args.splits if args.mode == "splitk" else 1, split_partials=args.partials,
-                          tile=args.tile, raster=args.raster, swizzle=args.swizzle)
+                          tile=args.tile, raster=args.raster, swizzle=args.swizzle, overlap=args.overlap)
         nb = sk.sk_workspace_size(w.M, w.N, w.K, sms, sch, red)
         ws = torch.zeros(nb, dtype=torch.uint8, device=dev)
     plan = sk.sk_plan(w.M, w.N, w.K, sms, sch)
@@ -525,20 +561,30 @@ def main():
     launches_per_step = 2 if args.partials == 1 else 1
 
     # ---- the timed region: K steps, barrier + synchronize on both sides
-    for _ in range(args.warmup):
-        sk.sk_gemm(A, B, C, out_code, w.M, w.N, w.K, lay, sch, red, sms, ws, nb, stream)
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for i in range(args.warmup):
+        launch_set(i, sch, ws, nb, sms)
     clocks = ClockSampler(f"GPU-{props.uuid}")
     clocks.start()
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize(dev)
     wall0 = time.perf_counter()
-    for s, e in ev:
-        flush.zero_()
-        s.record(stream)
-        sk.sk_gemm(A, B, C, out_code, w.M, w.N, w.K, lay, sch, red, sms, ws, nb, stream)
-        e.record(stream)
+    if args.timing == "stream":
+        # One event pair around K launches back to back; step i uses input set i mod n_sets.
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))]
+        ev[0][0].record(stream)
+        for i in range(args.steps):
+            launch_set(i, sch, ws, nb, sms)
+        enqueue_s = time.perf_counter() - wall0
+        ev[0][1].record(stream)
+    else:
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        for s, e in ev:
+            flush.zero_()
+            s.record(stream)
+            sk.sk_gemm(A, B, C, out_code, w.M, w.N, w.K, lay, sch, red, sms, ws, nb, stream)
+            e.record(stream)
+        enqueue_s = time.perf_counter() - wall0
     torch.cuda.synchronize(dev)
     if world > 1:
         dist.barrier()
@@ -548,6 +594,9 @@ def main():
     if status != sk.SK_OK:
         raise RuntimeError(f"device status {sk.sk_strerror(status)}")
     step_ms = np.array([s.elapsed_time(e) for s, e in ev])
+    if red == sk.SK_DETERMINISTIC and args.timing == "stream":  # every set's C is the same, bit for bit
+        for _, _, c_ in sets[1:min(n_sets, max(args.warmup, args.steps))]:
+            assert torch.equal(c_, C)
     total_ms = max_over_ranks(float(step_ms.sum()), dist if world > 1 else None, dev)
     ms_per_step = total_ms / args.steps
     value = job_tflops(world, flops, args.steps, total_ms)
@@ -573,6 +622,28 @@ def main():
                                        "frac_of_measured_peak": flops / (med / 1e3) / 1e12 / peak_tf,
                                        "frac_of_nominal_peak": flops / (med / 1e3) / 1e12 / NOMINAL_BF16_TFLOPS}
         extras["schedules"] = table
+
+        # ---- the same launches back to back over the rotating sets, without and with the
+        # overlapped launch: what a stream of GEMMs pays per step beyond the kernel itself.
+        b2b = {}
+        for tile, name, nsms in ((2, "hybrid", 148), (2, "dp", 148), (2, "streamk", 148), (0, "hybrid", 148),
+                                 (2, "hybrid", dev_sms)):
+            mname = "splitk" if name.startswith("splitk") else name
+            row = {}
+            for ov in (0, 1):
+                s2, ws2, nb2 = make(mname, nsms, 2, tile, overlap=ov)
+                ms = stream_timed(s2, ws2, nb2, nsms, 400, 24)
+                row[f"overlap{ov}"] = {"us": ms * 1e3, "tflops": flops / (ms / 1e3) / 1e12,
+                                       "frac_of_measured_peak": flops / (ms / 1e3) / 1e12 / peak_tf}
+            b2b[f"{tile_names[tile]}/{name}@{nsms}"] = row
+        extras["back_to_back"] = {"sets": n_sets, "set_mb": set_bytes / 1e6, "steps": 400, "table": b2b}
+
+        # ---- the headline schedule timed one launch at a time, L2 flushed before each
+        iso = timed(sch, ws, nb, sms, 200, 10)
+        extras["isolated_launch"] = {"us_median": float(np.median(iso)) * 1e3, "us_mean": float(iso.mean()) * 1e3,
+                                     "tflops_median": flops / (float(np.median(iso)) / 1e3) / 1e12,
+                                     "how": "one event pair per launch, 256 MiB L2 flush before each; includes the "
+                                            "launch latency that back-to-back steps hide"}
 
         # ---- tail-wave idle SM-time from one traced launch each (outside the timed region):
         # sum over SMs of (last SM's end - this SM's end), DP against the headline schedule.
@@ -718,7 +789,11 @@ def main():
                    "raster": "along_n" if args.raster == 0 else "along_m", "swizzle": args.swizzle,
                    "tiles": int(plan[2]), "iters": int(plan[3]), "workers": int(plan[4]),
                    "resolved_mode": int(plan[1]), "sk_tiles": int(plan[5]), "sk_units": int(plan[6]),
-                   "l2": "flushed between timed steps (256 MiB write)", "accumulate": "fp32"},
+                   "overlap": args.overlap, "timing": args.timing,
+                   "l2": (f"inputs larger than L2: {n_sets} rotating sets of A, B and C ({n_sets * set_bytes / 1e6:.0f} MB, "
+                          f">= 4x the {l2_bytes / 1e6:.0f} MB L2), launched back to back"
+                          if args.timing == "stream" else "flushed between timed steps (256 MiB write)"),
+                   "accumulate": "fp32"},
         "roofline": {"bound": "tensor", "achieved": kernel_tflops, "peak": peak_tf, "unit": "TFLOP/s",
                      "frac": kernel_tflops / peak_tf, "traffic": traffic,
                      "nominal_peak": NOMINAL_BF16_TFLOPS, "frac_of_nominal": kernel_tflops / NOMINAL_BF16_TFLOPS,
@@ -726,6 +801,7 @@ def main():
         "gpu_launches": args.steps * launches_per_step,
         "clocks": clocks.summary(),
         "wall_s_timed_region": wall,
+        "host_enqueue_us_per_step": enqueue_s / args.steps * 1e6,
     }
     line.update(extras)
     print(json.dumps(line), flush=True)

@@ -38,7 +38,7 @@ SK_NOALLOC_SCRATCH_BYTES = 16 << 20
 class sk_schedule(ctypes.Structure):
     _fields_ = [("mode", ctypes.c_int32), ("splits", ctypes.c_int32), ("units", ctypes.c_int32),
                 ("min_iters", ctypes.c_int32), ("split_partials", ctypes.c_int32), ("tile", ctypes.c_int32),
-                ("raster", ctypes.c_int32), ("swizzle", ctypes.c_int32)]
+                ("raster", ctypes.c_int32), ("swizzle", ctypes.c_int32), ("overlap", ctypes.c_int32)]
 
 
 class sk_debug_opts(ctypes.Structure):
@@ -53,8 +53,8 @@ class SkError(RuntimeError):
 
 
 def schedule(mode: int, splits: int = 1, units: int = 0, min_iters: int = 0, split_partials: int = 0,
-             tile: int = 0, raster: int = 0, swizzle: int = 0) -> sk_schedule:
-    return sk_schedule(mode, splits, units, min_iters, split_partials, tile, raster, swizzle)
+             tile: int = 0, raster: int = 0, swizzle: int = 0, overlap: int = 0) -> sk_schedule:
+    return sk_schedule(mode, splits, units, min_iters, split_partials, tile, raster, swizzle, overlap)
 
 
 _lib = None

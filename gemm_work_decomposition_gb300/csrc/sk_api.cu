@@ -73,6 +73,7 @@ int32_t make_sched(int32_t M, int32_t N, int32_t K, int32_t num_sms, const sk_sc
     int32_t tm = 0, tn = 0, cg = 0;
     if (!tile_shape(s.tile, &tm, &tn, &cg)) return SK_EINVAL;
     if (s.raster < 0 || s.raster > 1 || s.swizzle < 0 || s.swizzle > 256) return SK_EINVAL;
+    if (s.overlap < 0 || s.overlap > 1) return SK_EINVAL;
     const int64_t tiles_n = (static_cast<int64_t>(N) + tn - 1) / tn;
     const int64_t tiles = ((static_cast<int64_t>(M) + tm - 1) / tm) * tiles_n;
     const int64_t iters = (static_cast<int64_t>(K) + kBlkK - 1) / kBlkK;
@@ -92,6 +93,7 @@ int32_t make_sched(int32_t M, int32_t N, int32_t K, int32_t num_sms, const sk_sc
     o.tiles_m = static_cast<int32_t>(tiles / tiles_n);
     o.raster = s.raster;
     o.swizzle = s.swizzle;
+    o.overlap = s.overlap;
 
     int32_t mode = s.mode;
     if (mode == SK_HYBRID) {
@@ -398,7 +400,8 @@ int32_t sk_gemm_debug(const void* A, const void* B, void* C, sk_dtype c_dtype, i
         return SK_ECUDA;
     }
     if (sch.partials == 1) {
-        if (launch_reduce(a.slabs, C, a.c_bf16, sch.splits, static_cast<int64_t>(M) * N, dev_sms, st) !=
+        if (launch_reduce(a.slabs, C, a.c_bf16, sch.splits, static_cast<int64_t>(M) * N, dev_sms,
+                          sch.overlap != 0, st) !=
             cudaSuccess) {
             cudaGetLastError();
             return SK_ECUDA;
@@ -426,7 +429,7 @@ int32_t sk_reduce_splits(const float* P, void* C, sk_dtype c_dtype, int32_t spli
     if (!P || !C || !aligned(P, 16) || !aligned(C, 16)) return SK_EINVAL;
     int dev_sms = 0, max_units[4];
     if (device_info(&dev_sms, max_units) != cudaSuccess) return SK_ECUDA;
-    if (launch_reduce(P, C, c_dtype == SK_BF16 ? 1 : 0, splits, mn, dev_sms, static_cast<cudaStream_t>(stream)) !=
+    if (launch_reduce(P, C, c_dtype == SK_BF16 ? 1 : 0, splits, mn, dev_sms, false, static_cast<cudaStream_t>(stream)) !=
         cudaSuccess) {
         cudaGetLastError();
         return SK_ECUDA;

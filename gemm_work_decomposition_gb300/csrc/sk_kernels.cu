@@ -819,7 +819,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int units = static_cast<int>(gridDim.x) / kCG;
     const int cid = static_cast<int>(blockIdx.x) / kCG;
     const int unit = args.reverse ? units - 1 - cid : cid;
-    const uint64_t deadline = globaltimer() + args.timeout_ns;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S::kStages; ++s) {
@@ -845,13 +844,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         cluster_sync();
     else
         __syncthreads();
-    if (args.trace && threadIdx.x == 0) args.trace[static_cast<int64_t>(blockIdx.x) * kTraceWords] = globaltimer();
 
-    // Warps 0 and 1 reconverge before the exit barrier: a CTA barrier counts a warp once
-    // any of its threads arrives, so all 32 lanes must arrive together.
+    // Everything above touches only this CTA's own shared memory and the kernel parameters,
+    // so under an overlapped launch it runs while the previous kernel on the stream is
+    // still finishing. Every thread that reads or writes global memory (A, B, C, the
+    // workspace, the debug buffers) first waits for that kernel; TMEM is allocated before
+    // the wait. Every thread signals the next overlapped launch once it is past its wait, so
+    // that launch may begin when all of this grid's CTAs are.
     uint32_t tmem_base = 0;
     if (warp == 0) {
-        if (lane == 0) run_producer<kNT, kCG, kBN>(args, &tmA, &tmB, sm, unit, rank, deadline, abort_flag);
+        grid_dep_wait();
+        grid_dep_launch();
+        const uint64_t deadline = globaltimer() + args.timeout_ns;  // wait limits count from here
+        if (lane == 0) {
+            if (args.trace) args.trace[static_cast<int64_t>(blockIdx.x) * kTraceWords] = globaltimer();
+            run_producer<kNT, kCG, kBN>(args, &tmA, &tmB, sm, unit, rank, deadline, abort_flag);
+        }
+        // Warps 0 and 1 reconverge before the exit barrier: a CTA barrier counts a warp once
+        // any of its threads arrives, so all 32 lanes must arrive together.
         __syncwarp();
     } else if (warp == 1) {
         if (kCG == 1) {
@@ -870,12 +880,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         tc_fence_after();
         tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_holder);
+        grid_dep_wait();
+        grid_dep_launch();
+        const uint64_t deadline = globaltimer() + args.timeout_ns;
         if (lane == 0 && rank == 0) run_mma<kNT, kCG, kBN>(args, sm, tmem_base, unit, deadline, abort_flag);
         __syncwarp();
     } else {
         named_bar_sync(2, 32 + kEpiThreads);
         tc_fence_after();
         tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_holder);
+        grid_dep_wait();
+        grid_dep_launch();
+        const uint64_t deadline = globaltimer() + args.timeout_ns;
         run_epilogue<kCG, kBN>(args, &tmC, &tmD, sm, tmem_base, unit, rank, deadline, abort_flag, last_flag);
     }
 
@@ -901,6 +917,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 // once). Pair shapes launch as clusters of 2 without that attribute: the host has checked
 // that every pair fits on the device at once (cudaOccupancyMaxActiveClusters), and an
 // owner only ever waits for producer segments that run first in their own units.
+// An overlapped launch (sch.overlap) adds programmatic stream serialization and, for the
+// one-CTA shapes, relies on the same host-side residency check instead of the cooperative
+// attribute. Its CTAs can only start once every CTA of the previous overlapped grid is past
+// its own wait (each issues grid_dep_launch there), and they hold SMs only where the
+// previous kernel's CTAs have left; once that kernel completes, all of this grid fits.
 template <bool kNT, int kCG, int kBN>
 cudaError_t launch_shape(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
                          const CUtensorMap& tmD, const KArgs& a, cudaStream_t stream) {
@@ -912,7 +933,11 @@ cudaError_t launch_shape(const CUtensorMap& tmA, const CUtensorMap& tmB, const C
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
     int n = 0;
-    if (kCG == 1) {
+    if (a.sch.overlap) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    } else if (kCG == 1) {
         attr[n].id = cudaLaunchAttributeCooperative;
         attr[n].val.cooperative = 1;
         ++n;

@@ -71,7 +71,8 @@ struct KArgs {
 };
 
 // Launch the persistent GEMM for a.sch's tile shape: a.sch.workers units of a.sch.cg CTAs,
-// cooperative where the device allows it. Returns a cudaError_t.
+// cooperative where the device allows it, or overlapped with the kernel before it on the
+// stream (programmatic stream serialization) when a.sch.overlap. Returns a cudaError_t.
 // tmC: where segments store — C [M,N] (FP32 or BF16) in boxes of 32 rows x 128 bytes, or
 // for Split-K slabs the FP32 [splits][M][N] map in boxes of 1 x 32 rows x 32 columns.
 // tmD: the C map (the last split of a tile writes the sum of the slabs there).
@@ -82,10 +83,12 @@ cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CU
 cudaError_t prepare_device(int num_sms, int* max_units);
 // Separate fixup pass for a plan with sch.sep: every Stream-K tile covered by more than one
 // unit gets C = its partial slots summed in k order (FP32), stored as BF16 or FP32.
+// Overlapped with the GEMM before it (programmatic stream serialization) when sch.overlap.
 cudaError_t launch_fixup(const Sched& sch, const float* slots, void* C, int32_t M, int32_t N, int c_bf16, int num_sms,
                          cudaStream_t stream);
-// C = sum_j P[j] in j order, FP32 -> c_bf16 ? BF16 : FP32. mn % 4 == 0.
-cudaError_t launch_reduce(const float* P, void* C, int c_bf16, int splits, int64_t mn, int num_sms,
+// C = sum_j P[j] in j order, FP32 -> c_bf16 ? BF16 : FP32. mn % 4 == 0. `overlap`: as for
+// launch_fixup.
+cudaError_t launch_reduce(const float* P, void* C, int c_bf16, int splits, int64_t mn, int num_sms, bool overlap,
                           cudaStream_t stream);
 
 }  // namespace sk

@@ -7,6 +7,7 @@
 #include <stdint.h>
 
 #include "sk_kernels.h"
+#include "sk_ptx.cuh"
 
 namespace sk {
 namespace {
@@ -14,6 +15,8 @@ namespace {
 // --------------------------------------------------------------------------- Split-K slab reduction
 __global__ void __launch_bounds__(256)
     sk_reduce_kernel(const float* __restrict__ P, void* __restrict__ C, int c_bf16, int splits, int64_t n4) {
+    grid_dep_wait();  // an overlapped launch reads P only once the GEMM that wrote it is done
+    grid_dep_launch();
     const float4* P4 = reinterpret_cast<const float4*>(P);
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4; i += stride) {
@@ -51,6 +54,8 @@ __global__ void __launch_bounds__(256)
 __global__ void __launch_bounds__(256)
     sk_fixup_kernel(const Sched sch, const float* __restrict__ slots, void* __restrict__ C, int32_t M, int32_t N,
                     int c_bf16) {
+    grid_dep_wait();  // as in sk_reduce_kernel
+    grid_dep_launch();
     const int lane = threadIdx.x & 31;
     const int chunks = sch.tile_n / 32;
     const int64_t per_tile = static_cast<int64_t>(sch.cg) * 4 * chunks * 4;
@@ -122,17 +127,33 @@ __global__ void __launch_bounds__(256)
     }
 }
 
+// A launch of `blocks` x 256 threads on `stream`, with programmatic stream serialization
+// when `overlap` is set (the kernels above wait for the previous kernel before any access).
+cudaLaunchConfig_t pass_config(int64_t blocks, cudaStream_t stream, bool overlap, cudaLaunchAttribute* attr) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(blocks), 1, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = overlap ? 1 : 0;
+    return cfg;
+}
+
 }  // namespace
 
-cudaError_t launch_reduce(const float* P, void* C, int c_bf16, int splits, int64_t mn, int num_sms,
+cudaError_t launch_reduce(const float* P, void* C, int c_bf16, int splits, int64_t mn, int num_sms, bool overlap,
                           cudaStream_t stream) {
     const int64_t n4 = mn / 4;
     int64_t blocks = (n4 + 255) / 256;
     const int64_t cap = static_cast<int64_t>(num_sms) * 8;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
-    sk_reduce_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(P, C, c_bf16, splits, n4);
-    return cudaGetLastError();
+    cudaLaunchAttribute attr[1];
+    const cudaLaunchConfig_t cfg = pass_config(blocks, stream, overlap, attr);
+    return cudaLaunchKernelEx(&cfg, sk_reduce_kernel, P, C, c_bf16, splits, n4);
 }
 
 cudaError_t launch_fixup(const Sched& sch, const float* slots, void* C, int32_t M, int32_t N, int c_bf16, int num_sms,
@@ -142,8 +163,9 @@ cudaError_t launch_fixup(const Sched& sch, const float* slots, void* C, int32_t 
     int64_t blocks = (warps + 7) / 8;
     const int64_t cap = static_cast<int64_t>(num_sms) * 8;
     if (blocks > cap) blocks = cap;
-    sk_fixup_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(sch, slots, C, M, N, c_bf16);
-    return cudaGetLastError();
+    cudaLaunchAttribute attr[1];
+    const cudaLaunchConfig_t cfg = pass_config(blocks, stream, sch.overlap != 0, attr);
+    return cudaLaunchKernelEx(&cfg, sk_fixup_kernel, sch, slots, C, M, N, c_bf16);
 }
 
 }  // namespace sk

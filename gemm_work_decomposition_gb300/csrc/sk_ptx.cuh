@@ -312,6 +312,14 @@ __device__ __forceinline__ void red_add_v4_f32(float* p, float a, float b, float
 __device__ __forceinline__ void fence_proxy_async_global() {
     asm volatile("fence.proxy.async.global;" ::: "memory");
 }
+// Programmatic dependent launch (PTX griddepcontrol, sm_90 and later). A kernel launched
+// with programmatic stream serialization may start while the kernel before it on the
+// stream is still running; grid_dep_wait blocks the calling thread until that kernel has
+// completed and its memory operations are visible. Without that launch attribute both
+// instructions do nothing. grid_dep_launch lets the next such launch begin once every
+// CTA of this grid has issued it or exited.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(int32_t* p, int32_t v) {
     uint32_t old;
     asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");

@@ -48,6 +48,9 @@ struct Sched {
     // Rasterization of the tile grid: tile ids walk along N (0) or M (1), in strips of
     // `swizzle` tiles across the walk (0 or 1: no strips).
     int32_t tiles_m, raster, swizzle;
+    // Launch option, not part of the plan: overlap each launch with the kernel before it on
+    // the stream (programmatic dependent launch).
+    int32_t overlap;
 };
 
 // (tile_m, tile_n, CTAs per tile) of each sk_tile value; false for an unknown value.

@@ -88,6 +88,18 @@ typedef struct {
                                cut into strips w tiles deep, and ids fill one strip at a
                                time, across its w tiles first (tiles that run together
                                then share A and B panels in L2) */
+    int32_t overlap;        /* launch option; the plan is the same either way. 0: each
+                               launch starts once the work before it on the stream is
+                               done. 1: programmatic dependent launch (CUDA): the GEMM's
+                               CTAs may start, initialise their barriers and allocate
+                               tensor memory while the kernel before it on the stream is
+                               still running; every thread waits for that kernel to
+                               complete (its writes visible) before it touches global
+                               memory, so the result is the same. The reduction or fixup
+                               pass of split_partials = 1 overlaps the GEMM the same way.
+                               Each device-side wait limit then counts from that wait.
+                               The one-CTA tiles then launch without the cooperative
+                               attribute, after the same residency check as the pairs. */
 } sk_schedule;
 
 #define SK_OK          0
@@ -199,8 +211,9 @@ typedef struct {
                                      ns, layout below */
 } sk_debug_opts;
 
-/* Per-CTA trace record (sk_debug_opts.trace), indexed by blockIdx: [0] start (after set-up),
- * [1] end (before the exit barrier), [2] segments walked, [3] reserved; then for segment i
+/* Per-CTA trace record (sk_debug_opts.trace), indexed by blockIdx: [0] start (after set-up
+ * and, for an overlapped launch, after the wait for the previous kernel), [1] end (before
+ * the exit barrier), [2] segments walked, [3] reserved; then for segment i
  * < SK_TRACE_SEGS, at 4 + 4 * i: [0] MMA issue of its first k-iteration (leader CTA only),
  * [1] MMA commit of its last, [2] epilogue has the accumulator, [3] epilogue done (after the
  * fixup and the stores). Unused words stay as the caller left them. */

@@ -107,6 +107,20 @@ def test_plan_rasterization(sk):
             sk.sk_plan(128, 128, 64, 4, sk.schedule(0, raster=bad[0], swizzle=bad[1]))
 
 
+def test_overlap_is_a_launch_option(sk):
+    # The overlapped launch changes how the kernels are launched, not what they compute:
+    # the plan and the workspace size are the same either way.
+    for M, N, K in [(2048, 2432, 4096), (512, 512, 65536), (96, 512, 2048), (300, 264, 520)]:
+        for tile in (0, 2):
+            for mode, splits, partials in ((S.DP, 1, 0), (S.STREAMK, 1, 0), (S.HYBRID, 1, 1), (S.SPLITK, 2, 1),
+                                           (S.SPLITK, 3, 2)):
+                a = sk.schedule(mode, splits, split_partials=partials, tile=tile)
+                b = sk.schedule(mode, splits, split_partials=partials, tile=tile, overlap=1)
+                assert np.array_equal(sk.sk_plan(M, N, K, 148, a), sk.sk_plan(M, N, K, 148, b))
+                for red in (0, 1):
+                    assert sk.sk_workspace_size(M, N, K, 148, a, red) == sk.sk_workspace_size(M, N, K, 148, b, red)
+
+
 def test_plan_toy_units_override(sk):
     a = _cmp(sk, 128, 640, 256, 148, S.STREAMK, units=4)
     b = _cmp(sk, 128, 640, 256, 4, S.STREAMK)
@@ -166,6 +180,8 @@ def test_errors(sk):
         (128, 128, 128, 4, sk.schedule(sk.SK_DP, 1, -1)),
         (128, 128, 128, 4, sk.schedule(sk.SK_DP, 1, 0, 0, 0, 4)),      # unknown tile shape
         (128, 128, 128, 1, sk.schedule(sk.SK_DP, 1, 0, 0, 0, 1)),      # a pair needs 2 SMs
+        (128, 128, 128, 4, sk.schedule(sk.SK_DP, overlap=2)),          # overlap is 0 or 1
+        (128, 128, 128, 4, sk.schedule(sk.SK_DP, overlap=-1)),
     ]
     for M, N, K, sms, sch in bad:
         with pytest.raises(sk.SkError) as e:

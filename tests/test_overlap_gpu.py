@@ -1,0 +1,147 @@
+"""Overlapped launches (sk_schedule.overlap = 1: programmatic dependent launch) against the
+same calls launched without overlap. Each overlapped kernel sets up while the kernel
+before it on the stream finishes, and must wait for it before touching global memory, so
+every result must equal the non-overlapped one bit for bit:
+  - chains where each GEMM reads the output of the GEMM just before it;
+  - inputs rewritten by a PyTorch kernel right before each GEMM;
+  - back-to-back calls with different inputs that share one workspace (turnstile flags,
+    slab arrival counters, atomic tiles and fixup slots carried from call to call).
+"""
+import numpy as np
+import pytest
+import torch
+
+import synth
+
+from . import gpu_util as U
+
+pytestmark = pytest.mark.gpu
+
+DET, ATOM = 0, 1
+
+
+@pytest.fixture(scope="module")
+def sk():
+    import __graft_entry__ as ge
+    ge.build()
+    import gemm_work_decomposition_gb300 as pkg
+    return pkg
+
+
+@pytest.fixture(scope="module")
+def dev():
+    assert torch.cuda.is_available()
+    return torch.device("cuda:0")
+
+
+SCHEDULES = [
+    ("dp", dict(mode=0)),
+    ("splitk3", dict(mode=1, splits=3)),
+    ("streamk", dict(mode=2)),
+    ("hybrid", dict(mode=3)),
+    ("slabs2", dict(mode=1, splits=2, split_partials=1)),
+    ("slabs3_one_launch", dict(mode=1, splits=3, split_partials=2)),
+    ("streamk_sep", dict(mode=2, split_partials=1)),
+]
+
+
+def _bf16(bits, dev):
+    return U.to_dev(bits, dev)
+
+
+def _chain(sk, dev, X0, Ws, M, K, kw, overlap, sms):
+    """X_{i+1} = X_i . W_i (NN, BF16 out) for every W_i, all launched back to back."""
+    sched = sk.schedule(overlap=overlap, **kw)
+    nbytes = sk.sk_workspace_size(M, K, K, sms, sched, DET)
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    xs = [X0]
+    # Every output starts as a sentinel so that a read ahead of its producer shows.
+    outs = [torch.full((M, K), U.SENTINEL, dtype=torch.bfloat16, device=dev) for _ in Ws]
+    torch.cuda.synchronize(dev)
+    for W, Y in zip(Ws, outs):
+        sk.sk_gemm(xs[-1], W, Y, sk.SK_BF16, M, K, K, sk.SK_NN, sched, DET, sms, ws, nbytes, stream)
+        xs.append(Y)
+    assert sk.sk_status(ws, stream) == sk.SK_OK
+    return [y.float().cpu().numpy() for y in outs]
+
+
+@pytest.mark.parametrize("tile", [0, 2])
+@pytest.mark.parametrize("name,kw", SCHEDULES)
+def test_overlapped_chain_equals_serial(sk, dev, name, kw, tile):
+    # 640 x 768 x 768 (ragged in M for both tile shapes), five dependent GEMMs: the grids
+    # are small enough that an overlapped GEMM's CTAs all fit beside the running one, so a
+    # missing wait would read its input before it is written.
+    M, K = 640, 768
+    X0 = _bf16(synth.make_inputs(synth.Workload("chain_x", M, K, K, seed=40))[0], dev)
+    Ws = [_bf16(synth.make_inputs(synth.Workload("chain_w", K, K, K, seed=41 + i))[1], dev) for i in range(5)]
+    kw = dict(kw, tile=tile)
+    ref = _chain(sk, dev, X0, Ws, M, K, kw, 0, 148)
+    got = _chain(sk, dev, X0, Ws, M, K, kw, 1, 148)
+    for i, (g, r) in enumerate(zip(got, ref)):
+        assert not np.any(r == U.SENTINEL)
+        assert np.array_equal(g, r), (name, tile, i)
+
+
+@pytest.mark.parametrize("tile", [0, 2])
+def test_overlapped_after_torch_kernel(sk, dev, tile):
+    # A PyTorch elementwise kernel rewrites A right before each overlapped GEMM; each GEMM
+    # must see that step's A.
+    M, N, K = 512, 640, 1024
+    srcs = [_bf16(synth.make_inputs(synth.Workload("torch_a", M, N, K, seed=50 + i))[0], dev) for i in range(6)]
+    B = _bf16(synth.make_inputs(synth.Workload("torch_b", M, N, K, seed=49))[1], dev)
+    A = torch.empty_like(srcs[0])
+    stream = torch.cuda.current_stream(dev)
+
+    def run(overlap):
+        sched = sk.schedule(mode=3, tile=tile, overlap=overlap)
+        nbytes = sk.sk_workspace_size(M, N, K, 148, sched, DET)
+        ws = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
+        C = torch.empty((M, N), dtype=torch.float32, device=dev)
+        outs = []
+        for s in srcs:
+            torch.mul(s, 1.0, out=A)
+            sk.sk_gemm(A, B, C, sk.SK_F32, M, N, K, sk.SK_NN, sched, DET, 148, ws, nbytes, stream)
+            outs.append(C.clone())
+        assert sk.sk_status(ws, stream) == sk.SK_OK
+        return [o.cpu().numpy() for o in outs]
+
+    ref, got = run(0), run(1)
+    for i, (g, r) in enumerate(zip(got, ref)):
+        assert np.array_equal(g, r), i
+    assert not np.array_equal(ref[0], ref[1])
+
+
+@pytest.mark.parametrize("red", [DET, ATOM])
+@pytest.mark.parametrize("tile", [0, 2])
+@pytest.mark.parametrize("name,kw", [("streamk", dict(mode=2)), ("hybrid", dict(mode=3)),
+                                     ("slabs3_one_launch", dict(mode=1, splits=3, split_partials=2)),
+                                     ("streamk_sep", dict(mode=2, split_partials=1))])
+def test_overlapped_back_to_back_shared_workspace(sk, dev, name, kw, tile, red):
+    # Twelve calls over three input sets, one workspace, no synchronisation in between:
+    # each call's flags, counters and partial tiles are reused by the next. Integer inputs
+    # keep every sum exact, so the atomic reduction must match exactly too.
+    M, N, K, sms = 768, 1024, 2048, 148
+    sets = []
+    for i in range(3):
+        a, b = synth.small_int_inputs(M, N, K, "NN", 60 + i)
+        sets.append((_bf16(a, dev), _bf16(b, dev)))
+    stream = torch.cuda.current_stream(dev)
+
+    def run(overlap):
+        sched = sk.schedule(tile=tile, overlap=overlap, **kw)
+        nbytes = sk.sk_workspace_size(M, N, K, sms, sched, red)
+        ws = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
+        outs = [torch.full((M, N), U.SENTINEL, dtype=torch.float32, device=dev) for _ in range(12)]
+        torch.cuda.synchronize(dev)
+        for i, C in enumerate(outs):
+            A, B = sets[i % 3]
+            sk.sk_gemm(A, B, C, sk.SK_F32, M, N, K, sk.SK_NN, sched, red, sms, ws, nbytes, stream)
+        assert sk.sk_status(ws, stream) == sk.SK_OK
+        return [o.cpu().numpy() for o in outs]
+
+    ref, got = run(0), run(1)
+    for i in range(12):
+        assert np.array_equal(got[i], ref[i % 3]), i
+        assert np.array_equal(ref[i], ref[i % 3]), i
+    assert not np.array_equal(ref[0], ref[1])
