@@ -50,7 +50,23 @@ struct Smem {
     __device__ uint32_t tempty(int b) const { return base + S::kSmemBarOff + 8 * (2 * S::kStages + 2 + b); }
     __device__ uint32_t done() const { return base + S::kSmemBarOff + 8 * (2 * S::kStages + 4); }
     __device__ uint32_t tready() const { return base + S::kSmemBarOff + 8 * (2 * S::kStages + 5); }
+    // Epilogue warp w's two barriers for partials fetched into the ring by bulk copies.
+    __device__ uint32_t pload(int w, int b) const { return base + S::kSmemBarOff + 256 + 8 * (2 * w + b); }
 };
+
+// Ring bytes an epilogue warp may use once the unit's MAC loop is over (the ring split four ways).
+constexpr uint32_t kWarpRingBytes = kRingBytes / 4;
+// One pass of an epilogue warp's block of a partial (32 rows x kPassCols FP32): the unit of the
+// bulk copies that bring a deterministic owner's peer partials into the ring.
+constexpr uint32_t kPartBytes = 32u * kPassCols * 4u;
+static_assert(2 * kPartBytes + 4 * 4096 <= kWarpRingBytes && 12 * 4096 <= kWarpRingBytes, "ring quarter");
+// Shared-memory word that hands the first partial copies of the unit's last (owner) segment
+// from the producer warp to the epilogue: 0 open; kPrefetchClosed once the epilogue has given
+// up on the segment (the producer must not start copies any more); kPrefetchIssued + k once
+// the producer started k copies per epilogue warp.
+constexpr int kPrefetchClosed = 1;
+constexpr int kPrefetchIssued = 2;
+
 
 __device__ __forceinline__ void record_timeout(const KArgs& a, volatile int* abort_flag) {
     *abort_flag = 1;
@@ -70,19 +86,57 @@ __device__ __forceinline__ int32_t seg_k(const Seg& g, bool rev, int32_t i) {
 }
 
 // --------------------------------------------------------------------------- warp 0
+// The unit's last segment g is a deterministic owner's (its peers' partials are summed in k
+// order by the epilogue): acquire the peers' flags; once every load of the unit (`issued` of
+// them) has been consumed by the MAC loop, the ring is free, so start the first one or two
+// partial copies of each epilogue warp into its ring quarter, while the epilogue is still
+// storing the segment before. Returns false when a wait gave up.
+template <int kCG, int kBN>
+__device__ bool prefetch_partials(const KArgs& a, const Smem<Shape<kCG, kBN>>& sm, const Seg& g, uint32_t rank,
+                                  uint32_t issued, uint64_t deadline, volatile int* abort_flag, int* prefetch) {
+    using S = Shape<kCG, kBN>;
+    // Indices outside the workspace: leave the segment to the epilogue, which reports them.
+    if (g.tile < 0 || g.tile >= a.sch.tiles || g.peer_begin < 0 || g.n_peers < 1 ||
+        g.peer_begin + g.n_peers > a.sch.n_slots)
+        return true;
+    for (int32_t pi = 0; pi < g.n_peers; ++pi) {
+        const int32_t* f = a.flags + (g.peer_begin + pi) * kCG + static_cast<int32_t>(rank);
+        for (uint32_t n = 0; ld_acquire_gpu(f) < 1; ++n) {
+            if ((n & 15u) == 15u && (*abort_flag || globaltimer() > deadline)) return false;
+            __nanosleep(32);
+        }
+    }
+    // Load `pos` went to stage pos % kStages; its consumption completes that stage's empty
+    // phase pos / kStages (as in the loop above, these are the only phases still open).
+    const uint32_t tail = issued < static_cast<uint32_t>(S::kStages) ? issued : S::kStages;
+    for (uint32_t i = 0; i < tail; ++i) {
+        const uint32_t pos = issued - 1 - i;
+        if (!mbar_wait(sm.empty(pos % S::kStages), (pos / S::kStages) & 1u, abort_flag, deadline)) return false;
+    }
+    const int k = S::kPasses * g.n_peers > 1 ? 2 : 1;
+    if (atomicCAS(prefetch, 0, kPrefetchIssued + k) != 0) return true;  // the epilogue has given up
+    fence_proxy_async_global();  // the flag acquires before the copies' reads
+    for (int ew = 0; ew < 4; ++ew)
+        for (int j = 0; j < k; ++j) fetch_partial(a, sm, g, rank, ew, j);
+    return true;
+}
+
 template <bool kNT, int kCG, int kBN>
 __device__ void run_producer(const KArgs& a, const CUtensorMap* tmA, const CUtensorMap* tmB,
                              const Smem<Shape<kCG, kBN>>& sm, int unit, uint32_t rank, uint64_t deadline,
-                             volatile int* abort_flag) {
+                             volatile int* abort_flag, int* prefetch) {
     using S = Shape<kCG, kBN>;
     Walk w;
     w.init(a.sch, unit);
-    Seg g;
+    Seg g, last;
+    int nseg = 0;
     int stage = 0;
     uint32_t phase = 0;
     uint32_t issued = 0;
     bool ok = true;
     while (ok && w.next(a.sch, g)) {
+        last = g;
+        ++nseg;
         // This CTA's rows of the tile and its half of the tile's columns of B.
         int32_t trow, tcolumn;
         tile_coords(a.sch, g.tile, &trow, &tcolumn);
@@ -126,6 +180,8 @@ __device__ void run_producer(const KArgs& a, const CUtensorMap* tmA, const CUten
             }
         }
     }
+    if (ok && kEpiGroups == 1 && nseg > 0 && last.role == kOwner && !a.sch.sep && !a.atomic)
+        ok = prefetch_partials<kCG, kBN>(a, sm, last, rank, issued, deadline, abort_flag, prefetch);
     if (!ok) record_timeout(a, abort_flag);
     // Let the last loads land before the CTA can exit (bounded). A pair's loads all
     // complete on the leader's barriers, so the leader drains for both.
@@ -251,24 +307,56 @@ __device__ __forceinline__ bool wait_flag(const int32_t* f, int32_t target, uint
 // (c * 8 + q) * 32 + lane, so each warp access covers 512 contiguous bytes.
 __device__ __forceinline__ int slot_f4(int c, int q, int lane) { return ((c * 8 + q) * 32 + lane) * 4; }
 
+// Lane 0 of epilogue warp `ew`: fetch item j of a deterministic owner's peer partials (pass
+// j / n_peers of peer j % n_peers, this warp's block) into the warp's ring buffer j % 2 with one
+// bulk copy, completing on that buffer's barrier. Warp ew + 2 reads TMEM lane quadrant
+// (ew + 2) % 4, whose rows are block (ew + 2) % 4 of the slot.
+template <class S>
+__device__ __forceinline__ void fetch_partial(const KArgs& a, const Smem<S>& sm, const Seg& g, uint32_t rank, int ew,
+                                              int j) {
+    constexpr int kChunks = kPassCols / 32;
+    const int p = j / g.n_peers, pi = j % g.n_peers;
+    const int quad = (ew + 2) & 3;
+    const float* src = a.slots + static_cast<int64_t>((g.peer_begin + pi) * S::kCtas + static_cast<int32_t>(rank)) *
+                                     S::kCtaSlotFloats +
+                       static_cast<int64_t>(quad) * S::kWarpSlotFloats + slot_f4(kChunks * p, 0, 0);
+    const uint32_t bar = sm.pload(ew, j & 1);
+    mbar_arrive_expect_tx(bar, kPartBytes);
+    bulk_load_g2s(sm.base + static_cast<uint32_t>(ew) * kWarpRingBytes + static_cast<uint32_t>(j & 1) * kPartBytes,
+                  src, kPartBytes, bar);
+}
+
 // Store kCols columns of this warp's 32 rows (one row per lane, in registers) through the
 // warp's two 4 KiB staging boxes with TMA tensor stores: BF16 C in boxes of 64 columns, FP32
 // C or slab in boxes of 32 columns, each box 32 rows x 128 bytes in the 128-byte swizzled
 // layout (16-byte chunk j of row r at chunk j ^ (r % 8)), so the shared stores are
 // conflict-free and the TMA clips the box at M and N. `slab` < 0 stores to C.
-// One 32-row x 128-byte box of this warp's rows (8 chunks of 16 bytes per row, given as
-// 32-bit words w[j][0..3]) through staging buffer nstore % kBoxes, stored by the TMA at
-// (x, y0) (or (x, y0, slab)).
-template <class F>
-__device__ __forceinline__ void store_box(const CUtensorMap* tmC, uint32_t staging, uint32_t& nstore, int32_t x,
-                                          int32_t y0, int32_t slab, F&& words) {
-    const int lane = threadIdx.x & 31;
-    const uint32_t buf = staging + (kBoxes == 1 ? 0u : (nstore & 1u) * 4096u);
-    if (nstore >= static_cast<uint32_t>(kBoxes)) {
-        // The store issued kBoxes boxes ago used this buffer: wait until the TMA read it.
-        if (lane == 0) bulk_wait_group_read<kBoxes - 1>();
+// Staging buffer of this warp's nstore-th box: the nbuf 4 KiB buffers at `staging` in
+// turn (nbuf is 1, 2, 4 or 12). Before a buffer is reused, wait until the TMA has read the
+// copy issued nbuf boxes ago.
+__device__ __forceinline__ uint32_t staging_buffer(uint32_t staging, uint32_t nbuf, uint32_t nstore) {
+    if (nstore >= nbuf) {
+        if ((threadIdx.x & 31) == 0) {
+            switch (nbuf) {
+                case 1: bulk_wait_group_read<0>(); break;
+                case 2: bulk_wait_group_read<1>(); break;
+                case 4: bulk_wait_group_read<3>(); break;
+                default: bulk_wait_group_read<11>(); break;
+            }
+        }
         __syncwarp();
     }
+    return staging + (nstore % nbuf) * 4096u;
+}
+
+// One 32-row x 128-byte box of this warp's rows (8 chunks of 16 bytes per row, given as
+// 32-bit words w[j][0..3]) through staging buffer nstore % nbuf, stored by the TMA at
+// (x, y0) (or (x, y0, slab)).
+template <class F>
+__device__ __forceinline__ void store_box(const CUtensorMap* tmC, uint32_t staging, uint32_t nbuf, uint32_t& nstore,
+                                          int32_t x, int32_t y0, int32_t slab, F&& words) {
+    const int lane = threadIdx.x & 31;
+    const uint32_t buf = staging_buffer(staging, nbuf, nstore);
     const uint32_t row = buf + static_cast<uint32_t>(lane) * 128u;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
@@ -290,17 +378,13 @@ __device__ __forceinline__ void store_box(const CUtensorMap* tmC, uint32_t stagi
 
 // One 4 KiB chunk of this warp's block of a partial slot (32 columns: float4 q of lane l at
 // byte (32 q + l) * 16, the slot's own order, so the chunk is one contiguous copy) through
-// staging buffer nstore % kBoxes, stored by a TMA bulk copy to dst. The lanes' shared stores
+// staging buffer nstore % nbuf, stored by a TMA bulk copy to dst. The lanes' shared stores
 // are 512 contiguous bytes per q, conflict-free.
 template <class F>
-__device__ __forceinline__ void store_partial_chunk(float* dst, uint32_t staging, uint32_t& nstore, F&& value) {
+__device__ __forceinline__ void store_partial_chunk(float* dst, uint32_t staging, uint32_t nbuf, uint32_t& nstore,
+                                                    F&& value) {
     const int lane = threadIdx.x & 31;
-    const uint32_t buf = staging + (kBoxes == 1 ? 0u : (nstore & 1u) * 4096u);
-    if (nstore >= static_cast<uint32_t>(kBoxes)) {
-        // The copy issued kBoxes chunks ago used this buffer: wait until the TMA read it.
-        if (lane == 0) bulk_wait_group_read<kBoxes - 1>();
-        __syncwarp();
-    }
+    const uint32_t buf = staging_buffer(staging, nbuf, nstore);
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
         const float4 x = value(q);
@@ -322,7 +406,7 @@ __device__ __forceinline__ void store_partial_chunk(float* dst, uint32_t staging
 // swizzled layout (16-byte chunk j of row r at chunk j ^ (r % 8)), so the shared stores are
 // conflict-free and the TMA clips the box at M and N. `slab` < 0 stores to C.
 template <int kCols>
-__device__ __forceinline__ void store_slice(const KArgs& a, const CUtensorMap* tmC, uint32_t staging,
+__device__ __forceinline__ void store_slice(const KArgs& a, const CUtensorMap* tmC, uint32_t staging, uint32_t nbuf,
                                             uint32_t& nstore, const float (&v)[kCols], int32_t x0, int32_t y0,
                                             int32_t slab) {
     if (y0 >= a.M) return;  // the warp's 32 rows lie below C
@@ -335,7 +419,7 @@ __device__ __forceinline__ void store_slice(const KArgs& a, const CUtensorMap* t
         for (int b = 0; b < kCols / 64; ++b) {
             const int32_t x = x0 + b * 64;
             if (x >= a.N) break;
-            store_box(tmC, staging, nstore, x, y0, slab, [&](int j, uint32_t& w0, uint32_t& w1, uint32_t& w2, uint32_t& w3) {
+            store_box(tmC, staging, nbuf, nstore, x, y0, slab, [&](int j, uint32_t& w0, uint32_t& w1, uint32_t& w2, uint32_t& w3) {
                 const int i = b * 64 + j * 8;
                 __nv_bfloat162 p0 = __floats2bfloat162_rn(v[i + 0], v[i + 1]);
                 __nv_bfloat162 p1 = __floats2bfloat162_rn(v[i + 2], v[i + 3]);
@@ -352,7 +436,7 @@ __device__ __forceinline__ void store_slice(const KArgs& a, const CUtensorMap* t
         for (int b = 0; b < kCols / 32; ++b) {
             const int32_t x = x0 + b * 32;
             if (x >= a.N) break;
-            store_box(tmC, staging, nstore, x, y0, slab, [&](int j, uint32_t& w0, uint32_t& w1, uint32_t& w2, uint32_t& w3) {
+            store_box(tmC, staging, nbuf, nstore, x, y0, slab, [&](int j, uint32_t& w0, uint32_t& w1, uint32_t& w2, uint32_t& w3) {
                 const int i = b * 32 + j * 4;
                 w0 = __float_as_uint(v[i + 0]);
                 w1 = __float_as_uint(v[i + 1]);
@@ -418,6 +502,13 @@ struct Epi {
     int lane, gt, quad, row;     // gt: thread index within the group
     int32_t r;
     uint32_t tcol, staging, nstore;
+    uint32_t nbuf;               // staging buffers in turn: kBoxes, or more in the ring (see `wide`)
+    uint32_t ring;               // this warp's quarter of the ring (free once the unit's MAC loop is over)
+    uint32_t pbar;               // this warp's two partial-load barriers, and their phase bits
+    uint32_t pph;
+    int ew;                      // index among the epilogue warps
+    int* prefetch;               // shared hand-off word of the producer warp's partial copies
+    volatile int* shared_tmp;    // shared word for the group's copy of an atomic result
     uint32_t tempty0, tempty1;   // accumulator-empty barriers (in the leader CTA)
     int64_t blk_off;
     int buf;                     // accumulator of the next segment (one group), and the phase parities
@@ -469,7 +560,7 @@ struct Epi {
                     }
                 }
             }
-            store_slice<kPassCols>(a, tmD, staging, nstore, v, c0, m0 + quad * 32, -1);
+            store_slice<kPassCols>(a, tmD, staging, nbuf, nstore, v, c0, m0 + quad * 32, -1);
         }
     }
 
@@ -545,19 +636,36 @@ struct Epi {
         return true;
     }
 
+    // Let this warp's partial copies still in flight (items waited .. issued - 1, all of them
+    // started) land before the CTA may exit; bounded.
+    __device__ __forceinline__ void drain_partials(int waited, int issued) {
+        const uint64_t until = globaltimer() + kDrainNs;
+        for (int j = waited; j < issued; ++j)
+            (void)mbar_wait_until(pbar + 8u * static_cast<uint32_t>(j & 1), (pph >> (j & 1)) & 1u, until);
+    }
+
     // One segment. kFixup: this segment is a split tile's owner and sums its peers' partials
-    // here (without the separate fixup pass). Returns false when a wait gave up or a check
-    // failed (the caller stops).
-    template <bool kFixup>
-    __device__ __forceinline__ bool segment(const Seg& g, uint64_t* tr, int seg) {
+    // here (without the separate fixup pass). `wide`: this is the unit's last segment, so once
+    // its accumulator is complete the MAC loop is over and the ring is free. This warp's
+    // quarter of the ring then stages all of its stores (12 buffers instead of kBoxes, so the
+    // copies go out without waiting for a buffer). kBulk (a deterministic owner's last
+    // segment, so also `wide`): the peers' partials come into the ring by bulk copies instead
+    // of register loads. The producer warp, idle by then, has acquired the peers' flags and
+    // started the first two copies as soon as the ring was free (run_producer); this warp
+    // consumes them and issues the rest. Returns false when a wait gave up or a check failed
+    // (the caller stops).
+    template <bool kFixup, bool kBulk>
+    __device__ __forceinline__ bool segment(const Seg& g, uint64_t* tr, int seg, bool wide) {
+        static_assert(kFixup || !kBulk, "bulk fetches are an owner's");
         constexpr int kChunks = kPassCols / 32;  // TMEM loads per pass
+        constexpr bool bulk = kBulk;
         if (!in_bounds(g)) {  // same answer in every epilogue thread
             *abort_flag = 1;
             atomicCAS(a.status, 0, kErrBounds);
             return false;
         }
         float v[kPassCols];
-        if (kFixup) {
+        if (kFixup && !bulk) {
             // Wait for every peer (this CTA's share of the partials), then fetch the first pass
             // of the first partial (or of the atomic sum) while this segment's MAC loop is
             // still running.
@@ -585,6 +693,18 @@ struct Epi {
         }
         tc_fence_after();
         if (tr && seg < kTraceSegs) tr[4 + 4 * seg + 2] = globaltimer();
+        // Ring quarter: [0, 2 kPartBytes) the two partial buffers of a bulk owner, then its
+        // 4 staging buffers; otherwise 12 staging buffers. Stores of earlier segments still in
+        // flight read the staging block after the ring, not these buffers.
+        if (wide) {
+            staging = bulk ? ring + 2 * kPartBytes : ring;
+            nbuf = bulk ? 4u : 12u;
+            nstore = 0;
+        }
+        const int n_items = bulk ? S::kPasses * g.n_peers : 0;
+        int issued = bulk ? (n_items > 1 ? 2 : 1) : 0;  // the producer warp's copies
+        int waited = 0;
+        bool failed = false;
 
         int32_t trow, tcolumn;
         tile_coords(a.sch, g.tile, &trow, &tcolumn);
@@ -598,7 +718,7 @@ struct Epi {
 
 #pragma unroll 1
         for (int p = 0; p < S::kPasses; ++p) {
-            if (kFixup && p > 0) {
+            if (kFixup && p > 0 && !bulk) {
                 if (a.atomic)
                     load_partial<false, true>(v, block(g.peer_begin), kChunks * p, lane);
                 else
@@ -608,7 +728,7 @@ struct Epi {
             // or for an owner 64 columns at a time added to the first partial (own + P1: the
             // first step of the k-order fold).
             const uint32_t taddr = tmem_base + tcol + static_cast<uint32_t>(b * kBN + p * kPassCols);
-            if (kFixup) {
+            if (kFixup && !bulk) {
 #pragma unroll
                 for (int h = 0; h < kPassCols / 64; ++h) {
                     uint32_t t[64];
@@ -636,13 +756,50 @@ struct Epi {
                     mbar_arrive_cluster(b ? tempty1 : tempty0);
             }
 
-            if (kFixup) {
+            if (kFixup && bulk) {
+                // Turnstile from the ring: own + P(first peer) + P(next) ..., in k order; each
+                // pass of each peer is one bulk copy, two in flight. A failed wait skips the
+                // rest (the group decides after the loop).
+#pragma unroll 1
+                for (int32_t pi = 0; pi < g.n_peers; ++pi) {
+                    const int j = p * g.n_peers + pi;
+                    const uint32_t bit = static_cast<uint32_t>(j & 1);
+                    if (!failed) failed = !mbar_wait(pbar + 8u * bit, (pph >> bit) & 1u, abort_flag, deadline);
+                    if (failed) continue;
+                    pph ^= 1u << bit;
+                    ++waited;
+                    const uint32_t src = ring + bit * kPartBytes;
+#pragma unroll
+                    for (int c = 0; c < kChunks; ++c)
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) {
+                            const float4 x = ld_shared_f4(src + static_cast<uint32_t>(slot_f4(c, q, lane)) * 4u);
+                            const int i = c * 32 + q * 4;
+                            v[i] += x.x;
+                            v[i + 1] += x.y;
+                            v[i + 2] += x.z;
+                            v[i + 3] += x.w;
+                        }
+                    __syncwarp();  // every lane has read buffer `bit` before it is refilled
+                    if (j + 2 < n_items) {
+                        if (lane == 0) {
+                            // The lanes' reads of the buffer, and (through the barrier) the
+                            // producer warp's flag acquires, before this copy.
+                            fence_proxy_async_smem();
+                            fence_proxy_async_global();
+                            fetch_partial(a, sm, g, static_cast<uint32_t>(r), ew, j + 2);
+                        }
+                        ++issued;
+                    }
+                }
+                if (!failed) store_slice<kPassCols>(a, tmC, staging, nbuf, nstore, v, n0 + p * kPassCols, wy, -1);
+            } else if (kFixup) {
                 // Turnstile: the remaining peers' partials, in k order.
                 if (!a.atomic) {
                     for (int32_t pi = 1; pi < g.n_peers; ++pi)
                         load_partial<true, false>(v, block(g.peer_begin + pi), kChunks * p, lane);
                 }
-                store_slice<kPassCols>(a, tmC, staging, nstore, v, n0 + p * kPassCols, wy, -1);
+                store_slice<kPassCols>(a, tmC, staging, nbuf, nstore, v, n0 + p * kPassCols, wy, -1);
             } else if (g.role == kProducer || g.role == sk::kOwner) {
                 // A producer's partial; with the separate fixup pass, an owner's too. The
                 // pass sums them in k order, so the reduction mode does not apply there.
@@ -657,16 +814,16 @@ struct Epi {
                             red_add_v4_f32(blk + slot_f4(kChunks * p + c, q, lane), v[i], v[i + 1], v[i + 2], v[i + 3]);
                         }
                     } else {
-                        store_partial_chunk(blk + slot_f4(kChunks * p + c, 0, 0), staging, nstore, [&](int q) {
+                        store_partial_chunk(blk + slot_f4(kChunks * p + c, 0, 0), staging, nbuf, nstore, [&](int q) {
                             const int i = c * 32 + q * 4;
                             return make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
                         });
                     }
                 }
             } else if (g.role == kSlab) {
-                store_slice<kPassCols>(a, tmC, staging, nstore, v, n0 + p * kPassCols, wy, g.slot);
+                store_slice<kPassCols>(a, tmC, staging, nbuf, nstore, v, n0 + p * kPassCols, wy, g.slot);
             } else {
-                store_slice<kPassCols>(a, tmC, staging, nstore, v, n0 + p * kPassCols, wy, -1);
+                store_slice<kPassCols>(a, tmC, staging, nbuf, nstore, v, n0 + p * kPassCols, wy, -1);
             }
         }
         if (b)
@@ -674,6 +831,15 @@ struct Epi {
         else
             uses0 ^= 1u;
         if (!kFixedBuf) buf ^= 1;
+        if (bulk && named_bar_or(kBar, kGroupThreads, failed)) {
+            // Close the hand-off. If the producer warp never started its copies it never will;
+            // otherwise let this warp's copies in flight land before the CTA may exit.
+            if (gt == 0) *shared_tmp = atomicCAS(prefetch, 0, kPrefetchClosed);
+            named_bar_sync(kBar, kGroupThreads);
+            if (*shared_tmp >= kPrefetchIssued) drain_partials(waited, issued);
+            record_timeout(a, abort_flag);
+            return false;
+        }
 
         if (g.role == kSlab && a.sch.partials == 2) {
             // Split-K slab, summed inside this launch (aligned split with a per-tile arrival
@@ -748,7 +914,8 @@ struct Epi {
 template <int kCG, int kBN, int kGroup>
 __device__ void run_epilogue_group(const KArgs& a, const CUtensorMap* tmC, const CUtensorMap* tmD,
                                    const Smem<Shape<kCG, kBN>>& sm, uint32_t tmem_base, int unit, uint32_t rank,
-                                   uint64_t deadline, volatile int* abort_flag, volatile int* last_flag) {
+                                   uint64_t deadline, volatile int* abort_flag, volatile int* last_flag,
+                                   int* prefetch, volatile int* shared_tmp) {
     using S = Shape<kCG, kBN>;
     const int warp = threadIdx.x >> 5;
     const int ew = warp - 2;                  // index among the epilogue warps
@@ -762,6 +929,13 @@ __device__ void run_epilogue_group(const KArgs& a, const CUtensorMap* tmC, const
     e.tcol = static_cast<uint32_t>(e.quad * 32) << 16;
     e.staging = sm.base + S::kStagingOff + static_cast<uint32_t>(ew * kBoxes) * 4096u;
     e.nstore = 0;
+    e.nbuf = kBoxes;
+    e.ring = sm.base + static_cast<uint32_t>(ew & 3) * kWarpRingBytes;
+    e.pbar = sm.pload(ew, 0);
+    e.pph = 0;
+    e.ew = ew;
+    e.prefetch = prefetch;
+    e.shared_tmp = shared_tmp;
     // The accumulator-empty barriers live in the leader CTA.
     e.tempty0 = kCG == 1 ? sm.tempty(0) : mapa_shared(sm.tempty(0), 0);
     e.tempty1 = kCG == 1 ? sm.tempty(1) : mapa_shared(sm.tempty(1), 0);
@@ -770,17 +944,36 @@ __device__ void run_epilogue_group(const KArgs& a, const CUtensorMap* tmC, const
     e.uses0 = e.uses1 = 0u;
     uint64_t* tr = (a.trace && e.gt == 0) ? a.trace + static_cast<int64_t>(blockIdx.x) * kTraceWords : nullptr;
     Walk w;
-    w.init(a.sch, unit);
     Seg g;
+    int n_seg = 0;  // segments of this unit (a walk of integer steps, before the first wait)
+    w.init(a.sch, unit);
+    while (w.next(a.sch, g)) ++n_seg;
+    w.init(a.sch, unit);
     int seg = 0;  // the unit's segment index; the MMA issuer puts segment i in accumulator i % 2
     while (w.next(a.sch, g)) {
         if (seg % kEpiGroups == kGroup) {
-            const bool ok = (g.role == kOwner && !a.sch.sep) ? e.template segment<true>(g, tr, seg)
-                                                              : e.template segment<false>(g, tr, seg);
+            // The unit's last segment stages through the ring. With two groups the other group
+            // may still be storing through its own buffers; the wide staging is for one only.
+            const bool wide = seg == n_seg - 1 && kEpiGroups == 1;
+            bool ok;
+            if (g.role == kOwner && !a.sch.sep)
+                ok = (wide && !a.atomic) ? e.template segment<true, true>(g, tr, seg, true)
+                                         : e.template segment<true, false>(g, tr, seg, wide);
+            else
+                ok = e.template segment<false, false>(g, tr, seg, wide);
             if (!ok) break;
             if (tr && seg < kTraceSegs) tr[4 + 4 * seg + 3] = globaltimer();
         }
         ++seg;
+    }
+    if (kEpiGroups == 1 && seg < n_seg - 1) {
+        // Stopped before the last segment: close the producer warp's hand-off, and if it has
+        // already started copies into the ring, let them land (bounded) before the CTA exits.
+        if (e.gt == 0) *shared_tmp = atomicCAS(prefetch, 0, kPrefetchClosed);
+        named_bar_sync(1, kGroupThreads);
+        const int k = *shared_tmp - kPrefetchIssued;
+        const uint64_t until = globaltimer() + kDrainNs;
+        for (int j = 0; j < k; ++j) (void)mbar_wait_until(e.pbar + 8u * static_cast<uint32_t>(j & 1), 0u, until);
     }
     // Every TMA store of this warp has written C before the CTA may exit.
     if (e.lane == 0) bulk_wait_group_all();
@@ -792,11 +985,14 @@ __device__ void run_epilogue_group(const KArgs& a, const CUtensorMap* tmC, const
 template <int kCG, int kBN>
 __device__ void run_epilogue(const KArgs& a, const CUtensorMap* tmC, const CUtensorMap* tmD,
                              const Smem<Shape<kCG, kBN>>& sm, uint32_t tmem_base, int unit, uint32_t rank,
-                             uint64_t deadline, volatile int* abort_flag, volatile int* last_flag) {
+                             uint64_t deadline, volatile int* abort_flag, volatile int* last_flag, int* prefetch,
+                             volatile int* shared_tmp) {
     if (kEpiGroups == 1 || (threadIdx.x >> 5) < 6)
-        run_epilogue_group<kCG, kBN, 0>(a, tmC, tmD, sm, tmem_base, unit, rank, deadline, abort_flag, last_flag);
+        run_epilogue_group<kCG, kBN, 0>(a, tmC, tmD, sm, tmem_base, unit, rank, deadline, abort_flag, last_flag,
+                                        prefetch, shared_tmp);
     else
-        run_epilogue_group<kCG, kBN, 1>(a, tmC, tmD, sm, tmem_base, unit, rank, deadline, abort_flag, last_flag);
+        run_epilogue_group<kCG, kBN, 1>(a, tmC, tmD, sm, tmem_base, unit, rank, deadline, abort_flag, last_flag,
+                                        prefetch, shared_tmp);
 }
 
 // --------------------------------------------------------------------------- kernel
@@ -812,6 +1008,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + S::kSmemBarOff + 192);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + S::kSmemBarOff + 196);
     volatile int* last_flag = reinterpret_cast<volatile int*>(smem + S::kSmemBarOff + 200);  // one per group
+    int* prefetch = reinterpret_cast<int*>(smem + S::kSmemBarOff + 208);  // partial-copy hand-off word
+    volatile int* shared_tmp = reinterpret_cast<volatile int*>(smem + S::kSmemBarOff + 212);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -831,7 +1029,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(sm.done(), 1);
         mbar_init(sm.tready(), 1);
+        for (int w = 0; w < kEpiWarps; ++w) {
+            mbar_init(sm.pload(w, 0), 1);
+            mbar_init(sm.pload(w, 1), 1);
+        }
         *abort_flag = 0;
+        *prefetch = 0;
         fence_mbar_init();
         prefetch_tmap(&tmA);
         prefetch_tmap(&tmB);
@@ -858,7 +1061,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t deadline = globaltimer() + args.timeout_ns;  // wait limits count from here
         if (lane == 0) {
             if (args.trace) args.trace[static_cast<int64_t>(blockIdx.x) * kTraceWords] = globaltimer();
-            run_producer<kNT, kCG, kBN>(args, &tmA, &tmB, sm, unit, rank, deadline, abort_flag);
+            run_producer<kNT, kCG, kBN>(args, &tmA, &tmB, sm, unit, rank, deadline, abort_flag, prefetch);
         }
         // Warps 0 and 1 reconverge before the exit barrier: a CTA barrier counts a warp once
         // any of its threads arrives, so all 32 lanes must arrive together.
@@ -892,7 +1095,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         grid_dep_wait();
         grid_dep_launch();
         const uint64_t deadline = globaltimer() + args.timeout_ns;
-        run_epilogue<kCG, kBN>(args, &tmC, &tmD, sm, tmem_base, unit, rank, deadline, abort_flag, last_flag);
+        run_epilogue<kCG, kBN>(args, &tmC, &tmD, sm, tmem_base, unit, rank, deadline, abort_flag, last_flag, prefetch,
+                               shared_tmp);
     }
 
     tc_fence_before();

@@ -32,6 +32,7 @@ constexpr int kTraceWords = 4 + 4 * kTraceSegs; // SK_TRACE_WORDS
 // tcgen05 cta_group::2), work tile (128 * kCG) x kBN, k-iteration depth 64.
 template <int kCG, int kBN>
 struct Shape {
+    static constexpr int kCtas = kCG;                      // CTAs per work tile
     static constexpr int kBNc = kBN / kCG;                 // B columns held by one CTA
     static constexpr int kABytes = kCtaRows * kBlkK * 2;   // 16 KiB of A per stage
     static constexpr int kBBytes = kBNc * kBlkK * 2;       // 8 / 16 / 32 KiB of B per stage
@@ -42,13 +43,16 @@ struct Shape {
     static constexpr int kStagingOff = kStages * kStageBytes;
     static constexpr int kStagingBytes = kEpiWarps * kBoxes * 4096;
     static constexpr int kSmemBarOff = kStagingOff + kStagingBytes;
-    static constexpr int kSmemBytes = kSmemBarOff + 256 + 1024;
+    // Barrier block: the pipeline barriers and flags in its first 256 bytes, then two
+    // partial-load barriers per epilogue warp.
+    static constexpr int kSmemBytes = kSmemBarOff + 512 + 1024;
     static constexpr int kTmemCols = 2 * kBN;               // two accumulators of kBN columns
     static constexpr int kTxBytes = kCG * kStageBytes;      // bytes landing on the leader per stage
     static constexpr int kPasses = kBN / kPassCols;         // a thread's row, kPassCols at a time
     static constexpr int kWarpSlotFloats = 32 * kBN;        // one epilogue warp's block of a partial
     static constexpr int kCtaSlotFloats = kCtaRows * kBN;   // a CTA's share of one partial slot
     static_assert(kBNc % 64 == 0 && kBN % 128 == 0, "tile shape");
+    static_assert(kSmemBytes <= 232448 && 256 + 16 * kEpiWarps <= 512, "shared memory");
 };
 
 struct KArgs {

@@ -107,6 +107,20 @@ __device__ __forceinline__ void bulk_store_s2g(void* gdst, uint32_t ssrc, uint32
     asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(ssrc), "r"(bytes)
                  : "memory");
 }
+// Copy `bytes` contiguous bytes of global memory into this CTA's shared memory with the TMA
+// unit; the copy completes `bytes` of transaction count on mbarrier `bar`. Both addresses
+// 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_load_g2s(uint32_t sdst, const void* gsrc, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(sdst),
+                 "l"(gsrc), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+__device__ __forceinline__ float4 ld_shared_f4(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr)
+                 : "memory");
+    return v;
+}
 // Wait until at most N of this thread's bulk groups still read their shared-memory source.
 template <int N>
 __device__ __forceinline__ void bulk_wait_group_read() {
