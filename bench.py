@@ -48,11 +48,11 @@ WORKLOADS = {"waveq": synth.WAVEQ, "skinny": synth.SKINNY, "large": synth.LARGE,
 NOMINAL_BF16_TFLOPS = 2250.0
 NOMINAL_HBM_GBS = 8000.0
 TRAFFIC = {
-    "waveq_2048x2432x4096/hybrid/tile2@148": {"bytes": 36786944 + 1604864, "kernel_sha": "ec85194d81863f1c",
+    "waveq_2048x2432x4096/hybrid/tile2@148": {"bytes": 36798976 + 1763072, "kernel_sha": "14675fd62483d21d",
                                               "profile": "profiles/sk_gemm_kernel_waveq_2048x2432x4096_pair256_hybrid148.md"},
-    "large_8192x8192x8192/dp/tile2@148": {"bytes": 2065371392 + 129376768, "kernel_sha": "ec85194d81863f1c",
+    "large_8192x8192x8192/dp/tile2@148": {"bytes": 2166546688 + 129797376, "kernel_sha": "14675fd62483d21d",
                                           "profile": "profiles/sk_gemm_kernel_large_8192_pair256_dp148_raster.md"},
-    "large_8192x8192x8192/dp/tile2@148/r0s8": {"bytes": 1032425984 + 125851904, "kernel_sha": "ec85194d81863f1c",
+    "large_8192x8192x8192/dp/tile2@148/r0s8": {"bytes": 1064061184 + 126596608, "kernel_sha": "14675fd62483d21d",
                                                "profile": "profiles/sk_gemm_kernel_large_8192_pair256_dp148_raster.md"},
 }
 
@@ -670,6 +670,55 @@ def main():
             return {"tail_idle_sm_us": v[0], "span_us": v[1], "ctas": ncta}
         dp_idle = idle("dp", sms, args.tile)
         hd_idle = idle(args.mode, sms, args.tile)
+        # ---- timeline of two consecutive launches inside a back-to-back run of the timed
+        # schedule (launches 20 and 21 over the rotating sets), with and without the
+        # overlapped launch: the gap between launches, the cold start, and how the units' ends
+        # spread after their last MMA (the epilogue work each unit has left).
+        def b2b_timeline(ov):
+            s4 = sk.schedule(modes[args.mode], args.splits if args.mode == "splitk" else 1, units=0,
+                             split_partials=args.partials, tile=args.tile, raster=args.raster, swizzle=args.swizzle,
+                             overlap=ov)
+            nb4 = sk.sk_workspace_size(w.M, w.N, w.K, sms, s4, red)
+            ws4 = torch.zeros(nb4, dtype=torch.uint8, device=dev)
+            plan4 = sk.sk_plan(w.M, w.N, w.K, sms, s4)
+            cg = int(plan4[14])
+            ncta = int(plan4[4]) * cg
+            trs = [torch.zeros(ncta * sk.SK_TRACE_WORDS, dtype=torch.int64, device=dev) for _ in range(2)]
+            torch.cuda.synchronize(dev)
+            for i in range(24):
+                a_, b_, c_ = sets[i % n_sets]
+                if i in (20, 21):
+                    sk.sk_gemm_debug(a_, b_, c_, out_code, w.M, w.N, w.K, lay, s4, red, sms, ws4, nb4, stream,
+                                     trace=trs[i - 20])
+                else:
+                    sk.sk_gemm(a_, b_, c_, out_code, w.M, w.N, w.K, lay, s4, red, sms, ws4, nb4, stream)
+            torch.cuda.synchronize(dev)
+            assert sk.sk_status(ws4, stream) == sk.SK_OK
+            segs = {}
+            for i in range(int(plan4[7])):
+                r = plan4[sk.SK_MAP_HEADER + sk.SK_MAP_SEG * i: sk.SK_MAP_HEADER + sk.SK_MAP_SEG * (i + 1)]
+                segs.setdefault(int(r[0]), []).append((int(r[1]), "FOPS"[int(r[5])] + str(int(r[4]) - int(r[3]))))
+            out = []
+            for tr in trs:
+                T = tr.cpu().numpy().reshape(ncta, sk.SK_TRACE_WORDS).astype(np.int64)
+                nseg = np.minimum(T[:, 2], sk.SK_TRACE_SEGS)
+                st = [T[c, 4:4 + 4 * nseg[c]].reshape(-1, 4) for c in range(ncta)]
+                end = np.array([max(T[c, 1], st[c].max(initial=0)) for c in range(ncta)])
+                lead = [c for c in range(ncta) if c % cg == 0 and nseg[c] > 0]
+                first = np.array([st[c][0, 0] - T[c, 0] for c in lead]) / 1e3
+                commit = np.array([st[c][-1, 1] for c in lead])
+                tail = np.array([end[c] - st[c][-1, 1] for c in lead]) / 1e3
+                late = sorted(lead, key=lambda c: -end[c])[:3]
+                out.append({"start": int(T[:, 0].min()), "end": int(end.max()),
+                            "first_mma_after_start_us_median": float(np.median(first)),
+                            "last_commit_spread_us": float((commit.max() - commit.min()) / 1e3),
+                            "end_spread_us": float((end.max() - end.min()) / 1e3),
+                            "end_after_last_commit_us": {"median": float(np.median(tail)), "max": float(tail.max())},
+                            "latest_units": [" ".join(s for _, s in sorted(segs.get(c // cg, []))) for c in late]})
+            return {"overlap": ov, "gap_between_launches_us": (out[1]["start"] - out[0]["end"]) / 1e3,
+                    "launch": [{k: v for k, v in o.items() if k not in ("start", "end")} for o in out]}
+        extras["b2b_timeline"] = [b2b_timeline(1), b2b_timeline(0)]
+
         extras["tail_idle"] = {"dp": dp_idle, args.mode: hd_idle,
                                "dp_over_schedule": dp_idle["tail_idle_sm_us"] / max(1e-9, hd_idle["tail_idle_sm_us"]),
                                "definition": "sum over the device's SMs of (kernel end - SM end), per-CTA globaltimer"}

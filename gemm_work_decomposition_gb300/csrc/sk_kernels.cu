@@ -664,6 +664,16 @@ struct Epi {
             atomicCAS(a.status, 0, kErrBounds);
             return false;
         }
+        // Where this CTA's rows of the tile go (computed before the accumulator waits).
+        int32_t trow, tcolumn;
+        tile_coords(a.sch, g.tile, &trow, &tcolumn);
+        const int32_t m0 = trow * (kCtaRows * kCG) + r * kCtaRows;
+        const int32_t n0 = tcolumn * kBN;
+        const int32_t wy = m0 + quad * 32;  // first row of this warp's 32
+        float* dump = a.dump ? a.dump +
+                                   (static_cast<int64_t>(g.tile) * a.sch.iters + g.k_begin) * (kCtaRows * kCG * kBN) +
+                                   static_cast<int64_t>(r * kCtaRows + row) * kBN
+                             : nullptr;
         float v[kPassCols];
         if (kFixup && !bulk) {
             // Wait for every peer (this CTA's share of the partials), then fetch the first pass
@@ -706,15 +716,7 @@ struct Epi {
         int waited = 0;
         bool failed = false;
 
-        int32_t trow, tcolumn;
-        tile_coords(a.sch, g.tile, &trow, &tcolumn);
-        const int32_t m0 = trow * (kCtaRows * kCG) + r * kCtaRows;
-        const int32_t n0 = tcolumn * kBN;
-        const int32_t wy = m0 + quad * 32;  // first row of this warp's 32
-        float* dump = a.dump ? a.dump +
-                                   (static_cast<int64_t>(g.tile) * a.sch.iters + g.k_begin) * (kCtaRows * kCG * kBN) +
-                                   static_cast<int64_t>(r * kCtaRows + row) * kBN
-                             : nullptr;
+
 
 #pragma unroll 1
         for (int p = 0; p < S::kPasses; ++p) {
@@ -897,8 +899,10 @@ struct Epi {
                     st_release_gpu(a.flags + g.slot * kCG + r, 1);
             }
         } else if (kFixup) {
-            // Every epilogue thread has read the partials: re-arm the flags / counter.
-            named_bar_sync(kBar, kGroupThreads);
+            // Every epilogue thread has read the partials: re-arm the flags / counter. (With
+            // bulk fetches every copy had completed before its warp read it, and the group
+            // barrier after the passes already has every thread past its reads.)
+            if (!bulk) named_bar_sync(kBar, kGroupThreads);
             if (gt == 0) {
                 if (a.atomic) {
                     a.flags[g.peer_begin * kCG + r] = 0;
