@@ -121,6 +121,37 @@ __device__ bool prefetch_partials(const KArgs& a, const Smem<Shape<kCG, kBN>>& s
     return true;
 }
 
+// An overlapped launch, before its wait for the previous kernel: prefetch into L2 the A and B
+// boxes of the unit's first kStages loads (the ones run_producer issues first), so that they
+// come from L2 instead of HBM once the wait is over. A prefetch has no effect on what later
+// loads read: if the previous kernel writes these bytes, L2 holds its writes.
+template <bool kNT, int kCG, int kBN>
+__device__ void prefetch_first_loads(const KArgs& a, const CUtensorMap* tmA, const CUtensorMap* tmB, int unit,
+                                     uint32_t rank) {
+    using S = Shape<kCG, kBN>;
+    Walk w;
+    w.init(a.sch, unit);
+    Seg g;
+    int n = 0;
+    while (n < S::kStages && w.next(a.sch, g)) {
+        int32_t trow, tcolumn;
+        tile_coords(a.sch, g.tile, &trow, &tcolumn);
+        const int32_t m0 = trow * (kCtaRows * kCG) + static_cast<int32_t>(rank) * kCtaRows;
+        const int32_t nb = tcolumn * kBN + static_cast<int32_t>(rank) * S::kBNc;
+        const bool rev = reversed_segment(a.sch, g);
+        for (int32_t i = 0; i < g.k_end - g.k_begin && n < S::kStages; ++i, ++n) {
+            const int32_t k0 = seg_k(g, rev, i) * kBlkK;
+            tma_prefetch_2d(tmA, k0, m0);
+            if (kNT) {
+                tma_prefetch_2d(tmB, k0, nb);
+            } else {
+#pragma unroll
+                for (int j = 0; j < S::kBNc / 64; ++j) tma_prefetch_2d(tmB, nb + 64 * j, k0);
+            }
+        }
+    }
+}
+
 template <bool kNT, int kCG, int kBN>
 __device__ void run_producer(const KArgs& a, const CUtensorMap* tmA, const CUtensorMap* tmB,
                              const Smem<Shape<kCG, kBN>>& sm, int unit, uint32_t rank, uint64_t deadline,
@@ -1054,12 +1085,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // Everything above touches only this CTA's own shared memory and the kernel parameters,
     // so under an overlapped launch it runs while the previous kernel on the stream is
-    // still finishing. Every thread that reads or writes global memory (A, B, C, the
+    // still finishing (as do the producer's L2 prefetches of its first loads). Every thread that reads or writes global memory (A, B, C, the
     // workspace, the debug buffers) first waits for that kernel; TMEM is allocated before
     // the wait. Every thread signals the next overlapped launch once it is past its wait, so
     // that launch may begin when all of this grid's CTAs are.
     uint32_t tmem_base = 0;
     if (warp == 0) {
+        if (args.sch.overlap && lane == 0) prefetch_first_loads<kNT, kCG, kBN>(args, &tmA, &tmB, unit, rank);
         grid_dep_wait();
         grid_dep_launch();
         const uint64_t deadline = globaltimer() + args.timeout_ns;  // wait limits count from here

@@ -77,6 +77,14 @@ __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
 // 2-D tiled bulk tensor load into shared memory, completing `bytes` on mbarrier `bar`.
 // c0 is the innermost (contiguous) coordinate in elements; it must be a multiple of 8 for
 // 16-bit data (16-byte boundary). Out-of-range parts of the box are filled with zeros.
+// Prefetch the 2-D box at (c0, c1) of a tensor map into L2 (a hint: no shared memory, no
+// barrier, no effect on what later loads read). Same coordinate rules as tma_load_2d.
+__device__ __forceinline__ void tma_prefetch_2d(const void* tmap, int32_t c0, int32_t c1) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(tmap)),
+                 "r"(c0), "r"(c1)
+                 : "memory");
+}
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, uint32_t bar, int32_t c0,
                                             int32_t c1) {
     asm volatile(
