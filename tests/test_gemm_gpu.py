@@ -367,22 +367,27 @@ def test_reduce_splits(sk, dev, s, mn, out):
 
 
 # --------------------------------------------------------------------------- time-out
-@pytest.mark.parametrize("tile", [0, 1])
-def test_wait_timeout_reports_status(sk, dev, tile):
+@pytest.mark.parametrize("red", [DET, ATOM])
+@pytest.mark.parametrize("overlap", [0, 1])
+@pytest.mark.parametrize("tile", [0, 1, 2])
+def test_wait_timeout_reports_status(sk, dev, tile, overlap, red):
     # Producers store but never raise their flag: every owner's wait runs out after 50 ms,
     # the kernel unwinds and records SK_ETIMEOUT; the context stays usable and the
-    # workspace works again once zeroed.
+    # workspace works again once zeroed. Toy problem on 4 units: unit 0 ends with a 1-iteration
+    # owner segment, so with the deterministic reduction its peers' partials go through the
+    # producer warp's ring copies, and the time-out runs out in the producer warp's flag wait
+    # and in the epilogue's copy wait (the hand-off word stays closed).
     w = synth.TOY
-    sched = sk.schedule(2, units=4, tile=tile)
+    sched = sk.schedule(2, units=4, tile=tile, overlap=overlap)
     A_bits, B_bits = U.inputs(w)
     A, B = U.to_dev(A_bits, dev), U.to_dev(B_bits, dev)
-    ws = U.new_workspace(sk, w.M, w.N, w.K, 4, sched, DET, dev)
-    _, _, _, status = U.gemm(sk, A, B, w.M, w.N, w.K, "NN", sched, DET, 4, "f32", dev, ws,
+    ws = U.new_workspace(sk, w.M, w.N, w.K, 4, sched, red, dev)
+    _, _, _, status = U.gemm(sk, A, B, w.M, w.N, w.K, "NN", sched, red, 4, "f32", dev, ws,
                              skip_producer_signal=1, timeout_ns=50_000_000)
     assert status == sk.SK_ETIMEOUT
     assert sk.sk_status(ws[0]) == sk.SK_OK
     ws[0].zero_()
-    got, guards, _, status = U.gemm(sk, A, B, w.M, w.N, w.K, "NN", sched, DET, 4, "f32", dev, ws)
+    got, guards, _, status = U.gemm(sk, A, B, w.M, w.N, w.K, "NN", sched, red, 4, "f32", dev, ws)
     assert status == sk.SK_OK and guards
     U.assert_close(got, U.reference(w), "after time-out")
 

@@ -145,3 +145,35 @@ def test_overlapped_back_to_back_shared_workspace(sk, dev, name, kw, tile, red):
         assert np.array_equal(got[i], ref[i % 3]), i
         assert np.array_equal(ref[i], ref[i % 3]), i
     assert not np.array_equal(ref[0], ref[1])
+
+
+def test_bench_configuration_back_to_back(sk, dev):
+    # The wave-quantized GEMM (2048 x 2432 x 4096, BF16 out) in the configuration bench.py
+    # times: hybrid rule on 148 SMs, 256 x 256 CTA pairs, overlapped launches back to back
+    # over rotating input sets sharing one workspace. Three sets with different seeds, nine
+    # launches; every output against the FP64 oracle on sampled rows, and outputs of the same
+    # set equal bit for bit.
+    from oracle import gemm as og
+    base = synth.WAVEQ
+    ws_ = [synth.Workload(base.name, base.M, base.N, base.K, base.layout, base.dist, seed, out=base.out)
+           for seed in (base.seed, 31, 32)]
+    bits = [synth.make_inputs(w) for w in ws_]
+    sets = [(_bf16(a, dev), _bf16(b, dev)) for a, b in bits]
+    M, N, K = base.M, base.N, base.K
+    sched = sk.schedule(3, tile=2, overlap=1)
+    nbytes = sk.sk_workspace_size(M, N, K, 148, sched, DET)
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
+    outs = [torch.full((M, N), U.SENTINEL, dtype=torch.bfloat16, device=dev) for _ in range(9)]
+    stream = torch.cuda.current_stream(dev)
+    torch.cuda.synchronize(dev)
+    for i, C in enumerate(outs):
+        A, B = sets[i % 3]
+        sk.sk_gemm(A, B, C, sk.SK_BF16, M, N, K, sk.SK_NN, sched, DET, 148, ws, nbytes, stream)
+    assert sk.sk_status(ws, stream) == sk.SK_OK
+    got = [o.float().cpu().numpy().astype(np.float64) for o in outs]
+    rows = U.sample_rows(M, 24, seed=5)
+    for j, (a, b) in enumerate(bits):
+        ref = og.ref_rows(a, b, base.layout, rows)
+        U.assert_close(got[j][rows], ref, f"set {j}")
+        for i in range(j + 3, 9, 3):
+            assert np.array_equal(got[i], got[j]), (i, j)
