@@ -781,12 +781,17 @@ struct Epi {
                 }
             }
             if (p == S::kPasses - 1) {
-                // The whole accumulator has been read: hand it back to the MMA issuer.
+                // The whole accumulator has been read: hand it back to the MMA issuer. One
+                // thread per CTA arrives, after the group's barrier, and it is one that issues
+                // no bulk copies (a release arrive waits for its thread's copies in flight).
                 tc_fence_before();
-                if (kCG == 1)
-                    mbar_arrive(b ? tempty1 : tempty0);
-                else
-                    mbar_arrive_cluster(b ? tempty1 : tempty0);
+                named_bar_sync(kBar, kGroupThreads);
+                if (gt == 1) {
+                    if (kCG == 1)
+                        mbar_arrive(b ? tempty1 : tempty0);
+                    else
+                        mbar_arrive_cluster(b ? tempty1 : tempty0);
+                }
             }
 
             if (kFixup && bulk) {
@@ -1060,7 +1065,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(sm.tfull(b), 1);
-            mbar_init(sm.tempty(b), kGroupThreads * kCG);  // one group reads each accumulator
+            mbar_init(sm.tempty(b), kCG);  // one arrive per CTA of the group that read it
         }
         mbar_init(sm.done(), 1);
         mbar_init(sm.tready(), 1);
