@@ -48,11 +48,11 @@ WORKLOADS = {"waveq": synth.WAVEQ, "skinny": synth.SKINNY, "large": synth.LARGE,
 NOMINAL_BF16_TFLOPS = 2250.0
 NOMINAL_HBM_GBS = 8000.0
 TRAFFIC = {
-    "waveq_2048x2432x4096/hybrid/tile2@148": {"bytes": 36798976 + 1763072, "kernel_sha": "14675fd62483d21d",
+    "waveq_2048x2432x4096/hybrid/tile2@148": {"bytes": 36805376 + 1889280, "kernel_sha": "42e2e66e1c6e67d8",
                                               "profile": "profiles/sk_gemm_kernel_waveq_2048x2432x4096_pair256_hybrid148.md"},
-    "large_8192x8192x8192/dp/tile2@148": {"bytes": 2166546688 + 129797376, "kernel_sha": "14675fd62483d21d",
+    "large_8192x8192x8192/dp/tile2@148": {"bytes": 2055938304 + 131556608, "kernel_sha": "42e2e66e1c6e67d8",
                                           "profile": "profiles/sk_gemm_kernel_large_8192_pair256_dp148_raster.md"},
-    "large_8192x8192x8192/dp/tile2@148/r0s8": {"bytes": 1064061184 + 126596608, "kernel_sha": "14675fd62483d21d",
+    "large_8192x8192x8192/dp/tile2@148/r0s8": {"bytes": 1050543616 + 127944960, "kernel_sha": "42e2e66e1c6e67d8",
                                                "profile": "profiles/sk_gemm_kernel_large_8192_pair256_dp148_raster.md"},
 }
 
