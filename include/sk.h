@@ -178,13 +178,17 @@ int64_t sk_workspace_size(int32_t M, int32_t N, int32_t K, int32_t num_sms, sk_s
  * [M,N] of c_dtype. Requirements: K % 8 == 0 and N % 8 == 0 (16-byte row strides for
  * the tensor-memory-access loads and vector stores); A and B 16-byte aligned, C
  * 16-byte aligned; inputs must not overlap C or the workspace. M == 0 or N == 0 does
- * nothing; K == 0 writes zeros. The persistent units run as one cooperative launch
- * of `workers` CTAs, one per SM, so workers may not exceed the device's SM count
- * (else SK_ERESIDENCY). Errors are returned before anything is enqueued. A device-side
- * wait that runs past its limit makes the kernel stop early and record SK_ETIMEOUT in
- * the workspace status word (read it with sk_status); C is then undefined and the
- * workspace must be zero-filled again before reuse. Concurrent calls must not share
- * a workspace. */
+ * nothing; K == 0 writes zeros. The persistent units run as one launch in which every
+ * unit (one CTA, or a CTA pair for the pair tiles) is resident at once: a cooperative
+ * launch, or a launch after an occupancy check (pair tiles, and any overlapped launch),
+ * so the units may not exceed what the device holds at once (else SK_ERESIDENCY).
+ * With s.overlap the launch may begin before the kernel ahead of it on the stream has
+ * finished, and waits for it before touching memory. Errors are returned before anything
+ * is enqueued. A device-side wait that runs past its limit makes the kernel stop early and
+ * record SK_ETIMEOUT in the workspace status word (read it with sk_status); C is then
+ * undefined and the workspace must be zero-filled again before reuse. Concurrent calls
+ * must not share a workspace; calls one after another on one stream may, overlapped or
+ * not. */
 int32_t sk_gemm(const void* A, const void* B, void* C, sk_dtype c_dtype,
                 int32_t M, int32_t N, int32_t K, sk_layout layout, sk_schedule s,
                 sk_reduction r, int32_t num_sms, void* workspace, size_t ws_bytes,
