@@ -203,10 +203,13 @@ def run_reference(args, w, rank, world):
     print(json.dumps(line), flush=True)
 
 
-def run_sweep(sk, torch, dev, path, red, flush, stream, peak_tf, dev_sms):
+def run_sweep(sk, torch, dev, path, red, flush, stream, peak_tf, dev_sms, l2_bytes):
     """Tile-count sweep: M = N = 128 .. 4096, K = 4096, every schedule plus the hybrid
     rule's choice, with the pages' 128 x 128 tile and the 256 x 256 CTA-pair tile, on 148
-    SMs and on the device's SM count; one JSON line per point."""
+    SMs and on the device's SM count; one JSON line per point. Each point is timed two ways:
+    `us`, the median of 30 single launches with the L2 flushed before each; and `us_b2b`,
+    60 overlapped launches back to back over rotating copies of A, B and C that together
+    exceed 4x the L2 (the headline's method), mean per launch."""
     with open(path, "w") as f:
         for m in synth.SWEEP_SIZES:
             ww = synth.sweep(m)
@@ -214,6 +217,9 @@ def run_sweep(sk, torch, dev, path, red, flush, stream, peak_tf, dev_sms):
             A = torch.from_numpy(A_bits.view(np.int16)).view(torch.bfloat16).to(dev)
             B = torch.from_numpy(B_bits.view(np.int16)).view(torch.bfloat16).to(dev)
             C = torch.empty((m, m), dtype=torch.bfloat16, device=dev)
+            set_b = (A.numel() + B.numel() + C.numel()) * 2
+            rot = [(A, B, C)] + [(A.clone(), B.clone(), torch.empty_like(C))
+                                 for _ in range(max(2, -(-4 * l2_bytes // set_b)) - 1)]
             fl = 2.0 * m * m * ww.K
             for nsms, tile in ((148, 0), (dev_sms, 0), (148, 2), (dev_sms, 2)):
                 for name, mode, s in (("dp", sk.SK_DP, 1), ("splitk2", sk.SK_SPLITK, 2), ("splitk4", sk.SK_SPLITK, 4),
@@ -235,9 +241,25 @@ def run_sweep(sk, torch, dev, path, red, flush, stream, peak_tf, dev_sms):
                     assert sk.sk_status(ws, stream) == sk.SK_OK
                     t = float(np.median([a.elapsed_time(b) for a, b in ev]))
                     tf = fl / (t / 1e3) / 1e12
+                    sch_o = sk.schedule(mode, s, tile=tile, overlap=1)
+                    for i in range(10):
+                        a_, b_, c_ = rot[i % len(rot)]
+                        sk.sk_gemm(a_, b_, c_, sk.SK_BF16, m, m, ww.K, sk.SK_NN, sch_o, red, nsms, ws, nb, stream)
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    for i in range(60):
+                        a_, b_, c_ = rot[i % len(rot)]
+                        sk.sk_gemm(a_, b_, c_, sk.SK_BF16, m, m, ww.K, sk.SK_NN, sch_o, red, nsms, ws, nb, stream)
+                    e1.record(stream)
+                    torch.cuda.synchronize(dev)
+                    assert sk.sk_status(ws, stream) == sk.SK_OK
+                    tb = e0.elapsed_time(e1) / 60
+                    tfb = fl / (tb / 1e3) / 1e12
                     f.write(json.dumps({"M": m, "N": m, "K": ww.K, "tile": tile, "tiles": int(plan[2]), "num_sms": nsms,
                                         "schedule": name, "resolved_mode": int(plan[1]), "label": int(plan[9]),
-                                        "us": t * 1e3, "tflops": tf, "frac_of_measured_peak": tf / peak_tf}) + "\n")
+                                        "us": t * 1e3, "tflops": tf, "frac_of_measured_peak": tf / peak_tf,
+                                        "us_b2b": tb * 1e3, "tflops_b2b": tfb,
+                                        "frac_of_measured_peak_b2b": tfb / peak_tf, "rotating_sets": len(rot)}) + "\n")
                     f.flush()
 
 
@@ -814,7 +836,7 @@ def main():
         extras["raster_8192"] = run_raster(sk, torch, dev, flush, stream, peak_tf)
 
         if args.sweep:
-            run_sweep(sk, torch, dev, args.sweep, red, flush, stream, peak_tf, dev_sms)
+            run_sweep(sk, torch, dev, args.sweep, red, flush, stream, peak_tf, dev_sms, l2_bytes)
         if args.experiments:
             run_experiments(sk, torch, dev, flush, stream, args.experiments)
 
