@@ -269,21 +269,24 @@ def run_smallm(sk, torch, dev, flush, stream, dev_sms):
     slab; a reduction pass sums them, two launches), the same slabs summed inside the one
     launch (the splits of a tile share the sum when all run at once, else the last to
     arrive sums it), and the owner-wait fixups, timed one GEMM per event pair (L2 flushed
-    before each) and packed 8 back to back (complete GPU time / 8)."""
+    before each), packed 8 back to back (complete GPU time / 8), and (`us_b2b`) 200 overlapped
+    launches back to back over rotating inputs of at least 4x the L2."""
     out = {}
     for w in (synth.SMALLM_96, synth.SMALLM_256):
         A_bits, B_bits = synth.make_inputs(w)
         A = torch.from_numpy(A_bits.view(np.int16)).view(torch.bfloat16).to(dev)
         B = torch.from_numpy(B_bits.view(np.int16)).view(torch.bfloat16).to(dev)
         C = torch.empty((w.M, w.N), dtype=torch.float32, device=dev)
+        set_b = A.numel() * 2 + B.numel() * 2 + C.numel() * 4
+        rot = [(A, B, C)] + [(A.clone(), B.clone(), torch.empty_like(C)) for _ in range(-(-4 * (129 << 20) // set_b) - 1)]
         fl = 2.0 * w.M * w.N * w.K
         rows = {}
-        cases = [(f"slabs_s{s}", sk.schedule(sk.SK_SPLITK, s, split_partials=1), dev_sms) for s in (2, 4, 8, 16)]
-        cases += [(f"slabs_1launch_s{s}", sk.schedule(sk.SK_SPLITK, s, split_partials=2), dev_sms) for s in (2, 4, 8, 16)]
-        cases += [("splitk8_fixup", sk.schedule(sk.SK_SPLITK, 8), dev_sms), ("streamk", sk.schedule(sk.SK_STREAMK), dev_sms),
-                  ("streamk_pass", sk.schedule(sk.SK_STREAMK, split_partials=1), dev_sms),
-                  ("hybrid", sk.schedule(sk.SK_HYBRID), dev_sms)]
-        for name, sch, nsms in cases:
+        kws = [(f"slabs_s{s}", dict(mode=sk.SK_SPLITK, splits=s, split_partials=1)) for s in (2, 4, 8, 16)]
+        kws += [(f"slabs_1launch_s{s}", dict(mode=sk.SK_SPLITK, splits=s, split_partials=2)) for s in (2, 4, 8, 16)]
+        kws += [("splitk8_fixup", dict(mode=sk.SK_SPLITK, splits=8)), ("streamk", dict(mode=sk.SK_STREAMK)),
+                ("streamk_pass", dict(mode=sk.SK_STREAMK, split_partials=1)), ("hybrid", dict(mode=sk.SK_HYBRID))]
+        for name, kw in kws:
+            sch, sch_o, nsms = sk.schedule(**kw), sk.schedule(overlap=1, **kw), dev_sms
             nb = sk.sk_workspace_size(w.M, w.N, w.K, nsms, sch, 0)
             ws = torch.zeros(nb, dtype=torch.uint8, device=dev)
             g = lambda: sk.sk_gemm(A, B, C, sk.SK_F32, w.M, w.N, w.K, sk.SK_NT, sch, 0, nsms, ws, nb, stream)
@@ -308,9 +311,21 @@ def run_smallm(sk, torch, dev, flush, stream, dev_sms):
                 packs.append((a0, a1))
             torch.cuda.synchronize(dev)
             pack8 = float(np.median([a0.elapsed_time(a1) for a0, a1 in packs])) * 1e3 / 8
+            for i in range(20):
+                a_, b_, c_ = rot[i % len(rot)]
+                sk.sk_gemm(a_, b_, c_, sk.SK_F32, w.M, w.N, w.K, sk.SK_NT, sch_o, 0, nsms, ws, nb, stream)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for i in range(200):
+                a_, b_, c_ = rot[i % len(rot)]
+                sk.sk_gemm(a_, b_, c_, sk.SK_F32, w.M, w.N, w.K, sk.SK_NT, sch_o, 0, nsms, ws, nb, stream)
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            b2b = e0.elapsed_time(e1) / 200 * 1e3
             assert sk.sk_status(ws, stream) == sk.SK_OK
             launches = 2 if (name.startswith("slabs_s") or name.endswith("_pass")) else 1
-            rows[name] = {"us": one, "us_pack8": pack8, "launches": launches, "tflops": fl / (one / 1e6) / 1e12}
+            rows[name] = {"us": one, "us_pack8": pack8, "us_b2b": b2b, "launches": launches,
+                          "tflops": fl / (one / 1e6) / 1e12, "tflops_b2b": fl / (b2b / 1e6) / 1e12}
         out[w.name] = rows
     return out
 
