@@ -48,11 +48,11 @@ WORKLOADS = {"waveq": synth.WAVEQ, "skinny": synth.SKINNY, "large": synth.LARGE,
 NOMINAL_BF16_TFLOPS = 2250.0
 NOMINAL_HBM_GBS = 8000.0
 TRAFFIC = {
-    "waveq_2048x2432x4096/hybrid/tile2@148": {"bytes": 36805376 + 1889280, "kernel_sha": "42e2e66e1c6e67d8",
+    "waveq_2048x2432x4096/hybrid/tile2@148": {"bytes": 36806912 + 1764864, "kernel_sha": "8cb49bdcdadc2650",
                                               "profile": "profiles/sk_gemm_kernel_waveq_2048x2432x4096_pair256_hybrid148.md"},
-    "large_8192x8192x8192/dp/tile2@148": {"bytes": 2055938304 + 131556608, "kernel_sha": "42e2e66e1c6e67d8",
+    "large_8192x8192x8192/dp/tile2@148": {"bytes": 2129598464 + 128950528, "kernel_sha": "8cb49bdcdadc2650",
                                           "profile": "profiles/sk_gemm_kernel_large_8192_pair256_dp148_raster.md"},
-    "large_8192x8192x8192/dp/tile2@148/r0s8": {"bytes": 1050543616 + 127944960, "kernel_sha": "42e2e66e1c6e67d8",
+    "large_8192x8192x8192/dp/tile2@148/r0s8": {"bytes": 1064943616 + 126574592, "kernel_sha": "8cb49bdcdadc2650",
                                                "profile": "profiles/sk_gemm_kernel_large_8192_pair256_dp148_raster.md"},
 }
 
@@ -475,7 +475,7 @@ def main():
     ap.add_argument("--splits", type=int, default=2)
     ap.add_argument("--tile", type=int, default=2,
                     help="work-tile shape: 0 = 128x128 (one CTA), 1 = 256x128 (CTA pair), "
-                         "2 = 256x256 (CTA pair), 3 = 128x256 (one CTA)")
+                         "2 = 256x256 (CTA pair), 3 = 128x256 (one CTA), 4 = 256x512 (two CTA pairs, A multicast)")
     ap.add_argument("--reduction", default="deterministic", choices=["deterministic", "atomic"])
     ap.add_argument("--raster", type=int, default=0, choices=[0, 1], help="tile ids along N (0) or M (1)")
     ap.add_argument("--swizzle", type=int, default=0, help="tile-id strips this many tiles deep (0: none)")
@@ -643,12 +643,12 @@ def main():
     if not args.no_extras and rank == 0:
         # ---- per-schedule table (the metric is per schedule)
         table = {}
-        tile_names = {0: "128x128", 1: "pair256x128", 2: "pair256x256", 3: "128x256"}
+        tile_names = {0: "128x128", 1: "pair256x128", 2: "pair256x256", 3: "128x256", 4: "quad256x512"}
         for tile, name, nsms in ((0, "dp", 148), (0, "splitk2", 148), (0, "streamk", 148), (0, "hybrid", 148),
                                  (0, "dp", dev_sms), (0, "hybrid", dev_sms),
                                  (2, "dp", 148), (2, "splitk2", 148), (2, "streamk", 148), (2, "hybrid", 148),
                                  (2, "dp", dev_sms), (2, "hybrid", dev_sms),
-                                 (3, "hybrid", 148), (1, "hybrid", 148)):
+                                 (3, "hybrid", 148), (1, "hybrid", 148), (4, "hybrid", 144), (4, "dp", 144)):
             mname = "splitk" if name.startswith("splitk") else name
             s2, ws2, nb2 = make(mname, nsms, 2, tile)
             t = timed(s2, ws2, nb2, nsms, 200, 10)
@@ -664,7 +664,7 @@ def main():
         # overlapped launch: what a stream of GEMMs pays per step beyond the kernel itself.
         b2b = {}
         for tile, name, nsms in ((2, "hybrid", 148), (2, "dp", 148), (2, "streamk", 148), (0, "hybrid", 148),
-                                 (2, "hybrid", dev_sms)):
+                                 (2, "hybrid", dev_sms), (4, "hybrid", 144), (4, "dp", 144)):
             mname = "splitk" if name.startswith("splitk") else name
             row = {}
             for ov in (0, 1):
@@ -746,7 +746,11 @@ def main():
                 commit = np.array([st[c][-1, 1] for c in lead])
                 tail = np.array([end[c] - st[c][-1, 1] for c in lead]) / 1e3
                 late = sorted(lead, key=lambda c: -end[c])[:3]
+                span = np.maximum(T[:, 1] - T[:, 0], 1)
                 out.append({"start": int(T[:, 0].min()), "end": int(end.max()),
+                            # SM clock while each CTA ran (its cycle count over its span): under a
+                            # full tensor load it sits below the clock nvidia-smi samples report.
+                            "sm_clock_mhz_in_kernel_median": float(np.median(T[:, 3] / span * 1e3)),
                             "first_mma_after_start_us_median": float(np.median(first)),
                             "last_commit_spread_us": float((commit.max() - commit.min()) / 1e3),
                             "end_spread_us": float((end.max() - end.min()) / 1e3),
@@ -870,7 +874,8 @@ def main():
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "layout": w.layout, "out": w.out,
                    "schedule": args.mode, "split_partials": args.partials, "reduction": args.reduction, "num_sms": sms, "device_sms": dev_sms,
-                   "tile": {0: "128x128", 1: "256x128 CTA pair", 2: "256x256 CTA pair", 3: "128x256"}[args.tile],
+                   "tile": {0: "128x128", 1: "256x128 CTA pair", 2: "256x256 CTA pair", 3: "128x256",
+                            4: "256x512 two CTA pairs, A multicast"}[args.tile],
                    "tile_m": int(plan[12]), "tile_n": int(plan[13]), "ctas_per_tile": int(plan[14]),
                    "raster": "along_n" if args.raster == 0 else "along_m", "swizzle": args.swizzle,
                    "tiles": int(plan[2]), "iters": int(plan[3]), "workers": int(plan[4]),

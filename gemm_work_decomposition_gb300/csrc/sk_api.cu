@@ -72,6 +72,9 @@ int32_t make_sched(int32_t M, int32_t N, int32_t K, int32_t num_sms, const sk_sc
     if (s.split_partials != 0 && s.mode == SK_DP) return SK_EINVAL;
     int32_t tm = 0, tn = 0, cg = 0;
     if (!tile_shape(s.tile, &tm, &tn, &cg)) return SK_EINVAL;
+    // The four-CTA tile runs data-parallel, Stream-K and the hybrid rule with the in-kernel
+    // fixup only (no Split-K slabs, no separate pass).
+    if (cg == 4 && (s.mode == SK_SPLITK || s.split_partials != 0)) return SK_EINVAL;
     if (s.raster < 0 || s.raster > 1 || s.swizzle < 0 || s.swizzle > 256) return SK_EINVAL;
     if (s.overlap < 0 || s.overlap > 1) return SK_EINVAL;
     const int64_t tiles_n = (static_cast<int64_t>(N) + tn - 1) / tn;
@@ -172,7 +175,7 @@ struct DeviceInfo {
     bool ready = false;
     cudaError_t err = cudaSuccess;
     int sms = 0;
-    int max_units[4] = {0, 0, 0, 0};  // resident units per sk_tile value
+    int max_units[kTileShapes] = {};  // resident units per sk_tile value
 };
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_mu;
@@ -190,7 +193,7 @@ cudaError_t device_info(int* sms, int* max_units) {
         d.ready = true;
     }
     *sms = d.sms;
-    for (int i = 0; i < 4; ++i) max_units[i] = d.max_units[i];
+    for (int i = 0; i < kTileShapes; ++i) max_units[i] = d.max_units[i];
     return d.err;
 }
 
@@ -346,7 +349,7 @@ int32_t sk_gemm_debug(const void* A, const void* B, void* C, sk_dtype c_dtype, i
     const int64_t need = workspace_bytes(sch, M, N);
     if (!workspace || !aligned(workspace, 256) || static_cast<int64_t>(ws_bytes) < need) return SK_EWORKSPACE;
 
-    int dev_sms = 0, max_units[4];
+    int dev_sms = 0, max_units[kTileShapes];
     if (device_info(&dev_sms, max_units) != cudaSuccess) return SK_ECUDA;
     if (sch.workers > max_units[s.tile]) return SK_ERESIDENCY;
 
@@ -427,7 +430,7 @@ int32_t sk_reduce_splits(const float* P, void* C, sk_dtype c_dtype, int32_t spli
     if (c_dtype != SK_F32 && c_dtype != SK_BF16) return SK_EINVAL;
     if (mn == 0) return SK_OK;
     if (!P || !C || !aligned(P, 16) || !aligned(C, 16)) return SK_EINVAL;
-    int dev_sms = 0, max_units[4];
+    int dev_sms = 0, max_units[kTileShapes];
     if (device_info(&dev_sms, max_units) != cudaSuccess) return SK_ECUDA;
     if (launch_reduce(P, C, c_dtype == SK_BF16 ? 1 : 0, splits, mn, dev_sms, false, static_cast<cudaStream_t>(stream)) !=
         cudaSuccess) {

@@ -73,6 +73,16 @@ __device__ __forceinline__ void record_timeout(const KArgs& a, volatile int* abo
     atomicCAS(a.status, 0, kErrTimeout);
 }
 
+// Where a CTA sits in its work tile: `rank` in its MMA pair (0 = the pair's leader, which
+// issues the MMAs; its rows are rank * 128 ..), `pair` among the tile's pairs (its columns
+// are pair * kBN ..), and `cta` = 2 * pair + rank among the tile's CTAs (its block of every
+// partial slot and its flag). One-CTA tiles: all zero.
+struct CtaPos {
+    uint32_t rank;
+    int pair;
+    int cta;
+};
+
 // A Stream-K producer segment covers [k_begin, iters) of its tile: it runs its k-loop from
 // the last k-iteration down, so that all units start on the same k-slab of A and B (shared
 // through L2) instead of each on its own (an HBM burst of every unit's data at once when
@@ -92,7 +102,7 @@ __device__ __forceinline__ int32_t seg_k(const Seg& g, bool rev, int32_t i) {
 // partial copies of each epilogue warp into its ring quarter, while the epilogue is still
 // storing the segment before. Returns false when a wait gave up.
 template <int kCG, int kBN>
-__device__ bool prefetch_partials(const KArgs& a, const Smem<Shape<kCG, kBN>>& sm, const Seg& g, uint32_t rank,
+__device__ bool prefetch_partials(const KArgs& a, const Smem<Shape<kCG, kBN>>& sm, const Seg& g, const CtaPos& pos,
                                   uint32_t issued, uint64_t deadline, volatile int* abort_flag, int* prefetch) {
     using S = Shape<kCG, kBN>;
     // Indices outside the workspace: leave the segment to the epilogue, which reports them.
@@ -100,7 +110,7 @@ __device__ bool prefetch_partials(const KArgs& a, const Smem<Shape<kCG, kBN>>& s
         g.peer_begin + g.n_peers > a.sch.n_slots)
         return true;
     for (int32_t pi = 0; pi < g.n_peers; ++pi) {
-        const int32_t* f = a.flags + (g.peer_begin + pi) * kCG + static_cast<int32_t>(rank);
+        const int32_t* f = a.flags + (g.peer_begin + pi) * a.sch.cg + pos.cta;
         for (uint32_t n = 0; ld_acquire_gpu(f) < 1; ++n) {
             if ((n & 15u) == 15u && (*abort_flag || globaltimer() > deadline)) return false;
             __nanosleep(32);
@@ -110,14 +120,14 @@ __device__ bool prefetch_partials(const KArgs& a, const Smem<Shape<kCG, kBN>>& s
     // phase pos / kStages (as in the loop above, these are the only phases still open).
     const uint32_t tail = issued < static_cast<uint32_t>(S::kStages) ? issued : S::kStages;
     for (uint32_t i = 0; i < tail; ++i) {
-        const uint32_t pos = issued - 1 - i;
-        if (!mbar_wait(sm.empty(pos % S::kStages), (pos / S::kStages) & 1u, abort_flag, deadline)) return false;
+        const uint32_t n = issued - 1 - i;
+        if (!mbar_wait(sm.empty(n % S::kStages), (n / S::kStages) & 1u, abort_flag, deadline)) return false;
     }
     const int k = S::kPasses * g.n_peers > 1 ? 2 : 1;
     if (atomicCAS(prefetch, 0, kPrefetchIssued + k) != 0) return true;  // the epilogue has given up
     fence_proxy_async_global();  // the flag acquires before the copies' reads
     for (int ew = 0; ew < 4; ++ew)
-        for (int j = 0; j < k; ++j) fetch_partial(a, sm, g, rank, ew, j);
+        for (int j = 0; j < k; ++j) fetch_partial(a, sm, g, pos.cta, ew, j);
     return true;
 }
 
@@ -127,7 +137,7 @@ __device__ bool prefetch_partials(const KArgs& a, const Smem<Shape<kCG, kBN>>& s
 // loads read: if the previous kernel writes these bytes, L2 holds its writes.
 template <bool kNT, int kCG, int kBN>
 __device__ void prefetch_first_loads(const KArgs& a, const CUtensorMap* tmA, const CUtensorMap* tmB, int unit,
-                                     uint32_t rank) {
+                                     const CtaPos& pos) {
     using S = Shape<kCG, kBN>;
     Walk w;
     w.init(a.sch, unit);
@@ -136,8 +146,8 @@ __device__ void prefetch_first_loads(const KArgs& a, const CUtensorMap* tmA, con
     while (n < S::kStages && w.next(a.sch, g)) {
         int32_t trow, tcolumn;
         tile_coords(a.sch, g.tile, &trow, &tcolumn);
-        const int32_t m0 = trow * (kCtaRows * kCG) + static_cast<int32_t>(rank) * kCtaRows;
-        const int32_t nb = tcolumn * kBN + static_cast<int32_t>(rank) * S::kBNc;
+        const int32_t m0 = trow * (kCtaRows * kCG) + static_cast<int32_t>(pos.rank) * kCtaRows;
+        const int32_t nb = tcolumn * a.sch.tile_n + pos.pair * kBN + static_cast<int32_t>(pos.rank) * S::kBNc;
         const bool rev = reversed_segment(a.sch, g);
         for (int32_t i = 0; i < g.k_end - g.k_begin && n < S::kStages; ++i, ++n) {
             const int32_t k0 = seg_k(g, rev, i) * kBlkK;
@@ -152,11 +162,16 @@ __device__ void prefetch_first_loads(const KArgs& a, const CUtensorMap* tmA, con
     }
 }
 
-template <bool kNT, int kCG, int kBN>
+// kMC = 2 (the four-CTA tile): the two pairs compute the tile's two column halves over the same
+// rows, so pair 0 loads each half of A once and multicasts it to the same-rank CTA of both
+// pairs; pair 1 loads only its B. Every CTA waits until both pairs have consumed a stage (its
+// empty barrier counts one commit per pair) before anything lands there again.
+template <bool kNT, int kCG, int kBN, int kMC>
 __device__ void run_producer(const KArgs& a, const CUtensorMap* tmA, const CUtensorMap* tmB,
-                             const Smem<Shape<kCG, kBN>>& sm, int unit, uint32_t rank, uint64_t deadline,
+                             const Smem<Shape<kCG, kBN>>& sm, int unit, const CtaPos& pos, uint64_t deadline,
                              volatile int* abort_flag, int* prefetch) {
     using S = Shape<kCG, kBN>;
+    const uint32_t rank = pos.rank;
     Walk w;
     w.init(a.sch, unit);
     Seg g, last;
@@ -172,7 +187,7 @@ __device__ void run_producer(const KArgs& a, const CUtensorMap* tmA, const CUten
         int32_t trow, tcolumn;
         tile_coords(a.sch, g.tile, &trow, &tcolumn);
         const int32_t m0 = trow * (kCtaRows * kCG) + static_cast<int32_t>(rank) * kCtaRows;
-        const int32_t nb = tcolumn * kBN + static_cast<int32_t>(rank) * S::kBNc;
+        const int32_t nb = tcolumn * a.sch.tile_n + pos.pair * kBN + static_cast<int32_t>(rank) * S::kBNc;
         const bool rev = reversed_segment(a.sch, g);
         for (int32_t i = 0; i < g.k_end - g.k_begin; ++i) {
             if (!mbar_wait(sm.empty(stage), phase ^ 1u, abort_flag, deadline)) {
@@ -193,9 +208,13 @@ __device__ void run_producer(const KArgs& a, const CUtensorMap* tmA, const CUten
             } else {
                 // Both CTAs' loads complete on the leader's barrier, which the leader arms
                 // for the bytes of both.
-                const uint32_t fb = mapa_shared(sm.full(stage), 0);
+                const uint32_t fb = mapa_shared(sm.full(stage), static_cast<uint32_t>(2 * pos.pair));
                 if (rank == 0) mbar_arrive_expect_tx(sm.full(stage), S::kTxBytes);
-                tma_load_2d_pair(sm.a(stage), tmA, fb, k0, m0);
+                if (kMC == 1)
+                    tma_load_2d_pair(sm.a(stage), tmA, fb, k0, m0);
+                else if (pos.pair == 0)
+                    tma_load_2d_pair_mc(sm.a(stage), tmA, fb, k0, m0,
+                                        static_cast<uint16_t>((1u << rank) | (1u << (rank + 2))));
                 if (kNT) {
                     tma_load_2d_pair(sm.b(stage), tmB, fb, k0, nb);
                 } else {
@@ -212,10 +231,10 @@ __device__ void run_producer(const KArgs& a, const CUtensorMap* tmA, const CUten
         }
     }
     if (ok && kEpiGroups == 1 && nseg > 0 && last.role == kOwner && !a.sch.sep && !a.atomic)
-        ok = prefetch_partials<kCG, kBN>(a, sm, last, rank, issued, deadline, abort_flag, prefetch);
+        ok = prefetch_partials<kCG, kBN>(a, sm, last, pos, issued, deadline, abort_flag, prefetch);
     if (!ok) record_timeout(a, abort_flag);
-    // Let the last loads land before the CTA can exit (bounded). A pair's loads all
-    // complete on the leader's barriers, so the leader drains for both.
+    // Let the last loads land before the CTA can exit (bounded). A pair's loads (and the A
+    // multicast into it) all complete on the leader's barriers, so the leader drains for both.
     if (rank == 0) {
         const uint64_t drain = globaltimer() + kDrainNs;
         const uint32_t outstanding = issued < static_cast<uint32_t>(S::kStages) ? issued : S::kStages;
@@ -227,10 +246,15 @@ __device__ void run_producer(const KArgs& a, const CUtensorMap* tmA, const CUten
 }
 
 // --------------------------------------------------------------------------- warp 1
-template <bool kNT, int kCG, int kBN>
-__device__ void run_mma(const KArgs& a, const Smem<Shape<kCG, kBN>>& sm, uint32_t tmem_base, int unit,
+// The leader of each pair issues its pair's MMAs. Its commits reach both CTAs of the pair
+// (cluster ranks 2 * pair and 2 * pair + 1), and with kMC = 2 a stage's commit reaches all
+// four CTAs, since a stage of A lands in both pairs.
+template <bool kNT, int kCG, int kBN, int kMC>
+__device__ void run_mma(const KArgs& a, const Smem<Shape<kCG, kBN>>& sm, uint32_t tmem_base, int unit, int pair,
                         uint64_t deadline, volatile int* abort_flag) {
     using S = Shape<kCG, kBN>;
+    const uint16_t pair_mask = static_cast<uint16_t>(0x3u << (2 * pair));
+    const uint16_t stage_mask = kMC == 2 ? static_cast<uint16_t>(0xF) : pair_mask;
     constexpr uint32_t kIdesc = idesc_bf16_f32(kCtaRows * kCG, kBN, kNT ? 0u : 1u);
     // K advance per 16-deep MMA inside one 64-deep stage: K-major operands move 32 bytes
     // along the swizzled row; the MN-major B of NN moves 16 rows of 128 bytes.
@@ -278,7 +302,7 @@ __device__ void run_mma(const KArgs& a, const Smem<Shape<kCG, kBN>>& sm, uint32_
             if (kCG == 1)
                 umma_commit(sm.empty(stage));
             else
-                umma_commit_pair(sm.empty(stage), 0x3);
+                umma_commit_pair(sm.empty(stage), stage_mask);
             if (++stage == S::kStages) {
                 stage = 0;
                 phase ^= 1u;
@@ -288,7 +312,7 @@ __device__ void run_mma(const KArgs& a, const Smem<Shape<kCG, kBN>>& sm, uint32_
         if (kCG == 1)
             umma_commit(sm.tfull(buf));
         else
-            umma_commit_pair(sm.tfull(buf), 0x3);
+            umma_commit_pair(sm.tfull(buf), pair_mask);
         if (tr && seg < kTraceSegs) tr[4 + 4 * seg + 1] = globaltimer();
         ++seg;
         if (buf)
@@ -303,7 +327,7 @@ __device__ void run_mma(const KArgs& a, const Smem<Shape<kCG, kBN>>& sm, uint32_
     if (kCG == 1)
         umma_commit(sm.done());
     else
-        umma_commit_pair(sm.done(), 0x1);
+        umma_commit_pair(sm.done(), static_cast<uint16_t>(0x1u << (2 * pair)));
     mbar_wait_until(sm.done(), 0u, globaltimer() + kDrainNs);
 }
 
@@ -343,13 +367,11 @@ __device__ __forceinline__ int slot_f4(int c, int q, int lane) { return ((c * 8 
 // bulk copy, completing on that buffer's barrier. Warp ew + 2 reads TMEM lane quadrant
 // (ew + 2) % 4, whose rows are block (ew + 2) % 4 of the slot.
 template <class S>
-__device__ __forceinline__ void fetch_partial(const KArgs& a, const Smem<S>& sm, const Seg& g, uint32_t rank, int ew,
-                                              int j) {
+__device__ __forceinline__ void fetch_partial(const KArgs& a, const Smem<S>& sm, const Seg& g, int cta, int ew, int j) {
     constexpr int kChunks = kPassCols / 32;
     const int p = j / g.n_peers, pi = j % g.n_peers;
     const int quad = (ew + 2) & 3;
-    const float* src = a.slots + static_cast<int64_t>((g.peer_begin + pi) * S::kCtas + static_cast<int32_t>(rank)) *
-                                     S::kCtaSlotFloats +
+    const float* src = a.slots + static_cast<int64_t>((g.peer_begin + pi) * a.sch.cg + cta) * S::kCtaSlotFloats +
                        static_cast<int64_t>(quad) * S::kWarpSlotFloats + slot_f4(kChunks * p, 0, 0);
     const uint32_t bar = sm.pload(ew, j & 1);
     mbar_arrive_expect_tx(bar, kPartBytes);
@@ -531,7 +553,9 @@ struct Epi {
     uint64_t deadline;
     volatile int* abort_flag;
     int lane, gt, quad, row;     // gt: thread index within the group
-    int32_t r;
+    int32_t r;                   // rank in the MMA pair: this CTA's rows are r * 128 .. of the tile
+    int pair;                    // pair within the tile: its columns are pair * kBN ..
+    int cta;                     // CTA within the tile: its block of a partial slot, its flags
     uint32_t tcol, staging, nstore;
     uint32_t nbuf;               // staging buffers in turn: kBoxes, or more in the ring (see `wide`)
     uint32_t ring;               // this warp's quarter of the ring (free once the unit's MAC loop is over)
@@ -547,7 +571,7 @@ struct Epi {
     volatile int* last_flag;     // shared word: this group took a tile's last slab
 
     __device__ __forceinline__ float* block(int32_t slot) const {
-        return a.slots + static_cast<int64_t>(slot * kCG + r) * S::kCtaSlotFloats + blk_off;
+        return a.slots + static_cast<int64_t>(slot * a.sch.cg + cta) * S::kCtaSlotFloats + blk_off;
     }
 
     // Split-K slabs, last arriver: this CTA's rows of tile g.tile in C = P[0] + P[1] + ...
@@ -556,7 +580,7 @@ struct Epi {
         int32_t trow, tcolumn;
         tile_coords(a.sch, g.tile, &trow, &tcolumn);
         const int32_t m0 = trow * (kCtaRows * kCG) + r * kCtaRows;
-        const int32_t n0 = tcolumn * kBN;
+        const int32_t n0 = tcolumn * a.sch.tile_n + pair * kBN;
         const int32_t gr = m0 + row;
         const int64_t slab = static_cast<int64_t>(a.M) * a.N;
 #pragma unroll 1
@@ -607,7 +631,7 @@ struct Epi {
         const int32_t r_begin = g.slot * rows_per;
         const int32_t r_end = imin(kCtaRows, r_begin + rows_per);
         const int32_t m0 = trow * (kCtaRows * kCG) + r * kCtaRows;
-        const int32_t n0 = tcolumn * kBN;
+        const int32_t n0 = tcolumn * a.sch.tile_n + pair * kBN;
         const int64_t slab = static_cast<int64_t>(a.M) * a.N;
         constexpr int kGroups = kBN / 4;  // 4-column groups per row
         constexpr int kBatch = 8;
@@ -699,11 +723,12 @@ struct Epi {
         int32_t trow, tcolumn;
         tile_coords(a.sch, g.tile, &trow, &tcolumn);
         const int32_t m0 = trow * (kCtaRows * kCG) + r * kCtaRows;
-        const int32_t n0 = tcolumn * kBN;
+        const int32_t n0 = tcolumn * a.sch.tile_n + pair * kBN;
         const int32_t wy = m0 + quad * 32;  // first row of this warp's 32
         float* dump = a.dump ? a.dump +
-                                   (static_cast<int64_t>(g.tile) * a.sch.iters + g.k_begin) * (kCtaRows * kCG * kBN) +
-                                   static_cast<int64_t>(r * kCtaRows + row) * kBN
+                                   (static_cast<int64_t>(g.tile) * a.sch.iters + g.k_begin) *
+                                       (static_cast<int64_t>(kCtaRows * kCG) * a.sch.tile_n) +
+                                   static_cast<int64_t>(r * kCtaRows + row) * a.sch.tile_n + pair * kBN
                              : nullptr;
         float v[kPassCols];
         if (kFixup && !bulk) {
@@ -712,10 +737,10 @@ struct Epi {
             // still running.
             bool ok = true;
             if (a.atomic) {
-                ok = wait_flag(a.flags + g.peer_begin * kCG + r, g.n_peers, deadline, abort_flag);
+                ok = wait_flag(a.flags + g.peer_begin * a.sch.cg + cta, g.n_peers, deadline, abort_flag);
             } else {
                 for (int32_t pi = 0; pi < g.n_peers && ok; ++pi)
-                    ok = wait_flag(a.flags + (g.peer_begin + pi) * kCG + r, 1, deadline, abort_flag);
+                    ok = wait_flag(a.flags + (g.peer_begin + pi) * a.sch.cg + cta, 1, deadline, abort_flag);
             }
             if (named_bar_or(kBar, kGroupThreads, !ok)) {
                 record_timeout(a, abort_flag);
@@ -825,7 +850,7 @@ struct Epi {
                             // producer warp's flag acquires, before this copy.
                             fence_proxy_async_smem();
                             fence_proxy_async_global();
-                            fetch_partial(a, sm, g, static_cast<uint32_t>(r), ew, j + 2);
+                            fetch_partial(a, sm, g, cta, ew, j + 2);
                         }
                         ++issued;
                     }
@@ -891,7 +916,7 @@ struct Epi {
             }
             __syncwarp();
             named_bar_sync(kBar, kGroupThreads);
-            int32_t* cnt = a.counters + g.tile * kCG + r;
+            int32_t* cnt = a.counters + g.tile * a.sch.cg + cta;
             if (a.sch.coop) {
                 // Every split of the tile is running (one work item per unit): wait until all
                 // have arrived, then each sums its share of the rows. The counter goes on to
@@ -912,10 +937,10 @@ struct Epi {
             if (gt == 0) *last_flag = atom_add_acq_rel_gpu(cnt, 1) == static_cast<uint32_t>(a.sch.splits - 1);
             named_bar_sync(kBar, kGroupThreads);
             if (*last_flag) {
-                (void)ld_acquire_gpu(a.counters + g.tile * kCG + r);
+                (void)ld_acquire_gpu(a.counters + g.tile * a.sch.cg + cta);
                 reduce_slabs(g);
                 named_bar_sync(kBar, kGroupThreads);
-                if (gt == 0) a.counters[g.tile * kCG + r] = 0;
+                if (gt == 0) a.counters[g.tile * a.sch.cg + cta] = 0;
             }
         } else if (g.role == kProducer && !a.sch.sep) {
             // Every epilogue thread's share is stored: publish it. Each warp's bulk copies
@@ -930,9 +955,9 @@ struct Epi {
             named_bar_sync(kBar, kGroupThreads);
             if (gt == 0 && !a.skip_signal) {
                 if (a.atomic)
-                    red_release_add_gpu(a.flags + g.peer_begin * kCG + r, 1);
+                    red_release_add_gpu(a.flags + g.peer_begin * a.sch.cg + cta, 1);
                 else
-                    st_release_gpu(a.flags + g.slot * kCG + r, 1);
+                    st_release_gpu(a.flags + g.slot * a.sch.cg + cta, 1);
             }
         } else if (kFixup) {
             // Every epilogue thread has read the partials: re-arm the flags / counter. (With
@@ -941,9 +966,9 @@ struct Epi {
             if (!bulk) named_bar_sync(kBar, kGroupThreads);
             if (gt == 0) {
                 if (a.atomic) {
-                    a.flags[g.peer_begin * kCG + r] = 0;
+                    a.flags[g.peer_begin * a.sch.cg + cta] = 0;
                 } else {
-                    for (int32_t pi = 0; pi < g.n_peers; ++pi) a.flags[(g.peer_begin + pi) * kCG + r] = 0;
+                    for (int32_t pi = 0; pi < g.n_peers; ++pi) a.flags[(g.peer_begin + pi) * a.sch.cg + cta] = 0;
                 }
             }
         }
@@ -953,7 +978,7 @@ struct Epi {
 
 template <int kCG, int kBN, int kGroup>
 __device__ void run_epilogue_group(const KArgs& a, const CUtensorMap* tmC, const CUtensorMap* tmD,
-                                   const Smem<Shape<kCG, kBN>>& sm, uint32_t tmem_base, int unit, uint32_t rank,
+                                   const Smem<Shape<kCG, kBN>>& sm, uint32_t tmem_base, int unit, const CtaPos& pos,
                                    uint64_t deadline, volatile int* abort_flag, volatile int* last_flag,
                                    int* prefetch, volatile int* shared_tmp) {
     using S = Shape<kCG, kBN>;
@@ -965,7 +990,9 @@ __device__ void run_epilogue_group(const KArgs& a, const CUtensorMap* tmC, const
     e.gt = (ew & 3) * 32 + e.lane;            // index within the group
     e.quad = warp & 3;                        // TMEM lanes this warp may read: 32*quad ..
     e.row = e.quad * 32 + e.lane;             // row of this CTA's part of the tile
-    e.r = static_cast<int32_t>(rank);
+    e.r = static_cast<int32_t>(pos.rank);
+    e.pair = pos.pair;
+    e.cta = pos.cta;
     e.tcol = static_cast<uint32_t>(e.quad * 32) << 16;
     e.staging = sm.base + S::kStagingOff + static_cast<uint32_t>(ew * kBoxes) * 4096u;
     e.nstore = 0;
@@ -976,9 +1003,10 @@ __device__ void run_epilogue_group(const KArgs& a, const CUtensorMap* tmC, const
     e.ew = ew;
     e.prefetch = prefetch;
     e.shared_tmp = shared_tmp;
-    // The accumulator-empty barriers live in the leader CTA.
-    e.tempty0 = kCG == 1 ? sm.tempty(0) : mapa_shared(sm.tempty(0), 0);
-    e.tempty1 = kCG == 1 ? sm.tempty(1) : mapa_shared(sm.tempty(1), 0);
+    // The accumulator-empty barriers live in the pair's leader CTA.
+    const uint32_t leader = static_cast<uint32_t>(2 * pos.pair);
+    e.tempty0 = kCG == 1 ? sm.tempty(0) : mapa_shared(sm.tempty(0), leader);
+    e.tempty1 = kCG == 1 ? sm.tempty(1) : mapa_shared(sm.tempty(1), leader);
     e.blk_off = static_cast<int64_t>(e.quad) * S::kWarpSlotFloats;
     e.buf = 0;
     e.uses0 = e.uses1 = 0u;
@@ -1024,19 +1052,21 @@ __device__ void run_epilogue_group(const KArgs& a, const CUtensorMap* tmC, const
 // Epilogue warps: group 0 (warps 2-5) and, with two groups, group 1 (warps 6-9).
 template <int kCG, int kBN>
 __device__ void run_epilogue(const KArgs& a, const CUtensorMap* tmC, const CUtensorMap* tmD,
-                             const Smem<Shape<kCG, kBN>>& sm, uint32_t tmem_base, int unit, uint32_t rank,
+                             const Smem<Shape<kCG, kBN>>& sm, uint32_t tmem_base, int unit, const CtaPos& pos,
                              uint64_t deadline, volatile int* abort_flag, volatile int* last_flag, int* prefetch,
                              volatile int* shared_tmp) {
     if (kEpiGroups == 1 || (threadIdx.x >> 5) < 6)
-        run_epilogue_group<kCG, kBN, 0>(a, tmC, tmD, sm, tmem_base, unit, rank, deadline, abort_flag, last_flag,
+        run_epilogue_group<kCG, kBN, 0>(a, tmC, tmD, sm, tmem_base, unit, pos, deadline, abort_flag, last_flag,
                                         prefetch, shared_tmp);
     else
-        run_epilogue_group<kCG, kBN, 1>(a, tmC, tmD, sm, tmem_base, unit, rank, deadline, abort_flag, last_flag,
+        run_epilogue_group<kCG, kBN, 1>(a, tmC, tmD, sm, tmem_base, unit, pos, deadline, abort_flag, last_flag,
                                         prefetch, shared_tmp);
 }
 
 // --------------------------------------------------------------------------- kernel
-template <bool kNT, int kCG, int kBN>
+// kCG CTAs per MMA (1, or a pair with cta_group::2); kMC pairs per work tile (2: the four-CTA
+// tile, one cluster of two pairs sharing A by multicast); kBN accumulator columns per CTA.
+template <bool kNT, int kCG, int kBN, int kMC>
 __global__ void __launch_bounds__(kThreads, 1)
     sk_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmD,
@@ -1053,15 +1083,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const uint32_t rank = kCG == 2 ? cluster_ctarank() : 0u;
-    const int units = static_cast<int>(gridDim.x) / kCG;
-    const int cid = static_cast<int>(blockIdx.x) / kCG;
+    static_assert(kMC == 1 || (kMC == 2 && kCG == 2), "A is shared between CTA pairs only");
+    constexpr int kTileCtas = kCG * kMC;
+    const uint32_t crank = kCG == 2 ? cluster_ctarank() : 0u;
+    const CtaPos pos{crank & 1u, static_cast<int>(crank >> 1), static_cast<int>(crank)};
+    const uint32_t rank = pos.rank;
+    const int units = static_cast<int>(gridDim.x) / kTileCtas;
+    const int cid = static_cast<int>(blockIdx.x) / kTileCtas;
     const int unit = args.reverse ? units - 1 - cid : cid;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S::kStages; ++s) {
             mbar_init(sm.full(s), 1);
-            mbar_init(sm.empty(s), 1);
+            mbar_init(sm.empty(s), kMC);  // one commit per pair that reads the stage
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(sm.tfull(b), 1);
@@ -1081,8 +1115,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tmap(&tmC);
         prefetch_tmap(&tmD);
     }
-    // Barriers are initialised (in both CTAs of a pair) before anyone signals them. TMEM is
-    // allocated afterwards, while the producer's first loads are already in flight.
+    // Barriers are initialised (in every CTA of the cluster) before anyone signals them. TMEM
+    // is allocated afterwards, while the producer's first loads are already in flight.
     if (kCG == 2)
         cluster_sync();
     else
@@ -1095,14 +1129,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the wait. Every thread signals the next overlapped launch once it is past its wait, so
     // that launch may begin when all of this grid's CTAs are.
     uint32_t tmem_base = 0;
+    uint64_t start_clk = 0;  // thread 0, traced launches: SM clock at the start stamp
     if (warp == 0) {
-        if (args.sch.overlap && lane == 0) prefetch_first_loads<kNT, kCG, kBN>(args, &tmA, &tmB, unit, rank);
+        if (args.sch.overlap && lane == 0) prefetch_first_loads<kNT, kCG, kBN>(args, &tmA, &tmB, unit, pos);
         grid_dep_wait();
         grid_dep_launch();
         const uint64_t deadline = globaltimer() + args.timeout_ns;  // wait limits count from here
         if (lane == 0) {
-            if (args.trace) args.trace[static_cast<int64_t>(blockIdx.x) * kTraceWords] = globaltimer();
-            run_producer<kNT, kCG, kBN>(args, &tmA, &tmB, sm, unit, rank, deadline, abort_flag, prefetch);
+            if (args.trace) {
+                args.trace[static_cast<int64_t>(blockIdx.x) * kTraceWords] = globaltimer();
+                start_clk = clock64();
+            }
+            run_producer<kNT, kCG, kBN, kMC>(args, &tmA, &tmB, sm, unit, pos, deadline, abort_flag, prefetch);
         }
         // Warps 0 and 1 reconverge before the exit barrier: a CTA barrier counts a warp once
         // any of its threads arrives, so all 32 lanes must arrive together.
@@ -1120,14 +1158,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         // leader's own allocation precedes its MMAs in this warp's program order).
         tc_fence_before();
         named_bar_arrive(2, 32 + kEpiThreads);
-        if (kCG == 2 && rank != 0 && lane == 0) mbar_arrive_cluster(mapa_shared(sm.tready(), 0));
+        if (kCG == 2 && rank != 0 && lane == 0)
+            mbar_arrive_cluster(mapa_shared(sm.tready(), static_cast<uint32_t>(2 * pos.pair)));
         __syncwarp();
         tc_fence_after();
         tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_holder);
         grid_dep_wait();
         grid_dep_launch();
         const uint64_t deadline = globaltimer() + args.timeout_ns;
-        if (lane == 0 && rank == 0) run_mma<kNT, kCG, kBN>(args, sm, tmem_base, unit, deadline, abort_flag);
+        if (lane == 0 && rank == 0)
+            run_mma<kNT, kCG, kBN, kMC>(args, sm, tmem_base, unit, pos.pair, deadline, abort_flag);
         __syncwarp();
     } else {
         named_bar_sync(2, 32 + kEpiThreads);
@@ -1136,7 +1176,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         grid_dep_wait();
         grid_dep_launch();
         const uint64_t deadline = globaltimer() + args.timeout_ns;
-        run_epilogue<kCG, kBN>(args, &tmC, &tmD, sm, tmem_base, unit, rank, deadline, abort_flag, last_flag, prefetch,
+        run_epilogue<kCG, kBN>(args, &tmC, &tmD, sm, tmem_base, unit, pos, deadline, abort_flag, last_flag, prefetch,
                                shared_tmp);
     }
 
@@ -1145,8 +1185,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         cluster_sync();
     else
         __syncthreads();
-    if (args.trace && threadIdx.x == 0)
+    if (args.trace && threadIdx.x == 0) {
         args.trace[static_cast<int64_t>(blockIdx.x) * kTraceWords + 1] = globaltimer();
+        args.trace[static_cast<int64_t>(blockIdx.x) * kTraceWords + 3] = static_cast<uint64_t>(clock64()) - start_clk;
+    }
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
@@ -1167,12 +1209,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 // attribute. Its CTAs can only start once every CTA of the previous overlapped grid is past
 // its own wait (each issues grid_dep_launch there), and they hold SMs only where the
 // previous kernel's CTAs have left; once that kernel completes, all of this grid fits.
-template <bool kNT, int kCG, int kBN>
+template <bool kNT, int kCG, int kBN, int kMC>
 cudaError_t launch_shape(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
                          const CUtensorMap& tmD, const KArgs& a, cudaStream_t stream) {
     using S = Shape<kCG, kBN>;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(a.sch.workers * kCG), 1, 1);
+    cfg.gridDim = dim3(static_cast<unsigned>(a.sch.workers * kCG * kMC), 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = S::kSmemBytes;
     cfg.stream = stream;
@@ -1189,51 +1231,52 @@ cudaError_t launch_shape(const CUtensorMap& tmA, const CUtensorMap& tmB, const C
     }
     if (kCG == 2) {
         attr[n].id = cudaLaunchAttributeClusterDimension;
-        attr[n].val.clusterDim.x = 2;
+        attr[n].val.clusterDim.x = kCG * kMC;
         attr[n].val.clusterDim.y = 1;
         attr[n].val.clusterDim.z = 1;
         ++n;
     }
     cfg.attrs = attr;
     cfg.numAttrs = n;
-    return cudaLaunchKernelEx(&cfg, sk_gemm_kernel<kNT, kCG, kBN>, tmA, tmB, tmC, tmD, a);
+    return cudaLaunchKernelEx(&cfg, sk_gemm_kernel<kNT, kCG, kBN, kMC>, tmA, tmB, tmC, tmD, a);
 }
 
-template <int kCG, int kBN>
+template <int kCG, int kBN, int kMC>
 cudaError_t prepare_shape(int num_sms, int* max_units) {
     using S = Shape<kCG, kBN>;
-    cudaError_t e = cudaFuncSetAttribute(sk_gemm_kernel<false, kCG, kBN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         S::kSmemBytes);
+    cudaError_t e = cudaFuncSetAttribute(sk_gemm_kernel<false, kCG, kBN, kMC>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmemBytes);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(sk_gemm_kernel<true, kCG, kBN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(sk_gemm_kernel<true, kCG, kBN, kMC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              S::kSmemBytes);
     if (e != cudaSuccess) return e;
     if (kCG == 1) {
         int n0 = 0, n1 = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n0, sk_gemm_kernel<false, kCG, kBN>, kThreads,
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n0, sk_gemm_kernel<false, kCG, kBN, kMC>, kThreads,
                                                           S::kSmemBytes);
         if (e != cudaSuccess) return e;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n1, sk_gemm_kernel<true, kCG, kBN>, kThreads,
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n1, sk_gemm_kernel<true, kCG, kBN, kMC>, kThreads,
                                                           S::kSmemBytes);
         if (e != cudaSuccess) return e;
         *max_units = (n0 < n1 ? n0 : n1) * num_sms;
         return cudaSuccess;
     }
+    // Units are clusters of kCG * kMC CTAs: as many as can be resident at once.
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(2 * num_sms), 1, 1);
+    cfg.gridDim = dim3(static_cast<unsigned>(kCG * kMC * (num_sms / (kCG * kMC))), 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = S::kSmemBytes;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.x = kCG * kMC;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int c0 = 0, c1 = 0;
-    e = cudaOccupancyMaxActiveClusters(&c0, sk_gemm_kernel<false, kCG, kBN>, &cfg);
+    e = cudaOccupancyMaxActiveClusters(&c0, sk_gemm_kernel<false, kCG, kBN, kMC>, &cfg);
     if (e != cudaSuccess) return e;
-    e = cudaOccupancyMaxActiveClusters(&c1, sk_gemm_kernel<true, kCG, kBN>, &cfg);
+    e = cudaOccupancyMaxActiveClusters(&c1, sk_gemm_kernel<true, kCG, kBN, kMC>, &cfg);
     if (e != cudaSuccess) return e;
     *max_units = c0 < c1 ? c0 : c1;
     return cudaSuccess;
@@ -1242,23 +1285,25 @@ cudaError_t prepare_shape(int num_sms, int* max_units) {
 }  // namespace
 
 cudaError_t prepare_device(int num_sms, int* max_units) {
-    cudaError_t e = prepare_shape<1, 128>(num_sms, &max_units[0]);
-    if (e == cudaSuccess) e = prepare_shape<2, 128>(num_sms, &max_units[1]);
-    if (e == cudaSuccess) e = prepare_shape<2, 256>(num_sms, &max_units[2]);
-    if (e == cudaSuccess) e = prepare_shape<1, 256>(num_sms, &max_units[3]);
+    cudaError_t e = prepare_shape<1, 128, 1>(num_sms, &max_units[0]);
+    if (e == cudaSuccess) e = prepare_shape<2, 128, 1>(num_sms, &max_units[1]);
+    if (e == cudaSuccess) e = prepare_shape<2, 256, 1>(num_sms, &max_units[2]);
+    if (e == cudaSuccess) e = prepare_shape<1, 256, 1>(num_sms, &max_units[3]);
+    if (e == cudaSuccess) e = prepare_shape<2, 256, 2>(num_sms, &max_units[4]);
     return e;
 }
 
 cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
                         const CUtensorMap& tmD, bool nt, const KArgs& a, cudaStream_t stream) {
     const int cg = a.sch.cg, bn = a.sch.tile_n;
-#define SK_LAUNCH(CG, BN)                                                                 \
-    return nt ? launch_shape<true, CG, BN>(tmA, tmB, tmC, tmD, a, stream)                \
-              : launch_shape<false, CG, BN>(tmA, tmB, tmC, tmD, a, stream)
-    if (cg == 1 && bn == 128) SK_LAUNCH(1, 128);
-    if (cg == 2 && bn == 128) SK_LAUNCH(2, 128);
-    if (cg == 2 && bn == 256) SK_LAUNCH(2, 256);
-    if (cg == 1 && bn == 256) SK_LAUNCH(1, 256);
+#define SK_LAUNCH(CG, BN, MC)                                                             \
+    return nt ? launch_shape<true, CG, BN, MC>(tmA, tmB, tmC, tmD, a, stream)            \
+              : launch_shape<false, CG, BN, MC>(tmA, tmB, tmC, tmD, a, stream)
+    if (cg == 1 && bn == 128) SK_LAUNCH(1, 128, 1);
+    if (cg == 2 && bn == 128) SK_LAUNCH(2, 128, 1);
+    if (cg == 2 && bn == 256) SK_LAUNCH(2, 256, 1);
+    if (cg == 1 && bn == 256) SK_LAUNCH(1, 256, 1);
+    if (cg == 4 && bn == 512) SK_LAUNCH(2, 256, 2);
 #undef SK_LAUNCH
     return cudaErrorInvalidValue;
 }

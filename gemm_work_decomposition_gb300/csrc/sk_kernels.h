@@ -26,6 +26,7 @@ constexpr int kBoxes = 2 / kEpiGroups;          // 4 KiB staging boxes per epilo
 constexpr int kCtaRows = 128;     // rows of a work tile held by one CTA (its TMEM lanes)
 constexpr int kRingBytes = 196608;
 constexpr int kTraceSegs = 15;                  // SK_TRACE_SEGS
+constexpr int kTileShapes = 5;                  // sk_tile values
 constexpr int kTraceWords = 4 + 4 * kTraceSegs; // SK_TRACE_WORDS
 
 // Compile-time shape of one kernel instance: kCG CTAs per work tile (1, or a pair with
@@ -83,7 +84,7 @@ struct KArgs {
 cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
                         const CUtensorMap& tmD, bool nt, const KArgs& a, cudaStream_t stream);
 // Configure the kernels' shared-memory limit on the current device and report, per
-// sk_tile value, how many units of that shape can be resident at once.
+// sk_tile value (kTileShapes of them), how many units of that shape can be resident at once.
 cudaError_t prepare_device(int num_sms, int* max_units);
 // Separate fixup pass for a plan with sch.sep: every Stream-K tile covered by more than one
 // unit gets C = its partial slots summed in k order (FP32), stored as BF16 or FP32.

@@ -60,6 +60,7 @@ SK_HD bool tile_shape(int32_t tile, int32_t* tm, int32_t* tn, int32_t* cg) {
         case 1: *tm = 256; *tn = 128; *cg = 2; return true;
         case 2: *tm = 256; *tn = 256; *cg = 2; return true;
         case 3: *tm = 128; *tn = 256; *cg = 1; return true;
+        case 4: *tm = 256; *tn = 512; *cg = 4; return true;
         default: return false;
     }
 }

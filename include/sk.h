@@ -56,7 +56,18 @@ typedef enum { SK_ROLE_FULL = 0, SK_ROLE_OWNER = 1, SK_ROLE_PRODUCER = 2, SK_ROL
  * cta_group::2, each CTA holding half of the tile's rows and half of B's columns), so a
  * persistent unit is a CTA pair and num_sms SMs give num_sms / 2 units; CUTLASS
  * example 74 on the first page uses the 256 x 128 pair tile. */
-typedef enum { SK_TILE_128x128 = 0, SK_TILE_256x128_PAIR = 1, SK_TILE_256x256_PAIR = 2, SK_TILE_128x256 = 3 } sk_tile;
+/* SK_TILE_256x512_QUAD: two CTA pairs side by side in a cluster of four, each pair computing
+ * one 256 x 256 half of the tile; the A rows they share are loaded once and multicast to both
+ * pairs (half the A bytes read from L2). A unit is the cluster, so num_sms SMs give
+ * num_sms / 4 units. Planned for SK_DP, SK_STREAMK and SK_HYBRID with split_partials = 0
+ * only (SK_EINVAL otherwise). */
+typedef enum {
+    SK_TILE_128x128 = 0,
+    SK_TILE_256x128_PAIR = 1,
+    SK_TILE_256x256_PAIR = 2,
+    SK_TILE_128x256 = 3,
+    SK_TILE_256x512_QUAD = 4
+} sk_tile;
 
 typedef struct {
     int32_t mode;           /* sk_mode */
@@ -216,8 +227,9 @@ typedef struct {
 } sk_debug_opts;
 
 /* Per-CTA trace record (sk_debug_opts.trace), indexed by blockIdx: [0] start (after set-up
- * and, for an overlapped launch, after the wait for the previous kernel), [1] end (before
- * the exit barrier), [2] segments walked, [3] reserved; then for segment i
+ * and, for an overlapped launch, after the wait for the previous kernel), [1] end (after
+ * the exit barrier), [2] segments walked, [3] SM clock cycles from [0] to [1] (so
+ * [3] / ([1] - [0]) is the SM's clock while it ran); then for segment i
  * < SK_TRACE_SEGS, at 4 + 4 * i: [0] MMA issue of its first k-iteration (leader CTA only),
  * [1] MMA commit of its last, [2] epilogue has the accumulator, [3] epilogue done (after the
  * fixup and the stores). Unused words stay as the caller left them. */

@@ -33,8 +33,11 @@ FULL, OWNER, PRODUCER, SLAB = 0, 1, 2, 3
 LABEL_NONE, LABEL_DP, LABEL_SPLITK, LABEL_STREAMK = -1, 0, 1, 2
 
 # work-tile shapes: (tile_m, tile_n, CTAs per tile). A tile of the pair shapes is computed by
-# two CTAs together, so a unit is a CTA pair and num_sms SMs give num_sms // 2 units.
-TILE_SHAPES = {0: (128, 128, 1), 1: (256, 128, 2), 2: (256, 256, 2), 3: (128, 256, 1)}
+# two CTAs together, so a unit is a CTA pair and num_sms SMs give num_sms // 2 units; a tile of
+# shape 4 by four CTAs (two pairs side by side), num_sms // 4 units.
+TILE_SHAPES = {0: (128, 128, 1), 1: (256, 128, 2), 2: (256, 256, 2), 3: (128, 256, 1), 4: (256, 512, 4)}
+# Shapes planned only with the in-kernel fixup: no Split-K slabs, no separate fixup pass.
+TILES_WITHOUT_PASSES = (4,)
 
 MAP_VERSION = 2
 HEADER_LEN = 17
@@ -221,8 +224,10 @@ def build_plan(M: int, N: int, K: int, num_sms: int, mode: int, splits: int = 1,
       - DP (Mental model, Case 2 data_parallel): unit w runs tiles w, w + W, ... with
         W = min(units, tiles), each tile FULL.
       - Tile shape (`tile`, TILE_SHAPES): the pages' tile is 128 x 128 (tile 0). The
-        CTA-pair shapes make one unit of two SMs, so `units` defaults to num_sms // 2;
-        the schedule itself is the same over the coarser tile grid.
+        CTA-pair shapes make one unit of two SMs, so `units` defaults to num_sms // 2, and
+        the 256 x 512 shape one unit of four SMs (num_sms // 4); the schedule itself is the
+        same over the coarser tile grid. The four-CTA shape is planned for data-parallel,
+        Stream-K and the hybrid rule with the in-kernel fixup only.
       - Split-K (Case 2 split_k; the split-K report's "final split is clamped"): split j
         of a tile covers k-iterations [j*chunk, min((j+1)*chunk, iters)), chunk =
         ceil(iters / s); empty trailing splits are dropped (s_eff = ceil(iters / chunk)).
@@ -255,6 +260,8 @@ def build_plan(M: int, N: int, K: int, num_sms: int, mode: int, splits: int = 1,
         raise ValueError("data-parallel tiles have no partials")
     if tile not in TILE_SHAPES:
         raise ValueError("bad tile shape")
+    if tile in TILES_WITHOUT_PASSES and (mode == SPLITK or split_partials):
+        raise ValueError("this tile shape has no Split-K or separate-pass plans")
     if raster not in (0, 1) or not 0 <= swizzle <= 256:
         raise ValueError("bad rasterization")
     tile_m, tile_n, cg = TILE_SHAPES[tile]

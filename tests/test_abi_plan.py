@@ -83,12 +83,13 @@ def test_plan_matches_oracle_on_workloads(sk):
             _cmp(sk, M, 512, 2048, 148, S.SPLITK, splits=s)
     _cmp(sk, 2048, 2432, 4096, 148, S.SPLITK, splits=2)
     for m in range(128, 4097, 128):
-        for tile in (0, 1, 2, 3):
+        for tile in (0, 1, 2, 3, 4):
             for mode in (S.DP, S.STREAMK, S.HYBRID):
                 _cmp(sk, m, m, 4096, 148, mode, tile=tile)
-            for s in (2, 4):
-                _cmp(sk, m, m, 4096, 148, S.SPLITK, splits=s, tile=tile)
-    for tile in (1, 2, 3):
+            if tile != 4:
+                for s in (2, 4):
+                    _cmp(sk, m, m, 4096, 148, S.SPLITK, splits=s, tile=tile)
+    for tile in (1, 2, 3, 4):
         for M, N, K, sms, mode in cases:
             _cmp(sk, M, N, K, sms, mode, tile=tile)
 
@@ -131,9 +132,11 @@ def test_plan_bruteforce_small(sk):
     # M, N <= 640, K <= 512, 1..20 SMs, every mode.
     for M, N, K in itertools.product((1, 128, 129, 300, 640), (8, 128, 256, 640), (8, 64, 65, 200, 512)):
         for sms in range(1, 21):
-            for tile in (0, 1, 2, 3):
+            for tile in (0, 1, 2, 3, 4):
                 for mode in (S.DP, S.STREAMK, S.HYBRID):
                     _cmp(sk, M, N, K, sms, mode, tile=tile)
+                if tile == 4:  # in-kernel fixup only
+                    continue
                 for mode in (S.STREAMK, S.HYBRID):
                     _cmp(sk, M, N, K, sms, mode, partials=1, tile=tile)
                 iters = S.cdiv(K, 64)
@@ -154,7 +157,9 @@ def test_workspace_size(sk):
              (96, 512, 2048, 148, S.SPLITK, 8, 1), (96, 512, 2048, 148, S.SPLITK, 8, 2),
             (2048, 2432, 4096, 148, S.SPLITK, 2, 0), (2048, 2432, 4096, 148, S.HYBRID, 1, 1),
             (512, 512, 65536, 148, S.STREAMK, 1, 1),
-             (2048, 2432, 4096, 148, S.DP, 1, 0)], (0, 1, 2, 3)):
+             (2048, 2432, 4096, 148, S.DP, 1, 0)], (0, 1, 2, 3, 4)):
+        if tile == 4 and (mode == S.SPLITK or part):
+            continue
         sch = sk.schedule(mode, s, 0, 0, part, tile)
         m = sk.sk_plan(M, N, K, sms, sch)
         n_slots, splits = int(m[11]), int(m[8])
@@ -178,8 +183,11 @@ def test_errors(sk):
         (128, 128, 128, 4, sk.schedule(sk.SK_DP, 1, 0, 0, 1)),       # data-parallel tiles have no partials
         (128, 128, 128, 4, sk.schedule(sk.SK_SPLITK, 2, 0, 0, 3)),   # unknown slab reduction
         (128, 128, 128, 4, sk.schedule(sk.SK_DP, 1, -1)),
-        (128, 128, 128, 4, sk.schedule(sk.SK_DP, 1, 0, 0, 0, 4)),      # unknown tile shape
         (128, 128, 128, 1, sk.schedule(sk.SK_DP, 1, 0, 0, 0, 1)),      # a pair needs 2 SMs
+        (128, 128, 128, 3, sk.schedule(sk.SK_DP, 1, 0, 0, 0, 4)),      # four CTAs need 4 SMs
+        (128, 128, 128, 8, sk.schedule(sk.SK_SPLITK, 2, 0, 0, 0, 4)),  # no Split-K on the four-CTA tile
+        (128, 128, 512, 8, sk.schedule(sk.SK_STREAMK, 1, 0, 0, 1, 4)),  # nor the separate pass
+        (128, 128, 128, 4, sk.schedule(sk.SK_DP, 1, 0, 0, 0, 5)),      # unknown tile shape
         (128, 128, 128, 4, sk.schedule(sk.SK_DP, overlap=2)),          # overlap is 0 or 1
         (128, 128, 128, 4, sk.schedule(sk.SK_DP, overlap=-1)),
     ]
