@@ -439,3 +439,39 @@ def test_case3_interpreter_claims(sk, dev):
     assert np.array_equal(own40, rev40)
     at40, _ = _run(sk, dev, w, sk.schedule(2, units=40), ATOM, 148, reverse_units=1)
     U.assert_close(at40, ref, "atomic 40")
+
+
+# --------------------------------------------------------------------------- trace record
+@pytest.mark.parametrize("tile,nsms", [(0, 148), (2, 148), (4, 144)])
+def test_trace_record(sk, dev, tile, nsms):
+    # The per-CTA trace (sk_debug_opts.trace) of the hybrid rule on the wave-quantized GEMM,
+    # checked against the plan map: every CTA walks its unit's segments; start <= end; for
+    # each traced segment the MMA leader's first issue <= last commit, and the epilogue takes
+    # the accumulator after that commit and finishes after it takes it; word 3 counts the SM
+    # cycles between start and end, a clock between 0.5 and 3 GHz. The GEMM's result is still
+    # the oracle's.
+    w = synth.WAVEQ
+    sched = sk.schedule(3, tile=tile)
+    plan = sk.sk_plan(w.M, w.N, w.K, nsms, sched)
+    cg, workers = int(plan[14]), int(plan[4])
+    ncta = workers * cg
+    segs = {}
+    for i in range(int(plan[7])):
+        r = plan[sk.SK_MAP_HEADER + sk.SK_MAP_SEG * i: sk.SK_MAP_HEADER + sk.SK_MAP_SEG * (i + 1)]
+        segs[int(r[0])] = segs.get(int(r[0]), 0) + 1
+    tr = torch.zeros(ncta * sk.SK_TRACE_WORDS, dtype=torch.int64, device=dev)
+    got, _ = _run(sk, dev, w, sched, DET, nsms, trace=tr)
+    U.assert_close(got, U.reference(w), "traced")
+    T = tr.cpu().numpy().reshape(ncta, sk.SK_TRACE_WORDS).astype(np.int64)
+    for c in range(ncta):
+        unit, rank_in_pair = c // cg, (c % cg) % 2
+        n = segs.get(unit, 0)
+        assert T[c, 2] == n, (c, T[c, 2], n)
+        assert 0 < T[c, 0] <= T[c, 1]
+        mhz = T[c, 3] / max(1, T[c, 1] - T[c, 0]) * 1e3
+        assert 500 <= mhz <= 3000, (c, mhz)
+        for s in range(min(n, sk.SK_TRACE_SEGS)):
+            issue, commit, acc, done = T[c, 4 + 4 * s: 8 + 4 * s]
+            assert T[c, 0] <= acc <= done <= T[c, 1] + 10_000, (c, s)
+            if rank_in_pair == 0:  # the MMA stamps come from the leader of each MMA pair
+                assert T[c, 0] <= issue <= commit <= acc + 10_000, (c, s)

@@ -127,3 +127,32 @@ def test_quad_wait_timeout_reports_status(sk, dev, red):
     got, guards, _, status = U.gemm(sk, A, B, w.M, w.N, w.K, "NN", sched, red, 16, "f32", dev, ws)
     assert status == sk.SK_OK and guards
     U.assert_close(got, U.reference(w), "after time-out")
+
+
+@pytest.mark.parametrize("name,mode", MODES)
+def test_quad_overlapped_chain_equals_serial(sk, dev, name, mode):
+    # Five dependent GEMMs X_{i+1} = X_i . W_i (640 x 768 x 768, BF16 out), launched back to
+    # back with and without the overlapped launch: a missing wait for the previous kernel
+    # would read X_i before it is written, so both chains must agree bit for bit.
+    M, K = 640, 768
+    X0 = U.to_dev(synth.make_inputs(synth.Workload("chain_x", M, K, K, seed=40))[0], dev)
+    Ws = [U.to_dev(synth.make_inputs(synth.Workload("chain_w", K, K, K, seed=41 + i))[1], dev) for i in range(5)]
+    stream = torch.cuda.current_stream(dev)
+
+    def chain(overlap):
+        sched = sk.schedule(mode, tile=QUAD, overlap=overlap)
+        nb = sk.sk_workspace_size(M, K, K, 144, sched, DET)
+        ws = torch.zeros(nb, dtype=torch.uint8, device=dev)
+        outs = [torch.full((M, K), U.SENTINEL, dtype=torch.bfloat16, device=dev) for _ in Ws]
+        x = X0
+        torch.cuda.synchronize(dev)
+        for W, Y in zip(Ws, outs):
+            sk.sk_gemm(x, W, Y, sk.SK_BF16, M, K, K, sk.SK_NN, sched, DET, 144, ws, nb, stream)
+            x = Y
+        assert sk.sk_status(ws, stream) == sk.SK_OK
+        return [y.float().cpu().numpy() for y in outs]
+
+    ref, got = chain(0), chain(1)
+    for i, (g, r) in enumerate(zip(got, ref)):
+        assert not np.any(r == U.SENTINEL)
+        assert np.array_equal(g, r), (name, i)
