@@ -261,6 +261,42 @@ def run_sweep(sk, torch, dev, path, red, flush, stream, peak_tf, dev_sms, l2_byt
                                         "us_b2b": tb * 1e3, "tflops_b2b": tfb,
                                         "frac_of_measured_peak_b2b": tfb / peak_tf, "rotating_sets": len(rot)}) + "\n")
                     f.flush()
+            # The library GEMM (cuBLAS through torch.matmul, BF16 out) on the same operands, timed
+            # the same two ways: context for the schedules above, outside any timed step.
+            t, tb = library_timed(torch, dev, flush, stream, rot, m, m)
+            f.write(json.dumps({"M": m, "N": m, "K": ww.K, "tile": None, "num_sms": dev_sms, "schedule": "cublas",
+                                "us": t * 1e3, "tflops": fl / (t / 1e3) / 1e12,
+                                "frac_of_measured_peak": fl / (t / 1e3) / 1e12 / peak_tf,
+                                "us_b2b": tb * 1e3, "tflops_b2b": fl / (tb / 1e3) / 1e12,
+                                "frac_of_measured_peak_b2b": fl / (tb / 1e3) / 1e12 / peak_tf,
+                                "rotating_sets": len(rot)}) + "\n")
+            f.flush()
+
+
+def library_timed(torch, dev, flush, stream, rot, M, N, nt=False, flushed=30, b2b=60):
+    """torch.matmul (cuBLAS) on the rotating sets `rot` of (A, B, C) with BF16 C: the median of
+    `flushed` single calls with the L2 flushed before each, and the mean of `b2b` calls back to
+    back over the sets; both in ms. With `nt` B is stored N x K and passed transposed."""
+    def call(i):
+        a_, b_, c_ = rot[i % len(rot)]
+        torch.matmul(a_, b_.t() if nt else b_, out=c_)
+
+    with torch.cuda.stream(stream):
+        for i in range(10):
+            call(i)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(flushed)]
+        for a, b in ev:
+            flush.zero_()
+            a.record(stream)
+            call(0)
+            b.record(stream)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(b2b):
+            call(i)
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    return float(np.median([a.elapsed_time(b) for a, b in ev])), e0.elapsed_time(e1) / b2b
 
 
 def run_smallm(sk, torch, dev, flush, stream, dev_sms):
@@ -674,6 +710,14 @@ def main():
                                        "frac_of_measured_peak": flops / (ms / 1e3) / 1e12 / peak_tf}
             b2b[f"{tile_names[tile]}/{name}@{nsms}"] = row
         extras["back_to_back"] = {"sets": n_sets, "set_mb": set_bytes / 1e6, "steps": 400, "table": b2b}
+
+        # ---- the library GEMM on the same shape, output type and rotating sets (context only)
+        if out_code == sk.SK_BF16:
+            t, tb = library_timed(torch, dev, flush, stream, sets, w.M, w.N, nt=lay == sk.SK_NT, b2b=400)
+            extras["library_gemm"] = {"what": "torch.matmul (cuBLAS), BF16 out",
+                                      "us_b2b": tb * 1e3, "tflops_b2b": flops / (tb / 1e3) / 1e12,
+                                      "frac_of_measured_peak_b2b": flops / (tb / 1e3) / 1e12 / peak_tf,
+                                      "us_isolated_median": t * 1e3, "tflops_isolated": flops / (t / 1e3) / 1e12}
 
         # ---- the headline schedule timed one launch at a time, L2 flushed before each
         iso = timed(sch, ws, nb, sms, 200, 10)

@@ -51,7 +51,7 @@ struct Smem {
     __device__ uint32_t done() const { return base + S::kSmemBarOff + 8 * (2 * S::kStages + 4); }
     __device__ uint32_t tready() const { return base + S::kSmemBarOff + 8 * (2 * S::kStages + 5); }
     // Epilogue warp w's two barriers for partials fetched into the ring by bulk copies.
-    __device__ uint32_t pload(int w, int b) const { return base + S::kSmemBarOff + 256 + 8 * (2 * w + b); }
+    __device__ uint32_t pload(int w, int b) const { return base + S::kSmemBarOff + kBarPload + 8 * (2 * w + b); }
 };
 
 // Ring bytes an epilogue warp may use once the unit's MAC loop is over (the ring split four ways).
@@ -101,6 +101,10 @@ __device__ __forceinline__ int32_t seg_k(const Seg& g, bool rev, int32_t i) {
 // them) has been consumed by the MAC loop, the ring is free, so start the first one or two
 // partial copies of each epilogue warp into its ring quarter, while the epilogue is still
 // storing the segment before. Returns false when a wait gave up.
+// The MMA issuer commits each stage's empty barrier after that stage's MMAs, and a commit
+// arrives only once every MMA issued before it has completed, so the last load's stage
+// turning empty means every stage has been read: one wait, not one per stage (each wait
+// costs about 0.13 us even on a phase long complete).
 template <int kCG, int kBN>
 __device__ bool prefetch_partials(const KArgs& a, const Smem<Shape<kCG, kBN>>& sm, const Seg& g, const CtaPos& pos,
                                   uint32_t issued, uint64_t deadline, volatile int* abort_flag, int* prefetch) {
@@ -116,11 +120,10 @@ __device__ bool prefetch_partials(const KArgs& a, const Smem<Shape<kCG, kBN>>& s
             __nanosleep(32);
         }
     }
-    // Load `pos` went to stage pos % kStages; its consumption completes that stage's empty
-    // phase pos / kStages (as in the loop above, these are the only phases still open).
-    const uint32_t tail = issued < static_cast<uint32_t>(S::kStages) ? issued : S::kStages;
-    for (uint32_t i = 0; i < tail; ++i) {
-        const uint32_t n = issued - 1 - i;
+    // Load n went to stage n % kStages; its consumption completes that stage's empty phase
+    // n / kStages.
+    if (issued > 0) {
+        const uint32_t n = issued - 1;
         if (!mbar_wait(sm.empty(n % S::kStages), (n / S::kStages) & 1u, abort_flag, deadline)) return false;
     }
     const int k = S::kPasses * g.n_peers > 1 ? 2 : 1;
@@ -707,10 +710,12 @@ struct Epi {
     // segment, so also `wide`): the peers' partials come into the ring by bulk copies instead
     // of register loads. The producer warp, idle by then, has acquired the peers' flags and
     // started the first two copies as soon as the ring was free (run_producer); this warp
-    // consumes them and issues the rest. Returns false when a wait gave up or a check failed
-    // (the caller stops).
+    // consumes them and issues the rest. `release`: a later segment of the unit will run in
+    // this accumulator (the MMA issuer waits for it two segments on), so hand it back once
+    // read; for the unit's last two segments nobody waits, and the group goes on unsynchronised.
+    // Returns false when a wait gave up or a check failed (the caller stops).
     template <bool kFixup, bool kBulk>
-    __device__ __forceinline__ bool segment(const Seg& g, uint64_t* tr, int seg, bool wide) {
+    __device__ __forceinline__ bool segment(const Seg& g, uint64_t* tr, int seg, bool wide, bool release) {
         static_assert(kFixup || !kBulk, "bulk fetches are an owner's");
         constexpr int kChunks = kPassCols / 32;  // TMEM loads per pass
         constexpr bool bulk = kBulk;
@@ -805,7 +810,7 @@ struct Epi {
                     for (int h = 0; h < kPassCols / 64; ++h) dump_row<kPassCols>(dump + p * kPassCols + h * 64, t, h * 64);
                 }
             }
-            if (p == S::kPasses - 1) {
+            if (p == S::kPasses - 1 && release) {
                 // The whole accumulator has been read: hand it back to the MMA issuer. One
                 // thread per CTA arrives, after the group's barrier, and it is one that issues
                 // no bulk copies (a release arrive waits for its thread's copies in flight).
@@ -1023,12 +1028,13 @@ __device__ void run_epilogue_group(const KArgs& a, const CUtensorMap* tmC, const
             // The unit's last segment stages through the ring. With two groups the other group
             // may still be storing through its own buffers; the wide staging is for one only.
             const bool wide = seg == n_seg - 1 && kEpiGroups == 1;
+            const bool release = seg + 2 < n_seg;
             bool ok;
             if (g.role == kOwner && !a.sch.sep)
-                ok = (wide && !a.atomic) ? e.template segment<true, true>(g, tr, seg, true)
-                                         : e.template segment<true, false>(g, tr, seg, wide);
+                ok = (wide && !a.atomic) ? e.template segment<true, true>(g, tr, seg, true, release)
+                                         : e.template segment<true, false>(g, tr, seg, wide, release);
             else
-                ok = e.template segment<false, false>(g, tr, seg, wide);
+                ok = e.template segment<false, false>(g, tr, seg, wide, release);
             if (!ok) break;
             if (tr && seg < kTraceSegs) tr[4 + 4 * seg + 3] = globaltimer();
         }
@@ -1043,8 +1049,10 @@ __device__ void run_epilogue_group(const KArgs& a, const CUtensorMap* tmC, const
         const uint64_t until = globaltimer() + kDrainNs;
         for (int j = 0; j < k; ++j) (void)mbar_wait_until(e.pbar + 8u * static_cast<uint32_t>(j & 1), 0u, until);
     }
-    // Every TMA store of this warp has written C before the CTA may exit.
-    if (e.lane == 0) bulk_wait_group_all();
+    // Every TMA store of this warp has read its staging buffer before the CTA may exit. The
+    // writes need not have landed: the grid completes only once they have, and nothing in
+    // this launch reads C (partials and slabs are waited for in full before their flags).
+    if (e.lane == 0) bulk_wait_group_read<0>();
     __syncwarp();
     if (tr && kGroup == 0) tr[2] = static_cast<uint64_t>(seg);
 }
@@ -1075,11 +1083,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     Smem<S> sm{smem_u32(smem)};
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + S::kSmemBarOff + 192);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + S::kSmemBarOff + 196);
-    volatile int* last_flag = reinterpret_cast<volatile int*>(smem + S::kSmemBarOff + 200);  // one per group
-    int* prefetch = reinterpret_cast<int*>(smem + S::kSmemBarOff + 208);  // partial-copy hand-off word
-    volatile int* shared_tmp = reinterpret_cast<volatile int*>(smem + S::kSmemBarOff + 212);
+    uint8_t* bars = smem + S::kSmemBarOff;
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + kBarTmemHolder);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + kBarAbort);
+    volatile int* last_flag = reinterpret_cast<volatile int*>(bars + kBarLastFlag);  // one per group
+    int* prefetch = reinterpret_cast<int*>(bars + kBarPrefetch);
+    volatile int* shared_tmp = reinterpret_cast<volatile int*>(bars + kBarSharedTmp);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;

@@ -27,6 +27,21 @@ constexpr int kCtaRows = 128;     // rows of a work tile held by one CTA (its TM
 constexpr int kRingBytes = 196608;
 constexpr int kTraceSegs = 15;                  // SK_TRACE_SEGS
 constexpr int kTileShapes = 5;                  // sk_tile values
+
+// Layout of the barrier block at the end of shared memory (byte offsets within it): the
+// pipeline mbarriers from 0 (full and empty per ring stage, tfull and tempty per accumulator,
+// done, tready: at most 8 * (2 * 8 + 6) = 176 bytes), then single words, then two
+// partial-load mbarriers per epilogue warp.
+constexpr int kBarTmemHolder = 192;  // u32: TMEM base address written by the allocator
+constexpr int kBarAbort = 196;       // int: this CTA gave up (a wait ran out or a check failed)
+constexpr int kBarLastFlag = 200;    // int per epilogue group: this group took a tile's last slab
+constexpr int kBarPrefetch = 208;    // int: hand-off word of the producer warp's partial copies
+constexpr int kBarSharedTmp = 212;   // int: a group's shared copy of an atomic result
+constexpr int kBarPload = 256;       // two mbarriers per epilogue warp
+constexpr int kBarBlockBytes = 512;
+static_assert(8 * (2 * 8 + 6) <= kBarTmemHolder && kBarLastFlag + 4 * 2 <= kBarPrefetch &&
+                  kBarSharedTmp + 4 <= kBarPload && kBarPload + 16 * kEpiWarps <= kBarBlockBytes,
+              "barrier block layout");
 constexpr int kTraceWords = 4 + 4 * kTraceSegs; // SK_TRACE_WORDS
 
 // Compile-time shape of one kernel instance: kCG CTAs per work tile (1, or a pair with
@@ -44,16 +59,14 @@ struct Shape {
     static constexpr int kStagingOff = kStages * kStageBytes;
     static constexpr int kStagingBytes = kEpiWarps * kBoxes * 4096;
     static constexpr int kSmemBarOff = kStagingOff + kStagingBytes;
-    // Barrier block: the pipeline barriers and flags in its first 256 bytes, then two
-    // partial-load barriers per epilogue warp.
-    static constexpr int kSmemBytes = kSmemBarOff + 512 + 1024;
+    static constexpr int kSmemBytes = kSmemBarOff + kBarBlockBytes + 1024;
     static constexpr int kTmemCols = 2 * kBN;               // two accumulators of kBN columns
     static constexpr int kTxBytes = kCG * kStageBytes;      // bytes landing on the leader per stage
     static constexpr int kPasses = kBN / kPassCols;         // a thread's row, kPassCols at a time
     static constexpr int kWarpSlotFloats = 32 * kBN;        // one epilogue warp's block of a partial
     static constexpr int kCtaSlotFloats = kCtaRows * kBN;   // a CTA's share of one partial slot
     static_assert(kBNc % 64 == 0 && kBN % 128 == 0, "tile shape");
-    static_assert(kSmemBytes <= 232448 && 256 + 16 * kEpiWarps <= 512, "shared memory");
+    static_assert(kSmemBytes <= 232448 && kStages <= 8, "shared memory");
 };
 
 struct KArgs {
