@@ -48,11 +48,11 @@ WORKLOADS = {"waveq": synth.WAVEQ, "skinny": synth.SKINNY, "large": synth.LARGE,
 NOMINAL_BF16_TFLOPS = 2250.0
 NOMINAL_HBM_GBS = 8000.0
 TRAFFIC = {
-    "waveq_2048x2432x4096/hybrid/tile2@148": {"bytes": 36806912 + 1764864, "kernel_sha": "8cb49bdcdadc2650",
+    "waveq_2048x2432x4096/hybrid/tile2@148": {"bytes": 36802560 + 1651712, "kernel_sha": "44ef8a5ac95fbc1a",
                                               "profile": "profiles/sk_gemm_kernel_waveq_2048x2432x4096_pair256_hybrid148.md"},
-    "large_8192x8192x8192/dp/tile2@148": {"bytes": 2129598464 + 128950528, "kernel_sha": "8cb49bdcdadc2650",
+    "large_8192x8192x8192/dp/tile2@148": {"bytes": 2054986496 + 129315328, "kernel_sha": "44ef8a5ac95fbc1a",
                                           "profile": "profiles/sk_gemm_kernel_large_8192_pair256_dp148_raster.md"},
-    "large_8192x8192x8192/dp/tile2@148/r0s8": {"bytes": 1064943616 + 126574592, "kernel_sha": "8cb49bdcdadc2650",
+    "large_8192x8192x8192/dp/tile2@148/r0s8": {"bytes": 1042791680 + 125039616, "kernel_sha": "44ef8a5ac95fbc1a",
                                                "profile": "profiles/sk_gemm_kernel_large_8192_pair256_dp148_raster.md"},
 }
 
