@@ -282,33 +282,45 @@ __device__ void run_mma(const KArgs& a, const Smem<Shape<kCG, kBN>>& sm, uint32_
         }
         tc_fence_after();
         const uint32_t d = tmem_base + static_cast<uint32_t>(buf * kBN);
-        for (int32_t i = 0; i < g.k_end - g.k_begin; ++i) {
-            if (!mbar_wait(sm.full(stage), phase, abort_flag, deadline)) {
+        const int32_t len = g.k_end - g.k_begin;
+        // Two stages per turn: one wait covers both (their barrier round trips overlap), then
+        // eight MMAs and two commits. A segment's odd last stage is waited for alone.
+        for (int32_t i = 0; i < len; i += 2) {
+            const bool two = i + 1 < len;
+            const int stage1 = stage + 1 == S::kStages ? 0 : stage + 1;
+            const uint32_t phase1 = stage + 1 == S::kStages ? phase ^ 1u : phase;
+            const bool got = two ? mbar_wait2(sm.full(stage), phase, sm.full(stage1), phase1, abort_flag, deadline)
+                                 : mbar_wait(sm.full(stage), phase, abort_flag, deadline);
+            if (!got) {
                 ok = false;
                 break;
             }
             tc_fence_after();
             if (tr && i == 0 && seg < kTraceSegs) tr[4 + 4 * seg] = globaltimer();
-            // A: K-major, 8-row groups 1024 bytes apart. B: K-major likewise (NT), or
-            // MN-major (NN) in 64-column boxes 8 KiB apart.
-            const uint64_t adesc = smem_desc_sw128(sm.a(stage), 16, 1024);
-            const uint64_t bdesc =
-                kNT ? smem_desc_sw128(sm.b(stage), 16, 1024) : smem_desc_sw128(sm.b(stage), 8192, 1024);
 #pragma unroll
-            for (int kk = 0; kk < kBlkK / 16; ++kk) {
-                const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
+            for (int h = 0; h < 2; ++h) {
+                if (h == 1 && !two) break;
+                // A: K-major, 8-row groups 1024 bytes apart. B: K-major likewise (NT), or
+                // MN-major (NN) in 64-column boxes 8 KiB apart.
+                const uint64_t adesc = smem_desc_sw128(sm.a(stage), 16, 1024);
+                const uint64_t bdesc =
+                    kNT ? smem_desc_sw128(sm.b(stage), 16, 1024) : smem_desc_sw128(sm.b(stage), 8192, 1024);
+#pragma unroll
+                for (int kk = 0; kk < kBlkK / 16; ++kk) {
+                    const uint32_t acc = (i + h > 0 || kk > 0) ? 1u : 0u;
+                    if (kCG == 1)
+                        umma_bf16(d, adesc + kk * kAStep, bdesc + kk * kBStep, kIdesc, acc);
+                    else
+                        umma_bf16_pair(d, adesc + kk * kAStep, bdesc + kk * kBStep, kIdesc, acc);
+                }
                 if (kCG == 1)
-                    umma_bf16(d, adesc + kk * kAStep, bdesc + kk * kBStep, kIdesc, acc);
+                    umma_commit(sm.empty(stage));
                 else
-                    umma_bf16_pair(d, adesc + kk * kAStep, bdesc + kk * kBStep, kIdesc, acc);
-            }
-            if (kCG == 1)
-                umma_commit(sm.empty(stage));
-            else
-                umma_commit_pair(sm.empty(stage), stage_mask);
-            if (++stage == S::kStages) {
-                stage = 0;
-                phase ^= 1u;
+                    umma_commit_pair(sm.empty(stage), stage_mask);
+                if (++stage == S::kStages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
             }
         }
         if (!ok) break;
