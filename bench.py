@@ -48,11 +48,11 @@ WORKLOADS = {"waveq": synth.WAVEQ, "skinny": synth.SKINNY, "large": synth.LARGE,
 NOMINAL_BF16_TFLOPS = 2250.0
 NOMINAL_HBM_GBS = 8000.0
 TRAFFIC = {
-    "waveq_2048x2432x4096/hybrid/tile2@148": {"bytes": 36802560 + 1651712, "kernel_sha": "44ef8a5ac95fbc1a",
+    "waveq_2048x2432x4096/hybrid/tile2@148": {"bytes": 36805632 + 1980160, "kernel_sha": "e7e7e2659fdb6834",
                                               "profile": "profiles/sk_gemm_kernel_waveq_2048x2432x4096_pair256_hybrid148.md"},
-    "large_8192x8192x8192/dp/tile2@148": {"bytes": 2054986496 + 129315328, "kernel_sha": "44ef8a5ac95fbc1a",
+    "large_8192x8192x8192/dp/tile2@148": {"bytes": 2053219072 + 129263616, "kernel_sha": "e7e7e2659fdb6834",
                                           "profile": "profiles/sk_gemm_kernel_large_8192_pair256_dp148_raster.md"},
-    "large_8192x8192x8192/dp/tile2@148/r0s8": {"bytes": 1042791680 + 125039616, "kernel_sha": "44ef8a5ac95fbc1a",
+    "large_8192x8192x8192/dp/tile2@148/r0s8": {"bytes": 1067753472 + 125707008, "kernel_sha": "e7e7e2659fdb6834",
                                                "profile": "profiles/sk_gemm_kernel_large_8192_pair256_dp148_raster.md"},
 }
 

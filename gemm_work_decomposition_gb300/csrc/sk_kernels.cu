@@ -284,9 +284,12 @@ __device__ void run_mma(const KArgs& a, const Smem<Shape<kCG, kBN>>& sm, uint32_
         const uint32_t d = tmem_base + static_cast<uint32_t>(buf * kBN);
         const int32_t len = g.k_end - g.k_begin;
         // Two stages per turn: one wait covers both (their barrier round trips overlap), then
-        // eight MMAs and two commits. A segment's odd last stage is waited for alone.
-        for (int32_t i = 0; i < len; i += 2) {
-            const bool two = i + 1 < len;
+        // eight MMAs and two commits. A segment's odd last stage is waited for alone, and so is
+        // every stage of a ring shorter than six (the 128 x 256 tile's four stages of 48 KiB):
+        // holding two of four would leave only two loading.
+        constexpr bool kPairTurns = S::kStages >= 6;
+        for (int32_t i = 0; i < len;) {
+            const bool two = kPairTurns && i + 1 < len;
             const int stage1 = stage + 1 == S::kStages ? 0 : stage + 1;
             const uint32_t phase1 = stage + 1 == S::kStages ? phase ^ 1u : phase;
             const bool got = two ? mbar_wait2(sm.full(stage), phase, sm.full(stage1), phase1, abort_flag, deadline)
@@ -322,6 +325,7 @@ __device__ void run_mma(const KArgs& a, const Smem<Shape<kCG, kBN>>& sm, uint32_
                     phase ^= 1u;
                 }
             }
+            i += two ? 2 : 1;
         }
         if (!ok) break;
         if (kCG == 1)
