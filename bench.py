@@ -48,11 +48,11 @@ WORKLOADS = {"waveq": synth.WAVEQ, "skinny": synth.SKINNY, "large": synth.LARGE,
 NOMINAL_BF16_TFLOPS = 2250.0
 NOMINAL_HBM_GBS = 8000.0
 TRAFFIC = {
-    "waveq_2048x2432x4096/hybrid/tile2@148": {"bytes": 36805632 + 1980160, "kernel_sha": "e7e7e2659fdb6834",
+    "waveq_2048x2432x4096/hybrid/tile2@148": {"bytes": 36802304 + 1830912, "kernel_sha": "bbdcce6f971680a6",
                                               "profile": "profiles/sk_gemm_kernel_waveq_2048x2432x4096_pair256_hybrid148.md"},
-    "large_8192x8192x8192/dp/tile2@148": {"bytes": 2053219072 + 129263616, "kernel_sha": "e7e7e2659fdb6834",
+    "large_8192x8192x8192/dp/tile2@148": {"bytes": 2053938176 + 129377280, "kernel_sha": "bbdcce6f971680a6",
                                           "profile": "profiles/sk_gemm_kernel_large_8192_pair256_dp148_raster.md"},
-    "large_8192x8192x8192/dp/tile2@148/r0s8": {"bytes": 1067753472 + 125707008, "kernel_sha": "e7e7e2659fdb6834",
+    "large_8192x8192x8192/dp/tile2@148/r0s8": {"bytes": 1061767424 + 125147904, "kernel_sha": "bbdcce6f971680a6",
                                                "profile": "profiles/sk_gemm_kernel_large_8192_pair256_dp148_raster.md"},
 }
 

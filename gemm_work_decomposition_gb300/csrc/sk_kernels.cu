@@ -283,17 +283,30 @@ __device__ void run_mma(const KArgs& a, const Smem<Shape<kCG, kBN>>& sm, uint32_
         tc_fence_after();
         const uint32_t d = tmem_base + static_cast<uint32_t>(buf * kBN);
         const int32_t len = g.k_end - g.k_begin;
-        // Two stages per turn: one wait covers both (their barrier round trips overlap), then
-        // eight MMAs and two commits. A segment's odd last stage is waited for alone, and so is
-        // every stage of a ring shorter than six (the 128 x 256 tile's four stages of 48 KiB):
-        // holding two of four would leave only two loading.
-        constexpr bool kPairTurns = S::kStages >= 6;
+        // Several stages per turn: one wait covers all of them (their barrier round trips
+        // overlap), then four MMAs and a commit per stage. Three for an 8-stage ring, two for
+        // a 6-stage one, one for the 128 x 256 tile's four stages of 48 KiB; a deeper turn on a
+        // shallower ring leaves too few stages loading while the issuer waits. A segment's
+        // last stages form a shorter turn.
+        constexpr int kTurn = S::kStages >= 8 ? 3 : (S::kStages >= 6 ? 2 : 1);
         for (int32_t i = 0; i < len;) {
-            const bool two = kPairTurns && i + 1 < len;
-            const int stage1 = stage + 1 == S::kStages ? 0 : stage + 1;
-            const uint32_t phase1 = stage + 1 == S::kStages ? phase ^ 1u : phase;
-            const bool got = two ? mbar_wait2(sm.full(stage), phase, sm.full(stage1), phase1, abort_flag, deadline)
-                                 : mbar_wait(sm.full(stage), phase, abort_flag, deadline);
+            const int nt = len - i < kTurn ? len - i : kTurn;
+            uint32_t tb[3], tp[3];
+            {
+                int st = stage;
+                uint32_t ph = phase;
+#pragma unroll
+                for (int h = 0; h < 3; ++h) {
+                    tb[h] = sm.full(st);
+                    tp[h] = ph;
+                    if (++st == S::kStages) {
+                        st = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+            const bool got = nt == 1 ? mbar_wait(tb[0], tp[0], abort_flag, deadline)
+                                     : mbar_wait_n(nt, tb, tp, abort_flag, deadline);
             if (!got) {
                 ok = false;
                 break;
@@ -301,8 +314,8 @@ __device__ void run_mma(const KArgs& a, const Smem<Shape<kCG, kBN>>& sm, uint32_
             tc_fence_after();
             if (tr && i == 0 && seg < kTraceSegs) tr[4 + 4 * seg] = globaltimer();
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                if (h == 1 && !two) break;
+            for (int h = 0; h < 3; ++h) {
+                if (h >= nt) break;
                 // A: K-major, 8-row groups 1024 bytes apart. B: K-major likewise (NT), or
                 // MN-major (NN) in 64-column boxes 8 KiB apart.
                 const uint64_t adesc = smem_desc_sw128(sm.a(stage), 16, 1024);
@@ -325,7 +338,7 @@ __device__ void run_mma(const KArgs& a, const Smem<Shape<kCG, kBN>>& sm, uint32_
                     phase ^= 1u;
                 }
             }
-            i += two ? 2 : 1;
+            i += nt;
         }
         if (!ok) break;
         if (kCG == 1)

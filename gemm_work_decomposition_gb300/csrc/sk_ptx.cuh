@@ -70,9 +70,9 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const v
     }
 }
 
-// Two phases at once (barrier b0's of parity p0 and b1's of parity p1): both probes are
-// non-blocking and issue back to back, so the two round trips to the barriers overlap.
-// Bounded like mbar_wait.
+// Two or three phases at once (barrier b0's of parity p0, b1's of parity p1, ...): the probes
+// are non-blocking and issue back to back, so their round trips to the barriers overlap.
+// mbar_wait_n is bounded like mbar_wait.
 __device__ __forceinline__ bool mbar_test2(uint32_t b0, uint32_t p0, uint32_t b1, uint32_t p1) {
     uint32_t ok;
     asm volatile(
@@ -86,11 +86,30 @@ __device__ __forceinline__ bool mbar_test2(uint32_t b0, uint32_t p0, uint32_t b1
         : "memory");
     return ok != 0;
 }
-__device__ __forceinline__ bool mbar_wait2(uint32_t b0, uint32_t p0, uint32_t b1, uint32_t p1,
-                                           const volatile int* abort_flag, uint64_t deadline) {
-    for (uint32_t n = 0;; ++n) {
-        if (mbar_test2(b0, p0, b1, p1)) return true;
-        if ((n & 63u) == 63u) {
+__device__ __forceinline__ bool mbar_test3(uint32_t b0, uint32_t p0, uint32_t b1, uint32_t p1, uint32_t b2,
+                                           uint32_t p2) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred q0, q1, q2;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 q0, [%1], %2;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 q1, [%3], %4;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 q2, [%5], %6;\n\t"
+        "and.pred q0, q0, q1;\n\t"
+        "and.pred q0, q0, q2;\n\t"
+        "selp.u32 %0, 1, 0, q0;\n\t}"
+        : "=r"(ok)
+        : "r"(b0), "r"(p0), "r"(b1), "r"(p1), "r"(b2), "r"(p2)
+        : "memory");
+    return ok != 0;
+}
+// The phases of parity p[j] of barriers b[j], j < n (n = 2 or 3), all at once.
+__device__ __forceinline__ bool mbar_wait_n(int n, const uint32_t (&b)[3], const uint32_t (&p)[3],
+                                            const volatile int* abort_flag, uint64_t deadline) {
+    for (uint32_t k = 0;; ++k) {
+        const bool done =
+            n == 3 ? mbar_test3(b[0], p[0], b[1], p[1], b[2], p[2]) : mbar_test2(b[0], p[0], b[1], p[1]);
+        if (done) return true;
+        if ((k & 63u) == 63u) {
             if (*abort_flag) return false;
             if (globaltimer() > deadline) return false;
         }
