@@ -22,6 +22,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import itertools
 import json
 import os
 import subprocess
@@ -203,74 +204,114 @@ def run_reference(args, w, rank, world):
     print(json.dumps(line), flush=True)
 
 
-def run_sweep(sk, torch, dev, path, red, flush, stream, peak_tf, dev_sms, l2_bytes):
-    """Tile-count sweep: M = N = 128 .. 4096, K = 4096, every schedule plus the hybrid
-    rule's choice, with the pages' 128 x 128 tile and the 256 x 256 CTA-pair tile, on 148
-    SMs and on the device's SM count; one JSON line per point. Each point is timed two ways:
-    `us`, the median of 30 single launches with the L2 flushed before each; and `us_b2b`,
-    60 overlapped launches back to back over rotating copies of A, B and C that together
-    exceed 4x the L2 (the headline's method), mean per launch."""
-    with open(path, "w") as f:
-        for m in synth.SWEEP_SIZES:
-            ww = synth.sweep(m)
-            A_bits, B_bits = synth.make_inputs(ww)
-            A = torch.from_numpy(A_bits.view(np.int16)).view(torch.bfloat16).to(dev)
-            B = torch.from_numpy(B_bits.view(np.int16)).view(torch.bfloat16).to(dev)
-            C = torch.empty((m, m), dtype=torch.bfloat16, device=dev)
-            set_b = (A.numel() + B.numel() + C.numel()) * 2
-            rot = [(A, B, C)] + [(A.clone(), B.clone(), torch.empty_like(C))
-                                 for _ in range(max(2, -(-4 * l2_bytes // set_b)) - 1)]
-            fl = 2.0 * m * m * ww.K
-            for nsms, tile in ((148, 0), (dev_sms, 0), (148, 2), (dev_sms, 2)):
-                for name, mode, s in (("dp", sk.SK_DP, 1), ("splitk2", sk.SK_SPLITK, 2), ("splitk4", sk.SK_SPLITK, 4),
-                                      ("streamk", sk.SK_STREAMK, 1), ("hybrid", sk.SK_HYBRID, 1)):
-                    sch = sk.schedule(mode, s, tile=tile)
-                    nb = sk.sk_workspace_size(m, m, ww.K, nsms, sch, red)
-                    ws = torch.zeros(nb, dtype=torch.uint8, device=dev)
-                    plan = sk.sk_plan(m, m, ww.K, nsms, sch)
+SWEEP_COMPACT = (1024, 1536, 2048, 2304, 2432, 3072, 3840, 4096)
+SWEEP_SCHEDULES = (("dp", 0, 1), ("splitk2", 1, 2), ("streamk", 2, 1), ("hybrid", 3, 1))
+
+
+def sweep_points(sk, torch, dev, red, flush, stream, peak_tf, l2_bytes, sizes, configs, flushed=0, b2b=40,
+                 library=False):
+    """Tile-count sweep over square M = N in `sizes`, K = 4096 (the tile-count sweep
+    workload): every schedule of SWEEP_SCHEDULES (data-parallel, Split-K s = 2, Stream-K and
+    the hybrid rule, which is the decision rule's own choice) for each (num_sms, tile) of
+    `configs`. Each point is timed `b2b` overlapped launches back to back over rotating copies
+    of A, B and C that together exceed 4x the L2 (the headline's method, mean per launch),
+    and, with `flushed` > 0, as the median of that many single launches with the L2 flushed
+    before each. Yields one dict per point (and per size a cuBLAS row with `library`)."""
+    for m in sizes:
+        ww = synth.sweep(m)
+        A_bits, B_bits = synth.make_inputs(ww)
+        A = torch.from_numpy(A_bits.view(np.int16)).view(torch.bfloat16).to(dev)
+        B = torch.from_numpy(B_bits.view(np.int16)).view(torch.bfloat16).to(dev)
+        C = torch.empty((m, m), dtype=torch.bfloat16, device=dev)
+        set_b = (A.numel() + B.numel() + C.numel()) * 2
+        rot = [(A, B, C)] + [(A.clone(), B.clone(), torch.empty_like(C))
+                             for _ in range(max(2, -(-4 * l2_bytes // set_b)) - 1)]
+        fl = 2.0 * m * m * ww.K
+        for nsms, tile in configs:
+            for name, mode, s in SWEEP_SCHEDULES:
+                sch = sk.schedule(mode, s, tile=tile)
+                nb = sk.sk_workspace_size(m, m, ww.K, nsms, sch, red)
+                ws = torch.zeros(nb, dtype=torch.uint8, device=dev)
+                plan = sk.sk_plan(m, m, ww.K, nsms, sch)
+                row = {"M": m, "N": m, "K": ww.K, "tile": tile, "tiles": int(plan[2]), "num_sms": nsms,
+                       "schedule": name, "resolved_mode": int(plan[1]), "label": int(plan[9])}
+                if flushed:
                     for _ in range(5):
                         sk.sk_gemm(A, B, C, sk.SK_BF16, m, m, ww.K, sk.SK_NN, sch, red, nsms, ws, nb, stream)
                     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                          for _ in range(30)]
+                          for _ in range(flushed)]
                     for a, b in ev:
                         flush.zero_()
                         a.record(stream)
                         sk.sk_gemm(A, B, C, sk.SK_BF16, m, m, ww.K, sk.SK_NN, sch, red, nsms, ws, nb, stream)
                         b.record(stream)
                     torch.cuda.synchronize(dev)
-                    assert sk.sk_status(ws, stream) == sk.SK_OK
                     t = float(np.median([a.elapsed_time(b) for a, b in ev]))
-                    tf = fl / (t / 1e3) / 1e12
-                    sch_o = sk.schedule(mode, s, tile=tile, overlap=1)
-                    for i in range(10):
-                        a_, b_, c_ = rot[i % len(rot)]
-                        sk.sk_gemm(a_, b_, c_, sk.SK_BF16, m, m, ww.K, sk.SK_NN, sch_o, red, nsms, ws, nb, stream)
-                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                    e0.record(stream)
-                    for i in range(60):
-                        a_, b_, c_ = rot[i % len(rot)]
-                        sk.sk_gemm(a_, b_, c_, sk.SK_BF16, m, m, ww.K, sk.SK_NN, sch_o, red, nsms, ws, nb, stream)
-                    e1.record(stream)
-                    torch.cuda.synchronize(dev)
-                    assert sk.sk_status(ws, stream) == sk.SK_OK
-                    tb = e0.elapsed_time(e1) / 60
-                    tfb = fl / (tb / 1e3) / 1e12
-                    f.write(json.dumps({"M": m, "N": m, "K": ww.K, "tile": tile, "tiles": int(plan[2]), "num_sms": nsms,
-                                        "schedule": name, "resolved_mode": int(plan[1]), "label": int(plan[9]),
-                                        "us": t * 1e3, "tflops": tf, "frac_of_measured_peak": tf / peak_tf,
-                                        "us_b2b": tb * 1e3, "tflops_b2b": tfb,
-                                        "frac_of_measured_peak_b2b": tfb / peak_tf, "rotating_sets": len(rot)}) + "\n")
-                    f.flush()
-            # The library GEMM (cuBLAS through torch.matmul, BF16 out) on the same operands, timed
-            # the same two ways: context for the schedules above, outside any timed step.
-            t, tb = library_timed(torch, dev, flush, stream, rot, m, m)
-            f.write(json.dumps({"M": m, "N": m, "K": ww.K, "tile": None, "num_sms": dev_sms, "schedule": "cublas",
-                                "us": t * 1e3, "tflops": fl / (t / 1e3) / 1e12,
-                                "frac_of_measured_peak": fl / (t / 1e3) / 1e12 / peak_tf,
-                                "us_b2b": tb * 1e3, "tflops_b2b": fl / (tb / 1e3) / 1e12,
-                                "frac_of_measured_peak_b2b": fl / (tb / 1e3) / 1e12 / peak_tf,
-                                "rotating_sets": len(rot)}) + "\n")
+                    row.update({"us": t * 1e3, "tflops": fl / (t / 1e3) / 1e12,
+                                "frac_of_measured_peak": fl / (t / 1e3) / 1e12 / peak_tf})
+                sch_o = sk.schedule(mode, s, tile=tile, overlap=1)
+                for i in range(10):
+                    a_, b_, c_ = rot[i % len(rot)]
+                    sk.sk_gemm(a_, b_, c_, sk.SK_BF16, m, m, ww.K, sk.SK_NN, sch_o, red, nsms, ws, nb, stream)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                for i in range(b2b):
+                    a_, b_, c_ = rot[i % len(rot)]
+                    sk.sk_gemm(a_, b_, c_, sk.SK_BF16, m, m, ww.K, sk.SK_NN, sch_o, red, nsms, ws, nb, stream)
+                e1.record(stream)
+                torch.cuda.synchronize(dev)
+                assert sk.sk_status(ws, stream) == sk.SK_OK
+                tb = e0.elapsed_time(e1) / b2b
+                tfb = fl / (tb / 1e3) / 1e12
+                row.update({"us_b2b": tb * 1e3, "tflops_b2b": tfb, "frac_of_measured_peak_b2b": tfb / peak_tf,
+                            "rotating_sets": len(rot)})
+                yield row
+        if library:
+            # The library GEMM (cuBLAS through torch.matmul, BF16 out) on the same operands,
+            # timed the same two ways: context for the schedules, outside any timed step.
+            t, tb = library_timed(torch, dev, flush, stream, rot, m, m, flushed=max(flushed, 10), b2b=b2b)
+            yield {"M": m, "N": m, "K": ww.K, "tile": None, "num_sms": None, "schedule": "cublas",
+                   "us": t * 1e3, "tflops": fl / (t / 1e3) / 1e12, "frac_of_measured_peak": fl / (t / 1e3) / 1e12 / peak_tf,
+                   "us_b2b": tb * 1e3, "tflops_b2b": fl / (tb / 1e3) / 1e12,
+                   "frac_of_measured_peak_b2b": fl / (tb / 1e3) / 1e12 / peak_tf, "rotating_sets": len(rot)}
+        del rot, A, B, C
+
+
+def run_sweep(sk, torch, dev, path, red, flush, stream, peak_tf, dev_sms, l2_bytes):
+    """The full tile-count sweep: M = N = 128 .. 4096 step 128, K = 4096, every schedule with
+    the pages' 128 x 128 tile and the 256 x 256 CTA-pair tile, on 148 SMs and on the device's
+    SM count; one JSON line per point, 30 flushed single launches and 60 back to back."""
+    with open(path, "w") as f:
+        for row in sweep_points(sk, torch, dev, red, flush, stream, peak_tf, l2_bytes, synth.SWEEP_SIZES,
+                                ((148, 0), (dev_sms, 0), (148, 2), (dev_sms, 2)), flushed=30, b2b=60, library=True):
+            f.write(json.dumps(row) + "\n")
             f.flush()
+
+
+def run_sweep_compact(sk, torch, dev, red, flush, stream, peak_tf, l2_bytes):
+    """The tile-count sweep in the default bench line: M = N in SWEEP_COMPACT, K = 4096, the
+    four schedules with the pages' 128 x 128 tile and the 256 x 256 CTA-pair tile on 148 SMs,
+    back to back (40 launches per point). Per size: TFLOP/s and fraction of the measured peak
+    per schedule and tile, the rule's choice, and the best."""
+    table = {}
+    for row in sweep_points(sk, torch, dev, red, flush, stream, peak_tf, l2_bytes, SWEEP_COMPACT,
+                            ((148, 0), (148, 2)), flushed=0, b2b=40, library=True):
+        key = str(row["M"])
+        ent = table.setdefault(key, {"tiles_128x128": (row["M"] // 128) ** 2})
+        if row["schedule"] == "cublas":
+            ent["cublas_tflops"] = round(row["tflops_b2b"], 1)
+            continue
+        tname = {0: "128x128", 2: "pair256x256"}[row["tile"]]
+        ent[f"{tname}/{row['schedule']}"] = {"us": round(row["us_b2b"], 2), "tflops": round(row["tflops_b2b"], 1),
+                                             "frac_of_measured_peak": round(row["frac_of_measured_peak_b2b"], 4)}
+        if row["schedule"] == "hybrid":
+            ent[f"{tname}/rule_choice"] = {0: "dp", 3: "hybrid"}.get(row["resolved_mode"], str(row["resolved_mode"]))
+    for ent in table.values():
+        pts = {k: v for k, v in ent.items() if isinstance(v, dict)}
+        best = max(pts, key=lambda k: pts[k]["tflops"])
+        ent["best"] = {"schedule": best, **pts[best]}
+    return {"K": 4096, "num_sms": 148, "timing": "back to back, 40 overlapped launches over rotating inputs >= 4x L2",
+            "sizes": table}
 
 
 def library_timed(torch, dev, flush, stream, rot, M, N, nt=False, flushed=30, b2b=60):
@@ -370,7 +411,8 @@ def run_fixups(sk, torch, dev, flush, stream, peak_tf, peak_gbs):
     """Stream-K fixups compared on the skinny shape 512 x 512 x 65536 (many contributors per
     tile) and on the wave-quantized shape: the owner waits and sums in k order, FP32
     atomics, and the separate fixup pass (every partial to its slot, then a second
-    launch sums each tile in k order). 128 x 128 and 256 x 256 pair tiles, 148 SMs."""
+    launch sums each tile in k order). 128 x 128 and 256 x 256 pair tiles, 148 SMs, with one
+    Stream-K group and with up to 8 groups (`/groupsG`: the first page's max_sk_groups_)."""
     out = {}
     for w, mode in ((synth.SKINNY, sk.SK_STREAMK), (synth.WAVEQ, sk.SK_HYBRID)):
         A_bits, B_bits = synth.make_inputs(w)
@@ -383,12 +425,13 @@ def run_fixups(sk, torch, dev, flush, stream, peak_tf, peak_gbs):
         hbm_bytes = 2.0 * (w.M * w.K + w.K * w.N) + 2.0 * w.M * w.N
         bound_us = max(fl / (peak_tf * 1e12), hbm_bytes / (peak_gbs * 1e9)) * 1e6
         rows = {"roofline_us": bound_us}
-        for tile, tname in ((0, "128x128"), (2, "pair256x256")):
-            plan = sk.sk_plan(w.M, w.N, w.K, 148, sk.schedule(mode, tile=tile))
+        for (tile, tname), groups in itertools.product(((0, "128x128"), (2, "pair256x256")), (0, 8)):
+            plan = sk.sk_plan(w.M, w.N, w.K, 148, sk.schedule(mode, tile=tile, sk_groups=groups))
             contrib = plan[-sk.SK_MAP_TILE * int(plan[2]) + 1::sk.SK_MAP_TILE]
+            gname = f"/groups{int(plan[17])}" if groups else ""
             for name, part, red in (("owner", 0, sk.SK_DETERMINISTIC), ("atomic", 0, sk.SK_ATOMIC),
                                     ("pass", 1, sk.SK_DETERMINISTIC)):
-                sch = sk.schedule(mode, split_partials=part, tile=tile)
+                sch = sk.schedule(mode, split_partials=part, tile=tile, sk_groups=groups)
                 nb = sk.sk_workspace_size(w.M, w.N, w.K, 148, sch, red)
                 ws = torch.zeros(nb, dtype=torch.uint8, device=dev)
                 g = lambda: sk.sk_gemm(A, B, C, sk.SK_BF16, w.M, w.N, w.K, sk.SK_NN, sch, red, 148, ws, nb, stream)
@@ -403,7 +446,7 @@ def run_fixups(sk, torch, dev, flush, stream, peak_tf, peak_gbs):
                 torch.cuda.synchronize(dev)
                 assert sk.sk_status(ws, stream) == sk.SK_OK
                 us = float(np.median([a0.elapsed_time(a1) for a0, a1 in ev])) * 1e3
-                rows[f"{tname}/{name}"] = {"us": us, "tflops": fl / (us / 1e6) / 1e12, "launches": 2 if part else 1,
+                rows[f"{tname}/{name}{gname}"] = {"us": us, "tflops": fl / (us / 1e6) / 1e12, "launches": 2 if part else 1,
                                            "max_contributors_per_tile": int(max(contrib)),
                                            "frac_of_roofline": bound_us / us}
         out[w.name] = rows
@@ -509,14 +552,15 @@ def main():
     ap.add_argument("--sms", type=int, default=148, help="SM count the schedule is built for (0 = device)")
     ap.add_argument("--mode", default="hybrid", choices=["dp", "splitk", "streamk", "hybrid"])
     ap.add_argument("--splits", type=int, default=2)
-    ap.add_argument("--tile", type=int, default=2,
+    ap.add_argument("--tile", type=int, default=2, choices=[0, 1, 2, 3],
                     help="work-tile shape: 0 = 128x128 (one CTA), 1 = 256x128 (CTA pair), "
-                         "2 = 256x256 (CTA pair), 3 = 128x256 (one CTA), 4 = 256x512 (two CTA pairs, A multicast)")
+                         "2 = 256x256 (CTA pair), 3 = 128x256 (one CTA)")
     ap.add_argument("--reduction", default="deterministic", choices=["deterministic", "atomic"])
     ap.add_argument("--raster", type=int, default=0, choices=[0, 1], help="tile ids along N (0) or M (1)")
     ap.add_argument("--swizzle", type=int, default=0, help="tile-id strips this many tiles deep (0: none)")
     ap.add_argument("--partials", type=int, default=0, choices=[0, 1, 2],
                     help="split_partials of the timed schedule (Split-K slabs; Stream-K/hybrid separate fixup pass)")
+    ap.add_argument("--sk-groups", type=int, default=0, help="Stream-K groups of the timed schedule (0: one group)")
     ap.add_argument("--overlap", type=int, default=1, choices=[0, 1],
                     help="launch each step overlapped with the one before it (programmatic dependent launch)")
     ap.add_argument("--timing", default="stream", choices=["stream", "flush"],
@@ -579,9 +623,10 @@ def main():
     n_sets = max(2, -(-4 * l2_bytes // set_bytes))
     sets = [(A, B, C)] + [(A.clone(), B.clone(), torch.empty_like(C)) for _ in range(n_sets - 1)]
 
-    def make(mode_name, nsms, splits=1, tile=args.tile, raster=args.raster, swizzle=args.swizzle, overlap=0):
+    def make(mode_name, nsms, splits=1, tile=args.tile, raster=args.raster, swizzle=args.swizzle, overlap=0,
+             groups=args.sk_groups):
         sch = sk.schedule(modes[mode_name], splits if mode_name == "splitk" else 1, tile=tile, raster=raster,
-                          swizzle=swizzle, overlap=overlap)
+                          swizzle=swizzle, overlap=overlap, sk_groups=groups)
         nb = sk.sk_workspace_size(w.M, w.N, w.K, nsms, sch, red)
         ws = torch.zeros(nb, dtype=torch.uint8, device=dev)
         return sch, ws, nb
@@ -625,7 +670,8 @@ def main():
     sch, ws, nb = make(args.mode, sms, args.splits, overlap=args.overlap)
     if args.partials:
         sch = sk.schedule(modes[args.mode], args.splits if args.mode == "splitk" else 1, split_partials=args.partials,
-                          tile=args.tile, raster=args.raster, swizzle=args.swizzle, overlap=args.overlap)
+                          tile=args.tile, raster=args.raster, swizzle=args.swizzle, overlap=args.overlap,
+                          sk_groups=args.sk_groups)
         nb = sk.sk_workspace_size(w.M, w.N, w.K, sms, sch, red)
         ws = torch.zeros(nb, dtype=torch.uint8, device=dev)
     plan = sk.sk_plan(w.M, w.N, w.K, sms, sch)
@@ -679,12 +725,12 @@ def main():
     if not args.no_extras and rank == 0:
         # ---- per-schedule table (the metric is per schedule)
         table = {}
-        tile_names = {0: "128x128", 1: "pair256x128", 2: "pair256x256", 3: "128x256", 4: "quad256x512"}
+        tile_names = {0: "128x128", 1: "pair256x128", 2: "pair256x256", 3: "128x256"}
         for tile, name, nsms in ((0, "dp", 148), (0, "splitk2", 148), (0, "streamk", 148), (0, "hybrid", 148),
                                  (0, "dp", dev_sms), (0, "hybrid", dev_sms),
                                  (2, "dp", 148), (2, "splitk2", 148), (2, "streamk", 148), (2, "hybrid", 148),
                                  (2, "dp", dev_sms), (2, "hybrid", dev_sms),
-                                 (3, "hybrid", 148), (1, "hybrid", 148), (4, "hybrid", 144), (4, "dp", 144)):
+                                 (3, "hybrid", 148), (1, "hybrid", 148)):
             mname = "splitk" if name.startswith("splitk") else name
             s2, ws2, nb2 = make(mname, nsms, 2, tile)
             t = timed(s2, ws2, nb2, nsms, 200, 10)
@@ -700,7 +746,7 @@ def main():
         # overlapped launch: what a stream of GEMMs pays per step beyond the kernel itself.
         b2b = {}
         for tile, name, nsms in ((2, "hybrid", 148), (2, "dp", 148), (2, "streamk", 148), (0, "hybrid", 148),
-                                 (2, "hybrid", dev_sms), (4, "hybrid", 144), (4, "dp", 144)):
+                                 (2, "hybrid", dev_sms)):
             mname = "splitk" if name.startswith("splitk") else name
             row = {}
             for ov in (0, 1):
@@ -758,7 +804,7 @@ def main():
         def b2b_timeline(ov):
             s4 = sk.schedule(modes[args.mode], args.splits if args.mode == "splitk" else 1, units=0,
                              split_partials=args.partials, tile=args.tile, raster=args.raster, swizzle=args.swizzle,
-                             overlap=ov)
+                             overlap=ov, sk_groups=args.sk_groups)
             nb4 = sk.sk_workspace_size(w.M, w.N, w.K, sms, s4, red)
             ws4 = torch.zeros(nb4, dtype=torch.uint8, device=dev)
             plan4 = sk.sk_plan(w.M, w.N, w.K, sms, s4)
@@ -897,6 +943,7 @@ def main():
         extras["smallm_nt"] = run_smallm(sk, torch, dev, flush, stream, dev_sms)
         extras["fixups"] = run_fixups(sk, torch, dev, flush, stream, peak_tf, float(peaks["hbm_gbs"]))
         extras["raster_8192"] = run_raster(sk, torch, dev, flush, stream, peak_tf)
+        extras["sweep"] = run_sweep_compact(sk, torch, dev, red, flush, stream, peak_tf, l2_bytes)
 
         if args.sweep:
             run_sweep(sk, torch, dev, args.sweep, red, flush, stream, peak_tf, dev_sms, l2_bytes)
@@ -918,10 +965,10 @@ def main():
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "layout": w.layout, "out": w.out,
                    "schedule": args.mode, "split_partials": args.partials, "reduction": args.reduction, "num_sms": sms, "device_sms": dev_sms,
-                   "tile": {0: "128x128", 1: "256x128 CTA pair", 2: "256x256 CTA pair", 3: "128x256",
-                            4: "256x512 two CTA pairs, A multicast"}[args.tile],
+                   "tile": {0: "128x128", 1: "256x128 CTA pair", 2: "256x256 CTA pair", 3: "128x256"}[args.tile],
                    "tile_m": int(plan[12]), "tile_n": int(plan[13]), "ctas_per_tile": int(plan[14]),
                    "raster": "along_n" if args.raster == 0 else "along_m", "swizzle": args.swizzle,
+                   "sk_groups": int(plan[17]),
                    "tiles": int(plan[2]), "iters": int(plan[3]), "workers": int(plan[4]),
                    "resolved_mode": int(plan[1]), "sk_tiles": int(plan[5]), "sk_units": int(plan[6]),
                    "overlap": args.overlap, "timing": args.timing,

@@ -24,7 +24,7 @@ SK_F32, SK_BF16 = 0, 1
 SK_ROLE_FULL, SK_ROLE_OWNER, SK_ROLE_PRODUCER, SK_ROLE_SLAB = 0, 1, 2, 3
 SK_OK, SK_EINVAL, SK_EWORKSPACE, SK_ECUDA, SK_ETIMEOUT, SK_ECAPACITY, SK_ERESIDENCY, SK_EBOUNDS = 0, -1, -2, -3, -4, -5, -6, -7
 SK_TILE_M, SK_TILE_N, SK_BLK_K = 128, 128, 64
-SK_MAP_VERSION, SK_MAP_HEADER, SK_MAP_SEG, SK_MAP_TILE = 2, 17, 9, 4
+SK_MAP_VERSION, SK_MAP_HEADER, SK_MAP_SEG, SK_MAP_TILE = 3, 18, 9, 4
 SK_TILE_128x128, SK_TILE_256x128_PAIR, SK_TILE_256x256_PAIR, SK_TILE_128x256 = 0, 1, 2, 3
 SK_WS_HEADER_BYTES = 256
 SK_TRACE_SEGS = 15
@@ -38,12 +38,14 @@ SK_NOALLOC_SCRATCH_BYTES = 16 << 20
 class sk_schedule(ctypes.Structure):
     _fields_ = [("mode", ctypes.c_int32), ("splits", ctypes.c_int32), ("units", ctypes.c_int32),
                 ("min_iters", ctypes.c_int32), ("split_partials", ctypes.c_int32), ("tile", ctypes.c_int32),
-                ("raster", ctypes.c_int32), ("swizzle", ctypes.c_int32), ("overlap", ctypes.c_int32)]
+                ("raster", ctypes.c_int32), ("swizzle", ctypes.c_int32), ("overlap", ctypes.c_int32),
+                ("sk_groups", ctypes.c_int32)]
 
 
 class sk_debug_opts(ctypes.Structure):
     _fields_ = [("reverse_units", ctypes.c_int32), ("skip_producer_signal", ctypes.c_int32),
-                ("timeout_ns", ctypes.c_int64), ("dump", ctypes.c_void_p), ("trace", ctypes.c_void_p)]
+                ("timeout_ns", ctypes.c_int64), ("dump", ctypes.c_void_p), ("trace", ctypes.c_void_p),
+                ("zero_partials", ctypes.c_int32)]
 
 
 class SkError(RuntimeError):
@@ -53,8 +55,8 @@ class SkError(RuntimeError):
 
 
 def schedule(mode: int, splits: int = 1, units: int = 0, min_iters: int = 0, split_partials: int = 0,
-             tile: int = 0, raster: int = 0, swizzle: int = 0, overlap: int = 0) -> sk_schedule:
-    return sk_schedule(mode, splits, units, min_iters, split_partials, tile, raster, swizzle, overlap)
+             tile: int = 0, raster: int = 0, swizzle: int = 0, overlap: int = 0, sk_groups: int = 0) -> sk_schedule:
+    return sk_schedule(mode, splits, units, min_iters, split_partials, tile, raster, swizzle, overlap, sk_groups)
 
 
 _lib = None
@@ -141,8 +143,10 @@ def sk_gemm(A, B, C, c_dtype: int, M: int, N: int, K: int, layout: int, sched: s
 
 def sk_gemm_debug(A, B, C, c_dtype: int, M: int, N: int, K: int, layout: int, sched: sk_schedule, reduction: int,
                   num_sms: int, workspace, ws_bytes: int, stream=None, reverse_units: int = 0,
-                  skip_producer_signal: int = 0, timeout_ns: int = 0, dump=None, trace=None) -> int:
-    opts = sk_debug_opts(reverse_units, skip_producer_signal, timeout_ns, _ptr(dump) or None, _ptr(trace) or None)
+                  skip_producer_signal: int = 0, timeout_ns: int = 0, dump=None, trace=None,
+                  zero_partials: int = 0) -> int:
+    opts = sk_debug_opts(reverse_units, skip_producer_signal, timeout_ns, _ptr(dump) or None, _ptr(trace) or None,
+                         zero_partials)
     return _check(lib().sk_gemm_debug(_ptr(A), _ptr(B), _ptr(C), c_dtype, M, N, K, layout, sched, reduction,
                                       num_sms, _ptr(workspace), ws_bytes, _stream(stream), ctypes.byref(opts)),
                   "sk_gemm_debug")

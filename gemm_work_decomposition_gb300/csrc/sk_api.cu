@@ -51,13 +51,14 @@ void heuristic(int64_t tiles, int64_t iters, int64_t sms, int64_t min_iters, int
     }
 }
 
-void set_streamk(Sched& o, int64_t base, int64_t sk_tiles, int64_t units, bool sep) {
+void set_streamk(Sched& o, int64_t base, int64_t sk_tiles, int64_t units, bool sep, int32_t groups) {
     const int64_t total = sk_tiles * o.iters;
     o.sk_base = static_cast<int32_t>(base);
     o.sk_tiles = static_cast<int32_t>(sk_tiles);
     o.sk_units = static_cast<int32_t>(units);
     o.sk_q = static_cast<int32_t>(total / units);
     o.sk_big = static_cast<int32_t>(total % units);
+    o.sk_groups = sk_group_count(o.sk_tiles, o.iters, o.sk_units, groups);
     o.sep = sep ? 1 : 0;
     o.n_slots = static_cast<int32_t>((sep ? 2 : 1) * units);
 }
@@ -72,11 +73,9 @@ int32_t make_sched(int32_t M, int32_t N, int32_t K, int32_t num_sms, const sk_sc
     if (s.split_partials != 0 && s.mode == SK_DP) return SK_EINVAL;
     int32_t tm = 0, tn = 0, cg = 0;
     if (!tile_shape(s.tile, &tm, &tn, &cg)) return SK_EINVAL;
-    // The four-CTA tile runs data-parallel, Stream-K and the hybrid rule with the in-kernel
-    // fixup only (no Split-K slabs, no separate pass).
-    if (cg == 4 && (s.mode == SK_SPLITK || s.split_partials != 0)) return SK_EINVAL;
     if (s.raster < 0 || s.raster > 1 || s.swizzle < 0 || s.swizzle > 256) return SK_EINVAL;
     if (s.overlap < 0 || s.overlap > 1) return SK_EINVAL;
+    if (s.sk_groups < 0 || s.sk_groups > 64) return SK_EINVAL;
     const int64_t tiles_n = (static_cast<int64_t>(N) + tn - 1) / tn;
     const int64_t tiles = ((static_cast<int64_t>(M) + tm - 1) / tm) * tiles_n;
     const int64_t iters = (static_cast<int64_t>(K) + kBlkK - 1) / kBlkK;
@@ -110,7 +109,7 @@ int32_t make_sched(int32_t M, int32_t N, int32_t K, int32_t num_sms, const sk_sc
         } else {
             const int64_t dp_tiles = tiles - skt;
             o.mode = kHybrid;
-            set_streamk(o, dp_tiles, skt, sku, s.split_partials == 1);
+            set_streamk(o, dp_tiles, skt, sku, s.split_partials == 1, s.sk_groups);
             o.dp_tiles = static_cast<int32_t>(dp_tiles);
             const int64_t dpw = dp_tiles < S ? dp_tiles : S;
             o.workers = static_cast<int32_t>(sku > dpw ? sku : dpw);
@@ -125,7 +124,7 @@ int32_t make_sched(int32_t M, int32_t N, int32_t K, int32_t num_sms, const sk_sc
         const int64_t total = tiles * iters;
         const int64_t U = total < S ? total : S;
         o.mode = kStreamK;
-        set_streamk(o, 0, tiles, U, s.split_partials == 1);
+        set_streamk(o, 0, tiles, U, s.split_partials == 1, s.sk_groups);
         o.workers = static_cast<int32_t>(U);
     } else {  // SK_SPLITK
         if (s.splits < 1 || s.splits > iters) return SK_EINVAL;
@@ -248,6 +247,29 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 }  // namespace
 
+namespace sk {
+int32_t workspace_zero_spans(int32_t M, int32_t N, int32_t K, int32_t num_sms, const void* sched, int32_t reduction,
+                             int64_t (&off)[2], int64_t (&len)[2]) {
+    Sched s;
+    const int32_t e = make_sched(M, N, K, num_sms, *static_cast<const sk_schedule*>(sched), s);
+    if (e != SK_OK) return e;
+    off[0] = 0;
+    off[1] = 0;
+    len[1] = 0;
+    if (s.partials) {
+        // header | slabs (written in full by every launch) | arrival counters
+        const int64_t c = slab_counters_offset(s.splits, M, N);
+        len[0] = SK_WS_HEADER_BYTES;
+        off[1] = c;
+        len[1] = workspace_bytes(s, M, N) - c;
+    } else {
+        // header | flags | slots; atomic peers add into the slots, which start at zero
+        len[0] = reduction == SK_ATOMIC ? workspace_bytes(s, M, N) : slots_offset(s);
+    }
+    return SK_OK;
+}
+}  // namespace sk
+
 extern "C" {
 
 const char* sk_strerror(int32_t code) {
@@ -296,6 +318,7 @@ int32_t sk_plan(int32_t M, int32_t N, int32_t K, int32_t num_sms, sk_schedule s,
     h[14] = sch.cg;
     h[15] = sch.raster;
     h[16] = sch.swizzle;
+    h[17] = sch.sk_groups;
     int32_t* seg = map + SK_MAP_HEADER;
     int32_t* trow = seg + SK_MAP_SEG * nseg;
     for (int32_t t = 0; t < sch.tiles; ++t) {
@@ -381,6 +404,7 @@ int32_t sk_gemm_debug(const void* A, const void* B, void* C, sk_dtype c_dtype, i
     if (opts) {
         a.reverse = opts->reverse_units ? 1 : 0;
         a.skip_signal = opts->skip_producer_signal ? 1 : 0;
+        a.zero_partials = opts->zero_partials ? 1 : 0;
         if (opts->timeout_ns > 0) a.timeout_ns = static_cast<uint64_t>(opts->timeout_ns);
         a.dump = opts->dump;
         if (a.dump && !aligned(a.dump, 16)) return SK_EINVAL;

@@ -74,13 +74,10 @@ __device__ __forceinline__ void record_timeout(const KArgs& a, volatile int* abo
 }
 
 // Where a CTA sits in its work tile: `rank` in its MMA pair (0 = the pair's leader, which
-// issues the MMAs; its rows are rank * 128 ..), `pair` among the tile's pairs (its columns
-// are pair * kBN ..), and `cta` = 2 * pair + rank among the tile's CTAs (its block of every
-// partial slot and its flag). One-CTA tiles: all zero.
+// issues the MMAs; its rows are rank * 128 .. of the tile, and its block of every partial
+// slot and its flag are number `rank`). One-CTA tiles: zero.
 struct CtaPos {
     uint32_t rank;
-    int pair;
-    int cta;
 };
 
 // A Stream-K producer segment covers [k_begin, iters) of its tile: it runs its k-loop from
@@ -114,7 +111,7 @@ __device__ bool prefetch_partials(const KArgs& a, const Smem<Shape<kCG, kBN>>& s
         g.peer_begin + g.n_peers > a.sch.n_slots)
         return true;
     for (int32_t pi = 0; pi < g.n_peers; ++pi) {
-        const int32_t* f = a.flags + (g.peer_begin + pi) * a.sch.cg + pos.cta;
+        const int32_t* f = a.flags + (g.peer_begin + pi) * a.sch.cg + static_cast<int>(pos.rank);
         for (uint32_t n = 0; ld_acquire_gpu(f) < 1; ++n) {
             if ((n & 15u) == 15u && (*abort_flag || globaltimer() > deadline)) return false;
             __nanosleep(32);
@@ -130,7 +127,7 @@ __device__ bool prefetch_partials(const KArgs& a, const Smem<Shape<kCG, kBN>>& s
     if (atomicCAS(prefetch, 0, kPrefetchIssued + k) != 0) return true;  // the epilogue has given up
     fence_proxy_async_global();  // the flag acquires before the copies' reads
     for (int ew = 0; ew < 4; ++ew)
-        for (int j = 0; j < k; ++j) fetch_partial(a, sm, g, pos.cta, ew, j);
+        for (int j = 0; j < k; ++j) fetch_partial(a, sm, g, static_cast<int>(pos.rank), ew, j);
     return true;
 }
 
@@ -150,7 +147,7 @@ __device__ void prefetch_first_loads(const KArgs& a, const CUtensorMap* tmA, con
         int32_t trow, tcolumn;
         tile_coords(a.sch, g.tile, &trow, &tcolumn);
         const int32_t m0 = trow * (kCtaRows * kCG) + static_cast<int32_t>(pos.rank) * kCtaRows;
-        const int32_t nb = tcolumn * a.sch.tile_n + pos.pair * kBN + static_cast<int32_t>(pos.rank) * S::kBNc;
+        const int32_t nb = tcolumn * a.sch.tile_n + static_cast<int32_t>(pos.rank) * S::kBNc;
         const bool rev = reversed_segment(a.sch, g);
         for (int32_t i = 0; i < g.k_end - g.k_begin && n < S::kStages; ++i, ++n) {
             const int32_t k0 = seg_k(g, rev, i) * kBlkK;
@@ -165,11 +162,7 @@ __device__ void prefetch_first_loads(const KArgs& a, const CUtensorMap* tmA, con
     }
 }
 
-// kMC = 2 (the four-CTA tile): the two pairs compute the tile's two column halves over the same
-// rows, so pair 0 loads each half of A once and multicasts it to the same-rank CTA of both
-// pairs; pair 1 loads only its B. Every CTA waits until both pairs have consumed a stage (its
-// empty barrier counts one commit per pair) before anything lands there again.
-template <bool kNT, int kCG, int kBN, int kMC>
+template <bool kNT, int kCG, int kBN>
 __device__ void run_producer(const KArgs& a, const CUtensorMap* tmA, const CUtensorMap* tmB,
                              const Smem<Shape<kCG, kBN>>& sm, int unit, const CtaPos& pos, uint64_t deadline,
                              volatile int* abort_flag, int* prefetch) {
@@ -190,7 +183,7 @@ __device__ void run_producer(const KArgs& a, const CUtensorMap* tmA, const CUten
         int32_t trow, tcolumn;
         tile_coords(a.sch, g.tile, &trow, &tcolumn);
         const int32_t m0 = trow * (kCtaRows * kCG) + static_cast<int32_t>(rank) * kCtaRows;
-        const int32_t nb = tcolumn * a.sch.tile_n + pos.pair * kBN + static_cast<int32_t>(rank) * S::kBNc;
+        const int32_t nb = tcolumn * a.sch.tile_n + static_cast<int32_t>(rank) * S::kBNc;
         const bool rev = reversed_segment(a.sch, g);
         for (int32_t i = 0; i < g.k_end - g.k_begin; ++i) {
             if (!mbar_wait(sm.empty(stage), phase ^ 1u, abort_flag, deadline)) {
@@ -211,13 +204,9 @@ __device__ void run_producer(const KArgs& a, const CUtensorMap* tmA, const CUten
             } else {
                 // Both CTAs' loads complete on the leader's barrier, which the leader arms
                 // for the bytes of both.
-                const uint32_t fb = mapa_shared(sm.full(stage), static_cast<uint32_t>(2 * pos.pair));
+                const uint32_t fb = mapa_shared(sm.full(stage), 0u);
                 if (rank == 0) mbar_arrive_expect_tx(sm.full(stage), S::kTxBytes);
-                if (kMC == 1)
-                    tma_load_2d_pair(sm.a(stage), tmA, fb, k0, m0);
-                else if (pos.pair == 0)
-                    tma_load_2d_pair_mc(sm.a(stage), tmA, fb, k0, m0,
-                                        static_cast<uint16_t>((1u << rank) | (1u << (rank + 2))));
+                tma_load_2d_pair(sm.a(stage), tmA, fb, k0, m0);
                 if (kNT) {
                     tma_load_2d_pair(sm.b(stage), tmB, fb, k0, nb);
                 } else {
@@ -236,8 +225,8 @@ __device__ void run_producer(const KArgs& a, const CUtensorMap* tmA, const CUten
     if (ok && kEpiGroups == 1 && nseg > 0 && last.role == kOwner && !a.sch.sep && !a.atomic)
         ok = prefetch_partials<kCG, kBN>(a, sm, last, pos, issued, deadline, abort_flag, prefetch);
     if (!ok) record_timeout(a, abort_flag);
-    // Let the last loads land before the CTA can exit (bounded). A pair's loads (and the A
-    // multicast into it) all complete on the leader's barriers, so the leader drains for both.
+    // Let the last loads land before the CTA can exit (bounded). A pair's loads all complete
+    // on the leader's barriers, so the leader drains for both.
     if (rank == 0) {
         const uint64_t drain = globaltimer() + kDrainNs;
         const uint32_t outstanding = issued < static_cast<uint32_t>(S::kStages) ? issued : S::kStages;
@@ -250,14 +239,12 @@ __device__ void run_producer(const KArgs& a, const CUtensorMap* tmA, const CUten
 
 // --------------------------------------------------------------------------- warp 1
 // The leader of each pair issues its pair's MMAs. Its commits reach both CTAs of the pair
-// (cluster ranks 2 * pair and 2 * pair + 1), and with kMC = 2 a stage's commit reaches all
-// four CTAs, since a stage of A lands in both pairs.
-template <bool kNT, int kCG, int kBN, int kMC>
-__device__ void run_mma(const KArgs& a, const Smem<Shape<kCG, kBN>>& sm, uint32_t tmem_base, int unit, int pair,
+// (cluster ranks 0 and 1) through a cluster-multicast mbarrier arrive.
+template <bool kNT, int kCG, int kBN>
+__device__ void run_mma(const KArgs& a, const Smem<Shape<kCG, kBN>>& sm, uint32_t tmem_base, int unit,
                         uint64_t deadline, volatile int* abort_flag) {
     using S = Shape<kCG, kBN>;
-    const uint16_t pair_mask = static_cast<uint16_t>(0x3u << (2 * pair));
-    const uint16_t stage_mask = kMC == 2 ? static_cast<uint16_t>(0xF) : pair_mask;
+    constexpr uint16_t pair_mask = 0x3u;
     constexpr uint32_t kIdesc = idesc_bf16_f32(kCtaRows * kCG, kBN, kNT ? 0u : 1u);
     // K advance per 16-deep MMA inside one 64-deep stage: K-major operands move 32 bytes
     // along the swizzled row; the MN-major B of NN moves 16 rows of 128 bytes.
@@ -332,7 +319,7 @@ __device__ void run_mma(const KArgs& a, const Smem<Shape<kCG, kBN>>& sm, uint32_
                 if (kCG == 1)
                     umma_commit(sm.empty(stage));
                 else
-                    umma_commit_pair(sm.empty(stage), stage_mask);
+                    umma_commit_pair(sm.empty(stage), pair_mask);
                 if (++stage == S::kStages) {
                     stage = 0;
                     phase ^= 1u;
@@ -359,7 +346,7 @@ __device__ void run_mma(const KArgs& a, const Smem<Shape<kCG, kBN>>& sm, uint32_
     if (kCG == 1)
         umma_commit(sm.done());
     else
-        umma_commit_pair(sm.done(), static_cast<uint16_t>(0x1u << (2 * pair)));
+        umma_commit_pair(sm.done(), static_cast<uint16_t>(0x1u));
     mbar_wait_until(sm.done(), 0u, globaltimer() + kDrainNs);
 }
 
@@ -586,7 +573,6 @@ struct Epi {
     volatile int* abort_flag;
     int lane, gt, quad, row;     // gt: thread index within the group
     int32_t r;                   // rank in the MMA pair: this CTA's rows are r * 128 .. of the tile
-    int pair;                    // pair within the tile: its columns are pair * kBN ..
     int cta;                     // CTA within the tile: its block of a partial slot, its flags
     uint32_t tcol, staging, nstore;
     uint32_t nbuf;               // staging buffers in turn: kBoxes, or more in the ring (see `wide`)
@@ -612,7 +598,7 @@ struct Epi {
         int32_t trow, tcolumn;
         tile_coords(a.sch, g.tile, &trow, &tcolumn);
         const int32_t m0 = trow * (kCtaRows * kCG) + r * kCtaRows;
-        const int32_t n0 = tcolumn * a.sch.tile_n + pair * kBN;
+        const int32_t n0 = tcolumn * a.sch.tile_n;
         const int32_t gr = m0 + row;
         const int64_t slab = static_cast<int64_t>(a.M) * a.N;
 #pragma unroll 1
@@ -663,7 +649,7 @@ struct Epi {
         const int32_t r_begin = g.slot * rows_per;
         const int32_t r_end = imin(kCtaRows, r_begin + rows_per);
         const int32_t m0 = trow * (kCtaRows * kCG) + r * kCtaRows;
-        const int32_t n0 = tcolumn * a.sch.tile_n + pair * kBN;
+        const int32_t n0 = tcolumn * a.sch.tile_n;
         const int64_t slab = static_cast<int64_t>(a.M) * a.N;
         constexpr int kGroups = kBN / 4;  // 4-column groups per row
         constexpr int kBatch = 8;
@@ -757,12 +743,12 @@ struct Epi {
         int32_t trow, tcolumn;
         tile_coords(a.sch, g.tile, &trow, &tcolumn);
         const int32_t m0 = trow * (kCtaRows * kCG) + r * kCtaRows;
-        const int32_t n0 = tcolumn * a.sch.tile_n + pair * kBN;
+        const int32_t n0 = tcolumn * a.sch.tile_n;
         const int32_t wy = m0 + quad * 32;  // first row of this warp's 32
         float* dump = a.dump ? a.dump +
                                    (static_cast<int64_t>(g.tile) * a.sch.iters + g.k_begin) *
                                        (static_cast<int64_t>(kCtaRows * kCG) * a.sch.tile_n) +
-                                   static_cast<int64_t>(r * kCtaRows + row) * a.sch.tile_n + pair * kBN
+                                   static_cast<int64_t>(r * kCtaRows + row) * a.sch.tile_n
                              : nullptr;
         float v[kPassCols];
         if (kFixup && !bulk) {
@@ -802,6 +788,11 @@ struct Epi {
             nstore = 0;
         }
         const int n_items = bulk ? S::kPasses * g.n_peers : 0;
+        // Numerical control (tests): every partial this segment hands on (a producer's
+        // partial, a Split-K slab, an owner's slot of the separate pass) is stored as zeros,
+        // with its flags and counters raised as usual.
+        const bool zero_store = a.zero_partials != 0 &&
+                                (g.role == kProducer || g.role == kSlab || (g.role == kOwner && a.sch.sep != 0));
         int issued = bulk ? (n_items > 1 ? 2 : 1) : 0;  // the producer warp's copies
         int waited = 0;
         bool failed = false;
@@ -837,6 +828,10 @@ struct Epi {
                 if (dump) {
 #pragma unroll
                     for (int h = 0; h < kPassCols / 64; ++h) dump_row<kPassCols>(dump + p * kPassCols + h * 64, t, h * 64);
+                }
+                if (zero_store) {
+#pragma unroll
+                    for (int i = 0; i < kPassCols; ++i) v[i] = 0.f;
                 }
             }
             if (p == S::kPasses - 1 && release) {
@@ -1025,8 +1020,7 @@ __device__ void run_epilogue_group(const KArgs& a, const CUtensorMap* tmC, const
     e.quad = warp & 3;                        // TMEM lanes this warp may read: 32*quad ..
     e.row = e.quad * 32 + e.lane;             // row of this CTA's part of the tile
     e.r = static_cast<int32_t>(pos.rank);
-    e.pair = pos.pair;
-    e.cta = pos.cta;
+    e.cta = static_cast<int>(pos.rank);
     e.tcol = static_cast<uint32_t>(e.quad * 32) << 16;
     e.staging = sm.base + S::kStagingOff + static_cast<uint32_t>(ew * kBoxes) * 4096u;
     e.nstore = 0;
@@ -1038,7 +1032,7 @@ __device__ void run_epilogue_group(const KArgs& a, const CUtensorMap* tmC, const
     e.prefetch = prefetch;
     e.shared_tmp = shared_tmp;
     // The accumulator-empty barriers live in the pair's leader CTA.
-    const uint32_t leader = static_cast<uint32_t>(2 * pos.pair);
+    const uint32_t leader = 0u;
     e.tempty0 = kCG == 1 ? sm.tempty(0) : mapa_shared(sm.tempty(0), leader);
     e.tempty1 = kCG == 1 ? sm.tempty(1) : mapa_shared(sm.tempty(1), leader);
     e.blk_off = static_cast<int64_t>(e.quad) * S::kWarpSlotFloats;
@@ -1101,9 +1095,9 @@ __device__ void run_epilogue(const KArgs& a, const CUtensorMap* tmC, const CUten
 }
 
 // --------------------------------------------------------------------------- kernel
-// kCG CTAs per MMA (1, or a pair with cta_group::2); kMC pairs per work tile (2: the four-CTA
-// tile, one cluster of two pairs sharing A by multicast); kBN accumulator columns per CTA.
-template <bool kNT, int kCG, int kBN, int kMC>
+// kCG CTAs per MMA and per work tile (1, or a pair with cta_group::2); kBN accumulator
+// columns per CTA.
+template <bool kNT, int kCG, int kBN>
 __global__ void __launch_bounds__(kThreads, 1)
     sk_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmD,
@@ -1121,10 +1115,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    static_assert(kMC == 1 || (kMC == 2 && kCG == 2), "A is shared between CTA pairs only");
-    constexpr int kTileCtas = kCG * kMC;
+    constexpr int kTileCtas = kCG;
     const uint32_t crank = kCG == 2 ? cluster_ctarank() : 0u;
-    const CtaPos pos{crank & 1u, static_cast<int>(crank >> 1), static_cast<int>(crank)};
+    const CtaPos pos{crank};
     const uint32_t rank = pos.rank;
     const int units = static_cast<int>(gridDim.x) / kTileCtas;
     const int cid = static_cast<int>(blockIdx.x) / kTileCtas;
@@ -1133,7 +1126,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < S::kStages; ++s) {
             mbar_init(sm.full(s), 1);
-            mbar_init(sm.empty(s), kMC);  // one commit per pair that reads the stage
+            mbar_init(sm.empty(s), 1);  // one commit by the MMA issuer
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(sm.tfull(b), 1);
@@ -1178,7 +1171,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 args.trace[static_cast<int64_t>(blockIdx.x) * kTraceWords] = globaltimer();
                 start_clk = clock64();
             }
-            run_producer<kNT, kCG, kBN, kMC>(args, &tmA, &tmB, sm, unit, pos, deadline, abort_flag, prefetch);
+            run_producer<kNT, kCG, kBN>(args, &tmA, &tmB, sm, unit, pos, deadline, abort_flag, prefetch);
         }
         // Warps 0 and 1 reconverge before the exit barrier: a CTA barrier counts a warp once
         // any of its threads arrives, so all 32 lanes must arrive together.
@@ -1197,7 +1190,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         named_bar_arrive(2, 32 + kEpiThreads);
         if (kCG == 2 && rank != 0 && lane == 0)
-            mbar_arrive_cluster(mapa_shared(sm.tready(), static_cast<uint32_t>(2 * pos.pair)));
+            mbar_arrive_cluster(mapa_shared(sm.tready(), 0u));
         __syncwarp();
         tc_fence_after();
         tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_holder);
@@ -1205,7 +1198,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         grid_dep_launch();
         const uint64_t deadline = globaltimer() + args.timeout_ns;
         if (lane == 0 && rank == 0)
-            run_mma<kNT, kCG, kBN, kMC>(args, sm, tmem_base, unit, pos.pair, deadline, abort_flag);
+            run_mma<kNT, kCG, kBN>(args, sm, tmem_base, unit, deadline, abort_flag);
         __syncwarp();
     } else {
         named_bar_sync(2, 32 + kEpiThreads);
@@ -1247,12 +1240,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 // attribute. Its CTAs can only start once every CTA of the previous overlapped grid is past
 // its own wait (each issues grid_dep_launch there), and they hold SMs only where the
 // previous kernel's CTAs have left; once that kernel completes, all of this grid fits.
-template <bool kNT, int kCG, int kBN, int kMC>
+template <bool kNT, int kCG, int kBN>
 cudaError_t launch_shape(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
                          const CUtensorMap& tmD, const KArgs& a, cudaStream_t stream) {
     using S = Shape<kCG, kBN>;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(a.sch.workers * kCG * kMC), 1, 1);
+    cfg.gridDim = dim3(static_cast<unsigned>(a.sch.workers * kCG), 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = S::kSmemBytes;
     cfg.stream = stream;
@@ -1269,52 +1262,52 @@ cudaError_t launch_shape(const CUtensorMap& tmA, const CUtensorMap& tmB, const C
     }
     if (kCG == 2) {
         attr[n].id = cudaLaunchAttributeClusterDimension;
-        attr[n].val.clusterDim.x = kCG * kMC;
+        attr[n].val.clusterDim.x = kCG;
         attr[n].val.clusterDim.y = 1;
         attr[n].val.clusterDim.z = 1;
         ++n;
     }
     cfg.attrs = attr;
     cfg.numAttrs = n;
-    return cudaLaunchKernelEx(&cfg, sk_gemm_kernel<kNT, kCG, kBN, kMC>, tmA, tmB, tmC, tmD, a);
+    return cudaLaunchKernelEx(&cfg, sk_gemm_kernel<kNT, kCG, kBN>, tmA, tmB, tmC, tmD, a);
 }
 
-template <int kCG, int kBN, int kMC>
+template <int kCG, int kBN>
 cudaError_t prepare_shape(int num_sms, int* max_units) {
     using S = Shape<kCG, kBN>;
-    cudaError_t e = cudaFuncSetAttribute(sk_gemm_kernel<false, kCG, kBN, kMC>,
+    cudaError_t e = cudaFuncSetAttribute(sk_gemm_kernel<false, kCG, kBN>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmemBytes);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(sk_gemm_kernel<true, kCG, kBN, kMC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(sk_gemm_kernel<true, kCG, kBN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              S::kSmemBytes);
     if (e != cudaSuccess) return e;
     if (kCG == 1) {
         int n0 = 0, n1 = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n0, sk_gemm_kernel<false, kCG, kBN, kMC>, kThreads,
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n0, sk_gemm_kernel<false, kCG, kBN>, kThreads,
                                                           S::kSmemBytes);
         if (e != cudaSuccess) return e;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n1, sk_gemm_kernel<true, kCG, kBN, kMC>, kThreads,
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n1, sk_gemm_kernel<true, kCG, kBN>, kThreads,
                                                           S::kSmemBytes);
         if (e != cudaSuccess) return e;
         *max_units = (n0 < n1 ? n0 : n1) * num_sms;
         return cudaSuccess;
     }
-    // Units are clusters of kCG * kMC CTAs: as many as can be resident at once.
+    // Units are clusters of kCG CTAs: as many as can be resident at once.
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(kCG * kMC * (num_sms / (kCG * kMC))), 1, 1);
+    cfg.gridDim = dim3(static_cast<unsigned>(kCG * (num_sms / kCG)), 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = S::kSmemBytes;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = kCG * kMC;
+    attr[0].val.clusterDim.x = kCG;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int c0 = 0, c1 = 0;
-    e = cudaOccupancyMaxActiveClusters(&c0, sk_gemm_kernel<false, kCG, kBN, kMC>, &cfg);
+    e = cudaOccupancyMaxActiveClusters(&c0, sk_gemm_kernel<false, kCG, kBN>, &cfg);
     if (e != cudaSuccess) return e;
-    e = cudaOccupancyMaxActiveClusters(&c1, sk_gemm_kernel<true, kCG, kBN, kMC>, &cfg);
+    e = cudaOccupancyMaxActiveClusters(&c1, sk_gemm_kernel<true, kCG, kBN>, &cfg);
     if (e != cudaSuccess) return e;
     *max_units = c0 < c1 ? c0 : c1;
     return cudaSuccess;
@@ -1323,25 +1316,23 @@ cudaError_t prepare_shape(int num_sms, int* max_units) {
 }  // namespace
 
 cudaError_t prepare_device(int num_sms, int* max_units) {
-    cudaError_t e = prepare_shape<1, 128, 1>(num_sms, &max_units[0]);
-    if (e == cudaSuccess) e = prepare_shape<2, 128, 1>(num_sms, &max_units[1]);
-    if (e == cudaSuccess) e = prepare_shape<2, 256, 1>(num_sms, &max_units[2]);
-    if (e == cudaSuccess) e = prepare_shape<1, 256, 1>(num_sms, &max_units[3]);
-    if (e == cudaSuccess) e = prepare_shape<2, 256, 2>(num_sms, &max_units[4]);
+    cudaError_t e = prepare_shape<1, 128>(num_sms, &max_units[0]);
+    if (e == cudaSuccess) e = prepare_shape<2, 128>(num_sms, &max_units[1]);
+    if (e == cudaSuccess) e = prepare_shape<2, 256>(num_sms, &max_units[2]);
+    if (e == cudaSuccess) e = prepare_shape<1, 256>(num_sms, &max_units[3]);
     return e;
 }
 
 cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
                         const CUtensorMap& tmD, bool nt, const KArgs& a, cudaStream_t stream) {
     const int cg = a.sch.cg, bn = a.sch.tile_n;
-#define SK_LAUNCH(CG, BN, MC)                                                             \
-    return nt ? launch_shape<true, CG, BN, MC>(tmA, tmB, tmC, tmD, a, stream)            \
-              : launch_shape<false, CG, BN, MC>(tmA, tmB, tmC, tmD, a, stream)
-    if (cg == 1 && bn == 128) SK_LAUNCH(1, 128, 1);
-    if (cg == 2 && bn == 128) SK_LAUNCH(2, 128, 1);
-    if (cg == 2 && bn == 256) SK_LAUNCH(2, 256, 1);
-    if (cg == 1 && bn == 256) SK_LAUNCH(1, 256, 1);
-    if (cg == 4 && bn == 512) SK_LAUNCH(2, 256, 2);
+#define SK_LAUNCH(CG, BN)                                                             \
+    return nt ? launch_shape<true, CG, BN>(tmA, tmB, tmC, tmD, a, stream)            \
+              : launch_shape<false, CG, BN>(tmA, tmB, tmC, tmD, a, stream)
+    if (cg == 1 && bn == 128) SK_LAUNCH(1, 128);
+    if (cg == 2 && bn == 128) SK_LAUNCH(2, 128);
+    if (cg == 2 && bn == 256) SK_LAUNCH(2, 256);
+    if (cg == 1 && bn == 256) SK_LAUNCH(1, 256);
 #undef SK_LAUNCH
     return cudaErrorInvalidValue;
 }

@@ -26,7 +26,7 @@ constexpr int kBoxes = 2 / kEpiGroups;          // 4 KiB staging boxes per epilo
 constexpr int kCtaRows = 128;     // rows of a work tile held by one CTA (its TMEM lanes)
 constexpr int kRingBytes = 196608;
 constexpr int kTraceSegs = 15;                  // SK_TRACE_SEGS
-constexpr int kTileShapes = 5;                  // sk_tile values
+constexpr int kTileShapes = 4;                  // sk_tile values
 
 // Layout of the barrier block at the end of shared memory (byte offsets within it): the
 // pipeline mbarriers from 0 (full and empty per ring stage, tfull and tempty per accumulator,
@@ -86,6 +86,8 @@ struct KArgs {
     int32_t reverse;    // unit order reversed over the CTAs (or CTA pairs)
     int32_t skip_signal;// producers store but never raise their flag, and slab splits that share
                         // the sum never count their arrival (time-out tests)
+    int32_t zero_partials;  // every partial and slab is stored as zeros, signalled as usual
+                            // (numerical control of the tests)
 };
 
 // Launch the persistent GEMM for a.sch's tile shape: a.sch.workers units of a.sch.cg CTAs,
@@ -104,6 +106,12 @@ cudaError_t prepare_device(int num_sms, int* max_units);
 // Overlapped with the GEMM before it (programmatic stream serialization) when sch.overlap.
 cudaError_t launch_fixup(const Sched& sch, const float* slots, void* C, int32_t M, int32_t N, int c_bf16, int num_sms,
                          cudaStream_t stream);
+// Host side: the parts of a workspace that must hold zeros before a launch (the status word,
+// the flags or arrival counters, and with atomic reduction the partial tiles the peers add
+// into), as up to two byte ranges [off[i], off[i] + len[i]); unused ranges have len 0. The
+// same layout rule as sk_workspace_size. Returns SK_OK or the sk_plan error code.
+int32_t workspace_zero_spans(int32_t M, int32_t N, int32_t K, int32_t num_sms, const void* sched, int32_t reduction,
+                             int64_t (&off)[2], int64_t (&len)[2]);
 // C = sum_j P[j] in j order, FP32 -> c_bf16 ? BF16 : FP32. mn % 4 == 0. `overlap`: as for
 // launch_fixup.
 cudaError_t launch_reduce(const float* P, void* C, int c_bf16, int splits, int64_t mn, int num_sms, bool overlap,

@@ -20,7 +20,7 @@
 #include <mutex>
 
 #include "sk.h"
-#include "sk_schedule.h"
+#include "sk_kernels.h"
 
 namespace {
 
@@ -60,27 +60,22 @@ extern "C" int32_t sk_gemm_noalloc(const void* A, const void* B, void* C, sk_dty
     void* ws = nullptr;
     const int32_t e = scratch_address(&ws);
     if (e != SK_OK) return e;
-    // What must start at zero: the status word; the per-slot flags/counters (and, with
-    // atomic reduction, the partial tiles, which peers accumulate into); in split-partials
-    // mode the per-tile arrival counters after the slabs (the slabs are written in full).
-    int32_t tm = 0, tn = 0, cg = 0;
-    if (!sk::tile_shape(s.tile, &tm, &tn, &cg)) return SK_EINVAL;
+    // What must start at zero, by the workspace layout of this schedule: the status word and
+    // the flags or counters (and, with atomic reduction, the partial tiles, which peers
+    // accumulate into); in Split-K slab mode the per-tile arrival counters after the slabs
+    // (the slabs themselves are written in full).
+    int64_t off[2], len[2];
+    const int32_t ez = sk::workspace_zero_spans(M, N, K, num_sms, &s, r, off, len);
+    if (ez != SK_OK) return ez;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    int64_t clear = SK_WS_HEADER_BYTES;
-    int64_t tail = 0;  // bytes to clear at the end of the used region
-    if (s.split_partials) {
-        const int64_t tiles = ((static_cast<int64_t>(M) + tm - 1) / tm) * ((static_cast<int64_t>(N) + tn - 1) / tn);
-        tail = (4 * tiles * cg + 255) / 256 * 256;
-    } else {
-        const int64_t slot_bytes = static_cast<int64_t>(tm) * tn * 4;
-        const int64_t n_slots = (need - SK_WS_HEADER_BYTES) / slot_bytes;
-        clear = r == SK_ATOMIC ? need : need - n_slots * slot_bytes;
-    }
-    if (cudaMemsetAsync(ws, 0, static_cast<size_t>(clear), st) != cudaSuccess ||
-        (tail > 0 && cudaMemsetAsync(static_cast<unsigned char*>(ws) + need - tail, 0, static_cast<size_t>(tail), st) !=
-                         cudaSuccess)) {
-        cudaGetLastError();
-        return SK_ECUDA;
+    for (int i = 0; i < 2; ++i) {
+        if (len[i] <= 0) continue;
+        if (off[i] < 0 || off[i] + len[i] > need ||
+            cudaMemsetAsync(static_cast<unsigned char*>(ws) + off[i], 0, static_cast<size_t>(len[i]), st) !=
+                cudaSuccess) {
+            cudaGetLastError();
+            return SK_ECUDA;
+        }
     }
     return sk_gemm(A, B, C, c_dtype, M, N, K, layout, s, r, num_sms, ws, static_cast<size_t>(need), stream);
 }

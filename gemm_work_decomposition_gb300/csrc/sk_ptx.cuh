@@ -306,17 +306,6 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void* tmap,
         "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar_cluster), "r"(c0), "r"(c1)
         : "memory");
 }
-// tma_load_2d_pair, multicast: the box lands at the same offset in the shared memory of every
-// CTA in `cta_mask` (cluster ranks), and each destination's bytes complete on the barrier at
-// `bar_cluster`'s offset in that destination's pair leader (the even rank of its pair).
-__device__ __forceinline__ void tma_load_2d_pair_mc(uint32_t dst, const void* tmap, uint32_t bar_cluster, int32_t c0,
-                                                    int32_t c1, uint16_t cta_mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-        ".cta_group::2 [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar_cluster), "r"(c0), "r"(c1), "h"(cta_mask)
-        : "memory");
-}
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
     asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
                  "r"(ncols)

@@ -30,9 +30,12 @@ struct Sched {
     int32_t mode;          // resolved mode
     int32_t tiles, iters, tiles_n;
     int32_t workers;       // persistent units launched
-    // Stream-K region: tiles [sk_base, sk_base + sk_tiles) over sk_units units,
-    // unit u owning flattened iterations [u*q + min(u, big), (u+1)*q + min(u+1, big)).
-    int32_t sk_tiles, sk_units, sk_q, sk_big, sk_base;
+    // Stream-K region: tiles [sk_base, sk_base + sk_tiles) over sk_units units. With one
+    // group, unit u owns flattened iterations [u*q + min(u, big), (u+1)*q + min(u+1, big)).
+    // With sk_groups > 1 (Case 4 knob table, max_sk_groups_) the region's tiles and units are
+    // each cut big-first into sk_groups consecutive groups, and group j's units split only
+    // group j's tiles by the same rule.
+    int32_t sk_tiles, sk_units, sk_q, sk_big, sk_base, sk_groups;
     // Data-parallel region: tiles [0, dp_tiles), unit w runs w, w + workers, ...
     int32_t dp_tiles;
     // Split-K: effective split count, k-iterations per split, slab mode (1 reduction pass,
@@ -60,7 +63,6 @@ SK_HD bool tile_shape(int32_t tile, int32_t* tm, int32_t* tn, int32_t* cg) {
         case 1: *tm = 256; *tn = 128; *cg = 2; return true;
         case 2: *tm = 256; *tn = 256; *cg = 2; return true;
         case 3: *tm = 128; *tn = 256; *cg = 1; return true;
-        case 4: *tm = 256; *tn = 512; *cg = 4; return true;
         default: return false;
     }
 }
@@ -101,14 +103,56 @@ SK_HD void tile_coords(const Sched& s, int32_t t, int32_t* row, int32_t* col) {
     *col = s.raster == 0 ? b : a;
 }
 
+// n items cut into `parts` consecutive runs, the first n % parts runs one longer (the divmod
+// split of Case 2 stream_k_units): the first item of run j, and the run holding item i.
+// parts <= n, so every run is at least one long.
+SK_HD int32_t run_begin(int32_t n, int32_t parts, int32_t j) { return j * (n / parts) + imin(j, n % parts); }
+SK_HD int32_t run_of(int32_t n, int32_t parts, int32_t i) {
+    const int32_t q = n / parts, big = n % parts, edge = big * (q + 1);
+    return i < edge ? i / (q + 1) : big + (i - edge) / q;
+}
+
 // First flattened iteration of Stream-K unit u (divmod split, the first `big` units
-// one iteration longer: Case 2 stream_k_units).
-SK_HD int32_t sk_unit_begin(const Sched& s, int32_t u) { return u * s.sk_q + imin(u, s.sk_big); }
+// one iteration longer: Case 2 stream_k_units); u = sk_units gives the region's end.
+// With groups: the unit's group, its place in the group, and the group's split.
+SK_HD int32_t sk_unit_begin(const Sched& s, int32_t u) {
+    if (s.sk_groups <= 1) return u * s.sk_q + imin(u, s.sk_big);
+    if (u >= s.sk_units) return s.sk_tiles * s.iters;
+    const int32_t g = s.sk_groups;
+    const int32_t j = run_of(s.sk_units, g, u);
+    const int32_t u0 = run_begin(s.sk_units, g, j), nu = run_begin(s.sk_units, g, j + 1) - u0;
+    const int32_t t0 = run_begin(s.sk_tiles, g, j), nt = run_begin(s.sk_tiles, g, j + 1) - t0;
+    return t0 * s.iters + run_begin(nt * s.iters, nu, u - u0);
+}
 
 // The unit whose range holds flattened iteration i.
 SK_HD int32_t sk_unit_of(const Sched& s, int32_t i) {
-    const int32_t edge = s.sk_big * (s.sk_q + 1);
-    return i < edge ? i / (s.sk_q + 1) : s.sk_big + (i - edge) / s.sk_q;
+    if (s.sk_groups <= 1) {
+        const int32_t edge = s.sk_big * (s.sk_q + 1);
+        return i < edge ? i / (s.sk_q + 1) : s.sk_big + (i - edge) / s.sk_q;
+    }
+    const int32_t g = s.sk_groups;
+    const int32_t j = run_of(s.sk_tiles, g, i / s.iters);
+    const int32_t u0 = run_begin(s.sk_units, g, j), nu = run_begin(s.sk_units, g, j + 1) - u0;
+    const int32_t t0 = run_begin(s.sk_tiles, g, j), nt = run_begin(s.sk_tiles, g, j + 1) - t0;
+    return u0 + run_of(nt * s.iters, nu, i - t0 * s.iters);
+}
+
+// Groups actually used when up to `requested` are asked for: the largest g <= min(requested,
+// tiles, units) for which every group has at least as many k-iterations as units, so that no
+// unit is left empty (the knob table's "up to"); 0 or 1 gives one group.
+SK_HD int32_t sk_group_count(int32_t tiles, int32_t iters, int32_t units, int32_t requested) {
+    int32_t g = imin(imin(requested > 1 ? requested : 1, tiles), units);
+    for (; g > 1; --g) {
+        bool ok = true;
+        for (int32_t j = 0; j < g && ok; ++j) {
+            const int32_t nu = run_begin(units, g, j + 1) - run_begin(units, g, j);
+            const int32_t nt = run_begin(tiles, g, j + 1) - run_begin(tiles, g, j);
+            ok = static_cast<int64_t>(nu) <= static_cast<int64_t>(nt) * iters;
+        }
+        if (ok) break;
+    }
+    return g;
 }
 
 // Iterator over one unit's segments in run order: its Stream-K range first (if any),

@@ -39,8 +39,9 @@ typedef enum { SK_DP = 0, SK_SPLITK = 1, SK_STREAMK = 2, SK_HYBRID = 3 } sk_mode
 typedef enum { SK_NN = 0, SK_NT = 1 } sk_layout;
 /* Reduction modes (Case 4): deterministic = the owner adds its peers' FP32
  * partials in k order (a turnstile); atomic = peers add FP32 partials into one
- * workspace tile with atomics, so rounding depends on arrival order once a tile
- * has three or more contributors (Case 3). */
+ * workspace tile with atomics. With two peers the sum 0 + a + b is the same either
+ * way round; from three contributors on, the FP32 additions happen in whatever order
+ * the peers finish, so the result's last bits can change from run to run (Case 3). */
 typedef enum { SK_DETERMINISTIC = 0, SK_ATOMIC = 1 } sk_reduction;
 typedef enum { SK_F32 = 0, SK_BF16 = 1 } sk_dtype;
 /* Segment roles in the work-unit map. FULL: one unit runs the whole K loop of a
@@ -56,17 +57,11 @@ typedef enum { SK_ROLE_FULL = 0, SK_ROLE_OWNER = 1, SK_ROLE_PRODUCER = 2, SK_ROL
  * cta_group::2, each CTA holding half of the tile's rows and half of B's columns), so a
  * persistent unit is a CTA pair and num_sms SMs give num_sms / 2 units; CUTLASS
  * example 74 on the first page uses the 256 x 128 pair tile. */
-/* SK_TILE_256x512_QUAD: two CTA pairs side by side in a cluster of four, each pair computing
- * one 256 x 256 half of the tile; the A rows they share are loaded once and multicast to both
- * pairs (half the A bytes read from L2). A unit is the cluster, so num_sms SMs give
- * num_sms / 4 units. Planned for SK_DP, SK_STREAMK and SK_HYBRID with split_partials = 0
- * only (SK_EINVAL otherwise). */
 typedef enum {
     SK_TILE_128x128 = 0,
     SK_TILE_256x128_PAIR = 1,
     SK_TILE_256x256_PAIR = 2,
-    SK_TILE_128x256 = 3,
-    SK_TILE_256x512_QUAD = 4
+    SK_TILE_128x256 = 3
 } sk_tile;
 
 typedef struct {
@@ -111,6 +106,18 @@ typedef struct {
                                Each device-side wait limit then counts from that wait.
                                The one-CTA tiles then launch without the cooperative
                                attribute, after the same residency check as the pairs. */
+    int32_t sk_groups;      /* Stream-K grouping (first page, Case 4 knob table,
+                               max_sk_groups_: units split into up to 8 groups so that
+                               partial tiles computed together stay close in L2). 0 or 1:
+                               one group, the page's simulator plan. g >= 2 (at most 64):
+                               the Stream-K region's tiles and its units are each cut into
+                               up to g consecutive groups, big-first (the first tiles % g
+                               and units % g groups one larger), and a group's units split
+                               only its own tiles by the divmod rule. Fewer groups are
+                               used when g exceeds the region's tiles or units, or when a
+                               group would hold fewer k-iterations than units; the map
+                               header reports the count used. Ignored by data-parallel
+                               and Split-K plans. */
 } sk_schedule;
 
 #define SK_OK          0
@@ -137,6 +144,7 @@ typedef struct {
  *   [10] the label's split count   [11] n_slots: FP32 partial-tile slots used
  *   [12] tile_m   [13] tile_n   [14] CTAs per tile (1 or 2)
  *   [15] raster   [16] swizzle (the tile-id order of sk_schedule)
+ *   [17] Stream-K groups used (1 with one group; 0 without a Stream-K region)
  * then n_segments rows of SK_MAP_SEG values, in (unit, run order) order:
  *   unit, order, tile, k_begin, k_end, role, slot, peer_begin, n_peers
  *   (k_begin/k_end in k-iterations; PRODUCER: slot = its partial slot; OWNER: its peers'
@@ -148,8 +156,8 @@ typedef struct {
  * then `tiles` rows of SK_MAP_TILE values: owner unit (runs k = 0), contributors, and
  * the tile's row and column in the tile grid (its output rows start at row * tile_m, its
  * columns at column * tile_n). */
-#define SK_MAP_VERSION 2
-#define SK_MAP_HEADER 17
+#define SK_MAP_VERSION 3
+#define SK_MAP_HEADER 18
 #define SK_MAP_SEG 9
 #define SK_MAP_TILE 4
 
@@ -224,6 +232,14 @@ typedef struct {
     uint64_t* trace;              /* NULL, or a device buffer of SK_TRACE_WORDS uint64 per
                                      CTA (workers * CTAs per tile): %globaltimer stamps in
                                      ns, layout below */
+    int32_t zero_partials;        /* 1: numerical control ("Consecutive-B split-K NAX GEMM",
+                                     Contract and numerical coverage: a candidate whose
+                                     partial store is zeroed must fail the checks). Every
+                                     partial a segment hands on (a Stream-K or Split-K
+                                     producer's partial, a Split-K slab, an owner's slot of
+                                     the separate fixup pass) is stored as zeros; flags and
+                                     counters are raised as usual, so nothing waits longer.
+                                     The result is then wrong wherever a tile was split. */
 } sk_debug_opts;
 
 /* Per-CTA trace record (sk_debug_opts.trace), indexed by blockIdx: [0] start (after set-up

@@ -9,7 +9,7 @@ For each PART it also fits the single free unit of the model, microseconds per
 k-iteration plus a launch constant, by least squares. This is a report, not a parity
 check: no number here feeds a test.
 
-    python -m oracle.model_vs_gpu gpurun_out/experiments.jsonl
+    python -m oracle.model_vs_gpu FILE      # FILE: the output of bench.py --experiments FILE
 """
 from __future__ import annotations
 

@@ -11,9 +11,9 @@ persistent CTA (one per SM); the fixup combines a split tile's FP32 partials.
 
 Map format produced by `plan_map` (int32 list), the contract the C library's
 sk_plan must reproduce exactly:
-  header (17): version, mode_resolved, tiles, iters, workers, sk_tiles, sk_units,
+  header (18): version, mode_resolved, tiles, iters, workers, sk_tiles, sk_units,
                n_segments, splits, label, label_splits, n_slots, tile_m, tile_n, cta_group,
-               raster, swizzle
+               raster, swizzle, sk_groups
   n_segments rows (9): unit, order, tile, k_begin, k_end, role, slot, peer_begin, n_peers
   tiles rows (4): owner_unit, n_contrib, tile row, tile column
 """
@@ -33,14 +33,11 @@ FULL, OWNER, PRODUCER, SLAB = 0, 1, 2, 3
 LABEL_NONE, LABEL_DP, LABEL_SPLITK, LABEL_STREAMK = -1, 0, 1, 2
 
 # work-tile shapes: (tile_m, tile_n, CTAs per tile). A tile of the pair shapes is computed by
-# two CTAs together, so a unit is a CTA pair and num_sms SMs give num_sms // 2 units; a tile of
-# shape 4 by four CTAs (two pairs side by side), num_sms // 4 units.
-TILE_SHAPES = {0: (128, 128, 1), 1: (256, 128, 2), 2: (256, 256, 2), 3: (128, 256, 1), 4: (256, 512, 4)}
-# Shapes planned only with the in-kernel fixup: no Split-K slabs, no separate fixup pass.
-TILES_WITHOUT_PASSES = (4,)
+# two CTAs together, so a unit is a CTA pair and num_sms SMs give num_sms // 2 units.
+TILE_SHAPES = {0: (128, 128, 1), 1: (256, 128, 2), 2: (256, 256, 2), 3: (128, 256, 1)}
 
-MAP_VERSION = 2
-HEADER_LEN = 17
+MAP_VERSION = 3
+HEADER_LEN = 18
 SEG_LEN = 9
 TILE_ROW_LEN = 4
 
@@ -163,12 +160,45 @@ class Plan:
     tiles_m: int = 0
     raster: int = 0
     swizzle: int = 0
+    sk_groups: int = 0   # groups the Stream-K region was split into (0: no Stream-K region)
 
     def segments(self):
         return [s for segs in self.units for s in segs]
 
 
-def _streamk_region(tiles_base: int, n_tiles: int, iters: int, n_units: int, separate: bool = False):
+def sk_group_count(n_tiles: int, iters: int, n_units: int, requested: int) -> int:
+    """How many groups the Stream-K region is cut into (page, Case 4 knob table:
+    `max_sk_groups_`, "Stream-K units are split into up to 8 groups, so that partial tiles
+    computed together stay close in L2"). Reading taken: `requested` is that upper bound
+    (0 or 1: one group). A group needs at least one tile and one unit, and no unit may be
+    left without an iteration, so the count is the largest g <= min(requested, n_tiles,
+    n_units) for which every group, tiles and units each divided big-first
+    (group_bounds), has at least as many k-iterations as units."""
+    g = min(max(1, requested), n_tiles, n_units)
+    while g > 1:
+        tb, ub = divmod_bounds(n_tiles, g), divmod_bounds(n_units, g)
+        if all(u1 - u0 <= (t1 - t0) * iters for (t0, t1), (u0, u1) in zip(tb, ub)):
+            return g
+        g -= 1
+    return 1
+
+
+def group_bounds(n_tiles: int, iters: int, n_units: int, groups: int):
+    """Flattened iteration range of every Stream-K unit when the region is cut into
+    `groups` groups. Reading of the knob table's one sentence: the tiles of the region are
+    divided into `groups` contiguous runs, and the units into as many consecutive groups,
+    both big-first like the units of one region (the first n % g runs one larger); group j's
+    units split only group j's run of tiles, by the divmod rule of stream_k_units (Case 2).
+    With one group this is divmod_bounds(n_tiles * iters, n_units)."""
+    out = []
+    for (t0, t1), (u0, u1) in zip(divmod_bounds(n_tiles, groups), divmod_bounds(n_units, groups)):
+        base = t0 * iters
+        out += [(base + b, base + e) for b, e in divmod_bounds((t1 - t0) * iters, u1 - u0)]
+    return out
+
+
+def _streamk_region(tiles_base: int, n_tiles: int, iters: int, n_units: int, separate: bool = False,
+                    groups: int = 1):
     """Per-unit segments of Stream-K over tiles [tiles_base, tiles_base + n_tiles).
 
     Follows the page's per-unit algorithm (Case 2 stream_k_units; Mental model): each unit
@@ -183,8 +213,11 @@ def _streamk_region(tiles_base: int, n_tiles: int, iters: int, n_units: int, sep
     every partial segment, the owner's too, stores to a fixed slot per (unit, first/last
     segment): slot 2u for the unit's first segment, 2u + 1 for a later one. A unit has at
     most two partial segments, its first and its last; a producer is always a unit's first
-    segment."""
-    bounds = divmod_bounds(n_tiles * iters, n_units)
+    segment.
+
+    `groups` (at least 1, from sk_group_count): the unit ranges of group_bounds, so that no
+    tile is shared between units of different groups."""
+    bounds = group_bounds(n_tiles, iters, n_units, groups)
     out = []
     for u, (b, e) in enumerate(bounds):
         segs = []
@@ -216,7 +249,7 @@ def _streamk_region(tiles_base: int, n_tiles: int, iters: int, n_units: int, sep
 
 def build_plan(M: int, N: int, K: int, num_sms: int, mode: int, splits: int = 1,
                units: int = 0, min_iters: int = 8, split_partials: int = 0, tile: int = 0,
-               raster: int = 0, swizzle: int = 0) -> Plan:
+               raster: int = 0, swizzle: int = 0, sk_groups: int = 0) -> Plan:
     """The integer work-unit map for one GEMM.
 
     `units` > 0 replaces num_sms as the number of persistent units (the toy case is
@@ -224,10 +257,8 @@ def build_plan(M: int, N: int, K: int, num_sms: int, mode: int, splits: int = 1,
       - DP (Mental model, Case 2 data_parallel): unit w runs tiles w, w + W, ... with
         W = min(units, tiles), each tile FULL.
       - Tile shape (`tile`, TILE_SHAPES): the pages' tile is 128 x 128 (tile 0). The
-        CTA-pair shapes make one unit of two SMs, so `units` defaults to num_sms // 2, and
-        the 256 x 512 shape one unit of four SMs (num_sms // 4); the schedule itself is the
-        same over the coarser tile grid. The four-CTA shape is planned for data-parallel,
-        Stream-K and the hybrid rule with the in-kernel fixup only.
+        CTA-pair shapes make one unit of two SMs, so `units` defaults to num_sms // 2; the
+        schedule itself is the same over the coarser tile grid.
       - Split-K (Case 2 split_k; the split-K report's "final split is clamped"): split j
         of a tile covers k-iterations [j*chunk, min((j+1)*chunk, iters)), chunk =
         ceil(iters / s); empty trailing splits are dropped (s_eff = ceil(iters / chunk)).
@@ -247,6 +278,10 @@ def build_plan(M: int, N: int, K: int, num_sms: int, mode: int, splits: int = 1,
       - Stream-K and hybrid with split_partials = 1: the Stream-K tiles are merged by a
         separate fixup pass (Case 3), so every partial segment stores to its (unit,
         first/last) slot; see _streamk_region. A hybrid that resolves to DP has no partials.
+      - sk_groups (Case 4 knob table, `max_sk_groups_`): the Stream-K region is cut into up
+        to sk_groups groups of tiles and units (sk_group_count, group_bounds); 0 or 1 keeps
+        one group, the plan of the page's simulator. Data-parallel and Split-K plans have
+        no Stream-K region and ignore it.
     """
     if min(M, N, K) < 1 or num_sms < 1 or units < 0 or min_iters < 1:
         raise ValueError("bad problem")
@@ -260,16 +295,16 @@ def build_plan(M: int, N: int, K: int, num_sms: int, mode: int, splits: int = 1,
         raise ValueError("data-parallel tiles have no partials")
     if tile not in TILE_SHAPES:
         raise ValueError("bad tile shape")
-    if tile in TILES_WITHOUT_PASSES and (mode == SPLITK or split_partials):
-        raise ValueError("this tile shape has no Split-K or separate-pass plans")
     if raster not in (0, 1) or not 0 <= swizzle <= 256:
         raise ValueError("bad rasterization")
+    if not 0 <= sk_groups <= 64:
+        raise ValueError("bad sk_groups")
     tile_m, tile_n, cg = TILE_SHAPES[tile]
     tiles_m, tiles_n, tiles, iters = problem_shape(M, N, K, tile_m, tile_n)
     S = units if units > 0 else num_sms // cg
     if S < 1:
         raise ValueError("no units")
-    p = _build(S, mode, splits, min_iters, split_partials, tiles, tiles_n, iters)
+    p = _build(S, mode, splits, min_iters, split_partials, tiles, tiles_n, iters, sk_groups)
     p.tile_m, p.tile_n, p.cta_group = tile_m, tile_n, cg
     p.tiles_m, p.raster, p.swizzle = tiles_m, raster, swizzle
     return p
@@ -291,7 +326,7 @@ def tile_coords(p: Plan, t: int):
     return (a, b) if p.raster == 0 else (b, a)
 
 
-def _build(S, mode, splits, min_iters, split_partials, tiles, tiles_n, iters) -> Plan:
+def _build(S, mode, splits, min_iters, split_partials, tiles, tiles_n, iters, sk_groups=0) -> Plan:
     if mode == HYBRID:
         label, sk_tiles, sk_units, lsp = heuristic(tiles, iters, S, min_iters)
         if label == LABEL_DP:
@@ -303,7 +338,8 @@ def _build(S, mode, splits, min_iters, split_partials, tiles, tiles_n, iters) ->
         sep = bool(split_partials)
         p = Plan(HYBRID, tiles, iters, tiles_n, W, sk_tiles, sk_units, 0, label, lsp,
                  (2 if sep else 1) * sk_units)
-        region = _streamk_region(dp_tiles, sk_tiles, iters, sk_units, sep)
+        p.sk_groups = sk_group_count(sk_tiles, iters, sk_units, sk_groups)
+        region = _streamk_region(dp_tiles, sk_tiles, iters, sk_units, sep, p.sk_groups)
         for w in range(W):
             segs = list(region[w]) if w < sk_units else []
             for t in range(w, dp_tiles, W):
@@ -318,7 +354,8 @@ def _build(S, mode, splits, min_iters, split_partials, tiles, tiles_n, iters) ->
         U = min(S, tiles * iters)
         sep = bool(split_partials)
         p = Plan(STREAMK, tiles, iters, tiles_n, U, tiles, U, 0, LABEL_NONE, 0, (2 if sep else 1) * U)
-        p.units = _streamk_region(0, tiles, iters, U, sep)
+        p.sk_groups = sk_group_count(tiles, iters, U, sk_groups)
+        p.units = _streamk_region(0, tiles, iters, U, sep, p.sk_groups)
     else:  # SPLITK
         if splits < 1 or splits > iters:
             raise ValueError("bad splits")
@@ -377,7 +414,7 @@ def plan_map(p: Plan):
     segs = p.segments()
     out = [MAP_VERSION, p.mode, p.tiles, p.iters, p.workers, p.sk_tiles, p.sk_units,
            len(segs), p.splits, p.label, p.label_splits, p.n_slots, p.tile_m, p.tile_n, p.cta_group,
-           p.raster, p.swizzle]
+           p.raster, p.swizzle, p.sk_groups]
     for s in segs:
         out += [s.unit, s.order, s.tile, s.k_begin, s.k_end, s.role, s.slot, s.peer_begin, s.n_peers]
     for t, (o, c) in enumerate(tile_rows(p)):

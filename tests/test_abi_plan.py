@@ -47,18 +47,20 @@ def test_exports_every_declared_symbol(sk):
     assert set(sk.EXPORTS) == declared
 
 
-def _cmp(sk, M, N, K, sms, mode, splits=1, units=0, min_iters=0, partials=0, tile=0, raster=0, swizzle=0):
+def _cmp(sk, M, N, K, sms, mode, splits=1, units=0, min_iters=0, partials=0, tile=0, raster=0, swizzle=0,
+         groups=0):
+    sched = sk.schedule(mode, splits, units, min_iters, partials, tile, raster, swizzle, sk_groups=groups)
     try:
         want = S.plan_map(S.build_plan(M, N, K, sms, mode, splits=splits, units=units,
                                        min_iters=min_iters or 8, split_partials=partials, tile=tile,
-                                       raster=raster, swizzle=swizzle))
+                                       raster=raster, swizzle=swizzle, sk_groups=groups))
     except ValueError:
         with pytest.raises(sk.SkError) as e:
-            sk.sk_plan(M, N, K, sms, sk.schedule(mode, splits, units, min_iters, partials, tile, raster, swizzle))
+            sk.sk_plan(M, N, K, sms, sched)
         assert e.value.code == sk.SK_EINVAL
         return None
-    got = sk.sk_plan(M, N, K, sms, sk.schedule(mode, splits, units, min_iters, partials, tile, raster, swizzle))
-    assert got.tolist() == want, (M, N, K, sms, mode, splits, units, partials, tile, raster, swizzle)
+    got = sk.sk_plan(M, N, K, sms, sched)
+    assert got.tolist() == want, (M, N, K, sms, mode, splits, units, partials, tile, raster, swizzle, groups)
     return got
 
 
@@ -83,13 +85,12 @@ def test_plan_matches_oracle_on_workloads(sk):
             _cmp(sk, M, 512, 2048, 148, S.SPLITK, splits=s)
     _cmp(sk, 2048, 2432, 4096, 148, S.SPLITK, splits=2)
     for m in range(128, 4097, 128):
-        for tile in (0, 1, 2, 3, 4):
+        for tile in (0, 1, 2, 3):
             for mode in (S.DP, S.STREAMK, S.HYBRID):
                 _cmp(sk, m, m, 4096, 148, mode, tile=tile)
-            if tile != 4:
-                for s in (2, 4):
-                    _cmp(sk, m, m, 4096, 148, S.SPLITK, splits=s, tile=tile)
-    for tile in (1, 2, 3, 4):
+            for s in (2, 4):
+                _cmp(sk, m, m, 4096, 148, S.SPLITK, splits=s, tile=tile)
+    for tile in (1, 2, 3):
         for M, N, K, sms, mode in cases:
             _cmp(sk, M, N, K, sms, mode, tile=tile)
 
@@ -122,6 +123,28 @@ def test_overlap_is_a_launch_option(sk):
                     assert sk.sk_workspace_size(M, N, K, 148, a, red) == sk.sk_workspace_size(M, N, K, 148, b, red)
 
 
+def test_plan_streamk_groups(sk):
+    # max_sk_groups_ grouping (first page, Case 4 knob table): the C planner's map equals
+    # the oracle's for every group count on the workloads and a brute-force grid, with and
+    # without the separate fixup pass.
+    for M, N, K in [(128, 640, 256), (2048, 2432, 4096), (512, 512, 65536), (96, 512, 2048), (256, 512, 2048),
+                    (1536, 1536, 4096), (3840, 3840, 4096), (8192, 8192, 8192)]:
+        for tile in (0, 1, 2, 3):
+            for g in (0, 1, 2, 3, 4, 8, 16, 64):
+                for mode in (S.STREAMK, S.HYBRID):
+                    _cmp(sk, M, N, K, 148, mode, tile=tile, groups=g)
+                    _cmp(sk, M, N, K, 148, mode, tile=tile, groups=g, partials=1)
+    for M, N, K in itertools.product((128, 300, 640), (128, 256, 640), (64, 200, 512)):
+        for sms in (1, 2, 3, 5, 8, 13, 20):
+            for g in (2, 3, 8):
+                for mode in (S.STREAMK, S.HYBRID):
+                    _cmp(sk, M, N, K, sms, mode, groups=g)
+                    _cmp(sk, M, N, K, sms, mode, groups=g, tile=2)
+    for bad in (-1, 65):
+        with pytest.raises(sk.SkError):
+            sk.sk_plan(128, 128, 64, 4, sk.schedule(2, sk_groups=bad))
+
+
 def test_plan_toy_units_override(sk):
     a = _cmp(sk, 128, 640, 256, 148, S.STREAMK, units=4)
     b = _cmp(sk, 128, 640, 256, 4, S.STREAMK)
@@ -132,11 +155,9 @@ def test_plan_bruteforce_small(sk):
     # M, N <= 640, K <= 512, 1..20 SMs, every mode.
     for M, N, K in itertools.product((1, 128, 129, 300, 640), (8, 128, 256, 640), (8, 64, 65, 200, 512)):
         for sms in range(1, 21):
-            for tile in (0, 1, 2, 3, 4):
+            for tile in (0, 1, 2, 3):
                 for mode in (S.DP, S.STREAMK, S.HYBRID):
                     _cmp(sk, M, N, K, sms, mode, tile=tile)
-                if tile == 4:  # in-kernel fixup only
-                    continue
                 for mode in (S.STREAMK, S.HYBRID):
                     _cmp(sk, M, N, K, sms, mode, partials=1, tile=tile)
                 iters = S.cdiv(K, 64)
@@ -157,9 +178,7 @@ def test_workspace_size(sk):
              (96, 512, 2048, 148, S.SPLITK, 8, 1), (96, 512, 2048, 148, S.SPLITK, 8, 2),
             (2048, 2432, 4096, 148, S.SPLITK, 2, 0), (2048, 2432, 4096, 148, S.HYBRID, 1, 1),
             (512, 512, 65536, 148, S.STREAMK, 1, 1),
-             (2048, 2432, 4096, 148, S.DP, 1, 0)], (0, 1, 2, 3, 4)):
-        if tile == 4 and (mode == S.SPLITK or part):
-            continue
+             (2048, 2432, 4096, 148, S.DP, 1, 0)], (0, 1, 2, 3)):
         sch = sk.schedule(mode, s, 0, 0, part, tile)
         m = sk.sk_plan(M, N, K, sms, sch)
         n_slots, splits = int(m[11]), int(m[8])
@@ -184,10 +203,7 @@ def test_errors(sk):
         (128, 128, 128, 4, sk.schedule(sk.SK_SPLITK, 2, 0, 0, 3)),   # unknown slab reduction
         (128, 128, 128, 4, sk.schedule(sk.SK_DP, 1, -1)),
         (128, 128, 128, 1, sk.schedule(sk.SK_DP, 1, 0, 0, 0, 1)),      # a pair needs 2 SMs
-        (128, 128, 128, 3, sk.schedule(sk.SK_DP, 1, 0, 0, 0, 4)),      # four CTAs need 4 SMs
-        (128, 128, 128, 8, sk.schedule(sk.SK_SPLITK, 2, 0, 0, 0, 4)),  # no Split-K on the four-CTA tile
-        (128, 128, 512, 8, sk.schedule(sk.SK_STREAMK, 1, 0, 0, 1, 4)),  # nor the separate pass
-        (128, 128, 128, 4, sk.schedule(sk.SK_DP, 1, 0, 0, 0, 5)),      # unknown tile shape
+        (128, 128, 128, 4, sk.schedule(sk.SK_DP, 1, 0, 0, 0, 4)),      # unknown tile shape
         (128, 128, 128, 4, sk.schedule(sk.SK_DP, overlap=2)),          # overlap is 0 or 1
         (128, 128, 128, 4, sk.schedule(sk.SK_DP, overlap=-1)),
     ]

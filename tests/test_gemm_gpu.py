@@ -305,8 +305,9 @@ def test_rasterized_waveq_and_large(sk, dev, raster, swizzle):
 # --------------------------------------------------------------------------- atomics
 @pytest.mark.parametrize("tile", [0, 1, 2])
 def test_atomic_many_contributors(sk, dev, tile):
-    # Skinny shape, up to 11 contributors per tile: within tolerance (bits may vary with
-    # arrival order once a tile has three or more contributors).
+    # Skinny shape, up to 11 contributors per tile: within tolerance. With three or more
+    # contributors the FP32 additions follow the peers' finishing order, so the last bits
+    # may differ from run to run (first page, Case 3).
     w = synth.SKINNY
     got, ws = _run(sk, dev, w, sk.schedule(2, tile=tile), ATOM, 148)
     U.assert_close(got, U.reference(w), "atomic")
@@ -442,7 +443,7 @@ def test_case3_interpreter_claims(sk, dev):
 
 
 # --------------------------------------------------------------------------- trace record
-@pytest.mark.parametrize("tile,nsms", [(0, 148), (2, 148), (4, 144)])
+@pytest.mark.parametrize("tile,nsms", [(0, 148), (2, 148), (1, 148), (3, 148)])
 def test_trace_record(sk, dev, tile, nsms):
     # The per-CTA trace (sk_debug_opts.trace) of the hybrid rule on the wave-quantized GEMM,
     # checked against the plan map: every CTA walks its unit's segments; start <= end; for
@@ -475,3 +476,75 @@ def test_trace_record(sk, dev, tile, nsms):
             assert T[c, 0] <= acc <= done <= T[c, 1] + 10_000, (c, s)
             if rank_in_pair == 0:  # the MMA stamps come from the leader of each MMA pair
                 assert T[c, 0] <= issue <= commit <= acc + 10_000, (c, s)
+
+
+# --------------------------------------------------------------------------- numerical control
+CONTROL_CASES = [
+    # (id, workload, schedule, reduction, units)
+    ("toy_streamk", synth.TOY, dict(mode=2, units=4), DET, 4),
+    ("toy_streamk_atomic", synth.TOY, dict(mode=2, units=4), ATOM, 4),
+    ("waveq_hybrid_pair", synth.WAVEQ, dict(mode=3, tile=2), DET, 148),
+    ("waveq_hybrid_sep", synth.WAVEQ, dict(mode=3, tile=2, split_partials=1), DET, 148),
+    ("skinny_streamk", synth.SKINNY, dict(mode=2, tile=0), DET, 148),
+    ("smallm96_slabs8", synth.SMALLM_96, dict(mode=1, splits=8, split_partials=1), DET, 148),
+    ("smallm256_slabs4_last", synth.SMALLM_256, dict(mode=1, splits=4, split_partials=2), DET, 148),
+]
+
+
+@pytest.mark.parametrize("name,w,kw,red,sms", CONTROL_CASES, ids=[c[0] for c in CONTROL_CASES])
+def test_zeroed_partials_fail_the_checks(sk, dev, name, w, kw, red, sms):
+    # Numerical control ("Consecutive-B split-K NAX GEMM", Contract and numerical coverage):
+    # with every partial store zeroed on the GPU (flags still raised), the same parity check
+    # that passes on the real result must fail. Sampled rows keep the full-size cases quick.
+    sched = sk.schedule(**kw)
+    A_bits, B_bits = U.inputs(w)
+    rows = U.sample_rows(w.M, 24, seed=7)
+    ref = og.ref_rows(A_bits, B_bits, w.layout, rows)
+    good, _ = _run(sk, dev, w, sched, red, sms)
+    U.assert_close(good[rows], ref, name)
+    bad, _ = _run(sk, dev, w, sched, red, sms, zero_partials=1)
+    with pytest.raises(AssertionError):
+        U.assert_close(bad[rows], ref, name + " (zeroed partials)")
+    # Only the handed-on partials changed: tiles no unit split are still right.
+    m = sk.sk_plan(w.M, w.N, w.K, sms, sched)
+    tiles = int(m[2])
+    trows = m[len(m) - sk.SK_MAP_TILE * tiles:].reshape(tiles, sk.SK_MAP_TILE)
+    tm, tn = int(m[12]), int(m[13])
+    for t in range(tiles):
+        if int(trows[t, 1]) == 1 and not kw.get("split_partials"):
+            r, c = int(trows[t, 2]) * tm, int(trows[t, 3]) * tn
+            assert np.array_equal(bad[r:r + tm, c:c + tn], good[r:r + tm, c:c + tn])
+
+
+# --------------------------------------------------------------------------- Stream-K groups
+GROUP_CASES = [
+    # (id, workload, schedule, units)
+    ("toy_g2", synth.TOY, dict(mode=2, units=4, sk_groups=2), 4),
+    ("toy_g2_sep", synth.TOY, dict(mode=2, units=4, sk_groups=2, split_partials=1), 4),
+    ("skinny_g8", synth.SKINNY, dict(mode=2, sk_groups=8), 148),
+    ("skinny_pair_g4_sep", synth.SKINNY, dict(mode=2, tile=2, sk_groups=4, split_partials=1), 148),
+    ("waveq_hybrid_g8", synth.WAVEQ, dict(mode=3, sk_groups=8), 148),
+    ("waveq_hybrid_pair_g8", synth.WAVEQ, dict(mode=3, tile=2, sk_groups=8), 148),
+    ("large_streamk_pair_g8", synth.LARGE, dict(mode=2, tile=2, sk_groups=8), 148),
+]
+
+
+@pytest.mark.parametrize("red", [DET, ATOM])
+@pytest.mark.parametrize("name,w,kw,sms", GROUP_CASES, ids=[c[0] for c in GROUP_CASES])
+def test_streamk_groups(sk, dev, name, w, kw, sms, red):
+    # max_sk_groups_ grouping (first page, Case 4 knob table): the grouped plan (planner ==
+    # oracle on the host) runs to the oracle's result; deterministic runs are bit-identical
+    # under reversed unit order, and the map uses more than one group.
+    sched = sk.schedule(**kw)
+    plan = sk.sk_plan(w.M, w.N, w.K, sms, sched)
+    assert int(plan[17]) >= 2
+    got, _ = _run(sk, dev, w, sched, red, sms)
+    A_bits, B_bits = U.inputs(w)
+    if w.M * w.N <= 2048 * 2432:
+        U.assert_close(got, U.reference(w), name)
+    else:
+        rows = U.sample_rows(w.M, 16, seed=3)
+        U.assert_close(got[rows], og.ref_rows(A_bits, B_bits, w.layout, rows), name)
+    if red == DET:
+        rev, _ = _run(sk, dev, w, sched, DET, sms, reverse_units=1)
+        assert np.array_equal(got, rev)

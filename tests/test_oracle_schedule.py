@@ -76,6 +76,61 @@ def test_toy_case(golden_dir):
     assert S.plan_map(sk2) == S.plan_map(sk)
 
 
+def test_streamk_groups_toy(golden_dir):
+    # Hand-worked map of the toy case cut into two groups (fixture comment has the steps).
+    p = S.build_plan(128, 640, 256, 4, S.STREAMK, sk_groups=2)
+    assert p.sk_groups == 2
+    expect = _rows(os.path.join(golden_dir, "toy_streamk_groups2_map.csv"))
+    roles = {"FULL": S.FULL, "OWNER": S.OWNER, "PRODUCER": S.PRODUCER}
+    got = [(s.unit, s.tile, s.k_begin, s.k_end, s.role) for s in p.segments()]
+    assert got == [(int(u), int(t), int(a), int(b), roles[r]) for u, t, a, b, r in expect]
+    own = [s for s in p.segments() if s.role == S.OWNER][0]
+    assert (own.peer_begin, own.n_peers) == (1, 1)
+    # One group (0 or 1) is the page's plan.
+    for g in (0, 1):
+        assert S.plan_map(S.build_plan(128, 640, 256, 4, S.STREAMK, sk_groups=g))[S.HEADER_LEN:] == \
+            S.plan_map(S.build_plan(128, 640, 256, 4, S.STREAMK))[S.HEADER_LEN:]
+
+
+def test_streamk_group_count():
+    # "Up to" the requested count: never more groups than tiles or units, and never a group
+    # with more units than k-iterations (no empty unit).
+    assert S.sk_group_count(5, 4, 4, 8) == 4          # min(8, 5 tiles, 4 units)
+    assert S.sk_group_count(16, 1024, 148, 8) == 8
+    assert S.sk_group_count(2, 64, 128, 8) == 2         # 64 units on 64 iterations each
+    assert S.sk_group_count(2, 64, 129, 8) == 1         # 65 units on a 64-iteration tile: one group
+    # 3 tiles x 2 iterations on 6 units: 2 groups would give tiles 2, 1 and units 3, 3, and
+    # group 1 would hold 2 iterations for 3 units; so one group.
+    assert S.sk_group_count(3, 2, 6, 2) == 1
+    assert S.sk_group_count(10, 4, 7, 0) == 1 and S.sk_group_count(10, 4, 7, 1) == 1
+
+
+def test_streamk_groups_bruteforce():
+    # Every grouping: (tile, k) covered exactly once, each unit's range inside one group's
+    # tiles, no empty unit, units of a group within one iteration of each other, tiles of
+    # different groups never shared, owner = lowest contributor.
+    for tiles, iters, units, req in itertools.product(range(1, 13), (1, 2, 3, 4, 8), range(1, 15), (2, 3, 4, 8)):
+        if units > tiles * iters:
+            continue
+        g = S.sk_group_count(tiles, iters, units, req)
+        b = S.group_bounds(tiles, iters, units, g)
+        assert b[0][0] == 0 and b[-1][1] == tiles * iters
+        assert all(b[i][1] == b[i + 1][0] for i in range(units - 1))
+        assert all(e > s for s, e in b)
+        tg, ug = S.divmod_bounds(tiles, g), S.divmod_bounds(units, g)
+        for (t0, t1), (u0, u1) in zip(tg, ug):
+            sizes = [b[u][1] - b[u][0] for u in range(u0, u1)]
+            assert max(sizes) - min(sizes) <= 1
+            assert b[u0][0] == t0 * iters and b[u1 - 1][1] == t1 * iters
+        segs = [x for segs in S._streamk_region(0, tiles, iters, units, False, g) for x in segs]
+        cover = sorted((x.tile, k) for x in segs for k in range(x.k_begin, x.k_end))
+        assert cover == [(t, k) for t in range(tiles) for k in range(iters)]
+        for x in segs:
+            if x.role == S.OWNER:
+                assert all(y.unit > x.unit for y in segs if y.tile == x.tile and y is not x)
+                assert x.n_peers == sum(1 for y in segs if y.tile == x.tile) - 1
+
+
 def test_triton_partition(golden_dir):
     for units, tiles, ipt, total, q, peers in _rows(os.path.join(golden_dir, "triton_partition.csv")):
         units, ipt, total = int(units), int(ipt), int(total)
@@ -88,6 +143,42 @@ def test_triton_partition(golden_dir):
                 lo, hi = t * ipt, (t + 1) * ipt
                 most = max(most, sum(1 for (x, y) in b if x < hi and y > lo))
             assert most == int(peers)
+
+
+def test_docc_floor_partition_worked_example():
+    # docc StreamK rewrite: block b walks iterations [b*TOTAL/NBLOCKS, (b+1)*TOTAL/NBLOCKS)
+    # with integer (floor) division. Worked by hand for TOTAL = 20, NBLOCKS = 6:
+    # 0, 20/6 = 3, 40/6 = 6, 60/6 = 10, 80/6 = 13, 100/6 = 16, 120/6 = 20.
+    assert S.floor_bounds(20, 6) == [(0, 3), (3, 6), (6, 10), (10, 13), (13, 16), (16, 20)]
+    # TOTAL = 7, NBLOCKS = 3: 0, 7/3 = 2, 14/3 = 4, 21/3 = 7.
+    assert S.floor_bounds(7, 3) == [(0, 2), (2, 4), (4, 7)]
+    # More blocks than iterations leaves some blocks empty: floor(b*2/5) = 0, 0, 0, 1, 1, 2.
+    assert S.floor_bounds(2, 5) == [(0, 0), (0, 0), (0, 1), (1, 1), (1, 2)]
+
+
+def test_docc_floor_partition_aligned_split():
+    # docc, aligned split: with NBLOCKS = tiles * S and S dividing the panel count P, block
+    # bid owns panels [s*P/S, (s+1)*P/S) of tile t = bid / S (s = bid % S). In the flattened
+    # (tile, panel) space that is [t*P + s*P/S, t*P + (s+1)*P/S).
+    for tiles in (1, 2, 5, 16):
+        for P in (4, 8, 12, 64):
+            for Sd in (1, 2, 4):
+                if P % Sd:
+                    continue
+                got = S.floor_bounds(tiles * P, tiles * Sd)
+                want = [(bid // Sd * P + bid % Sd * P // Sd, bid // Sd * P + (bid % Sd + 1) * P // Sd)
+                        for bid in range(tiles * Sd)]
+                assert got == want
+
+
+def test_docc_floor_partition_invariants():
+    # The ranges tile [0, TOTAL) in order, and every size is floor or ceil of TOTAL / NBLOCKS.
+    for total in range(0, 60):
+        for n in range(1, 25):
+            b = S.floor_bounds(total, n)
+            assert b[0][0] == 0 and b[-1][1] == total
+            assert all(b[i][1] == b[i + 1][0] for i in range(n - 1))
+            assert {y - x for x, y in b} <= {total // n, -(-total // n)}
 
 
 def test_heuristic_decisions():
@@ -258,7 +349,7 @@ def test_hybrid_waveq_on_148():
 def test_map_layout():
     p = S.build_plan(128, 640, 256, 4, S.STREAMK)
     m = S.plan_map(p)
-    assert m[:S.HEADER_LEN] == [2, S.STREAMK, 5, 4, 4, 5, 4, 8, 0, -1, 0, 4, 128, 128, 1, 0, 0]
+    assert m[:S.HEADER_LEN] == [3, S.STREAMK, 5, 4, 4, 5, 4, 8, 0, -1, 0, 4, 128, 128, 1, 0, 0, 1]
     assert len(m) == S.HEADER_LEN + 8 * S.SEG_LEN + 5 * S.TILE_ROW_LEN
     # The toy's five tiles in one tile row, t at column t (the page's tile order).
     assert m[-5 * S.TILE_ROW_LEN:] == [0, 1, 0, 0, 0, 2, 0, 1, 1, 2, 0, 2, 2, 2, 0, 3, 3, 1, 0, 4]
@@ -326,10 +417,32 @@ def test_split_k_separate_makespan_bruteforce(tiles, iters, sms, s, EPI, PART):
 
 
 def test_rule_stops_best_scan():
+    # Where the scan says the rule first stops being best after being best, check it by hand
+    # from the page's rule and closed-form makespan bounds (EPI = PART = 2, 128 x 128 tiles,
+    # 64 k-iterations, 132 SMs), not from the scan itself:
+    #   m = 768: 6 * 32 = 192 tiles, tail 60, 2 * 60 < 132 -> the rule takes Stream-K;
+    #   m = 896: 7 * 32 = 224 tiles, tail 92, 2 * 92 >= 132 -> the rule stays data-parallel,
+    #            whose makespan is 2 waves * (64 + EPI) = 132;
+    #   Stream-K at m = 896 puts 224 * 64 = 14336 iterations on 132 units, q = 108 (+1 for
+    #   the first 80). A unit runs at most 109 iterations, holds at most one owner segment
+    #   (EPI, plus PART per peer: a 109-iteration range meets at most 3 tiles of 64, so at
+    #   most 2 peers) and at most one producer segment (PART), so it ends by
+    #   109 + 2 + 2 * 2 + 2 = 117 < 132.
+    tiles_896 = (896 // 128) * (4096 // 128)
+    tail = tiles_896 - (tiles_896 // 132) * 132
+    assert (tiles_896, tail) == (224, 92) and 2 * tail >= 132
+    assert S.heuristic(tiles_896, 64, 132)[0] == S.LABEL_DP
+    assert S.makespan(S.build_plan(896, 4096, 4096, 132, S.DP), 2, 2) == 2 * (64 + 2)
+    assert S.makespan(S.build_plan(896, 4096, 4096, 132, S.STREAMK), 2, 2) <= 109 + 2 + 2 * 2 + 2
+    assert S.heuristic(192, 64, 132)[0] == S.LABEL_STREAMK
     first, misses = S.rule_stops_best(range(128, 2049, 128), 4096, 4096, 132, 2, 2)
-    assert misses[:3] == [128, 256, 384] and first == 896
+    # The scan's own contract: every miss is a shape where the rule's makespan exceeds the
+    # best of the four, and `first` is the first miss that follows a hit.
     for m in misses:
         assert not S.schedule_choice(m, 4096, 4096, 132, 2, 2)["rule_is_best"]
+    hits = [m for m in range(128, 2049, 128) if m not in misses]
+    assert first == min(m for m in misses if m - 128 in hits)
+    assert first == 896
 
 
 def test_model_vs_gpu_report_fits_synthetic_timings(tmp_path, capsys):

@@ -36,10 +36,16 @@ def test_noalloc_matches_sk_gemm_twice():
     dev = torch.device("cuda:0")
     stream = torch.cuda.current_stream(dev)
     cases = [
-        # (workload, schedule, reduction, units): wave-quantized hybrid on 148 SMs, then the
-        # toy Stream-K case with atomic reduction on 4 units.
+        # (workload, schedule, reduction, units): wave-quantized hybrid on 148 SMs; the toy
+        # Stream-K case with atomic reduction on 4 units; small-M Split-K slabs summed by the
+        # reduction pass (split_partials 1) and inside the launch (2); Stream-K merged by the
+        # separate fixup pass (split_partials 1), whose workspace has the slot layout.
         (synth.WAVEQ, sk.schedule(sk.SK_HYBRID), sk.SK_DETERMINISTIC, 148),
         (synth.TOY, sk.schedule(sk.SK_STREAMK, units=4), sk.SK_ATOMIC, 4),
+        (synth.SMALLM_96, sk.schedule(sk.SK_SPLITK, splits=8, split_partials=1), sk.SK_DETERMINISTIC, 148),
+        (synth.SMALLM_96, sk.schedule(sk.SK_SPLITK, splits=4, split_partials=2), sk.SK_DETERMINISTIC, 148),
+        (synth.TOY, sk.schedule(sk.SK_STREAMK, units=4, split_partials=1), sk.SK_DETERMINISTIC, 4),
+        (synth.SMALLM_256, sk.schedule(sk.SK_STREAMK, units=40, split_partials=1), sk.SK_DETERMINISTIC, 148),
     ]
     for call, (w, sched, red, sms) in enumerate(cases * 2):
         A_bits, B_bits = U.inputs(w)
