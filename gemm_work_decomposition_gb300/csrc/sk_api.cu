@@ -63,7 +63,25 @@ void set_streamk(Sched& o, int64_t base, int64_t sk_tiles, int64_t units, bool s
     o.n_slots = static_cast<int32_t>((sep ? 2 : 1) * units);
 }
 
+int32_t make_sched_core(int32_t M, int32_t N, int32_t K, int32_t num_sms, const sk_schedule& s, Sched& o);
+
+// The schedule plus the walk's fast divisors (sk_schedule.h FastDiv).
 int32_t make_sched(int32_t M, int32_t N, int32_t K, int32_t num_sms, const sk_schedule& s, Sched& o) {
+    const int32_t e = make_sched_core(M, N, K, num_sms, s, o);
+    if (e != SK_OK) return e;
+    const int32_t w = o.swizzle > 1 ? o.swizzle : 1;
+    const int32_t along = o.raster == 0 ? o.tiles_n : o.tiles_m;
+    if (static_cast<int64_t>(w) * along > INT32_MAX) return SK_EINVAL;
+    o.fd_iters = make_fastdiv(static_cast<uint32_t>(o.iters));
+    o.fd_q1 = make_fastdiv(static_cast<uint32_t>(o.sk_q) + 1u);
+    o.fd_q = make_fastdiv(static_cast<uint32_t>(o.sk_q > 0 ? o.sk_q : 1));
+    o.fd_splits = make_fastdiv(static_cast<uint32_t>(o.splits > 0 ? o.splits : 1));
+    o.fd_strip = make_fastdiv(static_cast<uint32_t>(w * along));
+    o.fd_w = make_fastdiv(static_cast<uint32_t>(w));
+    return SK_OK;
+}
+
+int32_t make_sched_core(int32_t M, int32_t N, int32_t K, int32_t num_sms, const sk_schedule& s, Sched& o) {
     if (M < 1 || N < 1 || K < 1 || num_sms < 1 || s.units < 0 || s.min_iters < 0) return SK_EINVAL;
     if (s.mode < SK_DP || s.mode > SK_HYBRID) return SK_EINVAL;
     // split_partials: Split-K slabs (1 pass, 2 last arriver), or for Stream-K and the hybrid
@@ -210,10 +228,51 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
+// Encoded tensor maps of this host thread's recent calls, keyed by every argument of the
+// encoding, so that calls on the same buffers (the usual case: a GEMM called again and again
+// on the same operands) skip the driver's encoder. A map is plain host data; a hit returns a
+// copy of the bytes the encoder wrote for exactly these arguments.
+struct TmapKey {
+    const void* ptr;
+    uint64_t v[4];
+    uint32_t kind;
+};
+struct TmapEntry {
+    TmapKey key;
+    CUtensorMap map;
+    bool used;
+};
+constexpr int kTmapCache = 32;
+thread_local TmapEntry t_tmaps[kTmapCache];
+thread_local int t_tmap_next = 0;
+
+bool same_key(const TmapKey& a, const TmapKey& b) {
+    return a.ptr == b.ptr && a.kind == b.kind && a.v[0] == b.v[0] && a.v[1] == b.v[1] && a.v[2] == b.v[2] &&
+           a.v[3] == b.v[3];
+}
+bool tmap_lookup(const TmapKey& k, CUtensorMap* m) {
+    for (int i = 0; i < kTmapCache; ++i) {
+        if (t_tmaps[i].used && same_key(t_tmaps[i].key, k)) {
+            *m = t_tmaps[i].map;
+            return true;
+        }
+    }
+    return false;
+}
+void tmap_store(const TmapKey& k, const CUtensorMap& m) {
+    TmapEntry& e = t_tmaps[t_tmap_next];
+    t_tmap_next = (t_tmap_next + 1) % kTmapCache;
+    e.key = k;
+    e.map = m;
+    e.used = true;
+}
+
 // Row-major BF16 matrix of `outer` rows x `inner` columns, copied in boxes of
 // box_outer x box_inner with the 128-byte swizzle; out-of-range elements read as zero.
 bool encode_2d(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_inner,
                uint32_t box_outer) {
+    const TmapKey key{ptr, {inner, outer, box_inner, box_outer}, 1u};
+    if (tmap_lookup(key, m)) return true;
     PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[2] = {inner, outer};
@@ -223,13 +282,17 @@ bool encode_2d(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, 
     CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
+    if (r != CUDA_SUCCESS) return false;
+    tmap_store(key, *m);
+    return true;
 }
 
 // Output map: rows of `inner` elements of `esize` bytes, `outer` rows per slab and `slabs`
 // slabs, stored in boxes of 32 rows x 128 bytes (one box per epilogue warp and store) with
 // the 128-byte swizzle the epilogue's staging uses.
 bool encode_out(CUtensorMap* m, void* ptr, bool bf16, uint64_t inner, uint64_t outer, uint64_t slabs, uint32_t rank) {
+    const TmapKey key{ptr, {inner, outer, slabs, (static_cast<uint64_t>(rank) << 1) | (bf16 ? 1u : 0u)}, 2u};
+    if (tmap_lookup(key, m)) return true;
     PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
     if (!fn) return false;
     const uint64_t esize = bf16 ? 2 : 4;
@@ -240,7 +303,9 @@ bool encode_out(CUtensorMap* m, void* ptr, bool bf16, uint64_t inner, uint64_t o
     CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, rank,
                     ptr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
+    if (r != CUDA_SUCCESS) return false;
+    tmap_store(key, *m);
+    return true;
 }
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }

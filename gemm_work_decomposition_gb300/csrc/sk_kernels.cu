@@ -68,6 +68,7 @@ constexpr int kPrefetchClosed = 1;
 constexpr int kPrefetchIssued = 2;
 
 
+
 __device__ __forceinline__ void record_timeout(const KArgs& a, volatile int* abort_flag) {
     *abort_flag = 1;
     atomicCAS(a.status, 0, kErrTimeout);
@@ -101,7 +102,8 @@ __device__ __forceinline__ int32_t seg_k(const Seg& g, bool rev, int32_t i) {
 // The MMA issuer commits each stage's empty barrier after that stage's MMAs, and a commit
 // arrives only once every MMA issued before it has completed, so the last load's stage
 // turning empty means every stage has been read: one wait, not one per stage (each wait
-// costs about 0.13 us even on a phase long complete).
+// costs about 0.13 us even on a phase long complete). Issuing each copy as soon as the
+// stages under its own buffer were free for good was measured too: no faster.
 template <int kCG, int kBN>
 __device__ bool prefetch_partials(const KArgs& a, const Smem<Shape<kCG, kBN>>& sm, const Seg& g, const CtaPos& pos,
                                   uint32_t issued, uint64_t deadline, volatile int* abort_flag, int* prefetch) {
@@ -164,19 +166,17 @@ __device__ void prefetch_first_loads(const KArgs& a, const CUtensorMap* tmA, con
 
 template <bool kNT, int kCG, int kBN>
 __device__ void run_producer(const KArgs& a, const CUtensorMap* tmA, const CUtensorMap* tmB,
-                             const Smem<Shape<kCG, kBN>>& sm, int unit, const CtaPos& pos, uint64_t deadline,
-                             volatile int* abort_flag, int* prefetch) {
+                             const Smem<Shape<kCG, kBN>>& sm, Walk w, Seg g, bool have, const CtaPos& pos,
+                             uint64_t deadline, volatile int* abort_flag, int* prefetch) {
     using S = Shape<kCG, kBN>;
     const uint32_t rank = pos.rank;
-    Walk w;
-    w.init(a.sch, unit);
-    Seg g, last;
+    Seg last;
     int nseg = 0;
     int stage = 0;
     uint32_t phase = 0;
     uint32_t issued = 0;
     bool ok = true;
-    while (ok && w.next(a.sch, g)) {
+    for (; ok && have; have = w.next(a.sch, g)) {
         last = g;
         ++nseg;
         // This CTA's rows of the tile and its half of the tile's columns of B.
@@ -241,8 +241,8 @@ __device__ void run_producer(const KArgs& a, const CUtensorMap* tmA, const CUten
 // The leader of each pair issues its pair's MMAs. Its commits reach both CTAs of the pair
 // (cluster ranks 0 and 1) through a cluster-multicast mbarrier arrive.
 template <bool kNT, int kCG, int kBN>
-__device__ void run_mma(const KArgs& a, const Smem<Shape<kCG, kBN>>& sm, uint32_t tmem_base, int unit,
-                        uint64_t deadline, volatile int* abort_flag) {
+__device__ void run_mma(const KArgs& a, const Smem<Shape<kCG, kBN>>& sm, uint32_t tmem_base, Walk w, Seg g,
+                        bool have, uint64_t deadline, volatile int* abort_flag) {
     using S = Shape<kCG, kBN>;
     constexpr uint16_t pair_mask = 0x3u;
     constexpr uint32_t kIdesc = idesc_bf16_f32(kCtaRows * kCG, kBN, kNT ? 0u : 1u);
@@ -250,9 +250,6 @@ __device__ void run_mma(const KArgs& a, const Smem<Shape<kCG, kBN>>& sm, uint32_
     // along the swizzled row; the MN-major B of NN moves 16 rows of 128 bytes.
     constexpr uint32_t kAStep = (16 * 2) >> 4;
     constexpr uint32_t kBStep = kNT ? ((16 * 2) >> 4) : ((16 * 128) >> 4);
-    Walk w;
-    w.init(a.sch, unit);
-    Seg g;
     int stage = 0;
     uint32_t phase = 0;
     int buf = 0;
@@ -262,7 +259,7 @@ __device__ void run_mma(const KArgs& a, const Smem<Shape<kCG, kBN>>& sm, uint32_
     int seg = 0;
     // A pair's MMA writes both CTAs' TMEM: wait until the peer has allocated its part.
     if (kCG == 2 && !mbar_wait<true>(sm.tready(), 0u, abort_flag, deadline)) ok = false;
-    while (ok && w.next(a.sch, g)) {
+    for (; ok && have; have = w.next(a.sch, g)) {
         if (!mbar_wait<kCG == 2>(sm.tempty(buf), (buf ? uses1 : uses0) ^ 1u, abort_flag, deadline)) {
             ok = false;
             break;
@@ -443,30 +440,6 @@ __device__ __forceinline__ void store_box(const CUtensorMap* tmC, uint32_t stagi
             tma_store_2d(tmC, buf, x, y0);
         else
             tma_store_3d(tmC, buf, x, y0, slab);
-        bulk_commit_group();
-    }
-    ++nstore;
-}
-
-// One 4 KiB chunk of this warp's block of a partial slot (32 columns: float4 q of lane l at
-// byte (32 q + l) * 16, the slot's own order, so the chunk is one contiguous copy) through
-// staging buffer nstore % nbuf, stored by a TMA bulk copy to dst. The lanes' shared stores
-// are 512 contiguous bytes per q, conflict-free.
-template <class F>
-__device__ __forceinline__ void store_partial_chunk(float* dst, uint32_t staging, uint32_t nbuf, uint32_t& nstore,
-                                                    F&& value) {
-    const int lane = threadIdx.x & 31;
-    const uint32_t buf = staging_buffer(staging, nbuf, nstore);
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-        const float4 x = value(q);
-        st_shared_v4(buf + static_cast<uint32_t>((q * 32 + lane) * 16), __float_as_uint(x.x), __float_as_uint(x.y),
-                     __float_as_uint(x.z), __float_as_uint(x.w));
-    }
-    fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) {
-        bulk_store_s2g(dst, buf, 4096u);
         bulk_commit_group();
     }
     ++nstore;
@@ -906,10 +879,13 @@ struct Epi {
                             red_add_v4_f32(blk + slot_f4(kChunks * p + c, q, lane), v[i], v[i + 1], v[i + 2], v[i + 3]);
                         }
                     } else {
-                        store_partial_chunk(blk + slot_f4(kChunks * p + c, 0, 0), staging, nbuf, nstore, [&](int q) {
+                        // Straight from registers: each warp store covers 512 contiguous bytes of
+                        // the slot, so no staging buffer (and no wait for one) is needed.
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) {
                             const int i = c * 32 + q * 4;
-                            return make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
-                        });
+                            st_cg_f4(blk + slot_f4(kChunks * p + c, q, lane), make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]));
+                        }
                     }
                 }
             } else if (g.role == kSlab) {
@@ -972,15 +948,11 @@ struct Epi {
                 if (gt == 0) a.counters[g.tile * a.sch.cg + cta] = 0;
             }
         } else if (g.role == kProducer && !a.sch.sep) {
-            // Every epilogue thread's share is stored: publish it. Each warp's bulk copies
-            // must have written the slot (async proxy) before the barrier, which orders all of
-            // them before one thread's release at GPU scope (release is cumulative). With the
-            // separate fixup pass nobody waits: the pass runs after this launch.
-            if (!a.atomic && lane == 0) {
-                bulk_wait_group_all();
-                fence_proxy_async_global();
-            }
-            __syncwarp();
+            // Every epilogue thread's share is stored (st.global from registers, or red.add in
+            // atomic mode): publish it. The group's barrier orders every thread's stores before
+            // one thread's release at GPU scope (release is cumulative), so an owner that
+            // acquires the flag sees the whole partial. With the separate fixup pass nobody
+            // waits: the pass runs after this launch.
             named_bar_sync(kBar, kGroupThreads);
             if (gt == 0 && !a.skip_signal) {
                 if (a.atomic)
@@ -1161,8 +1133,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     // that launch may begin when all of this grid's CTAs are.
     uint32_t tmem_base = 0;
     uint64_t start_clk = 0;  // thread 0, traced launches: SM clock at the start stamp
+    // The producer and the MMA issuer take their unit's first segment from the walk before the
+    // wait for the previous kernel: the walk reads only the kernel's arguments, and its first
+    // step (cold instruction and constant caches, integer divisions) costs about a microsecond.
+    Walk walk;
+    Seg first{};
+    bool have_first = false;
     if (warp == 0) {
-        if (args.sch.overlap && lane == 0) prefetch_first_loads<kNT, kCG, kBN>(args, &tmA, &tmB, unit, pos);
+        if (lane == 0) {
+            if (args.sch.overlap) prefetch_first_loads<kNT, kCG, kBN>(args, &tmA, &tmB, unit, pos);
+            walk.init(args.sch, unit);
+            have_first = walk.next(args.sch, first);
+        }
         grid_dep_wait();
         grid_dep_launch();
         const uint64_t deadline = globaltimer() + args.timeout_ns;  // wait limits count from here
@@ -1171,7 +1153,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 args.trace[static_cast<int64_t>(blockIdx.x) * kTraceWords] = globaltimer();
                 start_clk = clock64();
             }
-            run_producer<kNT, kCG, kBN>(args, &tmA, &tmB, sm, unit, pos, deadline, abort_flag, prefetch);
+            run_producer<kNT, kCG, kBN>(args, &tmA, &tmB, sm, walk, first, have_first, pos, deadline, abort_flag,
+                                        prefetch);
         }
         // Warps 0 and 1 reconverge before the exit barrier: a CTA barrier counts a warp once
         // any of its threads arrives, so all 32 lanes must arrive together.
@@ -1194,11 +1177,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         tc_fence_after();
         tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_holder);
+        if (lane == 0 && rank == 0) {
+            walk.init(args.sch, unit);
+            have_first = walk.next(args.sch, first);
+        }
         grid_dep_wait();
         grid_dep_launch();
         const uint64_t deadline = globaltimer() + args.timeout_ns;
         if (lane == 0 && rank == 0)
-            run_mma<kNT, kCG, kBN>(args, sm, tmem_base, unit, deadline, abort_flag);
+            run_mma<kNT, kCG, kBN>(args, sm, tmem_base, walk, first, have_first, deadline, abort_flag);
         __syncwarp();
     } else {
         named_bar_sync(2, 32 + kEpiThreads);

@@ -17,6 +17,21 @@
 
 namespace sk {
 
+// Division by a divisor fixed for the launch, as a multiply-high, an add and a shift (the
+// "round-up" method of Hacker's Delight, chapter 10): with s = ceil(log2 d) and
+// m = floor(2^32 (2^s - d) / d) + 1, n / d = (mulhi(n, m) + n) >> s for every 32-bit n. A
+// hardware-less integer division costs tens of dependent instructions; the schedule walk
+// divides by the same few numbers again and again, one thread at a time.
+struct FastDiv {
+    uint32_t d, m, s;
+};
+inline FastDiv make_fastdiv(uint32_t d) {
+    FastDiv f{d > 0 ? d : 1u, 0u, 0u};
+    while ((1ull << f.s) < f.d) ++f.s;
+    f.m = static_cast<uint32_t>(((1ull << 32) * ((1ull << f.s) - f.d)) / f.d + 1);
+    return f;
+}
+
 enum Mode : int32_t { kDP = 0, kSplitK = 1, kStreamK = 2, kHybrid = 3 };
 enum Role : int32_t { kFull = 0, kOwner = 1, kProducer = 2, kSlab = 3 };
 enum Label : int32_t { kLabelNone = -1, kLabelDP = 0, kLabelSplitK = 1, kLabelStreamK = 2 };
@@ -54,6 +69,9 @@ struct Sched {
     // Launch option, not part of the plan: overlap each launch with the kernel before it on
     // the stream (programmatic dependent launch).
     int32_t overlap;
+    // The walk's divisors: iters, sk_q + 1, sk_q (at least 1 wherever it is used), splits, and
+    // for the tile order the strip size swizzle * (tiles along the walk) and the swizzle.
+    FastDiv fd_iters, fd_q1, fd_q, fd_splits, fd_strip, fd_w;
 };
 
 // (tile_m, tile_n, CTAs per tile) of each sk_tile value; false for an unknown value.
@@ -82,6 +100,16 @@ struct Seg {
 };
 
 SK_HD int32_t cdiv(int32_t a, int32_t b) { return (a + b - 1) / b; }
+// n / f.d for 0 <= n < 2^31.
+SK_HD int32_t fdiv(const FastDiv& f, int32_t n) {
+    const uint32_t u = static_cast<uint32_t>(n);
+#if defined(__CUDA_ARCH__)
+    const uint32_t hi = __umulhi(u, f.m);
+#else
+    const uint32_t hi = static_cast<uint32_t>((static_cast<uint64_t>(u) * f.m) >> 32);
+#endif
+    return static_cast<int32_t>((static_cast<uint64_t>(hi) + u) >> f.s);
+}
 SK_HD int32_t imin(int32_t a, int32_t b) { return a < b ? a : b; }
 SK_HD int32_t imax(int32_t a, int32_t b) { return a > b ? a : b; }
 
@@ -94,11 +122,12 @@ SK_HD void tile_coords(const Sched& s, int32_t t, int32_t* row, int32_t* col) {
     const int32_t across = s.raster == 0 ? s.tiles_m : s.tiles_n;
     const int32_t along = s.raster == 0 ? s.tiles_n : s.tiles_m;
     const int32_t w = s.swizzle > 1 ? s.swizzle : 1;
-    const int32_t strip = t / (w * along);
+    const int32_t strip = fdiv(s.fd_strip, t);
     const int32_t i = t - strip * w * along;
     const int32_t h = imin(w, across - strip * w);
-    const int32_t a = strip * w + i % h;
-    const int32_t b = i / h;
+    const int32_t q = h == w ? fdiv(s.fd_w, i) : i / h;  // a full strip, or the last one
+    const int32_t a = strip * w + (i - q * h);
+    const int32_t b = q;
     *row = s.raster == 0 ? a : b;
     *col = s.raster == 0 ? b : a;
 }
@@ -129,10 +158,10 @@ SK_HD int32_t sk_unit_begin(const Sched& s, int32_t u) {
 SK_HD int32_t sk_unit_of(const Sched& s, int32_t i) {
     if (s.sk_groups <= 1) {
         const int32_t edge = s.sk_big * (s.sk_q + 1);
-        return i < edge ? i / (s.sk_q + 1) : s.sk_big + (i - edge) / s.sk_q;
+        return i < edge ? fdiv(s.fd_q1, i) : s.sk_big + fdiv(s.fd_q, i - edge);
     }
     const int32_t g = s.sk_groups;
-    const int32_t j = run_of(s.sk_tiles, g, i / s.iters);
+    const int32_t j = run_of(s.sk_tiles, g, fdiv(s.fd_iters, i));
     const int32_t u0 = run_begin(s.sk_units, g, j), nu = run_begin(s.sk_units, g, j + 1) - u0;
     const int32_t t0 = run_begin(s.sk_tiles, g, j), nt = run_begin(s.sk_tiles, g, j + 1) - t0;
     return u0 + run_of(nt * s.iters, nu, i - t0 * s.iters);
@@ -184,7 +213,7 @@ struct Walk {
             if (it < end) {
                 // One segment: the rest of the current tile inside this unit's range.
                 const bool first = it == sk_unit_begin(s, unit);
-                const int32_t local = it / s.iters;
+                const int32_t local = fdiv(s.fd_iters, it);
                 const int32_t tb = local * s.iters;
                 const int32_t te = tb + s.iters;
                 const int32_t se = imin(end, te);
@@ -224,8 +253,8 @@ struct Walk {
                 if (s.mode == kSplitK) {
                     // Work items queued tile by tile with the owner (split 0) last, so a
                     // unit never waits on an item queued behind it.
-                    const int32_t t = it / s.splits;
-                    const int32_t j = s.splits - 1 - it % s.splits;
+                    const int32_t t = fdiv(s.fd_splits, it);
+                    const int32_t j = s.splits - 1 - (it - t * s.splits);
                     g.tile = t;
                     g.k_begin = j * s.chunk;
                     g.k_end = imin(g.k_begin + s.chunk, s.iters);
