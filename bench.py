@@ -15,8 +15,10 @@ before each instead (also reported, as `isolated_launch`).
 
 Prints ONE JSON line (rank 0). `--impl reference` times the CPU oracle (FP64 dot products
 over the BF16 inputs) on a bounded row sample of the same workload instead.
-Multi-GPU (torchrun): every rank runs its own independent instance (weak scaling); a
-barrier brackets the timed region and the slowest rank's time is reported.
+Multi-GPU (torchrun): the job is one GEMM of N * 2048 rows split by rows over the N ranks
+(m_shard), B replicated, no collective on the data path (weak scaling: each rank's share is
+the headline shape); a barrier brackets the timed region and the slowest rank's time is
+reported.
 """
 from __future__ import annotations
 
@@ -129,10 +131,19 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(mhz)}
 
 
-def rank_workload(w, rank: int):
-    """Each rank's independent instance: the same shape with its own input seed."""
+def m_shard(M: int, world: int, rank: int):
+    """Rows of C (and of A) that rank `rank` computes when a GEMM's M is split over `world`
+    devices with B replicated: (first row, row count), divmod split with the first M % world
+    ranks one row longer. The shards tile [0, M) in rank order; no data is exchanged."""
+    q, big = divmod(M, world)
+    return rank * q + min(rank, big), q + (1 if rank < big else 0)
+
+
+def sharded_workload(w, world: int):
+    """The job on `world` devices: one GEMM of world * M rows (the workload's seed and value
+    recipe, rows added), each device computing its M-row shard against the whole B."""
     import dataclasses
-    return dataclasses.replace(w, seed=w.seed + 1000 * rank)
+    return dataclasses.replace(w, name=f"{w.name}_msplit{world}", M=w.M * world)
 
 
 def max_over_ranks(x: float, dist, device) -> float:
@@ -604,9 +615,13 @@ def main():
     lay = sk.SK_NN if w.layout == "NN" else sk.SK_NT
     flops = 2.0 * w.M * w.N * w.K
 
-    # Inputs: seeded per rank (independent instances), copied once into HBM.
-    wr = rank_workload(w, rank)
-    A_bits, B_bits = synth.make_inputs(wr)
+    # Inputs, copied once into HBM. On several devices the job is one GEMM with world * M rows,
+    # split by rows (B replicated, output tiles independent, so no collective): this rank
+    # generates its row block of A and the whole B.
+    wg = sharded_workload(w, world) if world > 1 else w
+    r0, rows = m_shard(wg.M, world, rank)
+    assert rows == w.M
+    A_bits, B_bits = synth.make_row_block(wg, r0, r0 + rows)
     A_host = torch.from_numpy(A_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
     B_host = torch.from_numpy(B_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
     A = A_host.to(dev)
@@ -685,14 +700,18 @@ def main():
     # summed in a second launch.
     launches_per_step = 2 if args.partials == 1 else 1
 
-    # ---- the timed region: K steps, barrier + synchronize on both sides
-    for i in range(args.warmup):
-        launch_set(i, sch, ws, nb, sms)
+    # ---- the timed region: K steps, barrier + synchronize on both sides. The clock sampler
+    # starts first (starting nvidia-smi takes a while), so the warm-up steps run right before
+    # the region and the GPU does not sit idle between them.
     clocks = ClockSampler(f"GPU-{props.uuid}")
     clocks.start()
     if world > 1:
         dist.barrier()
+    for i in range(args.warmup):
+        launch_set(i, sch, ws, nb, sms)
     torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
     wall0 = time.perf_counter()
     if args.timing == "stream":
         # One event pair around K launches back to back; step i uses input set i mod n_sets.
@@ -978,6 +997,8 @@ def main():
                    "tiles": int(plan[2]), "iters": int(plan[3]), "workers": int(plan[4]),
                    "resolved_mode": int(plan[1]), "sk_tiles": int(plan[5]), "sk_units": int(plan[6]),
                    "overlap": args.overlap, "timing": args.timing,
+                   "parallelism": (f"M-split over {world} GPUs: one {wg.M} x {w.N} x {w.K} GEMM, {rows} rows of A and C "
+                                   f"per GPU, B replicated, no collective" if world > 1 else "one GPU"),
                    "l2": (f"inputs larger than L2: {n_sets} rotating sets of A, B and C ({n_sets * set_bytes / 1e6:.0f} MB, "
                           f">= 4x the {l2_bytes / 1e6:.0f} MB L2), launched back to back"
                           if args.timing == "stream" else "flushed between timed steps (256 MiB write)"),

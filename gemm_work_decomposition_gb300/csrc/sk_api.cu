@@ -242,7 +242,7 @@ struct TmapEntry {
     CUtensorMap map;
     bool used;
 };
-constexpr int kTmapCache = 32;
+constexpr int kTmapCache = 128;
 thread_local TmapEntry t_tmaps[kTmapCache];
 thread_local int t_tmap_next = 0;
 

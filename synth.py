@@ -79,6 +79,29 @@ def normal(key: int, n: int) -> np.ndarray:
     return out
 
 
+def normal_range(key: int, start: int, n: int) -> np.ndarray:
+    """Values start .. start+n-1 of the stream `normal(key, .)` (start even), without drawing
+    the ones before: pair p still uses stream values 2p and 2p+1."""
+    if start % 2:
+        raise ValueError("start must be even")
+    out = np.empty(n, dtype=np.float64)
+    pairs = (n + 1) // 2
+    p_base = start // 2
+    for p0 in range(0, pairs, _CHUNK):
+        p1 = min(pairs, p0 + _CHUNK)
+        x = splitmix64(key, 2 * (p_base + p0), 2 * (p1 - p0)) >> np.uint64(11)
+        u1 = (x[0::2].astype(np.float64) + 1.0) * (2.0 ** -53)
+        u2 = x[1::2].astype(np.float64) * (2.0 ** -53)
+        r = np.sqrt(-2.0 * np.log(u1))
+        z = np.empty(2 * (p1 - p0), dtype=np.float64)
+        z[0::2] = r * np.cos(2.0 * math.pi * u2)
+        z[1::2] = r * np.sin(2.0 * math.pi * u2)
+        lo = 2 * p0
+        hi = min(n, 2 * p1)
+        out[lo:hi] = z[: hi - lo]
+    return out
+
+
 def uniform(key: int, n: int, lo: float, hi: float) -> np.ndarray:
     out = np.empty(n, dtype=np.float64)
     for s in range(0, n, _CHUNK):
@@ -133,6 +156,43 @@ def make_inputs(w: Workload):
     if w.scale_last_row != 1.0 and M > 1:
         a[M - 1, :] *= w.scale_last_row
     b = draw(1, K * N)
+    b = b.reshape(K, N) if w.layout == "NN" else b.reshape(N, K)
+    return bf16_bits(a), bf16_bits(b)
+
+
+def make_row_block(w: Workload, r0: int, r1: int):
+    """Rows r0 .. r1-1 of make_inputs(w)'s A, and the whole B: the inputs of one shard of a GEMM
+    whose rows are split over several devices. Bit-identical to slicing make_inputs(w)[0]."""
+    M, N, K = w.M, w.N, w.K
+    if not 0 <= r0 <= r1 <= M:
+        raise ValueError("bad row block")
+    key = stream_key(w.seed, 0)
+    if w.dist == "uniform":
+        a = np.empty((r1 - r0) * K, dtype=np.float64)
+        for s in range(0, a.size, _CHUNK):
+            e = min(a.size, s + _CHUNK)
+            a[s:e] = -1.0 + 2.0 * uniform01(key, r0 * K + s, e - s)
+    else:
+        if (r0 * K) % 2:
+            a = normal(key, r1 * K)[r0 * K:]
+        else:
+            a = normal_range(key, r0 * K, (r1 - r0) * K)
+        if w.dist == "normal_sqrtk":
+            a *= 1.0 / math.sqrt(K)
+        elif w.dist != "normal":
+            raise ValueError(f"unknown distribution {w.dist}")
+    a = a.reshape(r1 - r0, K)
+    if w.zero_first_row and r0 == 0 and r1 > 0:
+        a[0, :] = 0.0
+    if w.scale_last_row != 1.0 and M > 1 and r0 <= M - 1 < r1:
+        a[M - 1 - r0, :] *= w.scale_last_row
+    kb = stream_key(w.seed, 1)
+    if w.dist == "uniform":
+        b = uniform(kb, K * N, -1.0, 1.0)
+    else:
+        b = normal(kb, K * N)
+        if w.dist == "normal_sqrtk":
+            b *= 1.0 / math.sqrt(K)
     b = b.reshape(K, N) if w.layout == "NN" else b.reshape(N, K)
     return bf16_bits(a), bf16_bits(b)
 
