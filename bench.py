@@ -60,6 +60,20 @@ TRAFFIC = {
 }
 
 
+def graph_upload(graph, stream):
+    """Upload an instantiated CUDA graph to the device (cuGraphUpload), so that its first replay
+    does not pay for it. Best effort: without the handle or the driver entry point the first
+    replay uploads the graph itself."""
+    try:
+        import ctypes
+        h = graph.raw_cuda_graph_exec()
+        cu = ctypes.CDLL("libcuda.so.1")
+        cu.cuGraphUpload.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
+        return cu.cuGraphUpload(ctypes.c_void_p(int(h)), ctypes.c_void_p(int(stream.cuda_stream))) == 0
+    except Exception:
+        return False
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -574,8 +588,10 @@ def main():
     ap.add_argument("--sk-groups", type=int, default=0, help="Stream-K groups of the timed schedule (0: one group)")
     ap.add_argument("--overlap", type=int, default=1, choices=[0, 1],
                     help="launch each step overlapped with the one before it (programmatic dependent launch)")
-    ap.add_argument("--timing", default="stream", choices=["stream", "flush"],
-                    help="stream: steps back to back over rotating input sets of at least 4x the L2; "
+    ap.add_argument("--timing", default="graph", choices=["graph", "stream", "flush"],
+                    help="graph: the K steps' calls captured as one CUDA graph (outside the timed region) "
+                         "and replayed once, back to back over rotating input sets of at least 4x the L2; "
+                         "stream: the same K calls launched one by one; "
                          "flush: one event pair per step with a 256 MiB L2 flush before each")
     ap.add_argument("--no-extras", action="store_true", help="skip the schedule table, e2e and CPU baseline")
     ap.add_argument("--ref-seconds", type=float, default=10.0)
@@ -700,6 +716,22 @@ def main():
     # summed in a second launch.
     launches_per_step = 2 if args.partials == 1 else 1
 
+    # ---- the K steps as one CUDA graph (--timing graph): the same K public-API calls, captured
+    # on a side stream and uploaded to the device before the timed region, then replayed once
+    # inside it. The graph keeps each launch's programmatic dependency on the one before it.
+    graph = None
+    if args.timing == "graph":
+        cap = torch.cuda.Stream(dev)
+        cap_h = cap.cuda_stream
+        graph = torch.cuda.CUDAGraph()
+        torch.cuda.synchronize(dev)
+        with torch.cuda.graph(graph, stream=cap):
+            for i in range(args.steps):
+                a_, b_, c_ = set_ptrs[i % n_sets]
+                sk.sk_gemm(a_, b_, c_, out_code, w.M, w.N, w.K, lay, sch, red, sms, ws.data_ptr(), nb, cap_h)
+        graph_upload(graph, stream)
+        torch.cuda.synchronize(dev)
+
     # ---- the timed region: K steps, barrier + synchronize on both sides. The clock sampler
     # starts first (starting nvidia-smi takes a while), so the warm-up steps run right before
     # the region and the GPU does not sit idle between them.
@@ -713,12 +745,15 @@ def main():
     if world > 1:
         dist.barrier()
     wall0 = time.perf_counter()
-    if args.timing == "stream":
+    if args.timing in ("stream", "graph"):
         # One event pair around K launches back to back; step i uses input set i mod n_sets.
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))]
         ev[0][0].record(stream)
-        for i in range(args.steps):
-            launch_set(i, sch, ws, nb, sms)
+        if graph is not None:
+            graph.replay()
+        else:
+            for i in range(args.steps):
+                launch_set(i, sch, ws, nb, sms)
         enqueue_s = time.perf_counter() - wall0
         ev[0][1].record(stream)
     else:
@@ -738,7 +773,7 @@ def main():
     if status != sk.SK_OK:
         raise RuntimeError(f"device status {sk.sk_strerror(status)}")
     step_ms = np.array([s.elapsed_time(e) for s, e in ev])
-    if red == sk.SK_DETERMINISTIC and args.timing == "stream":  # every set's C is the same, bit for bit
+    if red == sk.SK_DETERMINISTIC and args.timing != "flush":  # every set's C is the same, bit for bit
         for _, _, c_ in sets[1:min(n_sets, max(args.warmup, args.steps))]:
             assert torch.equal(c_, C)
     total_ms = max_over_ranks(float(step_ms.sum()), dist if world > 1 else None, dev)
@@ -747,6 +782,21 @@ def main():
     kernel_tflops = flops / (ms_per_step / 1e3) / 1e12
 
     extras = {}
+    if args.timing == "graph" and rank == 0:
+        # ---- the same K steps launched one call at a time (no graph), timed the same way
+        for i in range(args.warmup):
+            launch_set(i, sch, ws, nb, sms)
+        torch.cuda.synchronize(dev)
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        for i in range(args.steps):
+            launch_set(i, sch, ws, nb, sms)
+        s1.record(stream)
+        torch.cuda.synchronize(dev)
+        sms_ = s0.elapsed_time(s1) / args.steps
+        extras["stream_launches"] = {"ms_per_step": sms_, "tflops": flops / (sms_ / 1e3) / 1e12,
+                                     "frac_of_measured_peak": flops / (sms_ / 1e3) / 1e12 / peak_tf,
+                                     "how": "the timed region's K steps launched one sk_gemm call at a time"}
     if not args.no_extras and rank == 0:
         # ---- per-schedule table (the metric is per schedule)
         table = {}
@@ -1001,7 +1051,11 @@ def main():
                                    f"per GPU, B replicated, no collective" if world > 1 else "one GPU"),
                    "l2": (f"inputs larger than L2: {n_sets} rotating sets of A, B and C ({n_sets * set_bytes / 1e6:.0f} MB, "
                           f">= 4x the {l2_bytes / 1e6:.0f} MB L2), launched back to back"
-                          if args.timing == "stream" else "flushed between timed steps (256 MiB write)"),
+                          if args.timing != "flush" else "flushed between timed steps (256 MiB write)"),
+                   "launch": ({"graph": "the K steps' sk_gemm calls captured as one CUDA graph before the timed region "
+                                        "(uploaded there) and replayed once inside it",
+                               "stream": "K sk_gemm calls launched one by one inside the timed region",
+                               "flush": "one sk_gemm call per event pair"}[args.timing]),
                    "accumulate": "fp32"},
         "roofline": {"bound": "tensor", "achieved": kernel_tflops, "peak": peak_tf, "unit": "TFLOP/s",
                      "frac": kernel_tflops / peak_tf, "traffic": traffic,
