@@ -1199,8 +1199,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     tc_fence_before();
+    // No remote shared-memory operation is outstanding here: the accumulator-empty arrives
+    // stop two segments before the end, and every load and commit into the other CTA has
+    // been waited on. So the exit barrier needs no release ordering.
     if (kCG == 2)
-        cluster_sync();
+        cluster_sync_relaxed();
     else
         __syncthreads();
     if (args.trace && threadIdx.x == 0) {

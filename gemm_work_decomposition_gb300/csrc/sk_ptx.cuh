@@ -293,6 +293,13 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
 }
+// The same barrier without memory ordering: every thread of both CTAs arrives, then waits.
+// For the exit, where nothing written before it is read by the other CTA afterwards (the MMAs
+// into both CTAs' tensor memory have completed, as the accumulator waits showed); the release
+// form waited for this thread's earlier memory operations, which cost about 0.4 us per GEMM.
+__device__ __forceinline__ void cluster_sync_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed;\n\tbarrier.cluster.wait;" ::: "memory");
+}
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
