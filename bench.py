@@ -747,7 +747,11 @@ def main():
     wall0 = time.perf_counter()
     if args.timing in ("stream", "graph"):
         # One event pair around K launches back to back; step i uses input set i mod n_sets.
+        # The L2 flush queued ahead of the start event keeps the device busy while the host
+        # enqueues the event and the K steps, so the start stamp is not taken on an idle
+        # device before the first step has even been submitted.
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))]
+        flush.zero_()
         ev[0][0].record(stream)
         if graph is not None:
             graph.replay()
@@ -788,6 +792,7 @@ def main():
             launch_set(i, sch, ws, nb, sms)
         torch.cuda.synchronize(dev)
         s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        flush.zero_()
         s0.record(stream)
         for i in range(args.steps):
             launch_set(i, sch, ws, nb, sms)
@@ -1053,8 +1058,10 @@ def main():
                           f">= 4x the {l2_bytes / 1e6:.0f} MB L2), launched back to back"
                           if args.timing != "flush" else "flushed between timed steps (256 MiB write)"),
                    "launch": ({"graph": "the K steps' sk_gemm calls captured as one CUDA graph before the timed region "
-                                        "(uploaded there) and replayed once inside it",
-                               "stream": "K sk_gemm calls launched one by one inside the timed region",
+                                        "(uploaded there) and replayed once inside it; a 256 MiB L2 flush queued "
+                                        "before the start event covers the host's enqueue",
+                               "stream": "K sk_gemm calls launched one by one inside the timed region, behind a "
+                                         "256 MiB L2 flush queued before the start event",
                                "flush": "one sk_gemm call per event pair"}[args.timing]),
                    "accumulate": "fp32"},
         "roofline": {"bound": "tensor", "achieved": kernel_tflops, "peak": peak_tf, "unit": "TFLOP/s",

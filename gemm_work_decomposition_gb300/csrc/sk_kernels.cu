@@ -610,12 +610,30 @@ struct Epi {
         }
     }
 
+    // One 4-column group of C (row gr, columns gc .. gc + 3) from its FP32 sum.
+    __device__ __forceinline__ void store_c4(int32_t gr, int32_t gc, const float4& acc) const {
+        const int64_t off = static_cast<int64_t>(gr) * a.N + gc;
+        if (a.c_bf16) {
+            __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+            __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+            uint2 pk;
+            pk.x = *reinterpret_cast<uint32_t*>(&lo);
+            pk.y = *reinterpret_cast<uint32_t*>(&hi);
+            *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.C) + off) = pk;
+        } else {
+            *reinterpret_cast<float4*>(static_cast<float*>(a.C) + off) = acc;
+        }
+    }
+
     // Split-K slabs, shared sum: split g.slot's share of this CTA's 128 rows of tile g.tile,
     // rows [j * R, (j + 1) * R) with R = ceil(128 / splits), summed over the slabs in split
-    // order (the reduction pass's order) and stored to C. Work items are (row, 4 columns),
-    // consecutive threads on consecutive columns of a row (512 contiguous bytes per warp
-    // load); an item's loads from all slabs go out together, 8 at a time.
-    __device__ __forceinline__ void reduce_slab_share(const Seg& g) {
+    // order (the reduction pass's order) and stored to C. The MAC loop is over (this is the
+    // CTA's only work item), so the ring is idle: each epilogue warp takes every fourth row of
+    // the share and brings that row's kBN columns from every slab into its quarter of the
+    // ring with one bulk copy per (row, slab), all in flight at once, then sums them from
+    // shared memory. A sum through registers would be bound by load latency (a thread can
+    // keep only a few loads outstanding here). Returns false if a copy did not land in time.
+    __device__ __forceinline__ bool reduce_slab_share(const Seg& g) {
         int32_t trow, tcolumn;
         tile_coords(a.sch, g.tile, &trow, &tcolumn);
         const int32_t rows_per = (kCtaRows + a.sch.splits - 1) / a.sch.splits;
@@ -624,6 +642,69 @@ struct Epi {
         const int32_t m0 = trow * (kCtaRows * kCG) + r * kCtaRows;
         const int32_t n0 = tcolumn * a.sch.tile_n;
         const int64_t slab = static_cast<int64_t>(a.M) * a.N;
+        constexpr uint32_t kRowBytes = kBN * 4u;
+        // Columns of the tile inside C: N % 8 == 0, so a row's copy is a multiple of 32 bytes,
+        // and every source address (row * N + n0 floats) is 32-byte aligned.
+        const int32_t cols = imin(kBN, a.N - n0);
+        const int32_t rows_round = static_cast<int32_t>(kWarpRingBytes / (static_cast<uint32_t>(a.sch.splits) * kRowBytes));
+        if (rows_round < 1) {
+            reduce_slab_share_regs(m0, n0, r_begin, r_end, slab);
+            return true;
+        }
+        const int wq = ew & 3;
+        const uint32_t bar = pbar;  // this warp's first partial-load barrier
+#pragma unroll 1
+        for (int32_t r0 = r_begin + wq; r0 < r_end; r0 += 4 * rows_round) {
+            const int32_t nr = imin(rows_round, (r_end - r0 + 3) / 4);  // rows r0, r0 + 4, ...
+            if (lane == 0) {
+                uint32_t bytes = 0;
+                for (int32_t k = 0; k < nr; ++k)
+                    if (m0 + r0 + 4 * k < a.M) bytes += static_cast<uint32_t>(a.sch.splits * cols) * 4u;
+                fence_proxy_async_smem();  // this warp's earlier reads of the buffer come first
+                mbar_arrive_expect_tx(bar, bytes);
+                for (int32_t k = 0; k < nr; ++k) {
+                    const int32_t gr = m0 + r0 + 4 * k;
+                    if (gr >= a.M) continue;
+                    const float* src = a.slabs + static_cast<int64_t>(gr) * a.N + n0;
+                    for (int32_t j = 0; j < a.sch.splits; ++j)
+                        bulk_load_g2s(ring + static_cast<uint32_t>(k * a.sch.splits + j) * kRowBytes, src + j * slab,
+                                      static_cast<uint32_t>(cols) * 4u, bar);
+                }
+            }
+            const uint32_t parity = pph & 1u;
+            pph ^= 1u;
+            if (!mbar_wait(bar, parity, abort_flag, deadline)) {
+                (void)mbar_wait_until(bar, parity, globaltimer() + kDrainNs);  // let the copies land
+                return false;
+            }
+            for (int32_t k = 0; k < nr; ++k) {
+                const int32_t gr = m0 + r0 + 4 * k;
+                if (gr >= a.M) continue;
+                const uint32_t rowbuf = ring + static_cast<uint32_t>(k * a.sch.splits) * kRowBytes;
+#pragma unroll 1
+                for (int32_t c4 = lane; 4 * c4 < cols; c4 += 32) {
+                    float4 acc = ld_shared_f4(rowbuf + 16u * c4);
+#pragma unroll 4
+                    for (int32_t j = 1; j < a.sch.splits; ++j) {
+                        const float4 x = ld_shared_f4(rowbuf + static_cast<uint32_t>(j) * kRowBytes + 16u * c4);
+                        acc.x += x.x;
+                        acc.y += x.y;
+                        acc.z += x.z;
+                        acc.w += x.w;
+                    }
+                    store_c4(gr, n0 + 4 * c4, acc);
+                }
+            }
+            __syncwarp();
+        }
+        return true;
+    }
+
+    // The shared sum through registers, for splits whose rows do not fit a ring quarter: work
+    // items are (row, 4 columns), consecutive threads on consecutive columns of a row (512
+    // contiguous bytes per warp load); an item's loads from all slabs go out 8 at a time.
+    __device__ __forceinline__ void reduce_slab_share_regs(int32_t m0, int32_t n0, int32_t r_begin, int32_t r_end,
+                                                           int64_t slab) {
         constexpr int kGroups = kBN / 4;  // 4-column groups per row
         constexpr int kBatch = 8;
         const int32_t items = (r_end > r_begin ? r_end - r_begin : 0) * kGroups;
@@ -653,17 +734,7 @@ struct Epi {
                     }
                 }
             }
-            const int64_t off = static_cast<int64_t>(gr) * a.N + gc;
-            if (a.c_bf16) {
-                __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
-                __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
-                uint2 pk;
-                pk.x = *reinterpret_cast<uint32_t*>(&lo);
-                pk.y = *reinterpret_cast<uint32_t*>(&hi);
-                *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.C) + off) = pk;
-            } else {
-                *reinterpret_cast<float4*>(static_cast<float*>(a.C) + off) = acc;
-            }
+            store_c4(gr, gc, acc);
         }
     }
 
@@ -933,8 +1004,11 @@ struct Epi {
                     record_timeout(a, abort_flag);
                     return false;
                 }
-                reduce_slab_share(g);
-                named_bar_sync(kBar, kGroupThreads);
+                fence_proxy_async_global();  // the peers' slabs, acquired above, are read by bulk copies
+                if (named_bar_or(kBar, kGroupThreads, !reduce_slab_share(g))) {
+                    record_timeout(a, abort_flag);
+                    return false;
+                }
                 if (gt == 0 && atom_add_acq_rel_gpu(cnt, 1) == static_cast<uint32_t>(2 * a.sch.splits - 1))
                     atomicExch(cnt, 0);
                 return true;

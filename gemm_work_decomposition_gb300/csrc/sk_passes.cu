@@ -12,21 +12,44 @@
 namespace sk {
 namespace {
 
+// Both passes are bound by how many loads are in flight: each thread keeps up to 16 float4
+// loads outstanding, within 128 registers, so four blocks of kPassThreads fit on an SM and a
+// grid of up to four blocks per SM runs in one wave (every load goes out in the first round
+// trip for the shapes whose partials fit in that). One block also fits beside a resident GEMM
+// CTA (255 registers x 192 threads), so part of an overlapped pass is resident early.
+constexpr int kPassThreads = 128;
+constexpr int kPassBlocksPerSm = 4;
+
 // --------------------------------------------------------------------------- Split-K slab reduction
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(kPassThreads, kPassBlocksPerSm)
     sk_reduce_kernel(const float* __restrict__ P, void* __restrict__ C, int c_bf16, int splits, int64_t n4) {
     grid_dep_wait();  // an overlapped launch reads P only once the GEMM that wrote it is done
     grid_dep_launch();
     const float4* P4 = reinterpret_cast<const float4*>(P);
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    // An element's loads from kBatch slabs go out together (one round trip to L2 per batch
+    // instead of one per slab); the adds stay a left fold in split order.
+    constexpr int kBatch = 16;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4; i += stride) {
-        float4 acc = __ldcs(P4 + i);
-        for (int j = 1; j < splits; ++j) {
-            const float4 x = __ldcs(P4 + static_cast<int64_t>(j) * n4 + i);
-            acc.x += x.x;
-            acc.y += x.y;
-            acc.z += x.z;
-            acc.w += x.w;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int j0 = 0; j0 < splits; j0 += kBatch) {
+            float4 x[kBatch];
+            const float4* q = P4 + static_cast<int64_t>(j0) * n4 + i;
+#pragma unroll
+            for (int jj = 0; jj < kBatch; ++jj, q += n4)
+                if (j0 + jj < splits) x[jj] = __ldcs(q);
+#pragma unroll
+            for (int jj = 0; jj < kBatch; ++jj) {
+                if (j0 + jj >= splits) break;
+                if (j0 + jj == 0) {
+                    acc = x[jj];
+                } else {
+                    acc.x += x[jj].x;
+                    acc.y += x[jj].y;
+                    acc.z += x[jj].z;
+                    acc.w += x[jj].w;
+                }
+            }
         }
         if (c_bf16) {
             __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
@@ -51,7 +74,7 @@ __global__ void __launch_bounds__(256)
 // lane l takes row 32 * quad + l of the CTA's 128 rows and columns 32c + 8h .. + 7, which
 // in the slot layout are the float4s (8c + 2h) * 32 + l and that + 32 (512 contiguous bytes
 // per warp access).
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(kPassThreads, kPassBlocksPerSm)
     sk_fixup_kernel(const Sched sch, const float* __restrict__ slots, void* __restrict__ C, int32_t M, int32_t N,
                     int c_bf16) {
     grid_dep_wait();  // as in sk_reduce_kernel
@@ -127,12 +150,12 @@ __global__ void __launch_bounds__(256)
     }
 }
 
-// A launch of `blocks` x 256 threads on `stream`, with programmatic stream serialization
+// A launch of `blocks` x kPassThreads threads on `stream`, with programmatic stream serialization
 // when `overlap` is set (the kernels above wait for the previous kernel before any access).
 cudaLaunchConfig_t pass_config(int64_t blocks, cudaStream_t stream, bool overlap, cudaLaunchAttribute* attr) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(blocks), 1, 1);
-    cfg.blockDim = dim3(256, 1, 1);
+    cfg.blockDim = dim3(kPassThreads, 1, 1);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -147,8 +170,8 @@ cudaLaunchConfig_t pass_config(int64_t blocks, cudaStream_t stream, bool overlap
 cudaError_t launch_reduce(const float* P, void* C, int c_bf16, int splits, int64_t mn, int num_sms, bool overlap,
                           cudaStream_t stream) {
     const int64_t n4 = mn / 4;
-    int64_t blocks = (n4 + 255) / 256;
-    const int64_t cap = static_cast<int64_t>(num_sms) * 8;
+    int64_t blocks = (n4 + kPassThreads - 1) / kPassThreads;
+    const int64_t cap = static_cast<int64_t>(num_sms) * kPassBlocksPerSm;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
     cudaLaunchAttribute attr[1];
@@ -160,8 +183,8 @@ cudaError_t launch_fixup(const Sched& sch, const float* slots, void* C, int32_t 
                          cudaStream_t stream) {
     const int64_t warps = static_cast<int64_t>(sch.sk_tiles) * sch.cg * 4 * (sch.tile_n / 32) * 4;
     if (warps == 0) return cudaSuccess;
-    int64_t blocks = (warps + 7) / 8;
-    const int64_t cap = static_cast<int64_t>(num_sms) * 8;
+    int64_t blocks = (warps + kPassThreads / 32 - 1) / (kPassThreads / 32);
+    const int64_t cap = static_cast<int64_t>(num_sms) * kPassBlocksPerSm;
     if (blocks > cap) blocks = cap;
     cudaLaunchAttribute attr[1];
     const cudaLaunchConfig_t cfg = pass_config(blocks, stream, sch.overlap != 0, attr);

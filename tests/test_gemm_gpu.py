@@ -137,7 +137,7 @@ def test_waveq_atomic_equals_deterministic_two_contributors(sk, dev):
 
 # --------------------------------------------------------------------------- small-M NT
 @pytest.mark.parametrize("partials", [1, 2], ids=["pass", "last"])
-@pytest.mark.parametrize("tile", [0, 1])
+@pytest.mark.parametrize("tile", TILES)
 @pytest.mark.parametrize("w", [synth.SMALLM_96, synth.SMALLM_256], ids=["m96", "m256"])
 @pytest.mark.parametrize("s", [2, 4, 8, 16])
 def test_smallm_split_slabs(sk, dev, dev_sms, w, s, tile, partials):
@@ -181,6 +181,30 @@ def test_smallm_fixup(sk, dev, w, name, kw, red, tile):
     assert np.abs(got - ref).max() <= 1e-4 * max(1.0, np.abs(ref).max())
 
 
+@pytest.mark.parametrize("out", ["f32", "bf16"])
+@pytest.mark.parametrize("s,partials", [(3, 1), (3, 2), (16, 2)], ids=["s3pass", "s3launch", "s16launch"])
+@pytest.mark.parametrize("tile", TILES)
+@pytest.mark.parametrize("M,N,K", [(1, 8, 4096), (127, 8, 8192), (129, 136, 1024), (200, 1000, 1000),
+                                   (300, 520, 2048)])
+def test_slab_edges(sk, dev, M, N, K, tile, s, partials, out):
+    # Split-K slabs at ragged edges (rows past M and columns past N inside a tile), summed by
+    # the reduction pass (split_partials 1) or inside the launch (2: shared among the splits
+    # when every split of a tile is resident, else by the last to arrive). C is the FP32
+    # left fold of the slabs, rounded once to the output type, bit for bit.
+    if s > -(-K // 64):
+        pytest.skip("more splits than k-iterations")
+    w = synth.Workload("slab_edge", M, N, K, "NT", "normal", 7, out=out)
+    sched = sk.schedule(1, splits=s, split_partials=partials, tile=tile)
+    got, (ws, _) = _run(sk, dev, w, sched, DET, 152)
+    U.assert_close(got, U.reference(w), f"slabs s={s} partials={partials}")
+    P = ws[sk.SK_WS_HEADER_BYTES:sk.SK_WS_HEADER_BYTES + 4 * s * M * N].view(torch.float32).reshape(s, M, N)
+    fold = P[0].clone()
+    for j in range(1, s):
+        fold = fold + P[j]
+    want = fold if out == "f32" else fold.to(torch.bfloat16).float()
+    assert np.array_equal(got, want.cpu().numpy().astype(np.float64))
+
+
 # --------------------------------------------------------------------------- sweep
 @pytest.mark.parametrize("tile", [0, 1, 2])
 @pytest.mark.parametrize("m", [128, 640, 1152, 1536, 2560, 4096])
@@ -197,10 +221,14 @@ def test_sweep(sk, dev, m, name, kw, tile):
 # --------------------------------------------------------------------------- large / long-K
 @pytest.mark.parametrize("tile", [0, 1, 2])
 @pytest.mark.parametrize("name,kw", [("hybrid", dict(mode=3)), ("streamk", dict(mode=2)),
-                                     ("streamk_sep", dict(mode=2, split_partials=1))])
+                                     ("streamk_sep", dict(mode=2, split_partials=1)),
+                                     ("splitk16_slabs", dict(mode=1, splits=16, split_partials=1)),
+                                     ("splitk16_launch", dict(mode=1, splits=16, split_partials=2))])
 def test_skinny_long_k(sk, dev, name, kw, tile):
     # 512 x 512 x 65536: 16 tiles x 1024 k-iterations, up to 11 contributors per tile
-    # (4 tiles over 74 pairs with the 256 x 256 pair tile: about 19 per tile).
+    # (4 tiles over 74 pairs with the 256 x 256 pair tile: about 19 per tile). Split-K in 16
+    # slabs: the pair tile's 64 work items are all resident and share each tile's sum; the
+    # 128 x 128 tile's 256 items are not, and the last split to arrive sums its tile.
     w = synth.SKINNY
     got, _ = _run(sk, dev, w, sk.schedule(tile=tile, **kw), DET, 148)
     U.assert_close(got, U.reference(w), name)
