@@ -51,11 +51,17 @@ WORKLOADS = {"waveq": synth.WAVEQ, "skinny": synth.SKINNY, "large": synth.LARGE,
 NOMINAL_BF16_TFLOPS = 2250.0
 NOMINAL_HBM_GBS = 8000.0
 TRAFFIC = {
-    "waveq_2048x2432x4096/hybrid/tile2@148": {"bytes": 36802304 + 1830912, "kernel_sha": "bbdcce6f971680a6",
+    "waveq_2048x2432x4096/hybrid/tile2@148": {"bytes": 36820480 + 1798400, "kernel_sha": "b7a78f33050ef606",
                                               "profile": "profiles/sk_gemm_kernel_waveq_2048x2432x4096_pair256_hybrid148.md"},
-    "large_8192x8192x8192/dp/tile2@148": {"bytes": 2053938176 + 129377280, "kernel_sha": "bbdcce6f971680a6",
+    "waveq_2048x2432x4096/dp/tile2@148": {"bytes": 36804096 + 2048, "kernel_sha": "b7a78f33050ef606",
+                                          "profile": "profiles/sk_gemm_kernel_waveq_2048x2432x4096_pair256_dp148_vs_hybrid.md"},
+    "waveq_2048x2432x4096/hybrid/tile0@148": {"bytes": 36819712 + 284416, "kernel_sha": "b7a78f33050ef606",
+                                              "profile": "profiles/sk_gemm_kernel_waveq_2048x2432x4096_tile128_hybrid148.md"},
+    "skinny_512x512x65536/splitk/s16p1/tile2@148": {"bytes": 134325504 + 3746560, "kernel_sha": "b7a78f33050ef606",
+                                              "profile": "profiles/sk_reduce_kernel_skinny_512x512x65536_pair256_splitk16.md"},
+    "large_8192x8192x8192/dp/tile2@148": {"bytes": 2043428864 + 130097664, "kernel_sha": "b7a78f33050ef606",
                                           "profile": "profiles/sk_gemm_kernel_large_8192_pair256_dp148_raster.md"},
-    "large_8192x8192x8192/dp/tile2@148/r0s8": {"bytes": 1061767424 + 125147904, "kernel_sha": "bbdcce6f971680a6",
+    "large_8192x8192x8192/dp/tile2@148/r0s8": {"bytes": 1061482752 + 126265344, "kernel_sha": "b7a78f33050ef606",
                                                "profile": "profiles/sk_gemm_kernel_large_8192_pair256_dp148_raster.md"},
 }
 
@@ -432,48 +438,83 @@ def run_smallm(sk, torch, dev, flush, stream, dev_sms):
     return out
 
 
-def run_fixups(sk, torch, dev, flush, stream, peak_tf, peak_gbs):
-    """Stream-K fixups compared on the skinny shape 512 x 512 x 65536 (many contributors per
-    tile) and on the wave-quantized shape: the owner waits and sums in k order, FP32
-    atomics, and the separate fixup pass (every partial to its slot, then a second
-    launch sums each tile in k order). 128 x 128 and 256 x 256 pair tiles, 148 SMs, with one
-    Stream-K group and with up to 8 groups (`/groupsG`: the first page's max_sk_groups_)."""
+def run_fixups(sk, torch, dev, flush, stream, peak_tf, peak_gbs, l2_bytes):
+    """Partial-tile merges compared on the skinny shape 512 x 512 x 65536 (many contributors per
+    tile) and on the wave-quantized shape. Stream-K (hybrid rule on the wave-quantized shape):
+    the owner waits and sums in k order, FP32 atomics, and the separate fixup pass (every
+    partial to its slot, then a second launch sums each tile in k order), with 128 x 128 and
+    256 x 256 pair tiles on 148 SMs, with one Stream-K group and with up to 8 groups
+    (`/groupsG`: the first page's max_sk_groups_). On the skinny shape also Split-K in 16 FP32
+    slabs, summed by the reduction pass or inside the launch. Each entry is timed back to back
+    (60 steps over rotating input sets of at least 4x the L2, behind a flush queued before the
+    start event, as the headline) and one flushed launch at a time (median of 20)."""
     out = {}
     for w, mode in ((synth.SKINNY, sk.SK_STREAMK), (synth.WAVEQ, sk.SK_HYBRID)):
         A_bits, B_bits = synth.make_inputs(w)
         A = torch.from_numpy(A_bits.view(np.int16)).view(torch.bfloat16).to(dev)
         B = torch.from_numpy(B_bits.view(np.int16)).view(torch.bfloat16).to(dev)
         C = torch.empty((w.M, w.N), dtype=torch.bfloat16, device=dev)
+        set_bytes = A.numel() * 2 + B.numel() * 2 + C.numel() * 2
+        n_sets = max(2, -(-4 * l2_bytes // set_bytes))
+        sets = [(A, B, C)] + [(A.clone(), B.clone(), torch.empty_like(C)) for _ in range(n_sets - 1)]
         fl = 2.0 * w.M * w.N * w.K
         # The shape's roofline time: the larger of its tensor time at the measured peak and the
         # time to move A, B and C once at the measured HBM bandwidth.
         hbm_bytes = 2.0 * (w.M * w.K + w.K * w.N) + 2.0 * w.M * w.N
         bound_us = max(fl / (peak_tf * 1e12), hbm_bytes / (peak_gbs * 1e9)) * 1e6
         rows = {"roofline_us": bound_us}
+        cases = []
         for (tile, tname), groups in itertools.product(((0, "128x128"), (2, "pair256x256")), (0, 8)):
-            plan = sk.sk_plan(w.M, w.N, w.K, 148, sk.schedule(mode, tile=tile, sk_groups=groups))
-            contrib = plan[-sk.SK_MAP_TILE * int(plan[2]) + 1::sk.SK_MAP_TILE]
-            gname = f"/groups{int(plan[17])}" if groups else ""
             for name, part, red in (("owner", 0, sk.SK_DETERMINISTIC), ("atomic", 0, sk.SK_ATOMIC),
                                     ("pass", 1, sk.SK_DETERMINISTIC)):
-                sch = sk.schedule(mode, split_partials=part, tile=tile, sk_groups=groups)
-                nb = sk.sk_workspace_size(w.M, w.N, w.K, 148, sch, red)
-                ws = torch.zeros(nb, dtype=torch.uint8, device=dev)
-                g = lambda: sk.sk_gemm(A, B, C, sk.SK_BF16, w.M, w.N, w.K, sk.SK_NN, sch, red, 148, ws, nb, stream)
-                for _ in range(5):
-                    g()
-                ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(40)]
-                for a0, a1 in ev:
-                    flush.zero_()
-                    a0.record(stream)
-                    g()
-                    a1.record(stream)
-                torch.cuda.synchronize(dev)
-                assert sk.sk_status(ws, stream) == sk.SK_OK
-                us = float(np.median([a0.elapsed_time(a1) for a0, a1 in ev])) * 1e3
-                rows[f"{tname}/{name}{gname}"] = {"us": us, "tflops": fl / (us / 1e6) / 1e12, "launches": 2 if part else 1,
-                                           "max_contributors_per_tile": int(max(contrib)),
-                                           "frac_of_roofline": bound_us / us}
+                cases.append((tname, name, sk.schedule(mode, split_partials=part, tile=tile, sk_groups=groups,
+                                                       overlap=1), red, groups))
+        if w is synth.SKINNY:
+            for tile, tname in ((2, "pair256x256"), (0, "128x128")):
+                cases.append((tname, "splitk16_slabs_pass",
+                              sk.schedule(sk.SK_SPLITK, 16, split_partials=1, tile=tile, overlap=1),
+                              sk.SK_DETERMINISTIC, 0))
+            cases.append(("pair256x256", "splitk16_slabs_in_launch",
+                          sk.schedule(sk.SK_SPLITK, 16, split_partials=2, tile=2, overlap=1), sk.SK_DETERMINISTIC, 0))
+        best = None
+        for tname, name, sch, red, groups in cases:
+            plan = sk.sk_plan(w.M, w.N, w.K, 148, sch)
+            contrib = plan[-sk.SK_MAP_TILE * int(plan[2]) + 1::sk.SK_MAP_TILE]
+            gname = f"/groups{int(plan[17])}" if groups else ""
+            nb = sk.sk_workspace_size(w.M, w.N, w.K, 148, sch, red)
+            ws = torch.zeros(nb, dtype=torch.uint8, device=dev)
+
+            def g(i):
+                a, b, c = sets[i % n_sets]
+                sk.sk_gemm(a, b, c, sk.SK_BF16, w.M, w.N, w.K, sk.SK_NN, sch, red, 148, ws, nb, stream)
+            for i in range(5):
+                g(i)
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(20)]
+            for a0, a1 in ev:
+                flush.zero_()
+                a0.record(stream)
+                g(0)
+                a1.record(stream)
+            torch.cuda.synchronize(dev)
+            flushed = float(np.median([a0.elapsed_time(a1) for a0, a1 in ev])) * 1e3
+            b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            flush.zero_()
+            b0.record(stream)
+            for i in range(60):
+                g(i)
+            b1.record(stream)
+            torch.cuda.synchronize(dev)
+            assert sk.sk_status(ws, stream) == sk.SK_OK
+            us = b0.elapsed_time(b1) * 1e3 / 60
+            key = f"{tname}/{name}{gname}"
+            rows[key] = {"us": us, "tflops": fl / (us / 1e6) / 1e12, "frac_of_roofline": bound_us / us,
+                         "us_flushed": flushed, "launches": 2 if sch.split_partials == 1 else 1,
+                         "max_contributors_per_tile": int(max(contrib)),
+                         "deterministic": red == sk.SK_DETERMINISTIC}
+            if red == sk.SK_DETERMINISTIC and (best is None or us < rows[best]["us"]):
+                best = key
+        rows["best_deterministic"] = {"schedule": best, "us": rows[best]["us"],
+                                      "frac_of_roofline": rows[best]["frac_of_roofline"]}
         out[w.name] = rows
     return out
 
@@ -1021,14 +1062,13 @@ def main():
                                             f"({cpu_s:.1f} s, numpy matmul, default BLAS threads)"}
 
         extras["smallm_nt"] = run_smallm(sk, torch, dev, flush, stream, dev_sms)
-        extras["fixups"] = run_fixups(sk, torch, dev, flush, stream, peak_tf, float(peaks["hbm_gbs"]))
+        extras["fixups"] = run_fixups(sk, torch, dev, flush, stream, peak_tf, float(peaks["hbm_gbs"]), l2_bytes)
         extras["raster_8192"] = run_raster(sk, torch, dev, flush, stream, peak_tf)
         extras["sweep"] = run_sweep_compact(sk, torch, dev, red, flush, stream, peak_tf, l2_bytes)
-
-        if args.sweep:
-            run_sweep(sk, torch, dev, args.sweep, red, flush, stream, peak_tf, dev_sms, l2_bytes)
-        if args.experiments:
-            run_experiments(sk, torch, dev, flush, stream, args.experiments)
+    if rank == 0 and args.sweep:
+        run_sweep(sk, torch, dev, args.sweep, red, flush, stream, peak_tf, dev_sms, l2_bytes)
+    if rank == 0 and args.experiments:
+        run_experiments(sk, torch, dev, flush, stream, args.experiments)
 
     if rank != 0:
         if world > 1:
@@ -1037,8 +1077,27 @@ def main():
 
     sha = kernel_sha()
     order = "" if (args.raster, args.swizzle) in ((0, 0), (0, 1)) else f"/r{args.raster}s{args.swizzle}"
-    tr = TRAFFIC.get(f"{w.name}/{args.mode}/tile{args.tile}@{sms}{order}")
+    split = f"/s{args.splits}p{args.partials}" if args.mode == "splitk" else ""
+    tr = TRAFFIC.get(f"{w.name}/{args.mode}{split}/tile{args.tile}@{sms}{order}")
     traffic = tr["bytes"] if tr and tr.get("kernel_sha") == sha else None
+    # The roofline that bounds the step: the tensor time of 2MNK at the measured BF16 peak, or
+    # (long-K shapes such as 512 x 512 x 65536) the time to read A and B and write C once at the
+    # measured HBM bandwidth, whichever is longer.
+    hbm_gbs = float(peaks["hbm_gbs"])
+    algo_bytes = 2.0 * (w.M * w.K + w.K * w.N) + (2.0 if w.out == "bf16" else 4.0) * w.M * w.N
+    kernel_name = "sk_gemm_kernel" + (" + its second launch" if launches_per_step == 2 else "")
+    if algo_bytes / (hbm_gbs * 1e9) > flops / (peak_tf * 1e12):
+        achieved_gbs = algo_bytes / (ms_per_step / 1e3) / 1e9
+        roofline = {"bound": "hbm", "achieved": achieved_gbs, "peak": hbm_gbs, "unit": "GB/s",
+                    "frac": achieved_gbs / hbm_gbs, "traffic": traffic, "algorithmic_bytes": algo_bytes,
+                    "nominal_peak": NOMINAL_HBM_GBS, "frac_of_nominal": achieved_gbs / NOMINAL_HBM_GBS,
+                    "peak_source": f"{peaks_src} HBM copy", "kernel": kernel_name,
+                    "tflops": kernel_tflops, "frac_of_bf16_peak": kernel_tflops / peak_tf}
+    else:
+        roofline = {"bound": "tensor", "achieved": kernel_tflops, "peak": peak_tf, "unit": "TFLOP/s",
+                    "frac": kernel_tflops / peak_tf, "traffic": traffic,
+                    "nominal_peak": NOMINAL_BF16_TFLOPS, "frac_of_nominal": kernel_tflops / NOMINAL_BF16_TFLOPS,
+                    "peak_source": f"{peaks_src} bf16 burst", "kernel": kernel_name}
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
@@ -1064,10 +1123,7 @@ def main():
                                          "256 MiB L2 flush queued before the start event",
                                "flush": "one sk_gemm call per event pair"}[args.timing]),
                    "accumulate": "fp32"},
-        "roofline": {"bound": "tensor", "achieved": kernel_tflops, "peak": peak_tf, "unit": "TFLOP/s",
-                     "frac": kernel_tflops / peak_tf, "traffic": traffic,
-                     "nominal_peak": NOMINAL_BF16_TFLOPS, "frac_of_nominal": kernel_tflops / NOMINAL_BF16_TFLOPS,
-                     "peak_source": f"{peaks_src} bf16 burst", "kernel": "sk_gemm_kernel"},
+        "roofline": roofline,
         "gpu_launches": args.steps * launches_per_step,
         "clocks": clocks.summary(),
         "wall_s_timed_region": wall,
