@@ -627,8 +627,9 @@ def main():
     ap.add_argument("--partials", type=int, default=0, choices=[0, 1, 2],
                     help="split_partials of the timed schedule (Split-K slabs; Stream-K/hybrid separate fixup pass)")
     ap.add_argument("--sk-groups", type=int, default=0, help="Stream-K groups of the timed schedule (0: one group)")
-    ap.add_argument("--overlap", type=int, default=1, choices=[0, 1],
-                    help="launch each step overlapped with the one before it (programmatic dependent launch)")
+    ap.add_argument("--overlap", type=int, default=1, choices=[0, 1, 2],
+                    help="launch each step overlapped with the one before it (programmatic dependent launch); "
+                         "2: and load A and B before it completes (each step's operands are independent)")
     ap.add_argument("--timing", default="graph", choices=["graph", "stream", "flush"],
                     help="graph: the K steps' calls captured as one CUDA graph (outside the timed region) "
                          "and replayed once, back to back over rotating input sets of at least 4x the L2; "
@@ -864,13 +865,15 @@ def main():
         extras["schedules"] = table
 
         # ---- the same launches back to back over the rotating sets, without and with the
-        # overlapped launch: what a stream of GEMMs pays per step beyond the kernel itself.
+        # overlapped launch (1), and with operand loads ahead of the previous step (2, the
+        # steps' operands being independent): what a stream of GEMMs pays per step beyond the
+        # kernel itself.
         b2b = {}
         for tile, name, nsms in ((2, "hybrid", 148), (2, "dp", 148), (2, "streamk", 148), (0, "hybrid", 148),
-                                 (2, "hybrid", dev_sms)):
+                                 (0, "dp", 148), (2, "hybrid", dev_sms)):
             mname = "splitk" if name.startswith("splitk") else name
             row = {}
-            for ov in (0, 1):
+            for ov in (0, 1, 2):
                 s2, ws2, nb2 = make(mname, nsms, 2, tile, overlap=ov)
                 ms = stream_timed(s2, ws2, nb2, nsms, 400, 24)
                 row[f"overlap{ov}"] = {"us": ms * 1e3, "tflops": flops / (ms / 1e3) / 1e12,

@@ -92,7 +92,7 @@ int32_t make_sched_core(int32_t M, int32_t N, int32_t K, int32_t num_sms, const 
     int32_t tm = 0, tn = 0, cg = 0;
     if (!tile_shape(s.tile, &tm, &tn, &cg)) return SK_EINVAL;
     if (s.raster < 0 || s.raster > 1 || s.swizzle < 0 || s.swizzle > 256) return SK_EINVAL;
-    if (s.overlap < 0 || s.overlap > 1) return SK_EINVAL;
+    if (s.overlap < 0 || s.overlap > 2) return SK_EINVAL;
     if (s.sk_groups < 0 || s.sk_groups > 64) return SK_EINVAL;
     const int64_t tiles_n = (static_cast<int64_t>(N) + tn - 1) / tn;
     const int64_t tiles = ((static_cast<int64_t>(M) + tm - 1) / tm) * tiles_n;

@@ -167,7 +167,7 @@ __device__ void prefetch_first_loads(const KArgs& a, const CUtensorMap* tmA, con
 template <bool kNT, int kCG, int kBN>
 __device__ void run_producer(const KArgs& a, const CUtensorMap* tmA, const CUtensorMap* tmB,
                              const Smem<Shape<kCG, kBN>>& sm, Walk w, Seg g, bool have, const CtaPos& pos,
-                             uint64_t deadline, volatile int* abort_flag, int* prefetch) {
+                             uint64_t deadline, volatile int* abort_flag, int* prefetch, bool early) {
     using S = Shape<kCG, kBN>;
     const uint32_t rank = pos.rank;
     Seg last;
@@ -177,6 +177,15 @@ __device__ void run_producer(const KArgs& a, const CUtensorMap* tmA, const CUten
     uint32_t issued = 0;
     bool ok = true;
     for (; ok && have; have = w.next(a.sch, g)) {
+        if (early && nseg == 2) {
+            // Operand loads ahead of the previous kernel (overlap = 2): the first two segments
+            // fill the two fresh accumulators. The third waits on the epilogue, which waits for
+            // that kernel, so from here on this warp waits for it too and its wait limits count
+            // from then.
+            grid_dep_wait();
+            early = false;
+            deadline = globaltimer() + a.timeout_ns;
+        }
         last = g;
         ++nseg;
         // This CTA's rows of the tile and its half of the tile's columns of B.
@@ -222,6 +231,13 @@ __device__ void run_producer(const KArgs& a, const CUtensorMap* tmA, const CUten
             }
         }
     }
+    // The workspace (flags, partial slots, status word) is touched only after the previous
+    // kernel has completed; the owner's partial fetch then waits within a limit counted
+    // from there.
+    if (early) {
+        grid_dep_wait();
+        deadline = globaltimer() + a.timeout_ns;
+    }
     if (ok && kEpiGroups == 1 && nseg > 0 && last.role == kOwner && !a.sch.sep && !a.atomic)
         ok = prefetch_partials<kCG, kBN>(a, sm, last, pos, issued, deadline, abort_flag, prefetch);
     if (!ok) record_timeout(a, abort_flag);
@@ -242,7 +258,7 @@ __device__ void run_producer(const KArgs& a, const CUtensorMap* tmA, const CUten
 // (cluster ranks 0 and 1) through a cluster-multicast mbarrier arrive.
 template <bool kNT, int kCG, int kBN>
 __device__ void run_mma(const KArgs& a, const Smem<Shape<kCG, kBN>>& sm, uint32_t tmem_base, Walk w, Seg g,
-                        bool have, uint64_t deadline, volatile int* abort_flag) {
+                        bool have, uint64_t deadline, volatile int* abort_flag, bool early) {
     using S = Shape<kCG, kBN>;
     constexpr uint16_t pair_mask = 0x3u;
     constexpr uint32_t kIdesc = idesc_bf16_f32(kCtaRows * kCG, kBN, kNT ? 0u : 1u);
@@ -260,6 +276,13 @@ __device__ void run_mma(const KArgs& a, const Smem<Shape<kCG, kBN>>& sm, uint32_
     // A pair's MMA writes both CTAs' TMEM: wait until the peer has allocated its part.
     if (kCG == 2 && !mbar_wait<true>(sm.tready(), 0u, abort_flag, deadline)) ok = false;
     for (; ok && have; have = w.next(a.sch, g)) {
+        if (early && seg == 2) {
+            // As in the producer (overlap = 2): the third segment reuses the first accumulator,
+            // which the epilogue hands back only after its own wait for the previous kernel.
+            grid_dep_wait();
+            early = false;
+            deadline = globaltimer() + a.timeout_ns;
+        }
         if (!mbar_wait<kCG == 2>(sm.tempty(buf), (buf ? uses1 : uses0) ^ 1u, abort_flag, deadline)) {
             ok = false;
             break;
@@ -337,7 +360,10 @@ __device__ void run_mma(const KArgs& a, const Smem<Shape<kCG, kBN>>& sm, uint32_
             uses0 ^= 1u;
         buf ^= 1;
     }
-    if (!ok) record_timeout(a, abort_flag);
+    if (!ok) {
+        if (early) grid_dep_wait();  // the status word is written after the previous kernel
+        record_timeout(a, abort_flag);
+    }
     // Every MMA issued so far has finished reading shared memory and writing TMEM (of
     // both CTAs of a pair) before this thread moves on to the exit barrier.
     if (kCG == 1)
@@ -1213,13 +1239,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     Walk walk;
     Seg first{};
     bool have_first = false;
+    // With overlap = 2 the caller states that A and B are not written by the kernel before
+    // this one on the stream: the producer and the MMA issuer then start their first two
+    // segments without waiting for it (they touch only A, B, shared and tensor memory until
+    // their own later wait). A traced launch waits as usual, since the trace is global memory.
+    const bool early = args.sch.overlap == 2 && args.trace == nullptr;
     if (warp == 0) {
         if (lane == 0) {
-            if (args.sch.overlap) prefetch_first_loads<kNT, kCG, kBN>(args, &tmA, &tmB, unit, pos);
+            if (args.sch.overlap == 1) prefetch_first_loads<kNT, kCG, kBN>(args, &tmA, &tmB, unit, pos);
             walk.init(args.sch, unit);
             have_first = walk.next(args.sch, first);
         }
-        grid_dep_wait();
+        if (!early) grid_dep_wait();
         grid_dep_launch();
         const uint64_t deadline = globaltimer() + args.timeout_ns;  // wait limits count from here
         if (lane == 0) {
@@ -1228,7 +1259,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 start_clk = clock64();
             }
             run_producer<kNT, kCG, kBN>(args, &tmA, &tmB, sm, walk, first, have_first, pos, deadline, abort_flag,
-                                        prefetch);
+                                        prefetch, early);
         }
         // Warps 0 and 1 reconverge before the exit barrier: a CTA barrier counts a warp once
         // any of its threads arrives, so all 32 lanes must arrive together.
@@ -1255,11 +1286,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             walk.init(args.sch, unit);
             have_first = walk.next(args.sch, first);
         }
-        grid_dep_wait();
+        if (!early) grid_dep_wait();
         grid_dep_launch();
         const uint64_t deadline = globaltimer() + args.timeout_ns;
         if (lane == 0 && rank == 0)
-            run_mma<kNT, kCG, kBN>(args, sm, tmem_base, walk, first, have_first, deadline, abort_flag);
+            run_mma<kNT, kCG, kBN>(args, sm, tmem_base, walk, first, have_first, deadline, abort_flag, early);
         __syncwarp();
     } else {
         named_bar_sync(2, 32 + kEpiThreads);

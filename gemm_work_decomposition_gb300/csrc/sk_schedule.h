@@ -67,7 +67,7 @@ struct Sched {
     // `swizzle` tiles across the walk (0 or 1: no strips).
     int32_t tiles_m, raster, swizzle;
     // Launch option, not part of the plan: overlap each launch with the kernel before it on
-    // the stream (programmatic dependent launch).
+    // the stream (programmatic dependent launch; 2: and load A and B before it completes).
     int32_t overlap;
     // The walk's divisors: iters, sk_q + 1, sk_q (at least 1 wherever it is used), splits, and
     // for the tile order the strip size swizzle * (tiles along the walk) and the swizzle.

@@ -105,7 +105,16 @@ typedef struct {
                                pass of split_partials = 1 overlaps the GEMM the same way.
                                Each device-side wait limit then counts from that wait.
                                The one-CTA tiles then launch without the cooperative
-                               attribute, after the same residency check as the pairs. */
+                               attribute, after the same residency check as the pairs.
+                               2: as 1, and the caller states that A and B are not
+                               written by the kernel just before this call on the stream
+                               (nor by any kernel that one may overlap): GEMMs over
+                               independent operands one after another. Each unit's TMA
+                               loads and MMAs of its first two segments (its two fresh
+                               accumulators) then start before that kernel has completed;
+                               C, the workspace and every flag are still touched only
+                               after it, so results are the same bit for bit as with 1.
+                               A caller whose A or B come from that kernel must use 1. */
     int32_t sk_groups;      /* Stream-K grouping (first page, Case 4 knob table,
                                max_sk_groups_: units split into up to 8 groups so that
                                partial tiles computed together stay close in L2). 0 or 1:

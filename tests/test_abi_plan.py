@@ -117,10 +117,12 @@ def test_overlap_is_a_launch_option(sk):
             for mode, splits, partials in ((S.DP, 1, 0), (S.STREAMK, 1, 0), (S.HYBRID, 1, 1), (S.SPLITK, 2, 1),
                                            (S.SPLITK, 3, 2)):
                 a = sk.schedule(mode, splits, split_partials=partials, tile=tile)
-                b = sk.schedule(mode, splits, split_partials=partials, tile=tile, overlap=1)
-                assert np.array_equal(sk.sk_plan(M, N, K, 148, a), sk.sk_plan(M, N, K, 148, b))
-                for red in (0, 1):
-                    assert sk.sk_workspace_size(M, N, K, 148, a, red) == sk.sk_workspace_size(M, N, K, 148, b, red)
+                for ov in (1, 2):
+                    b = sk.schedule(mode, splits, split_partials=partials, tile=tile, overlap=ov)
+                    assert np.array_equal(sk.sk_plan(M, N, K, 148, a), sk.sk_plan(M, N, K, 148, b))
+                    for red in (0, 1):
+                        assert (sk.sk_workspace_size(M, N, K, 148, a, red) ==
+                                sk.sk_workspace_size(M, N, K, 148, b, red))
 
 
 def test_plan_streamk_groups(sk):
@@ -204,7 +206,7 @@ def test_errors(sk):
         (128, 128, 128, 4, sk.schedule(sk.SK_DP, 1, -1)),
         (128, 128, 128, 1, sk.schedule(sk.SK_DP, 1, 0, 0, 0, 1)),      # a pair needs 2 SMs
         (128, 128, 128, 4, sk.schedule(sk.SK_DP, 1, 0, 0, 0, 4)),      # unknown tile shape
-        (128, 128, 128, 4, sk.schedule(sk.SK_DP, overlap=2)),          # overlap is 0 or 1
+        (128, 128, 128, 4, sk.schedule(sk.SK_DP, overlap=3)),          # overlap is 0, 1 or 2
         (128, 128, 128, 4, sk.schedule(sk.SK_DP, overlap=-1)),
     ]
     for M, N, K, sms, sch in bad:

@@ -6,6 +6,11 @@ every result must equal the non-overlapped one bit for bit:
   - inputs rewritten by a PyTorch kernel right before each GEMM;
   - back-to-back calls with different inputs that share one workspace (turnstile flags,
     slab arrival counters, atomic tiles and fixup slots carried from call to call).
+With overlap = 2 (A and B not written by the kernel before) the first two segments' loads
+and MMAs may also run before that kernel completes; C, the workspace and the flags may
+not, so back-to-back calls over independent operands, sharing one workspace or one C,
+must give the same bits as well, and wait limits must not run out while a long kernel
+ahead is still running.
 """
 import numpy as np
 import pytest
@@ -140,14 +145,102 @@ def test_overlapped_back_to_back_shared_workspace(sk, dev, name, kw, tile, red):
         assert sk.sk_status(ws, stream) == sk.SK_OK
         return [o.cpu().numpy() for o in outs]
 
-    ref, got = run(0), run(1)
+    ref, got, early = run(0), run(1), run(2)
     for i in range(12):
         assert np.array_equal(got[i], ref[i % 3]), i
+        assert np.array_equal(early[i], ref[i % 3]), i
         assert np.array_equal(ref[i], ref[i % 3]), i
     assert not np.array_equal(ref[0], ref[1])
 
 
-def test_bench_configuration_back_to_back(sk, dev):
+@pytest.mark.parametrize("red", [DET, ATOM])
+@pytest.mark.parametrize("tile", [0, 2])
+@pytest.mark.parametrize("name,kw", [("hybrid", dict(mode=3)), ("streamk", dict(mode=2)),
+                                     ("slabs2", dict(mode=1, splits=2, split_partials=1)),
+                                     ("streamk_sep", dict(mode=2, split_partials=1))])
+def test_early_operand_loads_one_output(sk, dev, name, kw, tile, red):
+    # overlap = 2: eight calls over independent operands (integer, so every sum is exact)
+    # write the same C one after another. Each call's epilogue must wait for the one before,
+    # so C ends as the last call's product, and each intermediate product (copied out right
+    # after its call) equals the non-overlapped result.
+    M, N, K, sms = 768, 1024, 2048, 148
+    sets = []
+    for i in range(4):
+        a, b = synth.small_int_inputs(M, N, K, "NN", 70 + i)
+        sets.append((_bf16(a, dev), _bf16(b, dev)))
+    stream = torch.cuda.current_stream(dev)
+
+    def run(overlap, copy_out):
+        sched = sk.schedule(tile=tile, overlap=overlap, **kw)
+        nbytes = sk.sk_workspace_size(M, N, K, sms, sched, red)
+        ws = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
+        C = torch.full((M, N), U.SENTINEL, dtype=torch.float32, device=dev)
+        outs = []
+        torch.cuda.synchronize(dev)
+        for i in range(8):
+            A, B = sets[i % 4]
+            sk.sk_gemm(A, B, C, sk.SK_F32, M, N, K, sk.SK_NN, sched, red, sms, ws, nbytes, stream)
+            if copy_out:
+                outs.append(C.clone())
+        assert sk.sk_status(ws, stream) == sk.SK_OK
+        return C.cpu().numpy(), [o.cpu().numpy() for o in outs]
+
+    ref_last, ref = run(0, True)
+    last, _ = run(2, False)
+    assert np.array_equal(last, ref[7])
+    _, got = run(2, True)
+    for i in range(8):
+        assert np.array_equal(got[i], ref[i]), i
+    assert not np.array_equal(ref[0], ref[1])
+
+
+@pytest.mark.parametrize("tile", [0, 2])
+def test_early_operand_loads_wait_limit(sk, dev, tile):
+    # overlap = 2 behind a GEMM of about a hundred microseconds or more: the next calls'
+    # first segments may start on SMs the long GEMM leaves free, long before it completes.
+    # Their wait limits (50 us here) count from their own wait for it, so no call may
+    # report a time-out, and every result is exact.
+    Mb = Nb = 4096
+    Kb = 8192
+    big_a = torch.ones((Mb, Kb), dtype=torch.bfloat16, device=dev)
+    big_b = torch.ones((Kb, Nb), dtype=torch.bfloat16, device=dev)
+    big_c = torch.empty((Mb, Nb), dtype=torch.bfloat16, device=dev)
+    M, N, K, sms = 512, 1024, 4096, 148
+    sets = []
+    for i in range(3):
+        a, b = synth.small_int_inputs(M, N, K, "NN", 80 + i)
+        sets.append((_bf16(a, dev), _bf16(b, dev)))
+    stream = torch.cuda.current_stream(dev)
+    big = sk.schedule(3, tile=2, overlap=1)
+    nb_big = sk.sk_workspace_size(Mb, Nb, Kb, sms, big, DET)
+    ws_big = torch.zeros(nb_big, dtype=torch.uint8, device=dev)
+
+    def run(overlap):
+        sched = sk.schedule(3, tile=tile, overlap=overlap)
+        nbytes = sk.sk_workspace_size(M, N, K, sms, sched, DET)
+        ws = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
+        outs = [torch.full((M, N), U.SENTINEL, dtype=torch.float32, device=dev) for _ in range(6)]
+        torch.cuda.synchronize(dev)
+        for i, C in enumerate(outs):
+            if i % 3 == 0:
+                sk.sk_gemm(big_a, big_b, big_c, sk.SK_BF16, Mb, Nb, Kb, sk.SK_NN, big, DET, sms, ws_big, nb_big,
+                           stream)
+            A, B = sets[i % 3]
+            sk.sk_gemm_debug(A, B, C, sk.SK_F32, M, N, K, sk.SK_NN, sched, DET, sms, ws, nbytes, stream,
+                             timeout_ns=50_000)
+        assert sk.sk_status(ws, stream) == sk.SK_OK
+        assert sk.sk_status(ws_big, stream) == sk.SK_OK
+        return [o.cpu().numpy() for o in outs]
+
+    got = run(2)
+    ref = run(0)
+    for i in range(6):
+        assert np.array_equal(got[i], ref[i]), i
+    assert np.all(big_c.float().cpu().numpy() == float(Kb))
+
+
+@pytest.mark.parametrize("overlap", [1, 2])
+def test_bench_configuration_back_to_back(sk, dev, overlap):
     # The wave-quantized GEMM (2048 x 2432 x 4096, BF16 out) in the configuration bench.py
     # times: hybrid rule on 148 SMs, 256 x 256 CTA pairs, overlapped launches back to back
     # over rotating input sets sharing one workspace. Three sets with different seeds, nine
@@ -160,7 +253,7 @@ def test_bench_configuration_back_to_back(sk, dev):
     bits = [synth.make_inputs(w) for w in ws_]
     sets = [(_bf16(a, dev), _bf16(b, dev)) for a, b in bits]
     M, N, K = base.M, base.N, base.K
-    sched = sk.schedule(3, tile=2, overlap=1)
+    sched = sk.schedule(3, tile=2, overlap=overlap)
     nbytes = sk.sk_workspace_size(M, N, K, 148, sched, DET)
     ws = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
     outs = [torch.full((M, N), U.SENTINEL, dtype=torch.bfloat16, device=dev) for _ in range(9)]
