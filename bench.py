@@ -445,7 +445,9 @@ def run_fixups(sk, torch, dev, flush, stream, peak_tf, peak_gbs, l2_bytes):
     partial to its slot, then a second launch sums each tile in k order), with 128 x 128 and
     256 x 256 pair tiles on 148 SMs, with one Stream-K group and with up to 8 groups
     (`/groupsG`: the first page's max_sk_groups_). On the skinny shape also Split-K in 16 FP32
-    slabs, summed by the reduction pass or inside the launch. Each entry is timed back to back
+    slabs, summed by the reduction pass or inside the launch, and the pass chain with
+    `overlap = 2` (`/overlap2`: the steps' operands are independent; reported apart, as
+    `best_deterministic_independent_operands`). Each entry is timed back to back
     (60 steps over rotating input sets of at least 4x the L2, behind a flush queued before the
     start event, as the headline) and one flushed launch at a time (median of 20)."""
     out = {}
@@ -476,7 +478,11 @@ def run_fixups(sk, torch, dev, flush, stream, peak_tf, peak_gbs, l2_bytes):
                               sk.SK_DETERMINISTIC, 0))
             cases.append(("pair256x256", "splitk16_slabs_in_launch",
                           sk.schedule(sk.SK_SPLITK, 16, split_partials=2, tile=2, overlap=1), sk.SK_DETERMINISTIC, 0))
-        best = None
+            # The same chain when the steps' operands are independent (overlap = 2): the next
+            # GEMM's first segments start while the reduction runs on the SMs this one leaves.
+            cases.append(("pair256x256", "splitk16_slabs_pass/overlap2",
+                          sk.schedule(sk.SK_SPLITK, 16, split_partials=1, tile=2, overlap=2), sk.SK_DETERMINISTIC, 0))
+        best = best2 = None
         for tname, name, sch, red, groups in cases:
             plan = sk.sk_plan(w.M, w.N, w.K, 148, sch)
             contrib = plan[-sk.SK_MAP_TILE * int(plan[2]) + 1::sk.SK_MAP_TILE]
@@ -511,10 +517,14 @@ def run_fixups(sk, torch, dev, flush, stream, peak_tf, peak_gbs, l2_bytes):
                          "us_flushed": flushed, "launches": 2 if sch.split_partials == 1 else 1,
                          "max_contributors_per_tile": int(max(contrib)),
                          "deterministic": red == sk.SK_DETERMINISTIC}
-            if red == sk.SK_DETERMINISTIC and (best is None or us < rows[best]["us"]):
+            if red == sk.SK_DETERMINISTIC and sch.overlap == 1 and (best is None or us < rows[best]["us"]):
                 best = key
+            if red == sk.SK_DETERMINISTIC and (best2 is None or us < rows[best2]["us"]):
+                best2 = key
         rows["best_deterministic"] = {"schedule": best, "us": rows[best]["us"],
                                       "frac_of_roofline": rows[best]["frac_of_roofline"]}
+        rows["best_deterministic_independent_operands"] = {"schedule": best2, "us": rows[best2]["us"],
+                                                           "frac_of_roofline": rows[best2]["frac_of_roofline"]}
         out[w.name] = rows
     return out
 

@@ -491,16 +491,16 @@ int32_t sk_gemm_debug(const void* A, const void* B, void* C, sk_dtype c_dtype, i
         cudaGetLastError();
         return SK_ECUDA;
     }
+    const int free_sms = dev_sms - sch.workers * sch.cg;  // SMs the GEMM's grid leaves idle
     if (sch.partials == 1) {
-        if (launch_reduce(a.slabs, C, a.c_bf16, sch.splits, static_cast<int64_t>(M) * N, dev_sms,
-                          sch.overlap != 0, st) !=
-            cudaSuccess) {
+        if (launch_reduce(a.slabs, C, a.c_bf16, sch.splits, static_cast<int64_t>(M) * N, dev_sms, sch.overlap,
+                          free_sms, st) != cudaSuccess) {
             cudaGetLastError();
             return SK_ECUDA;
         }
     }
     if (sch.sep) {
-        if (launch_fixup(sch, a.slots, C, M, N, a.c_bf16, dev_sms, st) != cudaSuccess) {
+        if (launch_fixup(sch, a.slots, C, M, N, a.c_bf16, dev_sms, free_sms, st) != cudaSuccess) {
             cudaGetLastError();
             return SK_ECUDA;
         }
@@ -521,7 +521,7 @@ int32_t sk_reduce_splits(const float* P, void* C, sk_dtype c_dtype, int32_t spli
     if (!P || !C || !aligned(P, 16) || !aligned(C, 16)) return SK_EINVAL;
     int dev_sms = 0, max_units[kTileShapes];
     if (device_info(&dev_sms, max_units) != cudaSuccess) return SK_ECUDA;
-    if (launch_reduce(P, C, c_dtype == SK_BF16 ? 1 : 0, splits, mn, dev_sms, false, static_cast<cudaStream_t>(stream)) !=
+    if (launch_reduce(P, C, c_dtype == SK_BF16 ? 1 : 0, splits, mn, dev_sms, 0, 0, static_cast<cudaStream_t>(stream)) !=
         cudaSuccess) {
         cudaGetLastError();
         return SK_ECUDA;

@@ -103,18 +103,20 @@ cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CU
 cudaError_t prepare_device(int num_sms, int* max_units);
 // Separate fixup pass for a plan with sch.sep: every Stream-K tile covered by more than one
 // unit gets C = its partial slots summed in k order (FP32), stored as BF16 or FP32.
-// Overlapped with the GEMM before it (programmatic stream serialization) when sch.overlap.
+// Overlapped with the GEMM before it (programmatic stream serialization) when sch.overlap;
+// `free_sms`: the device's SMs that GEMM leaves idle (with overlap = 2 the pass may run on
+// those alone, so that the next GEMM starts beside it).
 cudaError_t launch_fixup(const Sched& sch, const float* slots, void* C, int32_t M, int32_t N, int c_bf16, int num_sms,
-                         cudaStream_t stream);
+                         int free_sms, cudaStream_t stream);
 // Host side: the parts of a workspace that must hold zeros before a launch (the status word,
 // the flags or arrival counters, and with atomic reduction the partial tiles the peers add
 // into), as up to two byte ranges [off[i], off[i] + len[i]); unused ranges have len 0. The
 // same layout rule as sk_workspace_size. Returns SK_OK or the sk_plan error code.
 int32_t workspace_zero_spans(int32_t M, int32_t N, int32_t K, int32_t num_sms, const void* sched, int32_t reduction,
                              int64_t (&off)[2], int64_t (&len)[2]);
-// C = sum_j P[j] in j order, FP32 -> c_bf16 ? BF16 : FP32. mn % 4 == 0. `overlap`: as for
-// launch_fixup.
-cudaError_t launch_reduce(const float* P, void* C, int c_bf16, int splits, int64_t mn, int num_sms, bool overlap,
-                          cudaStream_t stream);
+// C = sum_j P[j] in j order, FP32 -> c_bf16 ? BF16 : FP32. mn % 4 == 0. `overlap` (the
+// GEMM's sch.overlap) and `free_sms`: as for launch_fixup.
+cudaError_t launch_reduce(const float* P, void* C, int c_bf16, int splits, int64_t mn, int num_sms, int overlap,
+                          int free_sms, cudaStream_t stream);
 
 }  // namespace sk

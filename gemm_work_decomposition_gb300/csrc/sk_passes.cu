@@ -19,12 +19,28 @@ namespace {
 // CTA (255 registers x 192 threads), so part of an overlapped pass is resident early.
 constexpr int kPassThreads = 128;
 constexpr int kPassBlocksPerSm = 4;
+// Behind a GEMM launched with overlap = 2 that leaves at least kMinFreeSms SMs idle, a pass
+// runs on those SMs alone: each block holds kPassHoldSmem bytes of shared memory, so it cannot
+// sit beside a GEMM CTA (which takes nearly all of an SM's), the grid fits on the idle SMs at
+// once, and the blocks let the next kernel launch before they wait for the GEMM. The next
+// GEMM's CTAs then take the SMs this GEMM leaves and run their first segments (overlap = 2)
+// while the pass sums; their stores still wait for the pass to complete.
+constexpr int kMinFreeSms = 8;
+constexpr int kPassHoldSmem = 8192;
 
 // --------------------------------------------------------------------------- Split-K slab reduction
 __global__ void __launch_bounds__(kPassThreads, kPassBlocksPerSm)
-    sk_reduce_kernel(const float* __restrict__ P, void* __restrict__ C, int c_bf16, int splits, int64_t n4) {
-    grid_dep_wait();  // an overlapped launch reads P only once the GEMM that wrote it is done
-    grid_dep_launch();
+    sk_reduce_kernel(const float* __restrict__ P, void* __restrict__ C, int c_bf16, int splits, int64_t n4,
+                     int early) {
+    // An overlapped launch reads P only once the GEMM that wrote it is done. `early`: the
+    // next kernel may launch first (see kMinFreeSms).
+    if (early) {
+        grid_dep_launch();
+        grid_dep_wait();
+    } else {
+        grid_dep_wait();
+        grid_dep_launch();
+    }
     const float4* P4 = reinterpret_cast<const float4*>(P);
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     // An element's loads from kBatch slabs go out together (one round trip to L2 per batch
@@ -76,9 +92,14 @@ __global__ void __launch_bounds__(kPassThreads, kPassBlocksPerSm)
 // per warp access).
 __global__ void __launch_bounds__(kPassThreads, kPassBlocksPerSm)
     sk_fixup_kernel(const Sched sch, const float* __restrict__ slots, void* __restrict__ C, int32_t M, int32_t N,
-                    int c_bf16) {
-    grid_dep_wait();  // as in sk_reduce_kernel
-    grid_dep_launch();
+                    int c_bf16, int early) {
+    if (early) {  // as in sk_reduce_kernel
+        grid_dep_launch();
+        grid_dep_wait();
+    } else {
+        grid_dep_wait();
+        grid_dep_launch();
+    }
     const int lane = threadIdx.x & 31;
     const int chunks = sch.tile_n / 32;
     const int64_t per_tile = static_cast<int64_t>(sch.cg) * 4 * chunks * 4;
@@ -150,13 +171,30 @@ __global__ void __launch_bounds__(kPassThreads, kPassBlocksPerSm)
     }
 }
 
-// A launch of `blocks` x kPassThreads threads on `stream`, with programmatic stream serialization
-// when `overlap` is set (the kernels above wait for the previous kernel before any access).
-cudaLaunchConfig_t pass_config(int64_t blocks, cudaStream_t stream, bool overlap, cudaLaunchAttribute* attr) {
+// Grid of a pass that wants `want` blocks behind a GEMM launched with `overlap` that leaves
+// `free_sms` SMs idle: one wave on every SM, or (overlap = 2, enough idle SMs) one wave on the
+// idle SMs with the shared-memory hold.
+struct PassShape {
+    int64_t blocks;
+    int smem;
+    int early;
+};
+PassShape pass_shape(int64_t want, int num_sms, int overlap, int free_sms) {
+    const bool early = overlap == 2 && free_sms >= kMinFreeSms;
+    int64_t cap = static_cast<int64_t>(early ? free_sms : num_sms) * kPassBlocksPerSm;
+    int64_t blocks = want < cap ? want : cap;
+    if (blocks < 1) blocks = 1;
+    return {blocks, early ? kPassHoldSmem : 0, early ? 1 : 0};
+}
+
+// A launch of `p.blocks` x kPassThreads threads on `stream`, with programmatic stream
+// serialization when `overlap` is set (the kernels above wait for the previous kernel before
+// any access).
+cudaLaunchConfig_t pass_config(const PassShape& p, cudaStream_t stream, bool overlap, cudaLaunchAttribute* attr) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(blocks), 1, 1);
+    cfg.gridDim = dim3(static_cast<unsigned>(p.blocks), 1, 1);
     cfg.blockDim = dim3(kPassThreads, 1, 1);
-    cfg.dynamicSmemBytes = 0;
+    cfg.dynamicSmemBytes = static_cast<size_t>(p.smem);
     cfg.stream = stream;
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -167,28 +205,24 @@ cudaLaunchConfig_t pass_config(int64_t blocks, cudaStream_t stream, bool overlap
 
 }  // namespace
 
-cudaError_t launch_reduce(const float* P, void* C, int c_bf16, int splits, int64_t mn, int num_sms, bool overlap,
-                          cudaStream_t stream) {
+cudaError_t launch_reduce(const float* P, void* C, int c_bf16, int splits, int64_t mn, int num_sms, int overlap,
+                          int free_sms, cudaStream_t stream) {
     const int64_t n4 = mn / 4;
-    int64_t blocks = (n4 + kPassThreads - 1) / kPassThreads;
-    const int64_t cap = static_cast<int64_t>(num_sms) * kPassBlocksPerSm;
-    if (blocks > cap) blocks = cap;
-    if (blocks < 1) blocks = 1;
+    const PassShape p = pass_shape((n4 + kPassThreads - 1) / kPassThreads, num_sms, overlap, free_sms);
     cudaLaunchAttribute attr[1];
-    const cudaLaunchConfig_t cfg = pass_config(blocks, stream, overlap, attr);
-    return cudaLaunchKernelEx(&cfg, sk_reduce_kernel, P, C, c_bf16, splits, n4);
+    const cudaLaunchConfig_t cfg = pass_config(p, stream, overlap != 0, attr);
+    return cudaLaunchKernelEx(&cfg, sk_reduce_kernel, P, C, c_bf16, splits, n4, p.early);
 }
 
 cudaError_t launch_fixup(const Sched& sch, const float* slots, void* C, int32_t M, int32_t N, int c_bf16, int num_sms,
-                         cudaStream_t stream) {
+                         int free_sms, cudaStream_t stream) {
     const int64_t warps = static_cast<int64_t>(sch.sk_tiles) * sch.cg * 4 * (sch.tile_n / 32) * 4;
     if (warps == 0) return cudaSuccess;
-    int64_t blocks = (warps + kPassThreads / 32 - 1) / (kPassThreads / 32);
-    const int64_t cap = static_cast<int64_t>(num_sms) * kPassBlocksPerSm;
-    if (blocks > cap) blocks = cap;
+    const PassShape p = pass_shape((warps + kPassThreads / 32 - 1) / (kPassThreads / 32), num_sms, sch.overlap,
+                                   free_sms);
     cudaLaunchAttribute attr[1];
-    const cudaLaunchConfig_t cfg = pass_config(blocks, stream, sch.overlap != 0, attr);
-    return cudaLaunchKernelEx(&cfg, sk_fixup_kernel, sch, slots, C, M, N, c_bf16);
+    const cudaLaunchConfig_t cfg = pass_config(p, stream, sch.overlap != 0, attr);
+    return cudaLaunchKernelEx(&cfg, sk_fixup_kernel, sch, slots, C, M, N, c_bf16, p.early);
 }
 
 }  // namespace sk
