@@ -51,17 +51,17 @@ WORKLOADS = {"waveq": synth.WAVEQ, "skinny": synth.SKINNY, "large": synth.LARGE,
 NOMINAL_BF16_TFLOPS = 2250.0
 NOMINAL_HBM_GBS = 8000.0
 TRAFFIC = {
-    "waveq_2048x2432x4096/hybrid/tile2@148": {"bytes": 36820480 + 1798400, "kernel_sha": "b7a78f33050ef606",
+    "waveq_2048x2432x4096/hybrid/tile2@148": {"bytes": 36822016 + 1379328, "kernel_sha": "06e5f6597b0a0f4a",
                                               "profile": "profiles/sk_gemm_kernel_waveq_2048x2432x4096_pair256_hybrid148.md"},
-    "waveq_2048x2432x4096/dp/tile2@148": {"bytes": 36804096 + 2048, "kernel_sha": "b7a78f33050ef606",
+    "waveq_2048x2432x4096/dp/tile2@148": {"bytes": 36804864 + 3328, "kernel_sha": "06e5f6597b0a0f4a",
                                           "profile": "profiles/sk_gemm_kernel_waveq_2048x2432x4096_pair256_dp148_vs_hybrid.md"},
-    "waveq_2048x2432x4096/hybrid/tile0@148": {"bytes": 36819712 + 284416, "kernel_sha": "b7a78f33050ef606",
+    "waveq_2048x2432x4096/hybrid/tile0@148": {"bytes": 36821504 + 398336, "kernel_sha": "06e5f6597b0a0f4a",
                                               "profile": "profiles/sk_gemm_kernel_waveq_2048x2432x4096_tile128_hybrid148.md"},
-    "skinny_512x512x65536/splitk/s16p1/tile2@148": {"bytes": 134325504 + 3746560, "kernel_sha": "b7a78f33050ef606",
-                                              "profile": "profiles/sk_reduce_kernel_skinny_512x512x65536_pair256_splitk16.md"},
-    "large_8192x8192x8192/dp/tile2@148": {"bytes": 2043428864 + 130097664, "kernel_sha": "b7a78f33050ef606",
+    "skinny_512x512x65536/splitk/s16p1/tile2@148": {"bytes": 134333696 + 4358656, "kernel_sha": "06e5f6597b0a0f4a",
+                                                    "profile": "profiles/sk_reduce_kernel_skinny_512x512x65536_pair256_splitk16.md"},
+    "large_8192x8192x8192/dp/tile2@148": {"bytes": 2030805760 + 130338048, "kernel_sha": "06e5f6597b0a0f4a",
                                           "profile": "profiles/sk_gemm_kernel_large_8192_pair256_dp148_raster.md"},
-    "large_8192x8192x8192/dp/tile2@148/r0s8": {"bytes": 1061482752 + 126265344, "kernel_sha": "b7a78f33050ef606",
+    "large_8192x8192x8192/dp/tile2@148/r0s8": {"bytes": 1036968704 + 126036224, "kernel_sha": "06e5f6597b0a0f4a",
                                                "profile": "profiles/sk_gemm_kernel_large_8192_pair256_dp148_raster.md"},
 }
 
