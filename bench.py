@@ -236,14 +236,18 @@ def run_reference(args, w, rank, world):
 
 
 SWEEP_COMPACT = (1024, 1536, 2048, 2304, 2432, 3072, 3840, 4096)
-SWEEP_SCHEDULES = (("dp", 0, 1), ("splitk2", 1, 2), ("streamk", 2, 1), ("hybrid", 3, 1))
+# (name, mode, splits); splits None: the CUTLASS page's Split-K factor for the shape
+# (sk_split_k_slices, clamped to the K loop).
+SWEEP_SCHEDULES = (("dp", 0, 1), ("splitk2", 1, 2), ("splitk4", 1, 4), ("splitk_cutlass", 1, None),
+                   ("streamk", 2, 1), ("hybrid", 3, 1))
 
 
 def sweep_points(sk, torch, dev, red, flush, stream, peak_tf, l2_bytes, sizes, configs, flushed=0, b2b=40,
                  library=False):
     """Tile-count sweep over square M = N in `sizes`, K = 4096 (the tile-count sweep
-    workload): every schedule of SWEEP_SCHEDULES (data-parallel, Split-K s = 2, Stream-K and
-    the hybrid rule, which is the decision rule's own choice) for each (num_sms, tile) of
+    workload): every schedule of SWEEP_SCHEDULES (data-parallel, Split-K s = 2 and 4, Split-K
+    with the CUTLASS page's factor heuristic, Stream-K and the hybrid rule, which is the
+    decision rule's own choice) for each (num_sms, tile) of
     `configs`. Each point is timed `b2b` overlapped launches back to back over rotating copies
     of A, B and C that together exceed 4x the L2 (the headline's method, mean per launch),
     and, with `flushed` > 0, as the median of that many single launches with the L2 flushed
@@ -260,12 +264,15 @@ def sweep_points(sk, torch, dev, red, flush, stream, peak_tf, l2_bytes, sizes, c
         fl = 2.0 * m * m * ww.K
         for nsms, tile in configs:
             for name, mode, s in SWEEP_SCHEDULES:
+                if s is None:
+                    s = min(sk.sk_split_k_slices(m, m, ww.K, nsms), -(-ww.K // 64))
                 sch = sk.schedule(mode, s, tile=tile)
                 nb = sk.sk_workspace_size(m, m, ww.K, nsms, sch, red)
                 ws = torch.zeros(nb, dtype=torch.uint8, device=dev)
                 plan = sk.sk_plan(m, m, ww.K, nsms, sch)
                 row = {"M": m, "N": m, "K": ww.K, "tile": tile, "tiles": int(plan[2]), "num_sms": nsms,
-                       "schedule": name, "resolved_mode": int(plan[1]), "label": int(plan[9])}
+                       "schedule": name, "splits": s if mode == 1 else None, "resolved_mode": int(plan[1]),
+                       "label": int(plan[9])}
                 if flushed:
                     for _ in range(5):
                         sk.sk_gemm(A, B, C, sk.SK_BF16, m, m, ww.K, sk.SK_NN, sch, red, nsms, ws, nb, stream)
@@ -321,7 +328,8 @@ def run_sweep(sk, torch, dev, path, red, flush, stream, peak_tf, dev_sms, l2_byt
 
 def run_sweep_compact(sk, torch, dev, red, flush, stream, peak_tf, l2_bytes):
     """The tile-count sweep in the default bench line: M = N in SWEEP_COMPACT, K = 4096, the
-    four schedules with the pages' 128 x 128 tile and the 256 x 256 CTA-pair tile on 148 SMs,
+    schedules of SWEEP_SCHEDULES with the pages' 128 x 128 tile and the 256 x 256 CTA-pair tile
+    on 148 SMs,
     back to back (40 launches per point). Per size: TFLOP/s and fraction of the measured peak
     per schedule and tile, the rule's choice, and the best."""
     table = {}
@@ -335,6 +343,8 @@ def run_sweep_compact(sk, torch, dev, red, flush, stream, peak_tf, l2_bytes):
         tname = {0: "128x128", 2: "pair256x256"}[row["tile"]]
         ent[f"{tname}/{row['schedule']}"] = {"us": round(row["us_b2b"], 2), "tflops": round(row["tflops_b2b"], 1),
                                              "frac_of_measured_peak": round(row["frac_of_measured_peak_b2b"], 4)}
+        if row["splits"] is not None:
+            ent[f"{tname}/{row['schedule']}"]["splits"] = row["splits"]
         if row["schedule"] == "hybrid":
             ent[f"{tname}/rule_choice"] = {0: "dp", 3: "hybrid"}.get(row["resolved_mode"], str(row["resolved_mode"]))
     for ent in table.values():

@@ -31,7 +31,7 @@ SK_TRACE_SEGS = 15
 SK_TRACE_WORDS = 4 + 4 * SK_TRACE_SEGS
 
 EXPORTS = ("sk_plan_size", "sk_plan", "sk_workspace_size", "sk_gemm", "sk_gemm_debug", "sk_reduce_splits",
-           "sk_status", "sk_strerror", "sk_gemm_noalloc")
+           "sk_status", "sk_strerror", "sk_gemm_noalloc", "sk_split_k_slices")
 SK_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
@@ -87,6 +87,8 @@ def lib() -> ctypes.CDLL:
         L.sk_status.restype = i32
         L.sk_gemm_noalloc.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, sk_schedule, i32, i32, vp]
         L.sk_gemm_noalloc.restype = i32
+        L.sk_split_k_slices.argtypes = [i32, i32, i32, i32]
+        L.sk_split_k_slices.restype = i32
         L.sk_strerror.argtypes = [i32]
         L.sk_strerror.restype = ctypes.c_char_p
         _lib = L
@@ -129,6 +131,11 @@ def sk_plan(M: int, N: int, K: int, num_sms: int, sched: sk_schedule) -> np.ndar
     out = np.zeros(n, dtype=np.int32)
     _check(lib().sk_plan(M, N, K, num_sms, sched, out.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), n), "sk_plan")
     return out
+
+
+def sk_split_k_slices(M: int, N: int, K: int, num_sms: int) -> int:
+    """The CUTLASS page's Split-K factor for this problem (include/sk.h)."""
+    return _check(lib().sk_split_k_slices(M, N, K, num_sms), "sk_split_k_slices")
 
 
 def sk_workspace_size(M: int, N: int, K: int, num_sms: int, sched: sk_schedule, reduction: int) -> int:

@@ -514,6 +514,17 @@ int32_t sk_gemm(const void* A, const void* B, void* C, sk_dtype c_dtype, int32_t
     return sk_gemm_debug(A, B, C, c_dtype, M, N, K, layout, s, r, num_sms, workspace, ws_bytes, stream, nullptr);
 }
 
+int32_t sk_split_k_slices(int32_t M, int32_t N, int32_t K, int32_t num_sms) {
+    (void)K;  // the heuristic looks at the output tiles only
+    if (M < 1 || N < 1 || num_sms < 1) return SK_EINVAL;
+    int64_t tiles = static_cast<int64_t>(M / 128) * (N / 128);
+    if (tiles < 1) tiles = 1;
+    if (tiles >= 2ll * num_sms) return 1;
+    const int64_t target = 4ll * num_sms;
+    const int64_t s = (target + tiles - 1) / tiles;
+    return static_cast<int32_t>(s < 32 ? s : 32);
+}
+
 int32_t sk_reduce_splits(const float* P, void* C, sk_dtype c_dtype, int32_t splits, int64_t mn, void* stream) {
     if (splits < 1 || mn < 0 || mn % 4 != 0) return SK_EINVAL;
     if (c_dtype != SK_F32 && c_dtype != SK_BF16) return SK_EINVAL;

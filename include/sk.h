@@ -184,6 +184,15 @@ typedef struct {
  * M, N, K >= 1; num_sms >= 1 (the SM count the schedule is built for). */
 int64_t sk_plan_size(int32_t M, int32_t N, int32_t K, int32_t num_sms, sk_schedule s);
 
+/* Split-K factor heuristic (CUTLASS "Optimization Techniques" page, Split-K section,
+ * "Optimal Split-K Factor"): the number of K splits for an M x N x K problem on num_sms
+ * SMs. Whole 128 x 128 tiles of M x N are counted (floor division; fewer than one counts
+ * as one); with at least 2 * num_sms tiles the answer is 1, else the splits per tile that
+ * reach 4 * num_sms blocks, rounded up and capped at 32. K does not enter; a caller
+ * clamps the factor to ceil(K / 64) before using it as sk_schedule.splits. Host-only.
+ * Returns the factor (1 .. 32), or SK_EINVAL unless M, N >= 1 and num_sms >= 1. */
+int32_t sk_split_k_slices(int32_t M, int32_t N, int32_t K, int32_t num_sms);
+
 /* Write the work-unit map (layout above) into the host buffer `map` of `cap` int32.
  * Host-only; touches no GPU. Each persistent unit of sk_gemm runs exactly the
  * segments listed for it here, in this order. Stream-K ranges use q, big =

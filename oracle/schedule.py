@@ -1,9 +1,10 @@
 """Schedule oracle: how the output tiles and their K loops are split over units.
 
 TEST INFRASTRUCTURE (see the package docstring): plain, slow Python written from
-the page "Split-K and Stream-K: The Last Wave of a GEMM" (kanthi.in). Every
-function below names the passage it follows. Where the page leaves a step open,
-the reading taken is stated at the function.
+the page "Split-K and Stream-K: The Last Wave of a GEMM" (kanthi.in), and, for the
+Split-K factor heuristic, from the CUTLASS "Optimization Techniques" page. Every
+function below names the passage it follows. Where a page leaves a step open, the
+reading taken is stated at the function.
 
 Terms (page, "Mental model" table): an output tile is BM x BN = 128 x 128; a
 MAC-loop iteration is one BK = 64 step of a tile's K loop; a unit is one
@@ -114,6 +115,24 @@ def heuristic(tiles: int, iters: int, sms: int, min_iters: int = 8):
     if sk_tiles < sk_units and sk_units % sk_tiles == 0:
         return LABEL_SPLITK, sk_tiles, sk_units, sk_units // sk_tiles
     return LABEL_STREAMK, sk_tiles, sk_units, 0
+
+
+def calculate_split_k(m: int, n: int, k: int, num_sms: int) -> int:
+    """Split-K factor heuristic (CUTLASS "Optimization Techniques" page, Split-K section,
+    "Optimal Split-K Factor"). Count the whole 128 x 128 tiles of M x N (floor division, as
+    printed); with at least two tiles per SM there is no split. Otherwise aim at four
+    blocks per SM: the factor is the number of splits per tile that reaches 4 * num_sms
+    blocks (rounded up), at most 32. K does not enter.
+
+    Reading: a problem with fewer than 128 rows or columns has no whole tile, where the
+    printed code would divide by zero; it counts as one tile here."""
+    if m < 1 or n < 1 or num_sms < 1:
+        raise ValueError("sizes and SM count must be positive")
+    num_tiles = max(1, (m // 128) * (n // 128))
+    if num_tiles >= 2 * num_sms:
+        return 1
+    target_blocks = 4 * num_sms
+    return min(cdiv(target_blocks, num_tiles), 32)
 
 
 def heuristic_text(label: int, sk_tiles: int, sk_units: int, label_splits: int) -> str:

@@ -109,6 +109,19 @@ def test_plan_rasterization(sk):
             sk.sk_plan(128, 128, 64, 4, sk.schedule(0, raster=bad[0], swizzle=bad[1]))
 
 
+def test_split_k_slices_matches_oracle(sk):
+    # The CUTLASS page's Split-K factor heuristic: the C entry point equals the oracle's on a
+    # grid of shapes (ragged and below one tile) and SM counts, and rejects bad sizes.
+    for sms in (1, 4, 16, 132, 148, 152):
+        for m in (1, 96, 127, 128, 200, 640, 1024, 1536, 2048, 2432, 4096, 8192):
+            for n in (8, 128, 512, 1000, 2432, 4096):
+                assert sk.sk_split_k_slices(m, n, 4096, sms) == S.calculate_split_k(m, n, 4096, sms), (m, n, sms)
+    for bad in ((0, 128, 128, 148), (128, 0, 128, 148), (128, 128, 128, 0)):
+        with pytest.raises(sk.SkError) as e:
+            sk.sk_split_k_slices(*bad)
+        assert e.value.code == sk.SK_EINVAL
+
+
 def test_overlap_is_a_launch_option(sk):
     # The overlapped launch changes how the kernels are launched, not what they compute:
     # the plan and the workspace size are the same either way.

@@ -181,6 +181,53 @@ def test_docc_floor_partition_invariants():
             assert {y - x for x, y in b} <= {total // n, -(-total // n)}
 
 
+def test_calculate_split_k_worked_examples():
+    # The CUTLASS page's Split-K factor heuristic, worked by hand on 148 SMs (2 x 148 = 296
+    # tiles switch the split off; the target is 4 x 148 = 592 blocks):
+    #   4096 x 4096: 32 x 32 = 1024 tiles >= 296            -> 1
+    #   2432 x 2432: 19 x 19 = 361 tiles >= 296             -> 1
+    #   2048 x 2048: 16 x 16 = 256 tiles, 592 / 256 = 2.3   -> 3
+    #   1024 x 1024: 8 x 8 = 64 tiles, 592 / 64 = 9.25      -> 10
+    #   512 x 512: 16 tiles, 592 / 16 = 37                  -> capped at 32
+    #   200 x 1000: floor: 1 x 7 = 7 tiles, 592 / 7 = 84.6  -> 32
+    #   96 x 512: no whole tile, read as one tile           -> 32
+    #   2048 x 2432 on 132 SMs: 16 x 19 = 304 >= 264        -> 1
+    #   1536 x 1536 on 132 SMs: 144 tiles, 528 / 144 = 3.67 -> 4
+    cases = [((4096, 4096, 148), 1), ((2432, 2432, 148), 1), ((2048, 2048, 148), 3), ((1024, 1024, 148), 10),
+             ((512, 512, 148), 32), ((200, 1000, 148), 32), ((96, 512, 148), 32), ((2048, 2432, 132), 1),
+             ((1536, 1536, 132), 4)]
+    for (m, n, sms), want in cases:
+        assert S.calculate_split_k(m, n, 4096, sms) == want, (m, n, sms)
+    # K does not enter.
+    assert S.calculate_split_k(1024, 1024, 64, 148) == S.calculate_split_k(1024, 1024, 65536, 148)
+    with pytest.raises(ValueError):
+        S.calculate_split_k(0, 128, 128, 148)
+
+
+def test_calculate_split_k_invariants():
+    # For every shape: a factor in 1..32; 1 exactly when the whole tiles fill two waves;
+    # otherwise the factor times the tiles reaches four blocks per SM unless capped, and one
+    # split fewer would not; and the factor never grows with M or N.
+    for sms in (4, 16, 132, 148, 152):
+        prev_row = None
+        for m in range(0, 4097, 128):
+            row = []
+            for n in range(0, 4097, 128):
+                mm, nn = max(m, 1), max(n, 1)
+                s = S.calculate_split_k(mm, nn, 4096, sms)
+                tiles = max(1, (mm // 128) * (nn // 128))
+                assert 1 <= s <= 32
+                assert (s == 1) == (tiles >= 2 * sms)
+                if tiles < 2 * sms and s < 32:
+                    assert s * tiles >= 4 * sms and (s - 1) * tiles < 4 * sms
+                if row:
+                    assert s <= row[-1]
+                row.append(s)
+            if prev_row:
+                assert all(a <= b for a, b in zip(row, prev_row))
+            prev_row = row
+
+
 def test_heuristic_decisions():
     # Case 2 narrative: 2 x 12 < 132 -> all 144 tiles to 132 Stream-K units; on B200 the rule
     # keeps five full waves data-parallel and gives the last 160 tiles to Stream-K; a tail
