@@ -209,9 +209,14 @@ def test_slab_edges(sk, dev, M, N, K, tile, s, partials, out):
 @pytest.mark.parametrize("tile", [0, 1, 2])
 @pytest.mark.parametrize("m", [128, 640, 1152, 1536, 2560, 4096])
 @pytest.mark.parametrize("name,kw", [("dp", dict(mode=0)), ("splitk2", dict(mode=1, splits=2)),
+                                     ("splitk4", dict(mode=1, splits=4)), ("splitk_cutlass", dict(mode=1)),
                                      ("streamk", dict(mode=2)), ("hybrid", dict(mode=3))])
 def test_sweep(sk, dev, m, name, kw, tile):
+    # The tile-count sweep's schedules; "splitk_cutlass" takes its split count from the
+    # CUTLASS page's factor heuristic (32 at M = 128, 1 from 2432 up on 148 SMs).
     w = synth.sweep(m)
+    if name == "splitk_cutlass":
+        kw = dict(kw, splits=min(sk.sk_split_k_slices(m, m, w.K, 148), -(-w.K // 64)))
     got, _ = _run(sk, dev, w, sk.schedule(tile=tile, **kw), DET, 148)
     A_bits, B_bits = U.inputs(w)
     rows = U.sample_rows(m, 32, seed=m)
