@@ -25,7 +25,10 @@ constexpr int kPassBlocksPerSm = 4;
 // once, and the blocks let the next kernel launch before they wait for the GEMM. The next
 // GEMM's CTAs then take the SMs this GEMM leaves and run their first segments (overlap = 2)
 // while the pass sums; their stores still wait for the pass to complete.
+// The idle SMs take the pass only while it is small: at most kMaxPinnedRounds grid-stride
+// rounds of their blocks (a large reduction, say 8192 x 8192 in two slabs, runs on every SM).
 constexpr int kMinFreeSms = 8;
+constexpr int kMaxPinnedRounds = 8;
 constexpr int kPassHoldSmem = 8192;
 
 // --------------------------------------------------------------------------- Split-K slab reduction
@@ -172,15 +175,16 @@ __global__ void __launch_bounds__(kPassThreads, kPassBlocksPerSm)
 }
 
 // Grid of a pass that wants `want` blocks behind a GEMM launched with `overlap` that leaves
-// `free_sms` SMs idle: one wave on every SM, or (overlap = 2, enough idle SMs) one wave on the
-// idle SMs with the shared-memory hold.
+// `free_sms` SMs idle: one wave on every SM, or (overlap = 2, enough idle SMs, a small pass)
+// one wave on the idle SMs with the shared-memory hold.
 struct PassShape {
     int64_t blocks;
     int smem;
     int early;
 };
 PassShape pass_shape(int64_t want, int num_sms, int overlap, int free_sms) {
-    const bool early = overlap == 2 && free_sms >= kMinFreeSms;
+    const bool early = overlap == 2 && free_sms >= kMinFreeSms &&
+                       want <= static_cast<int64_t>(kMaxPinnedRounds) * free_sms * kPassBlocksPerSm;
     int64_t cap = static_cast<int64_t>(early ? free_sms : num_sms) * kPassBlocksPerSm;
     int64_t blocks = want < cap ? want : cap;
     if (blocks < 1) blocks = 1;
