@@ -207,9 +207,31 @@ def cpu_oracle_sample(w, seconds: float, rows_per_block: int = 256):
     return flops / el / 1e12, el, n, rows
 
 
+MODE_IDS = {"dp": 0, "splitk": 1, "streamk": 2, "hybrid": 3}
+TILE_NAMES = {0: "128x128", 1: "256x128 CTA pair", 2: "256x256 CTA pair", 3: "128x256"}
+
+
+def schedule_config(args, w, plan, sms: int) -> dict:
+    """The config keys that name the workload and its schedule (shared by both arms); `plan`
+    is the work-unit map's header (sk_plan's, or the oracle's, which equals it)."""
+    return {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "layout": w.layout, "out": w.out,
+            "schedule": args.mode, "split_partials": args.partials, "reduction": args.reduction, "num_sms": sms,
+            "tile": TILE_NAMES[args.tile], "tile_m": int(plan[12]), "tile_n": int(plan[13]),
+            "ctas_per_tile": int(plan[14]), "raster": "along_n" if args.raster == 0 else "along_m",
+            "swizzle": args.swizzle, "sk_groups": int(plan[17]), "tiles": int(plan[2]), "iters": int(plan[3]),
+            "workers": int(plan[4]), "resolved_mode": int(plan[1]), "sk_tiles": int(plan[5]),
+            "sk_units": int(plan[6]), "accumulate": "fp32"}
+
+
 def run_reference(args, w, rank, world):
     if rank != 0:
         return
+    from oracle import schedule as osch
+    sms = args.sms or 148
+    plan = osch.plan_map(osch.build_plan(w.M, w.N, w.K, sms, MODE_IDS[args.mode],
+                                         splits=args.splits if args.mode == "splitk" else 1,
+                                         split_partials=args.partials, tile=args.tile, raster=args.raster,
+                                         swizzle=args.swizzle, sk_groups=args.sk_groups))
     seconds = args.ref_seconds
     for _ in range(args.warmup):
         cpu_oracle_sample(w, 0.0)
@@ -226,8 +248,8 @@ def run_reference(args, w, rank, world):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "layout": w.layout,
-                   "step": f"FP64 oracle GEMM on {rows} rows of C (bounded sample)"},
+        "config": dict(schedule_config(args, w, plan, sms),
+                       step=f"FP64 oracle GEMM on {rows} rows of C (bounded sample)"),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                          "sample": f"{rows} x {w.N} x {w.K} FP64 per step (numpy matmul, default BLAS threads)"},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -1160,14 +1182,7 @@ def main():
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "layout": w.layout, "out": w.out,
-                   "schedule": args.mode, "split_partials": args.partials, "reduction": args.reduction, "num_sms": sms, "device_sms": dev_sms,
-                   "tile": {0: "128x128", 1: "256x128 CTA pair", 2: "256x256 CTA pair", 3: "128x256"}[args.tile],
-                   "tile_m": int(plan[12]), "tile_n": int(plan[13]), "ctas_per_tile": int(plan[14]),
-                   "raster": "along_n" if args.raster == 0 else "along_m", "swizzle": args.swizzle,
-                   "sk_groups": int(plan[17]),
-                   "tiles": int(plan[2]), "iters": int(plan[3]), "workers": int(plan[4]),
-                   "resolved_mode": int(plan[1]), "sk_tiles": int(plan[5]), "sk_units": int(plan[6]),
+        "config": {**schedule_config(args, w, plan, sms), "device_sms": dev_sms,
                    "overlap": args.overlap, "timing": args.timing,
                    "parallelism": (f"M-split over {world} GPUs: one {wg.M} x {w.N} x {w.K} GEMM, {rows} rows of A and C "
                                    f"per GPU, B replicated, no collective" if world > 1 else "one GPU"),
