@@ -67,6 +67,10 @@ struct Shape {
     static constexpr int kCtaSlotFloats = kCtaRows * kBN;   // a CTA's share of one partial slot
     static_assert(kBNc % 64 == 0 && kBN % 128 == 0, "tile shape");
     static_assert(kSmemBytes <= 232448 && kStages <= 8, "shared memory");
+    // The unit's last epilogue reuses the idle ring in four quarters of kRingBytes / 4 (its
+    // staging buffers, an owner's partial copies, the shared slab sum): the stages must fill
+    // exactly kRingBytes, or the quarters would reach the staging boxes and the barriers.
+    static_assert(kStages * kStageBytes == kRingBytes, "ring quarters");
 };
 
 struct KArgs {
