@@ -563,7 +563,9 @@ def run_fixups(sk, torch, dev, flush, stream, peak_tf, peak_gbs, l2_bytes):
 
 def run_raster(sk, torch, dev, flush, stream, peak_tf):
     """Tile-id order on the 8192^3 GEMM (A and B, 268 MB, exceed the 129 MB L2): data-parallel
-    256 x 256 pair tiles on 148 SMs, along N or M, with and without swizzled strips."""
+    256 x 256 pair tiles on 148 SMs, along N or M, with and without swizzled strips; and the
+    same GEMM as pure Stream-K (the hybrid rule keeps it data-parallel) with one and with up to
+    8 Stream-K groups (`streamk/groupsG`: the first page's max_sk_groups_)."""
     w = synth.LARGE
     A_bits, B_bits = synth.make_inputs(w)
     A = torch.from_numpy(A_bits.view(np.int16)).view(torch.bfloat16).to(dev)
@@ -571,8 +573,14 @@ def run_raster(sk, torch, dev, flush, stream, peak_tf):
     C = torch.empty((w.M, w.N), dtype=torch.bfloat16, device=dev)
     fl = 2.0 * w.M * w.N * w.K
     out = {}
-    for raster, sw in ((0, 0), (0, 2), (0, 4), (0, 8), (0, 16), (1, 0), (1, 4), (1, 8)):
-        sch = sk.schedule(sk.SK_DP, tile=2, raster=raster, swizzle=sw)
+    cases = [(f"{'along_n' if raster == 0 else 'along_m'}/swizzle{sw}", sk.schedule(sk.SK_DP, tile=2, raster=raster,
+                                                                                      swizzle=sw))
+             for raster, sw in ((0, 0), (0, 2), (0, 4), (0, 8), (0, 16), (1, 0), (1, 4), (1, 8))]
+    for groups in (0, 8):
+        sch = sk.schedule(sk.SK_STREAMK, tile=2, sk_groups=groups)
+        used = int(sk.sk_plan(w.M, w.N, w.K, 148, sch)[17])
+        cases.append((f"streamk/groups{used}", sch))
+    for key, sch in cases:
         nb = sk.sk_workspace_size(w.M, w.N, w.K, 148, sch, sk.SK_DETERMINISTIC)
         ws = torch.zeros(nb, dtype=torch.uint8, device=dev)
         g = lambda: sk.sk_gemm(A, B, C, sk.SK_BF16, w.M, w.N, w.K, sk.SK_NN, sch, sk.SK_DETERMINISTIC, 148, ws, nb, stream)
@@ -587,8 +595,7 @@ def run_raster(sk, torch, dev, flush, stream, peak_tf):
         torch.cuda.synchronize(dev)
         assert sk.sk_status(ws, stream) == sk.SK_OK
         us = float(np.median([a0.elapsed_time(a1) for a0, a1 in ev])) * 1e3
-        out[f"{'along_n' if raster == 0 else 'along_m'}/swizzle{sw}"] = {
-            "us": us, "tflops": fl / (us / 1e6) / 1e12, "frac_of_measured_peak": fl / (us / 1e6) / 1e12 / peak_tf}
+        out[key] = {"us": us, "tflops": fl / (us / 1e6) / 1e12, "frac_of_measured_peak": fl / (us / 1e6) / 1e12 / peak_tf}
     return out
 
 
