@@ -6,6 +6,7 @@ entry-point query, so it needs no libcuda at link time.
 """
 from __future__ import annotations
 
+import fcntl
 import os
 import shutil
 import subprocess
@@ -50,10 +51,23 @@ def up_to_date() -> bool:
 
 
 def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
-    """Compile and link libsk.so next to this file; return its path."""
+    """Compile and link libsk.so next to this file; return its path. Processes that build at
+    the same time (the ranks of a multi-GPU run) take turns on a lock file, and the ones that
+    come later find the library up to date."""
     if not force and not ptxas_info and up_to_date():
         return LIB
     os.makedirs(BUILD_DIR, exist_ok=True)
+    with open(os.path.join(BUILD_DIR, ".lock"), "w") as lock:
+        fcntl.flock(lock, fcntl.LOCK_EX)
+        try:
+            if not force and not ptxas_info and up_to_date():
+                return LIB
+            return _build_locked(verbose, ptxas_info)
+        finally:
+            fcntl.flock(lock, fcntl.LOCK_UN)
+
+
+def _build_locked(verbose: bool, ptxas_info: bool) -> str:
     cc = nvcc()
     extra = ["-Xptxas", "-v"] if ptxas_info else []
 
