@@ -14,8 +14,9 @@ meet only in the seeded inputs of the top-level `synth` module.
 Sources (all on the page "Split-K and Stream-K: The Last Wave of a GEMM",
 kanthi.in, unless stated): the Mental model figure (toy 4-SM case), Case 1
 (wave arithmetic), Case 2 (cost model, cutlass_heuristic, hybrid), Case 3
-(k-order fixup, FP64 reference), Case 4 (reduction modes); and the
+(k-order fixup, FP64 reference), Case 4 (reduction modes, max_sk_groups_); the
 "Consecutive-B split-K NAX GEMM" report (docs.waffuru.ai), section "Contract
 and numerical coverage" (NT layout, [splits,M,N] partials, FP64 dot products
-over the rounded inputs).
+over the rounded inputs); and the CUTLASS "Optimization Techniques" page
+(Split-K factor heuristic, tile rasterization).
 """
