@@ -1,5 +1,6 @@
 // sk_api.cu - the C ABI (include/sk.h): planning, validation, tensor-map encoding and
 // launch. Host code only; the kernels live in sk_kernels.cu.
+#include <algorithm>
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -28,22 +29,18 @@ constexpr int kMaxDevices = 64;
 // evenly over more than one per tile.
 void heuristic(int64_t tiles, int64_t iters, int64_t sms, int64_t min_iters, int32_t* label, int64_t* sk_tiles,
                int64_t* sk_units, int32_t* label_splits) {
-    const int64_t full_waves = tiles / sms;
-    const int64_t total_waves = (tiles + sms - 1) / sms;
+    const int64_t whole = tiles / sms;  // full waves
+    const int64_t tail = tiles % sms;   // tiles of the last, partial wave
     *label = kLabelDP;
     *sk_tiles = 0;
     *sk_units = 0;
     *label_splits = 0;
-    if (full_waves == total_waves || iters <= min_iters) return;
-    const int64_t tail = tiles - full_waves * sms;
-    if (2 * tail >= sms) return;
-    const int64_t dp_waves = full_waves > 1 ? full_waves - 1 : 0;
-    const int64_t skt = tiles - dp_waves * sms;
-    int64_t sku = (iters * skt) / min_iters;
-    if (sku > sms) sku = sms;
+    if (tail == 0 || iters <= min_iters || 2 * tail >= sms) return;
+    const int64_t skt = tiles - sms * (whole > 1 ? whole - 1 : 0);  // the last two waves
+    const int64_t sku = std::min<int64_t>(sms, skt * iters / min_iters);
     *sk_tiles = skt;
     *sk_units = sku;
-    if (skt < sku && sku % skt == 0) {
+    if (sku % skt == 0 && sku / skt > 1) {
         *label = kLabelSplitK;
         *label_splits = static_cast<int32_t>(sku / skt);
     } else {

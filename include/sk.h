@@ -31,10 +31,10 @@ extern "C" {
 #endif
 
 /* Decomposition modes ("Split-K and Stream-K: The Last Wave of a GEMM", Case 4:
- * DataParallel | SplitK | StreamK | Heuristic). SK_HYBRID is the heuristic:
- * data-parallel when the tail wave is at least half full, otherwise the last
- * two waves' tiles go to Stream-K with at least min_iters k-iterations per unit
- * (Case 2, cutlass_heuristic and hybrid). */
+ * DataParallel | SplitK | StreamK | Heuristic). SK_HYBRID is the heuristic: a last
+ * wave that holds half the SMs or more keeps the GEMM data-parallel; a smaller one
+ * hands the tiles of the final two waves to Stream-K, with no unit given fewer than
+ * min_iters k-iterations (Case 2, cutlass_heuristic and hybrid). */
 typedef enum { SK_DP = 0, SK_SPLITK = 1, SK_STREAMK = 2, SK_HYBRID = 3 } sk_mode;
 typedef enum { SK_NN = 0, SK_NT = 1 } sk_layout;
 /* Reduction modes (Case 4): deterministic = the owner adds its peers' FP32
@@ -116,8 +116,9 @@ typedef struct {
                                after it, so results are the same bit for bit as with 1.
                                A caller whose A or B come from that kernel must use 1. */
     int32_t sk_groups;      /* Stream-K grouping (first page, Case 4 knob table,
-                               max_sk_groups_: units split into up to 8 groups so that
-                               partial tiles computed together stay close in L2). 0 or 1:
+                               max_sk_groups_: at most 8 groups of Stream-K units, so
+                               that partials made at about the same time still sit in
+                               L2 when their owners read them). 0 or 1:
                                one group, the page's simulator plan. g >= 2 (at most 64):
                                the Stream-K region's tiles and its units are each cut into
                                up to g consecutive groups, big-first (the first tiles % g

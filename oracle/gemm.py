@@ -5,9 +5,9 @@ additions ("Split-K and Stream-K: The Last Wave of a GEMM", Case 3 and The trap)
 so every schedule is judged against one plain definition:
     C_ref[i, j] = sum_k double(A[i, k]) * double(B[k, j])
 over the inputs exactly as rounded to BF16 ("Consecutive-B split-K NAX GEMM",
-Contract and numerical coverage: independent F64 dot products over the actual
-dtype-rounded inputs; the Case 3 driver of the first page also checks against an
-FP64 product). The FP64 matrix product of NumPy is the library primitive for the
+Contract and numerical coverage, which compares every slab with FP64 sums taken
+over the inputs after their rounding to the storage type; the Case 3 driver of the
+first page also checks against an FP64 product). The FP64 matrix product of NumPy is the library primitive for the
 sum; no blocking or reordering is added here.
 
 Layouts (split-K report, Contract): A is [M, K] row-major. In NN, B is [K, N]

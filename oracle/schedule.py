@@ -102,18 +102,15 @@ def heuristic(tiles: int, iters: int, sms: int, min_iters: int = 8):
     waves but the last data-parallel, give the remaining tiles to Stream-K over
     min(sms, iters * sk_tiles // min_iters) units, and call it Split-K when the units
     divide evenly over more than one per tile."""
-    full_waves = tiles // sms
-    total_waves = cdiv(tiles, sms)
-    if full_waves == total_waves or iters <= min_iters:
+    whole, tail = divmod(tiles, sms)          # full waves, and tiles left for a last one
+    if tail == 0 or iters <= min_iters or 2 * tail >= sms:
         return LABEL_DP, 0, 0, 0
-    tail = tiles - full_waves * sms
-    if 2 * tail >= sms:
-        return LABEL_DP, 0, 0, 0
-    dp_waves = full_waves - 1 if full_waves > 1 else 0
-    sk_tiles = tiles - dp_waves * sms
-    sk_units = min(sms, (iters * sk_tiles) // min_iters)
-    if sk_tiles < sk_units and sk_units % sk_tiles == 0:
-        return LABEL_SPLITK, sk_tiles, sk_units, sk_units // sk_tiles
+    dp_tiles = sms * max(whole - 1, 0)        # every full wave but the last stays DP
+    sk_tiles = tiles - dp_tiles
+    sk_units = min(sms, sk_tiles * iters // min_iters)
+    per_tile, spare = divmod(sk_units, sk_tiles)
+    if spare == 0 and per_tile > 1:
+        return LABEL_SPLITK, sk_tiles, sk_units, per_tile
     return LABEL_STREAMK, sk_tiles, sk_units, 0
 
 
@@ -187,8 +184,8 @@ class Plan:
 
 def sk_group_count(n_tiles: int, iters: int, n_units: int, requested: int) -> int:
     """How many groups the Stream-K region is cut into (page, Case 4 knob table:
-    `max_sk_groups_`, "Stream-K units are split into up to 8 groups, so that partial tiles
-    computed together stay close in L2"). Reading taken: `requested` is that upper bound
+    `max_sk_groups_` caps the number of groups the Stream-K units form at 8, so that partials
+    made at about the same time stay in L2). Reading taken: `requested` is that upper bound
     (0 or 1: one group). A group needs at least one tile and one unit, and no unit may be
     left without an iteration, so the count is the largest g <= min(requested, n_tiles,
     n_units) for which every group, tiles and units each divided big-first
@@ -230,38 +227,33 @@ def _streamk_region(tiles_base: int, n_tiles: int, iters: int, n_units: int, sep
 
     With `separate` (the page's Case 3 kernel: a separate fixup pass instead of waiting)
     every partial segment, the owner's too, stores to a fixed slot per (unit, first/last
-    segment): slot 2u for the unit's first segment, 2u + 1 for a later one. A unit has at
-    most two partial segments, its first and its last; a producer is always a unit's first
-    segment.
+    segment): slot 2u for the unit's first segment, 2u + 1 for a later one. Only a unit's
+    first and last segments can be partial, and a producer is always its first.
 
     `groups` (at least 1, from sk_group_count): the unit ranges of group_bounds, so that no
     tile is shared between units of different groups."""
     bounds = group_bounds(n_tiles, iters, n_units, groups)
+    starts = [b for b, _ in bounds]
     out = []
-    for u, (b, e) in enumerate(bounds):
+    for u in range(len(bounds)):
+        b, e = bounds[u]
         segs = []
-        it = b
-        while it < e:
-            local = it // iters
-            tile_begin = local * iters
-            tile_end = tile_begin + iters
-            seg_end = min(e, tile_end)
-            kb, ke = it - tile_begin, seg_end - tile_begin
-            tile = tiles_base + local
-            if kb == 0 and ke == iters:
-                segs.append(Segment(u, 0, tile, kb, ke, FULL))
-            elif kb == 0:
-                peers = []
-                v = u + 1
-                while v < n_units and bounds[v][0] < tile_end:
-                    peers.append(v)
-                    v += 1
-                slot = (2 * u + (0 if it == b else 1)) if separate else -1
-                segs.append(Segment(u, 0, tile, kb, ke, OWNER, slot, u + 1, len(peers)))
-            else:
-                owner = next(v for v in range(n_units) if bounds[v][0] <= tile_begin < bounds[v][1])
-                segs.append(Segment(u, 0, tile, kb, ke, PRODUCER, 2 * u if separate else u, owner + 1, 0))
-            it = seg_end
+        if e > b:
+            # The tiles the range [b, e) touches, and its piece of each.
+            for local in range(b // iters, (e - 1) // iters + 1):
+                t0 = local * iters
+                kb, ke = max(b, t0) - t0, min(e, t0 + iters) - t0
+                tile = tiles_base + local
+                if (kb, ke) == (0, iters):
+                    segs.append(Segment(u, 0, tile, kb, ke, FULL))
+                elif kb == 0:
+                    # Peers: the later units whose ranges begin inside the rest of the tile.
+                    n_peers = sum(1 for v in range(u + 1, n_units) if starts[v] < t0 + iters)
+                    slot = (2 * u + (0 if local == b // iters else 1)) if separate else -1
+                    segs.append(Segment(u, 0, tile, kb, ke, OWNER, slot, u + 1, n_peers))
+                else:
+                    owner = next(v for v in range(u) if bounds[v][0] <= t0 < bounds[v][1])
+                    segs.append(Segment(u, 0, tile, kb, ke, PRODUCER, 2 * u if separate else u, owner + 1, 0))
         out.append(segs)
     return out
 

@@ -229,9 +229,9 @@ def test_calculate_split_k_invariants():
 
 
 def test_heuristic_decisions():
-    # Case 2 narrative: 2 x 12 < 132 -> all 144 tiles to 132 Stream-K units; on B200 the rule
-    # keeps five full waves data-parallel and gives the last 160 tiles to Stream-K; a tail
-    # of 100/132 stays data-parallel.
+    # Case 2 narrative: 2 x 12 < 132 -> all 144 tiles to 132 Stream-K units; on B200
+    # (148 SMs, 900 tiles) data-parallel runs 5 full waves and Stream-K takes the 160
+    # tiles after them; a tail of 100 on 132 SMs stays data-parallel.
     assert S.heuristic(144, 64, 132) == (S.LABEL_STREAMK, 144, 132, 0)
     assert S.heuristic(900, 64, 148) == (S.LABEL_STREAMK, 160, 148, 0)
     assert S.heuristic(1024, 64, 132)[0] == S.LABEL_DP
