@@ -1062,84 +1062,46 @@ def main():
                                "dp_over_schedule": dp_idle["tail_idle_sm_us"] / max(1e-9, hd_idle["tail_idle_sm_us"]),
                                "definition": "sum over the device's SMs of (kernel end - SM end), per-CTA globaltimer"}
 
-        # ---- e2e: host buffers, copies inside the timed region, through the C ABI. Every step
-        # copies its A and B from pinned host memory and its C back. Pipelined: step i+1's
-        # uploads (A and B on two copy streams) and step i-1's download overlap step i's GEMM,
-        # with two device copies of A, B and C. Timed by device events from the first upload
-        # to the last download. The serial chain (one stream) is reported beside it.
+        # ---- e2e: host buffers, copies inside the timed region, through the C ABI's host-buffer
+        # call (sk_gemm_host). Every step copies its A and B from pinned host memory into a
+        # device staging set and its C back. Pipelined (depth 2): step i+1's uploads and step
+        # i-1's download run on two copy streams while step i's GEMM runs, over two staging
+        # sets. Timed by device events on the GEMM stream around the one call (the call makes
+        # that stream wait for the last download). The serial chain (depth 1, everything on one
+        # stream) is reported beside it.
         n_e2e = max(10, min(200, args.steps))
         h2d_bytes = int(A.numel() * 2 + B.numel() * 2)
         d2h_bytes = int(C.numel() * C.element_size())
         C_host = [torch.empty((w.M, w.N), dtype=cdt).pin_memory() for _ in range(2)]
-        A2 = [torch.empty_like(A) for _ in range(2)]
-        B2 = [torch.empty_like(B) for _ in range(2)]
-        C2 = [torch.empty_like(C) for _ in range(2)]
-        # Uploads: A and B on one copy stream each (four streams, each with half of A or of B,
-        # measured no faster: the host-to-device copies are capped near 240 GB/s here).
-        pieces = [(A_host, A2), (B_host, B2)]
-        s_up = [torch.cuda.Stream(dev) for _ in pieces]
-        s_out = torch.cuda.Stream(dev)
+        stage = {d: sk.sk_host_staging_size(w.M, w.N, w.K, out_code, d) for d in (1, 2)}
+        staging = torch.empty(stage[2], dtype=torch.uint8, device=dev)
+        s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
 
-        def e2e_pipelined(n):
-            ev = lambda: torch.cuda.Event(enable_timing=False)
-            up = [[ev() for _ in range(2)] for _ in pieces]
-            done = [ev() for _ in range(2)]
-            down = [ev() for _ in range(2)]
-            used = [False, False]
-            t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            t0.record(s_up[0])
-            for su in s_up[1:]:
-                su.wait_event(t0)
-            for i in range(n):
-                j = i % 2
-                for q, ((src, dst), su) in enumerate(zip(pieces, s_up)):
-                    if used[j]:  # inputs j are free once the GEMM that read them is done
-                        su.wait_event(done[j])
-                    with torch.cuda.stream(su):
-                        dst[j].copy_(src, non_blocking=True)
-                    up[q][j].record(su)
-                    stream.wait_event(up[q][j])
-                if used[j]:  # output j is free once its previous download is done
-                    stream.wait_event(down[j])
-                sk.sk_gemm(A2[j], B2[j], C2[j], out_code, w.M, w.N, w.K, lay, sch, red, sms, ws, nb, stream)
-                done[j].record(stream)
-                s_out.wait_event(done[j])
-                with torch.cuda.stream(s_out):
-                    C_host[j].copy_(C2[j], non_blocking=True)
-                down[j].record(s_out)
-                used[j] = True
-            for j in range(2):
-                s_out.wait_event(down[j])
-            t1.record(s_out)
-            torch.cuda.synchronize(dev)
-            return t0.elapsed_time(t1) / n
-
-        def e2e_serial(n):
+        def e2e_host(n, depth):
             t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             t0.record(stream)
-            for _ in range(n):
-                A2[0].copy_(A_host, non_blocking=True)
-                B2[0].copy_(B_host, non_blocking=True)
-                sk.sk_gemm(A2[0], B2[0], C2[0], out_code, w.M, w.N, w.K, lay, sch, red, sms, ws, nb, stream)
-                C_host[0].copy_(C2[0], non_blocking=True)
+            sk.sk_gemm_host([A_host] * n, [B_host] * n, [C_host[i % 2] for i in range(n)], out_code, w.M, w.N, w.K,
+                            lay, sch, red, sms, staging, stage[depth], depth, ws, nb, stream,
+                            s_in if depth == 2 else None, s_out if depth == 2 else None)
             t1.record(stream)
             torch.cuda.synchronize(dev)
             return t0.elapsed_time(t1) / n
 
-        e2e_pipelined(3)
-        e2e_serial(3)
-        pipe_ms = e2e_pipelined(n_e2e)
-        serial_ms = e2e_serial(n_e2e)
+        e2e_host(3, 2)
+        e2e_host(3, 1)
+        pipe_ms = e2e_host(n_e2e, 2)
         if red == sk.SK_DETERMINISTIC:  # the last step's result matches the timed kernel's, bit for bit
-            assert torch.equal(C2[(n_e2e - 1) % 2], C)
+            assert torch.equal(C_host[(n_e2e - 1) % 2], C.cpu())
+        serial_ms = e2e_host(n_e2e, 1)
         extras["e2e"] = {"value": flops / (pipe_ms / 1e3) / 1e12, "unit": "TFLOP/s",
                          "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes, "ms_per_step": pipe_ms,
                          "steps": n_e2e,
-                         "how": "pipelined: A and B uploads (one copy stream each) and the C download overlap the "
-                                "GEMM of the neighbouring steps; device events from the first upload to the last "
-                                "download",
+                         "how": "sk_gemm_host over pinned host buffers, depth 2: A and B uploads on one copy stream "
+                                "and the C download on another overlap the GEMM of the neighbouring steps; device "
+                                "events on the GEMM stream around the call",
                          "h2d_plus_d2h_gbs": (h2d_bytes + d2h_bytes) / (pipe_ms / 1e3) / 1e9,
-                         "serial": {"value": flops / (serial_ms / 1e3) / 1e12, "ms_per_step": serial_ms}}
+                         "serial": {"value": flops / (serial_ms / 1e3) / 1e12, "ms_per_step": serial_ms,
+                                    "how": "sk_gemm_host, depth 1: every copy and GEMM in order on one stream"}}
         assert sk.sk_status(ws, stream) == sk.SK_OK
 
         # ---- CPU oracle baseline on a bounded sample

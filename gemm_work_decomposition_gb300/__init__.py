@@ -31,7 +31,8 @@ SK_TRACE_SEGS = 15
 SK_TRACE_WORDS = 4 + 4 * SK_TRACE_SEGS
 
 EXPORTS = ("sk_plan_size", "sk_plan", "sk_workspace_size", "sk_gemm", "sk_gemm_debug", "sk_reduce_splits",
-           "sk_status", "sk_strerror", "sk_gemm_noalloc", "sk_split_k_slices")
+           "sk_status", "sk_strerror", "sk_gemm_noalloc", "sk_split_k_slices", "sk_host_staging_size",
+           "sk_gemm_host")
 SK_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
@@ -89,6 +90,11 @@ def lib() -> ctypes.CDLL:
         L.sk_gemm_noalloc.restype = i32
         L.sk_split_k_slices.argtypes = [i32, i32, i32, i32]
         L.sk_split_k_slices.restype = i32
+        L.sk_host_staging_size.argtypes = [i32, i32, i32, i32, i32]
+        L.sk_host_staging_size.restype = i64
+        L.sk_gemm_host.argtypes = [i32, ctypes.POINTER(vp), ctypes.POINTER(vp), ctypes.POINTER(vp), i32, i32, i32,
+                                   i32, i32, sk_schedule, i32, i32, vp, sz, i32, vp, sz, vp, vp, vp]
+        L.sk_gemm_host.restype = i32
         L.sk_strerror.argtypes = [i32]
         L.sk_strerror.restype = ctypes.c_char_p
         _lib = L
@@ -176,3 +182,22 @@ def sk_gemm_noalloc(A, B, C, c_dtype: int, M: int, N: int, K: int, layout: int, 
     """sk_gemm on the library-owned scratch (no workspace argument); see include/sk.h."""
     return _check(lib().sk_gemm_noalloc(_ptr(A), _ptr(B), _ptr(C), c_dtype, M, N, K, layout, sched, reduction,
                                         num_sms, _stream(stream)), "sk_gemm_noalloc")
+
+
+def sk_host_staging_size(M: int, N: int, K: int, c_dtype: int, depth: int) -> int:
+    return _check(lib().sk_host_staging_size(M, N, K, c_dtype, depth), "sk_host_staging_size")
+
+
+def sk_gemm_host(A, B, C, c_dtype: int, M: int, N: int, K: int, layout: int, sched: sk_schedule, reduction: int,
+                 num_sms: int, staging, staging_bytes: int, depth: int, workspace, ws_bytes: int, stream=None,
+                 copy_in=None, copy_out=None) -> int:
+    """`len(C)` GEMMs over host buffers (sequences of host pointers or CPU tensors, one per
+    problem) through the device staging buffer; see include/sk.h."""
+    n = len(C)
+    if len(A) != n or len(B) != n:
+        raise ValueError("A, B and C must hold one buffer per problem")
+    arr = ctypes.c_void_p * max(n, 1)
+    pa, pb, pc = arr(*[_ptr(x) for x in A]), arr(*[_ptr(x) for x in B]), arr(*[_ptr(x) for x in C])
+    return _check(lib().sk_gemm_host(n, pa, pb, pc, c_dtype, M, N, K, layout, sched, reduction, num_sms,
+                                     _ptr(staging), staging_bytes, depth, _ptr(workspace), ws_bytes,
+                                     _stream(stream), _stream(copy_in), _stream(copy_out)), "sk_gemm_host")

@@ -19,7 +19,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libsk.so")
-SOURCES = ("sk_kernels.cu", "sk_passes.cu", "sk_api.cu", "sk_noalloc.cu")
+SOURCES = ("sk_kernels.cu", "sk_passes.cu", "sk_api.cu", "sk_noalloc.cu", "sk_host.cu")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -307,6 +307,12 @@ bool encode_out(CUtensorMap* m, void* ptr, bool bf16, uint64_t inner, uint64_t o
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
+// Every check sk_gemm makes before it enqueues anything: arguments, schedule, workspace and
+// residency. On SK_OK with M, N, K > 0, *sch holds the plan and *dev_sms the device's SM count.
+int32_t check_gemm(const void* A, const void* B, const void* C, int32_t c_dtype, int32_t M, int32_t N, int32_t K,
+                   int32_t layout, const sk_schedule& s, int32_t r, int32_t num_sms, const void* workspace,
+                   size_t ws_bytes, Sched* sch, int* dev_sms);
+
 }  // namespace
 
 namespace sk {
@@ -329,6 +335,40 @@ int32_t workspace_zero_spans(int32_t M, int32_t N, int32_t K, int32_t num_sms, c
         len[0] = reduction == SK_ATOMIC ? workspace_bytes(s, M, N) : slots_offset(s);
     }
     return SK_OK;
+}
+}  // namespace sk
+
+namespace {
+int32_t check_gemm(const void* A, const void* B, const void* C, int32_t c_dtype, int32_t M, int32_t N, int32_t K,
+                   int32_t layout, const sk_schedule& s, int32_t r, int32_t num_sms, const void* workspace,
+                   size_t ws_bytes, Sched* sch, int* dev_sms) {
+    if (M < 0 || N < 0 || K < 0 || num_sms < 1) return SK_EINVAL;
+    if (c_dtype != SK_F32 && c_dtype != SK_BF16) return SK_EINVAL;
+    if (layout != SK_NN && layout != SK_NT) return SK_EINVAL;
+    if (r != SK_DETERMINISTIC && r != SK_ATOMIC) return SK_EINVAL;
+    if (M == 0 || N == 0) return SK_OK;
+    if (!C || !aligned(C, 16) || N % 8 != 0) return SK_EINVAL;
+    if (K == 0) return SK_OK;
+    if (!A || !B || !aligned(A, 16) || !aligned(B, 16) || K % 8 != 0) return SK_EINVAL;
+    const int32_t e = make_sched(M, N, K, num_sms, s, *sch);
+    if (e != SK_OK) return e;
+    const int64_t need = workspace_bytes(*sch, M, N);
+    if (!workspace || !aligned(workspace, 256) || static_cast<int64_t>(ws_bytes) < need) return SK_EWORKSPACE;
+    int max_units[kTileShapes];
+    if (device_info(dev_sms, max_units) != cudaSuccess) return SK_ECUDA;
+    if (sch->workers > max_units[s.tile]) return SK_ERESIDENCY;
+    return SK_OK;
+}
+}  // namespace
+
+namespace sk {
+int32_t gemm_check(const void* A, const void* B, const void* C, int32_t c_dtype, int32_t M, int32_t N, int32_t K,
+                   int32_t layout, const void* sched, int32_t reduction, int32_t num_sms, const void* workspace,
+                   size_t ws_bytes) {
+    Sched sch;
+    int dev_sms = 0;
+    return check_gemm(A, B, C, c_dtype, M, N, K, layout, *static_cast<const sk_schedule*>(sched), reduction, num_sms,
+                      workspace, ws_bytes, &sch, &dev_sms);
 }
 }  // namespace sk
 
@@ -416,27 +456,15 @@ int64_t sk_workspace_size(int32_t M, int32_t N, int32_t K, int32_t num_sms, sk_s
 int32_t sk_gemm_debug(const void* A, const void* B, void* C, sk_dtype c_dtype, int32_t M, int32_t N, int32_t K,
                       sk_layout layout, sk_schedule s, sk_reduction r, int32_t num_sms, void* workspace,
                       size_t ws_bytes, void* stream, const sk_debug_opts* opts) {
-    if (M < 0 || N < 0 || K < 0 || num_sms < 1) return SK_EINVAL;
-    if (c_dtype != SK_F32 && c_dtype != SK_BF16) return SK_EINVAL;
-    if (layout != SK_NN && layout != SK_NT) return SK_EINVAL;
-    if (r != SK_DETERMINISTIC && r != SK_ATOMIC) return SK_EINVAL;
-    if (M == 0 || N == 0) return SK_OK;
-    if (!C || !aligned(C, 16) || N % 8 != 0) return SK_EINVAL;
+    Sched sch;
+    int dev_sms = 0;
+    const int32_t e = check_gemm(A, B, C, c_dtype, M, N, K, layout, s, r, num_sms, workspace, ws_bytes, &sch, &dev_sms);
+    if (e != SK_OK || M == 0 || N == 0) return e;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const size_t esz = c_dtype == SK_BF16 ? 2 : 4;
     if (K == 0) {
+        const size_t esz = c_dtype == SK_BF16 ? 2 : 4;
         return cudaMemsetAsync(C, 0, static_cast<size_t>(M) * N * esz, st) == cudaSuccess ? SK_OK : SK_ECUDA;
     }
-    if (!A || !B || !aligned(A, 16) || !aligned(B, 16) || K % 8 != 0) return SK_EINVAL;
-    Sched sch;
-    int32_t e = make_sched(M, N, K, num_sms, s, sch);
-    if (e != SK_OK) return e;
-    const int64_t need = workspace_bytes(sch, M, N);
-    if (!workspace || !aligned(workspace, 256) || static_cast<int64_t>(ws_bytes) < need) return SK_EWORKSPACE;
-
-    int dev_sms = 0, max_units[kTileShapes];
-    if (device_info(&dev_sms, max_units) != cudaSuccess) return SK_ECUDA;
-    if (sch.workers > max_units[s.tile]) return SK_ERESIDENCY;
 
     // A in 128-row boxes (one CTA's rows); B in boxes of one CTA's share of the tile's
     // columns (NT) or in 64 x 64 boxes (NN).

@@ -118,6 +118,12 @@ cudaError_t launch_fixup(const Sched& sch, const float* slots, void* C, int32_t 
 // same layout rule as sk_workspace_size. Returns SK_OK or the sk_plan error code.
 int32_t workspace_zero_spans(int32_t M, int32_t N, int32_t K, int32_t num_sms, const void* sched, int32_t reduction,
                              int64_t (&off)[2], int64_t (&len)[2]);
+// Host side: every check sk_gemm makes before it enqueues anything (arguments, schedule,
+// workspace size and alignment, residency), with `sched` pointing at an sk_schedule. SK_OK
+// when sk_gemm with the same arguments would enqueue its work, else its error code.
+int32_t gemm_check(const void* A, const void* B, const void* C, int32_t c_dtype, int32_t M, int32_t N, int32_t K,
+                   int32_t layout, const void* sched, int32_t reduction, int32_t num_sms, const void* workspace,
+                   size_t ws_bytes);
 // C = sum_j P[j] in j order, FP32 -> c_bf16 ? BF16 : FP32. mn % 4 == 0. `overlap` (the
 // GEMM's sch.overlap) and `free_sms`: as for launch_fixup.
 cudaError_t launch_reduce(const float* P, void* C, int c_bf16, int splits, int64_t mn, int num_sms, int overlap,

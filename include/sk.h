@@ -16,8 +16,9 @@
  *     once, after the fixup).
  *   - The caller owns every buffer. No entry point allocates memory.
  *   - Device pointers are plain CUDA device addresses; `stream` is a cudaStream_t
- *     (NULL = the legacy default stream). sk_gemm and sk_reduce_splits are
- *     asynchronous on that stream.
+ *     (NULL = the legacy default stream). sk_gemm, sk_reduce_splits and sk_gemm_host
+ *     are asynchronous on that stream. Only sk_gemm_host takes host pointers for A, B
+ *     and C.
  *   - Return value: SK_OK (0) or a negative SK_E* code; sk_strerror names it.
  */
 #ifndef SK_H_
@@ -305,6 +306,41 @@ int32_t sk_reduce_splits(const float* P, void* C, sk_dtype c_dtype, int32_t spli
 int32_t sk_gemm_noalloc(const void* A, const void* B, void* C, sk_dtype c_dtype,
                         int32_t M, int32_t N, int32_t K, sk_layout layout, sk_schedule s,
                         sk_reduction r, int32_t num_sms, void* stream);
+
+/* Bytes of device staging sk_gemm_host needs: `depth` sets (1 or 2) of A [M,K] BF16,
+ * B (K x N BF16) and C [M,N] of c_dtype, each part starting on a 256-byte boundary inside
+ * its set. Host-only. Returns the size, or SK_EINVAL for negative sizes, an unknown
+ * c_dtype or another depth. */
+int64_t sk_host_staging_size(int32_t M, int32_t N, int32_t K, sk_dtype c_dtype, int32_t depth);
+
+/* `count` GEMMs of one shape whose operands and results live in host memory: for problem
+ * i, A[i] and B[i] (host pointers, layouts as in sk_gemm) are copied into a device staging
+ * set, C = A . B runs there as sk_gemm with the given schedule, reduction and workspace, and
+ * C is copied to the host pointer C[i]. The pages have no counterpart: this is the end-to-end
+ * call for callers whose matrices are in host memory.
+ *   staging: device buffer of at least sk_host_staging_size(M, N, K, c_dtype, depth) bytes,
+ *     256-byte aligned, owned by the caller (else SK_EWORKSPACE).
+ *   depth 1: every copy and GEMM runs in order on `stream`; copy_in and copy_out are unused.
+ *   depth 2: two staging sets used in turn; the uploads run on `copy_in` and the downloads on
+ *     `copy_out` (two streams of the caller other than `stream`, else SK_EINVAL), so that
+ *     problem i + 1's uploads and problem i - 1's download overlap problem i's GEMM. Events
+ *     keep every buffer's writes and reads in order; the copy streams first wait for the
+ *     caller's earlier work on `stream`.
+ * Every GEMM runs on `stream`, one after another, sharing the workspace. The call is
+ * asynchronous: once `stream` has reached the point where the call returned, every C[i]
+ * has been written. Host buffers should be page-locked (cudaHostAlloc / cudaHostRegister)
+ * for the copies to run asynchronously; pageable memory works, but the host then waits in
+ * the copy calls. The host buffers must stay valid and A[i], B[i] unchanged until then; C
+ * pointers may repeat (later problems overwrite earlier ones). The call creates and
+ * releases seven CUDA events when depth is 2 and allocates no memory.
+ * Errors: argument, staging and every sk_gemm check (including SK_ERESIDENCY) are made
+ * before anything is enqueued. A CUDA failure after that (SK_ECUDA) returns at once,
+ * leaving the earlier problems' work enqueued: synchronise all three streams before reusing
+ * the buffers. count == 0, M == 0 or N == 0 does nothing. */
+int32_t sk_gemm_host(int32_t count, const void* const* A, const void* const* B, void* const* C,
+                     sk_dtype c_dtype, int32_t M, int32_t N, int32_t K, sk_layout layout, sk_schedule s,
+                     sk_reduction r, int32_t num_sms, void* staging, size_t staging_bytes, int32_t depth,
+                     void* workspace, size_t ws_bytes, void* stream, void* copy_in, void* copy_out);
 
 /* Synchronise `stream`, read the workspace status word, reset it to SK_OK and return
  * it: SK_OK, or SK_ETIMEOUT when a kernel on that workspace stopped at a wait limit.

@@ -240,3 +240,48 @@ def test_errors(sk):
     assert L.sk_gemm(0, 0, 0, sk.SK_F32, 0, 128, 64, sk.SK_NN, sch, 0, 148, 0, 0, None) == sk.SK_OK
     assert L.sk_reduce_splits(16, 16, sk.SK_F32, 0, 64, None) == sk.SK_EINVAL
     assert L.sk_reduce_splits(16, 16, sk.SK_F32, 2, 6, None) == sk.SK_EINVAL
+
+
+def test_host_staging_size(sk):
+    # One set holds A [M, K] and B [K, N] in BF16 and C [M, N], each part rounded up to 256
+    # bytes; depth 2 holds two sets.
+    up = lambda x: -(-x // 256) * 256
+    for M, N, K, dt, esz in [(128, 640, 256, sk.SK_F32, 4), (96, 512, 2048, sk.SK_BF16, 2),
+                             (3, 8, 8, sk.SK_BF16, 2), (0, 8, 8, sk.SK_F32, 4), (5, 24, 0, sk.SK_F32, 4)]:
+        one = up(M * K * 2) + up(K * N * 2) + up(M * N * esz)
+        assert sk.sk_host_staging_size(M, N, K, dt, 1) == one
+        assert sk.sk_host_staging_size(M, N, K, dt, 2) == 2 * one
+    for bad in [(-1, 8, 8, 0, 1), (8, 8, 8, 2, 1), (8, 8, 8, 0, 0), (8, 8, 8, 0, 3)]:
+        with pytest.raises(sk.SkError) as e:
+            sk.sk_host_staging_size(*bad)
+        assert e.value.code == sk.SK_EINVAL
+
+
+def test_gemm_host_argument_errors(sk):
+    # Rejected by the checks that run before any CUDA call, so no device is needed.
+    M, N, K = 128, 256, 128
+    a = np.zeros(M * K, np.uint16)
+    b = np.zeros(K * N, np.uint16)
+    c = np.zeros(M * N, np.float32)
+    pa, pb, pc = a.ctypes.data, b.ctypes.data, c.ctypes.data
+    sched = sk.schedule(sk.SK_HYBRID)
+    need = sk.sk_host_staging_size(M, N, K, sk.SK_F32, 2)
+
+    def call(A=(pa,), B=(pb,), C=(pc,), depth=1, staging=256, nbytes=need, copy_in=None, copy_out=None, m=M):
+        return sk.sk_gemm_host(list(A), list(B), list(C), sk.SK_F32, m, N, K, sk.SK_NN, sched, sk.SK_DETERMINISTIC,
+                               148, staging, nbytes, depth, 256, 1 << 20, None, copy_in, copy_out)
+
+    assert call(A=(), B=(), C=()) == sk.SK_OK  # no problems: nothing to do
+    assert call(m=0) == sk.SK_OK
+    for kw, code in [(dict(depth=0), sk.SK_EINVAL), (dict(depth=3), sk.SK_EINVAL), (dict(m=-1), sk.SK_EINVAL),
+                     (dict(C=(0,)), sk.SK_EINVAL), (dict(A=(0,)), sk.SK_EINVAL), (dict(B=(0,)), sk.SK_EINVAL),
+                     (dict(depth=2), sk.SK_EINVAL),  # depth 2 needs two copy streams
+                     (dict(depth=2, copy_in=7, copy_out=0), sk.SK_EINVAL),
+                     (dict(staging=0), sk.SK_EWORKSPACE), (dict(staging=128), sk.SK_EWORKSPACE),
+                     (dict(depth=2, copy_in=7, copy_out=9, nbytes=need - 1), sk.SK_EWORKSPACE)]:
+        with pytest.raises(sk.SkError) as e:
+            call(**kw)
+        assert e.value.code == code, kw
+    with pytest.raises(ValueError):
+        sk.sk_gemm_host([pa], [pb], [pc, pc], sk.SK_F32, M, N, K, sk.SK_NN, sched, sk.SK_DETERMINISTIC, 148, 256,
+                        need, 1, 256, 1 << 20)
