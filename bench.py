@@ -403,70 +403,104 @@ def library_timed(torch, dev, flush, stream, rot, M, N, nt=False, flushed=30, b2
     return float(np.median([a.elapsed_time(b) for a, b in ev])), e0.elapsed_time(e1) / b2b
 
 
-def run_smallm(sk, torch, dev, flush, stream, dev_sms):
+def run_smallm(sk, torch, dev, flush, stream, dev_sms, rounds=9, samples=40, warmup=20):
     """The split-K report's shapes (B stored [N,K], FP32 out): M = 96 and 256, N = 512,
     K = 2048. The [splits, M, N] slab chain at s = 2, 4, 8, 16 (every split stores its
     slab; a reduction pass sums them, two launches), the same slabs summed inside the one
     launch (the splits of a tile share the sum when all run at once, else the last to
-    arrive sums it), and the owner-wait fixups, timed one GEMM per event pair (L2 flushed
-    before each), packed 8 back to back (complete GPU time / 8), and (`us_b2b`) 200 overlapped
-    launches back to back over rotating inputs of at least 4x the L2."""
+    arrive sums it), and the owner-wait fixups.
+
+    Timed with the report's confirmation protocol ("Consecutive-B split-K NAX GEMM",
+    Confirmation): every arm gets `warmup` untimed calls; then `rounds` rounds of `samples`
+    samples, each sample running every arm once, with the arm order rotated by one from one
+    sample to the next; a second direction repeats this with the arm order reversed. An
+    arm-sample takes two event-timed measurements behind an L2 flush: pack 1, one whole
+    GEMM, and pack 8, eight whole GEMMs over the same inputs, divided by eight. Reported per
+    arm: median, p10 and p90 of pack 1 and of pack 8 over all samples of both directions, and
+    (`us_b2b`) the mean of 200 overlapped launches back to back over rotating inputs of at
+    least 4x the L2. Each arm's C is compared bit for bit before and after its timing."""
     out = {}
     for w in (synth.SMALLM_96, synth.SMALLM_256):
         A_bits, B_bits = synth.make_inputs(w)
         A = torch.from_numpy(A_bits.view(np.int16)).view(torch.bfloat16).to(dev)
         B = torch.from_numpy(B_bits.view(np.int16)).view(torch.bfloat16).to(dev)
-        C = torch.empty((w.M, w.N), dtype=torch.float32, device=dev)
-        set_b = A.numel() * 2 + B.numel() * 2 + C.numel() * 4
-        rot = [(A, B, C)] + [(A.clone(), B.clone(), torch.empty_like(C)) for _ in range(-(-4 * (129 << 20) // set_b) - 1)]
+        set_b = A.numel() * 2 + B.numel() * 2 + w.M * w.N * 4
+        rot = [(A.clone(), B.clone(), torch.empty((w.M, w.N), dtype=torch.float32, device=dev))
+               for _ in range(-(-4 * (129 << 20) // set_b))]
         fl = 2.0 * w.M * w.N * w.K
-        rows = {}
         kws = [(f"slabs_s{s}", dict(mode=sk.SK_SPLITK, splits=s, split_partials=1)) for s in (2, 4, 8, 16)]
         kws += [(f"slabs_1launch_s{s}", dict(mode=sk.SK_SPLITK, splits=s, split_partials=2)) for s in (2, 4, 8, 16)]
         kws += [("splitk8_fixup", dict(mode=sk.SK_SPLITK, splits=8)), ("streamk", dict(mode=sk.SK_STREAMK)),
                 ("streamk_pass", dict(mode=sk.SK_STREAMK, split_partials=1)), ("hybrid", dict(mode=sk.SK_HYBRID))]
+        arms = []
         for name, kw in kws:
-            sch, sch_o, nsms = sk.schedule(**kw), sk.schedule(overlap=1, **kw), dev_sms
-            nb = sk.sk_workspace_size(w.M, w.N, w.K, nsms, sch, 0)
+            sch = sk.schedule(**kw)
+            nb = sk.sk_workspace_size(w.M, w.N, w.K, dev_sms, sch, 0)
             ws = torch.zeros(nb, dtype=torch.uint8, device=dev)
-            g = lambda: sk.sk_gemm(A, B, C, sk.SK_F32, w.M, w.N, w.K, sk.SK_NT, sch, 0, nsms, ws, nb, stream)
-            for _ in range(5):
-                g()
-            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(40)]
-            for a0, a1 in ev:
-                flush.zero_()
-                a0.record(stream)
-                g()
-                a1.record(stream)
-            torch.cuda.synchronize(dev)
-            one = float(np.median([a0.elapsed_time(a1) for a0, a1 in ev])) * 1e3
-            packs = []
-            for _ in range(20):
-                flush.zero_()
-                a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                a0.record(stream)
-                for _ in range(8):
-                    g()
-                a1.record(stream)
-                packs.append((a0, a1))
-            torch.cuda.synchronize(dev)
-            pack8 = float(np.median([a0.elapsed_time(a1) for a0, a1 in packs])) * 1e3 / 8
+            C = torch.empty((w.M, w.N), dtype=torch.float32, device=dev)
+            arms.append(dict(name=name, sch=sch, sch_o=sk.schedule(overlap=1, **kw), ws=ws, nb=nb, C=C,
+                             one=[], pack8=[]))
+
+        def call(arm, a_=A, b_=B, c_=None, sch=None):
+            sk.sk_gemm(a_, b_, arm["C"] if c_ is None else c_, sk.SK_F32, w.M, w.N, w.K, sk.SK_NT,
+                       sch or arm["sch"], 0, dev_sms, arm["ws"], arm["nb"], stream)
+
+        for arm in arms:
+            for _ in range(warmup):
+                call(arm)
+        torch.cuda.synchronize(dev)
+        before = [arm["C"].clone() for arm in arms]
+        n = len(arms)
+        for direction in (1, -1):
+            order0 = list(range(n)) if direction == 1 else list(range(n - 1, -1, -1))
+            for _ in range(rounds):
+                pending = []
+                for j in range(samples):
+                    for a in order0[j % n:] + order0[:j % n]:
+                        arm = arms[a]
+                        ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+                        flush.zero_()
+                        ev[0].record(stream)
+                        call(arm)
+                        ev[1].record(stream)
+                        flush.zero_()
+                        ev[2].record(stream)
+                        for _ in range(8):
+                            call(arm)
+                        ev[3].record(stream)
+                        pending.append((arm, ev))
+                torch.cuda.synchronize(dev)
+                for arm, ev in pending:
+                    arm["one"].append(ev[0].elapsed_time(ev[1]) * 1e3)
+                    arm["pack8"].append(ev[2].elapsed_time(ev[3]) * 1e3 / 8)
+        rows = {}
+        for arm, c0 in zip(arms, before):
+            assert torch.equal(arm["C"], c0), f"{w.name}/{arm['name']}: C changed during timing"
             for i in range(20):
                 a_, b_, c_ = rot[i % len(rot)]
-                sk.sk_gemm(a_, b_, c_, sk.SK_F32, w.M, w.N, w.K, sk.SK_NT, sch_o, 0, nsms, ws, nb, stream)
+                call(arm, a_, b_, c_, arm["sch_o"])
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
             for i in range(200):
                 a_, b_, c_ = rot[i % len(rot)]
-                sk.sk_gemm(a_, b_, c_, sk.SK_F32, w.M, w.N, w.K, sk.SK_NT, sch_o, 0, nsms, ws, nb, stream)
+                call(arm, a_, b_, c_, arm["sch_o"])
             e1.record(stream)
             torch.cuda.synchronize(dev)
             b2b = e0.elapsed_time(e1) / 200 * 1e3
-            assert sk.sk_status(ws, stream) == sk.SK_OK
+            assert sk.sk_status(arm["ws"], stream) == sk.SK_OK
+            one, p8 = np.asarray(arm["one"]), np.asarray(arm["pack8"])
+            name = arm["name"]
             launches = 2 if (name.startswith("slabs_s") or name.endswith("_pass")) else 1
-            rows[name] = {"us": one, "us_pack8": pack8, "us_b2b": b2b, "launches": launches,
-                          "tflops": fl / (one / 1e6) / 1e12, "tflops_b2b": fl / (b2b / 1e6) / 1e12}
+            med = float(np.median(one))
+            rows[name] = {"us": med, "us_p10": float(np.percentile(one, 10)), "us_p90": float(np.percentile(one, 90)),
+                          "us_pack8": float(np.median(p8)), "us_pack8_p10": float(np.percentile(p8, 10)),
+                          "us_pack8_p90": float(np.percentile(p8, 90)), "samples": int(one.size),
+                          "us_b2b": b2b, "launches": launches,
+                          "tflops": fl / (med / 1e6) / 1e12, "tflops_b2b": fl / (b2b / 1e6) / 1e12}
         out[w.name] = rows
+    out["protocol"] = (f"per arm {warmup} warm-ups, then {rounds} rounds x {samples} samples in each of two "
+                       "directions (arm order rotated every sample; reversed in the second direction); pack 1 and "
+                       "pack 8 each behind an L2 flush; median, p10, p90; C checked bit for bit before and after")
     return out
 
 
