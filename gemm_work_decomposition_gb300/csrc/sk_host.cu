@@ -90,7 +90,8 @@ extern "C" int32_t sk_gemm_host(int32_t count, const void* const* A, const void*
         if (!C[i]) return SK_EINVAL;
         if (K > 0 && (!A[i] || !B[i])) return SK_EINVAL;
     }
-    if (depth == 2 && (!copy_in || !copy_out || copy_in == stream || copy_out == stream)) return SK_EINVAL;
+    if (depth == 2 && (!copy_in || !copy_out || copy_in == copy_out || copy_in == stream || copy_out == stream))
+        return SK_EINVAL;
     if (!staging || (reinterpret_cast<uintptr_t>(staging) & (kSetAlign - 1)) != 0 ||
         static_cast<int64_t>(staging_bytes) < depth * L.bytes)
         return SK_EWORKSPACE;

@@ -322,7 +322,8 @@ int64_t sk_host_staging_size(int32_t M, int32_t N, int32_t K, sk_dtype c_dtype, 
  *     256-byte aligned, owned by the caller (else SK_EWORKSPACE).
  *   depth 1: every copy and GEMM runs in order on `stream`; copy_in and copy_out are unused.
  *   depth 2: two staging sets used in turn; the uploads run on `copy_in` and the downloads on
- *     `copy_out` (two streams of the caller other than `stream`, else SK_EINVAL), so that
+ *     `copy_out` (two distinct non-NULL streams of the caller other than `stream`, else
+ *     SK_EINVAL), so that
  *     problem i + 1's uploads and problem i - 1's download overlap problem i's GEMM. Events
  *     keep every buffer's writes and reads in order; the copy streams first wait for the
  *     caller's earlier work on `stream`.

@@ -277,6 +277,7 @@ def test_gemm_host_argument_errors(sk):
                      (dict(C=(0,)), sk.SK_EINVAL), (dict(A=(0,)), sk.SK_EINVAL), (dict(B=(0,)), sk.SK_EINVAL),
                      (dict(depth=2), sk.SK_EINVAL),  # depth 2 needs two copy streams
                      (dict(depth=2, copy_in=7, copy_out=0), sk.SK_EINVAL),
+                     (dict(depth=2, copy_in=7, copy_out=7), sk.SK_EINVAL),
                      (dict(staging=0), sk.SK_EWORKSPACE), (dict(staging=128), sk.SK_EWORKSPACE),
                      (dict(depth=2, copy_in=7, copy_out=9, nbytes=need - 1), sk.SK_EWORKSPACE)]:
         with pytest.raises(sk.SkError) as e:
