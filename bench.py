@@ -258,18 +258,20 @@ def run_reference(args, w, rank, world):
 
 
 SWEEP_COMPACT = (1024, 1536, 2048, 2304, 2432, 3072, 3840, 4096)
-# (name, mode, splits); splits None: the CUTLASS page's Split-K factor for the shape
-# (sk_split_k_slices, clamped to the K loop).
-SWEEP_SCHEDULES = (("dp", 0, 1), ("splitk2", 1, 2), ("splitk4", 1, 4), ("splitk_cutlass", 1, None),
-                   ("streamk", 2, 1), ("hybrid", 3, 1))
+# (name, mode, splits, split_partials); splits None: the CUTLASS page's Split-K factor for the
+# shape (sk_split_k_slices, clamped to the K loop). The `_slabs` rows are Split-K with FP32
+# [s, M, N] slabs summed by the reduction pass (split_partials 1).
+SWEEP_SCHEDULES = (("dp", 0, 1, 0), ("splitk2", 1, 2, 0), ("splitk4", 1, 4, 0), ("splitk_cutlass", 1, None, 0),
+                   ("splitk2_slabs", 1, 2, 1), ("splitk4_slabs", 1, 4, 1), ("streamk", 2, 1, 0), ("hybrid", 3, 1, 0))
 
 
 def sweep_points(sk, torch, dev, red, flush, stream, peak_tf, l2_bytes, sizes, configs, flushed=0, b2b=40,
                  library=False):
     """Tile-count sweep over square M = N in `sizes`, K = 4096 (the tile-count sweep
-    workload): every schedule of SWEEP_SCHEDULES (data-parallel, Split-K s = 2 and 4, Split-K
-    with the CUTLASS page's factor heuristic, Stream-K and the hybrid rule, which is the
-    decision rule's own choice) for each (num_sms, tile) of
+    workload): every schedule of SWEEP_SCHEDULES (data-parallel, Split-K s = 2 and 4 with the
+    owner fixup and with FP32 slabs and the reduction pass, Split-K with the CUTLASS page's
+    factor heuristic, Stream-K
+    and the hybrid rule, which is the decision rule's own choice) for each (num_sms, tile) of
     `configs`. Each point is timed `b2b` overlapped launches back to back over rotating copies
     of A, B and C that together exceed 4x the L2 (the headline's method, mean per launch),
     and, with `flushed` > 0, as the median of that many single launches with the L2 flushed
@@ -285,10 +287,10 @@ def sweep_points(sk, torch, dev, red, flush, stream, peak_tf, l2_bytes, sizes, c
                              for _ in range(max(2, -(-4 * l2_bytes // set_b)) - 1)]
         fl = 2.0 * m * m * ww.K
         for nsms, tile in configs:
-            for name, mode, s in SWEEP_SCHEDULES:
+            for name, mode, s, parts in SWEEP_SCHEDULES:
                 if s is None:
                     s = min(sk.sk_split_k_slices(m, m, ww.K, nsms), -(-ww.K // 64))
-                sch = sk.schedule(mode, s, tile=tile)
+                sch = sk.schedule(mode, s, split_partials=parts, tile=tile)
                 nb = sk.sk_workspace_size(m, m, ww.K, nsms, sch, red)
                 ws = torch.zeros(nb, dtype=torch.uint8, device=dev)
                 plan = sk.sk_plan(m, m, ww.K, nsms, sch)
@@ -309,7 +311,7 @@ def sweep_points(sk, torch, dev, red, flush, stream, peak_tf, l2_bytes, sizes, c
                     t = float(np.median([a.elapsed_time(b) for a, b in ev]))
                     row.update({"us": t * 1e3, "tflops": fl / (t / 1e3) / 1e12,
                                 "frac_of_measured_peak": fl / (t / 1e3) / 1e12 / peak_tf})
-                sch_o = sk.schedule(mode, s, tile=tile, overlap=1)
+                sch_o = sk.schedule(mode, s, split_partials=parts, tile=tile, overlap=1)
                 for i in range(10):
                     a_, b_, c_ = rot[i % len(rot)]
                     sk.sk_gemm(a_, b_, c_, sk.SK_BF16, m, m, ww.K, sk.SK_NN, sch_o, red, nsms, ws, nb, stream)

@@ -210,6 +210,10 @@ def test_slab_edges(sk, dev, M, N, K, tile, s, partials, out):
 @pytest.mark.parametrize("m", [128, 640, 1152, 1536, 2560, 4096])
 @pytest.mark.parametrize("name,kw", [("dp", dict(mode=0)), ("splitk2", dict(mode=1, splits=2)),
                                      ("splitk4", dict(mode=1, splits=4)), ("splitk_cutlass", dict(mode=1)),
+                                     ("splitk2_slabs", dict(mode=1, splits=2, split_partials=1)),
+                                     ("splitk4_slabs", dict(mode=1, splits=4, split_partials=1)),
+                                     ("splitk2_slabs_1launch", dict(mode=1, splits=2, split_partials=2)),
+                                     ("splitk4_slabs_1launch", dict(mode=1, splits=4, split_partials=2)),
                                      ("streamk", dict(mode=2)), ("hybrid", dict(mode=3))])
 def test_sweep(sk, dev, m, name, kw, tile):
     # The tile-count sweep's schedules; "splitk_cutlass" takes its split count from the
