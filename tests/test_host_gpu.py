@@ -150,3 +150,29 @@ def test_gemm_host_device_errors_enqueue_nothing(sk):
         assert e.value.code == code
     torch.cuda.synchronize(dev)
     assert bool((C_h[0].float() == U.SENTINEL).all())
+
+
+def test_gemm_host_atomic_reduction(sk):
+    # FP32 atomics: the bits may depend on arrival order, so only the tolerance is checked.
+    dev = torch.device("cuda:0")
+    M, N, K, sms = 256, 640, 1024, 148
+    probs = _problems("atomic", M, N, K, "NN", "uniform", "f32", 3)
+    sched = sk.schedule(sk.SK_STREAMK)
+    nbytes = sk.sk_workspace_size(M, N, K, sms, sched, sk.SK_ATOMIC)
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
+    nstage = sk.sk_host_staging_size(M, N, K, sk.SK_F32, 2)
+    staging = torch.empty(nstage, dtype=torch.uint8, device=dev)
+    A_h, B_h = [], []
+    for w in probs:
+        a, b = U.inputs(w)
+        A_h.append(_host_bf16(a, True))
+        B_h.append(_host_bf16(b, True))
+    C_h = [torch.full((M, N), U.SENTINEL).pin_memory() for _ in probs]
+    s = [torch.cuda.Stream(dev) for _ in range(3)]
+    sk.sk_gemm_host(A_h, B_h, C_h, sk.SK_F32, M, N, K, sk.SK_NN, sched, sk.SK_ATOMIC, sms, staging, nstage, 2,
+                    ws, nbytes, s[0], s[1], s[2])
+    torch.cuda.synchronize(dev)
+    assert sk.sk_status(ws, s[0]) == sk.SK_OK
+    for w, c in zip(probs, C_h):
+        a, b = U.inputs(w)
+        U.assert_close(c.numpy().astype(np.float64), og.ref_gemm(a, b, "NN"), w.name)
