@@ -286,3 +286,16 @@ def test_gemm_host_argument_errors(sk):
     with pytest.raises(ValueError):
         sk.sk_gemm_host([pa], [pb], [pc, pc], sk.SK_F32, M, N, K, sk.SK_NN, sched, sk.SK_DETERMINISTIC, 148, 256,
                         need, 1, 256, 1 << 20)
+
+
+def test_header_is_plain_c():
+    # The boundary is a C ABI: include/sk.h must compile as C99 (and as C++) on its own.
+    import shutil
+    import subprocess
+    hdr = os.path.join(ROOT, "include", "sk.h")
+    for cc, lang, std in (("gcc", "c", "-std=c99"), ("g++", "c++", "-std=c++17")):
+        if shutil.which(cc) is None:
+            pytest.skip(f"{cc} not found")
+        p = subprocess.run([cc, std, "-Wall", "-Wextra", "-Werror", "-fsyntax-only", "-x", lang, hdr],
+                           capture_output=True, text=True)
+        assert p.returncode == 0, p.stderr
