@@ -299,3 +299,42 @@ def test_header_is_plain_c():
         p = subprocess.run([cc, std, "-Wall", "-Wextra", "-Werror", "-fsyntax-only", "-x", lang, hdr],
                            capture_output=True, text=True)
         assert p.returncode == 0, p.stderr
+
+
+C_CONSUMER = r"""
+#include <stdio.h>
+#include <stdlib.h>
+#include "sk.h"
+int main(void) {
+    sk_schedule s = {0};
+    s.mode = SK_STREAMK;
+    s.units = 4;
+    int64_t n = sk_plan_size(128, 640, 256, 4, s);
+    if (n < 0) return 2;
+    int32_t* map = (int32_t*)malloc((size_t)n * sizeof(int32_t));
+    if (!map || sk_plan(128, 640, 256, 4, s, map, n) != SK_OK) return 3;
+    for (int64_t i = 0; i < n; ++i) printf("%d\n", map[i]);
+    free(map);
+    return sk_plan(128, 640, 256, 4, s, NULL, 0) == SK_ECAPACITY ? 0 : 4;
+}
+"""
+
+
+def test_plain_c_consumer(sk, tmp_path):
+    # A C program, compiled and linked against libsk.so with no Python or torch in between,
+    # plans the toy Stream-K case (4 units, 5 tiles x 4 k-iterations) and gets the oracle's map.
+    import shutil
+    import subprocess
+    if shutil.which("gcc") is None:
+        pytest.skip("gcc not found")
+    src, exe = tmp_path / "consumer.c", tmp_path / "consumer"
+    src.write_text(C_CONSUMER)
+    libdir = os.path.dirname(sk.LIB_PATH)
+    p = subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"), str(src),
+                        "-L", libdir, "-lsk", f"-Wl,-rpath,{libdir}", "-o", str(exe)], capture_output=True, text=True)
+    assert p.returncode == 0, p.stderr
+    r = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert r.returncode == 0, (r.returncode, r.stderr)
+    got = np.array([int(x) for x in r.stdout.split()], dtype=np.int32)
+    want = S.plan_map(S.build_plan(128, 640, 256, 4, S.STREAMK, units=4))
+    assert np.array_equal(got, np.asarray(want, dtype=np.int32))
